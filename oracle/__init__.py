@@ -1,0 +1,180 @@
+"""ORACLE -- test infrastructure only.
+
+A plain, slow, obviously correct CPU statement of the paged-attention hot
+path, written from the PagedAttention pages.  Only ``tests/``,
+``__graft_entry__.smoke()`` and the CPU-baseline leg of ``bench.py`` may
+import it.  It shares no code with the CUDA library (``paged_kv_cache_280_gb300``)
+and never imports it.
+
+Parts:
+  * ``pa_oracle.c``  -- fp64 decode attention (direct and split + reduce),
+    the slot-mapped append and the copy-on-write block copy, as element
+    loops over host arrays.
+  * ``alloc_model``  -- a reference model of the block allocator
+    (on-demand blocks, refcounted sharing, copy-on-write).
+  * ``waste``        -- the memory accounting of the waste simulation on
+    the ohmygp.com page (contiguous reservation vs paged blocks).
+
+Inputs are numpy arrays: fp32 tensors as ``float32``, bf16 tensors as
+``uint16`` bit patterns (widened exactly inside the C code).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+from concurrent.futures import ThreadPoolExecutor
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "pa_oracle.c")
+_LIB = os.path.join(_HERE, "libpa_oracle.so")
+_lock = threading.Lock()
+_lib = None
+
+ERRORS = {-1: "bad argument", -2: "block id out of range", -3: "slot out of range", -4: "out of memory"}
+
+
+class OracleError(RuntimeError):
+    pass
+
+
+def build(force: bool = False) -> str:
+    """Compile ``libpa_oracle.so`` next to its source (plain gcc)."""
+    if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC):
+        tmp = _LIB + f".tmp{os.getpid()}"
+        subprocess.check_call(["gcc", "-O2", "-std=c11", "-fPIC", "-shared", _SRC, "-o", tmp, "-lm"])
+        os.replace(tmp, _LIB)
+    return _LIB
+
+
+def _open(path: str):
+    """Open a compiled oracle library and declare its C signatures."""
+    lib = ctypes.CDLL(path)
+    i32, f64, vp = ctypes.c_int32, ctypes.c_double, ctypes.c_void_p
+    lib.oracle_decode_attention.restype = ctypes.c_int
+    lib.oracle_decode_attention.argtypes = [ctypes.c_int, vp, vp, vp, vp, i32, vp, i32, i32, i32,
+                                            i32, i32, i32, f64, i32, i32, vp]
+    lib.oracle_decode_partials.restype = ctypes.c_int
+    lib.oracle_decode_partials.argtypes = [ctypes.c_int, vp, vp, vp, vp, i32, vp, i32, i32, i32,
+                                           i32, i32, i32, f64, i32, i32, vp, vp, vp]
+    lib.oracle_combine_partials.restype = ctypes.c_int
+    lib.oracle_combine_partials.argtypes = [i32, i32, i32, vp, vp, vp, vp]
+    lib.oracle_reshape_and_cache.restype = ctypes.c_int
+    lib.oracle_reshape_and_cache.argtypes = [i32, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32]
+    lib.oracle_copy_blocks.restype = ctypes.c_int
+    lib.oracle_copy_blocks.argtypes = [i32, vp, vp, vp, i32, i32, i32, i32, i32]
+    return lib
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            _lib = _open(build())
+    return _lib
+
+
+def _check(rc: int) -> None:
+    if rc != 0:
+        raise OracleError(ERRORS.get(rc, f"oracle error {rc}"))
+
+
+def _dtype_code(a: np.ndarray) -> int:
+    if a.dtype == np.float32:
+        return 0
+    if a.dtype == np.uint16:
+        return 1
+    raise TypeError(f"oracle tensors are float32 or uint16 (bf16 bits), got {a.dtype}")
+
+
+def _c(a: np.ndarray, dtype=None) -> np.ndarray:
+    a = np.ascontiguousarray(a if dtype is None else a.astype(dtype, copy=False))
+    return a
+
+
+def decode_attention(q, k_pool, v_pool, block_tables, seq_lens, scale, seqs=None, threads=1):
+    """fp64 decode attention.  Returns out[B][Hq][D] (float64).
+
+    q: [B][Hq][D]; pools: [num_blocks][Hkv][bs][D]; block_tables: [B][max_blocks] int32;
+    seq_lens: [B] int32.  ``seqs`` restricts the computation to those sequence
+    indices (other rows are NaN); ``threads`` > 1 runs sequences on a thread pool.
+    """
+    q, k_pool, v_pool = _c(q), _c(k_pool), _c(v_pool)
+    dt = _dtype_code(q)
+    if _dtype_code(k_pool) != dt or _dtype_code(v_pool) != dt:
+        raise TypeError("q and the pools must share a dtype")
+    bt = _c(block_tables, np.int32)
+    lens = _c(seq_lens, np.int32)
+    B, Hq, D = q.shape
+    nb, Hkv, bs, D2 = k_pool.shape
+    assert D2 == D and v_pool.shape == k_pool.shape and bt.shape[0] == B and lens.shape == (B,)
+    out = np.full((B, Hq, D), np.nan, np.float64)
+    lib = _load()
+    todo = list(range(B)) if seqs is None else sorted(set(int(s) for s in seqs))
+
+    def run(b):
+        _check(lib.oracle_decode_attention(dt, q.ctypes.data, k_pool.ctypes.data, v_pool.ctypes.data,
+                                           bt.ctypes.data, bt.shape[1], lens.ctypes.data, B, Hq, Hkv, D,
+                                           bs, nb, float(scale), b, b + 1, out.ctypes.data))
+
+    if threads <= 1:
+        for b in todo:
+            run(b)
+    else:
+        with ThreadPoolExecutor(threads) as ex:
+            list(ex.map(run, todo))
+    return out
+
+
+def decode_partials(q, k_pool, v_pool, block_tables, seq_lens, scale, partition_tokens):
+    """Per-partition (m, l, o) of the split form; shapes [B][Hq][P], [B][Hq][P], [B][Hq][P][D]."""
+    q, k_pool, v_pool = _c(q), _c(k_pool), _c(v_pool)
+    dt = _dtype_code(q)
+    bt = _c(block_tables, np.int32)
+    lens = _c(seq_lens, np.int32)
+    B, Hq, D = q.shape
+    nb, Hkv, bs, _ = k_pool.shape
+    n_part = max(1, int(-(-int(lens.max(initial=0)) // partition_tokens)))
+    m = np.empty((B, Hq, n_part), np.float64)
+    l = np.empty((B, Hq, n_part), np.float64)
+    o = np.empty((B, Hq, n_part, D), np.float64)
+    _check(_load().oracle_decode_partials(dt, q.ctypes.data, k_pool.ctypes.data, v_pool.ctypes.data,
+                                          bt.ctypes.data, bt.shape[1], lens.ctypes.data, B, Hq, Hkv, D, bs,
+                                          nb, float(scale), int(partition_tokens), n_part, m.ctypes.data,
+                                          l.ctypes.data, o.ctypes.data))
+    return m, l, o
+
+
+def combine_partials(m, l, o):
+    """The split-sequence reduce; returns out[..., D] (float64)."""
+    m, l, o = _c(m, np.float64), _c(l, np.float64), _c(o, np.float64)
+    lead = m.shape[:-1]
+    n_part, D = o.shape[-2], o.shape[-1]
+    rows = int(np.prod(lead)) if lead else 1
+    out = np.empty(lead + (D,), np.float64)
+    _check(_load().oracle_combine_partials(rows, n_part, D, m.ctypes.data, l.ctypes.data, o.ctypes.data,
+                                           out.ctypes.data))
+    return out
+
+
+def reshape_and_cache(k_new, v_new, k_pool, v_pool, slot_mapping):
+    """In-place slot-mapped append on host pools ([num_blocks][Hkv][bs][D])."""
+    assert k_pool.flags.c_contiguous and v_pool.flags.c_contiguous
+    k_new, v_new = _c(k_new), _c(v_new)
+    slots = _c(slot_mapping, np.int64)
+    nb, Hkv, bs, D = k_pool.shape
+    _check(_load().oracle_reshape_and_cache(k_pool.itemsize, k_new.ctypes.data, v_new.ctypes.data,
+                                            k_pool.ctypes.data, v_pool.ctypes.data, slots.ctypes.data,
+                                            len(slots), Hkv, D, bs, nb))
+
+
+def copy_blocks(k_pool, v_pool, pairs):
+    """In-place copy-on-write block copies on host pools; pairs is [n][2] (src, dst)."""
+    assert k_pool.flags.c_contiguous and v_pool.flags.c_contiguous
+    pairs = _c(np.asarray(pairs, np.int32).reshape(-1, 2))
+    nb, Hkv, bs, D = k_pool.shape
+    _check(_load().oracle_copy_blocks(k_pool.itemsize, k_pool.ctypes.data, v_pool.ctypes.data,
+                                      pairs.ctypes.data, len(pairs), Hkv, D, bs, nb))

@@ -1,0 +1,95 @@
+"""Planted mistakes in the oracle must be caught by its pins.
+
+Each mutant is a copy of the oracle's C source with one plausible slip
+(compiled on the CPU into a temporary directory); the pin tests of
+test_oracle_pins.py are rerun against it and at least one must fail.  The
+allocator model gets the same treatment through small subclasses.
+"""
+import os
+import subprocess
+import sys
+
+import pytest
+
+import oracle
+from oracle import alloc_model
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+
+C_MUTANTS = {
+    "scale_dropped": ("s[t] = scale * dot;", "s[t] = dot;"),
+    "offset_uses_block_index": ("(size_t)(t % block_size)) * head_dim;", "(size_t)(t / block_size)) * head_dim;"),
+    "logical_used_as_physical": ("int32_t phys = table[t / block_size];", "int32_t phys = t / block_size;"),
+    "kv_head_reversed": ("* num_kv_heads + g) * block_size", "* num_kv_heads + (num_kv_heads - 1 - g)) * block_size"),
+    "query_row_from_kv_head": ("size_t qrow = ((size_t)b * num_q_heads + h) * head_dim;\n                double m",
+                               "size_t qrow = ((size_t)b * num_q_heads + g) * head_dim;\n                double m"),
+    "softmax_not_normalised": ("double w = s[t] / denom;", "double w = s[t];"),
+    "reduce_weight_inverted": ("double w = exp(m[p] - M);", "double w = exp(M - m[p]);"),
+    "reduce_drops_l": ("L += w * l[p];", "L += w;"),
+    "partition_max_unscaled": ("if (scale * dot > m) m = scale * dot;", "if (dot > m) m = dot;"),
+}
+
+
+@pytest.fixture(scope="module")
+def src():
+    with open(oracle._SRC) as f:
+        return f.read()
+
+
+@pytest.mark.parametrize("name", sorted(C_MUTANTS))
+def test_c_mutant_is_caught(name, src, tmp_path):
+    old, new = C_MUTANTS[name]
+    assert src.count(old) >= 1, f"mutation site for {name} not found"
+    mutated = src.replace(old, new)
+    c = tmp_path / "mut.c"
+    c.write_text(mutated)
+    so = tmp_path / "libmut.so"
+    subprocess.check_call(["gcc", "-O2", "-std=c11", "-fPIC", "-shared", str(c), "-o", str(so), "-lm"])
+    # run the pin tests in a child process whose oracle loads the mutant
+    code = (
+        "import sys, pytest, oracle;"
+        f"oracle._lib = oracle._open({str(so)!r});"
+        f"sys.exit(pytest.main(['-q', '-x', '-p', 'no:cacheprovider', {os.path.join(HERE, 'test_oracle_pins.py')!r}]))"
+    )
+    r = subprocess.run([sys.executable, "-c", code], cwd=os.path.dirname(HERE), capture_output=True, text=True,
+                       env={**os.environ, "PYTHONPATH": os.pathsep.join([os.path.dirname(HERE), HERE])})
+    assert r.returncode != 0, f"mutant {name} passed every pin:\n{r.stdout[-2000:]}"
+
+
+class _CowOnAnyRef(alloc_model.RefAllocator):
+    def _append_one(self, sid, slots, pairs):  # copies even a private tail
+        table = self.tables[sid]
+        n = self.lens[sid]
+        if n % self.block_size and self.ref[table[-1]] >= 1 and len(table) > 1:
+            fresh = self._take()
+            pairs.append((table[-1], fresh))
+            self.ref[table[-1]] -= 1
+            table[-1] = fresh
+        elif n % self.block_size == 0:
+            table.append(self._take())
+        slots.append(table[n // self.block_size] * self.block_size + n % self.block_size)
+        self.lens[sid] = n + 1
+
+
+class _LifoFree(alloc_model.RefAllocator):
+    def free_seq(self, sid):
+        for b in self.tables[sid]:
+            self.ref[b] -= 1
+            if self.ref[b] == 0:
+                self.free.appendleft(b)
+        del self.tables[sid]
+        del self.lens[sid]
+
+
+class _ForkNoRef(alloc_model.RefAllocator):
+    def fork(self, parent, child):
+        self.tables[child] = list(self.tables[parent])
+        self.lens[child] = self.lens[parent]
+
+
+@pytest.mark.parametrize("cls", [_CowOnAnyRef, _LifoFree, _ForkNoRef])
+def test_alloc_model_mutant_is_caught(cls):
+    from test_alloc_model import run_trace
+
+    with pytest.raises(AssertionError):
+        run_trace(lambda nb, bs, order: cls(nb, bs, free_order=order))
