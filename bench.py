@@ -1,0 +1,498 @@
+#!/usr/bin/env python3
+"""Benchmark of the paged-attention decode step on GB300.
+
+Metric: paged decode attention KV-tokens/s (and HBM GB/s as a fraction of
+the measured HBM peak) at 1 GPU.  Workload (default): the bf16 decode batch
+of 64 sequences with the pages' skewed length mix (70 % U[32,511], 25 %
+U[512,2047], 5 % U[2048,4095]), 32 query / 8 KV heads, head_dim 128,
+16-token blocks scattered through a pool sized to demand + 10 %.
+
+One step = the whole hot path for one decode iteration of the batch:
+  a1 host allocator appends one token per sequence (slots, CoW pairs, tables)
+  a2 copy-on-write block copy (only when the allocator emitted pairs)
+  a3 slot-mapped append of the new K/V
+  a4/a5 paged decode attention over len + 1 tokens (split + on-device merge)
+`value` times a2-a5 on the device (CUDA events, inputs resident in HBM, L2
+flushed between steps); the host allocator runs before the timed loop and
+its time is reported separately.  `e2e` runs genuine decode steps through
+the public API: host allocator, pinned host -> device copies of the step's
+inputs, the kernels, and the device -> host copy of the output.
+
+N > 1 (torchrun): every rank owns its own 64 sequences (weak scaling, no
+data-path collective); the timed region is bracketed by barriers and the
+max time over ranks is used.
+"""
+from __future__ import annotations
+
+import argparse
+import ctypes
+import hashlib
+import json
+import math
+import os
+import statistics
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+METRIC = "paged decode attention KV-tokens/s and HBM GB/s (% of GB300 roofline) at 1 GPU"
+UNIT = "KV-tokens/s"
+FALLBACK_HBM_GBS = 6800.0
+L2_FLUSH_BYTES = 512 << 20
+
+
+# ---------------------------------------------------------------------------
+# distributed plumbing (host-level only: barriers and the max of the times)
+# ---------------------------------------------------------------------------
+def dist_env():
+    return int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")), int(os.environ.get("LOCAL_RANK", "0"))
+
+
+def dist_init(world: int, backend: str):
+    import torch.distributed as dist
+
+    if world > 1 and not dist.is_initialized():
+        dist.init_process_group(backend=backend)
+    return dist if world > 1 else None
+
+
+def shard_lengths(global_lengths: np.ndarray, rank: int, world: int, per_rank: int) -> np.ndarray:
+    """Sequences of this rank: a contiguous slice of the global draw (rank r owns r*per_rank ...)."""
+    assert len(global_lengths) >= world * per_rank
+    return np.asarray(global_lengths[rank * per_rank:(rank + 1) * per_rank], np.int32)
+
+
+def reduce_max(x: float, dist, device) -> float:
+    if dist is None:
+        return x
+    import torch
+
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def reduce_sum(x: float, dist, device) -> float:
+    if dist is None:
+        return x
+    import torch
+
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.SUM)
+    return float(t.item())
+
+
+# ---------------------------------------------------------------------------
+# clocks during the timed region (NVML through ctypes; nvidia-smi fallback)
+# ---------------------------------------------------------------------------
+REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown", 0x40: "hw_thermal_slowdown",
+           0x80: "hw_power_brake_slowdown", 0x2: "applications_clocks_setting", 0x1: "gpu_idle"}
+
+
+class ClockSampler:
+    def __init__(self, cuda_index: int, period_s: float = 0.002):
+        self.period = period_s
+        self.samples = []  # (sm_mhz, reasons_mask)
+        self.max_mhz = None
+        self._stop = threading.Event()
+        self._thread = None
+        self._nvml = None
+        self._handle = None
+        try:
+            nv = ctypes.CDLL("libnvidia-ml.so.1")
+            if nv.nvmlInit_v2() != 0:
+                raise OSError("nvmlInit")
+            handle = ctypes.c_void_p()
+            bus = self._pci_bus_id(cuda_index)
+            ok = bus is not None and nv.nvmlDeviceGetHandleByPciBusId_v2(bus.encode(), ctypes.byref(handle)) == 0
+            if not ok and nv.nvmlDeviceGetHandleByIndex_v2(cuda_index, ctypes.byref(handle)) != 0:
+                raise OSError("nvml handle")
+            mx = ctypes.c_uint(0)
+            if nv.nvmlDeviceGetMaxClockInfo(handle, 1, ctypes.byref(mx)) == 0:
+                self.max_mhz = int(mx.value)
+            self._nvml, self._handle = nv, handle
+        except OSError:
+            self._nvml = None
+
+    @staticmethod
+    def _pci_bus_id(idx):
+        try:
+            import torch
+
+            p = torch.cuda.get_device_properties(idx)
+            return f"{p.pci_domain_id:08X}:{p.pci_bus_id:02X}:{p.pci_device_id:02X}.0"
+        except Exception:
+            return None
+
+    def _loop_nvml(self):
+        nv, h = self._nvml, self._handle
+        clk, rs = ctypes.c_uint(0), ctypes.c_ulonglong(0)
+        get_reasons = getattr(nv, "nvmlDeviceGetCurrentClocksEventReasons", None) or nv.nvmlDeviceGetCurrentClocksThrottleReasons
+        while not self._stop.is_set():
+            if nv.nvmlDeviceGetClockInfo(h, 1, ctypes.byref(clk)) == 0 and get_reasons(h, ctypes.byref(rs)) == 0:
+                self.samples.append((int(clk.value), int(rs.value)))
+            time.sleep(self.period)
+
+    def start(self):
+        if self._nvml is not None:
+            self._thread = threading.Thread(target=self._loop_nvml, daemon=True)
+            self._thread.start()
+
+    def stop(self):
+        self._stop.set()
+        if self._thread:
+            self._thread.join()
+
+    def summary(self):
+        if not self.samples:
+            return {"sm_mhz": None, "sm_max_mhz": self.max_mhz, "reasons": [], "samples": 0,
+                    "source": "nvml" if self._nvml else "unavailable"}
+        mhz = [s[0] for s in self.samples]
+        mask = 0
+        for _, r in self.samples:
+            mask |= r
+        reasons = [name for bit, name in sorted(REASONS.items()) if mask & bit and name != "gpu_idle"]
+        return {"sm_mhz": statistics.median(mhz), "sm_max_mhz": self.max_mhz, "reasons": reasons,
+                "samples": len(mhz), "source": "nvml"}
+
+
+# ---------------------------------------------------------------------------
+# workload
+# ---------------------------------------------------------------------------
+def build_workload(name: str, rank: int, world: int, extra_steps: int):
+    import synth
+    import synth.workloads as W
+
+    if name != "gqa4_b64":
+        raise SystemExit(f"unknown workload {name}")
+    base = W.gqa4_b64()
+    per_rank = base.num_seqs
+    glob = synth.lengths_mix(synth.stream_seed(base.seed, W.TAG_LENGTHS), per_rank * world)
+    lengths = shard_lengths(glob, rank, world, per_rank)
+    demand = int(sum(-(-(int(x) + extra_steps) // base.block_size) for x in lengths))
+    seed = base.seed + 7919 * rank
+    return W.scaled(base, lengths=lengths, num_blocks=int(math.ceil(1.1 * demand)), seed=seed)
+
+
+def decode_bytes(lens, w) -> int:
+    """Algorithmic bytes of one decode launch: K and V of every token, tables, lengths, q and out."""
+    e = w.elem_bytes
+    kv = int(np.sum(lens, dtype=np.int64)) * w.num_kv_heads * w.head_dim * 2 * e
+    tables = int(sum(-(-int(x) // w.block_size) for x in lens)) * 4
+    qo = 2 * len(lens) * w.num_q_heads * w.head_dim * e
+    return kv + tables + 4 * len(lens) + qo
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "paged_kv_cache_280_gb300", "csrc")
+    for f in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, f), "rb") as fh:
+            h.update(f.encode() + fh.read())
+    return h.hexdigest()[:16]
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def recorded_traffic():
+    """DRAM bytes per decode launch from the committed ncu summary, if it was taken on this kernel source."""
+    path = os.path.join(ROOT, "profiles", "decode_gqa4_b64_traffic.txt")
+    try:
+        with open(path) as f:
+            kv = dict(line.split("=", 1) for line in f.read().split("\n") if "=" in line and not line.startswith("#"))
+        if kv.get("kernel_source_hash", "").strip() == kernel_source_hash():
+            return int(kv["dram_bytes_per_launch"].strip())
+    except (OSError, ValueError, KeyError):
+        pass
+    return None
+
+
+# ---------------------------------------------------------------------------
+# CPU baseline: the oracle, as it stands, on the host cores
+# ---------------------------------------------------------------------------
+def cpu_baseline(w, q, k_pool, v_pool, tables, lens, seconds: float):
+    import oracle
+
+    threads = os.cpu_count() or 1
+    B = len(lens)
+    done_tokens, t0, rounds = 0, time.perf_counter(), 0
+    seqs_done = 0
+    while True:
+        chunk = list(range(B))
+        oracle.decode_attention(q, k_pool, v_pool, tables, lens, w.scale, seqs=chunk, threads=threads)
+        done_tokens += int(np.sum(lens, dtype=np.int64))
+        seqs_done += len(chunk)
+        rounds += 1
+        if time.perf_counter() - t0 >= seconds:
+            break
+    dt = time.perf_counter() - t0
+    return {"value": done_tokens / dt, "unit": UNIT, "cores": threads, "kind": "oracle",
+            "sample": f"fp64 C oracle over the whole {B}-sequence batch, {rounds} pass(es) ({dt:.1f} s), "
+                      f"{threads} threads over sequences"}
+
+
+# ---------------------------------------------------------------------------
+# our arm
+# ---------------------------------------------------------------------------
+def run_ours(args, rank, world, local_rank):
+    import torch
+
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    dist = dist_init(world, "nccl")
+    import paged_kv_cache_280_gb300 as pa
+
+    K, Wm = args.steps, args.warmup
+    K_e2e = min(K, args.e2e_steps)
+    w = build_workload(args.workload, rank, world, extra_steps=1 + K_e2e + 2)
+    B, Hq, Hkv, D, bs = w.num_seqs, w.num_q_heads, w.num_kv_heads, w.head_dim, w.block_size
+    lib = pa.Allocator(w.num_blocks, bs, free_order=w.free_order())
+    for s, n in enumerate(w.lengths):
+        lib.create(s)
+        lib.append(s, int(n))
+    max_blocks = int(-(-(int(w.lengths.max()) + 2 + K_e2e) // bs))
+    ids = list(range(B))
+
+    def to_dev(a):
+        if a.dtype == np.uint16:
+            return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).to(dev)
+        return torch.from_numpy(np.ascontiguousarray(a)).to(dev)
+
+    k_host, v_host = w.pool_values("k"), w.pool_values("v")
+    dk, dv = to_dev(k_host), to_dev(v_host)
+
+    # ---- a1 once: the step's allocator outputs become device-resident inputs ----
+    t_alloc = time.perf_counter()
+    slots, pairs = lib.append_batch(ids)
+    tables, lens = lib.export_tables(ids, max_blocks)
+    host_alloc_us = (time.perf_counter() - t_alloc) * 1e6
+    q = w.queries(step=1)
+    k_new, v_new = w.new_tokens("k", B, step=1), w.new_tokens("v", B, step=1)
+    d_q, d_kn, d_vn = to_dev(q), to_dev(k_new), to_dev(v_new)
+    d_slots, d_tables, d_lens = to_dev(slots), to_dev(tables), to_dev(lens)
+    d_pairs = to_dev(pairs) if len(pairs) else None
+    out = torch.empty_like(d_q)
+    ws = torch.zeros(pa.pa_decode_workspace_bytes(B, Hq, Hkv, D), dtype=torch.uint8, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    max_len = int(lens.max())
+    stream = torch.cuda.current_stream()
+
+    def step():
+        if d_pairs is not None:
+            pa.pa_copy_blocks(dk, dv, d_pairs, status=ws[:4].view(torch.int32), stream=stream)
+        pa.pa_reshape_and_cache(d_kn, d_vn, dk, dv, d_slots, status=ws[:4].view(torch.int32), stream=stream)
+
+    def decode():
+        pa.pa_decode_attention(out, d_q, dk, dv, d_tables, d_lens, max_len, w.scale, ws, stream=stream)
+
+    for _ in range(Wm):
+        flush.zero_()
+        step()
+        decode()
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
+           torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    clocks = ClockSampler(local_rank)
+    clocks.start()
+    torch.cuda.synchronize()
+    for i in range(K):
+        flush.zero_()
+        ev[i][0].record(stream)
+        step()
+        ev[i][1].record(stream)
+        decode()
+        ev[i][2].record(stream)
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    clocks.stop()
+    step_ms = [a.elapsed_time(c) for a, b, c in ev]
+    dec_ms = [b.elapsed_time(c) for a, b, c in ev]
+    status = int(ws[:4].view(torch.int32).item())
+    if status:
+        raise SystemExit(f"device status word {status:#x}")
+    total_s = reduce_max(sum(step_ms) / 1e3, dist, dev)
+    tokens_step = int(np.sum(lens, dtype=np.int64))
+    all_tokens = reduce_sum(float(tokens_step * K), dist, dev)
+    value = all_tokens / total_s
+    dbytes = decode_bytes(lens, w)
+    dec_mean_s = statistics.mean(dec_ms) / 1e3
+    peak, peak_kind = measured_peaks()
+    achieved = dbytes / dec_mean_s / 1e9
+    ctas, stages, smem, mma = pa.pa_decode_launch_info(B, Hq, Hkv, D, bs, max_blocks, pa.PA_BF16)
+
+    # ---- e2e: genuine decode steps through the public API with host buffers ----
+    e2e_tokens, e2e_s, h2d, d2h = 0, 0.0, 0, 0
+    pin = lambda a: torch.from_numpy(np.ascontiguousarray(a)).pin_memory()  # noqa: E731
+    host_in = []
+    for s in range(K_e2e):
+        qs = w.queries(step=2 + s)
+        kn, vn = w.new_tokens("k", B, step=2 + s), w.new_tokens("v", B, step=2 + s)
+        host_in.append(tuple(pin(x.view(np.int16) if x.dtype == np.uint16 else x) for x in (qs, kn, vn)))
+    h_tables = torch.empty((B, max_blocks), dtype=torch.int32).pin_memory()
+    h_lens = torch.empty(B, dtype=torch.int32).pin_memory()
+    h_slots = torch.empty(B, dtype=torch.int64).pin_memory()
+    h_pairs = torch.empty((B, 2), dtype=torch.int32).pin_memory()
+    h_out = torch.empty((B, Hq, D), dtype=torch.int16).pin_memory()
+    e_tables = torch.empty((B, max_blocks), dtype=torch.int32, device=dev)
+    e_lens = torch.empty(B, dtype=torch.int32, device=dev)
+    e_slots = torch.empty(B, dtype=torch.int64, device=dev)
+    e_pairs = torch.empty((B, 2), dtype=torch.int32, device=dev)
+    e_q = torch.empty((B, Hq, D), dtype=torch.bfloat16, device=dev)
+    e_kn = torch.empty((B, Hkv, D), dtype=torch.bfloat16, device=dev)
+    e_vn = torch.empty((B, Hkv, D), dtype=torch.bfloat16, device=dev)
+    launches = 0
+    for s in range(K_e2e):
+        flush.zero_()
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        sl, pr = lib.append_batch(ids)
+        tb, ln = lib.export_tables(ids, max_blocks)
+        h_slots.numpy()[:] = sl
+        h_tables.numpy()[:] = tb
+        h_lens.numpy()[:] = ln
+        qs, kn, vn = host_in[s]
+        e_q.view(torch.int16).copy_(qs, non_blocking=True)
+        e_kn.view(torch.int16).copy_(kn, non_blocking=True)
+        e_vn.view(torch.int16).copy_(vn, non_blocking=True)
+        e_slots.copy_(h_slots, non_blocking=True)
+        e_tables.copy_(h_tables, non_blocking=True)
+        e_lens.copy_(h_lens, non_blocking=True)
+        nbytes = qs.numel() * 2 + kn.numel() * 2 + vn.numel() * 2 + B * 8 + tb.nbytes + B * 4
+        if len(pr):
+            h_pairs.numpy()[: len(pr)] = pr
+            e_pairs[: len(pr)].copy_(h_pairs[: len(pr)], non_blocking=True)
+            nbytes += len(pr) * 8
+            pa.pa_copy_blocks(dk, dv, e_pairs[: len(pr)], stream=stream)
+        pa.pa_reshape_and_cache(e_kn, e_vn, dk, dv, e_slots, stream=stream)
+        pa.pa_decode_attention(out, e_q, dk, dv, e_tables, e_lens, int(ln.max()), w.scale, ws, stream=stream)
+        h_out.copy_(out.view(torch.int16), non_blocking=True)
+        stream.synchronize()
+        e2e_s += time.perf_counter() - t0
+        e2e_tokens += int(np.sum(ln, dtype=np.int64))
+        h2d += nbytes
+        d2h += h_out.numel() * 2
+        launches += 2 + (1 if len(pr) else 0)
+    e2e_total = reduce_max(e2e_s, dist, dev)
+    e2e_value = reduce_sum(float(e2e_tokens), dist, dev) / e2e_total if K_e2e else None
+
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K, "warmup": Wm,
+        "ms_per_step": total_s * 1e3 / K, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16", "data": "synthetic (seeded; the pages' length mix, scattered 16-token blocks)",
+        "config": {
+            "workload": w.name if world == 1 else f"{w.name} per rank", "num_seqs_per_gpu": B, "num_q_heads": Hq,
+            "num_kv_heads": Hkv, "head_dim": D, "block_size": bs, "kv_tokens_per_step": tokens_step,
+            "decode_bytes_per_step": dbytes, "pool_blocks": w.num_blocks,
+            "l2": f"flushed between timed steps ({L2_FLUSH_BYTES >> 20} MiB write, untimed)",
+            "host_alloc_us_per_step": round(host_alloc_us, 1), "decode_ctas": ctas, "stages": stages,
+            "smem_bytes": smem, "path": "mma.sync" if mma else "fma",
+            "decode_ms_median": statistics.median(dec_ms), "decode_ms_min": min(dec_ms),
+            "step_gbs": (dbytes + 4 * B * Hkv * D * 2) / (total_s / K) / 1e9,
+        },
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+                     "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured" else "fallback",
+                     "kernel": "pa_decode_attention (decode_kernel)", "traffic": recorded_traffic()},
+        "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d // max(1, K_e2e),
+                "d2h_bytes_per_step": d2h // max(1, K_e2e), "steps": K_e2e,
+                "includes": "host allocator, pinned H2D of q/k_new/v_new/slots/tables/lens, kernels, D2H of out"},
+        "gpu_launches": K * (2 + (1 if d_pairs is not None else 0)),
+        "clocks": clocks.summary(),
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(w, q, k_host, v_host, tables, lens, args.cpu_seconds)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if dist:
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+# ---------------------------------------------------------------------------
+# reference arm: the oracle on the host cores, same metric and workload
+# ---------------------------------------------------------------------------
+def run_reference(args, rank, world):
+    if rank != 0:
+        return
+    import oracle
+    from oracle.alloc_model import RefAllocator
+
+    w = build_workload(args.workload, 0, 1, extra_steps=2)
+    B = w.num_seqs
+    ref = RefAllocator(w.num_blocks, w.block_size, free_order=w.free_order().tolist())
+    for s, n in enumerate(w.lengths):
+        ref.create(s)
+        ref.append(s, int(n))
+    ref.append_batch(list(range(B)))
+    max_blocks = int(-(-(int(w.lengths.max()) + 2) // w.block_size))
+    tables = np.zeros((B, max_blocks), np.int32)
+    for s in range(B):
+        t = ref.table(s)
+        tables[s, : len(t)] = t
+    lens = np.array([ref.length(s) for s in range(B)], np.int32)
+    k_pool, v_pool, q = w.pool_values("k"), w.pool_values("v"), w.queries(step=1)
+    threads = os.cpu_count() or 1
+    per_step = max(1, min(B, args.ref_seqs_per_step))
+    times, tokens = [], []
+    for i in range(args.warmup + args.steps):
+        seqs = [(i * per_step + j) % B for j in range(per_step)]
+        t0 = time.perf_counter()
+        oracle.decode_attention(q, k_pool, v_pool, tables, lens, w.scale, seqs=seqs, threads=threads)
+        dt = time.perf_counter() - t0
+        if i >= args.warmup:
+            times.append(dt)
+            tokens.append(int(sum(int(lens[s]) for s in seqs)))
+    value = sum(tokens) / sum(times)
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * sum(times) / len(times),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded; the pages' length mix, scattered 16-token blocks)",
+        "config": {"workload": w.name, "num_seqs_per_gpu": B, "num_q_heads": w.num_q_heads,
+                   "num_kv_heads": w.num_kv_heads, "head_dim": w.head_dim, "block_size": w.block_size},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle",
+                         "sample": f"{per_step} of the {B} sequences per step (rotating), fp64 C oracle, "
+                                   f"{threads} threads"},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=300)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="gqa4_b64")
+    ap.add_argument("--e2e-steps", type=int, default=32)
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--ref-seqs-per-step", type=int, default=16)
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        raise SystemExit("at least 3 warm-up steps")
+    rank, world, local_rank = dist_env()
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+    else:
+        run_ours(args, rank, world, local_rank)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,254 @@
+/*
+ * pa.h -- C ABI of the paged KV-cache library (single GB300, sm_103a).
+ *
+ * The library implements the data-parallel hot path of PagedAttention as the
+ * three PagedAttention pages describe it:
+ *   [P1] "Q32: vLLM PagedAttention 原理" (agentalpha.top/interview/basics-tk516)
+ *   [P2] "vLLM" (data.6616ai.com/article/vllm)
+ *   [P3] "batch-008-day-02-interview-1" (ohmygp.com/posts/...)
+ * Section names below refer to those pages.
+ *
+ * Conventions shared by every entry point
+ *   - Device pointers are plain CUDA device addresses owned by the caller.
+ *     The library never allocates, frees or retains device memory; each
+ *     call only reads and writes the buffers it is given.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ *     stream).  Device work is enqueued asynchronously on it; a PA_OK return
+ *     means "validated and launched", not "finished".
+ *   - Arguments are checked on the host before any launch; a failed check
+ *     returns an error status and launches nothing.  A failed launch returns
+ *     PA_ERR_CUDA.  No C++ exception crosses this interface.
+ *   - Faults the host cannot see (a block id or slot outside the pool, a
+ *     sequence length beyond its block table) are caught by bounds checks in
+ *     the kernels: the offending access is skipped or clamped to block 0, and
+ *     a bit is OR-ed into a caller-supplied int32 device status word
+ *     (PA_DEV_* below).  The kernels never trap.
+ *   - Layouts are contiguous row-major:
+ *       K pool, V pool   [num_blocks][num_kv_heads][block_size][head_dim]
+ *       q, out           [num_seqs][num_q_heads][head_dim]
+ *       k_new, v_new     [num_tokens][num_kv_heads][head_dim]
+ *       block_tables     int32 [num_seqs][max_blocks_per_seq]
+ *       seq_lens         int32 [num_seqs]
+ *       slot_mapping     int64 [num_tokens]
+ *       src_dst_pairs    int32 [num_pairs][2]
+ *     Device buffers must be 16-byte aligned.
+ *   - Supported shapes for the device kernels: block_size 16 or 32,
+ *     head_dim 64 or 128, num_q_heads a multiple of num_kv_heads with at most
+ *     8 query heads per KV head; element type fp32 or bf16.  Anything else
+ *     returns PA_ERR_UNSUPPORTED.
+ *   - The host allocator is not thread-safe; callers serialise access to one
+ *     allocator object.
+ */
+#ifndef PA_H
+#define PA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define PA_ABI_VERSION 1
+
+typedef enum pa_status {
+    PA_OK = 0,
+    PA_ERR_INVALID_ARG = 1,        /* null pointer, negative size, misaligned buffer, ... */
+    PA_ERR_UNSUPPORTED = 2,        /* shape or dtype outside the supported set */
+    PA_ERR_OUT_OF_BLOCKS = 3,      /* the pool has too few free blocks (state unchanged) */
+    PA_ERR_NO_SUCH_SEQ = 4,        /* unknown sequence id */
+    PA_ERR_SEQ_EXISTS = 5,         /* sequence id already in use */
+    PA_ERR_REFCOUNT_LIMIT = 6,     /* fork would push a block past the refcount cap */
+    PA_ERR_WORKSPACE_TOO_SMALL = 7,/* decode workspace smaller than pa_decode_workspace_bytes */
+    PA_ERR_BUFFER_TOO_SMALL = 8,   /* a host output array is too short */
+    PA_ERR_CUDA = 9,               /* a CUDA runtime call or launch failed */
+    PA_ERR_INTERNAL = 10           /* unexpected host failure (e.g. host memory exhausted) */
+} pa_status;
+
+typedef enum pa_dtype { PA_F32 = 0, PA_BF16 = 1 } pa_dtype;
+
+/* Bits of the device status word. */
+#define PA_DEV_BAD_BLOCK_ID 0x1 /* a block id outside [0, num_blocks) was read or given */
+#define PA_DEV_BAD_SLOT 0x2     /* a slot outside the pool was given */
+#define PA_DEV_BAD_SEQ_LEN 0x4  /* seq_lens[b] < 0, or beyond its block table or max_seq_len */
+#define PA_DEV_WAIT_TIMEOUT 0x8 /* an on-chip pipeline wait gave up (the output is not valid) */
+
+/* ------------------------------------------------------------------------ */
+/* Device kernels                                                            */
+/* ------------------------------------------------------------------------ */
+
+/*
+ * Slot-mapped append ("reshape_and_cache").
+ * [P3] 破局思路/按需分配: each decoded token takes one slot of the current
+ * block; [P1] §2 非连续存储: new tokens are written into the block, existing
+ * KV never moves.  For every token i with s = slot_mapping[i] >= 0:
+ *     k_pool[s / block_size][h][s % block_size][:] = k_new[i][h][:]   for all h
+ * and the same for V.  Negative slots are skipped (padding).  Bit-exact copy.
+ * A slot >= num_blocks * block_size sets PA_DEV_BAD_SLOT and is skipped.
+ * dev_status may be NULL (then out-of-range slots are skipped silently).
+ * Slots of one call must be distinct (two tokens writing one slot race).
+ */
+pa_status pa_reshape_and_cache(const void* k_new, const void* v_new, void* k_pool, void* v_pool,
+                               const int64_t* slot_mapping, int32_t num_tokens, int32_t num_kv_heads,
+                               int32_t head_dim, int32_t block_size, int32_t num_blocks, pa_dtype dtype,
+                               int32_t* dev_status, void* stream);
+
+/*
+ * Copy-on-write block copy.
+ * [P1] §3 Copy-on-Write, [P2] Copy-on-write 共享, [P3] 写时共享: a block shared
+ * by several sequences is copied to a new physical block when one of them
+ * writes into it.  For each pair p: pool[dst_p] = pool[src_p] over the whole
+ * block (every KV head, all block_size slots, all of head_dim), K and V.
+ * Bit-exact.  A block id outside [0, num_blocks) sets PA_DEV_BAD_BLOCK_ID and
+ * that pair is skipped.  Destinations must be distinct and no destination
+ * may be a source of the same call (the pairs are copied concurrently).
+ * Enqueue it before the pa_reshape_and_cache that writes the same step's
+ * tokens: a copy source may be written in place by its last sharer.
+ */
+pa_status pa_copy_blocks(void* k_pool, void* v_pool, const int32_t* src_dst_pairs, int32_t num_pairs,
+                         int32_t num_kv_heads, int32_t head_dim, int32_t block_size, int32_t num_blocks,
+                         pa_dtype dtype, int32_t* dev_status, void* stream);
+
+/*
+ * Size in bytes of the device workspace pa_decode_attention needs for these
+ * shapes on the current CUDA device.  The workspace holds the status word
+ * (first int32), one int32 merge counter per (sequence, KV head) and the
+ * split-sequence partial results.  The caller allocates it ONCE, zero-filled,
+ * and may reuse it across calls on one stream: every completed call leaves
+ * the counters at zero again.  Zero it again after a call that reported
+ * PA_DEV_WAIT_TIMEOUT.
+ */
+pa_status pa_decode_workspace_bytes(int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads,
+                                    int32_t head_dim, size_t* bytes_out);
+
+/*
+ * Paged decode attention, one query token per sequence.
+ * [P2] 把虚拟内存搬进 KV Cache: the attention kernel reads KV by block index,
+ * logically contiguous and physically scattered; [P1] follow-up 3
+ * (FlashAttention): KV is loaded block by block with the pointer indexing
+ * adapted to non-contiguous blocks.  For each sequence b and query head h,
+ * with g = h / (num_q_heads / num_kv_heads) and token t < seq_lens[b] in
+ * physical block block_tables[b][t / block_size] at offset t % block_size:
+ *     s_t = scale * q[b][h] . K[t],   out[b][h] = sum_t softmax(s)_t V[t]
+ * computed with an online (running max and sum) softmax in fp32, inputs in
+ * `dtype`, output in `dtype` (bf16 rounds to nearest even).  An empty
+ * sequence gives a zero output.
+ * Long sequences are split across CTAs (flash-decoding) and the partial
+ * results merged on the device.  partition_tokens = 0 splits anywhere on a
+ * block boundary to balance the work exactly; partition_tokens = P > 0
+ * (a multiple of block_size) allows splits only at multiples of P tokens.
+ * max_seq_len bounds every seq_lens[b]; a larger or negative length sets
+ * PA_DEV_BAD_SEQ_LEN and is clamped.  Table entries read for t < seq_len
+ * must be in [0, num_blocks); others set PA_DEV_BAD_BLOCK_ID.
+ * workspace: see pa_decode_workspace_bytes; its first int32 is the status
+ * word.  Concurrent calls must use different workspaces.
+ */
+pa_status pa_decode_attention(void* out, const void* q, const void* k_pool, const void* v_pool,
+                              const int32_t* block_tables, int32_t max_blocks_per_seq, const int32_t* seq_lens,
+                              int32_t max_seq_len, int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads,
+                              int32_t head_dim, int32_t block_size, int32_t num_blocks, float scale,
+                              int32_t partition_tokens, void* workspace, size_t workspace_bytes, pa_dtype dtype,
+                              void* stream);
+
+/*
+ * Launch facts of pa_decode_attention for these shapes on the current device
+ * (no launch): CTAs in the grid, pipeline stages per CTA, dynamic shared
+ * memory per CTA in bytes, and 1 if the tensor-core (mma) path is used, else
+ * 0 (CUDA-core FMA path).  Any output pointer may be NULL.
+ */
+pa_status pa_decode_launch_info(int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
+                                int32_t block_size, int32_t max_blocks_per_seq, pa_dtype dtype, int32_t* ctas,
+                                int32_t* stages, int32_t* smem_bytes, int32_t* uses_mma);
+
+/*
+ * Tuning: CTAs per SM of the decode grid (1..4; 0 restores the default, 2).
+ * Process-wide; affects later pa_decode_attention calls.  More CTAs per SM
+ * keep more tiles in flight but add split points (partials) at CTA edges.
+ */
+pa_status pa_decode_set_ctas_per_sm(int32_t ctas);
+
+/* ------------------------------------------------------------------------ */
+/* Host block allocator                                                      */
+/* ------------------------------------------------------------------------ */
+/*
+ * [P1] §2 分块管理/Block Table映射, [P2] 把虚拟内存搬进 KV Cache, [P3] 按需分配/
+ * 块表映射/写时共享.  Blocks are taken on demand, only when a sequence's tail
+ * block is full; each sequence keeps a block table (logical -> physical);
+ * forked sequences share blocks through reference counts, and a write into
+ * a block with refcount > 1 first copies it (copy-on-write).
+ * Readings of points the pages leave open:
+ *   - The free list is a FIFO queue: allocation pops the front, a freed block
+ *     is pushed at the back.  Its initial order is the caller's (free_order),
+ *     or 0..num_blocks-1.
+ *   - Append of one token to sequence s with length n: if n % block_size == 0
+ *     a new block is pushed onto the table; otherwise, if the tail block's
+ *     refcount is > 1, a new block d is taken, the pair (tail, d) is emitted,
+ *     the tail's refcount drops by one and the table entry points at d.  The
+ *     token's slot is table[n / block_size] * block_size + n % block_size.
+ *     So the last remaining sharer writes in place and a full shared block
+ *     is never copied.
+ *   - Fork copies the parent's table and length, adding one reference to
+ *     each block.  Free walks the table in logical order, dropping one
+ *     reference per block; blocks reaching zero go to the back of the free
+ *     list.
+ *   - Every call is all-or-nothing: on any error the allocator is unchanged.
+ * The allocator owns only host memory.
+ */
+typedef struct pa_allocator pa_allocator;
+
+typedef struct pa_alloc_stats_t {
+    int32_t num_blocks;
+    int32_t block_size;
+    int32_t free_blocks;
+    int32_t used_blocks;   /* blocks with refcount > 0 */
+    int32_t shared_blocks; /* blocks with refcount > 1 */
+    int32_t num_seqs;
+    int64_t tokens;        /* sum of the live sequences' lengths */
+    int64_t slots;         /* used_blocks * block_size */
+    int64_t cow_copies;    /* copy-on-write pairs emitted since creation */
+} pa_alloc_stats_t;
+
+/* free_order: num_blocks distinct ids (a permutation of 0..num_blocks-1), or NULL. */
+pa_status pa_alloc_create(int32_t num_blocks, int32_t block_size, const int32_t* free_order, pa_allocator** out);
+void pa_alloc_destroy(pa_allocator* a);
+/* Optional cap on a block's refcount (0 = none); fork fails with PA_ERR_REFCOUNT_LIMIT past it. */
+pa_status pa_alloc_set_max_refcount(pa_allocator* a, int32_t max_refcount);
+pa_status pa_seq_create(pa_allocator* a, int64_t seq_id);
+/*
+ * Append n_tokens to one sequence.  slots_out receives n_tokens slots;
+ * cow_pairs_out receives up to n_tokens (src, dst) pairs (at most one per
+ * call is possible) and *n_cow_out their count.
+ */
+pa_status pa_seq_append(pa_allocator* a, int64_t seq_id, int32_t n_tokens, int64_t* slots_out,
+                        int32_t* cow_pairs_out, int32_t* n_cow_out);
+/* One token for each of n ids, processed in the given order; arrays as above, sized n. */
+pa_status pa_append_batch(pa_allocator* a, const int64_t* seq_ids, int32_t n, int64_t* slots_out,
+                          int32_t* cow_pairs_out, int32_t* n_cow_out);
+pa_status pa_seq_fork(pa_allocator* a, int64_t parent, int64_t child);
+pa_status pa_seq_free(pa_allocator* a, int64_t seq_id);
+/* Copies the block table (cap entries at most) and its length into *n_out. */
+pa_status pa_seq_block_table(const pa_allocator* a, int64_t seq_id, int32_t* out, int32_t cap, int32_t* n_out);
+pa_status pa_seq_len(const pa_allocator* a, int64_t seq_id, int32_t* len_out);
+/*
+ * Block tables and lengths of n sequences in the layout pa_decode_attention
+ * reads: tables_out [n][max_blocks_per_seq] (unused entries set to 0) and
+ * lens_out [n].  PA_ERR_BUFFER_TOO_SMALL if a table is longer than
+ * max_blocks_per_seq.
+ */
+pa_status pa_export_tables(const pa_allocator* a, const int64_t* seq_ids, int32_t n, int32_t max_blocks_per_seq,
+                           int32_t* tables_out, int32_t* lens_out);
+/* Refcount of a block, or -1 if the id is out of range. */
+int32_t pa_block_refcount(const pa_allocator* a, int32_t block);
+pa_status pa_alloc_stats(const pa_allocator* a, pa_alloc_stats_t* out);
+/* The free list in pop order (cap entries at most); count in *n_out. */
+pa_status pa_alloc_free_list(const pa_allocator* a, int32_t* out, int32_t cap, int32_t* n_out);
+
+/* ------------------------------------------------------------------------ */
+const char* pa_status_str(pa_status s);
+int32_t pa_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PA_H */

@@ -1,0 +1,282 @@
+"""Python binding of libpa, the paged KV-cache library for one GB300 (sm_103a).
+
+Argument marshalling only: every function here passes tensor data pointers,
+sizes and the current CUDA stream to the C ABI declared in ``include/pa.h``
+and raises :class:`PAError` on a non-OK status.  All device work happens in
+the library's CUDA kernels; there is no fallback path.  The library is built
+in-tree by ``__graft_entry__.build()`` (or ``python -m
+paged_kv_cache_280_gb300._build``); importing this package without it raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libpa.so")
+
+if not os.path.exists(LIB_PATH):
+    raise ImportError(
+        f"{LIB_PATH} is missing: build it first (python -m paged_kv_cache_280_gb300._build)"
+    )
+
+_lib = ctypes.CDLL(LIB_PATH)
+
+PA_F32, PA_BF16 = 0, 1
+PA_DEV_BAD_BLOCK_ID, PA_DEV_BAD_SLOT, PA_DEV_BAD_SEQ_LEN, PA_DEV_WAIT_TIMEOUT = 1, 2, 4, 8
+STATUS_NAMES = {
+    0: "PA_OK", 1: "PA_ERR_INVALID_ARG", 2: "PA_ERR_UNSUPPORTED", 3: "PA_ERR_OUT_OF_BLOCKS",
+    4: "PA_ERR_NO_SUCH_SEQ", 5: "PA_ERR_SEQ_EXISTS", 6: "PA_ERR_REFCOUNT_LIMIT",
+    7: "PA_ERR_WORKSPACE_TOO_SMALL", 8: "PA_ERR_BUFFER_TOO_SMALL", 9: "PA_ERR_CUDA", 10: "PA_ERR_INTERNAL",
+}
+
+
+class PAError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        self.name = STATUS_NAMES.get(status, str(status))
+        super().__init__(f"{where}: {self.name} ({_lib.pa_status_str(status).decode()})")
+
+
+class pa_alloc_stats_t(ctypes.Structure):
+    _fields_ = [
+        ("num_blocks", ctypes.c_int32), ("block_size", ctypes.c_int32), ("free_blocks", ctypes.c_int32),
+        ("used_blocks", ctypes.c_int32), ("shared_blocks", ctypes.c_int32), ("num_seqs", ctypes.c_int32),
+        ("tokens", ctypes.c_int64), ("slots", ctypes.c_int64), ("cow_copies", ctypes.c_int64),
+    ]
+
+
+_i32, _i64, _f32, _vp, _sz = ctypes.c_int32, ctypes.c_int64, ctypes.c_float, ctypes.c_void_p, ctypes.c_size_t
+_pi32, _pi64, _psz = ctypes.POINTER(_i32), ctypes.POINTER(_i64), ctypes.POINTER(_sz)
+
+_SIGS = {
+    "pa_reshape_and_cache": (_i32, [_vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _i32, _i32, _vp, _vp]),
+    "pa_copy_blocks": (_i32, [_vp, _vp, _vp, _i32, _i32, _i32, _i32, _i32, _i32, _vp, _vp]),
+    "pa_decode_workspace_bytes": (_i32, [_i32, _i32, _i32, _i32, _psz]),
+    "pa_decode_attention": (_i32, [_vp, _vp, _vp, _vp, _vp, _i32, _vp, _i32, _i32, _i32, _i32, _i32, _i32, _i32,
+                                   _f32, _i32, _vp, _sz, _i32, _vp]),
+    "pa_decode_launch_info": (_i32, [_i32, _i32, _i32, _i32, _i32, _i32, _i32, _pi32, _pi32, _pi32, _pi32]),
+    "pa_decode_set_ctas_per_sm": (_i32, [_i32]),
+    "pa_alloc_create": (_i32, [_i32, _i32, _vp, ctypes.POINTER(_vp)]),
+    "pa_alloc_destroy": (None, [_vp]),
+    "pa_alloc_set_max_refcount": (_i32, [_vp, _i32]),
+    "pa_seq_create": (_i32, [_vp, _i64]),
+    "pa_seq_append": (_i32, [_vp, _i64, _i32, _vp, _vp, _pi32]),
+    "pa_append_batch": (_i32, [_vp, _vp, _i32, _vp, _vp, _pi32]),
+    "pa_seq_fork": (_i32, [_vp, _i64, _i64]),
+    "pa_seq_free": (_i32, [_vp, _i64]),
+    "pa_seq_block_table": (_i32, [_vp, _i64, _vp, _i32, _pi32]),
+    "pa_seq_len": (_i32, [_vp, _i64, _pi32]),
+    "pa_export_tables": (_i32, [_vp, _vp, _i32, _i32, _vp, _vp]),
+    "pa_block_refcount": (_i32, [_vp, _i32]),
+    "pa_alloc_stats": (_i32, [_vp, ctypes.POINTER(pa_alloc_stats_t)]),
+    "pa_alloc_free_list": (_i32, [_vp, _vp, _i32, _pi32]),
+    "pa_status_str": (ctypes.c_char_p, [_i32]),
+    "pa_abi_version": (_i32, []),
+}
+for _name, (_res, _args) in _SIGS.items():
+    _fn = getattr(_lib, _name)
+    _fn.restype = _res
+    _fn.argtypes = _args
+
+
+def _ok(status: int, where: str) -> None:
+    if status != 0:
+        raise PAError(status, where)
+
+
+def abi_version() -> int:
+    return int(_lib.pa_abi_version())
+
+
+# ---------------------------------------------------------------------------
+# device entry points (torch tensors on the current CUDA device)
+# ---------------------------------------------------------------------------
+
+def _torch():
+    import torch
+
+    return torch
+
+
+def _dtype_code(t) -> int:
+    torch = _torch()
+    if t.dtype == torch.float32:
+        return PA_F32
+    if t.dtype == torch.bfloat16:
+        return PA_BF16
+    raise PAError(2, f"dtype {t.dtype}")
+
+
+def _dev_ptr(t, name: str) -> int:
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    return t.data_ptr()
+
+
+def _stream(stream) -> int:
+    torch = _torch()
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def pa_reshape_and_cache(k_new, v_new, k_pool, v_pool, slot_mapping, status=None, stream=None):
+    """k_new/v_new [N][Hkv][D]; pools [num_blocks][Hkv][bs][D]; slot_mapping int64 [N]."""
+    nb, hkv, bs, d = k_pool.shape
+    n = slot_mapping.shape[0]
+    _ok(_lib.pa_reshape_and_cache(_dev_ptr(k_new, "k_new"), _dev_ptr(v_new, "v_new"), _dev_ptr(k_pool, "k_pool"),
+                                  _dev_ptr(v_pool, "v_pool"), _dev_ptr(slot_mapping, "slot_mapping"), n, hkv, d, bs,
+                                  nb, _dtype_code(k_pool), _dev_ptr(status, "status"), _stream(stream)),
+        "pa_reshape_and_cache")
+
+
+def pa_copy_blocks(k_pool, v_pool, src_dst_pairs, status=None, stream=None):
+    """src_dst_pairs int32 [n][2] on the device."""
+    nb, hkv, bs, d = k_pool.shape
+    n = src_dst_pairs.shape[0]
+    _ok(_lib.pa_copy_blocks(_dev_ptr(k_pool, "k_pool"), _dev_ptr(v_pool, "v_pool"),
+                            _dev_ptr(src_dst_pairs, "src_dst_pairs"), n, hkv, d, bs, nb, _dtype_code(k_pool),
+                            _dev_ptr(status, "status"), _stream(stream)),
+        "pa_copy_blocks")
+
+
+def pa_decode_workspace_bytes(num_seqs, num_q_heads, num_kv_heads, head_dim) -> int:
+    out = _sz(0)
+    _ok(_lib.pa_decode_workspace_bytes(num_seqs, num_q_heads, num_kv_heads, head_dim, ctypes.byref(out)),
+        "pa_decode_workspace_bytes")
+    return int(out.value)
+
+
+def pa_decode_attention(out, q, k_pool, v_pool, block_tables, seq_lens, max_seq_len, scale, workspace,
+                        partition_tokens=0, stream=None):
+    """out/q [B][Hq][D]; pools [num_blocks][Hkv][bs][D]; block_tables int32 [B][max_blocks]; seq_lens int32 [B];
+    workspace: a zero-initialised uint8 CUDA tensor of pa_decode_workspace_bytes bytes."""
+    b, hq, d = q.shape
+    nb, hkv, bs, _ = k_pool.shape
+    _ok(_lib.pa_decode_attention(_dev_ptr(out, "out"), _dev_ptr(q, "q"), _dev_ptr(k_pool, "k_pool"),
+                                 _dev_ptr(v_pool, "v_pool"), _dev_ptr(block_tables, "block_tables"),
+                                 block_tables.shape[1], _dev_ptr(seq_lens, "seq_lens"), int(max_seq_len), b, hq, hkv,
+                                 d, bs, nb, float(scale), int(partition_tokens), _dev_ptr(workspace, "workspace"),
+                                 workspace.numel() * workspace.element_size(), _dtype_code(q), _stream(stream)),
+        "pa_decode_attention")
+
+
+def pa_decode_launch_info(num_seqs, num_q_heads, num_kv_heads, head_dim, block_size, max_blocks_per_seq, dtype):
+    """(ctas, stages, smem_bytes, uses_mma) for these shapes on the current device; dtype is PA_F32/PA_BF16."""
+    vals = [_i32(0) for _ in range(4)]
+    _ok(_lib.pa_decode_launch_info(num_seqs, num_q_heads, num_kv_heads, head_dim, block_size, max_blocks_per_seq,
+                                   dtype, *[ctypes.byref(v) for v in vals]),
+        "pa_decode_launch_info")
+    return tuple(int(v.value) for v in vals)
+
+
+def pa_decode_set_ctas_per_sm(ctas: int) -> None:
+    _ok(_lib.pa_decode_set_ctas_per_sm(int(ctas)), "pa_decode_set_ctas_per_sm")
+
+
+# ---------------------------------------------------------------------------
+# host allocator
+# ---------------------------------------------------------------------------
+
+def _np():
+    import numpy as np
+
+    return np
+
+
+class Allocator:
+    """Host block allocator (pa_alloc_*): on-demand blocks, block tables, refcounts, copy-on-write."""
+
+    def __init__(self, num_blocks: int, block_size: int, free_order=None, max_refcount: int = 0):
+        np = _np()
+        self._h = _vp()
+        order = None
+        if free_order is not None:
+            order = np.ascontiguousarray(np.asarray(free_order, dtype=np.int32))
+            if order.shape != (num_blocks,):
+                raise ValueError("free_order must hold num_blocks ids")
+        _ok(_lib.pa_alloc_create(num_blocks, block_size, None if order is None else order.ctypes.data,
+                                 ctypes.byref(self._h)), "pa_alloc_create")
+        self.num_blocks = num_blocks
+        self.block_size = block_size
+        if max_refcount:
+            _ok(_lib.pa_alloc_set_max_refcount(self._h, max_refcount), "pa_alloc_set_max_refcount")
+
+    def __del__(self):
+        h = getattr(self, "_h", None)
+        if h is not None and h.value:
+            _lib.pa_alloc_destroy(h)
+            self._h = None
+
+    def create(self, seq_id: int) -> None:
+        _ok(_lib.pa_seq_create(self._h, seq_id), "pa_seq_create")
+
+    def append(self, seq_id: int, n_tokens: int):
+        """Returns (slots int64 [n], cow_pairs int32 [k][2])."""
+        np = _np()
+        slots = np.empty(max(1, n_tokens), np.int64)
+        pairs = np.empty((max(1, n_tokens), 2), np.int32)
+        n_cow = _i32(0)
+        _ok(_lib.pa_seq_append(self._h, seq_id, n_tokens, slots.ctypes.data, pairs.ctypes.data, ctypes.byref(n_cow)),
+            "pa_seq_append")
+        return slots[:n_tokens], pairs[: n_cow.value]
+
+    def append_batch(self, seq_ids):
+        np = _np()
+        ids = np.ascontiguousarray(np.asarray(seq_ids, dtype=np.int64))
+        n = len(ids)
+        slots = np.empty(max(1, n), np.int64)
+        pairs = np.empty((max(1, n), 2), np.int32)
+        n_cow = _i32(0)
+        _ok(_lib.pa_append_batch(self._h, ids.ctypes.data, n, slots.ctypes.data, pairs.ctypes.data,
+                                 ctypes.byref(n_cow)), "pa_append_batch")
+        return slots[:n], pairs[: n_cow.value]
+
+    def fork(self, parent: int, child: int) -> None:
+        _ok(_lib.pa_seq_fork(self._h, parent, child), "pa_seq_fork")
+
+    def free_seq(self, seq_id: int) -> None:
+        _ok(_lib.pa_seq_free(self._h, seq_id), "pa_seq_free")
+
+    def length(self, seq_id: int) -> int:
+        n = _i32(0)
+        _ok(_lib.pa_seq_len(self._h, seq_id, ctypes.byref(n)), "pa_seq_len")
+        return int(n.value)
+
+    def table(self, seq_id: int):
+        np = _np()
+        cap = self.length(seq_id) // self.block_size + 1
+        out = np.empty(max(1, cap), np.int32)
+        n = _i32(0)
+        _ok(_lib.pa_seq_block_table(self._h, seq_id, out.ctypes.data, cap, ctypes.byref(n)), "pa_seq_block_table")
+        return out[: n.value].tolist()
+
+    def export_tables(self, seq_ids, max_blocks_per_seq: int):
+        """(tables int32 [n][max_blocks_per_seq], lens int32 [n]) in the decode kernel's layout."""
+        np = _np()
+        ids = np.ascontiguousarray(np.asarray(seq_ids, dtype=np.int64))
+        tables = np.empty((len(ids), max_blocks_per_seq), np.int32)
+        lens = np.empty(len(ids), np.int32)
+        _ok(_lib.pa_export_tables(self._h, ids.ctypes.data, len(ids), max_blocks_per_seq, tables.ctypes.data,
+                                  lens.ctypes.data), "pa_export_tables")
+        return tables, lens
+
+    def refcount(self, block: int) -> int:
+        return int(_lib.pa_block_refcount(self._h, block))
+
+    def free_list(self):
+        np = _np()
+        out = np.empty(max(1, self.num_blocks), np.int32)
+        n = _i32(0)
+        _ok(_lib.pa_alloc_free_list(self._h, out.ctypes.data, self.num_blocks, ctypes.byref(n)), "pa_alloc_free_list")
+        return out[: n.value].tolist()
+
+    def stats(self) -> dict:
+        s = pa_alloc_stats_t()
+        _ok(_lib.pa_alloc_stats(self._h, ctypes.byref(s)), "pa_alloc_stats")
+        return {name: int(getattr(s, name)) for name, _ in s._fields_}

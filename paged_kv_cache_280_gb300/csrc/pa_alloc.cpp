@@ -1,0 +1,329 @@
+// Host block allocator of the paged KV cache (C ABI in include/pa.h).
+//
+// Pages: "Q32: vLLM PagedAttention 原理" §2 (分块管理, Block Table映射, 非连续存储)
+// and §3 (Copy-on-Write); data.6616ai.com "把虚拟内存搬进 KV Cache" and
+// "Copy-on-write 共享"; ohmygp.com "破局思路" (按需分配, 块表映射, 写时共享).
+//
+// State: a FIFO free list kept as a ring buffer over num_blocks entries (each
+// free block appears exactly once), one refcount per block, and per sequence
+// its block table and length.  Every public call first checks that it can
+// succeed (a dry run of the block demand) and only then mutates, so a failing
+// call leaves the allocator unchanged.
+#include <algorithm>
+#include <cstring>
+#include <new>
+#include <unordered_map>
+#include <vector>
+
+#include "../../include/pa.h"
+
+namespace {
+
+struct Sequence {
+    std::vector<int32_t> table;  // logical block -> physical block
+    int32_t len = 0;             // tokens written
+};
+
+}  // namespace
+
+struct pa_allocator {
+    int32_t num_blocks = 0;
+    int32_t block_size = 0;
+    int32_t max_refcount = 0;  // 0 = no cap
+    std::vector<int32_t> ring;  // free list storage
+    int32_t head = 0;           // index of the next block to pop
+    int32_t free_count = 0;
+    std::vector<int32_t> refcount;
+    std::unordered_map<int64_t, Sequence> seqs;
+    int64_t cow_copies = 0;
+
+    int32_t pop_free() {
+        int32_t b = ring[head];
+        head = (head + 1) % num_blocks;
+        --free_count;
+        refcount[b] = 1;
+        return b;
+    }
+    void push_free(int32_t b) {
+        ring[(head + free_count) % num_blocks] = b;
+        ++free_count;
+    }
+    // Blocks one append of n tokens to `s` will take: the blocks newly
+    // started plus one copy if the first token lands in a shared tail.
+    int64_t demand(const Sequence& s, int32_t n, int32_t tail_refs) const {
+        if (n <= 0) return 0;
+        int64_t before = (s.len + block_size - 1) / block_size;
+        int64_t after = ((int64_t)s.len + n + block_size - 1) / block_size;
+        int64_t copy = (s.len % block_size != 0 && tail_refs > 1) ? 1 : 0;
+        return (after - before) + copy;
+    }
+    // One token; caller guarantees a free block is available when needed.
+    void append_one(Sequence& s, int64_t* slot, int32_t* pairs, int32_t* n_pairs) {
+        const int32_t off = s.len % block_size;
+        if (off == 0) {
+            s.table.push_back(pop_free());
+        } else {
+            int32_t& tail = s.table.back();
+            if (refcount[tail] > 1) {
+                int32_t fresh = pop_free();
+                pairs[2 * *n_pairs] = tail;
+                pairs[2 * *n_pairs + 1] = fresh;
+                ++*n_pairs;
+                --refcount[tail];
+                tail = fresh;
+                ++cow_copies;
+            }
+        }
+        *slot = (int64_t)s.table[s.len / block_size] * block_size + off;
+        ++s.len;
+    }
+};
+
+#define PA_GUARD_BEGIN try {
+#define PA_GUARD_END                \
+    }                               \
+    catch (const std::bad_alloc&) { \
+        return PA_ERR_INTERNAL;     \
+    }                               \
+    catch (...) {                   \
+        return PA_ERR_INTERNAL;     \
+    }
+
+extern "C" {
+
+pa_status pa_alloc_create(int32_t num_blocks, int32_t block_size, const int32_t* free_order, pa_allocator** out) {
+    if (!out || num_blocks <= 0 || block_size <= 0) return PA_ERR_INVALID_ARG;
+    *out = nullptr;
+    PA_GUARD_BEGIN
+    pa_allocator* a = new pa_allocator();
+    a->num_blocks = num_blocks;
+    a->block_size = block_size;
+    a->ring.resize(num_blocks);
+    a->refcount.assign(num_blocks, 0);
+    if (free_order) {
+        std::vector<char> seen(num_blocks, 0);
+        for (int32_t i = 0; i < num_blocks; ++i) {
+            int32_t b = free_order[i];
+            if (b < 0 || b >= num_blocks || seen[b]) {
+                delete a;
+                return PA_ERR_INVALID_ARG;
+            }
+            seen[b] = 1;
+            a->ring[i] = b;
+        }
+    } else {
+        for (int32_t i = 0; i < num_blocks; ++i) a->ring[i] = i;
+    }
+    a->head = 0;
+    a->free_count = num_blocks;
+    *out = a;
+    return PA_OK;
+    PA_GUARD_END
+}
+
+void pa_alloc_destroy(pa_allocator* a) { delete a; }
+
+pa_status pa_alloc_set_max_refcount(pa_allocator* a, int32_t max_refcount) {
+    if (!a || max_refcount < 0) return PA_ERR_INVALID_ARG;
+    a->max_refcount = max_refcount;
+    return PA_OK;
+}
+
+pa_status pa_seq_create(pa_allocator* a, int64_t seq_id) {
+    if (!a) return PA_ERR_INVALID_ARG;
+    PA_GUARD_BEGIN
+    if (a->seqs.count(seq_id)) return PA_ERR_SEQ_EXISTS;
+    a->seqs.emplace(seq_id, Sequence());
+    return PA_OK;
+    PA_GUARD_END
+}
+
+pa_status pa_seq_append(pa_allocator* a, int64_t seq_id, int32_t n_tokens, int64_t* slots_out,
+                        int32_t* cow_pairs_out, int32_t* n_cow_out) {
+    if (!a || n_tokens < 0 || (n_tokens > 0 && (!slots_out || !cow_pairs_out)) || !n_cow_out)
+        return PA_ERR_INVALID_ARG;
+    PA_GUARD_BEGIN
+    auto it = a->seqs.find(seq_id);
+    if (it == a->seqs.end()) return PA_ERR_NO_SUCH_SEQ;
+    Sequence& s = it->second;
+    if ((int64_t)s.len + n_tokens > INT32_MAX) return PA_ERR_INVALID_ARG;
+    int32_t tail_refs = s.table.empty() ? 0 : a->refcount[s.table.back()];
+    if (a->demand(s, n_tokens, tail_refs) > a->free_count) return PA_ERR_OUT_OF_BLOCKS;
+    s.table.reserve((s.len + n_tokens + a->block_size - 1) / a->block_size);
+    *n_cow_out = 0;
+    for (int32_t i = 0; i < n_tokens; ++i) a->append_one(s, &slots_out[i], cow_pairs_out, n_cow_out);
+    return PA_OK;
+    PA_GUARD_END
+}
+
+pa_status pa_append_batch(pa_allocator* a, const int64_t* seq_ids, int32_t n, int64_t* slots_out,
+                          int32_t* cow_pairs_out, int32_t* n_cow_out) {
+    if (!a || n < 0 || (n > 0 && (!seq_ids || !slots_out || !cow_pairs_out)) || !n_cow_out)
+        return PA_ERR_INVALID_ARG;
+    PA_GUARD_BEGIN
+    // Dry run: the same id may appear more than once, and a copy made for an
+    // earlier id lowers the refcount a later sharer sees.
+    struct Shadow {
+        Sequence* s;
+        int32_t len;
+        bool tail_private;  // the tail is known to have refcount 1 at this point
+    };
+    std::unordered_map<int64_t, Shadow> shadow;
+    std::unordered_map<int32_t, int32_t> ref_drop;  // copies made so far per shared block
+    shadow.reserve(n * 2);
+    int64_t need = 0;
+    for (int32_t i = 0; i < n; ++i) {
+        auto f = shadow.find(seq_ids[i]);
+        if (f == shadow.end()) {
+            auto it = a->seqs.find(seq_ids[i]);
+            if (it == a->seqs.end()) return PA_ERR_NO_SUCH_SEQ;
+            f = shadow.emplace(seq_ids[i], Shadow{&it->second, it->second.len, false}).first;
+        }
+        Shadow& sh = f->second;
+        if (sh.len % a->block_size == 0) {
+            ++need;
+            sh.tail_private = true;
+        } else if (!sh.tail_private) {
+            int32_t tail = sh.s->table.back();
+            int32_t refs = a->refcount[tail] - ref_drop[tail];
+            if (refs > 1) {
+                ++need;
+                ++ref_drop[tail];
+            }
+            sh.tail_private = true;
+        }
+        if (sh.len == INT32_MAX) return PA_ERR_INVALID_ARG;
+        ++sh.len;
+    }
+    if (need > a->free_count) return PA_ERR_OUT_OF_BLOCKS;
+    for (auto& kv : shadow)  // so that the mutating loop below cannot fail half-way
+        kv.second.s->table.reserve((kv.second.len + a->block_size - 1) / a->block_size);
+    *n_cow_out = 0;
+    for (int32_t i = 0; i < n; ++i) {
+        Sequence& s = a->seqs.find(seq_ids[i])->second;
+        a->append_one(s, &slots_out[i], cow_pairs_out, n_cow_out);
+    }
+    return PA_OK;
+    PA_GUARD_END
+}
+
+pa_status pa_seq_fork(pa_allocator* a, int64_t parent, int64_t child) {
+    if (!a) return PA_ERR_INVALID_ARG;
+    PA_GUARD_BEGIN
+    auto it = a->seqs.find(parent);
+    if (it == a->seqs.end()) return PA_ERR_NO_SUCH_SEQ;
+    if (a->seqs.count(child)) return PA_ERR_SEQ_EXISTS;
+    if (a->max_refcount > 0)
+        for (int32_t b : it->second.table)
+            if (a->refcount[b] + 1 > a->max_refcount) return PA_ERR_REFCOUNT_LIMIT;
+    Sequence copy = it->second;  // may throw before any state changes
+    for (int32_t b : copy.table) ++a->refcount[b];
+    a->seqs.emplace(child, std::move(copy));
+    return PA_OK;
+    PA_GUARD_END
+}
+
+pa_status pa_seq_free(pa_allocator* a, int64_t seq_id) {
+    if (!a) return PA_ERR_INVALID_ARG;
+    PA_GUARD_BEGIN
+    auto it = a->seqs.find(seq_id);
+    if (it == a->seqs.end()) return PA_ERR_NO_SUCH_SEQ;
+    for (int32_t b : it->second.table)
+        if (--a->refcount[b] == 0) a->push_free(b);
+    a->seqs.erase(it);
+    return PA_OK;
+    PA_GUARD_END
+}
+
+pa_status pa_seq_block_table(const pa_allocator* a, int64_t seq_id, int32_t* out, int32_t cap, int32_t* n_out) {
+    if (!a || !n_out || cap < 0 || (cap > 0 && !out)) return PA_ERR_INVALID_ARG;
+    PA_GUARD_BEGIN
+    auto it = a->seqs.find(seq_id);
+    if (it == a->seqs.end()) return PA_ERR_NO_SUCH_SEQ;
+    const auto& t = it->second.table;
+    *n_out = (int32_t)t.size();
+    if ((int32_t)t.size() > cap) return PA_ERR_BUFFER_TOO_SMALL;
+    std::copy(t.begin(), t.end(), out);
+    return PA_OK;
+    PA_GUARD_END
+}
+
+pa_status pa_seq_len(const pa_allocator* a, int64_t seq_id, int32_t* len_out) {
+    if (!a || !len_out) return PA_ERR_INVALID_ARG;
+    PA_GUARD_BEGIN
+    auto it = a->seqs.find(seq_id);
+    if (it == a->seqs.end()) return PA_ERR_NO_SUCH_SEQ;
+    *len_out = it->second.len;
+    return PA_OK;
+    PA_GUARD_END
+}
+
+pa_status pa_export_tables(const pa_allocator* a, const int64_t* seq_ids, int32_t n, int32_t max_blocks_per_seq,
+                           int32_t* tables_out, int32_t* lens_out) {
+    if (!a || n < 0 || max_blocks_per_seq <= 0 || (n > 0 && (!seq_ids || !tables_out || !lens_out)))
+        return PA_ERR_INVALID_ARG;
+    PA_GUARD_BEGIN
+    for (int32_t i = 0; i < n; ++i) {
+        auto it = a->seqs.find(seq_ids[i]);
+        if (it == a->seqs.end()) return PA_ERR_NO_SUCH_SEQ;
+        if ((int32_t)it->second.table.size() > max_blocks_per_seq) return PA_ERR_BUFFER_TOO_SMALL;
+    }
+    for (int32_t i = 0; i < n; ++i) {
+        const Sequence& s = a->seqs.find(seq_ids[i])->second;
+        int32_t* row = tables_out + (size_t)i * max_blocks_per_seq;
+        std::copy(s.table.begin(), s.table.end(), row);
+        std::fill(row + s.table.size(), row + max_blocks_per_seq, 0);
+        lens_out[i] = s.len;
+    }
+    return PA_OK;
+    PA_GUARD_END
+}
+
+int32_t pa_block_refcount(const pa_allocator* a, int32_t block) {
+    if (!a || block < 0 || block >= a->num_blocks) return -1;
+    return a->refcount[block];
+}
+
+pa_status pa_alloc_stats(const pa_allocator* a, pa_alloc_stats_t* out) {
+    if (!a || !out) return PA_ERR_INVALID_ARG;
+    std::memset(out, 0, sizeof *out);
+    out->num_blocks = a->num_blocks;
+    out->block_size = a->block_size;
+    out->free_blocks = a->free_count;
+    out->used_blocks = a->num_blocks - a->free_count;
+    for (int32_t r : a->refcount) out->shared_blocks += (r > 1);
+    out->num_seqs = (int32_t)a->seqs.size();
+    for (const auto& kv : a->seqs) out->tokens += kv.second.len;
+    out->slots = (int64_t)out->used_blocks * a->block_size;
+    out->cow_copies = a->cow_copies;
+    return PA_OK;
+}
+
+pa_status pa_alloc_free_list(const pa_allocator* a, int32_t* out, int32_t cap, int32_t* n_out) {
+    if (!a || !n_out || cap < 0 || (cap > 0 && !out)) return PA_ERR_INVALID_ARG;
+    *n_out = a->free_count;
+    if (a->free_count > cap) return PA_ERR_BUFFER_TOO_SMALL;
+    for (int32_t i = 0; i < a->free_count; ++i) out[i] = a->ring[(a->head + i) % a->num_blocks];
+    return PA_OK;
+}
+
+const char* pa_status_str(pa_status s) {
+    switch (s) {
+        case PA_OK: return "ok";
+        case PA_ERR_INVALID_ARG: return "invalid argument";
+        case PA_ERR_UNSUPPORTED: return "unsupported shape or dtype";
+        case PA_ERR_OUT_OF_BLOCKS: return "out of free blocks";
+        case PA_ERR_NO_SUCH_SEQ: return "no such sequence";
+        case PA_ERR_SEQ_EXISTS: return "sequence already exists";
+        case PA_ERR_REFCOUNT_LIMIT: return "refcount limit reached";
+        case PA_ERR_WORKSPACE_TOO_SMALL: return "decode workspace too small";
+        case PA_ERR_BUFFER_TOO_SMALL: return "output buffer too small";
+        case PA_ERR_CUDA: return "CUDA error";
+        case PA_ERR_INTERNAL: return "internal error";
+    }
+    return "unknown status";
+}
+
+int32_t pa_abi_version(void) { return PA_ABI_VERSION; }
+
+}  // extern "C"

@@ -1,0 +1,230 @@
+// Host side of pa_decode_attention: argument checks, the workspace layout,
+// grid sizing, the TMA descriptors of the two pools, and the launch.
+#include <cudaTypedefs.h>
+
+#include <atomic>
+#include <cmath>
+#include <mutex>
+
+#include "pa_internal.h"
+
+namespace pa {
+namespace {
+
+constexpr int kMaxDevices = 64;
+std::atomic<int> g_ctas_per_sm{0};  // 0 = default (2)
+constexpr int kDefaultCtasPerSm = 2;
+
+struct DeviceInfo {
+    int sms = 0;
+};
+DeviceInfo g_dev[kMaxDevices];
+std::mutex g_mu;
+
+bool current_device(int* dev, int* sms) {
+    if (cudaGetDevice(dev) != cudaSuccess || *dev < 0 || *dev >= kMaxDevices) return false;
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (g_dev[*dev].sms == 0) {
+        int n = 0;
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, *dev) != cudaSuccess || n <= 0) return false;
+        g_dev[*dev].sms = n;
+    }
+    *sms = g_dev[*dev].sms;
+    return true;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q{};
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    });
+    return fn;
+}
+
+// 2-D view of a pool: rows = num_blocks * Hkv * BS, columns = head_dim; one
+// box = BS rows x 128 bytes, loaded with the 128-byte swizzle.
+bool encode_pool_map(CUtensorMap* map, const void* pool, int64_t rows, int head_dim, int block_size, pa_dtype dt) {
+    auto enc = tensor_map_encoder();
+    if (!enc) return false;
+    const int elem = dt == PA_F32 ? 4 : 2;
+    cuuint64_t dims[2] = {(cuuint64_t)head_dim, (cuuint64_t)rows};
+    cuuint64_t strides[1] = {(cuuint64_t)head_dim * elem};
+    cuuint32_t box[2] = {(cuuint32_t)(128 / elem), (cuuint32_t)block_size};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = enc(map, dt == PA_F32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
+                     const_cast<void*>(pool), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                     CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
+
+struct WorkspaceLayout {
+    size_t counters_off, partials_off, total;
+};
+
+WorkspaceLayout workspace_layout(int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
+                                 int sms) {
+    WorkspaceLayout w;
+    const size_t G = (size_t)(num_q_heads / num_kv_heads);
+    w.counters_off = 256;
+    w.partials_off = w.counters_off + align256((size_t)num_seqs * num_kv_heads * 4);
+    w.total = w.partials_off + (size_t)2 * sms * kMaxCtasPerSm * G * (head_dim + 2) * 4;
+    return w;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+pa_status check_shapes(int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
+                       int32_t block_size) {
+    if (num_seqs <= 0 || num_q_heads <= 0 || num_kv_heads <= 0) return PA_ERR_INVALID_ARG;
+    if (num_q_heads % num_kv_heads) return PA_ERR_INVALID_ARG;
+    if (num_q_heads / num_kv_heads > 8) return PA_ERR_UNSUPPORTED;
+    if (head_dim != 64 && head_dim != 128) return PA_ERR_UNSUPPORTED;
+    if (block_size != 16 && block_size != 32) return PA_ERR_UNSUPPORTED;
+    return PA_OK;
+}
+
+// Picks the compiled variant and the grid for these shapes on the current device.
+struct LaunchPlan {
+    DecodeVariant v;
+    bool mma;
+    int smem;
+    int grid;
+    int sms;
+};
+
+pa_status plan_launch(int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
+                      int32_t block_size, int32_t max_tiles_per_head, bool fixed, pa_dtype dtype, LaunchPlan* lp) {
+    int dev = 0;
+    if (!current_device(&dev, &lp->sms)) return PA_ERR_CUDA;
+    const int G = num_q_heads / num_kv_heads;
+    lp->mma = (dtype == PA_BF16 && G >= 4);
+    bool found = dtype == PA_F32 ? decode_variant_f32(head_dim, block_size, &lp->v)
+                                 : decode_variant_bf16(head_dim, block_size, lp->mma, &lp->v);
+    if (!found) return PA_ERR_UNSUPPORTED;
+    lp->smem = lp->v.smem_bytes(num_seqs, fixed);
+    if (lp->smem > kMaxSmem) return PA_ERR_UNSUPPORTED;
+    if (cudaFuncSetAttribute(lp->v.kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, lp->smem) != cudaSuccess)
+        return PA_ERR_CUDA;
+    int occ = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, lp->v.kernel, lp->v.threads, lp->smem) != cudaSuccess)
+        return PA_ERR_CUDA;
+    if (occ <= 0) return PA_ERR_UNSUPPORTED;
+    int want = g_ctas_per_sm.load();
+    if (want <= 0) want = kDefaultCtasPerSm;
+    const int per_sm = occ < want ? occ : want;
+    int64_t grid = (int64_t)lp->sms * per_sm;
+    const int64_t tiles_bound = (int64_t)num_seqs * num_kv_heads * max_tiles_per_head;
+    if (grid > tiles_bound) grid = tiles_bound;
+    if (grid < 1) grid = 1;
+    lp->grid = (int)grid;
+    return PA_OK;
+}
+
+}  // namespace
+}  // namespace pa
+
+using namespace pa;
+
+extern "C" pa_status pa_decode_workspace_bytes(int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads,
+                                               int32_t head_dim, size_t* bytes_out) {
+    if (!bytes_out) return PA_ERR_INVALID_ARG;
+    if (num_seqs <= 0 || num_q_heads <= 0 || num_kv_heads <= 0 || head_dim <= 0 || num_q_heads % num_kv_heads)
+        return PA_ERR_INVALID_ARG;
+    int dev = 0, sms = 0;
+    if (!current_device(&dev, &sms)) return PA_ERR_CUDA;
+    *bytes_out = workspace_layout(num_seqs, num_q_heads, num_kv_heads, head_dim, sms).total;
+    return PA_OK;
+}
+
+extern "C" pa_status pa_decode_set_ctas_per_sm(int32_t ctas) {
+    if (ctas < 0 || ctas > kMaxCtasPerSm) return PA_ERR_INVALID_ARG;
+    g_ctas_per_sm.store(ctas);
+    return PA_OK;
+}
+
+extern "C" pa_status pa_decode_launch_info(int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads,
+                                           int32_t head_dim, int32_t block_size, int32_t max_blocks_per_seq,
+                                           pa_dtype dtype, int32_t* ctas, int32_t* stages, int32_t* smem_bytes,
+                                           int32_t* uses_mma) {
+    if (dtype != PA_F32 && dtype != PA_BF16) return PA_ERR_UNSUPPORTED;
+    pa_status s = check_shapes(num_seqs, num_q_heads, num_kv_heads, head_dim, block_size);
+    if (s != PA_OK) return s;
+    if (max_blocks_per_seq <= 0) return PA_ERR_INVALID_ARG;
+    LaunchPlan lp;
+    s = plan_launch(num_seqs, num_q_heads, num_kv_heads, head_dim, block_size, max_blocks_per_seq, false, dtype, &lp);
+    if (s != PA_OK) return s;
+    if (ctas) *ctas = lp.grid;
+    if (stages) *stages = lp.v.stages;
+    if (smem_bytes) *smem_bytes = lp.smem;
+    if (uses_mma) *uses_mma = lp.mma ? 1 : 0;
+    return PA_OK;
+}
+
+extern "C" pa_status pa_decode_attention(void* out, const void* q, const void* k_pool, const void* v_pool,
+                                         const int32_t* block_tables, int32_t max_blocks_per_seq,
+                                         const int32_t* seq_lens, int32_t max_seq_len, int32_t num_seqs,
+                                         int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
+                                         int32_t block_size, int32_t num_blocks, float scale, int32_t partition_tokens,
+                                         void* workspace, size_t workspace_bytes, pa_dtype dtype, void* stream) {
+    if (dtype != PA_F32 && dtype != PA_BF16) return PA_ERR_UNSUPPORTED;
+    pa_status s = check_shapes(num_seqs, num_q_heads, num_kv_heads, head_dim, block_size);
+    if (s != PA_OK) return s;
+    if (!out || !q || !k_pool || !v_pool || !block_tables || !seq_lens || !workspace) return PA_ERR_INVALID_ARG;
+    if (!aligned16(out) || !aligned16(q) || !aligned16(k_pool) || !aligned16(v_pool) || !aligned16(workspace) ||
+        (reinterpret_cast<uintptr_t>(block_tables) & 3u) || (reinterpret_cast<uintptr_t>(seq_lens) & 3u))
+        return PA_ERR_INVALID_ARG;
+    if (max_blocks_per_seq <= 0 || num_blocks <= 0 || max_seq_len < 0) return PA_ERR_INVALID_ARG;
+    if (partition_tokens < 0 || (partition_tokens % block_size) != 0) return PA_ERR_INVALID_ARG;
+    if (!std::isfinite(scale)) return PA_ERR_INVALID_ARG;
+    const int64_t rows = (int64_t)num_blocks * num_kv_heads * block_size;
+    const int64_t tiles = (int64_t)num_seqs * num_kv_heads * max_blocks_per_seq;
+    if (rows >= INT32_MAX || tiles >= INT32_MAX || (int64_t)num_seqs * num_q_heads * head_dim >= INT32_MAX)
+        return PA_ERR_UNSUPPORTED;
+
+    const int64_t table_len = (int64_t)max_blocks_per_seq * block_size;
+    const int32_t max_len = (int32_t)(max_seq_len < table_len ? max_seq_len : table_len);
+    const int32_t max_tiles = (max_len + block_size - 1) / block_size;
+    const bool fixed = partition_tokens > 0;
+    LaunchPlan lp;
+    s = plan_launch(num_seqs, num_q_heads, num_kv_heads, head_dim, block_size, max_tiles > 0 ? max_tiles : 1, fixed,
+                    dtype, &lp);
+    if (s != PA_OK) return s;
+    const WorkspaceLayout wl = workspace_layout(num_seqs, num_q_heads, num_kv_heads, head_dim, lp.sms);
+    if (workspace_bytes < wl.total) return PA_ERR_WORKSPACE_TOO_SMALL;
+
+    CUtensorMap tk, tv;
+    if (!encode_pool_map(&tk, k_pool, rows, head_dim, block_size, dtype) ||
+        !encode_pool_map(&tv, v_pool, rows, head_dim, block_size, dtype))
+        return PA_ERR_CUDA;
+
+    DecodeParams p;
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    p.out = out;
+    p.q = q;
+    p.block_tables = block_tables;
+    p.seq_lens = seq_lens;
+    p.status = reinterpret_cast<int32_t*>(ws);
+    p.counters = reinterpret_cast<int32_t*>(ws + wl.counters_off);
+    p.partials = reinterpret_cast<float*>(ws + wl.partials_off);
+    p.max_blocks_per_seq = max_blocks_per_seq;
+    p.max_len = max_len;
+    p.num_seqs = num_seqs;
+    p.num_q_heads = num_q_heads;
+    p.num_kv_heads = num_kv_heads;
+    p.num_blocks = num_blocks;
+    p.group = num_q_heads / num_kv_heads;
+    p.partition_tiles = partition_tokens / block_size;
+    p.num_ctas = lp.grid;
+    p.scale_log2 = scale * 1.4426950408889634f;
+    lp.v.launch(p, tk, tv, lp.grid, lp.smem, static_cast<cudaStream_t>(stream));
+    return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+}

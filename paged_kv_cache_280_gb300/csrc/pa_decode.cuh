@@ -1,0 +1,769 @@
+// Paged decode attention for sm_103a (one query token per sequence).
+//
+// What it computes ("Q32: vLLM PagedAttention 原理" §2 and follow-up 3;
+// data.6616ai.com "把虚拟内存搬进 KV Cache"): for sequence b and query head h
+// (KV head g = h / G), softmax(scale * q K^T) V over the seq_lens[b] tokens
+// whose K/V rows sit in the physical blocks named by block_tables[b].
+//
+// Work decomposition.  A "tile" is one (physical block, KV head) pair: BS
+// tokens x D elements of K plus the same of V, contiguous in the pool.  The
+// tiles of segment (b, g) are its n_b = ceil(len_b / BS) blocks.  All tiles of
+// all segments are laid end to end (sequence-major, then KV head, then
+// block) and the grid's C CTAs take equal contiguous ranges of that list
+// (or, with a partition size P, ranges whose ends fall on multiples of P
+// tokens).  So every CTA moves the same number of bytes whatever the
+// length mix.  A CTA walks its range as "pieces" (the part of one segment
+// that lies in its range): a piece covering a whole segment is normalised
+// and written straight to `out`; a piece of a segment that straddles CTAs is
+// written as an unnormalised partial (m, l, o) to the workspace, and the
+// last CTA to finish a piece of that segment (an atomic counter per
+// segment) merges them:  M = max m_p,  out = sum e^(m_p-M) o_p / sum e^(m_p-M) l_p.
+//
+// CTA layout: warp 4 is the producer, warps 0-3 consume.  The producer reads
+// block-table entries 32 at a time and moves each tile with TMA
+// (cp.async.bulk.tensor, 128-byte swizzle, evict-first L2 hint) into an
+// S-stage ring of shared-memory buffers guarded by full/empty mbarriers;
+// the query rows of each piece arrive by a 1-D bulk copy.  Tile k of the CTA
+// goes to consumer warp k % 4, which keeps its own online-softmax state
+// (running max m, running sum l, accumulator o) in fp32; the four states are
+// merged through shared memory at the end of each piece.
+//
+// Two compute paths:
+//   MMA (bf16, G >= 4): tensor-core mma.sync m16n8k16.  S^T = K q^T with the
+//     16 tokens of a half-block as M and the (padded) 8 query heads as N;
+//     P^T is moved into B-fragment layout with movmatrix; O^T = V^T P^T with
+//     the head dimension as M.
+//   FMA (fp32, or bf16 with G < 4): CUDA cores; lane (t, part) forms the dot
+//     products of token t over half the head dimension, lanes own D/32
+//     output dimensions for P V.
+#pragma once
+
+#include <type_traits>
+
+#include "pa_device.cuh"
+#include "pa_internal.h"
+
+namespace pa {
+
+constexpr int kConsumerWarps = 4;
+constexpr int kThreads = (kConsumerWarps + 1) * 32;
+constexpr int kMaxGroup = 8;
+
+
+template <typename T>
+struct ElemBytes;
+template <>
+struct ElemBytes<float> {
+    static constexpr int value = 4;
+};
+template <>
+struct ElemBytes<__nv_bfloat16> {
+    static constexpr int value = 2;
+};
+
+// Pipeline depth: about 64 KB of tiles in flight per CTA, 4 to 16 stages,
+// a multiple of the consumer-warp count.
+constexpr int stages_for(int bs, int d, int e) {
+    int n = 65536 / (2 * bs * d * e);
+    n = n < 4 ? 4 : (n > 16 ? 16 : n);
+    return n & ~3;
+}
+
+template <typename T, int D, int BS>
+struct Layout {
+    static constexpr int E = ElemBytes<T>::value;
+    static constexpr int S = stages_for(BS, D, E);
+    static constexpr int kTileBytes = BS * D * E;  // K (or V) of one tile
+    static constexpr int kPanels = D * E / 128;    // 128-byte column panels per row
+    static constexpr int kStageBytes = 2 * kTileBytes;
+    static constexpr int kQSlotBytes = kMaxGroup * D * E;
+    static constexpr int kScratchStride = D + 4;  // floats per (warp, head) row of the merge buffer
+    static constexpr int kStagesOff = 0;
+    static constexpr int kQOff = kStagesOff + S * kStageBytes;
+    static constexpr int kQfOff = kQOff + 2 * kQSlotBytes;
+    static constexpr int kScratchOff = kQfOff + kMaxGroup * D * 4;
+    static constexpr int kMLOff = kScratchOff + kConsumerWarps * kMaxGroup * kScratchStride * 4;
+    static constexpr int kPTileOff = kMLOff + kConsumerWarps * kMaxGroup * 2 * 4;
+    static constexpr int kBarOff = kPTileOff + kConsumerWarps * 16 * kMaxGroup * 4;
+    static constexpr int kMiscOff = kBarOff + (2 * S + 4) * 8;
+    static constexpr int kPrefixOff = kMiscOff + 128;
+    static_assert(kTileBytes % 1024 == 0, "tiles must keep 1024-byte alignment for the 128B swizzle");
+    static_assert(kQSlotBytes % 16 == 0, "bulk-copy destination alignment");
+    // dynamic shared memory for num_seqs sequences (+1 KB to align the base)
+    static constexpr int bytes(int num_seqs, bool fixed) {
+        return kPrefixOff + (num_seqs + 1) * 4 * (fixed ? 2 : 1) + 1024;
+    }
+};
+
+// Where the tiles of one CTA start and end, and who holds which partial.
+struct Plan {
+    const int32_t* pref;   // pref[b] = blocks of sequences < b (per KV head)
+    const int32_t* upref;  // same in partitions (fixed mode)
+    int32_t B, Hkv, C, PT;
+    int64_t T, U;  // total tiles, total partitions
+
+    __device__ __forceinline__ int nblocks(int b) const { return pref[b + 1] - pref[b]; }
+    __device__ __forceinline__ int64_t seg_start(int b, int h) const {
+        return (int64_t)Hkv * pref[b] + (int64_t)h * nblocks(b);
+    }
+    // largest b in [0, B) with Hkv * pre[b] <= x
+    __device__ __forceinline__ int find_seq(const int32_t* pre, int64_t x) const {
+        int lo = 0, hi = B - 1;
+        while (lo < hi) {
+            int mid = (lo + hi + 1) >> 1;
+            if ((int64_t)Hkv * pre[mid] <= x)
+                lo = mid;
+            else
+                hi = mid - 1;
+        }
+        return lo;
+    }
+    __device__ __forceinline__ int64_t tile_of_unit(int64_t u) const {
+        if (u >= U) return T;
+        int b = find_seq(upref, u);
+        int64_t local = u - (int64_t)Hkv * upref[b];
+        int ub = upref[b + 1] - upref[b];
+        int h = (int)(local / ub), part = (int)(local % ub);
+        return seg_start(b, h) + (int64_t)part * PT;
+    }
+    __device__ __forceinline__ int64_t cta_start(int c) const {
+        if (PT == 0) return (int64_t)c * T / C;
+        return tile_of_unit((int64_t)c * U / C);
+    }
+    // the CTA whose range holds tile t
+    __device__ __forceinline__ int cta_of(int64_t t) const {
+        if (PT == 0) return (int)(((t + 1) * C - 1) / T);
+        int b = find_seq(pref, t);
+        int64_t local = t - (int64_t)Hkv * pref[b];
+        int nb = nblocks(b), ub = upref[b + 1] - upref[b];
+        int h = (int)(local / nb), j = (int)(local % nb);
+        int64_t u = (int64_t)Hkv * upref[b] + (int64_t)h * ub + j / PT;
+        return (int)(((u + 1) * C - 1) / U);
+    }
+};
+
+struct PieceIter {
+    int64_t t, t1;
+    int b;
+    __device__ __forceinline__ bool next(const Plan& P, int& b_out, int& h, int& j0, int& j1) {
+        if (t >= t1) return false;
+        while ((int64_t)P.Hkv * P.pref[b + 1] <= t) ++b;
+        const int nb = P.nblocks(b);
+        const int64_t local = t - (int64_t)P.Hkv * P.pref[b];
+        h = (int)(local / nb);
+        j0 = (int)(local % nb);
+        const int64_t room = t1 - t;
+        j1 = (int)((int64_t)(nb - j0) < room ? nb : j0 + room);
+        t += j1 - j0;
+        b_out = b;
+        return true;
+    }
+};
+
+// Warp-collective wait used by both roles: every lane of the warp calls it.
+__device__ __forceinline__ bool role_wait(uint32_t bar, uint32_t parity, volatile int32_t* abort_flag,
+                                          int32_t* status) {
+    if (__any_sync(0xffffffffu, *abort_flag != 0)) return false;
+    bool ok = mbar_wait(bar, parity);
+    ok = __all_sync(0xffffffffu, ok);
+    if (!ok) {
+        *abort_flag = 1;
+        if ((threadIdx.x & 31) == 0) flag_status(status, PA_DEV_WAIT_TIMEOUT);
+    }
+    return ok;
+}
+
+__device__ __forceinline__ int clamp_len(int len, int max_len) { return len < 0 ? 0 : (len > max_len ? max_len : len); }
+
+template <typename T>
+__device__ __forceinline__ T from_float(float x);
+template <>
+__device__ __forceinline__ float from_float<float>(float x) {
+    return x;
+}
+template <>
+__device__ __forceinline__ __nv_bfloat16 from_float<__nv_bfloat16>(float x) {
+    return __float2bfloat16_rn(x);
+}
+
+// Load 16 bytes of a tile row and widen to fp32 (8 bf16 or 4 fp32 values).
+template <typename T>
+__device__ __forceinline__ void load_chunk_f32(uint32_t addr, float* v);
+template <>
+__device__ __forceinline__ void load_chunk_f32<__nv_bfloat16>(uint32_t addr, float* v) {
+    uint32_t r0, r1, r2, r3;
+    asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3) : "r"(addr));
+    v[0] = bf16_lo(r0); v[1] = bf16_hi(r0); v[2] = bf16_lo(r1); v[3] = bf16_hi(r1);
+    v[4] = bf16_lo(r2); v[5] = bf16_hi(r2); v[6] = bf16_lo(r3); v[7] = bf16_hi(r3);
+}
+template <>
+__device__ __forceinline__ void load_chunk_f32<float>(uint32_t addr, float* v) {
+    asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];" : "=f"(v[0]), "=f"(v[1]), "=f"(v[2]), "=f"(v[3]) : "r"(addr));
+}
+
+// Load N consecutive elements (N * E <= 16 bytes, naturally aligned) and widen.
+template <typename T, int N>
+__device__ __forceinline__ void load_vec_f32(uint32_t addr, float* v) {
+    if constexpr (sizeof(T) == 2) {
+        if constexpr (N == 2) {
+            uint32_t r;
+            asm volatile("ld.shared.u32 %0, [%1];" : "=r"(r) : "r"(addr));
+            v[0] = bf16_lo(r); v[1] = bf16_hi(r);
+        } else {
+            static_assert(N == 4, "bf16 vector of 2 or 4");
+            uint32_t r0, r1;
+            asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(r0), "=r"(r1) : "r"(addr));
+            v[0] = bf16_lo(r0); v[1] = bf16_hi(r0); v[2] = bf16_lo(r1); v[3] = bf16_hi(r1);
+        }
+    } else {
+        if constexpr (N == 2) {
+            asm volatile("ld.shared.v2.f32 {%0, %1}, [%2];" : "=f"(v[0]), "=f"(v[1]) : "r"(addr));
+        } else {
+            static_assert(N == 4, "fp32 vector of 2 or 4");
+            asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];" : "=f"(v[0]), "=f"(v[1]), "=f"(v[2]), "=f"(v[3]) : "r"(addr));
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Per-warp online-softmax state of the two compute paths
+// ---------------------------------------------------------------------------
+
+// Tensor-core path.  Thread (g = lane/4, tig = lane%4) holds the running max
+// and sum of heads 2tig and 2tig+1, and O^T fragments o[mt] = rows (dims)
+// 16mt+g, 16mt+g+8 x columns (heads) 2tig, 2tig+1.
+template <int D, int BS>
+struct MmaState {
+    static constexpr int MT = D / 16;
+    uint32_t qb[MT][2];  // B fragments of q^T per 16-dim k-step
+    float m[2], l[2];
+    float o[MT][4];
+
+    __device__ __forceinline__ void reset() {
+        m[0] = m[1] = -INFINITY;
+        l[0] = l[1] = 0.f;
+#pragma unroll
+        for (int i = 0; i < MT; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
+    }
+
+    __device__ __forceinline__ void load_q(const uint8_t* qslot, int G, int lane) {
+        const int g = lane >> 2, tig = lane & 3;
+#pragma unroll
+        for (int s = 0; s < MT; ++s) {
+            uint32_t lo = 0, hi = 0;
+            if (g < G) {
+                const uint32_t* row = reinterpret_cast<const uint32_t*>(qslot + (size_t)g * D * 2);
+                lo = row[(16 * s + 2 * tig) >> 1];
+                hi = row[(16 * s + 2 * tig + 8) >> 1];
+            }
+            qb[s][0] = lo;
+            qb[s][1] = hi;
+        }
+    }
+
+    // One 16-token step: rows row0..row0+15 of the tile, `valid` of them real.
+    __device__ __forceinline__ void step(uint32_t kbase, uint32_t vbase, int row0, int valid, float scale_log2,
+                                         int lane) {
+        const int g = lane >> 2, tig = lane & 3;
+        float acc[4] = {0.f, 0.f, 0.f, 0.f};
+        {
+            const int row = row0 + (lane & 7) + (((lane >> 3) & 1) << 3);
+            const int csel = lane >> 4;
+#pragma unroll
+            for (int s = 0; s < MT; ++s) {
+                uint32_t a0, a1, a2, a3;
+                ldmatrix_x4(kbase + tile_chunk_offset<BS>(row, 2 * s + csel), a0, a1, a2, a3);
+                mma_bf16_16816(acc, a0, a1, a2, a3, qb[s][0], qb[s][1]);
+            }
+        }
+        // acc: (token g, head 2tig), (g, 2tig+1), (g+8, 2tig), (g+8, 2tig+1)
+        const bool v0 = g < valid, v1 = g + 8 < valid;
+        float x0 = v0 ? acc[0] * scale_log2 : -INFINITY;
+        float x1 = v0 ? acc[1] * scale_log2 : -INFINITY;
+        float x2 = v1 ? acc[2] * scale_log2 : -INFINITY;
+        float x3 = v1 ? acc[3] * scale_log2 : -INFINITY;
+        float mx0 = fmaxf(x0, x2), mx1 = fmaxf(x1, x3);
+#pragma unroll
+        for (int off = 4; off < 32; off <<= 1) {
+            mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
+            mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
+        }
+        const float mn0 = fmaxf(m[0], mx0), mn1 = fmaxf(m[1], mx1);
+        const float al0 = exp2f(m[0] - mn0), al1 = exp2f(m[1] - mn1);
+        const uint32_t P0 = pack_bf16x2(exp2f(x0 - mn0), exp2f(x1 - mn1));
+        const uint32_t P1 = pack_bf16x2(exp2f(x2 - mn0), exp2f(x3 - mn1));
+        // the sum uses the rounded weights that P V uses
+        l[0] = l[0] * al0 + bf16_lo(P0) + bf16_lo(P1);
+        l[1] = l[1] * al1 + bf16_hi(P0) + bf16_hi(P1);
+        m[0] = mn0;
+        m[1] = mn1;
+#pragma unroll
+        for (int i = 0; i < MT; ++i) {
+            o[i][0] *= al0;
+            o[i][1] *= al1;
+            o[i][2] *= al0;
+            o[i][3] *= al1;
+        }
+        const uint32_t b0 = movmatrix_trans(P0), b1 = movmatrix_trans(P1);
+        uint32_t m01 = 0xffffffffu, m89 = 0xffffffffu;
+        if (valid < 16) {  // zero V rows past the sequence end (their slots may hold anything)
+            m01 = (2 * tig < valid ? 0x0000ffffu : 0u) | (2 * tig + 1 < valid ? 0xffff0000u : 0u);
+            m89 = (2 * tig + 8 < valid ? 0x0000ffffu : 0u) | (2 * tig + 9 < valid ? 0xffff0000u : 0u);
+        }
+        const int row = row0 + (lane & 7) + ((lane >> 4) << 3);
+        const int csel = (lane >> 3) & 1;
+#pragma unroll
+        for (int i = 0; i < MT; ++i) {
+            uint32_t a0, a1, a2, a3;
+            ldmatrix_x4_trans(vbase + tile_chunk_offset<BS>(row, 2 * i + csel), a0, a1, a2, a3);
+            mma_bf16_16816(o[i], a0 & m01, a1 & m01, a2 & m89, a3 & m89, b0, b1);
+        }
+    }
+
+    // Write this warp's state into the merge buffers (heads < G only).
+    __device__ __forceinline__ void spill(float* scratch, float* ml, int G, int lane, int stride) {
+        const int g = lane >> 2, tig = lane & 3;
+        float l0 = l[0], l1 = l[1];
+#pragma unroll
+        for (int off = 4; off < 32; off <<= 1) {
+            l0 += __shfl_xor_sync(0xffffffffu, l0, off);
+            l1 += __shfl_xor_sync(0xffffffffu, l1, off);
+        }
+        const int h0 = 2 * tig, h1 = 2 * tig + 1;
+#pragma unroll
+        for (int i = 0; i < MT; ++i) {
+            if (h0 < G) {
+                scratch[h0 * stride + 16 * i + g] = o[i][0];
+                scratch[h0 * stride + 16 * i + g + 8] = o[i][2];
+            }
+            if (h1 < G) {
+                scratch[h1 * stride + 16 * i + g] = o[i][1];
+                scratch[h1 * stride + 16 * i + g + 8] = o[i][3];
+            }
+        }
+        if (g == 0) {
+            if (h0 < G) { ml[2 * h0] = m[0]; ml[2 * h0 + 1] = l0; }
+            if (h1 < G) { ml[2 * h1] = m[1]; ml[2 * h1 + 1] = l1; }
+        }
+    }
+};
+
+// CUDA-core path.  Lane = (token t = lane & 15, half = lane >> 4) for the dot
+// products; lane owns output dims [lane * VEC, lane * VEC + VEC) for P V.
+template <typename T, int D, int BS>
+struct FmaState {
+    static constexpr int E = ElemBytes<T>::value;
+    static constexpr int VEC = D / 32;
+    static constexpr int EPC = 16 / E;              // elements per 16-byte chunk
+    static constexpr int HALF_CHUNKS = D * E / 32;  // chunks per half row
+    float m[kMaxGroup], l[kMaxGroup];
+    float o[kMaxGroup][VEC];
+
+    __device__ __forceinline__ void reset() {
+#pragma unroll
+        for (int g = 0; g < kMaxGroup; ++g) {
+            m[g] = -INFINITY;
+            l[g] = 0.f;
+#pragma unroll
+            for (int v = 0; v < VEC; ++v) o[g][v] = 0.f;
+        }
+    }
+
+    // qf: [G][D] fp32 query rows pre-multiplied by scale*log2(e); ptile: this warp's [16][8] weights.
+    __device__ __forceinline__ void step(uint32_t kbase, uint32_t vbase, int row0, int valid, int G,
+                                         const float* qf, float* ptile, int lane) {
+        const int t = lane & 15, half = lane >> 4;
+        float acc[kMaxGroup];
+#pragma unroll
+        for (int g = 0; g < kMaxGroup; ++g) acc[g] = 0.f;
+        const int row = row0 + t;
+#pragma unroll
+        for (int cc = 0; cc < HALF_CHUNKS; ++cc) {
+            const int chunk = half * HALF_CHUNKS + cc;
+            float kv[EPC];
+            load_chunk_f32<T>(kbase + tile_chunk_offset<BS>(row, chunk), kv);
+#pragma unroll
+            for (int g = 0; g < kMaxGroup; ++g) {
+                if (g < G) {
+                    const float4* qp = reinterpret_cast<const float4*>(qf + g * D + chunk * EPC);
+#pragma unroll
+                    for (int e4 = 0; e4 < EPC / 4; ++e4) {
+                        const float4 qv = qp[e4];
+                        acc[g] = fmaf(qv.x, kv[4 * e4 + 0], acc[g]);
+                        acc[g] = fmaf(qv.y, kv[4 * e4 + 1], acc[g]);
+                        acc[g] = fmaf(qv.z, kv[4 * e4 + 2], acc[g]);
+                        acc[g] = fmaf(qv.w, kv[4 * e4 + 3], acc[g]);
+                    }
+                }
+            }
+        }
+        float alpha[kMaxGroup];
+#pragma unroll
+        for (int g = 0; g < kMaxGroup; ++g) {
+            if (g < G) {
+                float x = acc[g] + __shfl_xor_sync(0xffffffffu, acc[g], 16);
+                x = t < valid ? x : -INFINITY;
+                float mx = x;
+#pragma unroll
+                for (int off = 1; off < 16; off <<= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+                const float mn = fmaxf(m[g], mx);
+                alpha[g] = exp2f(m[g] - mn);
+                const float pw = exp2f(x - mn);
+                float s = pw;
+#pragma unroll
+                for (int off = 1; off < 16; off <<= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
+                l[g] = l[g] * alpha[g] + s;
+                m[g] = mn;
+                if (half == 0) ptile[t * kMaxGroup + g] = pw;
+            } else {
+                alpha[g] = 1.f;
+            }
+        }
+        __syncwarp();
+#pragma unroll
+        for (int g = 0; g < kMaxGroup; ++g)
+#pragma unroll
+            for (int v = 0; v < VEC; ++v) o[g][v] *= alpha[g];
+        const int byte0 = lane * VEC * E;
+        for (int tt = 0; tt < valid; ++tt) {
+            float vv[VEC];
+            load_vec_f32<T, VEC>(vbase + tile_chunk_offset<BS>(row0 + tt, byte0 >> 4) + (byte0 & 15), vv);
+            const float4 p0 = reinterpret_cast<const float4*>(ptile + tt * kMaxGroup)[0];
+            const float4 p1 = reinterpret_cast<const float4*>(ptile + tt * kMaxGroup)[1];
+            const float pg[8] = {p0.x, p0.y, p0.z, p0.w, p1.x, p1.y, p1.z, p1.w};
+#pragma unroll
+            for (int g = 0; g < kMaxGroup; ++g)
+                if (g < G)
+#pragma unroll
+                    for (int v = 0; v < VEC; ++v) o[g][v] = fmaf(pg[g], vv[v], o[g][v]);
+        }
+        __syncwarp();
+    }
+
+    __device__ __forceinline__ void spill(float* scratch, float* ml, int G, int lane, int stride) {
+#pragma unroll
+        for (int g = 0; g < kMaxGroup; ++g) {
+            if (g < G) {
+#pragma unroll
+                for (int v = 0; v < VEC; ++v) scratch[g * stride + lane * VEC + v] = o[g][v];
+                if (lane == 0) {
+                    ml[2 * g] = m[g];
+                    ml[2 * g + 1] = l[g];
+                }
+            }
+        }
+    }
+};
+
+// ---------------------------------------------------------------------------
+// The kernel
+// ---------------------------------------------------------------------------
+template <typename T, int D, int BS, bool MMA>
+__global__ void __launch_bounds__(kThreads, 2) decode_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tmap_k,
+                                                          const __grid_constant__ CUtensorMap tmap_v) {
+    using L = Layout<T, D, BS>;
+    constexpr int S = L::S;
+    constexpr int E = L::E;
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw_s = smem_u32(smem_raw);
+    const uint32_t base_s = (raw_s + 1023u) & ~1023u;
+    uint8_t* base = smem_raw + (base_s - raw_s);
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int B = p.num_seqs, Hkv = p.num_kv_heads, G = p.group, C = p.num_ctas, c = blockIdx.x;
+    const bool fixed = p.partition_tiles > 0;
+    int32_t* pref = reinterpret_cast<int32_t*>(base + L::kPrefixOff);
+    int32_t* upref = pref + (B + 1);
+    volatile int32_t* misc = reinterpret_cast<volatile int32_t*>(base + L::kMiscOff);
+    int32_t* wsum = reinterpret_cast<int32_t*>(base + L::kMiscOff + 32);  // [5] blocks, [5] partitions
+    const uint32_t bar0 = base_s + L::kBarOff;
+    auto full_bar = [&](int s) { return bar0 + 8u * s; };
+    auto empty_bar = [&](int s) { return bar0 + 8u * (S + s); };
+    auto qfull_bar = [&](int i) { return bar0 + 8u * (2 * S + i); };
+    auto qempty_bar = [&](int i) { return bar0 + 8u * (2 * S + 2 + i); };
+
+    if (tid == 0) {
+        for (int s = 0; s < S; ++s) {
+            mbar_init(full_bar(s), 1);
+            mbar_init(empty_bar(s), 1);
+        }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(qfull_bar(i), 1);
+            mbar_init(qempty_bar(i), 1);
+        }
+        fence_barrier_init();
+        misc[0] = 0;  // abort flag
+    }
+
+    // ---- plan: blocks (and partitions) per sequence, exclusive prefix sums ----
+    {
+        const int per = (B + kThreads - 1) / kThreads;
+        const int lo = min(B, tid * per), hi = min(B, lo + per);
+        int32_t nblk = 0, nprt = 0;
+        for (int b = lo; b < hi; ++b) {
+            const int raw_len = __ldg(p.seq_lens + b);
+            if ((raw_len < 0 || raw_len > p.max_len) && c == 0) flag_status(p.status, PA_DEV_BAD_SEQ_LEN);
+            const int nb = (clamp_len(raw_len, p.max_len) + BS - 1) / BS;
+            nblk += nb;
+            if (fixed) nprt += (nb + p.partition_tiles - 1) / p.partition_tiles;
+        }
+        int32_t xb = nblk, xp = nprt;  // inclusive warp scans
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const int32_t yb = __shfl_up_sync(0xffffffffu, xb, off);
+            const int32_t yp = __shfl_up_sync(0xffffffffu, xp, off);
+            if (lane >= off) {
+                xb += yb;
+                xp += yp;
+            }
+        }
+        if (lane == 31) {
+            wsum[warp] = xb;
+            wsum[8 + warp] = xp;
+        }
+        __syncthreads();
+        int32_t ob = 0, op = 0;
+        for (int w = 0; w < warp; ++w) {
+            ob += wsum[w];
+            op += wsum[8 + w];
+        }
+        int32_t rb = ob + xb - nblk, rp = op + xp - nprt;
+        for (int b = lo; b < hi; ++b) {
+            const int nb = (clamp_len(__ldg(p.seq_lens + b), p.max_len) + BS - 1) / BS;
+            pref[b] = rb;
+            rb += nb;
+            if (fixed) {
+                upref[b] = rp;
+                rp += (nb + p.partition_tiles - 1) / p.partition_tiles;
+            }
+        }
+        if (tid == kThreads - 1) {
+            pref[B] = ob + xb;
+            if (fixed) upref[B] = op + xp;
+        }
+    }
+    __syncthreads();
+
+    Plan P;
+    P.pref = pref;
+    P.upref = upref;
+    P.B = B;
+    P.Hkv = Hkv;
+    P.C = C;
+    P.PT = p.partition_tiles;
+    P.T = (int64_t)Hkv * pref[B];
+    P.U = fixed ? (int64_t)Hkv * upref[B] : 0;
+    const int64_t t0 = P.T > 0 ? P.cta_start(c) : 0;
+    const int64_t t1 = P.T > 0 ? P.cta_start(c + 1) : 0;
+    const int Hq = p.num_q_heads;
+
+    if (warp == kConsumerWarps) {
+        // =========================== producer ===========================
+        if (lane == 0) {
+            prefetch_tensormap(&tmap_k);
+            prefetch_tensormap(&tmap_v);
+        }
+        const uint64_t policy = policy_evict_first();
+        const uint32_t q_bytes = (uint32_t)(G * D * E);
+        uint32_t k = 0, pi = 0, k_issued = 0, pi_issued = 0;
+        PieceIter it{t0, t1, t0 < t1 ? P.find_seq(pref, t0) : 0};
+        int b, h, j0, j1;
+        while (it.next(P, b, h, j0, j1)) {
+            const int qs = pi & 1;
+            if (role_wait(qempty_bar(qs), ((pi >> 1) & 1) ^ 1, misc, p.status)) {
+                if (lane == 0) {
+                    mbar_arrive_expect_tx(qfull_bar(qs), q_bytes);
+                    const uint8_t* src = static_cast<const uint8_t*>(p.q) + ((size_t)b * Hq + (size_t)h * G) * D * E;
+                    bulk_load(base_s + L::kQOff + qs * L::kQSlotBytes, src, q_bytes, qfull_bar(qs));
+                }
+                pi_issued = pi + 1;
+            }
+            const int32_t* row = p.block_tables + (size_t)b * p.max_blocks_per_seq;
+            for (int jb = j0; jb < j1; jb += 32) {
+                const int n = min(32, j1 - jb);
+                int32_t blk = 0;
+                if (lane < n) {
+                    blk = __ldg(row + jb + lane);
+                    if (blk < 0 || blk >= p.num_blocks) {
+                        flag_status(p.status, PA_DEV_BAD_BLOCK_ID);
+                        blk = 0;
+                    }
+                }
+                for (int i = 0; i < n; ++i) {
+                    const int32_t bid = __shfl_sync(0xffffffffu, blk, i);
+                    const int st = k % S;
+                    if (role_wait(empty_bar(st), ((k / S) & 1) ^ 1, misc, p.status)) {
+                        if (lane == 0) {
+                            mbar_arrive_expect_tx(full_bar(st), (uint32_t)L::kStageBytes);
+                            const int32_t y = (bid * Hkv + h) * BS;
+                            const uint32_t ks = base_s + L::kStagesOff + st * L::kStageBytes;
+#pragma unroll
+                            for (int pn = 0; pn < L::kPanels; ++pn) {
+                                tma_load_2d(ks + pn * BS * 128, &tmap_k, pn * (128 / E), y, full_bar(st), policy);
+                                tma_load_2d(ks + L::kTileBytes + pn * BS * 128, &tmap_v, pn * (128 / E), y,
+                                            full_bar(st), policy);
+                            }
+                        }
+                        k_issued = k + 1;
+                    }
+                    ++k;
+                }
+            }
+            ++pi;
+        }
+        // never leave the CTA with copies still landing in its shared memory
+        for (uint32_t kk = k_issued > (uint32_t)S ? k_issued - S : 0; kk < k_issued; ++kk)
+            mbar_wait(full_bar(kk % S), (kk / S) & 1);
+        for (uint32_t qq = pi_issued > 2u ? pi_issued - 2 : 0; qq < pi_issued; ++qq)
+            mbar_wait(qfull_bar(qq & 1), (qq >> 1) & 1);
+    } else {
+        // =========================== consumers ===========================
+        // zero outputs of empty sequences
+        for (int bb = c; bb < B; bb += C) {
+            if (pref[bb + 1] == pref[bb]) {
+                T* o = static_cast<T*>(p.out) + (size_t)bb * Hq * D;
+                for (int e = tid; e < Hq * D; e += kConsumerWarps * 32) o[e] = from_float<T>(0.f);
+            }
+        }
+        float* scratch = reinterpret_cast<float*>(base + L::kScratchOff);
+        float* mlbuf = reinterpret_cast<float*>(base + L::kMLOff);
+        float* qf = reinterpret_cast<float*>(base + L::kQfOff);
+        float* ptile = reinterpret_cast<float*>(base + L::kPTileOff) + warp * 16 * kMaxGroup;
+        using State = typename std::conditional<MMA, MmaState<D, BS>, FmaState<T, D, BS>>::type;
+        State st;
+        uint32_t k = 0, pi = 0;
+        PieceIter it{t0, t1, t0 < t1 ? P.find_seq(pref, t0) : 0};
+        int b, h, j0, j1;
+        while (it.next(P, b, h, j0, j1)) {
+            const int qs = pi & 1;
+            const uint8_t* qslot = base + L::kQOff + qs * L::kQSlotBytes;
+            const bool qok = role_wait(qfull_bar(qs), (pi >> 1) & 1, misc, p.status);
+            if constexpr (MMA) {
+                if (qok) st.load_q(qslot, G, lane);
+            } else {
+                const T* qsrc = reinterpret_cast<const T*>(qslot);
+                for (int e = tid; e < G * D; e += kConsumerWarps * 32)
+                    qf[e] = qok ? static_cast<float>(qsrc[e]) * p.scale_log2 : 0.f;
+                named_barrier(1, kConsumerWarps * 32);
+            }
+            st.reset();
+            const int len = clamp_len(__ldg(p.seq_lens + b), p.max_len);
+            const int ntile = j1 - j0;
+            for (int i = warp - (int)(k & 3); i < ntile; i += kConsumerWarps) {
+                if (i < 0) continue;
+                const uint32_t kk = k + i;
+                const int sidx = kk % S;
+                if (role_wait(full_bar(sidx), (kk / S) & 1, misc, p.status)) {
+                    const uint32_t kb = base_s + L::kStagesOff + sidx * L::kStageBytes;
+                    const int tok0 = (j0 + i) * BS;
+#pragma unroll
+                    for (int sub = 0; sub < BS / 16; ++sub) {
+                        const int valid = min(16, len - (tok0 + sub * 16));
+                        if (valid > 0) {
+                            if constexpr (MMA)
+                                st.step(kb, kb + L::kTileBytes, sub * 16, valid, p.scale_log2, lane);
+                            else
+                                st.step(kb, kb + L::kTileBytes, sub * 16, valid, G, qf, ptile, lane);
+                        }
+                    }
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(empty_bar(sidx));
+            }
+            k += ntile;
+
+            // ---- merge the four warps' states ----
+            st.spill(scratch + warp * kMaxGroup * L::kScratchStride, mlbuf + warp * kMaxGroup * 2, G, lane,
+                     L::kScratchStride);
+            named_barrier(1, kConsumerWarps * 32);
+            const int nb = P.nblocks(b);
+            const bool whole = (j0 == 0 && j1 == nb);
+            const bool first_piece = (pi == 0);
+            float* slot = p.partials + (size_t)(2 * c + (first_piece ? 0 : 1)) * G * (D + 2);
+            for (int e = tid; e < G * D; e += kConsumerWarps * 32) {
+                const int g = e / D, i = e - g * D;
+                float M = -INFINITY;
+#pragma unroll
+                for (int w = 0; w < kConsumerWarps; ++w) M = fmaxf(M, mlbuf[(w * kMaxGroup + g) * 2]);
+                float acc = 0.f, Lsum = 0.f;
+#pragma unroll
+                for (int w = 0; w < kConsumerWarps; ++w) {
+                    const float mw = mlbuf[(w * kMaxGroup + g) * 2];
+                    if (mw != -INFINITY) {
+                        const float f = exp2f(mw - M);
+                        acc = fmaf(f, scratch[(w * kMaxGroup + g) * L::kScratchStride + i], acc);
+                        Lsum = fmaf(f, mlbuf[(w * kMaxGroup + g) * 2 + 1], Lsum);
+                    }
+                }
+                if (whole) {
+                    T* o = static_cast<T*>(p.out) + ((size_t)b * Hq + (size_t)h * G + g) * D;
+                    o[i] = from_float<T>(acc / Lsum);
+                } else {
+                    slot[g * D + i] = acc;
+                    if (i == 0) {
+                        slot[G * D + 2 * g] = M;
+                        slot[G * D + 2 * g + 1] = Lsum;
+                    }
+                }
+            }
+            if (!whole) __threadfence();
+            named_barrier(1, kConsumerWarps * 32);
+            if (tid == 0) mbar_arrive(qempty_bar(qs));
+            if (!whole) {
+                // ---- the last CTA to finish a piece of this segment merges them ----
+                const int64_t s0 = P.seg_start(b, h);
+                const int ca = P.cta_of(s0), cb = P.cta_of(s0 + nb - 1);
+                int32_t* cnt = p.counters + (size_t)b * Hkv + h;
+                if (tid == 0) {
+                    const int prev = atomicAdd(cnt, 1);
+                    const int last = (prev == cb - ca);
+                    if (last) __threadfence();
+                    misc[1] = last;
+                }
+                named_barrier(1, kConsumerWarps * 32);
+                if (misc[1]) {
+                    const bool ca_split = (s0 != P.cta_start(ca));
+                    for (int e = tid; e < G * D; e += kConsumerWarps * 32) {
+                        const int g = e / D, i = e - g * D;
+                        float M = -INFINITY;
+                        for (int cc = ca; cc <= cb; ++cc) {
+                            const float* sl = p.partials + (size_t)(2 * cc + (cc == ca && ca_split ? 1 : 0)) * G * (D + 2);
+                            M = fmaxf(M, __ldcg(sl + G * D + 2 * g));
+                        }
+                        float acc = 0.f, Lsum = 0.f;
+                        for (int cc = ca; cc <= cb; ++cc) {
+                            const float* sl = p.partials + (size_t)(2 * cc + (cc == ca && ca_split ? 1 : 0)) * G * (D + 2);
+                            const float mp = __ldcg(sl + G * D + 2 * g);
+                            if (mp != -INFINITY) {
+                                const float f = exp2f(mp - M);
+                                acc = fmaf(f, __ldcg(sl + g * D + i), acc);
+                                Lsum = fmaf(f, __ldcg(sl + G * D + 2 * g + 1), Lsum);
+                            }
+                        }
+                        T* o = static_cast<T*>(p.out) + ((size_t)b * Hq + (size_t)h * G + g) * D;
+                        o[i] = from_float<T>(acc / Lsum);
+                    }
+                    if (tid == 0) *cnt = 0;
+                }
+            }
+            ++pi;
+        }
+    }
+    __syncthreads();
+}
+
+// Host-side handle of one instantiation.
+template <typename T, int D, int BS, bool MMA>
+struct VariantOf {
+    static int smem_bytes(int num_seqs, bool fixed) { return Layout<T, D, BS>::bytes(num_seqs, fixed); }
+    static void launch(const DecodeParams& p, const CUtensorMap& tk, const CUtensorMap& tv, int grid, int smem,
+                       cudaStream_t stream) {
+        decode_kernel<T, D, BS, MMA><<<grid, kThreads, smem, stream>>>(p, tk, tv);
+    }
+    static DecodeVariant get() {
+        return DecodeVariant{reinterpret_cast<const void*>(&decode_kernel<T, D, BS, MMA>), Layout<T, D, BS>::S,
+                             kThreads, &smem_bytes, &launch};
+    }
+};
+
+}  // namespace pa
