@@ -4,8 +4,8 @@ Argument marshalling only: every function here passes tensor data pointers,
 sizes and the current CUDA stream to the C ABI declared in ``include/pa.h``
 and raises :class:`PAError` on a non-OK status.  All device work happens in
 the library's CUDA kernels; there is no fallback path.  The library is built
-in-tree by ``__graft_entry__.build()`` (or ``python -m
-paged_kv_cache_280_gb300._build``); importing this package without it raises.
+in-tree by ``__graft_entry__.build()`` (or ``python
+paged_kv_cache_280_gb300/_build.py``); importing this package without it raises.
 """
 from __future__ import annotations
 
@@ -17,7 +17,7 @@ LIB_PATH = os.path.join(_HERE, "libpa.so")
 
 if not os.path.exists(LIB_PATH):
     raise ImportError(
-        f"{LIB_PATH} is missing: build it first (python -m paged_kv_cache_280_gb300._build)"
+        f"{LIB_PATH} is missing: build it first (python paged_kv_cache_280_gb300/_build.py, or __graft_entry__.build())"
     )
 
 _lib = ctypes.CDLL(LIB_PATH)
