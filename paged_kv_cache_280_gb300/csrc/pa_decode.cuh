@@ -549,12 +549,17 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const DecodeParams 
     P.upref = upref;
     P.B = B;
     P.Hkv = Hkv;
-    P.C = C;
     P.PT = p.partition_tiles;
     P.T = (int64_t)Hkv * pref[B];
     P.U = fixed ? (int64_t)Hkv * upref[B] : 0;
-    const int64_t t0 = P.T > 0 ? P.cta_start(c) : 0;
-    const int64_t t1 = P.T > 0 ? P.cta_start(c + 1) : 0;
+    // Only the first min(C, T) CTAs (min(C, U) with partitions) take work, so every
+    // working CTA owns a non-empty range and a split segment's pieces come from
+    // consecutive CTAs -- which the merge count and slot rule rely on.
+    const int64_t units = fixed ? P.U : P.T;
+    P.C = units < (int64_t)C ? (int32_t)units : C;
+    const bool works = P.T > 0 && c < P.C;
+    const int64_t t0 = works ? P.cta_start(c) : 0;
+    const int64_t t1 = works ? P.cta_start(c + 1) : 0;
     const int Hq = p.num_q_heads;
 
     if (warp == kConsumerWarps) {
