@@ -151,6 +151,33 @@ pa_status pa_decode_attention(void* out, const void* q, const void* k_pool, cons
                               void* stream);
 
 /*
+ * Paged decode attention without a caller-supplied workspace.  The pages have
+ * no counterpart to this entry point: it exists for callers that cannot
+ * allocate device memory, such as a plugin inside a framework that owns every
+ * device allocation, or a serving loop that must not allocate once running.
+ * Arguments and results are those of pa_decode_attention, minus the
+ * workspace.  Its scratch is a static buffer of PA_STATIC_WORKSPACE_BYTES
+ * (8 MiB) in the library's device image, held on every GPU that loads the
+ * library until the process exits.  Shapes whose scratch
+ * (pa_decode_workspace_bytes) exceeds it return PA_ERR_WORKSPACE_TOO_SMALL
+ * before anything runs.  The call allocates nothing: it clears the status word
+ * and merge counters at the head of the buffer (cudaMemsetAsync) and enqueues
+ * the decode.  If dev_status_out is not NULL, the call's device status word
+ * (PA_DEV_* bits) is copied there on `stream` afterwards.
+ * The first call on a device looks up the buffer's device address; make that
+ * first call before any stream capture.  Every call on a device shares the
+ * one buffer, so calls that can overlap on the GPU (different streams, or
+ * concurrent host threads) race: serialise them.
+ */
+#define PA_STATIC_WORKSPACE_BYTES (8u << 20)
+pa_status pa_decode_attention_static(void* out, const void* q, const void* k_pool, const void* v_pool,
+                                     const int32_t* block_tables, int32_t max_blocks_per_seq, const int32_t* seq_lens,
+                                     int32_t max_seq_len, int32_t num_seqs, int32_t num_q_heads,
+                                     int32_t num_kv_heads, int32_t head_dim, int32_t block_size, int32_t num_blocks,
+                                     float scale, int32_t partition_tokens, pa_dtype dtype, int32_t* dev_status_out,
+                                     void* stream);
+
+/*
  * Launch facts of pa_decode_attention for these shapes on the current device
  * (no launch): CTAs in the grid, pipeline stages per CTA, dynamic shared
  * memory per CTA in bytes, and 1 if the tensor-core (mma) path is used, else

@@ -55,6 +55,8 @@ _SIGS = {
     "pa_decode_workspace_bytes": (_i32, [_i32, _i32, _i32, _i32, _psz]),
     "pa_decode_attention": (_i32, [_vp, _vp, _vp, _vp, _vp, _i32, _vp, _i32, _i32, _i32, _i32, _i32, _i32, _i32,
                                    _f32, _i32, _vp, _sz, _i32, _vp]),
+    "pa_decode_attention_static": (_i32, [_vp, _vp, _vp, _vp, _vp, _i32, _vp, _i32, _i32, _i32, _i32, _i32, _i32,
+                                          _i32, _f32, _i32, _i32, _vp, _vp]),
     "pa_decode_launch_info": (_i32, [_i32, _i32, _i32, _i32, _i32, _i32, _i32, _pi32, _pi32, _pi32, _pi32]),
     "pa_decode_set_ctas_per_sm": (_i32, [_i32]),
     "pa_alloc_create": (_i32, [_i32, _i32, _vp, ctypes.POINTER(_vp)]),
@@ -164,6 +166,25 @@ def pa_decode_attention(out, q, k_pool, v_pool, block_tables, seq_lens, max_seq_
                                  d, bs, nb, float(scale), int(partition_tokens), _dev_ptr(workspace, "workspace"),
                                  workspace.numel() * workspace.element_size(), _dtype_code(q), _stream(stream)),
         "pa_decode_attention")
+
+
+STATIC_WORKSPACE_BYTES = 8 << 20
+
+
+def pa_decode_attention_static(out, q, k_pool, v_pool, block_tables, seq_lens, max_seq_len, scale,
+                               partition_tokens=0, status=None, stream=None):
+    """pa_decode_attention without a workspace argument, for callers that cannot allocate device memory.
+
+    The library's own per-GPU static scratch (STATIC_WORKSPACE_BYTES) is used; calls that overlap on the GPU
+    race on it.  ``status``: optional int32 CUDA tensor that receives the device status word."""
+    b, hq, d = q.shape
+    nb, hkv, bs, _ = k_pool.shape
+    _ok(_lib.pa_decode_attention_static(_dev_ptr(out, "out"), _dev_ptr(q, "q"), _dev_ptr(k_pool, "k_pool"),
+                                        _dev_ptr(v_pool, "v_pool"), _dev_ptr(block_tables, "block_tables"),
+                                        block_tables.shape[1], _dev_ptr(seq_lens, "seq_lens"), int(max_seq_len), b,
+                                        hq, hkv, d, bs, nb, float(scale), int(partition_tokens), _dtype_code(q),
+                                        _dev_ptr(status, "status"), _stream(stream)),
+        "pa_decode_attention_static")
 
 
 def pa_decode_launch_info(num_seqs, num_q_heads, num_kv_heads, head_dim, block_size, max_blocks_per_seq, dtype):
