@@ -142,6 +142,12 @@ pa_status pa_decode_workspace_bytes(int32_t num_seqs, int32_t num_q_heads, int32
  * must be in [0, num_blocks); others set PA_DEV_BAD_BLOCK_ID.
  * workspace: see pa_decode_workspace_bytes; its first int32 is the status
  * word.  Concurrent calls must use different workspaces.
+ * The kernel is launched as a programmatic dependent of the preceding kernel
+ * on `stream`: when that kernel allows an early start (pa_reshape_and_cache
+ * does), this one computes its work split from seq_lens and block_tables and
+ * starts reading them while that kernel finishes; it reads the pools and q
+ * only after that kernel has completed.  So a kernel that allows early start
+ * must not write seq_lens or block_tables.
  */
 pa_status pa_decode_attention(void* out, const void* q, const void* k_pool, const void* v_pool,
                               const int32_t* block_tables, int32_t max_blocks_per_seq, const int32_t* seq_lens,
@@ -188,9 +194,10 @@ pa_status pa_decode_launch_info(int32_t num_seqs, int32_t num_q_heads, int32_t n
                                 int32_t* stages, int32_t* smem_bytes, int32_t* uses_mma);
 
 /*
- * Tuning: CTAs per SM of the decode grid (1..4; 0 restores the default, 2).
- * Process-wide; affects later pa_decode_attention calls.  More CTAs per SM
- * keep more tiles in flight but add split points (partials) at CTA edges.
+ * Tuning: CTAs per SM of the decode grid (1..8; 0 restores the default: as
+ * many as fit, at most 8).  Process-wide; affects later pa_decode_attention
+ * calls.  More CTAs per SM keep more tiles in flight but add split points
+ * (partials) at CTA edges.
  */
 pa_status pa_decode_set_ctas_per_sm(int32_t ctas);
 

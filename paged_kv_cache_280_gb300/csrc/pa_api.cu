@@ -12,8 +12,7 @@ namespace pa {
 namespace {
 
 constexpr int kMaxDevices = 64;
-std::atomic<int> g_ctas_per_sm{0};  // 0 = default (2)
-constexpr int kDefaultCtasPerSm = 2;
+std::atomic<int> g_ctas_per_sm{0};  // 0 = as many as fit (at most kMaxCtasPerSm)
 
 struct DeviceInfo {
     int sms = 0;
@@ -75,8 +74,8 @@ WorkspaceLayout workspace_layout(int32_t num_seqs, int32_t num_q_heads, int32_t 
     WorkspaceLayout w;
     const size_t G = (size_t)(num_q_heads / num_kv_heads);
     w.counters_off = 256;
-    w.partials_off = w.counters_off + align256((size_t)num_seqs * num_kv_heads * 4);
-    w.total = w.partials_off + (size_t)2 * sms * kMaxCtasPerSm * G * (head_dim + 2) * 4;
+    w.partials_off = w.counters_off + align256((size_t)num_seqs * num_kv_heads * kCountersPerSegment * 4);
+    w.total = w.partials_off + (size_t)2 * sms * kMaxCtasPerSm * partial_slot_floats((int)G, head_dim) * 4;
     return w;
 }
 
@@ -107,8 +106,9 @@ pa_status plan_launch(int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_head
     if (!current_device(&dev, &lp->sms)) return PA_ERR_CUDA;
     const int G = num_q_heads / num_kv_heads;
     lp->mma = (dtype == PA_BF16 && G >= 4);
-    bool found = dtype == PA_F32 ? decode_variant_f32(head_dim, block_size, &lp->v)
-                                 : decode_variant_bf16(head_dim, block_size, lp->mma, &lp->v);
+    bool found = dtype == PA_F32 ? decode_variant_f32(head_dim, block_size, G, &lp->v)
+                 : lp->mma         ? decode_variant_bf16_mma(head_dim, block_size, &lp->v)
+                                   : decode_variant_bf16_fma(head_dim, block_size, G, &lp->v);
     if (!found) return PA_ERR_UNSUPPORTED;
     lp->smem = lp->v.smem_bytes(num_seqs, fixed);
     if (lp->smem > kMaxSmem) return PA_ERR_UNSUPPORTED;
@@ -119,7 +119,7 @@ pa_status plan_launch(int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_head
         return PA_ERR_CUDA;
     if (occ <= 0) return PA_ERR_UNSUPPORTED;
     int want = g_ctas_per_sm.load();
-    if (want <= 0) want = kDefaultCtasPerSm;
+    if (want <= 0) want = kMaxCtasPerSm;
     const int per_sm = occ < want ? occ : want;
     int64_t grid = (int64_t)lp->sms * per_sm;
     const int64_t tiles_bound = (int64_t)num_seqs * num_kv_heads * max_tiles_per_head;

@@ -17,6 +17,7 @@ __global__ void __launch_bounds__(256) reshape_and_cache_kernel(const uint4* __r
                                                                 int32_t num_tokens, int32_t num_kv_heads,
                                                                 int32_t row_chunks, int32_t block_size,
                                                                 int64_t pool_slots, int32_t* status) {
+    pdl_launch_dependents();  // the decode that follows may start its prologue now
     const int64_t per_token = (int64_t)num_kv_heads * row_chunks;
     const int64_t total = (int64_t)num_tokens * per_token;
     for (int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; idx < total;

@@ -19,21 +19,21 @@
 // last CTA to finish a piece of that segment (an atomic counter per
 // segment) merges them:  M = max m_p,  out = sum e^(m_p-M) o_p / sum e^(m_p-M) l_p.
 //
-// CTA layout: warp 4 is the producer, warps 0-3 consume.  The producer reads
-// block-table entries 32 at a time and moves each tile with TMA
-// (cp.async.bulk.tensor, 128-byte swizzle, evict-first L2 hint) into an
-// S-stage ring of shared-memory buffers guarded by full/empty mbarriers;
-// the query rows of each piece arrive by a 1-D bulk copy.  Tile k of the CTA
-// goes to consumer warp k % 4, which keeps its own online-softmax state
-// (running max m, running sum l, accumulator o) in fp32; the four states are
-// merged through shared memory at the end of each piece.
+// CTA layout: two warps and several CTAs per SM.  The producer warp reads
+// block-table entries 32 at a time (one chunk ahead) and moves each tile with
+// TMA (cp.async.bulk.tensor, 128-byte swizzle, evict-first L2 hint) into an
+// S-stage ring of shared-memory buffers guarded by full/empty mbarriers; the
+// query rows of each piece arrive by a 1-D bulk copy.  The consumer warp
+// processes the tiles in order with an online softmax (running max m, running
+// sum l, fp32 accumulator o).  A piece end is a store from registers: there
+// is no merge between warps and no CTA-wide barrier in the loop.
 //
 // Two compute paths:
 //   MMA (bf16, G >= 4): tensor-core mma.sync m16n8k16.  S^T = K q^T with the
 //     16 tokens of a half-block as M and the (padded) 8 query heads as N;
 //     P^T is moved into B-fragment layout with movmatrix; O^T = V^T P^T with
 //     the head dimension as M.
-//   FMA (fp32, or bf16 with G < 4): CUDA cores; lane (t, part) forms the dot
+//   FMA (fp32, or bf16 with G < 4): CUDA cores; lane (t, half) forms the dot
 //     products of token t over half the head dimension, lanes own D/32
 //     output dimensions for P V.
 #pragma once
@@ -45,10 +45,12 @@
 
 namespace pa {
 
-constexpr int kConsumerWarps = 4;
-constexpr int kThreads = (kConsumerWarps + 1) * 32;
+constexpr int kConsumerWarp = 0;
+constexpr int kProducerWarp = 1;
+constexpr int kThreads = 64;
 constexpr int kMaxGroup = 8;
-
+constexpr int kQSlots = 2;          // query-row slots: the producer may run this many pieces ahead
+constexpr int kMaxMergeChunk = 32;  // partial slots staged at a time when merging a split segment
 
 template <typename T>
 struct ElemBytes;
@@ -61,15 +63,17 @@ struct ElemBytes<__nv_bfloat16> {
     static constexpr int value = 2;
 };
 
-// Pipeline depth: about 64 KB of tiles in flight per CTA, 4 to 16 stages,
-// a multiple of the consumer-warp count.
+// Pipeline depth: about PA_STAGE_BYTES (32 KB) of tiles in flight per CTA,
+// 2 to 16 stages.  Several CTAs share an SM.
+#ifndef PA_STAGE_BYTES
+#define PA_STAGE_BYTES 32768
+#endif
 constexpr int stages_for(int bs, int d, int e) {
-    int n = 65536 / (2 * bs * d * e);
-    n = n < 4 ? 4 : (n > 16 ? 16 : n);
-    return n & ~3;
+    int n = PA_STAGE_BYTES / (2 * bs * d * e);
+    return n < 2 ? 2 : (n > 16 ? 16 : n);
 }
 
-template <typename T, int D, int BS>
+template <typename T, int D, int BS, bool MMA>
 struct Layout {
     static constexpr int E = ElemBytes<T>::value;
     static constexpr int S = stages_for(BS, D, E);
@@ -77,21 +81,26 @@ struct Layout {
     static constexpr int kPanels = D * E / 128;    // 128-byte column panels per row
     static constexpr int kStageBytes = 2 * kTileBytes;
     static constexpr int kQSlotBytes = kMaxGroup * D * E;
-    static constexpr int kScratchStride = D + 4;  // floats per (warp, head) row of the merge buffer
     static constexpr int kStagesOff = 0;
     static constexpr int kQOff = kStagesOff + S * kStageBytes;
-    static constexpr int kQfOff = kQOff + 2 * kQSlotBytes;
-    static constexpr int kScratchOff = kQfOff + kMaxGroup * D * 4;
-    static constexpr int kMLOff = kScratchOff + kConsumerWarps * kMaxGroup * kScratchStride * 4;
-    static constexpr int kPTileOff = kMLOff + kConsumerWarps * kMaxGroup * 2 * 4;
-    static constexpr int kBarOff = kPTileOff + kConsumerWarps * 16 * kMaxGroup * 4;
-    static constexpr int kMiscOff = kBarOff + (2 * S + 4) * 8;
-    static constexpr int kPrefixOff = kMiscOff + 128;
+    // CUDA-core path only: fp32 query rows (pre-scaled) and one step's weights.
+    static constexpr int kQfOff = kQOff + kQSlots * kQSlotBytes;
+    static constexpr int kQfBytes = MMA ? 0 : kMaxGroup * D * 4;
+    static constexpr int kPTileOff = kQfOff + kQfBytes;
+    static constexpr int kPTileBytes = MMA ? 0 : 16 * kMaxGroup * 4;
+    // per-piece weights and per-head running max / sum when merging a split segment
+    static constexpr int kMergeOff = kPTileOff + kPTileBytes;
+    static constexpr int kMergeBytes = (kMaxMergeChunk * kMaxGroup + 3 * kMaxGroup) * 4;
+    static constexpr int kBarOff = kMergeOff + kMergeBytes;
+    static constexpr int kMiscOff = kBarOff + (2 * S + 2 * kQSlots + 1) * 8;
+    static constexpr int kPrefixOff = kMiscOff + 64;
     static_assert(kTileBytes % 1024 == 0, "tiles must keep 1024-byte alignment for the 128B swizzle");
     static_assert(kQSlotBytes % 16 == 0, "bulk-copy destination alignment");
-    // dynamic shared memory for num_seqs sequences (+1 KB to align the base)
+    static_assert(kBarOff % 8 == 0, "mbarrier alignment");
+    // dynamic shared memory for num_seqs sequences: prefix sums (two with a
+    // partition size), the clamped lengths, +1 KB to align the base
     static constexpr int bytes(int num_seqs, bool fixed) {
-        return kPrefixOff + (num_seqs + 1) * 4 * (fixed ? 2 : 1) + 1024;
+        return kPrefixOff + (num_seqs + 1) * 4 * (fixed ? 2 : 1) + num_seqs * 4 + 1024;
     }
 };
 
@@ -142,10 +151,19 @@ struct Plan {
     }
 };
 
+// The pieces of a CTA range [t0, t1) in order.  at_t0 marks the piece that
+// starts at t0 (it owns partial slot 0 of the CTA; a later partial piece can
+// only be the last one, which owns slot 1).
 struct PieceIter {
-    int64_t t, t1;
+    int64_t t, t1, t0;
     int b;
-    __device__ __forceinline__ bool next(const Plan& P, int& b_out, int& h, int& j0, int& j1) {
+    __device__ __forceinline__ void init(const Plan& P, int64_t t0_, int64_t t1_) {
+        t0 = t0_;
+        t = t0_;
+        t1 = t1_;
+        b = t0_ < t1_ ? P.find_seq(P.pref, t0_) : 0;
+    }
+    __device__ __forceinline__ bool next(const Plan& P, int& b_out, int& h, int& j0, int& j1, bool& at_t0) {
         if (t >= t1) return false;
         while ((int64_t)P.Hkv * P.pref[b + 1] <= t) ++b;
         const int nb = P.nblocks(b);
@@ -154,6 +172,7 @@ struct PieceIter {
         j0 = (int)(local % nb);
         const int64_t room = t1 - t;
         j1 = (int)((int64_t)(nb - j0) < room ? nb : j0 + room);
+        at_t0 = (t == t0);
         t += j1 - j0;
         b_out = b;
         return true;
@@ -226,7 +245,7 @@ __device__ __forceinline__ void load_vec_f32(uint32_t addr, float* v) {
 }
 
 // ---------------------------------------------------------------------------
-// Per-warp online-softmax state of the two compute paths
+// Online-softmax state of the consumer warp, per compute path
 // ---------------------------------------------------------------------------
 
 // Tensor-core path.  Thread (g = lane/4, tig = lane%4) holds the running max
@@ -265,7 +284,7 @@ struct MmaState {
     __device__ __forceinline__ void step(uint32_t kbase, uint32_t vbase, int row0, int valid, float scale_log2,
                                          int lane) {
         const int g = lane >> 2, tig = lane & 3;
-        float acc[4] = {0.f, 0.f, 0.f, 0.f};
+        float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};  // two chains over the k-steps
         {
             const int row = row0 + (lane & 7) + (((lane >> 3) & 1) << 3);
             const int csel = lane >> 4;
@@ -273,15 +292,15 @@ struct MmaState {
             for (int s = 0; s < MT; ++s) {
                 uint32_t a0, a1, a2, a3;
                 ldmatrix_x4(kbase + tile_chunk_offset<BS>(row, 2 * s + csel), a0, a1, a2, a3);
-                mma_bf16_16816(acc, a0, a1, a2, a3, qb[s][0], qb[s][1]);
+                mma_bf16_16816(acc[s & 1], a0, a1, a2, a3, qb[s][0], qb[s][1]);
             }
         }
-        // acc: (token g, head 2tig), (g, 2tig+1), (g+8, 2tig), (g+8, 2tig+1)
+        // (token g, head 2tig), (g, 2tig+1), (g+8, 2tig), (g+8, 2tig+1)
         const bool v0 = g < valid, v1 = g + 8 < valid;
-        float x0 = v0 ? acc[0] * scale_log2 : -INFINITY;
-        float x1 = v0 ? acc[1] * scale_log2 : -INFINITY;
-        float x2 = v1 ? acc[2] * scale_log2 : -INFINITY;
-        float x3 = v1 ? acc[3] * scale_log2 : -INFINITY;
+        const float x0 = v0 ? (acc[0][0] + acc[1][0]) * scale_log2 : -INFINITY;
+        const float x1 = v0 ? (acc[0][1] + acc[1][1]) * scale_log2 : -INFINITY;
+        const float x2 = v1 ? (acc[0][2] + acc[1][2]) * scale_log2 : -INFINITY;
+        const float x3 = v1 ? (acc[0][3] + acc[1][3]) * scale_log2 : -INFINITY;
         float mx0 = fmaxf(x0, x2), mx1 = fmaxf(x1, x3);
 #pragma unroll
         for (int off = 4; off < 32; off <<= 1) {
@@ -320,48 +339,75 @@ struct MmaState {
         }
     }
 
-    // Write this warp's state into the merge buffers (heads < G only).
-    __device__ __forceinline__ void spill(float* scratch, float* ml, int G, int lane, int stride) {
-        const int g = lane >> 2, tig = lane & 3;
-        float l0 = l[0], l1 = l[1];
+    // Sum the running sums over the 8 token rows (lanes with the same tig).
+    __device__ __forceinline__ void finish() {
 #pragma unroll
         for (int off = 4; off < 32; off <<= 1) {
-            l0 += __shfl_xor_sync(0xffffffffu, l0, off);
-            l1 += __shfl_xor_sync(0xffffffffu, l1, off);
+            l[0] += __shfl_xor_sync(0xffffffffu, l[0], off);
+            l[1] += __shfl_xor_sync(0xffffffffu, l[1], off);
         }
-        const int h0 = 2 * tig, h1 = 2 * tig + 1;
+    }
+
+    // Normalised output rows; `o_rows` points at out[b][h*G][0].
+    template <typename T>
+    __device__ __forceinline__ void store_out(T* o_rows, int G, int lane) const {
+        const int g = lane >> 2, h0 = 2 * (lane & 3), h1 = h0 + 1;
+        const float r0 = 1.f / l[0], r1 = 1.f / l[1];
 #pragma unroll
         for (int i = 0; i < MT; ++i) {
+            const int d0 = 16 * i + g;
             if (h0 < G) {
-                scratch[h0 * stride + 16 * i + g] = o[i][0];
-                scratch[h0 * stride + 16 * i + g + 8] = o[i][2];
+                o_rows[h0 * D + d0] = from_float<T>(o[i][0] * r0);
+                o_rows[h0 * D + d0 + 8] = from_float<T>(o[i][2] * r0);
             }
             if (h1 < G) {
-                scratch[h1 * stride + 16 * i + g] = o[i][1];
-                scratch[h1 * stride + 16 * i + g + 8] = o[i][3];
+                o_rows[h1 * D + d0] = from_float<T>(o[i][1] * r1);
+                o_rows[h1 * D + d0 + 8] = from_float<T>(o[i][3] * r1);
+            }
+        }
+    }
+
+    // Unnormalised partial: slot = [G][D] o, then [G] (m, l).
+    __device__ __forceinline__ void store_partial(float* slot, int G, int lane) const {
+        const int g = lane >> 2, h0 = 2 * (lane & 3), h1 = h0 + 1;
+#pragma unroll
+        for (int i = 0; i < MT; ++i) {
+            const int d0 = 16 * i + g;
+            if (h0 < G) {
+                slot[h0 * D + d0] = o[i][0];
+                slot[h0 * D + d0 + 8] = o[i][2];
+            }
+            if (h1 < G) {
+                slot[h1 * D + d0] = o[i][1];
+                slot[h1 * D + d0 + 8] = o[i][3];
             }
         }
         if (g == 0) {
-            if (h0 < G) { ml[2 * h0] = m[0]; ml[2 * h0 + 1] = l0; }
-            if (h1 < G) { ml[2 * h1] = m[1]; ml[2 * h1 + 1] = l1; }
+            if (h0 < G) { slot[G * D + 2 * h0] = m[0]; slot[G * D + 2 * h0 + 1] = l[0]; }
+            if (h1 < G) { slot[G * D + 2 * h1] = m[1]; slot[G * D + 2 * h1 + 1] = l[1]; }
         }
     }
 };
 
 // CUDA-core path.  Lane = (token t = lane & 15, half = lane >> 4) for the dot
 // products; lane owns output dims [lane * VEC, lane * VEC + VEC) for P V.
-template <typename T, int D, int BS>
+// GF > 0 fixes the query heads per KV head at compile time (no per-head
+// predication); GF == 0 handles any G <= 8 at run time.
+template <typename T, int D, int BS, int GF>
 struct FmaState {
     static constexpr int E = ElemBytes<T>::value;
     static constexpr int VEC = D / 32;
     static constexpr int EPC = 16 / E;              // elements per 16-byte chunk
     static constexpr int HALF_CHUNKS = D * E / 32;  // chunks per half row
-    float m[kMaxGroup], l[kMaxGroup];
-    float o[kMaxGroup][VEC];
+    static constexpr int GN = GF > 0 ? GF : kMaxGroup;
+    float m[GN], l[GN];
+    float o[GN][VEC];
+
+    __device__ __forceinline__ static bool active(int g, int G) { return GF > 0 || g < G; }
 
     __device__ __forceinline__ void reset() {
 #pragma unroll
-        for (int g = 0; g < kMaxGroup; ++g) {
+        for (int g = 0; g < GN; ++g) {
             m[g] = -INFINITY;
             l[g] = 0.f;
 #pragma unroll
@@ -369,13 +415,26 @@ struct FmaState {
         }
     }
 
-    // qf: [G][D] fp32 query rows pre-multiplied by scale*log2(e); ptile: this warp's [16][8] weights.
+    __device__ __forceinline__ void pv_token(uint32_t vbase, int row, int byte0, const float* ptile_row, int G) {
+        float vv[VEC];
+        load_vec_f32<T, VEC>(vbase + tile_chunk_offset<BS>(row, byte0 >> 4) + (byte0 & 15), vv);
+#pragma unroll
+        for (int g = 0; g < GN; ++g) {
+            if (active(g, G)) {
+                const float pw = ptile_row[g];
+#pragma unroll
+                for (int v = 0; v < VEC; ++v) o[g][v] = fmaf(pw, vv[v], o[g][v]);
+            }
+        }
+    }
+
+    // qf: [G][D] fp32 query rows pre-multiplied by scale*log2(e); ptile: [16][8] weights of one step.
     __device__ __forceinline__ void step(uint32_t kbase, uint32_t vbase, int row0, int valid, int G,
                                          const float* qf, float* ptile, int lane) {
         const int t = lane & 15, half = lane >> 4;
-        float acc[kMaxGroup];
+        float acc[GN][2];  // two chains per head (even / odd chunks)
 #pragma unroll
-        for (int g = 0; g < kMaxGroup; ++g) acc[g] = 0.f;
+        for (int g = 0; g < GN; ++g) acc[g][0] = acc[g][1] = 0.f;
         const int row = row0 + t;
 #pragma unroll
         for (int cc = 0; cc < HALF_CHUNKS; ++cc) {
@@ -383,25 +442,28 @@ struct FmaState {
             float kv[EPC];
             load_chunk_f32<T>(kbase + tile_chunk_offset<BS>(row, chunk), kv);
 #pragma unroll
-            for (int g = 0; g < kMaxGroup; ++g) {
-                if (g < G) {
+            for (int g = 0; g < GN; ++g) {
+                if (active(g, G)) {
                     const float4* qp = reinterpret_cast<const float4*>(qf + g * D + chunk * EPC);
 #pragma unroll
                     for (int e4 = 0; e4 < EPC / 4; ++e4) {
                         const float4 qv = qp[e4];
-                        acc[g] = fmaf(qv.x, kv[4 * e4 + 0], acc[g]);
-                        acc[g] = fmaf(qv.y, kv[4 * e4 + 1], acc[g]);
-                        acc[g] = fmaf(qv.z, kv[4 * e4 + 2], acc[g]);
-                        acc[g] = fmaf(qv.w, kv[4 * e4 + 3], acc[g]);
+                        float& a = acc[g][cc & 1];
+                        a = fmaf(qv.x, kv[4 * e4 + 0], a);
+                        a = fmaf(qv.y, kv[4 * e4 + 1], a);
+                        a = fmaf(qv.z, kv[4 * e4 + 2], a);
+                        a = fmaf(qv.w, kv[4 * e4 + 3], a);
                     }
                 }
             }
         }
-        float alpha[kMaxGroup];
+        float alpha[GN];
 #pragma unroll
-        for (int g = 0; g < kMaxGroup; ++g) {
-            if (g < G) {
-                float x = acc[g] + __shfl_xor_sync(0xffffffffu, acc[g], 16);
+        for (int g = 0; g < GN; ++g) {
+            alpha[g] = 1.f;
+            if (active(g, G)) {
+                float x = acc[g][0] + acc[g][1];
+                x += __shfl_xor_sync(0xffffffffu, x, 16);
                 x = t < valid ? x : -INFINITY;
                 float mx = x;
 #pragma unroll
@@ -409,59 +471,150 @@ struct FmaState {
                 const float mn = fmaxf(m[g], mx);
                 alpha[g] = exp2f(m[g] - mn);
                 const float pw = exp2f(x - mn);
-                float s = pw;
+                float sum = pw;
 #pragma unroll
-                for (int off = 1; off < 16; off <<= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
-                l[g] = l[g] * alpha[g] + s;
+                for (int off = 1; off < 16; off <<= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
+                l[g] = l[g] * alpha[g] + sum;
                 m[g] = mn;
                 if (half == 0) ptile[t * kMaxGroup + g] = pw;
-            } else {
-                alpha[g] = 1.f;
             }
         }
         __syncwarp();
 #pragma unroll
-        for (int g = 0; g < kMaxGroup; ++g)
+        for (int g = 0; g < GN; ++g)
 #pragma unroll
             for (int v = 0; v < VEC; ++v) o[g][v] *= alpha[g];
         const int byte0 = lane * VEC * E;
-        for (int tt = 0; tt < valid; ++tt) {
-            float vv[VEC];
-            load_vec_f32<T, VEC>(vbase + tile_chunk_offset<BS>(row0 + tt, byte0 >> 4) + (byte0 & 15), vv);
-            const float4 p0 = reinterpret_cast<const float4*>(ptile + tt * kMaxGroup)[0];
-            const float4 p1 = reinterpret_cast<const float4*>(ptile + tt * kMaxGroup)[1];
-            const float pg[8] = {p0.x, p0.y, p0.z, p0.w, p1.x, p1.y, p1.z, p1.w};
+        if (valid == 16) {
 #pragma unroll
-            for (int g = 0; g < kMaxGroup; ++g)
-                if (g < G)
-#pragma unroll
-                    for (int v = 0; v < VEC; ++v) o[g][v] = fmaf(pg[g], vv[v], o[g][v]);
+            for (int tt = 0; tt < 16; ++tt) pv_token(vbase, row0 + tt, byte0, ptile + tt * kMaxGroup, G);
+        } else {
+            for (int tt = 0; tt < valid; ++tt) pv_token(vbase, row0 + tt, byte0, ptile + tt * kMaxGroup, G);
         }
         __syncwarp();
     }
 
-    __device__ __forceinline__ void spill(float* scratch, float* ml, int G, int lane, int stride) {
+    // Normalised output rows; `o_rows` points at out[b][h*G][0].  m and l are
+    // the same in every lane (reduced by shuffles in step()).
+    template <typename TO>
+    __device__ __forceinline__ void store_out(TO* o_rows, int G, int lane) const {
 #pragma unroll
-        for (int g = 0; g < kMaxGroup; ++g) {
-            if (g < G) {
+        for (int g = 0; g < GN; ++g) {
+            if (active(g, G)) {
+                const float r = 1.f / l[g];
 #pragma unroll
-                for (int v = 0; v < VEC; ++v) scratch[g * stride + lane * VEC + v] = o[g][v];
+                for (int v = 0; v < VEC; ++v) o_rows[g * D + lane * VEC + v] = from_float<TO>(o[g][v] * r);
+            }
+        }
+    }
+
+    // Unnormalised partial: slot = [G][D] o, then [G] (m, l).
+    __device__ __forceinline__ void store_partial(float* slot, int G, int lane) const {
+#pragma unroll
+        for (int g = 0; g < GN; ++g) {
+            if (active(g, G)) {
+#pragma unroll
+                for (int v = 0; v < VEC; ++v) slot[g * D + lane * VEC + v] = o[g][v];
                 if (lane == 0) {
-                    ml[2 * g] = m[g];
-                    ml[2 * g + 1] = l[g];
+                    slot[G * D + 2 * g] = m[g];
+                    slot[G * D + 2 * g + 1] = l[g];
                 }
             }
         }
     }
 };
 
+// Merge of a split segment, done by the consumer warp of the CTA that
+// completed its last piece, after that warp's own pieces are done:
+//   M = max_p m_p,   out = sum_p e^(m_p-M) o_p / sum_p e^(m_p-M) l_p.
+// The pieces' partial slots are bulk-copied into the idle stage ring a chunk
+// at a time (one round trip per chunk); each head's running max and sum are
+// folded per chunk and the output elements (lane + 32 j) accumulated from
+// shared memory.
+template <typename T, int D>
+__device__ __forceinline__ void merge_staged(const float* partials, size_t slot_floats, T* orow, int ca, int cb,
+                                             bool ca_split, int G, int lane, const uint8_t* ring, uint32_t ring_s,
+                                             int ring_bytes, float* work, uint32_t mbar, uint32_t& mphase,
+                                             volatile int32_t* abort_flag, int32_t* status) {
+    constexpr int JN = kMaxGroup * D / 32;
+    const uint32_t slot_bytes = (uint32_t)(slot_floats * 4);
+    int per_chunk = ring_bytes / (int)slot_bytes;
+    per_chunk = per_chunk > kMaxMergeChunk ? kMaxMergeChunk : per_chunk;
+    float* wgt = work;                                 // [kMaxMergeChunk][kMaxGroup]
+    float* hst = work + kMaxMergeChunk * kMaxGroup;    // [0..7] max, [8..15] sum, [16..23] rescale
+    const float* buf = reinterpret_cast<const float*>(ring);
+    const int np = cb - ca + 1, nel = G * D;
+    auto slot_of = [&](int cc) { return partials + (size_t)(2 * cc + (cc == ca && ca_split ? 1 : 0)) * slot_floats; };
+    if (lane < G) {
+        hst[lane] = -INFINITY;
+        hst[8 + lane] = 0.f;
+    }
+    float acc[JN];
+#pragma unroll
+    for (int j = 0; j < JN; ++j) acc[j] = 0.f;
+    for (int c0 = 0; c0 < np; c0 += per_chunk) {
+        const int nc = min(per_chunk, np - c0);
+        __syncwarp();
+        if (lane == 0) {
+            // other CTAs wrote the slots (made visible by the counter protocol);
+            // this warp last read the ring through the generic proxy
+            fence_proxy_async_global();
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            mbar_arrive_expect_tx(mbar, nc * slot_bytes);
+            for (int i = 0; i < nc; ++i) bulk_load(ring_s + i * slot_bytes, slot_of(ca + c0 + i), slot_bytes, mbar);
+        }
+        // a bounded wait that also runs after an abort, so no copy is left in flight
+        bool ok = mbar_wait(mbar, mphase & 1);
+        ok = __all_sync(0xffffffffu, ok);
+        ++mphase;
+        if (!ok) {
+            *abort_flag = 1;
+            if (lane == 0) flag_status(status, PA_DEV_WAIT_TIMEOUT);
+            return;
+        }
+        if (lane < G) {
+            const int hd = lane;
+            float Mc = hst[hd];
+            for (int i = 0; i < nc; ++i) Mc = fmaxf(Mc, buf[i * slot_floats + G * D + 2 * hd]);
+            const float resc = exp2f(hst[hd] - Mc);
+            float Lr = hst[8 + hd] * resc;
+            for (int i = 0; i < nc; ++i) {
+                const float w = exp2f(buf[i * slot_floats + G * D + 2 * hd] - Mc);
+                wgt[i * kMaxGroup + hd] = w;
+                Lr = fmaf(w, buf[i * slot_floats + G * D + 2 * hd + 1], Lr);
+            }
+            hst[hd] = Mc;
+            hst[8 + hd] = Lr;
+            hst[16 + hd] = resc;
+        }
+        __syncwarp();
+#pragma unroll
+        for (int j = 0; j < JN; ++j) {
+            const int e = lane + 32 * j;
+            if (e < nel) {
+                const int hd = e / D;
+                float a = acc[j] * hst[16 + hd];
+                for (int i = 0; i < nc; ++i) a = fmaf(wgt[i * kMaxGroup + hd], buf[i * slot_floats + e], a);
+                acc[j] = a;
+            }
+        }
+    }
+    __syncwarp();
+#pragma unroll
+    for (int j = 0; j < JN; ++j) {
+        const int e = lane + 32 * j;
+        if (e < nel) orow[e] = from_float<T>(acc[j] / hst[8 + e / D]);
+    }
+    __syncwarp();
+}
+
 // ---------------------------------------------------------------------------
 // The kernel
 // ---------------------------------------------------------------------------
-template <typename T, int D, int BS, bool MMA>
-__global__ void __launch_bounds__(kThreads, 2) decode_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tmap_k,
+template <typename T, int D, int BS, bool MMA, int GF>
+__global__ void __launch_bounds__(kThreads) decode_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tmap_k,
                                                           const __grid_constant__ CUtensorMap tmap_v) {
-    using L = Layout<T, D, BS>;
+    using L = Layout<T, D, BS, MMA>;
     constexpr int S = L::S;
     constexpr int E = L::E;
     extern __shared__ uint8_t smem_raw[];
@@ -470,27 +623,31 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const DecodeParams 
     uint8_t* base = smem_raw + (base_s - raw_s);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int B = p.num_seqs, Hkv = p.num_kv_heads, G = p.group, C = p.num_ctas, c = blockIdx.x;
+    const int B = p.num_seqs, Hkv = p.num_kv_heads, C = p.num_ctas, c = blockIdx.x;
+    const int G = GF > 0 ? GF : p.group;  // query heads per KV head
     const bool fixed = p.partition_tiles > 0;
     int32_t* pref = reinterpret_cast<int32_t*>(base + L::kPrefixOff);
     int32_t* upref = pref + (B + 1);
+    int32_t* lens_s = upref + (fixed ? B + 1 : 0);  // clamped seq_lens
     volatile int32_t* misc = reinterpret_cast<volatile int32_t*>(base + L::kMiscOff);
-    int32_t* wsum = reinterpret_cast<int32_t*>(base + L::kMiscOff + 32);  // [5] blocks, [5] partitions
+    int32_t* wsum = reinterpret_cast<int32_t*>(base + L::kMiscOff + 16);  // [2] blocks, [2] partitions
     const uint32_t bar0 = base_s + L::kBarOff;
     auto full_bar = [&](int s) { return bar0 + 8u * s; };
     auto empty_bar = [&](int s) { return bar0 + 8u * (S + s); };
     auto qfull_bar = [&](int i) { return bar0 + 8u * (2 * S + i); };
-    auto qempty_bar = [&](int i) { return bar0 + 8u * (2 * S + 2 + i); };
+    auto qempty_bar = [&](int i) { return bar0 + 8u * (2 * S + kQSlots + i); };
+    const uint32_t merge_bar = bar0 + 8u * (2 * S + 2 * kQSlots);
 
     if (tid == 0) {
         for (int s = 0; s < S; ++s) {
             mbar_init(full_bar(s), 1);
             mbar_init(empty_bar(s), 1);
         }
-        for (int i = 0; i < 2; ++i) {
+        for (int i = 0; i < kQSlots; ++i) {
             mbar_init(qfull_bar(i), 1);
             mbar_init(qempty_bar(i), 1);
         }
+        mbar_init(merge_bar, 1);
         fence_barrier_init();
         misc[0] = 0;  // abort flag
     }
@@ -519,17 +676,19 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const DecodeParams 
         }
         if (lane == 31) {
             wsum[warp] = xb;
-            wsum[8 + warp] = xp;
+            wsum[2 + warp] = xp;
         }
         __syncthreads();
         int32_t ob = 0, op = 0;
         for (int w = 0; w < warp; ++w) {
             ob += wsum[w];
-            op += wsum[8 + w];
+            op += wsum[2 + w];
         }
         int32_t rb = ob + xb - nblk, rp = op + xp - nprt;
         for (int b = lo; b < hi; ++b) {
-            const int nb = (clamp_len(__ldg(p.seq_lens + b), p.max_len) + BS - 1) / BS;
+            const int len = clamp_len(__ldg(p.seq_lens + b), p.max_len);
+            const int nb = (len + BS - 1) / BS;
+            lens_s[b] = len;
             pref[b] = rb;
             rb += nb;
             if (fixed) {
@@ -561,8 +720,10 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const DecodeParams 
     const int64_t t0 = works ? P.cta_start(c) : 0;
     const int64_t t1 = works ? P.cta_start(c + 1) : 0;
     const int Hq = p.num_q_heads;
+    // one partial slot: [G][D] unnormalised o, then [4 quarters][G] (m, l)
+    const size_t slot_floats = partial_slot_floats(G, D);
 
-    if (warp == kConsumerWarps) {
+    if (warp == kProducerWarp) {
         // =========================== producer ===========================
         if (lane == 0) {
             prefetch_tensormap(&tmap_k);
@@ -571,91 +732,119 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const DecodeParams 
         const uint64_t policy = policy_evict_first();
         const uint32_t q_bytes = (uint32_t)(G * D * E);
         uint32_t k = 0, pi = 0, k_issued = 0, pi_issued = 0;
-        PieceIter it{t0, t1, t0 < t1 ? P.find_seq(pref, t0) : 0};
-        int b, h, j0, j1;
-        while (it.next(P, b, h, j0, j1)) {
-            const int qs = pi & 1;
-            if (role_wait(qempty_bar(qs), ((pi >> 1) & 1) ^ 1, misc, p.status)) {
-                if (lane == 0) {
-                    mbar_arrive_expect_tx(qfull_bar(qs), q_bytes);
-                    const uint8_t* src = static_cast<const uint8_t*>(p.q) + ((size_t)b * Hq + (size_t)h * G) * D * E;
-                    bulk_load(base_s + L::kQOff + qs * L::kQSlotBytes, src, q_bytes, qfull_bar(qs));
-                }
-                pi_issued = pi + 1;
-            }
-            const int32_t* row = p.block_tables + (size_t)b * p.max_blocks_per_seq;
-            for (int jb = j0; jb < j1; jb += 32) {
-                const int n = min(32, j1 - jb);
-                int32_t blk = 0;
-                if (lane < n) {
-                    blk = __ldg(row + jb + lane);
-                    if (blk < 0 || blk >= p.num_blocks) {
-                        flag_status(p.status, PA_DEV_BAD_BLOCK_ID);
-                        blk = 0;
+        // Walk the range in chunks of up to 32 tiles of one piece.  The block-table
+        // entries of the next chunk (of this piece or of the next one) are loaded
+        // before this chunk's tiles are issued, so their latency overlaps the issue.
+        PieceIter it;
+        it.init(P, t0, t1);
+        int b = 0, h = 0, j0 = 0, j1 = 0, nb_ = 0, nh = 0, nj0 = 0, nj1 = 0;
+        bool at0 = false;
+        bool have = it.next(P, b, h, j0, j1, at0);
+        bool have_next = have && it.next(P, nb_, nh, nj0, nj1, at0);
+        auto table_chunk = [&](int bb, int jfrom, int jend) -> int32_t {
+            return lane < jend - jfrom && lane < 32 ? __ldg(p.block_tables + (size_t)bb * p.max_blocks_per_seq + jfrom + lane)
+                                                    : 0;
+        };
+        int32_t blk_cur = have ? table_chunk(b, j0, j1) : 0;
+        // Everything above reads only seq_lens and block_tables, which the append and
+        // copy kernels of this library never write; pool and query reads wait for the
+        // preceding kernel (launched as a programmatic dependent, see pa_api.cu).
+        pdl_wait_prerequisites();
+        int jb = j0;
+        while (have) {
+            if (jb == j0) {  // first chunk of a piece: its query rows
+                const int qs = pi % kQSlots;
+                if (role_wait(qempty_bar(qs), ((pi / kQSlots) & 1) ^ 1, misc, p.status)) {
+                    if (lane == 0) {
+                        mbar_arrive_expect_tx(qfull_bar(qs), q_bytes);
+                        const uint8_t* src = static_cast<const uint8_t*>(p.q) + ((size_t)b * Hq + (size_t)h * G) * D * E;
+                        bulk_load(base_s + L::kQOff + qs * L::kQSlotBytes, src, q_bytes, qfull_bar(qs));
                     }
+                    pi_issued = pi + 1;
                 }
-                for (int i = 0; i < n; ++i) {
-                    const int32_t bid = __shfl_sync(0xffffffffu, blk, i);
-                    const int st = k % S;
-                    if (role_wait(empty_bar(st), ((k / S) & 1) ^ 1, misc, p.status)) {
-                        if (lane == 0) {
-                            mbar_arrive_expect_tx(full_bar(st), (uint32_t)L::kStageBytes);
-                            const int32_t y = (bid * Hkv + h) * BS;
-                            const uint32_t ks = base_s + L::kStagesOff + st * L::kStageBytes;
+            }
+            const int n = min(32, j1 - jb);
+            const bool more_here = jb + 32 < j1;
+            int32_t blk_nxt = 0;
+            if (more_here)
+                blk_nxt = table_chunk(b, jb + 32, j1);
+            else if (have_next)
+                blk_nxt = table_chunk(nb_, nj0, nj1);
+            for (int i = 0; i < n; ++i) {
+                int32_t bid = __shfl_sync(0xffffffffu, blk_cur, i);
+                if (bid < 0 || bid >= p.num_blocks) {  // warp-uniform
+                    if (lane == 0) flag_status(p.status, PA_DEV_BAD_BLOCK_ID);
+                    bid = 0;
+                }
+                const int st = k % S;
+                if (role_wait(empty_bar(st), ((k / S) & 1) ^ 1, misc, p.status)) {
+                    if (lane == 0) {
+                        mbar_arrive_expect_tx(full_bar(st), (uint32_t)L::kStageBytes);
+                        const int32_t y = (bid * Hkv + h) * BS;
+                        const uint32_t ks = base_s + L::kStagesOff + st * L::kStageBytes;
 #pragma unroll
-                            for (int pn = 0; pn < L::kPanels; ++pn) {
-                                tma_load_2d(ks + pn * BS * 128, &tmap_k, pn * (128 / E), y, full_bar(st), policy);
-                                tma_load_2d(ks + L::kTileBytes + pn * BS * 128, &tmap_v, pn * (128 / E), y,
-                                            full_bar(st), policy);
-                            }
+                        for (int pn = 0; pn < L::kPanels; ++pn) {
+                            tma_load_2d(ks + pn * BS * 128, &tmap_k, pn * (128 / E), y, full_bar(st), policy);
+                            tma_load_2d(ks + L::kTileBytes + pn * BS * 128, &tmap_v, pn * (128 / E), y, full_bar(st),
+                                        policy);
                         }
-                        k_issued = k + 1;
                     }
-                    ++k;
+                    k_issued = k + 1;
                 }
+                ++k;
             }
-            ++pi;
+            if (more_here) {
+                jb += 32;
+            } else {
+                ++pi;
+                b = nb_, h = nh, j0 = nj0, j1 = nj1;
+                jb = j0;
+                have = have_next;
+                have_next = have && it.next(P, nb_, nh, nj0, nj1, at0);
+            }
+            blk_cur = blk_nxt;
         }
         // never leave the CTA with copies still landing in its shared memory
         for (uint32_t kk = k_issued > (uint32_t)S ? k_issued - S : 0; kk < k_issued; ++kk)
             mbar_wait(full_bar(kk % S), (kk / S) & 1);
-        for (uint32_t qq = pi_issued > 2u ? pi_issued - 2 : 0; qq < pi_issued; ++qq)
-            mbar_wait(qfull_bar(qq & 1), (qq >> 1) & 1);
-    } else {
-        // =========================== consumers ===========================
+        for (uint32_t qq = pi_issued > (uint32_t)kQSlots ? pi_issued - kQSlots : 0; qq < pi_issued; ++qq)
+            mbar_wait(qfull_bar(qq % kQSlots), (qq / kQSlots) & 1);
+    } else if (warp == kConsumerWarp) {
+        // =========================== consumer ===========================
         // zero outputs of empty sequences
         for (int bb = c; bb < B; bb += C) {
             if (pref[bb + 1] == pref[bb]) {
                 T* o = static_cast<T*>(p.out) + (size_t)bb * Hq * D;
-                for (int e = tid; e < Hq * D; e += kConsumerWarps * 32) o[e] = from_float<T>(0.f);
+                for (int e = lane; e < Hq * D; e += 32) o[e] = from_float<T>(0.f);
             }
         }
-        float* scratch = reinterpret_cast<float*>(base + L::kScratchOff);
-        float* mlbuf = reinterpret_cast<float*>(base + L::kMLOff);
         float* qf = reinterpret_cast<float*>(base + L::kQfOff);
-        float* ptile = reinterpret_cast<float*>(base + L::kPTileOff) + warp * 16 * kMaxGroup;
-        using State = typename std::conditional<MMA, MmaState<D, BS>, FmaState<T, D, BS>>::type;
-        State st;
+        float* ptile = reinterpret_cast<float*>(base + L::kPTileOff);
+        typename std::conditional<MMA, MmaState<D, BS>, FmaState<T, D, BS, GF>>::type st;
         uint32_t k = 0, pi = 0;
-        PieceIter it{t0, t1, t0 < t1 ? P.find_seq(pref, t0) : 0};
+        PieceIter it;
+        it.init(P, t0, t1);
         int b, h, j0, j1;
-        while (it.next(P, b, h, j0, j1)) {
-            const int qs = pi & 1;
+        bool at_t0;
+        // merges left for after the loop (a CTA completes at most its two boundary segments)
+        int npend = 0, mb0 = 0, mh0 = 0, mca0 = 0, mcb0 = 0, mb1 = 0, mh1 = 0, mca1 = 0, mcb1 = 0;
+        bool msp0 = false, msp1 = false;
+        while (it.next(P, b, h, j0, j1, at_t0)) {
+            const int qs = pi % kQSlots;
             const uint8_t* qslot = base + L::kQOff + qs * L::kQSlotBytes;
-            const bool qok = role_wait(qfull_bar(qs), (pi >> 1) & 1, misc, p.status);
+            const bool qok = role_wait(qfull_bar(qs), (pi / kQSlots) & 1, misc, p.status);
             if constexpr (MMA) {
                 if (qok) st.load_q(qslot, G, lane);
             } else {
                 const T* qsrc = reinterpret_cast<const T*>(qslot);
-                for (int e = tid; e < G * D; e += kConsumerWarps * 32)
-                    qf[e] = qok ? static_cast<float>(qsrc[e]) * p.scale_log2 : 0.f;
-                named_barrier(1, kConsumerWarps * 32);
+                for (int e = lane; e < G * D; e += 32) qf[e] = qok ? static_cast<float>(qsrc[e]) * p.scale_log2 : 0.f;
             }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(qempty_bar(qs));
             st.reset();
-            const int len = clamp_len(__ldg(p.seq_lens + b), p.max_len);
+            const int len = lens_s[b];
             const int ntile = j1 - j0;
-            for (int i = warp - (int)(k & 3); i < ntile; i += kConsumerWarps) {
-                if (i < 0) continue;
+            for (int i = 0; i < ntile; ++i) {
                 const uint32_t kk = k + i;
                 const int sidx = kk % S;
                 if (role_wait(full_bar(sidx), (kk / S) & 1, misc, p.status)) {
@@ -676,97 +865,77 @@ __global__ void __launch_bounds__(kThreads, 2) decode_kernel(const DecodeParams 
                 if (lane == 0) mbar_arrive(empty_bar(sidx));
             }
             k += ntile;
-
-            // ---- merge the four warps' states ----
-            st.spill(scratch + warp * kMaxGroup * L::kScratchStride, mlbuf + warp * kMaxGroup * 2, G, lane,
-                     L::kScratchStride);
-            named_barrier(1, kConsumerWarps * 32);
+            if constexpr (MMA) st.finish();
             const int nb = P.nblocks(b);
-            const bool whole = (j0 == 0 && j1 == nb);
-            const bool first_piece = (pi == 0);
-            float* slot = p.partials + (size_t)(2 * c + (first_piece ? 0 : 1)) * G * (D + 2);
-            for (int e = tid; e < G * D; e += kConsumerWarps * 32) {
-                const int g = e / D, i = e - g * D;
-                float M = -INFINITY;
-#pragma unroll
-                for (int w = 0; w < kConsumerWarps; ++w) M = fmaxf(M, mlbuf[(w * kMaxGroup + g) * 2]);
-                float acc = 0.f, Lsum = 0.f;
-#pragma unroll
-                for (int w = 0; w < kConsumerWarps; ++w) {
-                    const float mw = mlbuf[(w * kMaxGroup + g) * 2];
-                    if (mw != -INFINITY) {
-                        const float f = exp2f(mw - M);
-                        acc = fmaf(f, scratch[(w * kMaxGroup + g) * L::kScratchStride + i], acc);
-                        Lsum = fmaf(f, mlbuf[(w * kMaxGroup + g) * 2 + 1], Lsum);
-                    }
-                }
-                if (whole) {
-                    T* o = static_cast<T*>(p.out) + ((size_t)b * Hq + (size_t)h * G + g) * D;
-                    o[i] = from_float<T>(acc / Lsum);
-                } else {
-                    slot[g * D + i] = acc;
-                    if (i == 0) {
-                        slot[G * D + 2 * g] = M;
-                        slot[G * D + 2 * g + 1] = Lsum;
-                    }
-                }
-            }
-            if (!whole) __threadfence();
-            named_barrier(1, kConsumerWarps * 32);
-            if (tid == 0) mbar_arrive(qempty_bar(qs));
-            if (!whole) {
-                // ---- the last CTA to finish a piece of this segment merges them ----
+            T* orow = static_cast<T*>(p.out) + ((size_t)b * Hq + (size_t)h * G) * D;
+            if (j0 == 0 && j1 == nb) {
+                st.store_out(orow, G, lane);
+            } else {
+                // Split segment: store the partial; the CTA that completes the last
+                // piece of (b, h) (an atomic counter per segment) merges them.
+                float* slot = p.partials + (size_t)(2 * c + (at_t0 ? 0 : 1)) * slot_floats;
+                st.store_partial(slot, G, lane);
+                __threadfence();
+                __syncwarp();
                 const int64_t s0 = P.seg_start(b, h);
                 const int ca = P.cta_of(s0), cb = P.cta_of(s0 + nb - 1);
                 int32_t* cnt = p.counters + (size_t)b * Hkv + h;
-                if (tid == 0) {
-                    const int prev = atomicAdd(cnt, 1);
-                    const int last = (prev == cb - ca);
+                int last = 0;
+                if (lane == 0) {
+                    last = atomicAdd(cnt, 1) == cb - ca;
                     if (last) __threadfence();
-                    misc[1] = last;
                 }
-                named_barrier(1, kConsumerWarps * 32);
-                if (misc[1]) {
-                    const bool ca_split = (s0 != P.cta_start(ca));
-                    for (int e = tid; e < G * D; e += kConsumerWarps * 32) {
-                        const int g = e / D, i = e - g * D;
-                        float M = -INFINITY;
-                        for (int cc = ca; cc <= cb; ++cc) {
-                            const float* sl = p.partials + (size_t)(2 * cc + (cc == ca && ca_split ? 1 : 0)) * G * (D + 2);
-                            M = fmaxf(M, __ldcg(sl + G * D + 2 * g));
-                        }
-                        float acc = 0.f, Lsum = 0.f;
-                        for (int cc = ca; cc <= cb; ++cc) {
-                            const float* sl = p.partials + (size_t)(2 * cc + (cc == ca && ca_split ? 1 : 0)) * G * (D + 2);
-                            const float mp = __ldcg(sl + G * D + 2 * g);
-                            if (mp != -INFINITY) {
-                                const float f = exp2f(mp - M);
-                                acc = fmaf(f, __ldcg(sl + g * D + i), acc);
-                                Lsum = fmaf(f, __ldcg(sl + G * D + 2 * g + 1), Lsum);
-                            }
-                        }
-                        T* o = static_cast<T*>(p.out) + ((size_t)b * Hq + (size_t)h * G + g) * D;
-                        o[i] = from_float<T>(acc / Lsum);
+                last = __shfl_sync(0xffffffffu, last, 0);
+                if (last) {  // merged once this CTA's own pieces are done
+                    const bool sp = s0 != P.cta_start(ca);
+                    if (npend == 0) {
+                        mb0 = b, mh0 = h, mca0 = ca, mcb0 = cb, msp0 = sp;
+                    } else {
+                        mb1 = b, mh1 = h, mca1 = ca, mcb1 = cb, msp1 = sp;
                     }
-                    if (tid == 0) *cnt = 0;
+                    ++npend;
                 }
             }
             ++pi;
+        }
+        // The stage ring is idle now (every issued tile has been consumed): use it
+        // to stage the partials of the split segments this CTA completed.
+        uint32_t mphase = 0;
+#pragma unroll 1
+        for (int i = 0; i < npend; ++i) {
+            const int mb = i ? mb1 : mb0, mh = i ? mh1 : mh0;
+            T* orow = static_cast<T*>(p.out) + ((size_t)mb * Hq + (size_t)mh * G) * D;
+            merge_staged<T, D>(p.partials, slot_floats, orow, i ? mca1 : mca0, i ? mcb1 : mcb0, i ? msp1 : msp0, G, lane,
+                               base, base_s, S * L::kStageBytes, reinterpret_cast<float*>(base + L::kMergeOff),
+                               merge_bar, mphase, misc, p.status);
+            if (lane == 0) p.counters[(size_t)mb * Hkv + mh] = 0;
         }
     }
     __syncthreads();
 }
 
 // Host-side handle of one instantiation.
-template <typename T, int D, int BS, bool MMA>
+template <typename T, int D, int BS, bool MMA, int GF>
 struct VariantOf {
-    static int smem_bytes(int num_seqs, bool fixed) { return Layout<T, D, BS>::bytes(num_seqs, fixed); }
+    static int smem_bytes(int num_seqs, bool fixed) { return Layout<T, D, BS, MMA>::bytes(num_seqs, fixed); }
+    // Launched as a programmatic dependent of the preceding kernel on the stream:
+    // the grid may start while that kernel finishes if it allowed it.
     static void launch(const DecodeParams& p, const CUtensorMap& tk, const CUtensorMap& tv, int grid, int smem,
                        cudaStream_t stream) {
-        decode_kernel<T, D, BS, MMA><<<grid, kThreads, smem, stream>>>(p, tk, tv);
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(grid);
+        cfg.blockDim = dim3(kThreads);
+        cfg.dynamicSmemBytes = smem;
+        cfg.stream = stream;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        cudaLaunchKernelEx(&cfg, decode_kernel<T, D, BS, MMA, GF>, p, tk, tv);
     }
     static DecodeVariant get() {
-        return DecodeVariant{reinterpret_cast<const void*>(&decode_kernel<T, D, BS, MMA>), Layout<T, D, BS>::S,
+        return DecodeVariant{reinterpret_cast<const void*>(&decode_kernel<T, D, BS, MMA, GF>), Layout<T, D, BS, MMA>::S,
                              kThreads, &smem_bytes, &launch};
     }
 };

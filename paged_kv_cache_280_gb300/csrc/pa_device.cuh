@@ -93,11 +93,22 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_
         : "memory");
 }
 
+// Order this thread's earlier (generic-proxy) view of global memory before its
+// later bulk copies (async proxy) read it.
+__device__ __forceinline__ void fence_proxy_async_global() { asm volatile("fence.proxy.async.global;" ::: "memory"); }
+
 __device__ __forceinline__ uint64_t policy_evict_first() {
     uint64_t p;
     asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
     return p;
 }
+
+// ---- programmatic dependent launch -----------------------------------------
+// Let the next kernel on the stream (if launched as a dependent) start now.
+__device__ __forceinline__ void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+// Wait until the preceding kernel on the stream has finished and its writes are visible
+// (returns at once when this kernel was not launched as a dependent).
+__device__ __forceinline__ void pdl_wait_prerequisites() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 
 // ---- named barrier over a subset of warps ---------------------------------
 __device__ __forceinline__ void named_barrier(uint32_t id, uint32_t threads) {

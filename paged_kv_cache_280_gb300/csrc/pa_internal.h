@@ -9,7 +9,15 @@
 
 namespace pa {
 
-constexpr int kMaxCtasPerSm = 4;  // bound used to size the decode workspace
+constexpr int kMaxCtasPerSm = 8;  // bound used to size the decode workspace
+// Decode workspace: one merge counter per (sequence, KV head); per partial
+// slot [G][D] floats of o plus [G][2] floats of (m, l).
+constexpr int kCountersPerSegment = 1;
+constexpr int kSlotExtraFloatsPerHead = 2;
+// floats of one partial slot, a multiple of 4 so that slots can be bulk-copied
+inline __host__ __device__ size_t partial_slot_floats(int G, int D) {
+    return ((size_t)G * (D + kSlotExtraFloatsPerHead) + 3) & ~(size_t)3;
+}
 constexpr int kMaxSmem = 227 * 1024;
 
 struct DecodeParams {
@@ -42,7 +50,11 @@ struct DecodeVariant {
                    cudaStream_t stream);
 };
 
-bool decode_variant_f32(int head_dim, int block_size, DecodeVariant* out);
-bool decode_variant_bf16(int head_dim, int block_size, bool mma, DecodeVariant* out);
+// Compiled variants.  `group` is Hq / Hkv; the CUDA-core path has exact
+// instantiations for some group sizes and a run-time-group fallback.
+bool decode_variant_f32(int head_dim, int block_size, int group, DecodeVariant* out);
+bool decode_variant_f32_pow2(int head_dim, int block_size, int group, DecodeVariant* out);
+bool decode_variant_bf16_mma(int head_dim, int block_size, DecodeVariant* out);
+bool decode_variant_bf16_fma(int head_dim, int block_size, int group, DecodeVariant* out);
 
 }  // namespace pa

@@ -61,7 +61,7 @@ extern "C" pa_status pa_decode_attention_static(void* out, const void* q, const 
     if (s != PA_OK) return s;
     // The buffer keeps the previous call's contents.  The status word and the
     // per-(sequence, KV head) merge counters at its head must start at zero.
-    const size_t head = 256 + round256((size_t)num_seqs * num_kv_heads * sizeof(int32_t));
+    const size_t head = 256 + round256((size_t)num_seqs * num_kv_heads * pa::kCountersPerSegment * sizeof(int32_t));
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     if (cudaMemsetAsync(ws, 0, head, st) != cudaSuccess) return PA_ERR_CUDA;
     s = pa_decode_attention(out, q, k_pool, v_pool, block_tables, max_blocks_per_seq, seq_lens, max_seq_len,
