@@ -194,8 +194,8 @@ pa_status pa_decode_launch_info(int32_t num_seqs, int32_t num_q_heads, int32_t n
                                 int32_t* stages, int32_t* smem_bytes, int32_t* uses_mma);
 
 /*
- * Tuning: CTAs per SM of the decode grid (1..8; 0 restores the default: as
- * many as fit, at most 8).  Process-wide; affects later pa_decode_attention
+ * Tuning: CTAs per SM of the decode grid (1..8; 0 restores the default: 4 on
+ * the tensor-core path, otherwise as many as fit, at most 8).  Process-wide; affects later pa_decode_attention
  * calls.  More CTAs per SM keep more tiles in flight but add split points
  * (partials) at CTA edges.
  */

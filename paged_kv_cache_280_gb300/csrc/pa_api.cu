@@ -12,7 +12,7 @@ namespace pa {
 namespace {
 
 constexpr int kMaxDevices = 64;
-std::atomic<int> g_ctas_per_sm{0};  // 0 = as many as fit (at most kMaxCtasPerSm)
+std::atomic<int> g_ctas_per_sm{0};  // 0 = the per-path default
 
 struct DeviceInfo {
     int sms = 0;
@@ -118,8 +118,11 @@ pa_status plan_launch(int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_head
     if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, lp->v.kernel, lp->v.threads, lp->smem) != cudaSuccess)
         return PA_ERR_CUDA;
     if (occ <= 0) return PA_ERR_UNSUPPORTED;
+    // Default: the tensor-core path, which spends little time per tile, keeps
+    // four CTAs per SM (about 128 KB of tiles in flight, enough to cover HBM
+    // latency with fewer split points); the CUDA-core path takes as many as fit.
     int want = g_ctas_per_sm.load();
-    if (want <= 0) want = kMaxCtasPerSm;
+    if (want <= 0) want = lp->mma ? kDefaultCtasPerSmMma : kMaxCtasPerSm;
     const int per_sm = occ < want ? occ : want;
     int64_t grid = (int64_t)lp->sms * per_sm;
     const int64_t tiles_bound = (int64_t)num_seqs * num_kv_heads * max_tiles_per_head;

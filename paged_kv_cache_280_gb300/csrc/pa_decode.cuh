@@ -90,7 +90,7 @@ struct Layout {
     static constexpr int kPTileBytes = MMA ? 0 : 16 * kMaxGroup * 4;
     // per-piece weights and per-head running max / sum when merging a split segment
     static constexpr int kMergeOff = kPTileOff + kPTileBytes;
-    static constexpr int kMergeBytes = (kMaxMergeChunk * kMaxGroup + 3 * kMaxGroup) * 4;
+    static constexpr int kMergeBytes = (kMaxMergeChunk * kMaxGroup + 4 * kMaxGroup) * 4;
     static constexpr int kBarOff = kMergeOff + kMergeBytes;
     static constexpr int kMiscOff = kBarOff + (2 * S + 2 * kQSlots + 1) * 8;
     static constexpr int kPrefixOff = kMiscOff + 64;
@@ -529,29 +529,30 @@ struct FmaState {
 //   M = max_p m_p,   out = sum_p e^(m_p-M) o_p / sum_p e^(m_p-M) l_p.
 // The pieces' partial slots are bulk-copied into the idle stage ring a chunk
 // at a time (one round trip per chunk); each head's running max and sum are
-// folded per chunk and the output elements (lane + 32 j) accumulated from
-// shared memory.
+// folded per chunk, then every output element is summed over the chunk's
+// slots straight from shared memory (one register per element, so nothing
+// spills whatever the group size).  When the pieces take more than one chunk
+// the running sums sit at the end of the ring, after the staged slots.
 template <typename T, int D>
-__device__ __forceinline__ void merge_staged(const float* partials, size_t slot_floats, T* orow, int ca, int cb,
+__device__ __forceinline__ bool merge_staged(const float* partials, size_t slot_floats, T* orow, int ca, int cb,
                                              bool ca_split, int G, int lane, const uint8_t* ring, uint32_t ring_s,
-                                             int ring_bytes, float* work, uint32_t mbar, uint32_t& mphase,
-                                             volatile int32_t* abort_flag, int32_t* status) {
-    constexpr int JN = kMaxGroup * D / 32;
+                                             int ring_bytes, float* work, uint32_t mbar, uint32_t& mphase) {
     const uint32_t slot_bytes = (uint32_t)(slot_floats * 4);
-    int per_chunk = ring_bytes / (int)slot_bytes;
-    per_chunk = per_chunk > kMaxMergeChunk ? kMaxMergeChunk : per_chunk;
-    float* wgt = work;                                 // [kMaxMergeChunk][kMaxGroup]
-    float* hst = work + kMaxMergeChunk * kMaxGroup;    // [0..7] max, [8..15] sum, [16..23] rescale
-    const float* buf = reinterpret_cast<const float*>(ring);
     const int np = cb - ca + 1, nel = G * D;
+    const int acc_bytes = (nel * 4 + 15) & ~15;
+    int per_chunk = min(ring_bytes / (int)slot_bytes, kMaxMergeChunk);
+    const bool multi = np > per_chunk;
+    if (multi) per_chunk = min((ring_bytes - acc_bytes) / (int)slot_bytes, kMaxMergeChunk);
+    if (per_chunk < 1) return false;  // cannot happen for the instantiated shapes
+    float* wgt = work;                               // [kMaxMergeChunk][kMaxGroup]
+    float* hst = work + kMaxMergeChunk * kMaxGroup;  // [0..7] max, [8..15] sum, [16..23] rescale, [24..31] 1/sum
+    const float* buf = reinterpret_cast<const float*>(ring);
+    float* acc_s = reinterpret_cast<float*>(const_cast<uint8_t*>(ring) + ring_bytes - acc_bytes);
     auto slot_of = [&](int cc) { return partials + (size_t)(2 * cc + (cc == ca && ca_split ? 1 : 0)) * slot_floats; };
     if (lane < G) {
         hst[lane] = -INFINITY;
         hst[8 + lane] = 0.f;
     }
-    float acc[JN];
-#pragma unroll
-    for (int j = 0; j < JN; ++j) acc[j] = 0.f;
     for (int c0 = 0; c0 < np; c0 += per_chunk) {
         const int nc = min(per_chunk, np - c0);
         __syncwarp();
@@ -567,11 +568,7 @@ __device__ __forceinline__ void merge_staged(const float* partials, size_t slot_
         bool ok = mbar_wait(mbar, mphase & 1);
         ok = __all_sync(0xffffffffu, ok);
         ++mphase;
-        if (!ok) {
-            *abort_flag = 1;
-            if (lane == 0) flag_status(status, PA_DEV_WAIT_TIMEOUT);
-            return;
-        }
+        if (!ok) return false;
         if (lane < G) {
             const int hd = lane;
             float Mc = hst[hd];
@@ -586,26 +583,38 @@ __device__ __forceinline__ void merge_staged(const float* partials, size_t slot_
             hst[hd] = Mc;
             hst[8 + hd] = Lr;
             hst[16 + hd] = resc;
+            hst[24 + hd] = 1.f / Lr;
         }
         __syncwarp();
+        const bool final_chunk = c0 + nc >= np;
+        // four independent sums per lane (elements e0 + 32u)
+        for (int e0 = lane; e0 < nel; e0 += 128) {
+            float a[4] = {0.f, 0.f, 0.f, 0.f};
+            int hd[4];
 #pragma unroll
-        for (int j = 0; j < JN; ++j) {
-            const int e = lane + 32 * j;
-            if (e < nel) {
-                const int hd = e / D;
-                float a = acc[j] * hst[16 + hd];
-                for (int i = 0; i < nc; ++i) a = fmaf(wgt[i * kMaxGroup + hd], buf[i * slot_floats + e], a);
-                acc[j] = a;
+            for (int u = 0; u < 4; ++u) hd[u] = min((e0 + 32 * u) / D, G - 1);
+            for (int i = 0; i < nc; ++i) {
+                const float* bi = buf + i * slot_floats + e0;
+#pragma unroll
+                for (int u = 0; u < 4; ++u)
+                    if (e0 + 32 * u < nel) a[u] = fmaf(wgt[i * kMaxGroup + hd[u]], bi[32 * u], a[u]);
+            }
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int e = e0 + 32 * u;
+                if (e < nel) {
+                    float v = a[u];
+                    if (c0 > 0) v = fmaf(acc_s[e], hst[16 + hd[u]], v);
+                    if (final_chunk)
+                        orow[e] = from_float<T>(v * hst[24 + hd[u]]);
+                    else
+                        acc_s[e] = v;
+                }
             }
         }
     }
     __syncwarp();
-#pragma unroll
-    for (int j = 0; j < JN; ++j) {
-        const int e = lane + 32 * j;
-        if (e < nel) orow[e] = from_float<T>(acc[j] / hst[8 + e / D]);
-    }
-    __syncwarp();
+    return true;
 }
 
 // ---------------------------------------------------------------------------
@@ -826,9 +835,8 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const DecodeParams p, 
         it.init(P, t0, t1);
         int b, h, j0, j1;
         bool at_t0;
-        // merges left for after the loop (a CTA completes at most its two boundary segments)
-        int npend = 0, mb0 = 0, mh0 = 0, mca0 = 0, mcb0 = 0, mb1 = 0, mh1 = 0, mca1 = 0, mcb1 = 0;
-        bool msp0 = false, msp1 = false;
+        // split pieces of this CTA, counted after the loop (at most two: its range's ends)
+        int npend = 0, mb0 = 0, mh0 = 0, mb1 = 0, mh1 = 0;
         while (it.next(P, b, h, j0, j1, at_t0)) {
             const int qs = pi % kQSlots;
             const uint8_t* qslot = base + L::kQOff + qs * L::kQSlotBytes;
@@ -871,43 +879,55 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const DecodeParams p, 
             if (j0 == 0 && j1 == nb) {
                 st.store_out(orow, G, lane);
             } else {
-                // Split segment: store the partial; the CTA that completes the last
-                // piece of (b, h) (an atomic counter per segment) merges them.
+                // Split segment: store the partial now; its completion is counted
+                // after the loop, so the fence and the atomic round trip stall
+                // this warp once, not once per split piece.  A CTA holds at most
+                // two split pieces (the first and the last of its range).
                 float* slot = p.partials + (size_t)(2 * c + (at_t0 ? 0 : 1)) * slot_floats;
                 st.store_partial(slot, G, lane);
-                __threadfence();
-                __syncwarp();
-                const int64_t s0 = P.seg_start(b, h);
-                const int ca = P.cta_of(s0), cb = P.cta_of(s0 + nb - 1);
-                int32_t* cnt = p.counters + (size_t)b * Hkv + h;
-                int last = 0;
-                if (lane == 0) {
-                    last = atomicAdd(cnt, 1) == cb - ca;
-                    if (last) __threadfence();
+                if (npend == 0) {
+                    mb0 = b, mh0 = h;
+                } else {
+                    mb1 = b, mh1 = h;
                 }
-                last = __shfl_sync(0xffffffffu, last, 0);
-                if (last) {  // merged once this CTA's own pieces are done
-                    const bool sp = s0 != P.cta_start(ca);
-                    if (npend == 0) {
-                        mb0 = b, mh0 = h, mca0 = ca, mcb0 = cb, msp0 = sp;
-                    } else {
-                        mb1 = b, mh1 = h, mca1 = ca, mcb1 = cb, msp1 = sp;
-                    }
-                    ++npend;
-                }
+                ++npend;
             }
             ++pi;
+        }
+        // Count this CTA's split pieces; the CTA that completes the last piece of
+        // segment (b, h) (an atomic counter per segment) merges its partials.
+        int lastmask = 0;
+        if (npend > 0) {
+            __threadfence();
+            __syncwarp();
+            if (lane == 0) {
+                for (int i = 0; i < npend; ++i) {
+                    const int mb = i ? mb1 : mb0, mh = i ? mh1 : mh0;
+                    const int64_t s0 = P.seg_start(mb, mh);
+                    const int span = P.cta_of(s0 + P.nblocks(mb) - 1) - P.cta_of(s0);
+                    if (atomicAdd(p.counters + (size_t)mb * Hkv + mh, 1) == span) lastmask |= 1 << i;
+                }
+                if (lastmask) __threadfence();
+            }
+            lastmask = __shfl_sync(0xffffffffu, lastmask, 0);
         }
         // The stage ring is idle now (every issued tile has been consumed): use it
         // to stage the partials of the split segments this CTA completed.
         uint32_t mphase = 0;
 #pragma unroll 1
         for (int i = 0; i < npend; ++i) {
+            if (!(lastmask & (1 << i))) continue;
             const int mb = i ? mb1 : mb0, mh = i ? mh1 : mh0;
+            const int64_t s0 = P.seg_start(mb, mh);
+            const int ca = P.cta_of(s0), cb = P.cta_of(s0 + P.nblocks(mb) - 1);
             T* orow = static_cast<T*>(p.out) + ((size_t)mb * Hq + (size_t)mh * G) * D;
-            merge_staged<T, D>(p.partials, slot_floats, orow, i ? mca1 : mca0, i ? mcb1 : mcb0, i ? msp1 : msp0, G, lane,
-                               base, base_s, S * L::kStageBytes, reinterpret_cast<float*>(base + L::kMergeOff),
-                               merge_bar, mphase, misc, p.status);
+            if (!merge_staged<T, D>(p.partials, slot_floats, orow, ca, cb, s0 != P.cta_start(ca), G, lane, base,
+                                    base_s, S * L::kStageBytes, reinterpret_cast<float*>(base + L::kMergeOff),
+                                    merge_bar, mphase)) {
+                misc[0] = 1;
+                if (lane == 0) flag_status(p.status, PA_DEV_WAIT_TIMEOUT);
+                break;
+            }
             if (lane == 0) p.counters[(size_t)mb * Hkv + mh] = 0;
         }
     }

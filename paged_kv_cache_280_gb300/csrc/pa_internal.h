@@ -9,7 +9,8 @@
 
 namespace pa {
 
-constexpr int kMaxCtasPerSm = 8;  // bound used to size the decode workspace
+constexpr int kMaxCtasPerSm = 8;
+constexpr int kDefaultCtasPerSmMma = 4;  // default CTAs per SM on the tensor-core path  // bound used to size the decode workspace
 // Decode workspace: one merge counter per (sequence, KV head); per partial
 // slot [G][D] floats of o plus [G][2] floats of (m, l).
 constexpr int kCountersPerSegment = 1;
