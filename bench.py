@@ -191,7 +191,7 @@ def decode_bytes(lens, w) -> int:
 def kernel_source_hash() -> str:
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "paged_kv_cache_280_gb300", "csrc")
-    for f in sorted(os.listdir(csrc)):
+    for f in sorted(x for x in os.listdir(csrc) if x.endswith((".cu", ".cuh", ".h", ".cpp"))):
         with open(os.path.join(csrc, f), "rb") as fh:
             h.update(f.encode() + fh.read())
     return h.hexdigest()[:16]
