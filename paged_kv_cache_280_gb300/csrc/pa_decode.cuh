@@ -724,7 +724,15 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const DecodeParams p, 
     // working CTA owns a non-empty range and a split segment's pieces come from
     // consecutive CTAs -- which the merge count and slot rule rely on.
     const int64_t units = fixed ? P.U : P.T;
-    P.C = units < (int64_t)C ? (int32_t)units : C;
+    int64_t ce = units < (int64_t)C ? units : C;
+    if (fixed && ce > 0) {
+        // Partitions are coarse: give every working CTA the same number of them
+        // (the fewest CTAs with the same largest share), so none is left with
+        // one partition more than the rest at the end of the kernel.
+        const int64_t per = (units + ce - 1) / ce;
+        ce = (units + per - 1) / per;
+    }
+    P.C = (int32_t)ce;
     const bool works = P.T > 0 && c < P.C;
     const int64_t t0 = works ? P.cta_start(c) : 0;
     const int64_t t1 = works ? P.cta_start(c + 1) : 0;
