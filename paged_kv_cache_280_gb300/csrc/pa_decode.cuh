@@ -63,31 +63,40 @@ struct ElemBytes<__nv_bfloat16> {
     static constexpr int value = 2;
 };
 
-// Pipeline depth: about PA_STAGE_BYTES (32 KB) of tiles in flight per CTA,
-// 2 to 16 stages.  Several CTAs share an SM.
+// Pipeline depth: about PA_STAGE_BYTES (32 KB) of tiles in flight per CTA on
+// the tensor-core path and PA_STAGE_BYTES_FMA (16 KB) on the CUDA-core path,
+// 2 to 16 stages.  Several CTAs share an SM: the CUDA-core path spends more
+// issue slots per tile, so it keeps a shallower ring and runs twice as many
+// CTAs (consumer warps) per SM for about the same bytes in flight.
 #ifndef PA_STAGE_BYTES
 #define PA_STAGE_BYTES 32768
 #endif
-constexpr int stages_for(int bs, int d, int e) {
-    int n = PA_STAGE_BYTES / (2 * bs * d * e);
+#ifndef PA_STAGE_BYTES_FMA
+#define PA_STAGE_BYTES_FMA 16384
+#endif
+constexpr int stages_for(int ring_bytes, int bs, int d, int e) {
+    int n = ring_bytes / (2 * bs * d * e);
     return n < 2 ? 2 : (n > 16 ? 16 : n);
 }
 
-template <typename T, int D, int BS, bool MMA>
+// Shared-memory layout of one CTA.  Query-row buffers are sized for the
+// group size of the instantiation (GF > 0) or for the largest group.
+template <typename T, int D, int BS, bool MMA, int GF>
 struct Layout {
     static constexpr int E = ElemBytes<T>::value;
-    static constexpr int S = stages_for(BS, D, E);
+    static constexpr int S = stages_for(MMA ? PA_STAGE_BYTES : PA_STAGE_BYTES_FMA, BS, D, E);
+    static constexpr int GN = GF > 0 ? GF : kMaxGroup;  // query rows a q slot holds
     static constexpr int kTileBytes = BS * D * E;  // K (or V) of one tile
     static constexpr int kPanels = D * E / 128;    // 128-byte column panels per row
     static constexpr int kStageBytes = 2 * kTileBytes;
-    static constexpr int kQSlotBytes = kMaxGroup * D * E;
+    static constexpr int kQSlotBytes = GN * D * E;
     static constexpr int kStagesOff = 0;
     static constexpr int kQOff = kStagesOff + S * kStageBytes;
     // CUDA-core path only: fp32 query rows (pre-scaled) and one step's weights.
     static constexpr int kQfOff = kQOff + kQSlots * kQSlotBytes;
-    static constexpr int kQfBytes = MMA ? 0 : kMaxGroup * D * 4;
+    static constexpr int kQfBytes = MMA ? 0 : GN * D * 4;
     static constexpr int kPTileOff = kQfOff + kQfBytes;
-    static constexpr int kPTileBytes = MMA ? 0 : 16 * kMaxGroup * 4;
+    static constexpr int kPTileBytes = MMA ? 0 : 16 * GN * 4;
     // per-piece weights and per-head running max / sum when merging a split segment
     static constexpr int kMergeOff = kPTileOff + kPTileBytes;
     static constexpr int kMergeBytes = (kMaxMergeChunk * kMaxGroup + 4 * kMaxGroup) * 4;
@@ -428,7 +437,7 @@ struct FmaState {
         }
     }
 
-    // qf: [G][D] fp32 query rows pre-multiplied by scale*log2(e); ptile: [16][8] weights of one step.
+    // qf: [G][D] fp32 query rows pre-multiplied by scale*log2(e); ptile: [16][GN] weights of one step.
     __device__ __forceinline__ void step(uint32_t kbase, uint32_t vbase, int row0, int valid, int G,
                                          const float* qf, float* ptile, int lane) {
         const int t = lane & 15, half = lane >> 4;
@@ -476,7 +485,7 @@ struct FmaState {
                 for (int off = 1; off < 16; off <<= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
                 l[g] = l[g] * alpha[g] + sum;
                 m[g] = mn;
-                if (half == 0) ptile[t * kMaxGroup + g] = pw;
+                if (half == 0) ptile[t * GN + g] = pw;
             }
         }
         __syncwarp();
@@ -487,9 +496,9 @@ struct FmaState {
         const int byte0 = lane * VEC * E;
         if (valid == 16) {
 #pragma unroll
-            for (int tt = 0; tt < 16; ++tt) pv_token(vbase, row0 + tt, byte0, ptile + tt * kMaxGroup, G);
+            for (int tt = 0; tt < 16; ++tt) pv_token(vbase, row0 + tt, byte0, ptile + tt * GN, G);
         } else {
-            for (int tt = 0; tt < valid; ++tt) pv_token(vbase, row0 + tt, byte0, ptile + tt * kMaxGroup, G);
+            for (int tt = 0; tt < valid; ++tt) pv_token(vbase, row0 + tt, byte0, ptile + tt * GN, G);
         }
         __syncwarp();
     }
@@ -623,7 +632,7 @@ __device__ __forceinline__ bool merge_staged(const float* partials, size_t slot_
 template <typename T, int D, int BS, bool MMA, int GF>
 __global__ void __launch_bounds__(kThreads) decode_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tmap_k,
                                                           const __grid_constant__ CUtensorMap tmap_v) {
-    using L = Layout<T, D, BS, MMA>;
+    using L = Layout<T, D, BS, MMA, GF>;
     constexpr int S = L::S;
     constexpr int E = L::E;
     extern __shared__ uint8_t smem_raw[];
@@ -945,7 +954,7 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const DecodeParams p, 
 // Host-side handle of one instantiation.
 template <typename T, int D, int BS, bool MMA, int GF>
 struct VariantOf {
-    static int smem_bytes(int num_seqs, bool fixed) { return Layout<T, D, BS, MMA>::bytes(num_seqs, fixed); }
+    static int smem_bytes(int num_seqs, bool fixed) { return Layout<T, D, BS, MMA, GF>::bytes(num_seqs, fixed); }
     // Launched as a programmatic dependent of the preceding kernel on the stream:
     // the grid may start while that kernel finishes if it allowed it.
     static void launch(const DecodeParams& p, const CUtensorMap& tk, const CUtensorMap& tv, int grid, int smem,
@@ -963,7 +972,7 @@ struct VariantOf {
         cudaLaunchKernelEx(&cfg, decode_kernel<T, D, BS, MMA, GF>, p, tk, tv);
     }
     static DecodeVariant get() {
-        return DecodeVariant{reinterpret_cast<const void*>(&decode_kernel<T, D, BS, MMA, GF>), Layout<T, D, BS, MMA>::S,
+        return DecodeVariant{reinterpret_cast<const void*>(&decode_kernel<T, D, BS, MMA, GF>), Layout<T, D, BS, MMA, GF>::S,
                              kThreads, &smem_bytes, &launch};
     }
 };
