@@ -164,19 +164,68 @@ class ClockSampler:
 # ---------------------------------------------------------------------------
 # workload
 # ---------------------------------------------------------------------------
+WORKLOADS = {
+    "gqa4_b64": "bf16 decode batch of 64 skew-mixed lengths, 32 query / 8 KV heads, d 128, 16-token blocks",
+    "mha_b256_append": "bf16 decode batch of 256 skew-mixed lengths, MHA 32 heads, d 128, one appended token per step",
+    "cow_sampling": "16 prompts of 1031 tokens forked into 8 samples each (refcount-shared blocks), tails U[0,256], "
+                    "32 query / 8 KV heads, d 128",
+    "long_context_bs16": "4 x 131072-token contexts, 64 query / 8 KV heads, d 128, 16-token blocks, 2048-token partitions",
+    "long_context_bs32": "4 x 131072-token contexts, 64 query / 8 KV heads, d 128, 32-token blocks, 2048-token partitions",
+}
+
+
 def build_workload(name: str, rank: int, world: int, extra_steps: int):
+    """The workload of this rank, with pool room for ``extra_steps`` more tokens per sequence."""
     import synth
     import synth.workloads as W
 
-    if name != "gqa4_b64":
-        raise SystemExit(f"unknown workload {name}")
-    base = W.gqa4_b64()
-    per_rank = base.num_seqs
-    glob = synth.lengths_mix(synth.stream_seed(base.seed, W.TAG_LENGTHS), per_rank * world)
-    lengths = shard_lengths(glob, rank, world, per_rank)
-    demand = int(sum(-(-(int(x) + extra_steps) // base.block_size) for x in lengths))
-    seed = base.seed + 7919 * rank
-    return W.scaled(base, lengths=lengths, num_blocks=int(math.ceil(1.1 * demand)), seed=seed)
+    if name not in WORKLOADS:
+        raise SystemExit(f"unknown workload {name}; one of {sorted(WORKLOADS)}")
+    seed_shift = 7919 * rank
+    if name == "gqa4_b64":
+        # every rank owns its own slice of one global length draw
+        base = W.gqa4_b64()
+        per_rank = base.num_seqs
+        glob = synth.lengths_mix(synth.stream_seed(base.seed, W.TAG_LENGTHS), per_rank * world)
+        lengths = shard_lengths(glob, rank, world, per_rank)
+        demand = int(sum(-(-(int(x) + extra_steps) // base.block_size) for x in lengths))
+        return W.scaled(base, lengths=lengths, num_blocks=int(math.ceil(1.1 * demand)), seed=base.seed + seed_shift)
+    if name == "cow_sampling":
+        base = W.cow_sampling()
+        room = base.prompts * base.samples * (-(-extra_steps // base.block_size) + 1)
+        return W.scaled(base, num_blocks=int(math.ceil(base.num_blocks + 1.1 * room)), seed=base.seed + seed_shift)
+    base = W.mha_b256_append() if name == "mha_b256_append" else W.long_context(block_size=int(name[-2:]))
+    demand = int(sum(-(-(int(x) + extra_steps) // base.block_size) for x in base.lengths))
+    return W.scaled(base, num_blocks=int(math.ceil(1.1 * demand)), seed=base.seed + seed_shift)
+
+
+def populate(alloc, w):
+    """Build the workload's cache state through an allocator (ours or the oracle's model).
+
+    Returns the ids of the decode batch's sequences, in batch order.  Parallel
+    sampling forks every prompt into its samples, frees the prompt (its blocks
+    stay shared by the samples), then appends the divergent tails one decode
+    step at a time, which copies each shared partial prompt block on its first
+    write.
+    """
+    if w.prompts:
+        P, S, L = w.prompts, w.samples, w.prompt_len
+        for p in range(P):
+            alloc.create(p)
+            alloc.append(p, L)
+        sid = lambda p, s: P + p * S + s  # noqa: E731
+        for p in range(P):
+            for s in range(S):
+                alloc.fork(p, sid(p, s))
+            alloc.free_seq(p)
+        tails = w.tails()
+        for t in range(int(tails.max())):
+            alloc.append_batch([sid(p, s) for p in range(P) for s in range(S) if tails[p * S + s] > t])
+        return [sid(p, s) for p in range(P) for s in range(S)]
+    for s, n in enumerate(w.lengths):
+        alloc.create(s)
+        alloc.append(s, int(n))
+    return list(range(len(w.lengths)))
 
 
 def decode_bytes(lens, w) -> int:
@@ -258,13 +307,11 @@ def run_ours(args, rank, world, local_rank):
     K, Wm = args.steps, args.warmup
     K_e2e = min(K, args.e2e_steps)
     w = build_workload(args.workload, rank, world, extra_steps=1 + K_e2e + 2)
-    B, Hq, Hkv, D, bs = w.num_seqs, w.num_q_heads, w.num_kv_heads, w.head_dim, w.block_size
+    Hq, Hkv, D, bs, PT = w.num_q_heads, w.num_kv_heads, w.head_dim, w.block_size, w.partition_tokens
     lib = pa.Allocator(w.num_blocks, bs, free_order=w.free_order())
-    for s, n in enumerate(w.lengths):
-        lib.create(s)
-        lib.append(s, int(n))
-    max_blocks = int(-(-(int(w.lengths.max()) + 2 + K_e2e) // bs))
-    ids = list(range(B))
+    ids = populate(lib, w)
+    B = len(ids)
+    max_blocks = int(-(-(max(lib.length(s) for s in ids) + 2 + K_e2e) // bs))
 
     def to_dev(a):
         if a.dtype == np.uint16:
@@ -304,7 +351,8 @@ def run_ours(args, rank, world, local_rank):
         pa.pa_reshape_and_cache(d_kn, d_vn, dk, dv, d_slots, status=ws[:4].view(torch.int32), stream=stream)
 
     def decode():
-        pa.pa_decode_attention(out, d_q, dk, dv, d_tables, d_lens, max_len, w.scale, ws, stream=stream)
+        pa.pa_decode_attention(out, d_q, dk, dv, d_tables, d_lens, max_len, w.scale, ws, partition_tokens=PT,
+                               stream=stream)
 
     for _ in range(Wm):
         flush_l2()
@@ -339,6 +387,10 @@ def run_ours(args, rank, world, local_rank):
     all_tokens = reduce_sum(float(tokens_step * K), dist, dev)
     value = all_tokens / total_s
     dbytes = decode_bytes(lens, w)
+    # KV bytes of the distinct physical blocks the step reads (below the per-sequence
+    # bytes when sequences share prefix blocks, which L2 then serves more than once)
+    used = [tables[i, : -(-int(n) // bs)] for i, n in enumerate(lens)]
+    unique_kv = int(np.unique(np.concatenate(used)).size) * bs * Hkv * D * 2 * w.elem_bytes if B else 0
     dec_mean_s = statistics.mean(dec_ms) / 1e3
     peak, peak_kind = measured_peaks()
     achieved = dbytes / dec_mean_s / 1e9
@@ -388,7 +440,8 @@ def run_ours(args, rank, world, local_rank):
             nbytes += len(pr) * 8
             pa.pa_copy_blocks(dk, dv, e_pairs[: len(pr)], stream=stream)
         pa.pa_reshape_and_cache(e_kn, e_vn, dk, dv, e_slots, stream=stream)
-        pa.pa_decode_attention(out, e_q, dk, dv, e_tables, e_lens, int(ln.max()), w.scale, ws, stream=stream)
+        pa.pa_decode_attention(out, e_q, dk, dv, e_tables, e_lens, int(ln.max()), w.scale, ws, partition_tokens=PT,
+                               stream=stream)
         h_out.copy_(out.view(torch.int16), non_blocking=True)
         stream.synchronize()
         e2e_s += time.perf_counter() - t0
@@ -402,15 +455,15 @@ def run_ours(args, rank, world, local_rank):
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K, "warmup": Wm,
         "ms_per_step": total_s * 1e3 / K, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": "bf16", "data": "synthetic (seeded; the pages' length mix, scattered 16-token blocks)",
+        "dtype": "bf16", "data": f"synthetic, seeded: {WORKLOADS[args.workload]}; blocks scattered by a seeded free-list order",
         "config": {
             "workload": w.name if world == 1 else f"{w.name} per rank", "num_seqs_per_gpu": B, "num_q_heads": Hq,
             "num_kv_heads": Hkv, "head_dim": D, "block_size": bs, "kv_tokens_per_step": tokens_step,
-            "decode_bytes_per_step": dbytes, "pool_blocks": w.num_blocks,
+            "decode_bytes_per_step": dbytes, "unique_block_kv_bytes_per_step": unique_kv, "pool_blocks": w.num_blocks,
             "l2": f"flushed between timed steps ({L2_FLUSH_BYTES >> 20} MiB write, then a {L2_FLUSH_BYTES >> 21} MiB read "
                   "so that no dirty line is left; untimed)",
             "host_alloc_us_per_step": round(host_alloc_us, 1), "decode_ctas": ctas, "stages": stages,
-            "smem_bytes": smem, "path": "mma.sync" if mma else "fma",
+            "smem_bytes": smem, "path": "mma.sync" if mma else "fma", "partition_tokens": PT,
             "decode_ms_median": statistics.median(dec_ms), "decode_ms_min": min(dec_ms),
             "step_gbs": (dbytes + 4 * B * Hkv * D * 2) / (total_s / K) / 1e9,
         },
@@ -442,18 +495,16 @@ def run_reference(args, rank, world):
     from oracle.alloc_model import RefAllocator
 
     w = build_workload(args.workload, 0, 1, extra_steps=2)
-    B = w.num_seqs
     ref = RefAllocator(w.num_blocks, w.block_size, free_order=w.free_order().tolist())
-    for s, n in enumerate(w.lengths):
-        ref.create(s)
-        ref.append(s, int(n))
-    ref.append_batch(list(range(B)))
-    max_blocks = int(-(-(int(w.lengths.max()) + 2) // w.block_size))
+    ids = populate(ref, w)
+    B = len(ids)
+    ref.append_batch(ids)
+    lens = np.array([ref.length(s) for s in ids], np.int32)
+    max_blocks = int(-(-int(lens.max()) // w.block_size))
     tables = np.zeros((B, max_blocks), np.int32)
-    for s in range(B):
+    for i, s in enumerate(ids):
         t = ref.table(s)
-        tables[s, : len(t)] = t
-    lens = np.array([ref.length(s) for s in range(B)], np.int32)
+        tables[i, : len(t)] = t
     k_pool, v_pool, q = w.pool_values("k"), w.pool_values("v"), w.queries(step=1)
     threads = os.cpu_count() or 1
     per_step = max(1, min(B, args.ref_seqs_per_step))
@@ -471,7 +522,7 @@ def run_reference(args, rank, world):
         "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * sum(times) / len(times),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-        "data": "synthetic (seeded; the pages' length mix, scattered 16-token blocks)",
+        "data": f"synthetic, seeded: {WORKLOADS[args.workload]}; blocks scattered by a seeded free-list order",
         "config": {"workload": w.name, "num_seqs_per_gpu": B, "num_q_heads": w.num_q_heads,
                    "num_kv_heads": w.num_kv_heads, "head_dim": w.head_dim, "block_size": w.block_size},
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle",
@@ -488,7 +539,7 @@ def main(argv=None):
     ap.add_argument("--steps", type=int, default=300)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", default="gqa4_b64")
+    ap.add_argument("--workload", default="gqa4_b64", choices=sorted(WORKLOADS))
     ap.add_argument("--e2e-steps", type=int, default=32)
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
