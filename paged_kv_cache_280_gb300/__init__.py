@@ -210,6 +210,21 @@ def _np():
     return np
 
 
+def _int64_array(seq_ids):
+    np = _np()
+    if isinstance(seq_ids, np.ndarray) and seq_ids.dtype == np.int64 and seq_ids.flags["C_CONTIGUOUS"]:
+        return seq_ids
+    return np.ascontiguousarray(np.asarray(seq_ids, dtype=np.int64))
+
+
+def _checked_out(a, dtype, n: int, cols: int):
+    """A caller-provided output array: C-contiguous, of dtype, with room for n rows of ``cols``."""
+    np = _np()
+    if not isinstance(a, np.ndarray) or a.dtype != dtype or not a.flags["C_CONTIGUOUS"] or a.size < max(1, n) * cols:
+        raise ValueError(f"output array must be C-contiguous {np.dtype(dtype).name} with room for {n} x {cols}")
+    return a.reshape(-1, cols) if cols > 1 else a.reshape(-1)
+
+
 class Allocator:
     """Host block allocator (pa_alloc_*): on-demand blocks, block tables, refcounts, copy-on-write."""
 
@@ -247,12 +262,17 @@ class Allocator:
             "pa_seq_append")
         return slots[:n_tokens], pairs[: n_cow.value]
 
-    def append_batch(self, seq_ids):
+    def append_batch(self, seq_ids, slots_out=None, pairs_out=None):
+        """One token per id, in order.  Returns (slots int64 [n], cow_pairs int32 [k][2]).
+
+        ``slots_out`` (int64, >= n entries) and ``pairs_out`` (int32 [>= n][2]),
+        when given, receive the results in place (e.g. pinned staging buffers).
+        """
         np = _np()
-        ids = np.ascontiguousarray(np.asarray(seq_ids, dtype=np.int64))
+        ids = _int64_array(seq_ids)
         n = len(ids)
-        slots = np.empty(max(1, n), np.int64)
-        pairs = np.empty((max(1, n), 2), np.int32)
+        slots = np.empty(max(1, n), np.int64) if slots_out is None else _checked_out(slots_out, np.int64, n, 1)
+        pairs = np.empty((max(1, n), 2), np.int32) if pairs_out is None else _checked_out(pairs_out, np.int32, n, 2)
         n_cow = _i32(0)
         _ok(_lib.pa_append_batch(self._h, ids.ctypes.data, n, slots.ctypes.data, pairs.ctypes.data,
                                  ctypes.byref(n_cow)), "pa_append_batch")
@@ -277,12 +297,21 @@ class Allocator:
         _ok(_lib.pa_seq_block_table(self._h, seq_id, out.ctypes.data, cap, ctypes.byref(n)), "pa_seq_block_table")
         return out[: n.value].tolist()
 
-    def export_tables(self, seq_ids, max_blocks_per_seq: int):
-        """(tables int32 [n][max_blocks_per_seq], lens int32 [n]) in the decode kernel's layout."""
+    def export_tables(self, seq_ids, max_blocks_per_seq: int, tables_out=None, lens_out=None):
+        """(tables int32 [n][max_blocks_per_seq], lens int32 [n]) in the decode kernel's layout.
+
+        ``tables_out`` / ``lens_out``, when given (C-contiguous int32 arrays of
+        exactly those shapes), are filled in place.
+        """
         np = _np()
-        ids = np.ascontiguousarray(np.asarray(seq_ids, dtype=np.int64))
-        tables = np.empty((len(ids), max_blocks_per_seq), np.int32)
-        lens = np.empty(len(ids), np.int32)
+        ids = _int64_array(seq_ids)
+        n = len(ids)
+        tables = np.empty((n, max_blocks_per_seq), np.int32) if tables_out is None else tables_out
+        lens = np.empty(n, np.int32) if lens_out is None else lens_out
+        if tables_out is not None or lens_out is not None:
+            for a, shape in ((tables, (n, max_blocks_per_seq)), (lens, (n,))):
+                if a.dtype != np.int32 or a.shape != shape or not a.flags["C_CONTIGUOUS"]:
+                    raise ValueError(f"output arrays must be C-contiguous int32 of shape {shape}")
         _ok(_lib.pa_export_tables(self._h, ids.ctypes.data, len(ids), max_blocks_per_seq, tables.ctypes.data,
                                   lens.ctypes.data), "pa_export_tables")
         return tables, lens

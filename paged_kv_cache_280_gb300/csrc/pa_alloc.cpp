@@ -22,6 +22,11 @@ namespace {
 struct Sequence {
     std::vector<int32_t> table;  // logical block -> physical block
     int32_t len = 0;             // tokens written
+    // dry-run state of the current pa_append_batch call (valid while mark
+    // equals the allocator's batch epoch)
+    uint64_t mark = 0;
+    int32_t dry_len = 0;
+    bool dry_private = false;  // the tail is known to have refcount 1 at this point
 };
 
 }  // namespace
@@ -36,6 +41,11 @@ struct pa_allocator {
     std::vector<int32_t> refcount;
     std::unordered_map<int64_t, Sequence> seqs;
     int64_t cow_copies = 0;
+    // scratch of pa_append_batch, reused across calls so a batch allocates nothing
+    uint64_t epoch = 0;               // batch calls so far
+    std::vector<uint64_t> drop_mark;  // per block: the epoch drop_count belongs to
+    std::vector<int32_t> drop_count;  // copies of a shared block planned in this call
+    std::vector<Sequence*> batch;     // the call's sequences, in order
 
     int32_t pop_free() {
         int32_t b = ring[head];
@@ -100,6 +110,8 @@ pa_status pa_alloc_create(int32_t num_blocks, int32_t block_size, const int32_t*
     a->block_size = block_size;
     a->ring.resize(num_blocks);
     a->refcount.assign(num_blocks, 0);
+    a->drop_mark.assign(num_blocks, 0);
+    a->drop_count.assign(num_blocks, 0);
     if (free_order) {
         std::vector<char> seen(num_blocks, 0);
         for (int32_t i = 0; i < num_blocks; ++i) {
@@ -162,47 +174,43 @@ pa_status pa_append_batch(pa_allocator* a, const int64_t* seq_ids, int32_t n, in
         return PA_ERR_INVALID_ARG;
     PA_GUARD_BEGIN
     // Dry run: the same id may appear more than once, and a copy made for an
-    // earlier id lowers the refcount a later sharer sees.
-    struct Shadow {
-        Sequence* s;
-        int32_t len;
-        bool tail_private;  // the tail is known to have refcount 1 at this point
-    };
-    std::unordered_map<int64_t, Shadow> shadow;
-    std::unordered_map<int32_t, int32_t> ref_drop;  // copies made so far per shared block
-    shadow.reserve(n * 2);
+    // earlier id lowers the refcount a later sharer sees.  Per-call state lives
+    // in the sequences and in per-block arrays, stamped with this call's epoch.
+    const uint64_t ep = ++a->epoch;
+    const int32_t bs = a->block_size;
+    a->batch.resize(n);
     int64_t need = 0;
     for (int32_t i = 0; i < n; ++i) {
-        auto f = shadow.find(seq_ids[i]);
-        if (f == shadow.end()) {
-            auto it = a->seqs.find(seq_ids[i]);
-            if (it == a->seqs.end()) return PA_ERR_NO_SUCH_SEQ;
-            f = shadow.emplace(seq_ids[i], Shadow{&it->second, it->second.len, false}).first;
+        auto it = a->seqs.find(seq_ids[i]);
+        if (it == a->seqs.end()) return PA_ERR_NO_SUCH_SEQ;
+        Sequence* s = &it->second;
+        a->batch[i] = s;
+        if (s->mark != ep) {
+            s->mark = ep;
+            s->dry_len = s->len;
+            s->dry_private = false;
         }
-        Shadow& sh = f->second;
-        if (sh.len % a->block_size == 0) {
+        if (s->dry_len % bs == 0) {
             ++need;
-            sh.tail_private = true;
-        } else if (!sh.tail_private) {
-            int32_t tail = sh.s->table.back();
-            int32_t refs = a->refcount[tail] - ref_drop[tail];
-            if (refs > 1) {
+            s->dry_private = true;
+        } else if (!s->dry_private) {
+            const int32_t tail = s->table.back();
+            const int32_t drop = a->drop_mark[tail] == ep ? a->drop_count[tail] : 0;
+            if (a->refcount[tail] - drop > 1) {
                 ++need;
-                ++ref_drop[tail];
+                a->drop_mark[tail] = ep;
+                a->drop_count[tail] = drop + 1;
             }
-            sh.tail_private = true;
+            s->dry_private = true;
         }
-        if (sh.len == INT32_MAX) return PA_ERR_INVALID_ARG;
-        ++sh.len;
+        if (s->dry_len == INT32_MAX) return PA_ERR_INVALID_ARG;
+        ++s->dry_len;
     }
     if (need > a->free_count) return PA_ERR_OUT_OF_BLOCKS;
-    for (auto& kv : shadow)  // so that the mutating loop below cannot fail half-way
-        kv.second.s->table.reserve((kv.second.len + a->block_size - 1) / a->block_size);
+    for (int32_t i = 0; i < n; ++i)  // so that the mutating loop below cannot fail half-way
+        a->batch[i]->table.reserve((a->batch[i]->dry_len + bs - 1) / bs);
     *n_cow_out = 0;
-    for (int32_t i = 0; i < n; ++i) {
-        Sequence& s = a->seqs.find(seq_ids[i])->second;
-        a->append_one(s, &slots_out[i], cow_pairs_out, n_cow_out);
-    }
+    for (int32_t i = 0; i < n; ++i) a->append_one(*a->batch[i], &slots_out[i], cow_pairs_out, n_cow_out);
     return PA_OK;
     PA_GUARD_END
 }

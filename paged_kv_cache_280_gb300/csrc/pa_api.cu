@@ -63,6 +63,76 @@ bool encode_pool_map(CUtensorMap* map, const void* pool, int64_t rows, int head_
     return r == CUDA_SUCCESS;
 }
 
+// The pool maps of recent calls: an encoded map depends only on the pool's
+// address and shape, so serving loops that pass the same pools every step
+// reuse it instead of encoding two maps per call.
+struct PoolMapEntry {
+    int dev;
+    const void* pool;
+    int64_t rows;
+    int head_dim, block_size;
+    pa_dtype dt;
+    CUtensorMap map;
+};
+constexpr int kPoolMapCache = 16;
+PoolMapEntry g_maps[kPoolMapCache];
+int g_maps_used = 0, g_maps_next = 0;
+
+bool pool_map(CUtensorMap* map, int dev, const void* pool, int64_t rows, int head_dim, int block_size, pa_dtype dt) {
+    std::lock_guard<std::mutex> lk(g_mu);
+    for (int i = 0; i < g_maps_used; ++i) {
+        const PoolMapEntry& e = g_maps[i];
+        if (e.dev == dev && e.pool == pool && e.rows == rows && e.head_dim == head_dim &&
+            e.block_size == block_size && e.dt == dt) {
+            *map = e.map;
+            return true;
+        }
+    }
+    if (!encode_pool_map(map, pool, rows, head_dim, block_size, dt)) return false;
+    PoolMapEntry& e = g_maps[g_maps_next];
+    e = PoolMapEntry{dev, pool, rows, head_dim, block_size, dt, *map};
+    g_maps_next = (g_maps_next + 1) % kPoolMapCache;
+    if (g_maps_used < kPoolMapCache) ++g_maps_used;
+    return true;
+}
+
+// Dynamic shared memory opted into, and the occupancy found, per (device,
+// kernel, shared-memory size): set and queried once instead of every call.
+struct KernelEntry {
+    int dev;
+    const void* kernel;
+    int smem_attr;  // largest dynamic shared memory opted into so far
+    int occ_smem;   // shared memory size of the cached occupancy
+    int occ;
+};
+constexpr int kKernelCache = 128;
+KernelEntry g_kernels[kKernelCache];
+int g_kernels_used = 0;
+
+bool kernel_occupancy(int dev, const void* kernel, int threads, int smem, int* occ) {
+    std::lock_guard<std::mutex> lk(g_mu);
+    KernelEntry* e = nullptr;
+    for (int i = 0; i < g_kernels_used; ++i)
+        if (g_kernels[i].dev == dev && g_kernels[i].kernel == kernel) e = &g_kernels[i];
+    if (e && e->occ_smem == smem) {
+        *occ = e->occ;
+        return true;
+    }
+    if (!e || e->smem_attr < smem) {
+        if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
+            return false;
+    }
+    int n = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kernel, threads, smem) != cudaSuccess) return false;
+    if (!e && g_kernels_used < kKernelCache) e = &g_kernels[g_kernels_used++];
+    if (e) {
+        const int attr = e->kernel == kernel && e->dev == dev && e->smem_attr > smem ? e->smem_attr : smem;
+        *e = KernelEntry{dev, kernel, attr, smem, n};
+    }
+    *occ = n;
+    return true;
+}
+
 size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 
 struct WorkspaceLayout {
@@ -112,11 +182,8 @@ pa_status plan_launch(int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_head
     if (!found) return PA_ERR_UNSUPPORTED;
     lp->smem = lp->v.smem_bytes(num_seqs, fixed);
     if (lp->smem > kMaxSmem) return PA_ERR_UNSUPPORTED;
-    if (cudaFuncSetAttribute(lp->v.kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, lp->smem) != cudaSuccess)
-        return PA_ERR_CUDA;
     int occ = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, lp->v.kernel, lp->v.threads, lp->smem) != cudaSuccess)
-        return PA_ERR_CUDA;
+    if (!kernel_occupancy(dev, lp->v.kernel, lp->v.threads, lp->smem, &occ)) return PA_ERR_CUDA;
     if (occ <= 0) return PA_ERR_UNSUPPORTED;
     // Default: the tensor-core path, which spends little time per tile, keeps
     // four CTAs per SM (about 128 KB of tiles in flight, enough to cover HBM
@@ -205,8 +272,10 @@ extern "C" pa_status pa_decode_attention(void* out, const void* q, const void* k
     if (workspace_bytes < wl.total) return PA_ERR_WORKSPACE_TOO_SMALL;
 
     CUtensorMap tk, tv;
-    if (!encode_pool_map(&tk, k_pool, rows, head_dim, block_size, dtype) ||
-        !encode_pool_map(&tv, v_pool, rows, head_dim, block_size, dtype))
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return PA_ERR_CUDA;
+    if (!pool_map(&tk, dev, k_pool, rows, head_dim, block_size, dtype) ||
+        !pool_map(&tv, dev, v_pool, rows, head_dim, block_size, dtype))
         return PA_ERR_CUDA;
 
     DecodeParams p;

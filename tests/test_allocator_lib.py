@@ -187,3 +187,32 @@ def test_waste_simulation_through_library_allocator():
     assert paged_waste < 0.04
     for s, n in enumerate(lens):  # waste only in the tail block
         assert 0 <= len(a.table(s)) * 16 - int(n) < 16
+
+
+def test_outputs_in_place():
+    """append_batch / export_tables write into caller arrays (pinned staging) exactly what they return."""
+    order = list(range(40))[::-1]
+    a = pa.Allocator(40, 16, free_order=order)
+    b = pa.Allocator(40, 16, free_order=order)
+    for s, n in enumerate([5, 16, 33]):
+        for x in (a, b):
+            x.create(s)
+            x.append(s, n)
+    a.fork(1, 9)
+    b.fork(1, 9)
+    ids = np.array([0, 1, 2, 9, 1], np.int64)
+    slots = np.full(8, -7, np.int64)
+    pairs = np.full((8, 2), -7, np.int32)
+    s_in, p_in = a.append_batch(ids, slots_out=slots, pairs_out=pairs)
+    s_ref, p_ref = b.append_batch(ids.tolist())
+    assert s_in.tolist() == s_ref.tolist() and p_in.tolist() == p_ref.tolist()
+    assert slots[:5].tolist() == s_ref.tolist() and slots[5:].tolist() == [-7] * 3
+    tables = np.zeros((4, 5), np.int32)
+    lens = np.zeros(4, np.int32)
+    a.export_tables([0, 1, 2, 9], 5, tables_out=tables, lens_out=lens)
+    t_ref, l_ref = b.export_tables([0, 1, 2, 9], 5)
+    assert np.array_equal(tables, t_ref) and np.array_equal(lens, l_ref)
+    with pytest.raises(ValueError):
+        a.append_batch([0], slots_out=np.zeros(4, np.int32))
+    with pytest.raises(ValueError):
+        a.export_tables([0], 5, tables_out=np.zeros((1, 4), np.int32), lens_out=np.zeros(1, np.int32))
