@@ -8,8 +8,8 @@ and never imports it.
 
 Parts:
   * ``pa_oracle.c``  -- fp64 decode attention (direct and split + reduce),
-    the slot-mapped append and the copy-on-write block copy, as element
-    loops over host arrays.
+    paged prefill (chunked causal) attention, the slot-mapped append and the
+    copy-on-write block copy, as element loops over host arrays.
   * ``alloc_model``  -- a reference model of the block allocator
     (on-demand blocks, refcounted sharing, copy-on-write).
   * ``waste``        -- the memory accounting of the waste simulation on
@@ -66,6 +66,9 @@ def _open(path: str):
     lib.oracle_reshape_and_cache.argtypes = [i32, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32]
     lib.oracle_copy_blocks.restype = ctypes.c_int
     lib.oracle_copy_blocks.argtypes = [i32, vp, vp, vp, i32, i32, i32, i32, i32]
+    lib.oracle_prefill_attention.restype = ctypes.c_int
+    lib.oracle_prefill_attention.argtypes = [ctypes.c_int, vp, vp, vp, vp, i32, vp, vp, i32, i32, i32, i32,
+                                             i32, i32, f64, i32, i32, vp]
     return lib
 
 
@@ -119,6 +122,43 @@ def decode_attention(q, k_pool, v_pool, block_tables, seq_lens, scale, seqs=None
         _check(lib.oracle_decode_attention(dt, q.ctypes.data, k_pool.ctypes.data, v_pool.ctypes.data,
                                            bt.ctypes.data, bt.shape[1], lens.ctypes.data, B, Hq, Hkv, D,
                                            bs, nb, float(scale), b, b + 1, out.ctypes.data))
+
+    if threads <= 1:
+        for b in todo:
+            run(b)
+    else:
+        with ThreadPoolExecutor(threads) as ex:
+            list(ex.map(run, todo))
+    return out
+
+
+def prefill_attention(q, k_pool, v_pool, block_tables, seq_lens, cu_q_lens, scale, seqs=None, threads=1):
+    """fp64 paged prefill (chunked causal) attention.  Returns out[T][Hq][D] (float64).
+
+    q: [T][Hq][D] with T = cu_q_lens[-1]; chunk token i of sequence b is row
+    cu_q_lens[b] + i at position seq_lens[b] - n_b + i, and sees keys 0..that
+    position.  ``seqs`` restricts the computation to those sequences (other
+    rows are NaN); ``threads`` > 1 runs sequences on a thread pool.
+    """
+    q, k_pool, v_pool = _c(q), _c(k_pool), _c(v_pool)
+    dt = _dtype_code(q)
+    if _dtype_code(k_pool) != dt or _dtype_code(v_pool) != dt:
+        raise TypeError("q and the pools must share a dtype")
+    bt = _c(block_tables, np.int32)
+    lens = _c(seq_lens, np.int32)
+    cu = _c(cu_q_lens, np.int32)
+    T, Hq, D = q.shape
+    nb, Hkv, bs, D2 = k_pool.shape
+    B = lens.shape[0]
+    assert D2 == D and v_pool.shape == k_pool.shape and bt.shape[0] == B and cu.shape == (B + 1,) and cu[-1] == T
+    out = np.full((T, Hq, D), np.nan, np.float64)
+    lib = _load()
+    todo = list(range(B)) if seqs is None else sorted(set(int(s) for s in seqs))
+
+    def run(b):
+        _check(lib.oracle_prefill_attention(dt, q.ctypes.data, k_pool.ctypes.data, v_pool.ctypes.data,
+                                            bt.ctypes.data, bt.shape[1], lens.ctypes.data, cu.ctypes.data, B, Hq,
+                                            Hkv, D, bs, nb, float(scale), b, b + 1, out.ctypes.data))
 
     if threads <= 1:
         for b in todo:

@@ -262,3 +262,77 @@ int oracle_copy_blocks(int32_t elem_bytes, void* k_pool, void* v_pool, const int
     }
     return ORACLE_OK;
 }
+
+/*
+ * Paged prefill (chunked append) attention.  The pages put the same block
+ * table in front of every attention read ("把虚拟内存搬进 KV Cache": the
+ * attention kernel reads KV by block index; "Q32" follow-up 3: FlashAttention
+ * loads the KV cache block by block, adapted to non-contiguous storage), and
+ * prefill is the step that computes a prompt's queries against that cache.
+ *
+ * Sequence b holds seq_lens[b] tokens in the cache; the last
+ * n_b = cu_q_lens[b+1] - cu_q_lens[b] of them are the chunk whose queries are
+ * given.  Chunk token i sits at position p = seq_lens[b] - n_b + i and, as in
+ * any causal language model, attends to the keys at positions 0..p:
+ *     s_t = scale * q . K^[t] (t <= p),  w = softmax(s),  out = sum_t w_t V^[t].
+ * q and out are [T][Hq][D] with T = cu_q_lens[num_seqs]; chunk token i of
+ * sequence b is row cu_q_lens[b] + i.  Writes the rows of sequences
+ * [seq_begin, seq_end) only.
+ */
+int oracle_prefill_attention(int dtype, const void* q, const void* k_pool, const void* v_pool,
+                             const int32_t* block_tables, int32_t max_blocks_per_seq,
+                             const int32_t* seq_lens, const int32_t* cu_q_lens, int32_t num_seqs,
+                             int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
+                             int32_t num_blocks, double scale, int32_t seq_begin, int32_t seq_end, double* out) {
+    int rc = check_common(num_seqs, num_q_heads, num_kv_heads, head_dim, block_size, seq_begin, seq_end);
+    if (rc) return rc;
+    const int32_t G = num_q_heads / num_kv_heads;
+    for (int32_t b = seq_begin; b < seq_end; ++b) {
+        const int32_t len = seq_lens[b];
+        const int32_t n = cu_q_lens[b + 1] - cu_q_lens[b];
+        if (n < 0 || len < n || (int64_t)len > (int64_t)max_blocks_per_seq * block_size) return ORACLE_BAD_ARG;
+        if (n == 0) continue;
+        double* K = (double*)malloc(sizeof(double) * (size_t)len * head_dim);
+        double* V = (double*)malloc(sizeof(double) * (size_t)len * head_dim);
+        double* s = (double*)malloc(sizeof(double) * (size_t)len);
+        if (!K || !V || !s) {
+            free(K); free(V); free(s);
+            return ORACLE_NOMEM;
+        }
+        const int32_t* table = block_tables + (size_t)b * max_blocks_per_seq;
+        for (int32_t g = 0; g < num_kv_heads && rc == ORACLE_OK; ++g) {
+            rc = gather_kv(dtype, k_pool, v_pool, table, len, num_kv_heads, head_dim, block_size,
+                           num_blocks, g, K, V);
+            if (rc) break;
+            for (int32_t i = 0; i < n; ++i) {
+                const int32_t p = len - n + i; /* this token's position: keys 0..p are visible */
+                const size_t row = (size_t)cu_q_lens[b] + (size_t)i;
+                for (int32_t h = g * G; h < (g + 1) * G; ++h) {
+                    const size_t qrow = (row * num_q_heads + h) * head_dim;
+                    double m = -INFINITY;
+                    for (int32_t t = 0; t <= p; ++t) {
+                        double dot = 0.0;
+                        for (int32_t d = 0; d < head_dim; ++d)
+                            dot += load_elem(dtype, q, qrow + d) * K[(size_t)t * head_dim + d];
+                        s[t] = scale * dot;
+                        if (s[t] > m) m = s[t];
+                    }
+                    double denom = 0.0;
+                    for (int32_t t = 0; t <= p; ++t) {
+                        s[t] = exp(s[t] - m);
+                        denom += s[t];
+                    }
+                    double* o = out + qrow;
+                    for (int32_t d = 0; d < head_dim; ++d) o[d] = 0.0;
+                    for (int32_t t = 0; t <= p; ++t) {
+                        const double w = s[t] / denom;
+                        for (int32_t d = 0; d < head_dim; ++d) o[d] += w * V[(size_t)t * head_dim + d];
+                    }
+                }
+            }
+        }
+        free(K); free(V); free(s);
+        if (rc) return rc;
+    }
+    return ORACLE_OK;
+}

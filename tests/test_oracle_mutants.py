@@ -27,7 +27,14 @@ C_MUTANTS = {
     "reduce_weight_inverted": ("double w = exp(m[p] - M);", "double w = exp(M - m[p]);"),
     "reduce_drops_l": ("L += w * l[p];", "L += w;"),
     "partition_max_unscaled": ("if (scale * dot > m) m = scale * dot;", "if (dot > m) m = dot;"),
+    "prefill_position_ignores_context": ("const int32_t p = len - n + i;", "const int32_t p = i;"),
+    "prefill_position_one_early": ("const int32_t p = len - n + i;", "const int32_t p = len - n + i - 1;"),
+    "prefill_rows_reversed": ("const size_t row = (size_t)cu_q_lens[b] + (size_t)i;",
+                              "const size_t row = (size_t)cu_q_lens[b + 1] - 1 - (size_t)i;"),
+    "prefill_not_causal": ("for (int32_t t = 0; t <= p; ++t) {\n                        double dot",
+                           "for (int32_t t = 0; t < len; ++t) {\n                        double dot"),
 }
+PIN_FILES = ["test_oracle_pins.py", "test_oracle_prefill_pins.py"]
 
 
 @pytest.fixture(scope="module")
@@ -49,7 +56,7 @@ def test_c_mutant_is_caught(name, src, tmp_path):
     code = (
         "import sys, pytest, oracle;"
         f"oracle._lib = oracle._open({str(so)!r});"
-        f"sys.exit(pytest.main(['-q', '-x', '-p', 'no:cacheprovider', {os.path.join(HERE, 'test_oracle_pins.py')!r}]))"
+        f"sys.exit(pytest.main(['-q', '-x', '-p', 'no:cacheprovider', *{[os.path.join(HERE, f) for f in PIN_FILES]!r}]))"
     )
     r = subprocess.run([sys.executable, "-c", code], cwd=os.path.dirname(HERE), capture_output=True, text=True,
                        env={**os.environ, "PYTHONPATH": os.pathsep.join([os.path.dirname(HERE), HERE])})
