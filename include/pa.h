@@ -201,6 +201,40 @@ pa_status pa_decode_launch_info(int32_t num_seqs, int32_t num_q_heads, int32_t n
  */
 pa_status pa_decode_set_ctas_per_sm(int32_t ctas);
 
+/*
+ * Paged prefill (chunked causal) attention, bf16.
+ *
+ * "Q32: vLLM PagedAttention 原理" follow-up 3 (FlashAttention loads the KV
+ * cache block by block, adapted to non-contiguous blocks) and
+ * data.6616ai.com "把虚拟内存搬进 KV Cache" (attention reads KV by block
+ * index).  Sequence b holds seq_lens[b] tokens in the pools, its K/V already
+ * appended (pa_reshape_and_cache); the last n_b = cu_q_lens[b+1] - cu_q_lens[b]
+ * of them are a chunk whose queries are given.  Chunk token i sits at position
+ * p = seq_lens[b] - n_b + i and attends to the keys at positions 0..p:
+ *     out[cu_q_lens[b] + i][h] = softmax_{t <= p}(scale q . K[t]) V[t],
+ * with query head h reading KV head h / (num_q_heads / num_kv_heads).
+ *
+ * Layouts (device, row-major, caller-owned): q and out [T][num_q_heads][head_dim]
+ * bf16 with T = cu_q_lens[num_seqs]; pools as for pa_decode_attention;
+ * block_tables int32 [num_seqs][max_blocks_per_seq]; seq_lens int32 [num_seqs];
+ * cu_q_lens int32 [num_seqs + 1], non-decreasing from 0; num_q_tokens = T,
+ * the rows of q and out.  max_q_len bounds every n_b (the grid is sized by
+ * it).  Supported: bf16, head_dim 64 or 128, block_size 16 or 32,
+ * num_q_heads / num_kv_heads <= 8, num_seqs <= 65535.
+ *
+ * Errors: host checks return a status before any launch.  A sequence with
+ * n_b > seq_lens[b], n_b > max_q_len, rows past num_q_tokens, or seq_lens[b]
+ * beyond its block table sets PA_DEV_BAD_SEQ_LEN in *dev_status (if not NULL)
+ * and its rows are not written; block ids outside [0, num_blocks) set PA_DEV_BAD_BLOCK_ID and block
+ * 0 is read instead; a pipeline wait that gives up sets PA_DEV_WAIT_TIMEOUT.
+ * Asynchronous on `stream` (cudaStream_t).  Allocates nothing.
+ */
+pa_status pa_prefill_attention(void* out, const void* q, const void* k_pool, const void* v_pool,
+                               const int32_t* block_tables, int32_t max_blocks_per_seq, const int32_t* seq_lens,
+                               const int32_t* cu_q_lens, int32_t num_seqs, int32_t num_q_tokens, int32_t max_q_len,
+                               int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
+                               int32_t num_blocks, float scale, pa_dtype dtype, int32_t* dev_status, void* stream);
+
 /* ------------------------------------------------------------------------ */
 /* Host block allocator                                                      */
 /* ------------------------------------------------------------------------ */

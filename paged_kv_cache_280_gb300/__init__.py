@@ -58,6 +58,8 @@ _SIGS = {
     "pa_decode_attention_static": (_i32, [_vp, _vp, _vp, _vp, _vp, _i32, _vp, _i32, _i32, _i32, _i32, _i32, _i32,
                                           _i32, _f32, _i32, _i32, _vp, _vp]),
     "pa_decode_launch_info": (_i32, [_i32, _i32, _i32, _i32, _i32, _i32, _i32, _pi32, _pi32, _pi32, _pi32]),
+    "pa_prefill_attention": (_i32, [_vp, _vp, _vp, _vp, _vp, _i32, _vp, _vp, _i32, _i32, _i32, _i32, _i32, _i32,
+                                    _i32, _i32, ctypes.c_float, _i32, _vp, _vp]),
     "pa_decode_set_ctas_per_sm": (_i32, [_i32]),
     "pa_alloc_create": (_i32, [_i32, _i32, _vp, ctypes.POINTER(_vp)]),
     "pa_alloc_destroy": (None, [_vp]),
@@ -194,6 +196,21 @@ def pa_decode_launch_info(num_seqs, num_q_heads, num_kv_heads, head_dim, block_s
                                    dtype, *[ctypes.byref(v) for v in vals]),
         "pa_decode_launch_info")
     return tuple(int(v.value) for v in vals)
+
+
+def pa_prefill_attention(out, q, k_pool, v_pool, block_tables, seq_lens, cu_q_lens, max_q_len, scale, status=None,
+                         stream=None):
+    """Paged prefill (chunked causal) attention, bf16.  out/q [T][Hq][D]; pools [num_blocks][Hkv][bs][D];
+    block_tables int32 [B][max_blocks]; seq_lens int32 [B] (context incl. the chunk); cu_q_lens int32 [B+1]."""
+    t, hq, d = q.shape
+    nb, hkv, bs, _ = k_pool.shape
+    b = seq_lens.shape[0]
+    _ok(_lib.pa_prefill_attention(_dev_ptr(out, "out"), _dev_ptr(q, "q"), _dev_ptr(k_pool, "k_pool"),
+                                  _dev_ptr(v_pool, "v_pool"), _dev_ptr(block_tables, "block_tables"),
+                                  block_tables.shape[1], _dev_ptr(seq_lens, "seq_lens"), _dev_ptr(cu_q_lens, "cu_q_lens"),
+                                  b, t, int(max_q_len), hq, hkv, d, bs, nb, float(scale), _dtype_code(q),
+                                  _dev_ptr(status, "status"), _stream(stream)),
+        "pa_prefill_attention")
 
 
 def pa_decode_set_ctas_per_sm(ctas: int) -> None:

@@ -63,6 +63,8 @@ bool encode_pool_map(CUtensorMap* map, const void* pool, int64_t rows, int head_
     return r == CUDA_SUCCESS;
 }
 
+}  // namespace
+
 // The pool maps of recent calls: an encoded map depends only on the pool's
 // address and shape, so serving loops that pass the same pools every step
 // reuse it instead of encoding two maps per call.
@@ -75,8 +77,8 @@ struct PoolMapEntry {
     CUtensorMap map;
 };
 constexpr int kPoolMapCache = 16;
-PoolMapEntry g_maps[kPoolMapCache];
-int g_maps_used = 0, g_maps_next = 0;
+static PoolMapEntry g_maps[kPoolMapCache];
+static int g_maps_used = 0, g_maps_next = 0;
 
 bool pool_map(CUtensorMap* map, int dev, const void* pool, int64_t rows, int head_dim, int block_size, pa_dtype dt) {
     std::lock_guard<std::mutex> lk(g_mu);
@@ -106,8 +108,8 @@ struct KernelEntry {
     int occ;
 };
 constexpr int kKernelCache = 128;
-KernelEntry g_kernels[kKernelCache];
-int g_kernels_used = 0;
+static KernelEntry g_kernels[kKernelCache];
+static int g_kernels_used = 0;
 
 bool kernel_occupancy(int dev, const void* kernel, int threads, int smem, int* occ) {
     std::lock_guard<std::mutex> lk(g_mu);
@@ -132,6 +134,8 @@ bool kernel_occupancy(int dev, const void* kernel, int threads, int smem, int* o
     *occ = n;
     return true;
 }
+
+namespace {
 
 size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 

@@ -58,4 +58,32 @@ bool decode_variant_f32_pow2(int head_dim, int block_size, int group, DecodeVari
 bool decode_variant_bf16_mma(int head_dim, int block_size, DecodeVariant* out);
 bool decode_variant_bf16_fma(int head_dim, int block_size, int group, DecodeVariant* out);
 
+// Host launch helpers shared by the attention entry points (pa_api.cu).
+// The TMA map of a pool viewed as [num_blocks * Hkv * block_size][head_dim]
+// rows, one box = block_size rows x 128 bytes with the 128-byte swizzle;
+// cached per (device, pool, shape).
+bool pool_map(CUtensorMap* map, int dev, const void* pool, int64_t rows, int head_dim, int block_size, pa_dtype dt);
+// Opts the kernel into `smem` bytes of dynamic shared memory and returns its
+// CTAs per SM; cached per (device, kernel, smem).
+bool kernel_occupancy(int dev, const void* kernel, int threads, int smem, int* occ);
+
+// Paged prefill (chunked causal) attention, bf16.
+struct PrefillParams {
+    void* out;
+    const void* q;
+    const int32_t* block_tables;
+    const int32_t* seq_lens;
+    const int32_t* cu_q_lens;
+    int32_t* status;
+    int32_t max_blocks_per_seq;
+    int32_t num_q_heads;
+    int32_t num_kv_heads;
+    int32_t num_blocks;
+    int32_t group;          // G = num_q_heads / num_kv_heads
+    int32_t tile_tokens;    // chunk tokens per 64-row query tile: 64 / G
+    int32_t num_q_tokens;   // rows of q and out
+    int32_t max_q_len;      // bound on every chunk (the grid is sized by it)
+    float scale_log2;
+};
+
 }  // namespace pa

@@ -125,3 +125,20 @@ class DecodeCase:
 
 def status_word(ws) -> int:
     return int(ws[:4].view(dtype=__import__("torch").int32).item())
+
+
+def poison_unused_slots(k_pool: np.ndarray, v_pool: np.ndarray, tables: np.ndarray, lens: np.ndarray) -> int:
+    """Fill every pool slot no sequence covers (free blocks, tails of partial blocks) with NaN, in place.
+
+    Those slots may hold any bits in a real pool; a kernel must not let them reach an output
+    (zero weight times NaN is NaN).  Returns the number of slots poisoned.
+    """
+    nb, _, bs, _ = k_pool.shape
+    used = np.zeros((nb, bs), bool)
+    for b, n in enumerate(lens):
+        for t in range(int(n)):
+            used[tables[b, t // bs], t % bs] = True
+    nan = np.uint16(0x7FC0) if k_pool.dtype == np.uint16 else np.float32("nan")
+    for pool in (k_pool, v_pool):
+        pool.transpose(0, 2, 1, 3)[~used] = nan
+    return int((~used).sum())

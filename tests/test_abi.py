@@ -35,3 +35,18 @@ def test_status_strings():
 
     for code in range(0, 11):
         assert pa._lib.pa_status_str(code)
+
+
+def test_prefill_host_checks_run_before_any_launch():
+    """Argument errors of pa_prefill_attention come back from the host checks (no GPU needed)."""
+    import paged_kv_cache_280_gb300 as pa
+
+    fake = ctypes.c_void_p(1 << 20)  # 16-byte aligned, never dereferenced
+    args = lambda dt, hd, bs: (fake, fake, fake, fake, fake, 4, fake, fake, 2, 10, 8, 8, 2, hd, bs, 100, 0.1, dt,  # noqa: E731
+                               None, None)
+    assert pa._lib.pa_prefill_attention(*args(pa.PA_F32, 128, 16)) == 2  # PA_ERR_UNSUPPORTED: fp32
+    assert pa._lib.pa_prefill_attention(*args(pa.PA_BF16, 96, 16)) == 2  # head_dim 96
+    assert pa._lib.pa_prefill_attention(*args(pa.PA_BF16, 128, 8)) == 2  # block_size 8
+    bad = list(args(pa.PA_BF16, 128, 16))
+    bad[1] = ctypes.c_void_p((1 << 20) + 2)  # misaligned q
+    assert pa._lib.pa_prefill_attention(*bad) == 1  # PA_ERR_INVALID_ARG

@@ -11,7 +11,7 @@ import numpy as np
 import pytest
 
 import synth.workloads as W
-from gpu_cases import DecodeCase, check_close, status_word, to_numpy, to_torch
+from gpu_cases import DecodeCase, check_close, poison_unused_slots, status_word, to_numpy, to_torch
 
 pytestmark = pytest.mark.gpu
 
@@ -151,3 +151,17 @@ def test_launch_info():
     assert mma == 1 and stages >= 4 and ctas >= 1 and smem > 0
     ctas, stages, smem, mma = pa.pa_decode_launch_info(4, 4, 4, 64, 16, 3, pa.PA_F32)
     assert mma == 0 and ctas <= 4 * 4 * 3
+
+
+@pytest.mark.parametrize("dtype,hq,hkv,d,bs", VARIANTS)
+def test_variants_ignore_nan_in_unused_slots(dtype, hq, hkv, d, bs):
+    """Free blocks and the unfilled tail of each last block hold NaN; no output may see them."""
+    w = W.random_case(700 + hq + d + bs, 9, hq, hkv, d, bs, dtype, max_len=200)
+    lens = w.lengths.copy()
+    lens[:4] = [1, bs - 1, bs + 1, 3 * bs - 5]
+    c = DecodeCase(w, lengths=lens)
+    assert poison_unused_slots(c.k_pool, c.v_pool, c.ref_tables, c.lengths) > 0
+    c.device()
+    ws = c.run()
+    check_close(to_numpy(c.dout), c.oracle(), dtype)
+    assert status_word(ws) == 0
