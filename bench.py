@@ -492,6 +492,207 @@ def run_ours(args, rank, world, local_rank):
 
 
 # ---------------------------------------------------------------------------
+# prefill path: prompt prefill of the parallel-sampling workload
+# ---------------------------------------------------------------------------
+PREFILL_METRIC = "paged prefill attention prompt-tokens/s and TFLOP/s (% of GB300 bf16 tensor roofline) at 1 GPU"
+PREFILL_UNIT = "prompt-tokens/s"
+
+
+def measured_tensor_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return float(json.load(f)["bf16_tflops"]), "measured (MEASURED_PEAKS.json bf16_tflops, burst)"
+    except (OSError, KeyError, ValueError):
+        return 1900.0, "fallback"
+
+
+def prefill_setup(rank: int, prompts: int):
+    """Prompts of the parallel-sampling workload, each prefilled as one chunk."""
+    import synth
+    import synth.workloads as W
+
+    base = W.cow_sampling()
+    P, L, bs = min(prompts, base.prompts), base.prompt_len, base.block_size
+    nb = int(math.ceil(1.1 * P * -(-L // bs)))
+    return W.scaled(base, prompts=P, num_blocks=nb, seed=base.seed + 7919 * rank), P, L
+
+
+def prefill_flops(L: int, P: int, hq: int, d: int) -> float:
+    """Causal attention of P fresh L-token prompts: 4 d Hq sum_p (p + 1) per prompt (QK^T and PV)."""
+    return 4.0 * d * hq * P * L * (L + 1) / 2
+
+
+def run_prefill(args, rank, world, local_rank):
+    import torch
+    import synth
+
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    dist = dist_init(world, "nccl")
+    import paged_kv_cache_280_gb300 as pa
+
+    K, Wm = args.steps, args.warmup
+    K_e2e = min(K, args.e2e_steps)
+    w, P, L = prefill_setup(rank, args.prompts)
+    Hq, Hkv, D, bs = w.num_q_heads, w.num_kv_heads, w.head_dim, w.block_size
+    T = P * L
+    lib = pa.Allocator(w.num_blocks, bs, free_order=w.free_order())
+    slots = []
+    for p_ in range(P):
+        lib.create(p_)
+        slots.append(lib.append(p_, L)[0])
+    slots = np.concatenate(slots)
+    max_blocks = -(-L // bs)
+    tables, lens = lib.export_tables(range(P), max_blocks)
+    cu = np.arange(0, T + 1, L, dtype=np.int32)
+    q = synth.normal(synth.stream_seed(w.seed, 4242), T * Hq * D, "bf16").reshape(T, Hq, D)
+    kn, vn = w.prompt_tokens("k")[:T], w.prompt_tokens("v")[:T]
+
+    def to_dev(a):
+        if a.dtype == np.uint16:
+            return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).to(dev)
+        return torch.from_numpy(np.ascontiguousarray(a)).to(dev)
+
+    k_host, v_host = w.pool_values("k"), w.pool_values("v")
+    dk, dv = to_dev(k_host), to_dev(v_host)
+    d_q, d_kn, d_vn = to_dev(q), to_dev(kn), to_dev(vn)
+    d_slots, d_tables, d_lens, d_cu = to_dev(slots), to_dev(tables), to_dev(lens), to_dev(cu)
+    out = torch.empty_like(d_q)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def flush_l2():
+        flush.zero_()
+        flush[: L2_FLUSH_BYTES // 2].view(torch.int32).sum()
+
+    def append(kk, vv, ss):
+        pa.pa_reshape_and_cache(kk, vv, dk, dv, ss, status=status, stream=stream)
+
+    def prefill(qq, tt, ll, cc):
+        pa.pa_prefill_attention(out, qq, dk, dv, tt, ll, cc, L, w.scale, status=status, stream=stream)
+
+    for _ in range(Wm):
+        flush_l2()
+        append(d_kn, d_vn, d_slots)
+        prefill(d_q, d_tables, d_lens, d_cu)
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    ev = [tuple(torch.cuda.Event(enable_timing=True) for _ in range(3)) for _ in range(K)]
+    clocks = ClockSampler(local_rank)
+    clocks.start()
+    torch.cuda.synchronize()
+    for i in range(K):
+        flush_l2()
+        ev[i][0].record(stream)
+        append(d_kn, d_vn, d_slots)
+        ev[i][1].record(stream)
+        prefill(d_q, d_tables, d_lens, d_cu)
+        ev[i][2].record(stream)
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    clocks.stop()
+    if status.item():
+        raise SystemExit(f"device status word {int(status.item()):#x}")
+    step_ms = [a.elapsed_time(c) for a, b, c in ev]
+    pf_ms = [b.elapsed_time(c) for a, b, c in ev]
+    total_s = reduce_max(sum(step_ms) / 1e3, dist, dev)
+    value = reduce_sum(float(T * K), dist, dev) / total_s
+    flops = prefill_flops(L, P, Hq, D)
+    peak, peak_kind = measured_tensor_peak()
+    achieved = flops / (statistics.mean(pf_ms) / 1e3) / 1e12
+
+    # e2e: one pinned staging buffer per step (q, new K/V, slots, tables, lengths, chunk offsets), one H2D,
+    # the two kernels, and the D2H of the output
+    regions = [("q", T * Hq * D * 2), ("kn", T * Hkv * D * 2), ("vn", T * Hkv * D * 2), ("slots", T * 8),
+               ("tables", P * max_blocks * 4), ("lens", P * 4), ("cu", (P + 1) * 4)]
+    offs, pos = {}, 0
+    for name, n in regions:
+        offs[name] = (pos, n)
+        pos += -(-n // 256) * 256
+    host_stage = torch.empty(pos, dtype=torch.uint8).pin_memory()
+    for name, src in (("q", q), ("kn", kn), ("vn", vn), ("slots", slots), ("tables", tables), ("lens", lens),
+                      ("cu", cu)):
+        o, n = offs[name]
+        host_stage.numpy()[o:o + n] = np.ascontiguousarray(src).view(np.uint8).reshape(-1)
+    dev_stage = torch.empty(pos, dtype=torch.uint8, device=dev)
+
+    def region(name, dtype, shape):
+        o, n = offs[name]
+        return dev_stage[o:o + n].view(dtype).view(shape)
+
+    e_q, e_kn, e_vn = region("q", torch.bfloat16, (T, Hq, D)), region("kn", torch.bfloat16, (T, Hkv, D)), \
+        region("vn", torch.bfloat16, (T, Hkv, D))
+    e_slots, e_tables = region("slots", torch.int64, (T,)), region("tables", torch.int32, (P, max_blocks))
+    e_lens, e_cu = region("lens", torch.int32, (P,)), region("cu", torch.int32, (P + 1,))
+    h_out = torch.empty((T, Hq, D), dtype=torch.int16).pin_memory()
+    e2e_s = 0.0
+    for _ in range(K_e2e):
+        flush_l2()
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        dev_stage.copy_(host_stage, non_blocking=True)
+        append(e_kn, e_vn, e_slots)
+        prefill(e_q, e_tables, e_lens, e_cu)
+        h_out.copy_(out.view(torch.int16), non_blocking=True)
+        stream.synchronize()
+        e2e_s += time.perf_counter() - t0
+    e2e_total = reduce_max(e2e_s, dist, dev)
+    e2e_value = reduce_sum(float(T * K_e2e), dist, dev) / e2e_total if K_e2e else None
+
+    line = {
+        "metric": PREFILL_METRIC, "value": value, "unit": PREFILL_UNIT, "n_gpus": world, "steps": K, "warmup": Wm,
+        "ms_per_step": total_s * 1e3 / K, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16", "data": f"synthetic, seeded: {P} prompts of {L} tokens (the parallel-sampling workload's "
+                                 f"prompts), 32 query / 8 KV heads, d 128, 16-token blocks scattered",
+        "config": {"workload": f"prefill_p{P}_len{L}_hq{Hq}_hkv{Hkv}_d{D}_bs{bs}_bf16", "prompts": P,
+                   "prompt_len": L, "num_q_heads": Hq, "num_kv_heads": Hkv, "head_dim": D, "block_size": bs,
+                   "flops_per_step": flops, "l2": "flushed between timed steps (512 MiB write, then a 256 MiB read)",
+                   "prefill_ms_median": statistics.median(pf_ms), "prefill_ms_min": min(pf_ms),
+                   "path": "mma.sync m16n8k16, TMA ring"},
+        "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
+                     "peak_source": peak_kind, "kernel": "pa_prefill_attention (prefill_kernel)", "traffic": None},
+        "e2e": {"value": e2e_value, "unit": PREFILL_UNIT, "h2d_bytes_per_step": pos,
+                "d2h_bytes_per_step": h_out.numel() * 2, "steps": K_e2e,
+                "includes": "one H2D of the pinned staging (q, new K/V, slots, tables, lengths, offsets), the append "
+                            "and prefill kernels, D2H of out"},
+        "gpu_launches": 2 * K,
+        "clocks": clocks.summary(),
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = prefill_cpu_baseline(w, q, k_host, v_host, kn, vn, slots, tables, lens, L, P,
+                                                    args.cpu_seconds)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if dist:
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+def prefill_cpu_baseline(w, q, k_pool, v_pool, kn, vn, slots, tables, lens, L, P, seconds):
+    """The oracle's prefill over whole prompts (one per host thread at a time), bounded by ``seconds``."""
+    import oracle
+
+    k_pool, v_pool = k_pool.copy(), v_pool.copy()
+    oracle.reshape_and_cache(kn, vn, k_pool, v_pool, slots)
+    threads = os.cpu_count() or 1
+    cu = np.arange(0, P * L + 1, L, dtype=np.int32)
+    done, t0 = 0, time.perf_counter()
+    while done < P:
+        seqs = list(range(done, min(P, done + threads)))
+        oracle.prefill_attention(q, k_pool, v_pool, tables, lens, cu, w.scale, seqs=seqs, threads=threads)
+        done += len(seqs)
+        if time.perf_counter() - t0 >= seconds:
+            break
+    dt = time.perf_counter() - t0
+    return {"value": done * L / dt, "unit": PREFILL_UNIT, "cores": threads, "kind": "oracle",
+            "sample": f"fp64 C oracle prefill of {done} of the {P} prompts ({dt:.1f} s), one prompt per thread"}
+
+
+# ---------------------------------------------------------------------------
 # reference arm: the oracle on the host cores, same metric and workload
 # ---------------------------------------------------------------------------
 def run_reference(args, rank, world):
@@ -539,6 +740,54 @@ def run_reference(args, rank, world):
     print(json.dumps(line), flush=True)
 
 
+def run_prefill_reference(args, rank, world):
+    """The oracle's prefill of the same prompts on the host cores, each step a bounded sample of one prompt."""
+    if rank != 0:
+        return
+    import synth
+
+    w, P, L = prefill_setup(0, args.prompts)
+    Hq, D = w.num_q_heads, w.head_dim
+    from oracle.alloc_model import RefAllocator
+
+    ref = RefAllocator(w.num_blocks, w.block_size, free_order=w.free_order().tolist())
+    slots = []
+    for p_ in range(P):
+        ref.create(p_)
+        slots.extend(ref.append(p_, L)[0])
+    tables = np.zeros((P, -(-L // w.block_size)), np.int32)
+    for p_ in range(P):
+        t = ref.table(p_)
+        tables[p_, : len(t)] = t
+    lens = np.full(P, L, np.int32)
+    q = synth.normal(synth.stream_seed(w.seed, 4242), P * L * Hq * D, "bf16").reshape(P * L, Hq, D)
+    kn, vn = w.prompt_tokens("k")[: P * L], w.prompt_tokens("v")[: P * L]
+    import oracle
+
+    k_pool, v_pool = w.pool_values("k"), w.pool_values("v")
+    oracle.reshape_and_cache(kn, vn, k_pool, v_pool, np.asarray(slots, np.int64))
+    cu = np.arange(0, P * L + 1, L, dtype=np.int32)
+    threads = os.cpu_count() or 1
+    times = []
+    for i in range(args.warmup + args.steps):
+        t0 = time.perf_counter()
+        oracle.prefill_attention(q, k_pool, v_pool, tables, lens, cu, w.scale, seqs=[i % P], threads=threads)
+        if i >= args.warmup:
+            times.append(time.perf_counter() - t0)
+    value = L * len(times) / sum(times)
+    line = {
+        "impl": "reference", "metric": PREFILL_METRIC, "value": value, "unit": PREFILL_UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * sum(times) / len(times),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": f"synthetic, seeded: {P} prompts of {L} tokens, 32 query / 8 KV heads, d 128",
+        "config": {"workload": f"prefill_p{P}_len{L}_hq{Hq}_hkv{w.num_kv_heads}_d{D}_bs{w.block_size}_bf16"},
+        "cpu_baseline": {"value": value, "unit": PREFILL_UNIT, "cores": 1, "kind": "oracle",
+                         "sample": "one whole prompt per step (rotating), fp64 C oracle, one thread"},
+        "e2e": {"value": value, "unit": PREFILL_UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -550,11 +799,19 @@ def main(argv=None):
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--ref-seqs-per-step", type=int, default=16)
+    ap.add_argument("--path", choices=["decode", "prefill"], default="decode",
+                    help="decode: the decode step (the headline); prefill: prompt prefill of the sampling prompts")
+    ap.add_argument("--prompts", type=int, default=16, help="prefill path: prompts per step (at most 16)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         raise SystemExit("at least 3 warm-up steps")
     rank, world, local_rank = dist_env()
-    if args.impl == "reference":
+    if args.path == "prefill":
+        if args.impl == "reference":
+            run_prefill_reference(args, rank, world)
+        else:
+            run_prefill(args, rank, world, local_rank)
+    elif args.impl == "reference":
         run_reference(args, rank, world)
     else:
         run_ours(args, rank, world, local_rank)
