@@ -62,7 +62,8 @@ typedef enum pa_status {
     PA_ERR_WORKSPACE_TOO_SMALL = 7,/* decode workspace smaller than pa_decode_workspace_bytes */
     PA_ERR_BUFFER_TOO_SMALL = 8,   /* a host output array is too short */
     PA_ERR_CUDA = 9,               /* a CUDA runtime call or launch failed */
-    PA_ERR_INTERNAL = 10           /* unexpected host failure (e.g. host memory exhausted) */
+    PA_ERR_INTERNAL = 10,          /* unexpected host failure (e.g. host memory exhausted) */
+    PA_ERR_SEQ_SWAPPED = 11        /* the sequence's blocks are swapped out (pa_seq_swap_out) */
 } pa_status;
 
 typedef enum pa_dtype { PA_F32 = 0, PA_BF16 = 1 } pa_dtype;
@@ -202,6 +203,30 @@ pa_status pa_decode_launch_info(int32_t num_seqs, int32_t num_q_heads, int32_t n
 pa_status pa_decode_set_ctas_per_sm(int32_t ctas);
 
 /*
+ * Swap a preempted sequence's blocks out to a block store and back
+ * (data.6616ai.com "PagedAttention 之外": KV swapped to CPU memory under
+ * memory pressure and restored to resume).
+ *
+ * pa_swap_out: for i < num, store[i] = pool[blocks[i]] over the whole block
+ * (every KV head, all block_size slots, all of head_dim), K and V.
+ * pa_swap_in:  for i < num, pool[blocks[i]] = store[i].  Bit-exact.
+ * The stores are [num][num_kv_heads][block_size][head_dim] in the pools'
+ * dtype and may be pinned host memory (cudaHostAlloc / pinned tensors): the
+ * kernels read or write it directly over the host link, with no device
+ * staging.  blocks (int32 [num]) must be device-accessible (device memory or
+ * pinned host memory).  Use the ids pa_seq_swap_out / pa_seq_swap_in return,
+ * enqueued in that order on the stream.  A block id outside [0, num_blocks)
+ * sets PA_DEV_BAD_BLOCK_ID in *dev_status (if not NULL) and that block is
+ * skipped.  Blocks of one call must be distinct for pa_swap_in.  num <= 65535.
+ */
+pa_status pa_swap_out(const void* k_pool, const void* v_pool, const int32_t* blocks, int32_t num, void* k_store,
+                      void* v_store, int32_t num_kv_heads, int32_t head_dim, int32_t block_size, int32_t num_blocks,
+                      pa_dtype dtype, int32_t* dev_status, void* stream);
+pa_status pa_swap_in(const void* k_store, const void* v_store, const int32_t* blocks, int32_t num, void* k_pool,
+                     void* v_pool, int32_t num_kv_heads, int32_t head_dim, int32_t block_size, int32_t num_blocks,
+                     pa_dtype dtype, int32_t* dev_status, void* stream);
+
+/*
  * Paged prefill (chunked causal) attention, bf16.
  *
  * "Q32: vLLM PagedAttention 原理" follow-up 3 (FlashAttention loads the KV
@@ -271,7 +296,7 @@ typedef struct pa_alloc_stats_t {
     int32_t used_blocks;   /* blocks with refcount > 0 */
     int32_t shared_blocks; /* blocks with refcount > 1 */
     int32_t num_seqs;
-    int64_t tokens;        /* sum of the live sequences' lengths */
+    int64_t tokens;        /* sum of the sequences' lengths (swapped-out ones included) */
     int64_t slots;         /* used_blocks * block_size */
     int64_t cow_copies;    /* copy-on-write pairs emitted since creation */
 } pa_alloc_stats_t;
@@ -305,6 +330,29 @@ pa_status pa_seq_len(const pa_allocator* a, int64_t seq_id, int32_t* len_out);
  */
 pa_status pa_export_tables(const pa_allocator* a, const int64_t* seq_ids, int32_t n, int32_t max_blocks_per_seq,
                            int32_t* tables_out, int32_t* lens_out);
+/*
+ * Swap-out of a preempted sequence (data.6616ai.com "PagedAttention 之外":
+ * when memory runs short the scheduler swaps a request's KV out to CPU memory
+ * and swaps it back in to resume; "可能的追问": low-priority requests' KV is
+ * moved to the CPU, then restored).
+ *
+ * pa_seq_swap_out writes the sequence's block table (physical ids in logical
+ * order, *n_out of them, cap at most) to blocks_out and then drops the
+ * sequence's references as pa_seq_free does (a block whose refcount reaches 0
+ * returns to the back of the free list).  The sequence keeps its id and length
+ * but holds no blocks: append, fork, block_table and export_tables on it
+ * return PA_ERR_SEQ_SWAPPED until pa_seq_swap_in.  The caller copies those
+ * blocks out (pa_swap_out) on the stream before anything that may reuse them.
+ *
+ * pa_seq_swap_in takes ceil(len / block_size) fresh blocks from the free list
+ * (refcount 1 each, so a block that was shared before the swap-out comes back
+ * private), makes them the sequence's table and writes them to blocks_out;
+ * the caller copies the saved contents in (pa_swap_in).  PA_ERR_OUT_OF_BLOCKS
+ * or PA_ERR_BUFFER_TOO_SMALL leave the state unchanged (*n_out still says how
+ * many blocks are needed); PA_ERR_INVALID_ARG if the sequence is not swapped.
+ */
+pa_status pa_seq_swap_out(pa_allocator* a, int64_t seq_id, int32_t* blocks_out, int32_t cap, int32_t* n_out);
+pa_status pa_seq_swap_in(pa_allocator* a, int64_t seq_id, int32_t* blocks_out, int32_t cap, int32_t* n_out);
 /* Refcount of a block, or -1 if the id is out of range. */
 int32_t pa_block_refcount(const pa_allocator* a, int32_t block);
 pa_status pa_alloc_stats(const pa_allocator* a, pa_alloc_stats_t* out);

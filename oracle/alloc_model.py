@@ -31,6 +31,12 @@ follows, stated here so the model can be checked by eye):
   reference per block and returning blocks that reach zero.
 * A batch append processes its sequence ids in the order given.
 * Every call is all-or-nothing: on failure the state is unchanged.
+* Swap-out of a preempted sequence (data.6616ai.com "PagedAttention 之外":
+  KV swapped to CPU memory when memory is short, restored to resume):
+  swap-out reports the table and then drops the sequence's references as
+  free does, keeping its id and length; the sequence then takes no appends,
+  forks or table reads.  Swap-in takes ceil(len / bs) fresh blocks from the
+  front of the free list (refcount 1 each), which become its table.
 """
 from __future__ import annotations
 
@@ -58,6 +64,10 @@ class RefcountLimit(AllocError):
     code = "refcount_limit"
 
 
+class SeqSwapped(AllocError):
+    code = "seq_swapped"
+
+
 class RefAllocator:
     def __init__(self, num_blocks, block_size, free_order=None, max_refcount=0):
         if free_order is None:
@@ -71,6 +81,7 @@ class RefAllocator:
         self.ref = [0] * self.num_blocks
         self.tables = {}
         self.lens = {}
+        self.swapped = set()
         self.cow_copies = 0
 
     # -- helpers -----------------------------------------------------------
@@ -115,10 +126,15 @@ class RefAllocator:
         self.tables[sid] = []
         self.lens[sid] = 0
 
-    def append(self, sid, n_tokens):
-        """Append n_tokens to one sequence; returns (slots, cow_pairs)."""
+    def _live(self, sid):
         if sid not in self.tables:
             raise NoSuchSeq()
+        if sid in self.swapped:
+            raise SeqSwapped()
+
+    def append(self, sid, n_tokens):
+        """Append n_tokens to one sequence; returns (slots, cow_pairs)."""
+        self._live(sid)
 
         def run():
             slots, pairs = [], []
@@ -131,8 +147,7 @@ class RefAllocator:
     def append_batch(self, sids):
         """One token for each id, in order; returns (slots, cow_pairs)."""
         for sid in sids:
-            if sid not in self.tables:
-                raise NoSuchSeq()
+            self._live(sid)
 
         def run():
             slots, pairs = [], []
@@ -143,8 +158,7 @@ class RefAllocator:
         return self._transaction(run)
 
     def fork(self, parent, child):
-        if parent not in self.tables:
-            raise NoSuchSeq()
+        self._live(parent)
         if child in self.tables:
             raise SeqExists()
         table = self.tables[parent]
@@ -166,8 +180,35 @@ class RefAllocator:
                 self.free.append(b)
         del self.tables[sid]
         del self.lens[sid]
+        self.swapped.discard(sid)
+
+    def swap_out(self, sid):
+        """Drop the sequence's blocks (as free does) but keep it; returns the table to copy out."""
+        self._live(sid)
+        table = self.tables[sid]
+        for b in table:
+            self.ref[b] -= 1
+            if self.ref[b] == 0:
+                self.free.append(b)
+        self.tables[sid] = []
+        self.swapped.add(sid)
+        return list(table)
+
+    def swap_in(self, sid):
+        """Fresh private blocks for a swapped-out sequence; returns them (its new table)."""
+        if sid not in self.tables:
+            raise NoSuchSeq()
+        if sid not in self.swapped:
+            raise AllocError()
+        need = -(-self.lens[sid] // self.block_size)
+        if need > len(self.free):
+            raise OutOfBlocks()
+        self.tables[sid] = [self._take() for _ in range(need)]
+        self.swapped.discard(sid)
+        return list(self.tables[sid])
 
     def table(self, sid):
+        self._live(sid)
         return list(self.tables[sid])
 
     def length(self, sid):

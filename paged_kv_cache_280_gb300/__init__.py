@@ -28,6 +28,7 @@ STATUS_NAMES = {
     0: "PA_OK", 1: "PA_ERR_INVALID_ARG", 2: "PA_ERR_UNSUPPORTED", 3: "PA_ERR_OUT_OF_BLOCKS",
     4: "PA_ERR_NO_SUCH_SEQ", 5: "PA_ERR_SEQ_EXISTS", 6: "PA_ERR_REFCOUNT_LIMIT",
     7: "PA_ERR_WORKSPACE_TOO_SMALL", 8: "PA_ERR_BUFFER_TOO_SMALL", 9: "PA_ERR_CUDA", 10: "PA_ERR_INTERNAL",
+    11: "PA_ERR_SEQ_SWAPPED",
 }
 
 
@@ -58,6 +59,10 @@ _SIGS = {
     "pa_decode_attention_static": (_i32, [_vp, _vp, _vp, _vp, _vp, _i32, _vp, _i32, _i32, _i32, _i32, _i32, _i32,
                                           _i32, _f32, _i32, _i32, _vp, _vp]),
     "pa_decode_launch_info": (_i32, [_i32, _i32, _i32, _i32, _i32, _i32, _i32, _pi32, _pi32, _pi32, _pi32]),
+    "pa_seq_swap_out": (_i32, [_vp, _i64, _vp, _i32, _pi32]),
+    "pa_seq_swap_in": (_i32, [_vp, _i64, _vp, _i32, _pi32]),
+    "pa_swap_out": (_i32, [_vp, _vp, _vp, _i32, _vp, _vp, _i32, _i32, _i32, _i32, _i32, _vp, _vp]),
+    "pa_swap_in": (_i32, [_vp, _vp, _vp, _i32, _vp, _vp, _i32, _i32, _i32, _i32, _i32, _vp, _vp]),
     "pa_prefill_attention": (_i32, [_vp, _vp, _vp, _vp, _vp, _i32, _vp, _vp, _i32, _i32, _i32, _i32, _i32, _i32,
                                     _i32, _i32, ctypes.c_float, _i32, _vp, _vp]),
     "pa_decode_set_ctas_per_sm": (_i32, [_i32]),
@@ -117,6 +122,17 @@ def _dev_ptr(t, name: str) -> int:
         return None
     if not t.is_cuda:
         raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    return t.data_ptr()
+
+
+def _acc_ptr(t, name: str) -> int:
+    """Pointer to a tensor the GPU can address: CUDA memory or pinned host memory."""
+    if t is None:
+        return None
+    if not (t.is_cuda or t.is_pinned()):
+        raise ValueError(f"{name} must be a CUDA tensor or pinned host memory")
     if not t.is_contiguous():
         raise ValueError(f"{name} must be contiguous")
     return t.data_ptr()
@@ -196,6 +212,25 @@ def pa_decode_launch_info(num_seqs, num_q_heads, num_kv_heads, head_dim, block_s
                                    dtype, *[ctypes.byref(v) for v in vals]),
         "pa_decode_launch_info")
     return tuple(int(v.value) for v in vals)
+
+
+def pa_swap_out(k_pool, v_pool, blocks, k_store, v_store, status=None, stream=None):
+    """store[i] = pool[blocks[i]] (whole blocks, K and V).  Stores [n][Hkv][bs][D] and blocks int32 [n] may be
+    CUDA tensors or pinned host tensors."""
+    nb, hkv, bs, d = k_pool.shape
+    _ok(_lib.pa_swap_out(_dev_ptr(k_pool, "k_pool"), _dev_ptr(v_pool, "v_pool"), _acc_ptr(blocks, "blocks"),
+                         blocks.shape[0], _acc_ptr(k_store, "k_store"), _acc_ptr(v_store, "v_store"), hkv, d, bs, nb,
+                         _dtype_code(k_pool), _dev_ptr(status, "status"), _stream(stream)),
+        "pa_swap_out")
+
+
+def pa_swap_in(k_store, v_store, blocks, k_pool, v_pool, status=None, stream=None):
+    """pool[blocks[i]] = store[i] (whole blocks, K and V); the inverse of pa_swap_out."""
+    nb, hkv, bs, d = k_pool.shape
+    _ok(_lib.pa_swap_in(_acc_ptr(k_store, "k_store"), _acc_ptr(v_store, "v_store"), _acc_ptr(blocks, "blocks"),
+                        blocks.shape[0], _dev_ptr(k_pool, "k_pool"), _dev_ptr(v_pool, "v_pool"), hkv, d, bs, nb,
+                        _dtype_code(k_pool), _dev_ptr(status, "status"), _stream(stream)),
+        "pa_swap_in")
 
 
 def pa_prefill_attention(out, q, k_pool, v_pool, block_tables, seq_lens, cu_q_lens, max_q_len, scale, status=None,
@@ -300,6 +335,24 @@ class Allocator:
 
     def free_seq(self, seq_id: int) -> None:
         _ok(_lib.pa_seq_free(self._h, seq_id), "pa_seq_free")
+
+    def swap_out(self, seq_id: int):
+        """Release the sequence's blocks for a swap-out; returns their ids (int32, logical order) to copy out."""
+        np = _np()
+        n = _i32(0)
+        cap = self.length(seq_id) // self.block_size + 1
+        out = np.empty(max(1, cap), np.int32)
+        _ok(_lib.pa_seq_swap_out(self._h, seq_id, out.ctypes.data, cap, ctypes.byref(n)), "pa_seq_swap_out")
+        return out[: n.value]
+
+    def swap_in(self, seq_id: int):
+        """Give a swapped-out sequence fresh blocks; returns their ids (int32, logical order) to copy back into."""
+        np = _np()
+        n = _i32(0)
+        cap = self.length(seq_id) // self.block_size + 1
+        out = np.empty(max(1, cap), np.int32)
+        _ok(_lib.pa_seq_swap_in(self._h, seq_id, out.ctypes.data, cap, ctypes.byref(n)), "pa_seq_swap_in")
+        return out[: n.value]
 
     def length(self, seq_id: int) -> int:
         n = _i32(0)

@@ -22,6 +22,7 @@ namespace {
 struct Sequence {
     std::vector<int32_t> table;  // logical block -> physical block
     int32_t len = 0;             // tokens written
+    bool swapped = false;        // blocks released to the host by pa_seq_swap_out; len kept
     // dry-run state of the current pa_append_batch call (valid while mark
     // equals the allocator's batch epoch)
     uint64_t mark = 0;
@@ -158,6 +159,7 @@ pa_status pa_seq_append(pa_allocator* a, int64_t seq_id, int32_t n_tokens, int64
     auto it = a->seqs.find(seq_id);
     if (it == a->seqs.end()) return PA_ERR_NO_SUCH_SEQ;
     Sequence& s = it->second;
+    if (s.swapped) return PA_ERR_SEQ_SWAPPED;
     if ((int64_t)s.len + n_tokens > INT32_MAX) return PA_ERR_INVALID_ARG;
     int32_t tail_refs = s.table.empty() ? 0 : a->refcount[s.table.back()];
     if (a->demand(s, n_tokens, tail_refs) > a->free_count) return PA_ERR_OUT_OF_BLOCKS;
@@ -184,6 +186,7 @@ pa_status pa_append_batch(pa_allocator* a, const int64_t* seq_ids, int32_t n, in
         auto it = a->seqs.find(seq_ids[i]);
         if (it == a->seqs.end()) return PA_ERR_NO_SUCH_SEQ;
         Sequence* s = &it->second;
+        if (s->swapped) return PA_ERR_SEQ_SWAPPED;
         a->batch[i] = s;
         if (s->mark != ep) {
             s->mark = ep;
@@ -220,6 +223,7 @@ pa_status pa_seq_fork(pa_allocator* a, int64_t parent, int64_t child) {
     PA_GUARD_BEGIN
     auto it = a->seqs.find(parent);
     if (it == a->seqs.end()) return PA_ERR_NO_SUCH_SEQ;
+    if (it->second.swapped) return PA_ERR_SEQ_SWAPPED;
     if (a->seqs.count(child)) return PA_ERR_SEQ_EXISTS;
     if (a->max_refcount > 0)
         for (int32_t b : it->second.table)
@@ -243,11 +247,50 @@ pa_status pa_seq_free(pa_allocator* a, int64_t seq_id) {
     PA_GUARD_END
 }
 
+pa_status pa_seq_swap_out(pa_allocator* a, int64_t seq_id, int32_t* blocks_out, int32_t cap, int32_t* n_out) {
+    if (!a || !n_out || cap < 0 || (cap > 0 && !blocks_out)) return PA_ERR_INVALID_ARG;
+    PA_GUARD_BEGIN
+    auto it = a->seqs.find(seq_id);
+    if (it == a->seqs.end()) return PA_ERR_NO_SUCH_SEQ;
+    Sequence& s = it->second;
+    if (s.swapped) return PA_ERR_SEQ_SWAPPED;
+    *n_out = (int32_t)s.table.size();
+    if ((int32_t)s.table.size() > cap) return PA_ERR_BUFFER_TOO_SMALL;
+    std::copy(s.table.begin(), s.table.end(), blocks_out);
+    // the sequence's references go, as in pa_seq_free; its length stays
+    for (int32_t b : s.table)
+        if (--a->refcount[b] == 0) a->push_free(b);
+    s.table.clear();
+    s.swapped = true;
+    return PA_OK;
+    PA_GUARD_END
+}
+
+pa_status pa_seq_swap_in(pa_allocator* a, int64_t seq_id, int32_t* blocks_out, int32_t cap, int32_t* n_out) {
+    if (!a || !n_out || cap < 0 || (cap > 0 && !blocks_out)) return PA_ERR_INVALID_ARG;
+    PA_GUARD_BEGIN
+    auto it = a->seqs.find(seq_id);
+    if (it == a->seqs.end()) return PA_ERR_NO_SUCH_SEQ;
+    Sequence& s = it->second;
+    if (!s.swapped) return PA_ERR_INVALID_ARG;
+    const int32_t need = (int32_t)(((int64_t)s.len + a->block_size - 1) / a->block_size);
+    *n_out = need;
+    if (need > cap) return PA_ERR_BUFFER_TOO_SMALL;
+    if (need > a->free_count) return PA_ERR_OUT_OF_BLOCKS;
+    s.table.reserve(need);  // may throw before any state changes
+    for (int32_t i = 0; i < need; ++i) s.table.push_back(a->pop_free());
+    std::copy(s.table.begin(), s.table.end(), blocks_out);
+    s.swapped = false;
+    return PA_OK;
+    PA_GUARD_END
+}
+
 pa_status pa_seq_block_table(const pa_allocator* a, int64_t seq_id, int32_t* out, int32_t cap, int32_t* n_out) {
     if (!a || !n_out || cap < 0 || (cap > 0 && !out)) return PA_ERR_INVALID_ARG;
     PA_GUARD_BEGIN
     auto it = a->seqs.find(seq_id);
     if (it == a->seqs.end()) return PA_ERR_NO_SUCH_SEQ;
+    if (it->second.swapped) return PA_ERR_SEQ_SWAPPED;
     const auto& t = it->second.table;
     *n_out = (int32_t)t.size();
     if ((int32_t)t.size() > cap) return PA_ERR_BUFFER_TOO_SMALL;
@@ -274,6 +317,7 @@ pa_status pa_export_tables(const pa_allocator* a, const int64_t* seq_ids, int32_
     for (int32_t i = 0; i < n; ++i) {
         auto it = a->seqs.find(seq_ids[i]);
         if (it == a->seqs.end()) return PA_ERR_NO_SUCH_SEQ;
+        if (it->second.swapped) return PA_ERR_SEQ_SWAPPED;
         if ((int32_t)it->second.table.size() > max_blocks_per_seq) return PA_ERR_BUFFER_TOO_SMALL;
     }
     for (int32_t i = 0; i < n; ++i) {
@@ -328,6 +372,7 @@ const char* pa_status_str(pa_status s) {
         case PA_ERR_BUFFER_TOO_SMALL: return "output buffer too small";
         case PA_ERR_CUDA: return "CUDA error";
         case PA_ERR_INTERNAL: return "internal error";
+        case PA_ERR_SEQ_SWAPPED: return "sequence is swapped out";
     }
     return "unknown status";
 }

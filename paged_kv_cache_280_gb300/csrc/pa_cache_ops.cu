@@ -62,6 +62,38 @@ __global__ void __launch_bounds__(256) copy_blocks_kernel(uint4* k_pool, uint4* 
     }
 }
 
+// Swap-out / swap-in of whole blocks between the pools and a block store
+// [n][Hkv][block_size][head_dim] that may live in pinned host memory (written
+// and read over NVLink-C2C by these kernels, no staging copy).  blockIdx.y
+// selects the block, blockIdx.x a slice of it.
+template <bool kOut>
+__global__ void __launch_bounds__(256) swap_blocks_kernel(uint4* k_pool, uint4* v_pool, const int32_t* __restrict__ blocks,
+                                                          uint4* k_store, uint4* v_store, int64_t block_chunks,
+                                                          int32_t num_blocks, int32_t* status) {
+    const int32_t i = blockIdx.y;
+    const int32_t b = blocks[i];
+    if (b < 0 || b >= num_blocks) {
+        if (threadIdx.x == 0 && blockIdx.x == 0) flag_status(status, PA_DEV_BAD_BLOCK_ID);
+        return;
+    }
+    uint4* kp = k_pool + (int64_t)b * block_chunks;
+    uint4* vp = v_pool + (int64_t)b * block_chunks;
+    uint4* ks = k_store + (int64_t)i * block_chunks;
+    uint4* vs = v_store + (int64_t)i * block_chunks;
+    for (int64_t c = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; c < block_chunks;
+         c += (int64_t)gridDim.x * blockDim.x) {
+        if (kOut) {
+            const uint4 a = kp[c], v = vp[c];
+            ks[c] = a;
+            vs[c] = v;
+        } else {
+            const uint4 a = ks[c], v = vs[c];
+            kp[c] = a;
+            vp[c] = v;
+        }
+    }
+}
+
 static int sm_count_of_current_device() {
     int dev = 0, n = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return 0;
@@ -127,4 +159,54 @@ extern "C" pa_status pa_copy_blocks(void* k_pool, void* v_pool, const int32_t* s
         static_cast<uint4*>(k_pool), static_cast<uint4*>(v_pool), src_dst_pairs, num_pairs, block_chunks, num_blocks,
         dev_status);
     return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+}
+
+namespace pa {
+
+static pa_status swap_blocks(bool out, void* k_pool, void* v_pool, const int32_t* blocks, int32_t n, void* k_store,
+                             void* v_store, int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
+                             int32_t num_blocks, pa_dtype dtype, int32_t* dev_status, void* stream) {
+    if (n < 0 || num_kv_heads <= 0 || num_blocks <= 0) return PA_ERR_INVALID_ARG;
+    if (dtype != PA_F32 && dtype != PA_BF16) return PA_ERR_UNSUPPORTED;
+    if (!shape_ok(head_dim, block_size)) return PA_ERR_UNSUPPORTED;
+    if (n == 0) return PA_OK;
+    if (n > 65535) return PA_ERR_UNSUPPORTED;  // one grid row per block
+    if (!k_pool || !v_pool || !blocks || !k_store || !v_store) return PA_ERR_INVALID_ARG;
+    if (!aligned16(k_pool) || !aligned16(v_pool) || !aligned16(k_store) || !aligned16(v_store) ||
+        (reinterpret_cast<uintptr_t>(blocks) & 3u) || (reinterpret_cast<uintptr_t>(dev_status) & 3u))
+        return PA_ERR_INVALID_ARG;
+    const int elem = dtype == PA_F32 ? 4 : 2;
+    const int64_t block_chunks = (int64_t)num_kv_heads * block_size * head_dim * elem / 16;
+    int64_t slices = (block_chunks + 256 * 4 - 1) / (256 * 4);  // ~4 chunks per thread
+    if (slices < 1) slices = 1;
+    if (slices > 1024) slices = 1024;
+    dim3 grid((unsigned)slices, (unsigned)n);
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (out)
+        swap_blocks_kernel<true><<<grid, 256, 0, st>>>(static_cast<uint4*>(k_pool), static_cast<uint4*>(v_pool), blocks,
+                                                       static_cast<uint4*>(k_store), static_cast<uint4*>(v_store),
+                                                       block_chunks, num_blocks, dev_status);
+    else
+        swap_blocks_kernel<false><<<grid, 256, 0, st>>>(static_cast<uint4*>(k_pool), static_cast<uint4*>(v_pool),
+                                                        blocks, static_cast<uint4*>(k_store),
+                                                        static_cast<uint4*>(v_store), block_chunks, num_blocks,
+                                                        dev_status);
+    return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+}
+
+}  // namespace pa
+
+extern "C" pa_status pa_swap_out(const void* k_pool, const void* v_pool, const int32_t* blocks, int32_t num,
+                                 void* k_store, void* v_store, int32_t num_kv_heads, int32_t head_dim,
+                                 int32_t block_size, int32_t num_blocks, pa_dtype dtype, int32_t* dev_status,
+                                 void* stream) {
+    return pa::swap_blocks(true, const_cast<void*>(k_pool), const_cast<void*>(v_pool), blocks, num, k_store, v_store,
+                           num_kv_heads, head_dim, block_size, num_blocks, dtype, dev_status, stream);
+}
+
+extern "C" pa_status pa_swap_in(const void* k_store, const void* v_store, const int32_t* blocks, int32_t num,
+                                void* k_pool, void* v_pool, int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
+                                int32_t num_blocks, pa_dtype dtype, int32_t* dev_status, void* stream) {
+    return pa::swap_blocks(false, k_pool, v_pool, blocks, num, const_cast<void*>(k_store), const_cast<void*>(v_store),
+                           num_kv_heads, head_dim, block_size, num_blocks, dtype, dev_status, stream);
 }

@@ -33,7 +33,7 @@ def test_library_exports_every_declared_symbol():
 def test_status_strings():
     import paged_kv_cache_280_gb300 as pa
 
-    for code in range(0, 11):
+    for code in range(0, 12):
         assert pa._lib.pa_status_str(code)
 
 
@@ -50,3 +50,15 @@ def test_prefill_host_checks_run_before_any_launch():
     bad = list(args(pa.PA_BF16, 128, 16))
     bad[1] = ctypes.c_void_p((1 << 20) + 2)  # misaligned q
     assert pa._lib.pa_prefill_attention(*bad) == 1  # PA_ERR_INVALID_ARG
+
+
+def test_swap_host_checks_run_before_any_launch():
+    import paged_kv_cache_280_gb300 as pa
+
+    fake = ctypes.c_void_p(1 << 20)
+    ok_args = [fake, fake, fake, 4, fake, fake, 8, 128, 16, 100, pa.PA_BF16, None, None]
+    assert pa._lib.pa_swap_out(*ok_args[:8], 12, *ok_args[9:]) == 2  # block_size 12: unsupported
+    bad = list(ok_args)
+    bad[4] = ctypes.c_void_p((1 << 20) + 8)  # misaligned store
+    assert pa._lib.pa_swap_out(*bad) == 1
+    assert pa._lib.pa_swap_in(*ok_args[:3], 0, *ok_args[4:]) == 0  # nothing to copy

@@ -185,3 +185,29 @@ def test_random_traces_keep_invariants(seed):
         except OutOfBlocks:
             pass
         _check_invariants(a)
+
+
+def test_model_swap_golden_trace():
+    """The same hand-computed swap trace on the reference model."""
+    from oracle.alloc_model import AllocError, OutOfBlocks, RefAllocator, SeqSwapped
+
+    a = RefAllocator(6, 4, free_order=[5, 2, 0, 4, 1, 3])
+    a.create(0)
+    a.append(0, 6)
+    a.fork(0, 1)
+    assert a.swap_out(1) == [5, 2]
+    assert (a.refcount(5), a.refcount(2)) == (1, 1) and a.free_list() == [0, 4, 1, 3]
+    with pytest.raises(SeqSwapped):
+        a.append(1, 1)
+    assert a.swap_out(0) == [5, 2] and a.free_list() == [0, 4, 1, 3, 5, 2]
+    assert a.swap_in(1) == [0, 4] and a.length(1) == 6 and a.refcount(0) == 1
+    slots, pairs = a.append(1, 1)
+    assert slots == [18] and pairs == []
+    with pytest.raises(AllocError):
+        a.swap_in(1)
+    a.create(2)
+    a.append(2, 16)
+    with pytest.raises(OutOfBlocks):
+        a.swap_in(0)
+    a.free_seq(0)
+    assert a.stats()["num_seqs"] == 2

@@ -216,3 +216,106 @@ def test_outputs_in_place():
         a.append_batch([0], slots_out=np.zeros(4, np.int32))
     with pytest.raises(ValueError):
         a.export_tables([0], 5, tables_out=np.zeros((1, 4), np.int32), lens_out=np.zeros(1, np.int32))
+
+
+@pytest.mark.parametrize("seed", range(6))
+def test_random_traces_with_swaps_match_model(seed):
+    """Appends, forks, frees and swap-outs/ins interleaved: the library and the model stay identical."""
+    from oracle.alloc_model import SeqSwapped
+
+    rnd = random.Random(5000 + seed)
+    nb, bs = rnd.choice([24, 64]), rnd.choice([4, 16])
+    order = rnd.sample(range(nb), nb)
+    lib = pa.Allocator(nb, bs, free_order=order)
+    ref = RefAllocator(nb, bs, free_order=order)
+    live, swapped, nxt = [], set(), 0
+
+    def same_error(fn_lib, fn_ref):
+        try:
+            r = fn_ref()
+        except OutOfBlocks:
+            with pytest.raises(pa.PAError) as e:
+                fn_lib()
+            assert e.value.name == "PA_ERR_OUT_OF_BLOCKS"
+            return None
+        return r, fn_lib()
+
+    for _ in range(400):
+        op = rnd.random()
+        active = [s for s in live if s not in swapped]
+        if op < 0.1 or not live:
+            lib.create(nxt)
+            ref.create(nxt)
+            live.append(nxt)
+            nxt += 1
+        elif op < 0.45 and active:
+            sid, n = rnd.choice(active), rnd.randint(0, 20)
+            out = same_error(lambda: lib.append(sid, n), lambda: ref.append(sid, n))
+            if out:
+                (rs, rp), (ls, lp) = out
+                assert ls.tolist() == rs and [tuple(x) for x in lp.tolist()] == rp
+        elif op < 0.6 and active:
+            parent = rnd.choice(active)
+            lib.fork(parent, nxt)
+            ref.fork(parent, nxt)
+            live.append(nxt)
+            nxt += 1
+        elif op < 0.75 and active:
+            sid = rnd.choice(active)
+            assert lib.swap_out(sid).tolist() == ref.swap_out(sid)
+            swapped.add(sid)
+        elif op < 0.9 and swapped:
+            sid = rnd.choice(sorted(swapped))
+            out = same_error(lambda: lib.swap_in(sid), lambda: ref.swap_in(sid))
+            if out:
+                assert out[1].tolist() == out[0]
+                swapped.discard(sid)
+        elif live:
+            sid = rnd.choice(live)
+            lib.free_seq(sid)
+            ref.free_seq(sid)
+            live.remove(sid)
+            swapped.discard(sid)
+        # state: free list, refcounts, tables of active sequences, lengths of all
+        assert lib.free_list() == ref.free_list()
+        for b in range(nb):
+            assert lib.refcount(b) == ref.refcount(b)
+        for sid in live:
+            assert lib.length(sid) == ref.length(sid)
+            if sid in swapped:
+                with pytest.raises(pa.PAError) as e:
+                    lib.table(sid)
+                assert e.value.name == "PA_ERR_SEQ_SWAPPED"
+                with pytest.raises(SeqSwapped):
+                    ref.table(sid)
+            else:
+                assert lib.table(sid) == ref.table(sid)
+
+
+def test_swap_golden_trace():
+    """A hand-computed swap trace: shared blocks survive a sharer's swap-out; swap-in takes fresh private blocks."""
+    a = pa.Allocator(6, 4, free_order=[5, 2, 0, 4, 1, 3])
+    a.create(0)
+    a.append(0, 6)                       # blocks 5, 2 (slots 20..23, 8..9)
+    a.fork(0, 1)                         # refcounts 5:2, 2:2
+    assert a.swap_out(1).tolist() == [5, 2]
+    assert (a.refcount(5), a.refcount(2)) == (1, 1) and a.free_list() == [0, 4, 1, 3]
+    with pytest.raises(pa.PAError) as e:
+        a.append(1, 1)
+    assert e.value.name == "PA_ERR_SEQ_SWAPPED"
+    assert a.swap_out(0).tolist() == [5, 2]
+    assert a.free_list() == [0, 4, 1, 3, 5, 2]
+    assert a.swap_in(1).tolist() == [0, 4] and a.length(1) == 6
+    assert a.table(1) == [0, 4] and a.refcount(0) == 1 and a.free_list() == [1, 3, 5, 2]
+    s, p = a.append(1, 1)                # private tail: written in place, no copy
+    assert s.tolist() == [4 * 4 + 2] and p.size == 0
+    with pytest.raises(pa.PAError) as e:
+        a.swap_in(1)                     # not swapped out
+    assert e.value.name == "PA_ERR_INVALID_ARG"
+    a.create(2)
+    a.append(2, 16)                      # takes 1, 3, 5, 2: the pool is full
+    with pytest.raises(pa.PAError) as e:
+        a.swap_in(0)
+    assert e.value.name == "PA_ERR_OUT_OF_BLOCKS" and a.length(0) == 6
+    a.free_seq(0)                        # a swapped-out sequence can be dropped
+    assert a.stats()["num_seqs"] == 2
