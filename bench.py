@@ -693,6 +693,114 @@ def prefill_cpu_baseline(w, q, k_pool, v_pool, kn, vn, slots, tables, lens, L, P
 
 
 # ---------------------------------------------------------------------------
+# swap path: preempt the whole decode batch to pinned host memory and back
+# ---------------------------------------------------------------------------
+SWAP_METRIC = "paged KV swap-out + swap-in GB/s (% of the pinned-memcpy link rate) at 1 GPU"
+
+
+def run_swap(args, rank, world, local_rank):
+    import torch
+
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    dist = dist_init(world, "nccl")
+    import paged_kv_cache_280_gb300 as pa
+
+    K, Wm = args.steps, args.warmup
+    w = build_workload("gqa4_b64", rank, world, extra_steps=0)
+    Hkv, D, bs = w.num_kv_heads, w.head_dim, w.block_size
+    lib = pa.Allocator(w.num_blocks, bs, free_order=w.free_order())
+    ids = populate(lib, w)
+    nblk = sum(-(-lib.length(s) // bs) for s in ids)
+    block_bytes = 2 * Hkv * bs * D * w.elem_bytes  # K and V
+    moved = nblk * block_bytes  # each way
+    dk = torch.from_numpy(w.pool_values("k").view(np.int16)).view(torch.bfloat16).to(dev)
+    dv = torch.from_numpy(w.pool_values("v").view(np.int16)).view(torch.bfloat16).to(dev)
+    kst = torch.empty((nblk, Hkv, bs, D), dtype=torch.bfloat16, pin_memory=True)
+    vst = torch.empty((nblk, Hkv, bs, D), dtype=torch.bfloat16, pin_memory=True)
+    bl_out = torch.empty(nblk, dtype=torch.int32, pin_memory=True)
+    bl_in = torch.empty(nblk, dtype=torch.int32, pin_memory=True)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def one_step(ev=None):
+        pos = 0
+        for s_ in ids:  # host: release every sequence's blocks, recording them in batch order
+            b = lib.swap_out(s_)
+            bl_out.numpy()[pos:pos + len(b)] = b
+            pos += len(b)
+        if ev:
+            ev[0].record(stream)
+        pa.pa_swap_out(dk, dv, bl_out, kst, vst, status=status, stream=stream)
+        if ev:
+            ev[1].record(stream)
+        pos = 0
+        for s_ in ids:  # host: fresh blocks for every sequence
+            b = lib.swap_in(s_)
+            bl_in.numpy()[pos:pos + len(b)] = b
+            pos += len(b)
+        if ev:
+            ev[2].record(stream)
+        pa.pa_swap_in(kst, vst, bl_in, dk, dv, status=status, stream=stream)
+        if ev:
+            ev[3].record(stream)
+        stream.synchronize()  # the pinned block lists are rewritten by the next step
+
+    for _ in range(Wm):
+        one_step()
+    evs = [tuple(torch.cuda.Event(enable_timing=True) for _ in range(4)) for _ in range(K)]
+    clocks = ClockSampler(local_rank)
+    clocks.start()
+    for i in range(K):
+        one_step(evs[i])
+    clocks.stop()
+    if status.item():
+        raise SystemExit(f"device status word {int(status.item()):#x}")
+    out_ms = [e[0].elapsed_time(e[1]) for e in evs]
+    in_ms = [e[2].elapsed_time(e[3]) for e in evs]
+    # the link's reference rate: copy-engine memcpy of the same bytes, device <-> pinned host
+    dbuf = torch.empty(moved, dtype=torch.uint8, device=dev)
+    hbuf = torch.empty(moved, dtype=torch.uint8, pin_memory=True)
+    rates = {}
+    for name, fn in (("d2h", lambda: hbuf.copy_(dbuf, non_blocking=True)),
+                     ("h2d", lambda: dbuf.copy_(hbuf, non_blocking=True))):
+        ts = []
+        for _ in range(Wm + K):
+            a, b_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            fn()
+            b_.record(stream)
+            stream.synchronize()
+            ts.append(a.elapsed_time(b_))
+        rates[name] = moved / (statistics.median(ts[Wm:]) / 1e3) / 1e9
+    total_s = reduce_max((sum(out_ms) + sum(in_ms)) / 1e3, dist, dev)
+    value = reduce_sum(2.0 * moved * K, dist, dev) / total_s / 1e9
+    out_gbs = moved / (statistics.median(out_ms) / 1e3) / 1e9
+    in_gbs = moved / (statistics.median(in_ms) / 1e3) / 1e9
+    peak = (rates["d2h"] + rates["h2d"]) / 2
+    line = {
+        "metric": SWAP_METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": K, "warmup": Wm,
+        "ms_per_step": total_s * 1e3 / K, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16", "data": f"synthetic, seeded: {WORKLOADS['gqa4_b64']}; every sequence swapped out and back",
+        "config": {"workload": "swap_gqa4_b64_all", "blocks": nblk, "bytes_each_way": moved,
+                   "swap_out_ms_median": statistics.median(out_ms), "swap_in_ms_median": statistics.median(in_ms),
+                   "swap_out_gbs": out_gbs, "swap_in_gbs": in_gbs, "memcpy_d2h_gbs": rates["d2h"],
+                   "memcpy_h2d_gbs": rates["h2d"],
+                   "store": "pinned host memory, written and read by the kernels over the host link"},
+        "roofline": {"bound": "host-link", "achieved": value, "peak": peak, "unit": "GB/s", "frac": value / peak,
+                     "peak_source": "copy-engine memcpy between device and pinned host memory, same bytes, same run",
+                     "kernel": "pa_swap_out + pa_swap_in (swap_blocks_kernel)", "traffic": None},
+        "gpu_launches": 2 * K,
+        "clocks": clocks.summary(),
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if dist:
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+# ---------------------------------------------------------------------------
 # reference arm: the oracle on the host cores, same metric and workload
 # ---------------------------------------------------------------------------
 def run_reference(args, rank, world):
@@ -799,14 +907,22 @@ def main(argv=None):
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--ref-seqs-per-step", type=int, default=16)
-    ap.add_argument("--path", choices=["decode", "prefill"], default="decode",
-                    help="decode: the decode step (the headline); prefill: prompt prefill of the sampling prompts")
+    ap.add_argument("--path", choices=["decode", "prefill", "swap"], default="decode",
+                    help="decode: the decode step (the headline); prefill: prompt prefill of the sampling prompts; "
+                         "swap: the whole decode batch swapped to pinned host memory and back")
     ap.add_argument("--prompts", type=int, default=16, help="prefill path: prompts per step (at most 16)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         raise SystemExit("at least 3 warm-up steps")
     rank, world, local_rank = dist_env()
-    if args.path == "prefill":
+    if args.path == "swap":
+        if args.impl == "reference":
+            if rank == 0:
+                print(json.dumps({"impl": "reference", "unavailable": "the swap path is plain block copies; the "
+                                  "oracle has no arithmetic to time for it"}), flush=True)
+        else:
+            run_swap(args, rank, world, local_rank)
+    elif args.path == "prefill":
         if args.impl == "reference":
             run_prefill_reference(args, rank, world)
         else:
