@@ -292,7 +292,7 @@ typedef struct pa_allocator pa_allocator;
 typedef struct pa_alloc_stats_t {
     int32_t num_blocks;
     int32_t block_size;
-    int32_t free_blocks;
+    int32_t free_blocks;   /* on the free list (cached evictable blocks are not) */
     int32_t used_blocks;   /* blocks with refcount > 0 */
     int32_t shared_blocks; /* blocks with refcount > 1 */
     int32_t num_seqs;
@@ -353,6 +353,35 @@ pa_status pa_export_tables(const pa_allocator* a, const int64_t* seq_ids, int32_
  */
 pa_status pa_seq_swap_out(pa_allocator* a, int64_t seq_id, int32_t* blocks_out, int32_t cap, int32_t* n_out);
 pa_status pa_seq_swap_in(pa_allocator* a, int64_t seq_id, int32_t* blocks_out, int32_t cap, int32_t* n_out);
+/*
+ * Prefix caching (data.6616ai.com, paging's second dividend: the KV blocks of
+ * a prefix common to many requests, such as a system prompt, are cached and
+ * reused across requests, so prefill computes only what is not cached).
+ *
+ * A full block is identified by the token ids of the whole prefix it
+ * completes (a chained 64-bit hash, every hit verified against the stored
+ * tokens and parent hash).  pa_seq_cache_prefix registers the first
+ * n_tokens / block_size full blocks of a sequence whose first n_tokens KV
+ * entries hold `tokens` (call it once they are written); a prefix already in
+ * the cache keeps its entry.  pa_seq_create_cached creates a sequence whose
+ * table starts with the longest run of cached blocks matching `tokens`, at
+ * most (n_tokens - 1) / block_size of them so that at least one prompt token
+ * is left to compute, each taking one more reference; *n_cached_out gets the
+ * tokens covered (a multiple of block_size), which become the sequence's
+ * length.  The caller appends the other n_tokens - *n_cached_out tokens and
+ * prefills them as one chunk (pa_prefill_attention).
+ *
+ * A cached block whose last reference goes is not freed: it stays cached and
+ * evictable.  An allocation takes the free list first, then evicts the cached
+ * block released longest ago, which also leaves the cache.  Without
+ * registered blocks the allocator behaves exactly as described above.
+ * pa_prefix_cache_stats reports the cached and the evictable block counts
+ * (either pointer may be NULL).
+ */
+pa_status pa_seq_create_cached(pa_allocator* a, int64_t seq_id, const int32_t* tokens, int32_t n_tokens,
+                               int32_t* n_cached_out);
+pa_status pa_seq_cache_prefix(pa_allocator* a, int64_t seq_id, const int32_t* tokens, int32_t n_tokens);
+pa_status pa_prefix_cache_stats(const pa_allocator* a, int32_t* cached_blocks, int32_t* evictable_blocks);
 /* Refcount of a block, or -1 if the id is out of range. */
 int32_t pa_block_refcount(const pa_allocator* a, int32_t block);
 pa_status pa_alloc_stats(const pa_allocator* a, pa_alloc_stats_t* out);

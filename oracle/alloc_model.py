@@ -37,11 +37,23 @@ follows, stated here so the model can be checked by eye):
   free does, keeping its id and length; the sequence then takes no appends,
   forks or table reads.  Swap-in takes ceil(len / bs) fresh blocks from the
   front of the free list (refcount 1 each), which become its table.
+* Prefix caching (data.6616ai.com, paging's second dividend: blocks of a
+  prefix common to many requests are cached and reused, so prefill computes
+  only the rest): a full block is identified by the token ids of the whole
+  prefix it completes.  Registering a sequence's first n tokens records its
+  first n // bs full blocks (a prefix already recorded, or a block already
+  recorded, keeps its entry).  A new sequence created from a prompt of n
+  tokens starts with the longest run of recorded blocks matching the prompt,
+  at most (n - 1) // bs of them (one prompt token is always left to compute),
+  each taking one more reference; its length is the tokens they cover.  A
+  recorded block whose last reference goes is not freed but kept, evictable;
+  allocation takes the free list first, then evicts the block released
+  longest ago (dropping its record).
 """
 from __future__ import annotations
 
 import copy
-from collections import deque
+from collections import OrderedDict, deque
 
 
 class AllocError(Exception):
@@ -83,15 +95,29 @@ class RefAllocator:
         self.lens = {}
         self.swapped = set()
         self.cow_copies = 0
+        self.prefix = {}               # token prefix (tuple) -> the block completing it
+        self.cached = {}               # recorded block -> its prefix
+        self.evictable = OrderedDict()  # recorded blocks with no reference, oldest release first
 
     # -- helpers -----------------------------------------------------------
     def _take(self):
-        if not self.free:
+        if self.free:
+            b = self.free.popleft()
+        elif self.evictable:
+            b, _ = self.evictable.popitem(last=False)
+            del self.prefix[self.cached.pop(b)]
+        else:
             raise OutOfBlocks()
-        b = self.free.popleft()
         assert self.ref[b] == 0
         self.ref[b] = 1
         return b
+
+    def _release(self, b):
+        """The block's last reference went: a recorded block stays recorded (evictable), others are freed."""
+        if b in self.cached:
+            self.evictable[b] = True
+        else:
+            self.free.append(b)
 
     def _append_one(self, sid, slots, pairs):
         table = self.tables[sid]
@@ -112,11 +138,12 @@ class RefAllocator:
 
     def _transaction(self, fn):
         saved = (copy.copy(self.free), list(self.ref), {k: list(v) for k, v in self.tables.items()},
-                 dict(self.lens), self.cow_copies)
+                 dict(self.lens), self.cow_copies, dict(self.prefix), dict(self.cached), OrderedDict(self.evictable))
         try:
             return fn()
         except AllocError:
-            self.free, self.ref, self.tables, self.lens, self.cow_copies = saved
+            (self.free, self.ref, self.tables, self.lens, self.cow_copies, self.prefix, self.cached,
+             self.evictable) = saved
             raise
 
     # -- API ---------------------------------------------------------------
@@ -177,7 +204,7 @@ class RefAllocator:
         for b in self.tables[sid]:
             self.ref[b] -= 1
             if self.ref[b] == 0:
-                self.free.append(b)
+                self._release(b)
         del self.tables[sid]
         del self.lens[sid]
         self.swapped.discard(sid)
@@ -189,7 +216,7 @@ class RefAllocator:
         for b in table:
             self.ref[b] -= 1
             if self.ref[b] == 0:
-                self.free.append(b)
+                self._release(b)
         self.tables[sid] = []
         self.swapped.add(sid)
         return list(table)
@@ -201,11 +228,44 @@ class RefAllocator:
         if sid not in self.swapped:
             raise AllocError()
         need = -(-self.lens[sid] // self.block_size)
-        if need > len(self.free):
+        if need > len(self.free) + len(self.evictable):
             raise OutOfBlocks()
         self.tables[sid] = [self._take() for _ in range(need)]
         self.swapped.discard(sid)
         return list(self.tables[sid])
+
+    def create_cached(self, sid, tokens):
+        """Create a sequence starting with the longest recorded run of full blocks of ``tokens``."""
+        if sid in self.tables:
+            raise SeqExists()
+        bs, tokens = self.block_size, [int(t) for t in tokens]
+        hits = []
+        for i in range(max(0, (len(tokens) - 1) // bs)):
+            b = self.prefix.get(tuple(tokens[: (i + 1) * bs]))
+            if b is None or (self.max_refcount > 0 and self.ref[b] + 1 > self.max_refcount):
+                break
+            hits.append(b)
+        for b in hits:
+            self.evictable.pop(b, None)
+            self.ref[b] += 1
+        self.tables[sid] = hits
+        self.lens[sid] = len(hits) * bs
+        return len(hits) * bs
+
+    def cache_prefix(self, sid, tokens):
+        """Record the full blocks of the sequence's first len(tokens) tokens."""
+        self._live(sid)
+        bs, tokens = self.block_size, [int(t) for t in tokens]
+        if len(tokens) > self.lens[sid]:
+            raise AllocError()
+        for i in range(len(tokens) // bs):
+            key, b = tuple(tokens[: (i + 1) * bs]), self.tables[sid][i]
+            if key not in self.prefix and b not in self.cached:
+                self.prefix[key] = b
+                self.cached[b] = key
+
+    def prefix_cache_stats(self):
+        return {"cached_blocks": len(self.cached), "evictable_blocks": len(self.evictable)}
 
     def table(self, sid):
         self._live(sid)

@@ -59,6 +59,9 @@ _SIGS = {
     "pa_decode_attention_static": (_i32, [_vp, _vp, _vp, _vp, _vp, _i32, _vp, _i32, _i32, _i32, _i32, _i32, _i32,
                                           _i32, _f32, _i32, _i32, _vp, _vp]),
     "pa_decode_launch_info": (_i32, [_i32, _i32, _i32, _i32, _i32, _i32, _i32, _pi32, _pi32, _pi32, _pi32]),
+    "pa_seq_create_cached": (_i32, [_vp, _i64, _vp, _i32, _pi32]),
+    "pa_seq_cache_prefix": (_i32, [_vp, _i64, _vp, _i32]),
+    "pa_prefix_cache_stats": (_i32, [_vp, _pi32, _pi32]),
     "pa_seq_swap_out": (_i32, [_vp, _i64, _vp, _i32, _pi32]),
     "pa_seq_swap_in": (_i32, [_vp, _i64, _vp, _i32, _pi32]),
     "pa_swap_out": (_i32, [_vp, _vp, _vp, _i32, _vp, _vp, _i32, _i32, _i32, _i32, _i32, _vp, _vp]),
@@ -335,6 +338,28 @@ class Allocator:
 
     def free_seq(self, seq_id: int) -> None:
         _ok(_lib.pa_seq_free(self._h, seq_id), "pa_seq_free")
+
+    def create_cached(self, seq_id: int, tokens) -> int:
+        """Create a sequence starting with the longest cached run of full blocks of ``tokens``; returns the
+        tokens covered (the new sequence's length)."""
+        np = _np()
+        tk = np.ascontiguousarray(np.asarray(tokens, dtype=np.int32))
+        n = _i32(0)
+        _ok(_lib.pa_seq_create_cached(self._h, seq_id, tk.ctypes.data if tk.size else None, tk.size, ctypes.byref(n)),
+            "pa_seq_create_cached")
+        return int(n.value)
+
+    def cache_prefix(self, seq_id: int, tokens) -> None:
+        """Register the full blocks of the sequence's first len(tokens) tokens in the prefix cache."""
+        np = _np()
+        tk = np.ascontiguousarray(np.asarray(tokens, dtype=np.int32))
+        _ok(_lib.pa_seq_cache_prefix(self._h, seq_id, tk.ctypes.data if tk.size else None, tk.size),
+            "pa_seq_cache_prefix")
+
+    def prefix_cache_stats(self) -> dict:
+        c, e = _i32(0), _i32(0)
+        _ok(_lib.pa_prefix_cache_stats(self._h, ctypes.byref(c), ctypes.byref(e)), "pa_prefix_cache_stats")
+        return {"cached_blocks": int(c.value), "evictable_blocks": int(e.value)}
 
     def swap_out(self, seq_id: int):
         """Release the sequence's blocks for a swap-out; returns their ids (int32, logical order) to copy out."""

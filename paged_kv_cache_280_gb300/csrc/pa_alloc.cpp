@@ -11,6 +11,7 @@
 // call leaves the allocator unchanged.
 #include <algorithm>
 #include <cstring>
+#include <list>
 #include <new>
 #include <unordered_map>
 #include <vector>
@@ -30,6 +31,30 @@ struct Sequence {
     bool dry_private = false;  // the tail is known to have refcount 1 at this point
 };
 
+// A full block registered in the prefix cache: the chained hash of the token
+// prefix it completes, and (to verify a hit exactly) its parent's hash and its
+// own token ids.
+struct CachedBlock {
+    uint64_t hash = 0, parent = 0;
+    std::vector<int32_t> tokens;
+    bool evictable = false;            // refcount 0: kept for reuse until its slot is needed
+    std::list<int32_t>::iterator lru;  // position in the evictable list while evictable
+};
+
+// Chained hash of block i: mixes the previous block's hash with this block's
+// token ids (splitmix64 finaliser as the mixing step).
+uint64_t mix64(uint64_t x) {
+    x += 0x9E3779B97F4A7C15ull;
+    x = (x ^ (x >> 30)) * 0xBF58476D1CE4E5B9ull;
+    x = (x ^ (x >> 27)) * 0x94D049BB133111EBull;
+    return x ^ (x >> 31);
+}
+uint64_t block_hash(uint64_t parent, const int32_t* tokens, int32_t n) {
+    uint64_t h = mix64(parent ^ 0x5052454649584B56ull);
+    for (int32_t i = 0; i < n; ++i) h = mix64(h ^ (uint64_t)(uint32_t)tokens[i]);
+    return h;
+}
+
 }  // namespace
 
 struct pa_allocator {
@@ -48,16 +73,43 @@ struct pa_allocator {
     std::vector<int32_t> drop_count;  // copies of a shared block planned in this call
     std::vector<Sequence*> batch;     // the call's sequences, in order
 
+    // prefix cache: chained hash -> block, registered blocks, evictable ones oldest first
+    std::unordered_map<uint64_t, int32_t> prefix_map;
+    std::unordered_map<int32_t, CachedBlock> cached;
+    std::list<int32_t> lru;
+
+    // Blocks an allocation may take: the free list, then evictable cached blocks.
+    int64_t available() const { return (int64_t)free_count + (int64_t)lru.size(); }
     int32_t pop_free() {
-        int32_t b = ring[head];
-        head = (head + 1) % num_blocks;
-        --free_count;
+        int32_t b;
+        if (free_count > 0) {
+            b = ring[head];
+            head = (head + 1) % num_blocks;
+            --free_count;
+        } else {  // evict the least recently released cached block
+            b = lru.front();
+            lru.pop_front();
+            auto it = cached.find(b);
+            prefix_map.erase(it->second.hash);
+            cached.erase(it);
+        }
         refcount[b] = 1;
         return b;
     }
     void push_free(int32_t b) {
         ring[(head + free_count) % num_blocks] = b;
         ++free_count;
+    }
+    // A block whose last reference went: a cached block stays cached (evictable,
+    // most recent at the back); any other returns to the back of the free list.
+    void release(int32_t b) {
+        auto it = cached.find(b);
+        if (it == cached.end()) {
+            push_free(b);
+            return;
+        }
+        it->second.evictable = true;
+        it->second.lru = lru.insert(lru.end(), b);
     }
     // Blocks one append of n tokens to `s` will take: the blocks newly
     // started plus one copy if the first token lands in a shared tail.
@@ -162,7 +214,7 @@ pa_status pa_seq_append(pa_allocator* a, int64_t seq_id, int32_t n_tokens, int64
     if (s.swapped) return PA_ERR_SEQ_SWAPPED;
     if ((int64_t)s.len + n_tokens > INT32_MAX) return PA_ERR_INVALID_ARG;
     int32_t tail_refs = s.table.empty() ? 0 : a->refcount[s.table.back()];
-    if (a->demand(s, n_tokens, tail_refs) > a->free_count) return PA_ERR_OUT_OF_BLOCKS;
+    if (a->demand(s, n_tokens, tail_refs) > a->available()) return PA_ERR_OUT_OF_BLOCKS;
     s.table.reserve((s.len + n_tokens + a->block_size - 1) / a->block_size);
     *n_cow_out = 0;
     for (int32_t i = 0; i < n_tokens; ++i) a->append_one(s, &slots_out[i], cow_pairs_out, n_cow_out);
@@ -209,7 +261,7 @@ pa_status pa_append_batch(pa_allocator* a, const int64_t* seq_ids, int32_t n, in
         if (s->dry_len == INT32_MAX) return PA_ERR_INVALID_ARG;
         ++s->dry_len;
     }
-    if (need > a->free_count) return PA_ERR_OUT_OF_BLOCKS;
+    if (need > a->available()) return PA_ERR_OUT_OF_BLOCKS;
     for (int32_t i = 0; i < n; ++i)  // so that the mutating loop below cannot fail half-way
         a->batch[i]->table.reserve((a->batch[i]->dry_len + bs - 1) / bs);
     *n_cow_out = 0;
@@ -241,7 +293,7 @@ pa_status pa_seq_free(pa_allocator* a, int64_t seq_id) {
     auto it = a->seqs.find(seq_id);
     if (it == a->seqs.end()) return PA_ERR_NO_SUCH_SEQ;
     for (int32_t b : it->second.table)
-        if (--a->refcount[b] == 0) a->push_free(b);
+        if (--a->refcount[b] == 0) a->release(b);
     a->seqs.erase(it);
     return PA_OK;
     PA_GUARD_END
@@ -259,7 +311,7 @@ pa_status pa_seq_swap_out(pa_allocator* a, int64_t seq_id, int32_t* blocks_out, 
     std::copy(s.table.begin(), s.table.end(), blocks_out);
     // the sequence's references go, as in pa_seq_free; its length stays
     for (int32_t b : s.table)
-        if (--a->refcount[b] == 0) a->push_free(b);
+        if (--a->refcount[b] == 0) a->release(b);
     s.table.clear();
     s.swapped = true;
     return PA_OK;
@@ -276,13 +328,99 @@ pa_status pa_seq_swap_in(pa_allocator* a, int64_t seq_id, int32_t* blocks_out, i
     const int32_t need = (int32_t)(((int64_t)s.len + a->block_size - 1) / a->block_size);
     *n_out = need;
     if (need > cap) return PA_ERR_BUFFER_TOO_SMALL;
-    if (need > a->free_count) return PA_ERR_OUT_OF_BLOCKS;
+    if (need > a->available()) return PA_ERR_OUT_OF_BLOCKS;
     s.table.reserve(need);  // may throw before any state changes
     for (int32_t i = 0; i < need; ++i) s.table.push_back(a->pop_free());
     std::copy(s.table.begin(), s.table.end(), blocks_out);
     s.swapped = false;
     return PA_OK;
     PA_GUARD_END
+}
+
+pa_status pa_seq_create_cached(pa_allocator* a, int64_t seq_id, const int32_t* tokens, int32_t n_tokens,
+                               int32_t* n_cached_out) {
+    if (!a || n_tokens < 0 || (n_tokens > 0 && !tokens) || !n_cached_out) return PA_ERR_INVALID_ARG;
+    PA_GUARD_BEGIN
+    if (a->seqs.count(seq_id)) return PA_ERR_SEQ_EXISTS;
+    const int32_t bs = a->block_size;
+    // the longest run of cached full blocks; at least one prompt token is left to compute
+    const int32_t max_blocks = n_tokens > 0 ? (n_tokens - 1) / bs : 0;
+    std::vector<int32_t> hits;
+    hits.reserve(max_blocks);
+    uint64_t h = 0;
+    for (int32_t i = 0; i < max_blocks; ++i) {
+        const int32_t* tk = tokens + (size_t)i * bs;
+        const uint64_t hi = block_hash(h, tk, bs);
+        auto m = a->prefix_map.find(hi);
+        if (m == a->prefix_map.end()) break;
+        const CachedBlock& cb = a->cached.find(m->second)->second;
+        if (cb.parent != h || !std::equal(cb.tokens.begin(), cb.tokens.end(), tk)) break;
+        if (a->max_refcount > 0 && a->refcount[m->second] + 1 > a->max_refcount) break;
+        hits.push_back(m->second);
+        h = hi;
+    }
+    Sequence s;
+    s.table = hits;  // may throw before any state changes
+    s.len = (int32_t)hits.size() * bs;
+    auto it = a->seqs.emplace(seq_id, std::move(s)).first;
+    for (int32_t b : it->second.table) {
+        CachedBlock& cb = a->cached.find(b)->second;
+        if (cb.evictable) {  // revived: leaves the evictable list
+            a->lru.erase(cb.lru);
+            cb.evictable = false;
+        }
+        ++a->refcount[b];
+    }
+    *n_cached_out = it->second.len;
+    return PA_OK;
+    PA_GUARD_END
+}
+
+pa_status pa_seq_cache_prefix(pa_allocator* a, int64_t seq_id, const int32_t* tokens, int32_t n_tokens) {
+    if (!a || n_tokens < 0 || (n_tokens > 0 && !tokens)) return PA_ERR_INVALID_ARG;
+    PA_GUARD_BEGIN
+    auto it = a->seqs.find(seq_id);
+    if (it == a->seqs.end()) return PA_ERR_NO_SUCH_SEQ;
+    const Sequence& s = it->second;
+    if (s.swapped) return PA_ERR_SEQ_SWAPPED;
+    if (n_tokens > s.len) return PA_ERR_INVALID_ARG;
+    const int32_t bs = a->block_size, nfull = n_tokens / bs;
+    // register the full blocks in order; a prefix already cached (the same block,
+    // or another block with the same content) keeps its entry
+    std::vector<CachedBlock> fresh;
+    std::vector<int32_t> fresh_blocks;
+    uint64_t h = 0;
+    for (int32_t i = 0; i < nfull; ++i) {
+        const int32_t* tk = tokens + (size_t)i * bs;
+        const uint64_t hi = block_hash(h, tk, bs);
+        const int32_t b = s.table[i];
+        bool dup = a->prefix_map.count(hi) || a->cached.count(b);
+        for (const CachedBlock& f : fresh) dup = dup || f.hash == hi;
+        if (!dup && std::find(fresh_blocks.begin(), fresh_blocks.end(), b) == fresh_blocks.end()) {
+            CachedBlock cb;
+            cb.hash = hi;
+            cb.parent = h;
+            cb.tokens.assign(tk, tk + bs);
+            fresh.push_back(std::move(cb));
+            fresh_blocks.push_back(b);
+        }
+        h = hi;
+    }
+    a->prefix_map.reserve(a->prefix_map.size() + fresh.size());  // may throw before any state changes
+    a->cached.reserve(a->cached.size() + fresh.size());
+    for (size_t k = 0; k < fresh.size(); ++k) {
+        a->prefix_map.emplace(fresh[k].hash, fresh_blocks[k]);
+        a->cached.emplace(fresh_blocks[k], std::move(fresh[k]));
+    }
+    return PA_OK;
+    PA_GUARD_END
+}
+
+pa_status pa_prefix_cache_stats(const pa_allocator* a, int32_t* cached_blocks, int32_t* evictable_blocks) {
+    if (!a) return PA_ERR_INVALID_ARG;
+    if (cached_blocks) *cached_blocks = (int32_t)a->cached.size();
+    if (evictable_blocks) *evictable_blocks = (int32_t)a->lru.size();
+    return PA_OK;
 }
 
 pa_status pa_seq_block_table(const pa_allocator* a, int64_t seq_id, int32_t* out, int32_t cap, int32_t* n_out) {
@@ -342,7 +480,7 @@ pa_status pa_alloc_stats(const pa_allocator* a, pa_alloc_stats_t* out) {
     out->num_blocks = a->num_blocks;
     out->block_size = a->block_size;
     out->free_blocks = a->free_count;
-    out->used_blocks = a->num_blocks - a->free_count;
+    for (int32_t r : a->refcount) out->used_blocks += (r > 0);
     for (int32_t r : a->refcount) out->shared_blocks += (r > 1);
     out->num_seqs = (int32_t)a->seqs.size();
     for (const auto& kv : a->seqs) out->tokens += kv.second.len;
