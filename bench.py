@@ -518,9 +518,11 @@ def prefill_setup(rank: int, prompts: int):
     return W.scaled(base, prompts=P, num_blocks=nb, seed=base.seed + 7919 * rank), P, L
 
 
-def prefill_flops(L: int, P: int, hq: int, d: int) -> float:
-    """Causal attention of P fresh L-token prompts: 4 d Hq sum_p (p + 1) per prompt (QK^T and PV)."""
-    return 4.0 * d * hq * P * L * (L + 1) / 2
+def prefill_flops(L: int, P: int, hq: int, d: int, chunk: int = 0) -> float:
+    """Causal attention of the last ``chunk`` tokens (all L by default) of P prompts of L tokens:
+    4 d Hq (p + 1) per chunk token at position p (QK^T and PV)."""
+    chunk = chunk or L
+    return 4.0 * d * hq * P * sum(L - chunk + i + 1 for i in range(chunk))
 
 
 def run_prefill(args, rank, world, local_rank):
@@ -536,16 +538,33 @@ def run_prefill(args, rank, world, local_rank):
     K_e2e = min(K, args.e2e_steps)
     w, P, L = prefill_setup(rank, args.prompts)
     Hq, Hkv, D, bs = w.num_q_heads, w.num_kv_heads, w.head_dim, w.block_size
-    T = P * L
     lib = pa.Allocator(w.num_blocks, bs, free_order=w.free_order())
     slots = []
-    for p_ in range(P):
-        lib.create(p_)
-        slots.append(lib.append(p_, L)[0])
+    if args.prefix_cached:
+        # The prompts share their first L - 7 tokens (a system prompt).  An earlier request
+        # computed that prefix and registered it (untimed): each prompt now reuses those
+        # blocks and computes only its own 7-token tail, attending to all L tokens.
+        chunk = 7
+        shared = [10_000 + t for t in range(L - chunk)]
+        toks = [shared + [100 * p_ + t for t in range(chunk)] for p_ in range(P)]
+        lib.create(1 << 40)
+        lib.append(1 << 40, L)
+        lib.cache_prefix(1 << 40, toks[0])
+        lib.free_seq(1 << 40)  # the prefix blocks stay cached
+        for p_ in range(P):
+            if lib.create_cached(p_, toks[p_]) != L - chunk:
+                raise SystemExit("prefix cache missed")
+            slots.append(lib.append(p_, chunk)[0])
+    else:
+        chunk = L
+        for p_ in range(P):
+            lib.create(p_)
+            slots.append(lib.append(p_, L)[0])
+    T = P * chunk
     slots = np.concatenate(slots)
     max_blocks = -(-L // bs)
     tables, lens = lib.export_tables(range(P), max_blocks)
-    cu = np.arange(0, T + 1, L, dtype=np.int32)
+    cu = np.arange(0, T + 1, chunk, dtype=np.int32)
     q = synth.normal(synth.stream_seed(w.seed, 4242), T * Hq * D, "bf16").reshape(T, Hq, D)
     kn, vn = w.prompt_tokens("k")[:T], w.prompt_tokens("v")[:T]
 
@@ -571,7 +590,7 @@ def run_prefill(args, rank, world, local_rank):
         pa.pa_reshape_and_cache(kk, vv, dk, dv, ss, status=status, stream=stream)
 
     def prefill(qq, tt, ll, cc):
-        pa.pa_prefill_attention(out, qq, dk, dv, tt, ll, cc, L, w.scale, status=status, stream=stream)
+        pa.pa_prefill_attention(out, qq, dk, dv, tt, ll, cc, chunk, w.scale, status=status, stream=stream)
 
     for _ in range(Wm):
         flush_l2()
@@ -600,8 +619,8 @@ def run_prefill(args, rank, world, local_rank):
     step_ms = [a.elapsed_time(c) for a, b, c in ev]
     pf_ms = [b.elapsed_time(c) for a, b, c in ev]
     total_s = reduce_max(sum(step_ms) / 1e3, dist, dev)
-    value = reduce_sum(float(T * K), dist, dev) / total_s
-    flops = prefill_flops(L, P, Hq, D)
+    value = reduce_sum(float(P * L * K), dist, dev) / total_s  # prompt tokens made ready (cached ones included)
+    flops = prefill_flops(L, P, Hq, D, chunk)
     peak, peak_kind = measured_tensor_peak()
     achieved = flops / (statistics.mean(pf_ms) / 1e3) / 1e12
 
@@ -641,15 +660,17 @@ def run_prefill(args, rank, world, local_rank):
         stream.synchronize()
         e2e_s += time.perf_counter() - t0
     e2e_total = reduce_max(e2e_s, dist, dev)
-    e2e_value = reduce_sum(float(T * K_e2e), dist, dev) / e2e_total if K_e2e else None
+    e2e_value = reduce_sum(float(P * L * K_e2e), dist, dev) / e2e_total if K_e2e else None
 
     line = {
         "metric": PREFILL_METRIC, "value": value, "unit": PREFILL_UNIT, "n_gpus": world, "steps": K, "warmup": Wm,
         "ms_per_step": total_s * 1e3 / K, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "bf16", "data": f"synthetic, seeded: {P} prompts of {L} tokens (the parallel-sampling workload's "
                                  f"prompts), 32 query / 8 KV heads, d 128, 16-token blocks scattered",
-        "config": {"workload": f"prefill_p{P}_len{L}_hq{Hq}_hkv{Hkv}_d{D}_bs{bs}_bf16", "prompts": P,
-                   "prompt_len": L, "num_q_heads": Hq, "num_kv_heads": Hkv, "head_dim": D, "block_size": bs,
+        "config": {"workload": f"prefill_p{P}_len{L}_hq{Hq}_hkv{Hkv}_d{D}_bs{bs}_bf16"
+                               + ("_prefix_cached" if args.prefix_cached else ""), "prompts": P,
+                   "prompt_len": L, "computed_tokens_per_prompt": chunk, "cached_tokens_per_prompt": L - chunk,
+                   "num_q_heads": Hq, "num_kv_heads": Hkv, "head_dim": D, "block_size": bs,
                    "flops_per_step": flops, "l2": "flushed between timed steps (512 MiB write, then a 256 MiB read)",
                    "prefill_ms_median": statistics.median(pf_ms), "prefill_ms_min": min(pf_ms),
                    "path": "mma.sync m16n8k16, TMA ring"},
@@ -663,7 +684,7 @@ def run_prefill(args, rank, world, local_rank):
         "clocks": clocks.summary(),
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        line["cpu_baseline"] = prefill_cpu_baseline(w, q, k_host, v_host, kn, vn, slots, tables, lens, L, P,
+        line["cpu_baseline"] = prefill_cpu_baseline(w, q, k_host, v_host, kn, vn, slots, tables, lens, L, P, chunk,
                                                     args.cpu_seconds)
     if rank == 0:
         print(json.dumps(line), flush=True)
@@ -672,14 +693,14 @@ def run_prefill(args, rank, world, local_rank):
         dist.destroy_process_group()
 
 
-def prefill_cpu_baseline(w, q, k_pool, v_pool, kn, vn, slots, tables, lens, L, P, seconds):
-    """The oracle's prefill over whole prompts (one per host thread at a time), bounded by ``seconds``."""
+def prefill_cpu_baseline(w, q, k_pool, v_pool, kn, vn, slots, tables, lens, L, P, chunk, seconds):
+    """The oracle's prefill of the same chunks (one prompt per host thread at a time), bounded by ``seconds``."""
     import oracle
 
     k_pool, v_pool = k_pool.copy(), v_pool.copy()
     oracle.reshape_and_cache(kn, vn, k_pool, v_pool, slots)
     threads = os.cpu_count() or 1
-    cu = np.arange(0, P * L + 1, L, dtype=np.int32)
+    cu = np.arange(0, P * chunk + 1, chunk, dtype=np.int32)
     done, t0 = 0, time.perf_counter()
     while done < P:
         seqs = list(range(done, min(P, done + threads)))
@@ -689,7 +710,8 @@ def prefill_cpu_baseline(w, q, k_pool, v_pool, kn, vn, slots, tables, lens, L, P
             break
     dt = time.perf_counter() - t0
     return {"value": done * L / dt, "unit": PREFILL_UNIT, "cores": threads, "kind": "oracle",
-            "sample": f"fp64 C oracle prefill of {done} of the {P} prompts ({dt:.1f} s), one prompt per thread"}
+            "sample": f"fp64 C oracle prefill of {done} of the {P} prompts ({chunk} computed tokens each, "
+                      f"{dt:.1f} s), one prompt per thread"}
 
 
 # ---------------------------------------------------------------------------
@@ -911,6 +933,8 @@ def main(argv=None):
                     help="decode: the decode step (the headline); prefill: prompt prefill of the sampling prompts; "
                          "swap: the whole decode batch swapped to pinned host memory and back")
     ap.add_argument("--prompts", type=int, default=16, help="prefill path: prompts per step (at most 16)")
+    ap.add_argument("--prefix-cached", action="store_true",
+                    help="prefill path: the prompts share all but their last 7 tokens, already cached")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         raise SystemExit("at least 3 warm-up steps")
