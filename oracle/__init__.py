@@ -8,8 +8,9 @@ and never imports it.
 
 Parts:
   * ``pa_oracle.c``  -- fp64 decode attention (direct and split + reduce),
-    paged prefill (chunked causal) attention, the slot-mapped append and the
-    copy-on-write block copy, as element loops over host arrays.
+    paged prefill (chunked causal) attention, the slot-mapped append, the
+    copy-on-write block copy, and the FP8 (E4M3) pool's codes, append and
+    decode, as element loops over host arrays.
   * ``alloc_model``  -- a reference model of the block allocator
     (on-demand blocks, refcounted sharing, copy-on-write).
   * ``waste``        -- the memory accounting of the waste simulation on
@@ -66,6 +67,16 @@ def _open(path: str):
     lib.oracle_reshape_and_cache.argtypes = [i32, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32]
     lib.oracle_copy_blocks.restype = ctypes.c_int
     lib.oracle_copy_blocks.argtypes = [i32, vp, vp, vp, i32, i32, i32, i32, i32]
+    lib.oracle_e4m3_encode_array.restype = None
+    lib.oracle_e4m3_encode_array.argtypes = [vp, ctypes.c_int64, vp]
+    lib.oracle_e4m3_value_array.restype = None
+    lib.oracle_e4m3_value_array.argtypes = [vp, ctypes.c_int64, vp]
+    lib.oracle_reshape_and_cache_fp8.restype = ctypes.c_int
+    lib.oracle_reshape_and_cache_fp8.argtypes = [ctypes.c_int, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32,
+                                                 ctypes.c_float, ctypes.c_float]
+    lib.oracle_decode_attention_fp8.restype = ctypes.c_int
+    lib.oracle_decode_attention_fp8.argtypes = [ctypes.c_int, vp, vp, vp, ctypes.c_float, ctypes.c_float, vp, i32,
+                                                vp, i32, i32, i32, i32, i32, i32, f64, i32, i32, vp]
     lib.oracle_prefill_attention.restype = ctypes.c_int
     lib.oracle_prefill_attention.argtypes = [ctypes.c_int, vp, vp, vp, vp, i32, vp, vp, i32, i32, i32, i32,
                                              i32, i32, f64, i32, i32, vp]
@@ -166,6 +177,66 @@ def prefill_attention(q, k_pool, v_pool, block_tables, seq_lens, cu_q_lens, scal
     else:
         with ThreadPoolExecutor(threads) as ex:
             list(ex.map(run, todo))
+    return out
+
+
+def e4m3_encode(x) -> np.ndarray:
+    """fp32 values -> OCP FP8 E4M3 codes (nearest, ties to even mantissa, saturating at 448)."""
+    x = _c(np.asarray(x, np.float32))
+    out = np.empty(x.shape, np.uint8)
+    _load().oracle_e4m3_encode_array(x.ctypes.data, x.size, out.ctypes.data)
+    return out
+
+
+def e4m3_value(codes) -> np.ndarray:
+    """E4M3 codes -> their values (float64; the NaN code gives NaN)."""
+    codes = _c(np.asarray(codes, np.uint8))
+    out = np.empty(codes.shape, np.float64)
+    _load().oracle_e4m3_value_array(codes.ctypes.data, codes.size, out.ctypes.data)
+    return out
+
+
+def reshape_and_cache_fp8(k_new, v_new, k_pool, v_pool, slot_mapping, k_scale, v_scale):
+    """In-place slot-mapped append into FP8 pools (uint8 codes of x / scale)."""
+    assert k_pool.dtype == np.uint8 and k_pool.flags.c_contiguous and v_pool.flags.c_contiguous
+    k_new, v_new = _c(k_new), _c(v_new)
+    slots = _c(slot_mapping, np.int64)
+    nb, Hkv, bs, D = k_pool.shape
+    _check(_load().oracle_reshape_and_cache_fp8(_dtype_code(k_new), k_new.ctypes.data, v_new.ctypes.data,
+                                                k_pool.ctypes.data, v_pool.ctypes.data, slots.ctypes.data, len(slots),
+                                                Hkv, D, bs, nb, float(k_scale), float(v_scale)))
+
+
+def decode_attention_fp8(q, k_pool, v_pool, k_scale, v_scale, block_tables, seq_lens, scale, seqs=None, threads=1):
+    """fp64 decode attention over FP8 pools (K^ = value * k_scale, V^ = value * v_scale); out[B][Hq][D]."""
+    q = _c(q)
+    dt = _dtype_code(q)
+    k_pool, v_pool = _c(k_pool, np.uint8), _c(v_pool, np.uint8)
+    bt = _c(block_tables, np.int32)
+    lens = _c(seq_lens, np.int32)
+    B, Hq, D = q.shape
+    nb, Hkv, bs, _ = k_pool.shape
+    out = np.full((B, Hq, D), np.nan, np.float64)
+    lib = _load()
+    todo = list(range(B)) if seqs is None else sorted(set(int(s) for s in seqs))
+    ranges = [(b, b + 1) for b in todo] if threads > 1 else [(min(todo), max(todo) + 1)] if todo else []
+
+    def run(r):
+        _check(lib.oracle_decode_attention_fp8(dt, q.ctypes.data, k_pool.ctypes.data, v_pool.ctypes.data,
+                                               float(k_scale), float(v_scale), bt.ctypes.data, bt.shape[1],
+                                               lens.ctypes.data, B, Hq, Hkv, D, bs, nb, float(scale), r[0], r[1],
+                                               out.ctypes.data))
+
+    if threads <= 1:
+        for r in ranges:
+            run(r)
+    else:
+        with ThreadPoolExecutor(threads) as ex:
+            list(ex.map(run, ranges))
+    if seqs is not None:
+        keep = np.zeros(B, bool)
+        keep[todo] = True
+        out[~keep] = np.nan
     return out
 
 

@@ -336,3 +336,111 @@ int oracle_prefill_attention(int dtype, const void* q, const void* k_pool, const
     }
     return ORACLE_OK;
 }
+
+/*
+ * FP8 KV pool (an extrapolation: the pages name FP8 only among the quantisation
+ * formats the ecosystem supports, data.6616ai.com "PagedAttention 之外").
+ *
+ * Codes are OCP FP8 E4M3 (1 sign, 4 exponent bits with bias 7, 3 mantissa
+ * bits; exponent field 0 holds subnormals m * 2^-9; the all-ones exponent with
+ * mantissa 7 is NaN and there is no infinity; the largest finite magnitude is
+ * 448).  A pool holds codes of x / scale, one fp32 scale per pool (K and V):
+ * the append computes y = x / scale in fp32 and rounds y to the nearest
+ * finite E4M3 value, ties to the code with an even mantissa, magnitudes past
+ * 448 saturating to 448.  Decode reads x^ = value(code) * scale.
+ */
+double oracle_e4m3_value(uint8_t c) {
+    const int s = c >> 7, e = (c >> 3) & 15, m = c & 7;
+    if (e == 15 && m == 7) return NAN;
+    const double mag = e == 0 ? ldexp((double)m, -9) : ldexp(1.0 + m / 8.0, e - 7);
+    return s ? -mag : mag;
+}
+
+/* Round an fp32 value to E4M3 as above, by search over the 127 finite magnitudes. */
+uint8_t oracle_e4m3_encode(float y) {
+    if (isnan(y)) return 0x7F;
+    const uint8_t sign = signbit(y) ? 0x80 : 0x00;
+    const double a = fabs((double)y);
+    int best = 0;
+    for (int c = 1; c <= 0x7E; ++c) {
+        const double dc = fabs(oracle_e4m3_value((uint8_t)c) - a), db = fabs(oracle_e4m3_value((uint8_t)best) - a);
+        if (dc < db || (dc == db && (c & 1) == 0 && (best & 1) == 1)) best = c;
+    }
+    return (uint8_t)(sign | best);
+}
+
+/* Slot-mapped append into FP8 pools: pool code = encode(fp32(x / scale)) (x fp32, or bf16 bits when dtype = 1). */
+int oracle_reshape_and_cache_fp8(int dtype, const void* k_new, const void* v_new, uint8_t* k_pool,
+                                 uint8_t* v_pool, const int64_t* slots, int32_t num_tokens, int32_t num_kv_heads,
+                                 int32_t head_dim, int32_t block_size, int32_t num_blocks, float k_scale,
+                                 float v_scale) {
+    if (num_tokens < 0 || num_kv_heads <= 0 || head_dim <= 0 || block_size <= 0) return ORACLE_BAD_ARG;
+    for (int32_t i = 0; i < num_tokens; ++i) {
+        const int64_t s = slots[i];
+        if (s < 0) continue;
+        if (s >= (int64_t)num_blocks * block_size) return ORACLE_BAD_SLOT;
+        const int64_t blk = s / block_size, off = s % block_size;
+        for (int32_t h = 0; h < num_kv_heads; ++h)
+            for (int32_t d = 0; d < head_dim; ++d) {
+                const size_t src = ((size_t)i * num_kv_heads + h) * head_dim + d;
+                const size_t dst = (((size_t)blk * num_kv_heads + h) * block_size + (size_t)off) * head_dim + d;
+                k_pool[dst] = oracle_e4m3_encode((float)load_elem(dtype, k_new, src) / k_scale);
+                v_pool[dst] = oracle_e4m3_encode((float)load_elem(dtype, v_new, src) / v_scale);
+            }
+    }
+    return ORACLE_OK;
+}
+
+/* Decode attention over FP8 pools: the decode definition above with K^ = value * k_scale, V^ = value * v_scale. */
+int oracle_decode_attention_fp8(int q_dtype, const void* q, const uint8_t* k_pool, const uint8_t* v_pool,
+                                float k_scale, float v_scale, const int32_t* block_tables, int32_t max_blocks_per_seq,
+                                const int32_t* seq_lens, int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads,
+                                int32_t head_dim, int32_t block_size, int32_t num_blocks, double scale,
+                                int32_t seq_begin, int32_t seq_end, double* out) {
+    int rc = check_common(num_seqs, num_q_heads, num_kv_heads, head_dim, block_size, seq_begin, seq_end);
+    if (rc) return rc;
+    /* widen the pools exactly (code values times the scales, in double) and reuse the fp64 definition */
+    const size_t n = (size_t)num_blocks * num_kv_heads * block_size * head_dim;
+    float* kf = (float*)malloc(sizeof(float) * n);
+    float* vf = (float*)malloc(sizeof(float) * n);
+    if (!kf || !vf) {
+        free(kf); free(vf);
+        return ORACLE_NOMEM;
+    }
+    int exact = 1;
+    for (size_t i = 0; i < n; ++i) {
+        const double kv = oracle_e4m3_value(k_pool[i]) * k_scale, vv = oracle_e4m3_value(v_pool[i]) * v_scale;
+        kf[i] = (float)kv;
+        vf[i] = (float)vv;
+        exact &= ((double)kf[i] == kv || isnan(kv)) && ((double)vf[i] == vv || isnan(vv));
+    }
+    /* a code value (4 significant bits) times an fp32 scale fits fp32 exactly unless it underflows */
+    if (!exact) rc = ORACLE_BAD_ARG;
+    if (!rc && q_dtype == 0) {
+        rc = oracle_decode_attention(0, q, kf, vf, block_tables, max_blocks_per_seq, seq_lens, num_seqs,
+                                     num_q_heads, num_kv_heads, head_dim, block_size, num_blocks, scale, seq_begin,
+                                     seq_end, out);
+    } else if (!rc) {
+        /* bf16 queries widen exactly to fp32 */
+        const size_t nq = (size_t)num_seqs * num_q_heads * head_dim;
+        float* qf = (float*)malloc(sizeof(float) * nq);
+        if (!qf) rc = ORACLE_NOMEM;
+        for (size_t i = 0; !rc && i < nq; ++i) qf[i] = (float)load_elem(1, q, i);
+        if (!rc)
+            rc = oracle_decode_attention(0, qf, kf, vf, block_tables, max_blocks_per_seq, seq_lens, num_seqs,
+                                         num_q_heads, num_kv_heads, head_dim, block_size, num_blocks, scale,
+                                         seq_begin, seq_end, out);
+        free(qf);
+    }
+    free(kf);
+    free(vf);
+    return rc;
+}
+
+/* Element-wise forms for the tests: out[i] = encode(x[i]); val[i] = value(codes[i]). */
+void oracle_e4m3_encode_array(const float* x, int64_t n, uint8_t* out) {
+    for (int64_t i = 0; i < n; ++i) out[i] = oracle_e4m3_encode(x[i]);
+}
+void oracle_e4m3_value_array(const uint8_t* codes, int64_t n, double* val) {
+    for (int64_t i = 0; i < n; ++i) val[i] = oracle_e4m3_value(codes[i]);
+}

@@ -33,8 +33,13 @@ C_MUTANTS = {
                               "const size_t row = (size_t)cu_q_lens[b + 1] - 1 - (size_t)i;"),
     "prefill_not_causal": ("for (int32_t t = 0; t <= p; ++t) {\n                        double dot",
                            "for (int32_t t = 0; t < len; ++t) {\n                        double dot"),
+    "e4m3_ties_to_odd": ("(dc == db && (c & 1) == 0 && (best & 1) == 1)", "(dc == db && (c & 1) == 1 && (best & 1) == 0)"),
+    "e4m3_subnormal_scale": ("ldexp((double)m, -9)", "ldexp((double)m, -10)"),
+    "e4m3_bias_8": ("ldexp(1.0 + m / 8.0, e - 7)", "ldexp(1.0 + m / 8.0, e - 8)"),
+    "e4m3_saturates_at_416": ("for (int c = 1; c <= 0x7E; ++c) {", "for (int c = 1; c <= 0x7D; ++c) {"),
+    "fp8_v_scale_dropped": ("vv = oracle_e4m3_value(v_pool[i]) * v_scale;", "vv = oracle_e4m3_value(v_pool[i]);"),
 }
-PIN_FILES = ["test_oracle_pins.py", "test_oracle_prefill_pins.py"]
+PIN_FILES = ["test_oracle_pins.py", "test_oracle_prefill_pins.py", "test_oracle_fp8_pins.py"]
 
 
 @pytest.fixture(scope="module")
