@@ -66,7 +66,10 @@ typedef enum pa_status {
     PA_ERR_SEQ_SWAPPED = 11        /* the sequence's blocks are swapped out (pa_seq_swap_out) */
 } pa_status;
 
-typedef enum pa_dtype { PA_F32 = 0, PA_BF16 = 1 } pa_dtype;
+/* Element types.  PA_FP8_E4M3 (OCP FP8 E4M3 codes, one byte) is a pool type
+ * only: pools of that type pair with bf16 queries and outputs through the
+ * *_fp8 entry points. */
+typedef enum pa_dtype { PA_F32 = 0, PA_BF16 = 1, PA_FP8_E4M3 = 2 } pa_dtype;
 
 /* Bits of the device status word. */
 #define PA_DEV_BAD_BLOCK_ID 0x1 /* a block id outside [0, num_blocks) was read or given */
@@ -203,12 +206,42 @@ pa_status pa_decode_launch_info(int32_t num_seqs, int32_t num_q_heads, int32_t n
 pa_status pa_decode_set_ctas_per_sm(int32_t ctas);
 
 /*
+ * FP8 KV pools (an extrapolation: the pages list FP8 among the quantisation
+ * formats the ecosystem supports, data.6616ai.com "PagedAttention 之外").
+ * Pools hold OCP E4M3 codes (PA_FP8_E4M3, one byte per element, head_dim
+ * 128), one fp32 scale per pool: element x is stored as the code of
+ * fp32(x / scale), rounded to nearest (ties to even) and saturated to +-448,
+ * and read back as value(code) * scale.
+ *
+ * pa_reshape_and_cache_fp8: the slot-mapped append of pa_reshape_and_cache
+ * with that quantisation; k_new / v_new are in_dtype (bf16 or fp32)
+ * [N][Hkv][128].  The codes are bit-exact against the definition.
+ *
+ * pa_decode_attention_fp8: pa_decode_attention over FP8 pools with bf16 q
+ * and out: out = softmax(scale q . (K code values * k_scale)) (V code values
+ * * v_scale).  Same layouts, workspace (pa_decode_workspace_bytes), split
+ * modes and error reporting; CUDA-core path.  k_scale and v_scale must be
+ * finite and > 0.
+ */
+pa_status pa_reshape_and_cache_fp8(const void* k_new, const void* v_new, void* k_pool, void* v_pool,
+                                   const int64_t* slot_mapping, int32_t num_tokens, int32_t num_kv_heads,
+                                   int32_t head_dim, int32_t block_size, int32_t num_blocks, pa_dtype in_dtype,
+                                   float k_scale, float v_scale, int32_t* dev_status, void* stream);
+pa_status pa_decode_attention_fp8(void* out, const void* q, const void* k_pool, const void* v_pool, float k_scale,
+                                  float v_scale, const int32_t* block_tables, int32_t max_blocks_per_seq,
+                                  const int32_t* seq_lens, int32_t max_seq_len, int32_t num_seqs,
+                                  int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
+                                  int32_t num_blocks, float scale, int32_t partition_tokens, void* workspace,
+                                  size_t workspace_bytes, void* stream);
+
+/*
  * Swap a preempted sequence's blocks out to a block store and back
  * (data.6616ai.com "PagedAttention 之外": KV swapped to CPU memory under
  * memory pressure and restored to resume).
  *
  * pa_swap_out: for i < num, store[i] = pool[blocks[i]] over the whole block
- * (every KV head, all block_size slots, all of head_dim), K and V.
+ * (every KV head, all block_size slots, all of head_dim), K and V.  Any pool
+ * dtype, FP8 included (pa_copy_blocks likewise).
  * pa_swap_in:  for i < num, pool[blocks[i]] = store[i].  Bit-exact.
  * The stores are [num][num_kv_heads][block_size][head_dim] in the pools'
  * dtype and may be pinned host memory (cudaHostAlloc / pinned tensors): the

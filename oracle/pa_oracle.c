@@ -36,6 +36,7 @@ enum { ORACLE_OK = 0, ORACLE_BAD_ARG = -1, ORACLE_BAD_BLOCK = -2, ORACLE_BAD_SLO
 
 static double load_elem(int dtype, const void* base, size_t idx) {
     if (dtype == 0) return (double)((const float*)base)[idx];
+    if (dtype == 2) return ((const double*)base)[idx]; /* widened FP8 pools */
     uint32_t bits = (uint32_t)((const uint16_t*)base)[idx] << 16; /* bf16 -> fp32 is exact */
     float f;
     memcpy(&f, &bits, sizeof f);
@@ -66,6 +67,13 @@ static int check_common(int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_he
     return ORACLE_OK;
 }
 
+/* Decode attention with separate element types for q and for the pools. */
+static int decode_impl(int q_dtype, const void* q, int kv_dtype, const void* k_pool, const void* v_pool,
+                       const int32_t* block_tables, int32_t max_blocks_per_seq, const int32_t* seq_lens,
+                       int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
+                       int32_t block_size, int32_t num_blocks, double scale, int32_t seq_begin, int32_t seq_end,
+                       double* out);
+
 /* Decode attention for sequences [seq_begin, seq_end); writes out[b] for those b only. */
 int oracle_decode_attention(int dtype, const void* q, const void* k_pool, const void* v_pool,
                             const int32_t* block_tables, int32_t max_blocks_per_seq,
@@ -73,6 +81,15 @@ int oracle_decode_attention(int dtype, const void* q, const void* k_pool, const 
                             int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
                             int32_t num_blocks, double scale, int32_t seq_begin, int32_t seq_end,
                             double* out) {
+    return decode_impl(dtype, q, dtype, k_pool, v_pool, block_tables, max_blocks_per_seq, seq_lens, num_seqs,
+                       num_q_heads, num_kv_heads, head_dim, block_size, num_blocks, scale, seq_begin, seq_end, out);
+}
+
+static int decode_impl(int q_dtype, const void* q, int kv_dtype, const void* k_pool, const void* v_pool,
+                       const int32_t* block_tables, int32_t max_blocks_per_seq, const int32_t* seq_lens,
+                       int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
+                       int32_t block_size, int32_t num_blocks, double scale, int32_t seq_begin, int32_t seq_end,
+                       double* out) {
     int rc = check_common(num_seqs, num_q_heads, num_kv_heads, head_dim, block_size, seq_begin, seq_end);
     if (rc) return rc;
     const int32_t G = num_q_heads / num_kv_heads;
@@ -93,7 +110,7 @@ int oracle_decode_attention(int dtype, const void* q, const void* k_pool, const 
         }
         const int32_t* table = block_tables + (size_t)b * max_blocks_per_seq;
         for (int32_t g = 0; g < num_kv_heads && rc == ORACLE_OK; ++g) {
-            rc = gather_kv(dtype, k_pool, v_pool, table, len, num_kv_heads, head_dim, block_size,
+            rc = gather_kv(kv_dtype, k_pool, v_pool, table, len, num_kv_heads, head_dim, block_size,
                            num_blocks, g, K, V);
             if (rc) break;
             for (int32_t h = g * G; h < (g + 1) * G; ++h) {
@@ -102,7 +119,7 @@ int oracle_decode_attention(int dtype, const void* q, const void* k_pool, const 
                 for (int32_t t = 0; t < len; ++t) {
                     double dot = 0.0;
                     for (int32_t i = 0; i < head_dim; ++i)
-                        dot += load_elem(dtype, q, qrow + i) * K[(size_t)t * head_dim + i];
+                        dot += load_elem(q_dtype, q, qrow + i) * K[(size_t)t * head_dim + i];
                     s[t] = scale * dot;
                     if (s[t] > m) m = s[t];
                 }
@@ -399,41 +416,22 @@ int oracle_decode_attention_fp8(int q_dtype, const void* q, const uint8_t* k_poo
                                 int32_t seq_begin, int32_t seq_end, double* out) {
     int rc = check_common(num_seqs, num_q_heads, num_kv_heads, head_dim, block_size, seq_begin, seq_end);
     if (rc) return rc;
-    /* widen the pools exactly (code values times the scales, in double) and reuse the fp64 definition */
+    /* widen the pools exactly (a 4-bit code value times an fp32 scale fits a double) and reuse the definition */
     const size_t n = (size_t)num_blocks * num_kv_heads * block_size * head_dim;
-    float* kf = (float*)malloc(sizeof(float) * n);
-    float* vf = (float*)malloc(sizeof(float) * n);
-    if (!kf || !vf) {
-        free(kf); free(vf);
+    double* kd = (double*)malloc(sizeof(double) * n);
+    double* vd = (double*)malloc(sizeof(double) * n);
+    if (!kd || !vd) {
+        free(kd); free(vd);
         return ORACLE_NOMEM;
     }
-    int exact = 1;
     for (size_t i = 0; i < n; ++i) {
-        const double kv = oracle_e4m3_value(k_pool[i]) * k_scale, vv = oracle_e4m3_value(v_pool[i]) * v_scale;
-        kf[i] = (float)kv;
-        vf[i] = (float)vv;
-        exact &= ((double)kf[i] == kv || isnan(kv)) && ((double)vf[i] == vv || isnan(vv));
+        kd[i] = oracle_e4m3_value(k_pool[i]) * (double)k_scale;
+        vd[i] = oracle_e4m3_value(v_pool[i]) * (double)v_scale;
     }
-    /* a code value (4 significant bits) times an fp32 scale fits fp32 exactly unless it underflows */
-    if (!exact) rc = ORACLE_BAD_ARG;
-    if (!rc && q_dtype == 0) {
-        rc = oracle_decode_attention(0, q, kf, vf, block_tables, max_blocks_per_seq, seq_lens, num_seqs,
-                                     num_q_heads, num_kv_heads, head_dim, block_size, num_blocks, scale, seq_begin,
-                                     seq_end, out);
-    } else if (!rc) {
-        /* bf16 queries widen exactly to fp32 */
-        const size_t nq = (size_t)num_seqs * num_q_heads * head_dim;
-        float* qf = (float*)malloc(sizeof(float) * nq);
-        if (!qf) rc = ORACLE_NOMEM;
-        for (size_t i = 0; !rc && i < nq; ++i) qf[i] = (float)load_elem(1, q, i);
-        if (!rc)
-            rc = oracle_decode_attention(0, qf, kf, vf, block_tables, max_blocks_per_seq, seq_lens, num_seqs,
-                                         num_q_heads, num_kv_heads, head_dim, block_size, num_blocks, scale,
-                                         seq_begin, seq_end, out);
-        free(qf);
-    }
-    free(kf);
-    free(vf);
+    rc = decode_impl(q_dtype, q, 2, kd, vd, block_tables, max_blocks_per_seq, seq_lens, num_seqs, num_q_heads,
+                     num_kv_heads, head_dim, block_size, num_blocks, scale, seq_begin, seq_end, out);
+    free(kd);
+    free(vd);
     return rc;
 }
 

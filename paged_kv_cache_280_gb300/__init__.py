@@ -22,7 +22,7 @@ if not os.path.exists(LIB_PATH):
 
 _lib = ctypes.CDLL(LIB_PATH)
 
-PA_F32, PA_BF16 = 0, 1
+PA_F32, PA_BF16, PA_FP8_E4M3 = 0, 1, 2
 PA_DEV_BAD_BLOCK_ID, PA_DEV_BAD_SLOT, PA_DEV_BAD_SEQ_LEN, PA_DEV_WAIT_TIMEOUT = 1, 2, 4, 8
 STATUS_NAMES = {
     0: "PA_OK", 1: "PA_ERR_INVALID_ARG", 2: "PA_ERR_UNSUPPORTED", 3: "PA_ERR_OUT_OF_BLOCKS",
@@ -66,6 +66,10 @@ _SIGS = {
     "pa_seq_swap_in": (_i32, [_vp, _i64, _vp, _i32, _pi32]),
     "pa_swap_out": (_i32, [_vp, _vp, _vp, _i32, _vp, _vp, _i32, _i32, _i32, _i32, _i32, _vp, _vp]),
     "pa_swap_in": (_i32, [_vp, _vp, _vp, _i32, _vp, _vp, _i32, _i32, _i32, _i32, _i32, _vp, _vp]),
+    "pa_reshape_and_cache_fp8": (_i32, [_vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _i32, _i32, ctypes.c_float,
+                                        ctypes.c_float, _vp, _vp]),
+    "pa_decode_attention_fp8": (_i32, [_vp, _vp, _vp, _vp, ctypes.c_float, ctypes.c_float, _vp, _i32, _vp, _i32,
+                                       _i32, _i32, _i32, _i32, _i32, _i32, ctypes.c_float, _i32, _vp, _sz, _vp]),
     "pa_prefill_attention": (_i32, [_vp, _vp, _vp, _vp, _vp, _i32, _vp, _vp, _i32, _i32, _i32, _i32, _i32, _i32,
                                     _i32, _i32, ctypes.c_float, _i32, _vp, _vp]),
     "pa_decode_set_ctas_per_sm": (_i32, [_i32]),
@@ -117,6 +121,8 @@ def _dtype_code(t) -> int:
         return PA_F32
     if t.dtype == torch.bfloat16:
         return PA_BF16
+    if t.dtype == torch.uint8 or t.dtype == getattr(torch, "float8_e4m3fn", None):
+        return PA_FP8_E4M3
     raise PAError(2, f"dtype {t.dtype}")
 
 
@@ -215,6 +221,32 @@ def pa_decode_launch_info(num_seqs, num_q_heads, num_kv_heads, head_dim, block_s
                                    dtype, *[ctypes.byref(v) for v in vals]),
         "pa_decode_launch_info")
     return tuple(int(v.value) for v in vals)
+
+
+def pa_reshape_and_cache_fp8(k_new, v_new, k_pool, v_pool, slot_mapping, k_scale, v_scale, status=None,
+                             stream=None):
+    """Slot-mapped append into FP8 pools (uint8 E4M3 codes [num_blocks][Hkv][bs][128]) of bf16/fp32 K/V."""
+    nb, hkv, bs, d = k_pool.shape
+    n = slot_mapping.shape[0]
+    _ok(_lib.pa_reshape_and_cache_fp8(_dev_ptr(k_new, "k_new"), _dev_ptr(v_new, "v_new"), _dev_ptr(k_pool, "k_pool"),
+                                      _dev_ptr(v_pool, "v_pool"), _dev_ptr(slot_mapping, "slot_mapping"), n, hkv, d,
+                                      bs, nb, _dtype_code(k_new), float(k_scale), float(v_scale),
+                                      _dev_ptr(status, "status"), _stream(stream)),
+        "pa_reshape_and_cache_fp8")
+
+
+def pa_decode_attention_fp8(out, q, k_pool, v_pool, k_scale, v_scale, block_tables, seq_lens, max_seq_len, scale,
+                            workspace, partition_tokens=0, stream=None):
+    """Decode over FP8 pools (uint8 E4M3 codes) with bf16 q/out; K^ = code value * k_scale, V^ likewise."""
+    b, hq, d = q.shape
+    nb, hkv, bs, _ = k_pool.shape
+    _ok(_lib.pa_decode_attention_fp8(_dev_ptr(out, "out"), _dev_ptr(q, "q"), _dev_ptr(k_pool, "k_pool"),
+                                     _dev_ptr(v_pool, "v_pool"), float(k_scale), float(v_scale),
+                                     _dev_ptr(block_tables, "block_tables"), block_tables.shape[1],
+                                     _dev_ptr(seq_lens, "seq_lens"), int(max_seq_len), b, hq, hkv, d, bs, nb,
+                                     float(scale), int(partition_tokens), _dev_ptr(workspace, "workspace"),
+                                     workspace.numel() * workspace.element_size(), _stream(stream)),
+        "pa_decode_attention_fp8")
 
 
 def pa_swap_out(k_pool, v_pool, blocks, k_store, v_store, status=None, stream=None):

@@ -12,7 +12,7 @@ OUT = os.path.join(HERE, "libpa.so")
 BUILD = os.path.join(HERE, "_build")
 SOURCES = [
     "pa_api.cu", "pa_cache_ops.cu", "pa_decode_bf16.cu", "pa_decode_bf16_fma.cu", "pa_decode_f32.cu",
-    "pa_decode_f32_pow2.cu", "pa_static_ws.cu", "pa_prefill.cu", "pa_alloc.cpp",
+    "pa_decode_f32_pow2.cu", "pa_decode_fp8.cu", "pa_static_ws.cu", "pa_prefill.cu", "pa_alloc.cpp",
 ]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 

@@ -51,12 +51,15 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
 bool encode_pool_map(CUtensorMap* map, const void* pool, int64_t rows, int head_dim, int block_size, pa_dtype dt) {
     auto enc = tensor_map_encoder();
     if (!enc) return false;
-    const int elem = dt == PA_F32 ? 4 : 2;
+    const int elem = dt == PA_F32 ? 4 : (dt == PA_BF16 ? 2 : 1);
     cuuint64_t dims[2] = {(cuuint64_t)head_dim, (cuuint64_t)rows};
     cuuint64_t strides[1] = {(cuuint64_t)head_dim * elem};
     cuuint32_t box[2] = {(cuuint32_t)(128 / elem), (cuuint32_t)block_size};
     cuuint32_t estr[2] = {1, 1};
-    CUresult r = enc(map, dt == PA_F32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
+    const CUtensorMapDataType ty = dt == PA_F32    ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
+                                   : dt == PA_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                                   : CU_TENSOR_MAP_DATA_TYPE_UINT8;
+    CUresult r = enc(map, ty, 2,
                      const_cast<void*>(pool), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                      CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
@@ -179,10 +182,12 @@ pa_status plan_launch(int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_head
     int dev = 0;
     if (!current_device(&dev, &lp->sms)) return PA_ERR_CUDA;
     const int G = num_q_heads / num_kv_heads;
+    // dtype is the pool's: PA_FP8_E4M3 pools pair with bf16 queries and take the CUDA-core path
     lp->mma = (dtype == PA_BF16 && G >= 4);
-    bool found = dtype == PA_F32 ? decode_variant_f32(head_dim, block_size, G, &lp->v)
-                 : lp->mma         ? decode_variant_bf16_mma(head_dim, block_size, &lp->v)
-                                   : decode_variant_bf16_fma(head_dim, block_size, G, &lp->v);
+    bool found = dtype == PA_F32         ? decode_variant_f32(head_dim, block_size, G, &lp->v)
+                 : dtype == PA_FP8_E4M3 ? decode_variant_fp8(head_dim, block_size, G, &lp->v)
+                 : lp->mma              ? decode_variant_bf16_mma(head_dim, block_size, &lp->v)
+                                        : decode_variant_bf16_fma(head_dim, block_size, G, &lp->v);
     if (!found) return PA_ERR_UNSUPPORTED;
     lp->smem = lp->v.smem_bytes(num_seqs, fixed);
     if (lp->smem > kMaxSmem) return PA_ERR_UNSUPPORTED;
@@ -229,7 +234,7 @@ extern "C" pa_status pa_decode_launch_info(int32_t num_seqs, int32_t num_q_heads
                                            int32_t head_dim, int32_t block_size, int32_t max_blocks_per_seq,
                                            pa_dtype dtype, int32_t* ctas, int32_t* stages, int32_t* smem_bytes,
                                            int32_t* uses_mma) {
-    if (dtype != PA_F32 && dtype != PA_BF16) return PA_ERR_UNSUPPORTED;
+    if (dtype != PA_F32 && dtype != PA_BF16 && dtype != PA_FP8_E4M3) return PA_ERR_UNSUPPORTED;
     pa_status s = check_shapes(num_seqs, num_q_heads, num_kv_heads, head_dim, block_size);
     if (s != PA_OK) return s;
     if (max_blocks_per_seq <= 0) return PA_ERR_INVALID_ARG;
@@ -243,15 +248,22 @@ extern "C" pa_status pa_decode_launch_info(int32_t num_seqs, int32_t num_q_heads
     return PA_OK;
 }
 
-extern "C" pa_status pa_decode_attention(void* out, const void* q, const void* k_pool, const void* v_pool,
-                                         const int32_t* block_tables, int32_t max_blocks_per_seq,
-                                         const int32_t* seq_lens, int32_t max_seq_len, int32_t num_seqs,
-                                         int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
-                                         int32_t block_size, int32_t num_blocks, float scale, int32_t partition_tokens,
-                                         void* workspace, size_t workspace_bytes, pa_dtype dtype, void* stream) {
-    if (dtype != PA_F32 && dtype != PA_BF16) return PA_ERR_UNSUPPORTED;
+namespace pa {
+namespace {
+
+// Shared by pa_decode_attention (pools of the query dtype) and
+// pa_decode_attention_fp8 (FP8 pools, bf16 queries, K and V scales).
+pa_status decode_common(void* out, const void* q, const void* k_pool, const void* v_pool, const int32_t* block_tables,
+                        int32_t max_blocks_per_seq, const int32_t* seq_lens, int32_t max_seq_len, int32_t num_seqs,
+                        int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
+                        int32_t num_blocks, float scale, int32_t partition_tokens, void* workspace,
+                        size_t workspace_bytes, pa_dtype dtype, float k_scale, float v_scale, void* stream) {
+    if (dtype != PA_F32 && dtype != PA_BF16 && dtype != PA_FP8_E4M3) return PA_ERR_UNSUPPORTED;
     pa_status s = check_shapes(num_seqs, num_q_heads, num_kv_heads, head_dim, block_size);
     if (s != PA_OK) return s;
+    if (dtype == PA_FP8_E4M3 && head_dim != 128) return PA_ERR_UNSUPPORTED;  // a pool row fills one 128-byte panel
+    if (!std::isfinite(k_scale) || !std::isfinite(v_scale) || !(k_scale > 0.f) || !(v_scale > 0.f))
+        return PA_ERR_INVALID_ARG;
     if (!out || !q || !k_pool || !v_pool || !block_tables || !seq_lens || !workspace) return PA_ERR_INVALID_ARG;
     if (!aligned16(out) || !aligned16(q) || !aligned16(k_pool) || !aligned16(v_pool) || !aligned16(workspace) ||
         (reinterpret_cast<uintptr_t>(block_tables) & 3u) || (reinterpret_cast<uintptr_t>(seq_lens) & 3u))
@@ -300,7 +312,35 @@ extern "C" pa_status pa_decode_attention(void* out, const void* q, const void* k
     p.group = num_q_heads / num_kv_heads;
     p.partition_tiles = partition_tokens / block_size;
     p.num_ctas = lp.grid;
-    p.scale_log2 = scale * 1.4426950408889634f;
+    p.scale_log2 = scale * 1.4426950408889634f * k_scale;
+    p.out_scale = v_scale;
     lp.v.launch(p, tk, tv, lp.grid, lp.smem, static_cast<cudaStream_t>(stream));
     return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+}
+
+}  // namespace
+}  // namespace pa
+
+extern "C" pa_status pa_decode_attention(void* out, const void* q, const void* k_pool, const void* v_pool,
+                                         const int32_t* block_tables, int32_t max_blocks_per_seq,
+                                         const int32_t* seq_lens, int32_t max_seq_len, int32_t num_seqs,
+                                         int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
+                                         int32_t block_size, int32_t num_blocks, float scale, int32_t partition_tokens,
+                                         void* workspace, size_t workspace_bytes, pa_dtype dtype, void* stream) {
+    if (dtype != PA_F32 && dtype != PA_BF16) return PA_ERR_UNSUPPORTED;
+    return pa::decode_common(out, q, k_pool, v_pool, block_tables, max_blocks_per_seq, seq_lens, max_seq_len, num_seqs,
+                             num_q_heads, num_kv_heads, head_dim, block_size, num_blocks, scale, partition_tokens,
+                             workspace, workspace_bytes, dtype, 1.f, 1.f, stream);
+}
+
+extern "C" pa_status pa_decode_attention_fp8(void* out, const void* q, const void* k_pool, const void* v_pool,
+                                             float k_scale, float v_scale, const int32_t* block_tables,
+                                             int32_t max_blocks_per_seq, const int32_t* seq_lens,
+                                             int32_t max_seq_len, int32_t num_seqs, int32_t num_q_heads,
+                                             int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
+                                             int32_t num_blocks, float scale, int32_t partition_tokens,
+                                             void* workspace, size_t workspace_bytes, void* stream) {
+    return pa::decode_common(out, q, k_pool, v_pool, block_tables, max_blocks_per_seq, seq_lens, max_seq_len, num_seqs,
+                             num_q_heads, num_kv_heads, head_dim, block_size, num_blocks, scale, partition_tokens,
+                             workspace, workspace_bytes, PA_FP8_E4M3, k_scale, v_scale, stream);
 }

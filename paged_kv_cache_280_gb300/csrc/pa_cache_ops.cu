@@ -4,6 +4,10 @@
 // K and the matching chunk of V per iteration of a grid-stride loop, so
 // consecutive threads touch consecutive bytes of one row (coalesced on both
 // sides).  Indices are checked against the pool before any access.
+#include <cuda_fp8.h>
+
+#include <cmath>
+
 #include "pa_device.cuh"
 #include "pa_internal.h"
 
@@ -35,6 +39,50 @@ __global__ void __launch_bounds__(256) reshape_and_cache_kernel(const uint4* __r
         const int64_t dst = ((blk * num_kv_heads + h) * block_size + off) * row_chunks + chunk;
         k_pool[dst] = __ldg(k_new + idx);
         v_pool[dst] = __ldg(v_new + idx);
+    }
+}
+
+// Slot-mapped append into FP8 (E4M3) pools: each element is quantised as
+// code = E4M3(fp32(x / scale)) with round-to-nearest-even and saturation to
+// +-448 (the hardware conversion with satfinite).  One thread converts 8
+// elements: 16 bytes of bf16 in, 8 bytes of codes out.
+template <typename TIn>
+__global__ void __launch_bounds__(256) reshape_and_cache_fp8_kernel(
+    const TIn* __restrict__ k_new, const TIn* __restrict__ v_new, uint2* k_pool, uint2* v_pool,
+    const int64_t* __restrict__ slot_mapping, int32_t num_tokens, int32_t num_kv_heads, int32_t row_groups,
+    int32_t block_size, int64_t num_slots, float k_scale, float v_scale, int32_t* status) {
+    pdl_launch_dependents();
+    const int64_t total = (int64_t)num_tokens * num_kv_heads * row_groups;
+    for (int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; idx < total;
+         idx += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t tok = idx / ((int64_t)num_kv_heads * row_groups);
+        const int64_t rem = idx - tok * num_kv_heads * row_groups;
+        const int64_t slot = __ldg(slot_mapping + tok);
+        if (slot < 0) continue;
+        if (slot >= num_slots) {
+            flag_status(status, PA_DEV_BAD_SLOT);
+            continue;
+        }
+        const int64_t blk = slot / block_size, off = slot % block_size;
+        const int64_t h = rem / row_groups, grp = rem - h * row_groups;
+        const int64_t dst = ((blk * num_kv_heads + h) * block_size + off) * row_groups + grp;
+        uint32_t kc[2], vc[2];
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+            uint32_t kw = 0, vw = 0;
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const int64_t src = idx * 8 + half * 4 + e;
+                const float kx = static_cast<float>(k_new[src]) / k_scale;
+                const float vx = static_cast<float>(v_new[src]) / v_scale;
+                kw |= (uint32_t)__nv_cvt_float_to_fp8(kx, __NV_SATFINITE, __NV_E4M3) << (8 * e);
+                vw |= (uint32_t)__nv_cvt_float_to_fp8(vx, __NV_SATFINITE, __NV_E4M3) << (8 * e);
+            }
+            kc[half] = kw;
+            vc[half] = vw;
+        }
+        k_pool[dst] = make_uint2(kc[0], kc[1]);
+        v_pool[dst] = make_uint2(vc[0], vc[1]);
     }
 }
 
@@ -141,15 +189,15 @@ extern "C" pa_status pa_copy_blocks(void* k_pool, void* v_pool, const int32_t* s
                                     pa_dtype dtype, int32_t* dev_status, void* stream) {
     using namespace pa;
     if (num_pairs < 0 || num_kv_heads <= 0 || num_blocks <= 0) return PA_ERR_INVALID_ARG;
-    if (dtype != PA_F32 && dtype != PA_BF16) return PA_ERR_UNSUPPORTED;
-    if (!shape_ok(head_dim, block_size)) return PA_ERR_UNSUPPORTED;
+    if (dtype != PA_F32 && dtype != PA_BF16 && dtype != PA_FP8_E4M3) return PA_ERR_UNSUPPORTED;
+    if (!shape_ok(head_dim, block_size) || (dtype == PA_FP8_E4M3 && head_dim != 128)) return PA_ERR_UNSUPPORTED;
     if (num_pairs == 0) return PA_OK;
     if (num_pairs > 65535) return PA_ERR_UNSUPPORTED;  // one grid row per pair
     if (!k_pool || !v_pool || !src_dst_pairs) return PA_ERR_INVALID_ARG;
     if (!aligned16(k_pool) || !aligned16(v_pool) || (reinterpret_cast<uintptr_t>(src_dst_pairs) & 3u) ||
         (reinterpret_cast<uintptr_t>(dev_status) & 3u))
         return PA_ERR_INVALID_ARG;
-    const int elem = dtype == PA_F32 ? 4 : 2;
+    const int elem = dtype == PA_F32 ? 4 : (dtype == PA_BF16 ? 2 : 1);
     const int64_t block_chunks = (int64_t)num_kv_heads * block_size * head_dim * elem / 16;
     int64_t slices = (block_chunks + 256 * 4 - 1) / (256 * 4);  // ~4 chunks per thread
     if (slices < 1) slices = 1;
@@ -167,15 +215,15 @@ static pa_status swap_blocks(bool out, void* k_pool, void* v_pool, const int32_t
                              void* v_store, int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
                              int32_t num_blocks, pa_dtype dtype, int32_t* dev_status, void* stream) {
     if (n < 0 || num_kv_heads <= 0 || num_blocks <= 0) return PA_ERR_INVALID_ARG;
-    if (dtype != PA_F32 && dtype != PA_BF16) return PA_ERR_UNSUPPORTED;
-    if (!shape_ok(head_dim, block_size)) return PA_ERR_UNSUPPORTED;
+    if (dtype != PA_F32 && dtype != PA_BF16 && dtype != PA_FP8_E4M3) return PA_ERR_UNSUPPORTED;
+    if (!shape_ok(head_dim, block_size) || (dtype == PA_FP8_E4M3 && head_dim != 128)) return PA_ERR_UNSUPPORTED;
     if (n == 0) return PA_OK;
     if (n > 65535) return PA_ERR_UNSUPPORTED;  // one grid row per block
     if (!k_pool || !v_pool || !blocks || !k_store || !v_store) return PA_ERR_INVALID_ARG;
     if (!aligned16(k_pool) || !aligned16(v_pool) || !aligned16(k_store) || !aligned16(v_store) ||
         (reinterpret_cast<uintptr_t>(blocks) & 3u) || (reinterpret_cast<uintptr_t>(dev_status) & 3u))
         return PA_ERR_INVALID_ARG;
-    const int elem = dtype == PA_F32 ? 4 : 2;
+    const int elem = dtype == PA_F32 ? 4 : (dtype == PA_BF16 ? 2 : 1);
     const int64_t block_chunks = (int64_t)num_kv_heads * block_size * head_dim * elem / 16;
     int64_t slices = (block_chunks + 256 * 4 - 1) / (256 * 4);  // ~4 chunks per thread
     if (slices < 1) slices = 1;
@@ -209,4 +257,40 @@ extern "C" pa_status pa_swap_in(const void* k_store, const void* v_store, const 
                                 int32_t num_blocks, pa_dtype dtype, int32_t* dev_status, void* stream) {
     return pa::swap_blocks(false, k_pool, v_pool, blocks, num, const_cast<void*>(k_store), const_cast<void*>(v_store),
                            num_kv_heads, head_dim, block_size, num_blocks, dtype, dev_status, stream);
+}
+
+extern "C" pa_status pa_reshape_and_cache_fp8(const void* k_new, const void* v_new, void* k_pool, void* v_pool,
+                                              const int64_t* slot_mapping, int32_t num_tokens, int32_t num_kv_heads,
+                                              int32_t head_dim, int32_t block_size, int32_t num_blocks,
+                                              pa_dtype in_dtype, float k_scale, float v_scale, int32_t* dev_status,
+                                              void* stream) {
+    using namespace pa;
+    if (num_tokens < 0 || num_kv_heads <= 0 || num_blocks <= 0) return PA_ERR_INVALID_ARG;
+    if (in_dtype != PA_F32 && in_dtype != PA_BF16) return PA_ERR_UNSUPPORTED;
+    if (head_dim != 128 || (block_size != 16 && block_size != 32)) return PA_ERR_UNSUPPORTED;
+    if (!std::isfinite(k_scale) || !std::isfinite(v_scale) || !(k_scale > 0.f) || !(v_scale > 0.f))
+        return PA_ERR_INVALID_ARG;
+    if (num_tokens == 0) return PA_OK;
+    if (!k_new || !v_new || !k_pool || !v_pool || !slot_mapping) return PA_ERR_INVALID_ARG;
+    if (!aligned16(k_new) || !aligned16(v_new) || !aligned16(k_pool) || !aligned16(v_pool) ||
+        (reinterpret_cast<uintptr_t>(slot_mapping) & 7u) || (reinterpret_cast<uintptr_t>(dev_status) & 3u))
+        return PA_ERR_INVALID_ARG;
+    const int32_t row_groups = head_dim / 8;
+    const int64_t total = (int64_t)num_tokens * num_kv_heads * row_groups;
+    const int sms = sm_count_of_current_device();
+    if (sms <= 0) return PA_ERR_CUDA;
+    const int64_t want = (total + 255) / 256;
+    const int grid = (int)(want < (int64_t)sms * 8 ? want : (int64_t)sms * 8);
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (in_dtype == PA_BF16)
+        reshape_and_cache_fp8_kernel<__nv_bfloat16><<<grid, 256, 0, st>>>(
+            static_cast<const __nv_bfloat16*>(k_new), static_cast<const __nv_bfloat16*>(v_new),
+            static_cast<uint2*>(k_pool), static_cast<uint2*>(v_pool), slot_mapping, num_tokens, num_kv_heads,
+            row_groups, block_size, (int64_t)num_blocks * block_size, k_scale, v_scale, dev_status);
+    else
+        reshape_and_cache_fp8_kernel<float><<<grid, 256, 0, st>>>(
+            static_cast<const float*>(k_new), static_cast<const float*>(v_new), static_cast<uint2*>(k_pool),
+            static_cast<uint2*>(v_pool), slot_mapping, num_tokens, num_kv_heads, row_groups, block_size,
+            (int64_t)num_blocks * block_size, k_scale, v_scale, dev_status);
+    return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }

@@ -38,6 +38,8 @@
 //     output dimensions for P V.
 #pragma once
 
+#include <cuda_fp8.h>
+
 #include <type_traits>
 
 #include "pa_device.cuh"
@@ -62,6 +64,10 @@ template <>
 struct ElemBytes<__nv_bfloat16> {
     static constexpr int value = 2;
 };
+template <>
+struct ElemBytes<__nv_fp8_e4m3> {  // FP8 pools (OCP E4M3 codes)
+    static constexpr int value = 1;
+};
 
 // Pipeline depth: about PA_STAGE_BYTES (32 KB) of tiles in flight per CTA on
 // the tensor-core path and PA_STAGE_BYTES_FMA (16 KB) on the CUDA-core path,
@@ -81,15 +87,16 @@ constexpr int stages_for(int ring_bytes, int bs, int d, int e) {
 
 // Shared-memory layout of one CTA.  Query-row buffers are sized for the
 // group size of the instantiation (GF > 0) or for the largest group.
-template <typename T, int D, int BS, bool MMA, int GF>
+template <typename T, int D, int BS, bool MMA, int GF, typename KV = T>
 struct Layout {
-    static constexpr int E = ElemBytes<T>::value;
+    static constexpr int E = ElemBytes<KV>::value;  // pool element bytes
+    static constexpr int EQ = ElemBytes<T>::value;  // query / output element bytes
     static constexpr int S = stages_for(MMA ? PA_STAGE_BYTES : PA_STAGE_BYTES_FMA, BS, D, E);
     static constexpr int GN = GF > 0 ? GF : kMaxGroup;  // query rows a q slot holds
     static constexpr int kTileBytes = BS * D * E;  // K (or V) of one tile
     static constexpr int kPanels = D * E / 128;    // 128-byte column panels per row
     static constexpr int kStageBytes = 2 * kTileBytes;
-    static constexpr int kQSlotBytes = GN * D * E;
+    static constexpr int kQSlotBytes = GN * D * EQ;
     static constexpr int kStagesOff = 0;
     static constexpr int kQOff = kStagesOff + S * kStageBytes;
     // CUDA-core path only: fp32 query rows (pre-scaled) and one step's weights.
@@ -229,10 +236,35 @@ __device__ __forceinline__ void load_chunk_f32<float>(uint32_t addr, float* v) {
     asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];" : "=f"(v[0]), "=f"(v[1]), "=f"(v[2]), "=f"(v[3]) : "r"(addr));
 }
 
+// Two E4M3 codes (low byte first) widened exactly to fp32, through fp16.
+__device__ __forceinline__ float2 e4m3x2_to_f32(uint32_t two) {
+    const __half2_raw h = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(two & 0xffffu), __NV_E4M3);
+    return __half22float2(*reinterpret_cast<const __half2*>(&h));
+}
+template <>
+__device__ __forceinline__ void load_chunk_f32<__nv_fp8_e4m3>(uint32_t addr, float* v) {
+    uint32_t r[4];
+    asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]) : "r"(addr));
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const float2 lo = e4m3x2_to_f32(r[i]), hi = e4m3x2_to_f32(r[i] >> 16);
+        v[4 * i] = lo.x;
+        v[4 * i + 1] = lo.y;
+        v[4 * i + 2] = hi.x;
+        v[4 * i + 3] = hi.y;
+    }
+}
+
 // Load N consecutive elements (N * E <= 16 bytes, naturally aligned) and widen.
 template <typename T, int N>
 __device__ __forceinline__ void load_vec_f32(uint32_t addr, float* v) {
-    if constexpr (sizeof(T) == 2) {
+    if constexpr (sizeof(T) == 1) {
+        static_assert(N == 4, "fp8 vector of 4");
+        uint32_t r;
+        asm volatile("ld.shared.u32 %0, [%1];" : "=r"(r) : "r"(addr));
+        const float2 lo = e4m3x2_to_f32(r), hi = e4m3x2_to_f32(r >> 16);
+        v[0] = lo.x; v[1] = lo.y; v[2] = hi.x; v[3] = hi.y;
+    } else if constexpr (sizeof(T) == 2) {
         if constexpr (N == 2) {
             uint32_t r;
             asm volatile("ld.shared.u32 %0, [%1];" : "=r"(r) : "r"(addr));
@@ -358,10 +390,11 @@ struct MmaState {
     }
 
     // Normalised output rows; `o_rows` points at out[b][h*G][0].
+    // oscale multiplies the output (the V scale of an FP8 pool, else 1).
     template <typename T>
-    __device__ __forceinline__ void store_out(T* o_rows, int G, int lane) const {
+    __device__ __forceinline__ void store_out(T* o_rows, int G, int lane, float oscale) const {
         const int g = lane >> 2, h0 = 2 * (lane & 3), h1 = h0 + 1;
-        const float r0 = 1.f / l[0], r1 = 1.f / l[1];
+        const float r0 = oscale / l[0], r1 = oscale / l[1];
 #pragma unroll
         for (int i = 0; i < MT; ++i) {
             const int d0 = 16 * i + g;
@@ -506,11 +539,11 @@ struct FmaState {
     // Normalised output rows; `o_rows` points at out[b][h*G][0].  m and l are
     // the same in every lane (reduced by shuffles in step()).
     template <typename TO>
-    __device__ __forceinline__ void store_out(TO* o_rows, int G, int lane) const {
+    __device__ __forceinline__ void store_out(TO* o_rows, int G, int lane, float oscale) const {
 #pragma unroll
         for (int g = 0; g < GN; ++g) {
             if (active(g, G)) {
-                const float r = 1.f / l[g];
+                const float r = oscale / l[g];
 #pragma unroll
                 for (int v = 0; v < VEC; ++v) o_rows[g * D + lane * VEC + v] = from_float<TO>(o[g][v] * r);
             }
@@ -545,7 +578,8 @@ struct FmaState {
 template <typename T, int D>
 __device__ __forceinline__ bool merge_staged(const float* partials, size_t slot_floats, T* orow, int ca, int cb,
                                              bool ca_split, int G, int lane, const uint8_t* ring, uint32_t ring_s,
-                                             int ring_bytes, float* work, uint32_t mbar, uint32_t& mphase) {
+                                             int ring_bytes, float* work, uint32_t mbar, uint32_t& mphase,
+                                             float oscale) {
     const uint32_t slot_bytes = (uint32_t)(slot_floats * 4);
     const int np = cb - ca + 1, nel = G * D;
     const int acc_bytes = (nel * 4 + 15) & ~15;
@@ -554,7 +588,7 @@ __device__ __forceinline__ bool merge_staged(const float* partials, size_t slot_
     if (multi) per_chunk = min((ring_bytes - acc_bytes) / (int)slot_bytes, kMaxMergeChunk);
     if (per_chunk < 1) return false;  // cannot happen for the instantiated shapes
     float* wgt = work;                               // [kMaxMergeChunk][kMaxGroup]
-    float* hst = work + kMaxMergeChunk * kMaxGroup;  // [0..7] max, [8..15] sum, [16..23] rescale, [24..31] 1/sum
+    float* hst = work + kMaxMergeChunk * kMaxGroup;  // [0..7] max, [8..15] sum, [16..23] rescale, [24..31] oscale/sum
     const float* buf = reinterpret_cast<const float*>(ring);
     float* acc_s = reinterpret_cast<float*>(const_cast<uint8_t*>(ring) + ring_bytes - acc_bytes);
     auto slot_of = [&](int cc) { return partials + (size_t)(2 * cc + (cc == ca && ca_split ? 1 : 0)) * slot_floats; };
@@ -592,7 +626,7 @@ __device__ __forceinline__ bool merge_staged(const float* partials, size_t slot_
             hst[hd] = Mc;
             hst[8 + hd] = Lr;
             hst[16 + hd] = resc;
-            hst[24 + hd] = 1.f / Lr;
+            hst[24 + hd] = oscale / Lr;
         }
         __syncwarp();
         const bool final_chunk = c0 + nc >= np;
@@ -629,10 +663,10 @@ __device__ __forceinline__ bool merge_staged(const float* partials, size_t slot_
 // ---------------------------------------------------------------------------
 // The kernel
 // ---------------------------------------------------------------------------
-template <typename T, int D, int BS, bool MMA, int GF>
+template <typename T, int D, int BS, bool MMA, int GF, typename KV>
 __global__ void __launch_bounds__(kThreads) decode_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tmap_k,
                                                           const __grid_constant__ CUtensorMap tmap_v) {
-    using L = Layout<T, D, BS, MMA, GF>;
+    using L = Layout<T, D, BS, MMA, GF, KV>;
     constexpr int S = L::S;
     constexpr int E = L::E;
     extern __shared__ uint8_t smem_raw[];
@@ -756,7 +790,7 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const DecodeParams p, 
             prefetch_tensormap(&tmap_v);
         }
         const uint64_t policy = policy_evict_first();
-        const uint32_t q_bytes = (uint32_t)(G * D * E);
+        const uint32_t q_bytes = (uint32_t)(G * D * L::EQ);
         uint32_t k = 0, pi = 0, k_issued = 0, pi_issued = 0;
         // Walk the range in chunks of up to 32 tiles of one piece.  The block-table
         // entries of the next chunk (of this piece or of the next one) are loaded
@@ -783,7 +817,7 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const DecodeParams p, 
                 if (role_wait(qempty_bar(qs), ((pi / kQSlots) & 1) ^ 1, misc, p.status)) {
                     if (lane == 0) {
                         mbar_arrive_expect_tx(qfull_bar(qs), q_bytes);
-                        const uint8_t* src = static_cast<const uint8_t*>(p.q) + ((size_t)b * Hq + (size_t)h * G) * D * E;
+                        const uint8_t* src = static_cast<const uint8_t*>(p.q) + ((size_t)b * Hq + (size_t)h * G) * D * L::EQ;
                         bulk_load(base_s + L::kQOff + qs * L::kQSlotBytes, src, q_bytes, qfull_bar(qs));
                     }
                     pi_issued = pi + 1;
@@ -846,7 +880,7 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const DecodeParams p, 
         }
         float* qf = reinterpret_cast<float*>(base + L::kQfOff);
         float* ptile = reinterpret_cast<float*>(base + L::kPTileOff);
-        typename std::conditional<MMA, MmaState<D, BS>, FmaState<T, D, BS, GF>>::type st;
+        typename std::conditional<MMA, MmaState<D, BS>, FmaState<KV, D, BS, GF>>::type st;
         uint32_t k = 0, pi = 0;
         PieceIter it;
         it.init(P, t0, t1);
@@ -894,7 +928,7 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const DecodeParams p, 
             const int nb = P.nblocks(b);
             T* orow = static_cast<T*>(p.out) + ((size_t)b * Hq + (size_t)h * G) * D;
             if (j0 == 0 && j1 == nb) {
-                st.store_out(orow, G, lane);
+                st.store_out(orow, G, lane, p.out_scale);
             } else {
                 // Split segment: store the partial now; its completion is counted
                 // after the loop, so the fence and the atomic round trip stall
@@ -940,7 +974,7 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const DecodeParams p, 
             T* orow = static_cast<T*>(p.out) + ((size_t)mb * Hq + (size_t)mh * G) * D;
             if (!merge_staged<T, D>(p.partials, slot_floats, orow, ca, cb, s0 != P.cta_start(ca), G, lane, base,
                                     base_s, S * L::kStageBytes, reinterpret_cast<float*>(base + L::kMergeOff),
-                                    merge_bar, mphase)) {
+                                    merge_bar, mphase, p.out_scale)) {
                 misc[0] = 1;
                 if (lane == 0) flag_status(p.status, PA_DEV_WAIT_TIMEOUT);
                 break;
@@ -952,9 +986,9 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const DecodeParams p, 
 }
 
 // Host-side handle of one instantiation.
-template <typename T, int D, int BS, bool MMA, int GF>
+template <typename T, int D, int BS, bool MMA, int GF, typename KV = T>
 struct VariantOf {
-    static int smem_bytes(int num_seqs, bool fixed) { return Layout<T, D, BS, MMA, GF>::bytes(num_seqs, fixed); }
+    static int smem_bytes(int num_seqs, bool fixed) { return Layout<T, D, BS, MMA, GF, KV>::bytes(num_seqs, fixed); }
     // Launched as a programmatic dependent of the preceding kernel on the stream:
     // the grid may start while that kernel finishes if it allowed it.
     static void launch(const DecodeParams& p, const CUtensorMap& tk, const CUtensorMap& tv, int grid, int smem,
@@ -969,10 +1003,11 @@ struct VariantOf {
         attr[0].val.programmaticStreamSerializationAllowed = 1;
         cfg.attrs = attr;
         cfg.numAttrs = 1;
-        cudaLaunchKernelEx(&cfg, decode_kernel<T, D, BS, MMA, GF>, p, tk, tv);
+        cudaLaunchKernelEx(&cfg, decode_kernel<T, D, BS, MMA, GF, KV>, p, tk, tv);
     }
     static DecodeVariant get() {
-        return DecodeVariant{reinterpret_cast<const void*>(&decode_kernel<T, D, BS, MMA, GF>), Layout<T, D, BS, MMA, GF>::S,
+        return DecodeVariant{reinterpret_cast<const void*>(&decode_kernel<T, D, BS, MMA, GF, KV>),
+                             Layout<T, D, BS, MMA, GF, KV>::S,
                              kThreads, &smem_bytes, &launch};
     }
 };

@@ -38,7 +38,8 @@ struct DecodeParams {
     int32_t group;            // G = num_q_heads / num_kv_heads
     int32_t partition_tiles;  // 0: split anywhere; else splits only at multiples of this
     int32_t num_ctas;
-    float scale_log2;  // scale * log2(e): scores are kept in the base-2 domain
+    float scale_log2;  // scale * log2(e) (times the K scale of an FP8 pool): scores in the base-2 domain
+    float out_scale;   // multiplies the output: the V scale of an FP8 pool, else 1
 };
 
 // One compiled decode kernel (dtype, head_dim, block_size, compute path).
@@ -57,6 +58,8 @@ bool decode_variant_f32(int head_dim, int block_size, int group, DecodeVariant* 
 bool decode_variant_f32_pow2(int head_dim, int block_size, int group, DecodeVariant* out);
 bool decode_variant_bf16_mma(int head_dim, int block_size, DecodeVariant* out);
 bool decode_variant_bf16_fma(int head_dim, int block_size, int group, DecodeVariant* out);
+// bf16 queries and outputs over FP8 (E4M3) pools, CUDA-core path.
+bool decode_variant_fp8(int head_dim, int block_size, int group, DecodeVariant* out);
 
 // Host launch helpers shared by the attention entry points (pa_api.cu).
 // The TMA map of a pool viewed as [num_blocks * Hkv * block_size][head_dim]

@@ -138,7 +138,7 @@ def poison_unused_slots(k_pool: np.ndarray, v_pool: np.ndarray, tables: np.ndarr
     for b, n in enumerate(lens):
         for t in range(int(n)):
             used[tables[b, t // bs], t % bs] = True
-    nan = np.uint16(0x7FC0) if k_pool.dtype == np.uint16 else np.float32("nan")
+    nan = {np.dtype(np.uint16): np.uint16(0x7FC0), np.dtype(np.uint8): np.uint8(0x7F)}.get(k_pool.dtype, np.float32("nan"))
     for pool in (k_pool, v_pool):
         pool.transpose(0, 2, 1, 3)[~used] = nan
     return int((~used).sum())
