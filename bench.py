@@ -228,10 +228,10 @@ def populate(alloc, w):
     return list(range(len(w.lengths)))
 
 
-def decode_bytes(lens, w) -> int:
+def decode_bytes(lens, w, kv_elem=None) -> int:
     """Algorithmic bytes of one decode launch: K and V of every token, tables, lengths, q and out."""
     e = w.elem_bytes
-    kv = int(np.sum(lens, dtype=np.int64)) * w.num_kv_heads * w.head_dim * 2 * e
+    kv = int(np.sum(lens, dtype=np.int64)) * w.num_kv_heads * w.head_dim * 2 * (kv_elem or e)
     tables = int(sum(-(-int(x) // w.block_size) for x in lens)) * 4
     qo = 2 * len(lens) * w.num_q_heads * w.head_dim * e
     return kv + tables + 4 * len(lens) + qo
@@ -272,7 +272,18 @@ def recorded_traffic():
 # ---------------------------------------------------------------------------
 # CPU baseline: the oracle, as it stands, on the host cores
 # ---------------------------------------------------------------------------
-def cpu_baseline(w, q, k_pool, v_pool, tables, lens, seconds: float):
+FP8_K_SCALE, FP8_V_SCALE = 1.0 / 64, 1.0 / 64  # N(0,1) draws over 1/64: codes up to about 300 of the 448 range
+
+
+def fp8_codes(bf16_bits: np.ndarray, scale: float) -> np.ndarray:
+    """E4M3 codes of bf16 values over a scale (synthetic pool contents, made with torch's conversion)."""
+    import torch
+
+    vals = torch.from_numpy(np.ascontiguousarray(bf16_bits).view(np.int16)).view(torch.bfloat16).float() / scale
+    return vals.to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+
+
+def cpu_baseline(w, q, k_pool, v_pool, tables, lens, seconds: float, scales=None):
     import oracle
 
     threads = os.cpu_count() or 1
@@ -281,7 +292,10 @@ def cpu_baseline(w, q, k_pool, v_pool, tables, lens, seconds: float):
     seqs_done = 0
     while True:
         chunk = list(range(B))
-        oracle.decode_attention(q, k_pool, v_pool, tables, lens, w.scale, seqs=chunk, threads=threads)
+        if scales:
+            oracle.decode_attention_fp8(q, k_pool, v_pool, *scales, tables, lens, w.scale, seqs=chunk, threads=threads)
+        else:
+            oracle.decode_attention(q, k_pool, v_pool, tables, lens, w.scale, seqs=chunk, threads=threads)
         done_tokens += int(np.sum(lens, dtype=np.int64))
         seqs_done += len(chunk)
         rounds += 1
@@ -319,7 +333,27 @@ def run_ours(args, rank, world, local_rank):
         return torch.from_numpy(np.ascontiguousarray(a)).to(dev)
 
     k_host, v_host = w.pool_values("k"), w.pool_values("v")
-    dk, dv = to_dev(k_host), to_dev(v_host)
+    fp8 = args.kv == "fp8"
+    KS, VS = FP8_K_SCALE, FP8_V_SCALE
+    if fp8:
+        # FP8 pools: E4M3 codes of the same N(0,1) draws over the pool scales (input data, made on the host)
+        k_host, v_host = fp8_codes(k_host, KS), fp8_codes(v_host, VS)
+        dk, dv = torch.from_numpy(k_host).to(dev), torch.from_numpy(v_host).to(dev)
+    else:
+        dk, dv = to_dev(k_host), to_dev(v_host)
+
+    def append(kn_, vn_, slots_, **kw):
+        if fp8:
+            pa.pa_reshape_and_cache_fp8(kn_, vn_, dk, dv, slots_, KS, VS, **kw)
+        else:
+            pa.pa_reshape_and_cache(kn_, vn_, dk, dv, slots_, **kw)
+
+    def attend(q_, tables_, lens_, max_len_, **kw):
+        if fp8:
+            pa.pa_decode_attention_fp8(out, q_, dk, dv, KS, VS, tables_, lens_, max_len_, w.scale, ws,
+                                       partition_tokens=PT, **kw)
+        else:
+            pa.pa_decode_attention(out, q_, dk, dv, tables_, lens_, max_len_, w.scale, ws, partition_tokens=PT, **kw)
 
     # ---- a1 once: the step's allocator outputs become device-resident inputs ----
     t_alloc = time.perf_counter()
@@ -348,11 +382,10 @@ def run_ours(args, rank, world, local_rank):
     def step():
         if d_pairs is not None:
             pa.pa_copy_blocks(dk, dv, d_pairs, status=ws[:4].view(torch.int32), stream=stream)
-        pa.pa_reshape_and_cache(d_kn, d_vn, dk, dv, d_slots, status=ws[:4].view(torch.int32), stream=stream)
+        append(d_kn, d_vn, d_slots, status=ws[:4].view(torch.int32), stream=stream)
 
     def decode():
-        pa.pa_decode_attention(out, d_q, dk, dv, d_tables, d_lens, max_len, w.scale, ws, partition_tokens=PT,
-                               stream=stream)
+        attend(d_q, d_tables, d_lens, max_len, stream=stream)
 
     for _ in range(Wm):
         flush_l2()
@@ -386,15 +419,16 @@ def run_ours(args, rank, world, local_rank):
     tokens_step = int(np.sum(lens, dtype=np.int64))
     all_tokens = reduce_sum(float(tokens_step * K), dist, dev)
     value = all_tokens / total_s
-    dbytes = decode_bytes(lens, w)
+    dbytes = decode_bytes(lens, w, kv_elem=1 if fp8 else w.elem_bytes)
     # KV bytes of the distinct physical blocks the step reads (below the per-sequence
     # bytes when sequences share prefix blocks, which L2 then serves more than once)
     used = [tables[i, : -(-int(n) // bs)] for i, n in enumerate(lens)]
-    unique_kv = int(np.unique(np.concatenate(used)).size) * bs * Hkv * D * 2 * w.elem_bytes if B else 0
+    unique_kv = int(np.unique(np.concatenate(used)).size) * bs * Hkv * D * 2 * (1 if fp8 else w.elem_bytes) if B else 0
     dec_mean_s = statistics.mean(dec_ms) / 1e3
     peak, peak_kind = measured_peaks()
     achieved = dbytes / dec_mean_s / 1e9
-    ctas, stages, smem, mma = pa.pa_decode_launch_info(B, Hq, Hkv, D, bs, max_blocks, pa.PA_BF16)
+    ctas, stages, smem, mma = pa.pa_decode_launch_info(B, Hq, Hkv, D, bs, max_blocks,
+                                                       pa.PA_FP8_E4M3 if fp8 else pa.PA_BF16)
 
     # ---- e2e: genuine decode steps through the public API with host buffers ----
     # Each step's inputs travel in one pinned staging buffer, copied to the device
@@ -444,9 +478,8 @@ def run_ours(args, rank, world, local_rank):
         dev_stage.copy_(hb, non_blocking=True)
         if len(pr):
             pa.pa_copy_blocks(dk, dv, e_pairs[: len(pr)], stream=stream)
-        pa.pa_reshape_and_cache(e_kn, e_vn, dk, dv, e_slots, stream=stream)
-        pa.pa_decode_attention(out, e_q, dk, dv, e_tables, e_lens, int(h_lens.max()), w.scale, ws,
-                               partition_tokens=PT, stream=stream)
+        append(e_kn, e_vn, e_slots, stream=stream)
+        attend(e_q, e_tables, e_lens, int(h_lens.max()), stream=stream)
         h_out.copy_(out.view(torch.int16), non_blocking=True)
         stream.synchronize()
         e2e_s += time.perf_counter() - t0
@@ -460,15 +493,18 @@ def run_ours(args, rank, world, local_rank):
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K, "warmup": Wm,
         "ms_per_step": total_s * 1e3 / K, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": "bf16", "data": f"synthetic, seeded: {WORKLOADS[args.workload]}; blocks scattered by a seeded free-list order",
+        "dtype": "fp8_e4m3 kv, bf16 q/out" if fp8 else "bf16",
+        "data": f"synthetic, seeded: {WORKLOADS[args.workload]}; blocks scattered by a seeded free-list order",
         "config": {
-            "workload": w.name if world == 1 else f"{w.name} per rank", "num_seqs_per_gpu": B, "num_q_heads": Hq,
+            "workload": (w.name + ("_fp8kv" if fp8 else "")) if world == 1 else f"{w.name} per rank",
+            "num_seqs_per_gpu": B, "num_q_heads": Hq,
             "num_kv_heads": Hkv, "head_dim": D, "block_size": bs, "kv_tokens_per_step": tokens_step,
             "decode_bytes_per_step": dbytes, "unique_block_kv_bytes_per_step": unique_kv, "pool_blocks": w.num_blocks,
             "l2": f"flushed between timed steps ({L2_FLUSH_BYTES >> 20} MiB write, then a {L2_FLUSH_BYTES >> 21} MiB read "
                   "so that no dirty line is left; untimed)",
             "host_alloc_us_per_step": round(host_alloc_us, 1), "decode_ctas": ctas, "stages": stages,
             "smem_bytes": smem, "path": "mma.sync" if mma else "fma", "partition_tokens": PT,
+            "kv_dtype": "fp8_e4m3" if fp8 else "bf16", **({"k_scale": KS, "v_scale": VS} if fp8 else {}),
             "decode_ms_median": statistics.median(dec_ms), "decode_ms_min": min(dec_ms),
             "step_gbs": (dbytes + 4 * B * Hkv * D * 2) / (total_s / K) / 1e9,
         },
@@ -483,7 +519,8 @@ def run_ours(args, rank, world, local_rank):
         "clocks": clocks.summary(),
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline(w, q, k_host, v_host, tables, lens, args.cpu_seconds)
+        line["cpu_baseline"] = cpu_baseline(w, q, k_host, v_host, tables, lens, args.cpu_seconds,
+                                            scales=(KS, VS) if fp8 else None)
     if rank == 0:
         print(json.dumps(line), flush=True)
     if dist:
@@ -933,6 +970,8 @@ def main(argv=None):
                     help="decode: the decode step (the headline); prefill: prompt prefill of the sampling prompts; "
                          "swap: the whole decode batch swapped to pinned host memory and back")
     ap.add_argument("--prompts", type=int, default=16, help="prefill path: prompts per step (at most 16)")
+    ap.add_argument("--kv", choices=["bf16", "fp8"], default="bf16",
+                    help="decode path: pool element type (fp8: E4M3 codes with per-pool scales, bf16 queries)")
     ap.add_argument("--prefix-cached", action="store_true",
                     help="prefill path: the prompts share all but their last 7 tokens, already cached")
     args = ap.parse_args(argv)
