@@ -199,7 +199,7 @@ pa_status pa_decode_launch_info(int32_t num_seqs, int32_t num_q_heads, int32_t n
 
 /*
  * Tuning: CTAs per SM of the decode grid (1..8; 0 restores the default: 4 on
- * the tensor-core path, otherwise as many as fit, at most 8).  Process-wide; affects later pa_decode_attention
+ * the bf16 tensor-core path, otherwise as many as fit, at most 8).  Process-wide; affects later pa_decode_attention
  * calls.  More CTAs per SM keep more tiles in flight but add split points
  * (partials) at CTA edges.
  */
@@ -220,7 +220,10 @@ pa_status pa_decode_set_ctas_per_sm(int32_t ctas);
  * pa_decode_attention_fp8: pa_decode_attention over FP8 pools with bf16 q
  * and out: out = softmax(scale q . (K code values * k_scale)) (V code values
  * * v_scale).  Same layouts, workspace (pa_decode_workspace_bytes), split
- * modes and error reporting; CUDA-core path.  k_scale and v_scale must be
+ * modes and error reporting.  4 or more query heads per KV head run on the
+ * tensor cores (each stage's codes widened to f16 in shared memory, f16
+ * mma.sync; the bf16 queries are rounded to f16, so their magnitudes must stay
+ * within f16 range), fewer on the CUDA cores.  k_scale and v_scale must be
  * finite and > 0.
  */
 pa_status pa_reshape_and_cache_fp8(const void* k_new, const void* v_new, void* k_pool, void* v_pool,

@@ -183,7 +183,7 @@ pa_status plan_launch(int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_head
     if (!current_device(&dev, &lp->sms)) return PA_ERR_CUDA;
     const int G = num_q_heads / num_kv_heads;
     // dtype is the pool's: PA_FP8_E4M3 pools pair with bf16 queries and take the CUDA-core path
-    lp->mma = (dtype == PA_BF16 && G >= 4);
+    lp->mma = ((dtype == PA_BF16 || dtype == PA_FP8_E4M3) && G >= 4);
     bool found = dtype == PA_F32         ? decode_variant_f32(head_dim, block_size, G, &lp->v)
                  : dtype == PA_FP8_E4M3 ? decode_variant_fp8(head_dim, block_size, G, &lp->v)
                  : lp->mma              ? decode_variant_bf16_mma(head_dim, block_size, &lp->v)
@@ -194,11 +194,12 @@ pa_status plan_launch(int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_head
     int occ = 0;
     if (!kernel_occupancy(dev, lp->v.kernel, lp->v.threads, lp->smem, &occ)) return PA_ERR_CUDA;
     if (occ <= 0) return PA_ERR_UNSUPPORTED;
-    // Default: the tensor-core path, which spends little time per tile, keeps
-    // four CTAs per SM (about 128 KB of tiles in flight, enough to cover HBM
-    // latency with fewer split points); the CUDA-core path takes as many as fit.
+    // Default: the bf16 tensor-core path, which spends little time per tile,
+    // keeps four CTAs per SM (about 128 KB of tiles in flight, enough to cover
+    // HBM latency with fewer split points); the CUDA-core path and the FP8
+    // tensor-core path (which widens every stage first) take as many as fit.
     int want = g_ctas_per_sm.load();
-    if (want <= 0) want = lp->mma ? kDefaultCtasPerSmMma : kMaxCtasPerSm;
+    if (want <= 0) want = lp->mma && dtype == PA_BF16 ? kDefaultCtasPerSmMma : kMaxCtasPerSm;
     const int per_sm = occ < want ? occ : want;
     int64_t grid = (int64_t)lp->sms * per_sm;
     const int64_t tiles_bound = (int64_t)num_seqs * num_kv_heads * max_tiles_per_head;

@@ -80,6 +80,9 @@ struct ElemBytes<__nv_fp8_e4m3> {  // FP8 pools (OCP E4M3 codes)
 #ifndef PA_STAGE_BYTES_FMA
 #define PA_STAGE_BYTES_FMA 16384
 #endif
+#ifndef PA_STAGE_BYTES_FP8  // tensor-core path over FP8 pools: a shallower ring, more CTAs per SM
+#define PA_STAGE_BYTES_FP8 16384
+#endif
 constexpr int stages_for(int ring_bytes, int bs, int d, int e) {
     int n = ring_bytes / (2 * bs * d * e);
     return n < 2 ? 2 : (n > 16 ? 16 : n);
@@ -91,14 +94,18 @@ template <typename T, int D, int BS, bool MMA, int GF, typename KV = T>
 struct Layout {
     static constexpr int E = ElemBytes<KV>::value;  // pool element bytes
     static constexpr int EQ = ElemBytes<T>::value;  // query / output element bytes
-    static constexpr int S = stages_for(MMA ? PA_STAGE_BYTES : PA_STAGE_BYTES_FMA, BS, D, E);
+    static constexpr int S = stages_for(MMA ? (E == 1 ? PA_STAGE_BYTES_FP8 : PA_STAGE_BYTES) : PA_STAGE_BYTES_FMA, BS, D, E);
     static constexpr int GN = GF > 0 ? GF : kMaxGroup;  // query rows a q slot holds
     static constexpr int kTileBytes = BS * D * E;  // K (or V) of one tile
     static constexpr int kPanels = D * E / 128;    // 128-byte column panels per row
     static constexpr int kStageBytes = 2 * kTileBytes;
     static constexpr int kQSlotBytes = GN * D * EQ;
     static constexpr int kStagesOff = 0;
-    static constexpr int kQOff = kStagesOff + S * kStageBytes;
+    // tensor-core path over an FP8 pool: one tile of K and one of V widened to f16
+    static constexpr bool kCvt = MMA && E == 1;
+    static constexpr int kCvtTileBytes = kCvt ? BS * D * 2 : 0;
+    static constexpr int kCvtOff = kStagesOff + S * kStageBytes;
+    static constexpr int kQOff = kCvtOff + 2 * kCvtTileBytes;
     // CUDA-core path only: fp32 query rows (pre-scaled) and one step's weights.
     static constexpr int kQfOff = kQOff + kQSlots * kQSlotBytes;
     static constexpr int kQfBytes = MMA ? 0 : GN * D * 4;
@@ -292,12 +299,30 @@ __device__ __forceinline__ void load_vec_f32(uint32_t addr, float* v) {
 // Tensor-core path.  Thread (g = lane/4, tig = lane%4) holds the running max
 // and sum of heads 2tig and 2tig+1, and O^T fragments o[mt] = rows (dims)
 // 16mt+g, 16mt+g+8 x columns (heads) 2tig, 2tig+1.
-template <int D, int BS>
+// F16: operands in f16 instead of bf16 (tiles widened from an FP8 pool; the
+// bf16 query rows are rounded to f16 when loaded).
+template <int D, int BS, bool F16 = false>
 struct MmaState {
     static constexpr int MT = D / 16;
     uint32_t qb[MT][2];  // B fragments of q^T per 16-dim k-step
     float m[2], l[2];
     float o[MT][4];
+
+    __device__ static __forceinline__ void mma16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                                    uint32_t b0, uint32_t b1) {
+        if constexpr (F16)
+            mma_f16_16816(d, a0, a1, a2, a3, b0, b1);
+        else
+            mma_bf16_16816(d, a0, a1, a2, a3, b0, b1);
+    }
+    __device__ static __forceinline__ uint32_t pack16(float lo, float hi) {
+        if constexpr (F16)
+            return pack_f16x2(lo, hi);
+        else
+            return pack_bf16x2(lo, hi);
+    }
+    __device__ static __forceinline__ float lo16(uint32_t v) { return F16 ? f16_lo(v) : bf16_lo(v); }
+    __device__ static __forceinline__ float hi16(uint32_t v) { return F16 ? f16_hi(v) : bf16_hi(v); }
 
     __device__ __forceinline__ void reset() {
         m[0] = m[1] = -INFINITY;
@@ -315,6 +340,10 @@ struct MmaState {
                 const uint32_t* row = reinterpret_cast<const uint32_t*>(qslot + (size_t)g * D * 2);
                 lo = row[(16 * s + 2 * tig) >> 1];
                 hi = row[(16 * s + 2 * tig + 8) >> 1];
+                if constexpr (F16) {
+                    lo = pack_f16x2(bf16_lo(lo), bf16_hi(lo));
+                    hi = pack_f16x2(bf16_lo(hi), bf16_hi(hi));
+                }
             }
             qb[s][0] = lo;
             qb[s][1] = hi;
@@ -333,7 +362,7 @@ struct MmaState {
             for (int s = 0; s < MT; ++s) {
                 uint32_t a0, a1, a2, a3;
                 ldmatrix_x4(kbase + tile_chunk_offset<BS>(row, 2 * s + csel), a0, a1, a2, a3);
-                mma_bf16_16816(acc[s & 1], a0, a1, a2, a3, qb[s][0], qb[s][1]);
+                mma16816(acc[s & 1], a0, a1, a2, a3, qb[s][0], qb[s][1]);
             }
         }
         // (token g, head 2tig), (g, 2tig+1), (g+8, 2tig), (g+8, 2tig+1)
@@ -350,11 +379,11 @@ struct MmaState {
         }
         const float mn0 = fmaxf(m[0], mx0), mn1 = fmaxf(m[1], mx1);
         const float al0 = exp2f(m[0] - mn0), al1 = exp2f(m[1] - mn1);
-        const uint32_t P0 = pack_bf16x2(exp2f(x0 - mn0), exp2f(x1 - mn1));
-        const uint32_t P1 = pack_bf16x2(exp2f(x2 - mn0), exp2f(x3 - mn1));
+        const uint32_t P0 = pack16(exp2f(x0 - mn0), exp2f(x1 - mn1));
+        const uint32_t P1 = pack16(exp2f(x2 - mn0), exp2f(x3 - mn1));
         // the sum uses the rounded weights that P V uses
-        l[0] = l[0] * al0 + bf16_lo(P0) + bf16_lo(P1);
-        l[1] = l[1] * al1 + bf16_hi(P0) + bf16_hi(P1);
+        l[0] = l[0] * al0 + lo16(P0) + lo16(P1);
+        l[1] = l[1] * al1 + hi16(P0) + hi16(P1);
         m[0] = mn0;
         m[1] = mn1;
 #pragma unroll
@@ -376,7 +405,7 @@ struct MmaState {
         for (int i = 0; i < MT; ++i) {
             uint32_t a0, a1, a2, a3;
             ldmatrix_x4_trans(vbase + tile_chunk_offset<BS>(row, 2 * i + csel), a0, a1, a2, a3);
-            mma_bf16_16816(o[i], a0 & m01, a1 & m01, a2 & m89, a3 & m89, b0, b1);
+            mma16816(o[i], a0 & m01, a1 & m01, a2 & m89, a3 & m89, b0, b1);
         }
     }
 
@@ -660,6 +689,38 @@ __device__ __forceinline__ bool merge_staged(const float* partials, size_t slot_
     return true;
 }
 
+// Widen one stage of an FP8 pool (K then V, BS rows of D codes each, one
+// 128-byte panel per row) to f16 tiles (BS rows of D halves, 128-byte panels),
+// both in the 128-byte-swizzled layout.  Every E4M3 value is exact in f16.
+template <int D, int BS>
+__device__ __forceinline__ void widen_fp8_stage(uint32_t src, uint32_t dst, int lane) {
+    constexpr int kSrcTile = BS * D, kDstTile = BS * D * 2, CPR = D / 16;  // 16-byte code chunks per row
+#pragma unroll
+    for (int i = lane; i < 2 * BS * CPR; i += 32) {
+        const int kv = i / (BS * CPR), r = (i / CPR) % BS, c = i % CPR;
+        uint32_t w[4];
+        asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                     : "=r"(w[0]), "=r"(w[1]), "=r"(w[2]), "=r"(w[3])
+                     : "r"(src + kv * kSrcTile + tile_chunk_offset<BS>(r, c)));
+        uint32_t h[8];
+#pragma unroll
+        for (int j = 0; j < 4; ++j)  // each code pair to an f16 pair, low code to the low half
+            asm("{\n\t.reg .b16 lo, hi;\n\t"
+                "mov.b32 {lo, hi}, %2;\n\t"
+                "cvt.rn.f16x2.e4m3x2 %0, lo;\n\t"
+                "cvt.rn.f16x2.e4m3x2 %1, hi;\n\t}"
+                : "=r"(h[2 * j]), "=r"(h[2 * j + 1])
+                : "r"(w[j]));
+        const uint32_t d = dst + kv * kDstTile;
+        asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(d + tile_chunk_offset<BS>(r, 2 * c)), "r"(h[0]),
+                     "r"(h[1]), "r"(h[2]), "r"(h[3])
+                     : "memory");
+        asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(d + tile_chunk_offset<BS>(r, 2 * c + 1)),
+                     "r"(h[4]), "r"(h[5]), "r"(h[6]), "r"(h[7])
+                     : "memory");
+    }
+}
+
 // ---------------------------------------------------------------------------
 // The kernel
 // ---------------------------------------------------------------------------
@@ -880,7 +941,7 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const DecodeParams p, 
         }
         float* qf = reinterpret_cast<float*>(base + L::kQfOff);
         float* ptile = reinterpret_cast<float*>(base + L::kPTileOff);
-        typename std::conditional<MMA, MmaState<D, BS>, FmaState<KV, D, BS, GF>>::type st;
+        typename std::conditional<MMA, MmaState<D, BS, L::kCvt>, FmaState<KV, D, BS, GF>>::type st;
         uint32_t k = 0, pi = 0;
         PieceIter it;
         it.init(P, t0, t1);
@@ -906,22 +967,33 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const DecodeParams p, 
             for (int i = 0; i < ntile; ++i) {
                 const uint32_t kk = k + i;
                 const int sidx = kk % S;
+                bool released = false;
                 if (role_wait(full_bar(sidx), (kk / S) & 1, misc, p.status)) {
-                    const uint32_t kb = base_s + L::kStagesOff + sidx * L::kStageBytes;
+                    uint32_t kb = base_s + L::kStagesOff + sidx * L::kStageBytes;
+                    uint32_t vb = kb + L::kTileBytes;
+                    if constexpr (L::kCvt) {
+                        // widen the codes, hand the stage back to the producer, compute on the copy
+                        widen_fp8_stage<D, BS>(kb, base_s + L::kCvtOff, lane);
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(empty_bar(sidx));
+                        released = true;
+                        kb = base_s + L::kCvtOff;
+                        vb = kb + L::kCvtTileBytes;
+                    }
                     const int tok0 = (j0 + i) * BS;
 #pragma unroll
                     for (int sub = 0; sub < BS / 16; ++sub) {
                         const int valid = min(16, len - (tok0 + sub * 16));
                         if (valid > 0) {
                             if constexpr (MMA)
-                                st.step(kb, kb + L::kTileBytes, sub * 16, valid, p.scale_log2, lane);
+                                st.step(kb, vb, sub * 16, valid, p.scale_log2, lane);
                             else
-                                st.step(kb, kb + L::kTileBytes, sub * 16, valid, G, qf, ptile, lane);
+                                st.step(kb, vb, sub * 16, valid, G, qf, ptile, lane);
                         }
                     }
                 }
                 __syncwarp();
-                if (lane == 0) mbar_arrive(empty_bar(sidx));
+                if (lane == 0 && !released) mbar_arrive(empty_bar(sidx));
             }
             k += ntile;
             if constexpr (MMA) st.finish();

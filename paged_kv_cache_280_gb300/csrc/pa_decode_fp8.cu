@@ -1,7 +1,8 @@
-// Decode over FP8 (E4M3) pools with bf16 queries and outputs, CUDA-core path
-// (exact instantiations for 1, 2, 4 and 8 query heads per KV head, a
-// run-time-group fallback otherwise).  head_dim 128: one pool row is one
-// 128-byte swizzle panel.
+// Decode over FP8 (E4M3) pools with bf16 queries and outputs.  4 or more
+// query heads per KV head take the tensor-core path (each stage's codes widened
+// to f16 in shared memory, f16 mma.sync); 1-3 take the CUDA-core path (exact
+// instantiations for 1 and 2, a run-time-group fallback for 3).  head_dim 128:
+// one pool row is one 128-byte swizzle panel.
 #include "pa_decode.cuh"
 
 namespace pa {
@@ -10,11 +11,14 @@ template <int BS>
 static bool pick(int group, DecodeVariant* out) {
     using T = __nv_bfloat16;
     using KV = __nv_fp8_e4m3;
+    // 4+ query heads per KV head: the tensor-core path, each stage widened to f16 in shared memory
+    if (group >= 4) {
+        *out = VariantOf<T, 128, BS, true, 0, KV>::get();
+        return true;
+    }
     switch (group) {
         case 1: *out = VariantOf<T, 128, BS, false, 1, KV>::get(); return true;
         case 2: *out = VariantOf<T, 128, BS, false, 2, KV>::get(); return true;
-        case 4: *out = VariantOf<T, 128, BS, false, 4, KV>::get(); return true;
-        case 8: *out = VariantOf<T, 128, BS, false, 8, KV>::get(); return true;
         default: *out = VariantOf<T, 128, BS, false, 0, KV>::get(); return true;
     }
 }
