@@ -139,7 +139,8 @@ pa_status pa_decode_workspace_bytes(int32_t num_seqs, int32_t num_q_heads, int32
  * sequence gives a zero output.
  * Long sequences are split across CTAs (flash-decoding) and the partial
  * results merged on the device.  partition_tokens = 0 splits anywhere on a
- * block boundary to balance the work exactly; partition_tokens = P > 0
+ * block boundary, so that every CTA gets the same share of blocks plus a
+ * fixed cost per (sequence, KV head) it touches; partition_tokens = P > 0
  * (a multiple of block_size) allows splits only at multiples of P tokens.
  * max_seq_len bounds every seq_lens[b]; a larger or negative length sets
  * PA_DEV_BAD_SEQ_LEN and is clamped.  Table entries read for t < seq_len

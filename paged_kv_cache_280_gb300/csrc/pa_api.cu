@@ -313,6 +313,7 @@ pa_status decode_common(void* out, const void* q, const void* k_pool, const void
     p.group = num_q_heads / num_kv_heads;
     p.partition_tiles = partition_tokens / block_size;
     p.num_ctas = lp.grid;
+    p.seg_units = lp.mma ? PA_SEG_UNITS_MMA : PA_SEG_UNITS_FMA;
     p.scale_log2 = scale * 1.4426950408889634f * k_scale;
     p.out_scale = v_scale;
     lp.v.launch(p, tk, tv, lp.grid, lp.smem, static_cast<cudaStream_t>(stream));

@@ -111,10 +111,9 @@ struct Layout {
     static constexpr int kQfBytes = MMA ? 0 : GN * D * 4;
     static constexpr int kPTileOff = kQfOff + kQfBytes;
     static constexpr int kPTileBytes = MMA ? 0 : 16 * GN * 4;
-    // per-piece weights and per-head running max / sum when merging a split segment
-    static constexpr int kMergeOff = kPTileOff + kPTileBytes;
-    static constexpr int kMergeBytes = (kMaxMergeChunk * kMaxGroup + 4 * kMaxGroup) * 4;
-    static constexpr int kBarOff = kMergeOff + kMergeBytes;
+    // the CTA's split segments (at most two): sequence, KV head, first CTA, pieces
+    static constexpr int kPendOff = kPTileOff + kPTileBytes;
+    static constexpr int kBarOff = kPendOff + 2 * 4 * 4;
     static constexpr int kMiscOff = kBarOff + (2 * S + 2 * kQSlots + 1) * 8;
     static constexpr int kPrefixOff = kMiscOff + 64;
     static_assert(kTileBytes % 1024 == 0, "tiles must keep 1024-byte alignment for the 128B swizzle");
@@ -127,12 +126,21 @@ struct Layout {
     }
 };
 
+// a / b with a 32-bit divide when both fit (the common case): the 64-bit one
+// is a long instruction sequence, and the plan runs before any tile is issued
+__device__ __forceinline__ int64_t div_nonneg(int64_t a, int64_t b) {
+    if (((uint64_t)a >> 32) == 0 && ((uint64_t)b >> 32) == 0) return (int64_t)((uint32_t)a / (uint32_t)b);
+    return a / b;
+}
+
 // Where the tiles of one CTA start and end, and who holds which partial.
 struct Plan {
     const int32_t* pref;   // pref[b] = blocks of sequences < b (per KV head)
     const int32_t* upref;  // same in partitions (fixed mode)
     int32_t B, Hkv, C, PT;
-    int64_t T, U;  // total tiles, total partitions
+    int32_t A;     // no partitions: a tile weighs kTileUnits units, a segment A more
+    static constexpr int K = kTileUnits;
+    int64_t T, U;  // total tiles; total partitions, or total weighted units
 
     __device__ __forceinline__ int nblocks(int b) const { return pref[b + 1] - pref[b]; }
     __device__ __forceinline__ int64_t seg_start(int b, int h) const {
@@ -158,13 +166,44 @@ struct Plan {
         int h = (int)(local / ub), part = (int)(local % ub);
         return seg_start(b, h) + (int64_t)part * PT;
     }
+    // Weighted units (no partitions): tile t of segment (b, h) sits at unit
+    //   K t + A (Hkv b + h + 1),
+    // i.e. every segment's tiles are preceded by A units of fixed work.
+    __device__ __forceinline__ int64_t unit_of_tile(int64_t t) const {
+        const int b = find_seq(pref, t);
+        const int h = (int)((t - (int64_t)Hkv * pref[b]) / nblocks(b));
+        return (int64_t)K * t + (int64_t)A * ((int64_t)Hkv * b + h + 1);
+    }
+    // the first tile at or after weighted unit x
+    __device__ __forceinline__ int64_t first_tile_at_unit(int64_t x) const {
+        int lo = 0, hi = B - 1;  // largest b whose units start at or before x
+        while (lo < hi) {
+            const int mid = (lo + hi + 1) >> 1;
+            if ((int64_t)Hkv * ((int64_t)K * pref[mid] + (int64_t)A * mid) <= x)
+                lo = mid;
+            else
+                hi = mid - 1;
+        }
+        const int b = lo, nb = nblocks(b);
+        const int64_t local = x - (int64_t)Hkv * ((int64_t)K * pref[b] + (int64_t)A * b);
+        const int64_t span = (int64_t)K * nb + A;  // units of one segment of sequence b
+        if (span == 0) return (int64_t)Hkv * pref[b];  // A = 0 and b empty: not reached (b is the last with its start)
+        const int64_t h = div_nonneg(local, span), r = local - h * span;
+        const int64_t j = r <= A ? 0 : (r - A + K - 1) / K;  // at most nb: then the next segment's first tile
+        return (int64_t)Hkv * pref[b] + h * nb + j;
+    }
     __device__ __forceinline__ int64_t cta_start(int c) const {
-        if (PT == 0) return (int64_t)c * T / C;
+        if (PT == 0) return c >= C ? T : first_tile_at_unit(div_nonneg(c * U + C - 1, C));
         return tile_of_unit((int64_t)c * U / C);
+    }
+    // the CTA whose range holds tile t of segment (b, h)
+    __device__ __forceinline__ int cta_of_seg(int64_t t, int b, int h) const {
+        if (PT == 0) return (int)div_nonneg(((int64_t)K * t + (int64_t)A * ((int64_t)Hkv * b + h + 1)) * C, U);
+        return cta_of(t);
     }
     // the CTA whose range holds tile t
     __device__ __forceinline__ int cta_of(int64_t t) const {
-        if (PT == 0) return (int)(((t + 1) * C - 1) / T);
+        if (PT == 0) return (int)(unit_of_tile(t) * C / U);
         int b = find_seq(pref, t);
         int64_t local = t - (int64_t)Hkv * pref[b];
         int nb = nblocks(b), ub = upref[b + 1] - upref[b];
@@ -595,92 +634,121 @@ struct FmaState {
     }
 };
 
+// Partial slot of piece cc of a split segment whose first piece is in CTA ca.
+// A split segment's first piece is the last piece of its CTA's range (slot 1);
+// every later piece starts its CTA's range (slot 0).  A CTA's two slots are
+// never both needed by one piece.
+__device__ __forceinline__ const float* piece_slot(const float* partials, size_t slot_floats, int cc, int ca) {
+    return partials + (size_t)(2 * cc + (cc == ca ? 1 : 0)) * slot_floats;
+}
+
+// Lane 0: bulk-copy the partial slots of pieces ca+c0 .. ca+c0+nc-1 to shared
+// address dst, completing on mbar (whose expected bytes the caller sets).
+// Other CTAs wrote the slots (made visible by the counter protocol) and this
+// warp last read the destination through the generic proxy.
+__device__ __forceinline__ void stage_pieces(const float* partials, size_t slot_floats, int ca, int c0, int nc,
+                                             uint32_t dst, uint32_t mbar) {
+    const uint32_t slot_bytes = (uint32_t)(slot_floats * 4);
+    for (int i = 0; i < nc; ++i)
+        bulk_load(dst + i * slot_bytes, piece_slot(partials, slot_floats, ca + c0 + i, ca), slot_bytes, mbar);
+}
+
+// 16 output elements (fp32 sums times sc) to 16-byte-aligned global memory.
+template <typename T>
+__device__ __forceinline__ void store16(T* dst, const float (&a)[16], float sc) {
+    if constexpr (std::is_same<T, float>::value) {
+        float4* d = reinterpret_cast<float4*>(dst);
+#pragma unroll
+        for (int v = 0; v < 4; ++v) d[v] = make_float4(a[4 * v] * sc, a[4 * v + 1] * sc, a[4 * v + 2] * sc, a[4 * v + 3] * sc);
+    } else {
+        uint4* d = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+        for (int v = 0; v < 2; ++v)
+            d[v] = make_uint4(pack_bf16x2(a[8 * v] * sc, a[8 * v + 1] * sc), pack_bf16x2(a[8 * v + 2] * sc, a[8 * v + 3] * sc),
+                              pack_bf16x2(a[8 * v + 4] * sc, a[8 * v + 5] * sc), pack_bf16x2(a[8 * v + 6] * sc, a[8 * v + 7] * sc));
+    }
+}
+
 // Merge of a split segment, done by the consumer warp of the CTA that
 // completed its last piece, after that warp's own pieces are done:
 //   M = max_p m_p,   out = sum_p e^(m_p-M) o_p / sum_p e^(m_p-M) l_p.
-// The pieces' partial slots are bulk-copied into the idle stage ring a chunk
-// at a time (one round trip per chunk); each head's running max and sum are
-// folded per chunk, then every output element is summed over the chunk's
-// slots straight from shared memory (one register per element, so nothing
-// spills whatever the group size).  When the pieces take more than one chunk
-// the running sums sit at the end of the ring, after the staged slots.
+// The np pieces' partial slots are bulk-copied into the idle stage ring a
+// chunk at a time (one round trip per chunk).  Each lane owns 16 consecutive
+// output elements of one head per pass of 512 elements: it folds that head's
+// max and sum itself and sums its elements over the staged slots with 16-byte
+// shared loads.  So the merge needs no scratch and no warp synchronisation,
+// and stays short: it runs once per CTA, from a cold instruction cache.  When
+// the pieces take more than one chunk, each lane keeps its running sums at
+// the end of the ring, after the staged slots.
+// staged_at >= 0: the caller already staged all the slots, in one chunk, at
+// that byte offset of the ring.
 template <typename T, int D>
-__device__ __forceinline__ bool merge_staged(const float* partials, size_t slot_floats, T* orow, int ca, int cb,
-                                             bool ca_split, int G, int lane, const uint8_t* ring, uint32_t ring_s,
-                                             int ring_bytes, float* work, uint32_t mbar, uint32_t& mphase,
-                                             float oscale) {
+__device__ __forceinline__ bool merge_staged(const float* partials, size_t slot_floats, T* orow, int ca, int np, int G,
+                                             int lane, uint32_t ring_s, int ring_bytes,
+                                             int staged_at, uint32_t mbar, uint32_t& mphase, float oscale) {
+    constexpr int kPass = (kMaxGroup * D + 511) / 512;
     const uint32_t slot_bytes = (uint32_t)(slot_floats * 4);
-    const int np = cb - ca + 1, nel = G * D;
+    const int nel = G * D;
     const int acc_bytes = (nel * 4 + 15) & ~15;
     int per_chunk = min(ring_bytes / (int)slot_bytes, kMaxMergeChunk);
     const bool multi = np > per_chunk;
     if (multi) per_chunk = min((ring_bytes - acc_bytes) / (int)slot_bytes, kMaxMergeChunk);
-    if (per_chunk < 1) return false;  // cannot happen for the instantiated shapes
-    float* wgt = work;                               // [kMaxMergeChunk][kMaxGroup]
-    float* hst = work + kMaxMergeChunk * kMaxGroup;  // [0..7] max, [8..15] sum, [16..23] rescale, [24..31] oscale/sum
-    const float* buf = reinterpret_cast<const float*>(ring);
-    float* acc_s = reinterpret_cast<float*>(const_cast<uint8_t*>(ring) + ring_bytes - acc_bytes);
-    auto slot_of = [&](int cc) { return partials + (size_t)(2 * cc + (cc == ca && ca_split ? 1 : 0)) * slot_floats; };
-    if (lane < G) {
-        hst[lane] = -INFINITY;
-        hst[8 + lane] = 0.f;
-    }
+    if (per_chunk < 1 || (staged_at >= 0 && multi)) return false;  // cannot happen for the instantiated shapes
+    const uint32_t acc_s = ring_s + (uint32_t)(ring_bytes - acc_bytes);
+    const uint32_t buf = ring_s + (uint32_t)(staged_at >= 0 ? staged_at : 0);
+    float mrun[kPass], lrun[kPass];
+#pragma unroll
+    for (int ps = 0; ps < kPass; ++ps) mrun[ps] = -INFINITY, lrun[ps] = 0.f;
     for (int c0 = 0; c0 < np; c0 += per_chunk) {
         const int nc = min(per_chunk, np - c0);
-        __syncwarp();
-        if (lane == 0) {
-            // other CTAs wrote the slots (made visible by the counter protocol);
-            // this warp last read the ring through the generic proxy
-            fence_proxy_async_global();
-            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-            mbar_arrive_expect_tx(mbar, nc * slot_bytes);
-            for (int i = 0; i < nc; ++i) bulk_load(ring_s + i * slot_bytes, slot_of(ca + c0 + i), slot_bytes, mbar);
-        }
-        // a bounded wait that also runs after an abort, so no copy is left in flight
-        bool ok = mbar_wait(mbar, mphase & 1);
-        ok = __all_sync(0xffffffffu, ok);
-        ++mphase;
-        if (!ok) return false;
-        if (lane < G) {
-            const int hd = lane;
-            float Mc = hst[hd];
-            for (int i = 0; i < nc; ++i) Mc = fmaxf(Mc, buf[i * slot_floats + G * D + 2 * hd]);
-            const float resc = exp2f(hst[hd] - Mc);
-            float Lr = hst[8 + hd] * resc;
-            for (int i = 0; i < nc; ++i) {
-                const float w = exp2f(buf[i * slot_floats + G * D + 2 * hd] - Mc);
-                wgt[i * kMaxGroup + hd] = w;
-                Lr = fmaf(w, buf[i * slot_floats + G * D + 2 * hd + 1], Lr);
+        if (staged_at < 0) {
+            __syncwarp();
+            if (lane == 0) {
+                fence_proxy_async_global();
+                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                mbar_arrive_expect_tx(mbar, nc * slot_bytes);
+                stage_pieces(partials, slot_floats, ca, c0, nc, buf, mbar);
             }
-            hst[hd] = Mc;
-            hst[8 + hd] = Lr;
-            hst[16 + hd] = resc;
-            hst[24 + hd] = oscale / Lr;
+            // a bounded wait that also runs after an abort, so no copy is left in flight
+            bool ok = mbar_wait(mbar, mphase & 1);
+            ok = __all_sync(0xffffffffu, ok);
+            ++mphase;
+            if (!ok) return false;
         }
-        __syncwarp();
-        const bool final_chunk = c0 + nc >= np;
-        // four independent sums per lane (elements e0 + 32u)
-        for (int e0 = lane; e0 < nel; e0 += 128) {
-            float a[4] = {0.f, 0.f, 0.f, 0.f};
-            int hd[4];
 #pragma unroll
-            for (int u = 0; u < 4; ++u) hd[u] = min((e0 + 32 * u) / D, G - 1);
-            for (int i = 0; i < nc; ++i) {
-                const float* bi = buf + i * slot_floats + e0;
+        for (int ps = 0; ps < kPass; ++ps) {
+            const int e0 = ps * 512 + lane * 16;
+            if (e0 < nel) {
+                const uint32_t ml = buf + (uint32_t)(nel + 2 * (e0 / D)) * 4;  // (m, l) of this head, slot 0
+                float mc = mrun[ps];
+                for (int i = 0; i < nc; ++i) mc = fmaxf(mc, lds_f32(ml + i * slot_bytes));
+                const float resc = exp2f(mrun[ps] - mc);  // 0 on the first chunk
+                float lr = lrun[ps] * resc;
+                float a[16];
 #pragma unroll
-                for (int u = 0; u < 4; ++u)
-                    if (e0 + 32 * u < nel) a[u] = fmaf(wgt[i * kMaxGroup + hd[u]], bi[32 * u], a[u]);
-            }
+                for (int v = 0; v < 4; ++v) {
+                    const float4 x = c0 > 0 ? lds_f32x4(acc_s + (uint32_t)(e0 + 4 * v) * 4) : make_float4(0.f, 0.f, 0.f, 0.f);
+                    a[4 * v] = x.x * resc, a[4 * v + 1] = x.y * resc, a[4 * v + 2] = x.z * resc, a[4 * v + 3] = x.w * resc;
+                }
+                for (int i = 0; i < nc; ++i) {
+                    const float2 m_l = lds_f32x2(ml + i * slot_bytes);
+                    const float w = exp2f(m_l.x - mc);
+                    lr = fmaf(w, m_l.y, lr);
+                    const uint32_t src = buf + i * slot_bytes + (uint32_t)e0 * 4;
 #pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                const int e = e0 + 32 * u;
-                if (e < nel) {
-                    float v = a[u];
-                    if (c0 > 0) v = fmaf(acc_s[e], hst[16 + hd[u]], v);
-                    if (final_chunk)
-                        orow[e] = from_float<T>(v * hst[24 + hd[u]]);
-                    else
-                        acc_s[e] = v;
+                    for (int v = 0; v < 4; ++v) {
+                        const float4 x = lds_f32x4(src + 16 * v);
+                        a[4 * v] = fmaf(w, x.x, a[4 * v]), a[4 * v + 1] = fmaf(w, x.y, a[4 * v + 1]);
+                        a[4 * v + 2] = fmaf(w, x.z, a[4 * v + 2]), a[4 * v + 3] = fmaf(w, x.w, a[4 * v + 3]);
+                    }
+                }
+                mrun[ps] = mc, lrun[ps] = lr;
+                if (c0 + nc >= np) {
+                    store16(orow + e0, a, __fdividef(oscale, lr));  // lr >= 1: the largest piece max weighs 1
+                } else {
+#pragma unroll
+                    for (int v = 0; v < 4; ++v)
+                        sts_f32x4(acc_s + (uint32_t)(e0 + 4 * v) * 4, a[4 * v], a[4 * v + 1], a[4 * v + 2], a[4 * v + 3]);
                 }
             }
         }
@@ -822,11 +890,14 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const DecodeParams p, 
     P.B = B;
     P.Hkv = Hkv;
     P.PT = p.partition_tiles;
+    P.A = p.seg_units;
     P.T = (int64_t)Hkv * pref[B];
-    P.U = fixed ? (int64_t)Hkv * upref[B] : 0;
-    // Only the first min(C, T) CTAs (min(C, U) with partitions) take work, so every
-    // working CTA owns a non-empty range and a split segment's pieces come from
-    // consecutive CTAs -- which the merge count and slot rule rely on.
+    P.U = fixed ? (int64_t)Hkv * upref[B] : (int64_t)P.K * P.T + (int64_t)P.A * Hkv * B;
+    // Only the first min(C, T) CTAs (min(C, U) with partitions) take work.  A split
+    // segment's pieces then come from consecutive CTAs, which the merge count and
+    // slot rule rely on: with partitions every working CTA owns at least one;
+    // without, a range is at least K units wide, so no range falls between two
+    // tiles of one segment (only in the gap at a segment's start can one be empty).
     const int64_t units = fixed ? P.U : P.T;
     int64_t ce = units < (int64_t)C ? units : C;
     if (fixed && ce > 0) {
@@ -838,10 +909,14 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const DecodeParams p, 
     }
     P.C = (int32_t)ce;
     const bool works = P.T > 0 && c < P.C;
-    const int64_t t0 = works ? P.cta_start(c) : 0;
-    const int64_t t1 = works ? P.cta_start(c + 1) : 0;
+    // the two ends of the range are two independent searches: lanes 0 and 1 of
+    // each warp run one each
+    int64_t tb = 0;
+    if (works && lane < 2) tb = P.cta_start(c + lane);
+    const int64_t t0 = __shfl_sync(0xffffffffu, tb, 0);
+    const int64_t t1 = __shfl_sync(0xffffffffu, tb, 1);
     const int Hq = p.num_q_heads;
-    // one partial slot: [G][D] unnormalised o, then [4 quarters][G] (m, l)
+    // one partial slot: [G][D] unnormalised o, then [G] (m, l)
     const size_t slot_floats = partial_slot_floats(G, D);
 
     if (warp == kProducerWarp) {
@@ -947,8 +1022,10 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const DecodeParams p, 
         it.init(P, t0, t1);
         int b, h, j0, j1;
         bool at_t0;
-        // split pieces of this CTA, counted after the loop (at most two: its range's ends)
-        int npend = 0, mb0 = 0, mh0 = 0, mb1 = 0, mh1 = 0;
+        // split pieces of this CTA, counted after the loop (at most two: its range's
+        // ends); pend[4 i ..] = sequence, KV head, first CTA of the segment, pieces
+        int npend = 0;
+        int32_t* pend = reinterpret_cast<int32_t*>(base + L::kPendOff);
         while (it.next(P, b, h, j0, j1, at_t0)) {
             const int qs = pi % kQSlots;
             const uint8_t* qslot = base + L::kQOff + qs * L::kQSlotBytes;
@@ -1006,12 +1083,13 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const DecodeParams p, 
                 // after the loop, so the fence and the atomic round trip stall
                 // this warp once, not once per split piece.  A CTA holds at most
                 // two split pieces (the first and the last of its range).
-                float* slot = p.partials + (size_t)(2 * c + (at_t0 ? 0 : 1)) * slot_floats;
+                float* slot = p.partials + (size_t)(2 * c + (j0 > 0 ? 0 : 1)) * slot_floats;
                 st.store_partial(slot, G, lane);
-                if (npend == 0) {
-                    mb0 = b, mh0 = h;
-                } else {
-                    mb1 = b, mh1 = h;
+                if (lane == 0) {
+                    const int64_t s0 = P.seg_start(b, h);
+                    const int ca = P.cta_of_seg(s0, b, h);
+                    int32_t* r = pend + 4 * npend;
+                    r[0] = b, r[1] = h, r[2] = ca, r[3] = P.cta_of_seg(s0 + nb - 1, b, h) - ca + 1;
                 }
                 ++npend;
             }
@@ -1019,39 +1097,65 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const DecodeParams p, 
         }
         // Count this CTA's split pieces; the CTA that completes the last piece of
         // segment (b, h) (an atomic counter per segment) merges its partials.
+        // Both counters are bumped before either result is read, so the two
+        // atomics take one round trip.
+        __syncwarp();
         int lastmask = 0;
         if (npend > 0) {
             __threadfence();
             __syncwarp();
             if (lane == 0) {
-                for (int i = 0; i < npend; ++i) {
-                    const int mb = i ? mb1 : mb0, mh = i ? mh1 : mh0;
-                    const int64_t s0 = P.seg_start(mb, mh);
-                    const int span = P.cta_of(s0 + P.nblocks(mb) - 1) - P.cta_of(s0);
-                    if (atomicAdd(p.counters + (size_t)mb * Hkv + mh, 1) == span) lastmask |= 1 << i;
-                }
+                const int old0 = atomicAdd(p.counters + (size_t)pend[0] * Hkv + pend[1], 1);
+                const int old1 = npend > 1 ? atomicAdd(p.counters + (size_t)pend[4] * Hkv + pend[5], 1) : -1;
+                if (old0 == pend[3] - 1) lastmask |= 1;
+                if (npend > 1 && old1 == pend[7] - 1) lastmask |= 2;
                 if (lastmask) __threadfence();
             }
             lastmask = __shfl_sync(0xffffffffu, lastmask, 0);
         }
         // The stage ring is idle now (every issued tile has been consumed): use it
-        // to stage the partials of the split segments this CTA completed.
+        // to stage the partials of the split segments this CTA completed.  When it
+        // completed both, and both sets of slots fit in the ring together, they are
+        // staged with one round trip.
         uint32_t mphase = 0;
+        const int ring_bytes = S * L::kStageBytes;
+        const uint32_t slot_bytes = (uint32_t)(slot_floats * 4);
+        int staged0 = -1, staged1 = -1;  // ring offsets of pre-staged slots
+        if (lastmask == 3 && (pend[3] + pend[7]) * (int)slot_bytes <= ring_bytes && pend[3] <= kMaxMergeChunk &&
+            pend[7] <= kMaxMergeChunk) {
+            if (lane == 0) {
+                fence_proxy_async_global();
+                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                mbar_arrive_expect_tx(merge_bar, (pend[3] + pend[7]) * slot_bytes);
+                stage_pieces(p.partials, slot_floats, pend[2], 0, pend[3], base_s, merge_bar);
+                stage_pieces(p.partials, slot_floats, pend[6], 0, pend[7],
+                             base_s + pend[3] * slot_bytes, merge_bar);
+            }
+            // bounded, and run by every lane, so no copy is left in flight
+            bool ok = mbar_wait(merge_bar, mphase & 1);
+            ok = __all_sync(0xffffffffu, ok);
+            ++mphase;
+            if (!ok) {
+                misc[0] = 1;
+                if (lane == 0) flag_status(p.status, PA_DEV_WAIT_TIMEOUT);
+                lastmask = 0;
+            } else {
+                staged0 = 0;
+                staged1 = pend[3] * (int)slot_bytes;
+            }
+        }
 #pragma unroll 1
         for (int i = 0; i < npend; ++i) {
             if (!(lastmask & (1 << i))) continue;
-            const int mb = i ? mb1 : mb0, mh = i ? mh1 : mh0;
-            const int64_t s0 = P.seg_start(mb, mh);
-            const int ca = P.cta_of(s0), cb = P.cta_of(s0 + P.nblocks(mb) - 1);
-            T* orow = static_cast<T*>(p.out) + ((size_t)mb * Hq + (size_t)mh * G) * D;
-            if (!merge_staged<T, D>(p.partials, slot_floats, orow, ca, cb, s0 != P.cta_start(ca), G, lane, base,
-                                    base_s, S * L::kStageBytes, reinterpret_cast<float*>(base + L::kMergeOff),
-                                    merge_bar, mphase, p.out_scale)) {
+            const int32_t* r = pend + 4 * i;
+            T* orow = static_cast<T*>(p.out) + ((size_t)r[0] * Hq + (size_t)r[1] * G) * D;
+            if (!merge_staged<T, D>(p.partials, slot_floats, orow, r[2], r[3], G, lane, base_s,
+                                    ring_bytes, i ? staged1 : staged0, merge_bar, mphase, p.out_scale)) {
                 misc[0] = 1;
                 if (lane == 0) flag_status(p.status, PA_DEV_WAIT_TIMEOUT);
                 break;
             }
-            if (lane == 0) p.counters[(size_t)mb * Hkv + mh] = 0;
+            if (lane == 0) p.counters[(size_t)r[0] * Hkv + r[1]] = 0;
         }
     }
     __syncthreads();

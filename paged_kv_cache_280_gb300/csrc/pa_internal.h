@@ -21,6 +21,18 @@ inline __host__ __device__ size_t partial_slot_floats(int G, int D) {
 }
 constexpr int kMaxSmem = 227 * 1024;
 
+// Cost weights of the range balance (see DecodeParams): 4 units a tile, and a
+// segment's fixed work in units per compute path.  Measured per-CTA loop ends
+// put a piece's fixed work near one tile of the stream on the tensor-core path
+// (4 CTAs per SM) and near half a tile on the CUDA-core path (8 CTAs per SM).
+constexpr int kTileUnits = 4;
+#ifndef PA_SEG_UNITS_MMA
+#define PA_SEG_UNITS_MMA 4
+#endif
+#ifndef PA_SEG_UNITS_FMA
+#define PA_SEG_UNITS_FMA 2
+#endif
+
 struct DecodeParams {
     void* out;
     const void* q;
@@ -38,6 +50,10 @@ struct DecodeParams {
     int32_t group;            // G = num_q_heads / num_kv_heads
     int32_t partition_tiles;  // 0: split anywhere; else splits only at multiples of this
     int32_t num_ctas;
+    // Without partitions, CTA ranges balance a cost in which a tile weighs
+    // kTileUnits and every (sequence, KV head) segment seg_units more: the
+    // fixed work of a piece (query load, softmax state, output store).
+    int32_t seg_units;
     float scale_log2;  // scale * log2(e) (times the K scale of an FP8 pool): scores in the base-2 domain
     float out_scale;   // multiplies the output: the V scale of an FP8 pool, else 1
 };

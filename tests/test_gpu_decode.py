@@ -81,6 +81,35 @@ def test_more_ctas_than_tiles():
     check_close(to_numpy(c.dout), c.oracle(), "f32")
 
 
+@pytest.mark.parametrize("dtype,hq,hkv,d,bs", [("bf16", 8, 2, 128, 16), ("f32", 2, 2, 64, 16)])
+def test_empty_ranges_and_long_merges(dtype, hq, hkv, d, bs):
+    """Runs of empty sequences between long ones, at 8 CTAs per SM over a few hundred
+    tiles.  Without partitions the ranges balance tiles plus a fixed cost per segment, so
+    ranges that fall in the gap before a segment are empty; long segments split into
+    pieces of a tile or two and merge over several staged chunks."""
+    import paged_kv_cache_280_gb300 as pa
+    import torch
+
+    w = W.random_case(31 + hq, 24, hq, hkv, d, bs, dtype, max_len=700, min_len=1)
+    lens = np.zeros(24, np.int32)
+    lens[[3, 9, 10, 17, 23]] = [700, 1, 333, 16 * 40, 47]
+    c = DecodeCase(w, lengths=lens).device()
+    ref = c.oracle()
+    try:
+        pa.pa_decode_set_ctas_per_sm(8)
+        ws = c.run()
+        first = to_numpy(c.dout).copy()
+        c.run(ws=ws)
+        assert np.array_equal(first, to_numpy(c.dout))
+    finally:
+        pa.pa_decode_set_ctas_per_sm(0)
+    check_close(first, ref, dtype)
+    assert status_word(ws) == 0
+    assert not first[lens == 0].any()
+    counters = ws[256:256 + 4 * 24 * hkv].view(dtype=torch.int32)
+    assert int(counters.abs().sum().item()) == 0
+
+
 def test_all_sequences_empty():
     w = W.random_case(9, 5, 4, 1, 64, 16, "bf16", max_len=0)
     c = DecodeCase(w, max_blocks=2).device()
