@@ -537,7 +537,7 @@ def run_ours(args, rank, world, local_rank):
                 "includes": "host allocator writing into pinned staging, one H2D of q/k_new/v_new/slots/pairs/tables/lens, "
                             "kernels, D2H of out",
                 "launch": "eager" if args.e2e_eager else "one CUDA graph per staging buffer (H2D, append, decode, D2H)"},
-        "gpu_launches": K * (2 + (1 if d_pairs is not None else 0)),
+        "gpu_launches": K * (3 + (1 if d_pairs is not None else 0)),  # append, decode, merge (+ CoW copy)
         "clocks": clocks.summary(),
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:

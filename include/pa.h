@@ -116,11 +116,10 @@ pa_status pa_copy_blocks(void* k_pool, void* v_pool, const int32_t* src_dst_pair
 /*
  * Size in bytes of the device workspace pa_decode_attention needs for these
  * shapes on the current CUDA device.  The workspace holds the status word
- * (first int32), one int32 merge counter per (sequence, KV head) and the
- * split-sequence partial results.  The caller allocates it ONCE, zero-filled,
- * and may reuse it across calls on one stream: every completed call leaves
- * the counters at zero again.  Zero it again after a call that reported
- * PA_DEV_WAIT_TIMEOUT.
+ * (first int32, in a 256-byte head) and two split-sequence partial slots per
+ * CTA the device can hold.  The caller allocates it ONCE, with the status word
+ * zeroed, and may reuse it across calls on one stream: the partial slots are
+ * written before they are read, and the status word only gathers error bits.
  */
 pa_status pa_decode_workspace_bytes(int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads,
                                     int32_t head_dim, size_t* bytes_out);
@@ -138,7 +137,10 @@ pa_status pa_decode_workspace_bytes(int32_t num_seqs, int32_t num_q_heads, int32
  * `dtype`, output in `dtype` (bf16 rounds to nearest even).  An empty
  * sequence gives a zero output.
  * Long sequences are split across CTAs (flash-decoding) and the partial
- * results merged on the device.  partition_tokens = 0 splits anywhere on a
+ * results merged on the device by a second kernel, launched right after the
+ * decode kernel as its programmatic dependent: it waits for the decode grid
+ * to finish and writes the output rows of split (sequence, KV head)
+ * segments; the decode kernel writes the others.  partition_tokens = 0 splits anywhere on a
  * block boundary, so that every CTA gets the same share of blocks plus a
  * fixed cost per (sequence, KV head) it touches; partition_tokens = P > 0
  * (a multiple of block_size) allows splits only at multiples of P tokens.
@@ -172,8 +174,7 @@ pa_status pa_decode_attention(void* out, const void* q, const void* k_pool, cons
  * library until the process exits.  Shapes whose scratch
  * (pa_decode_workspace_bytes) exceeds it return PA_ERR_WORKSPACE_TOO_SMALL
  * before anything runs.  The call allocates nothing: it clears the status word
- * and merge counters at the head of the buffer (cudaMemsetAsync) and enqueues
- * the decode.  If dev_status_out is not NULL, the call's device status word
+ * at the head of the buffer (cudaMemsetAsync) and enqueues the decode.  If dev_status_out is not NULL, the call's device status word
  * (PA_DEV_* bits) is copied there on `stream` afterwards.
  * The first call on a device looks up the buffer's device address; make that
  * first call before any stream capture.  Every call on a device shares the

@@ -143,15 +143,14 @@ namespace {
 size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 
 struct WorkspaceLayout {
-    size_t counters_off, partials_off, total;
+    size_t partials_off, total;
 };
 
 WorkspaceLayout workspace_layout(int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
                                  int sms) {
     WorkspaceLayout w;
     const size_t G = (size_t)(num_q_heads / num_kv_heads);
-    w.counters_off = 256;
-    w.partials_off = w.counters_off + align256((size_t)num_seqs * num_kv_heads * kCountersPerSegment * 4);
+    w.partials_off = 256;  // after the status word
     w.total = w.partials_off + (size_t)2 * sms * kMaxCtasPerSm * partial_slot_floats((int)G, head_dim) * 4;
     return w;
 }
@@ -175,6 +174,8 @@ struct LaunchPlan {
     int smem;
     int grid;
     int sms;
+    int merge_smem;
+    int merge_grid;
 };
 
 pa_status plan_launch(int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
@@ -206,6 +207,17 @@ pa_status plan_launch(int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_head
     if (grid > tiles_bound) grid = tiles_bound;
     if (grid < 1) grid = 1;
     lp->grid = (int)grid;
+    // the merge: a group of min(32, G D / 16) lanes per CTA boundary (at most one
+    // split segment each), at most one CTA per SM
+    lp->merge_smem = merge_smem_bytes(num_seqs, fixed);
+    if (lp->merge_smem > kMaxSmem) return PA_ERR_UNSUPPORTED;
+    int mocc = 0;
+    if (!kernel_occupancy(dev, lp->v.merge_kernel, kMergeThreads, lp->merge_smem, &mocc)) return PA_ERR_CUDA;
+    if (mocc <= 0) return PA_ERR_UNSUPPORTED;
+    const int lps = G * head_dim / 16 < 32 ? G * head_dim / 16 : 32;
+    const int64_t groups_per_cta = (kMergeThreads / 32) * (32 / lps);
+    const int64_t merge_ctas = (grid - 1 + groups_per_cta - 1) / groups_per_cta;
+    lp->merge_grid = (int)(merge_ctas < 1 ? 1 : merge_ctas < lp->sms ? merge_ctas : lp->sms);
     return PA_OK;
 }
 
@@ -302,7 +314,6 @@ pa_status decode_common(void* out, const void* q, const void* k_pool, const void
     p.block_tables = block_tables;
     p.seq_lens = seq_lens;
     p.status = reinterpret_cast<int32_t*>(ws);
-    p.counters = reinterpret_cast<int32_t*>(ws + wl.counters_off);
     p.partials = reinterpret_cast<float*>(ws + wl.partials_off);
     p.max_blocks_per_seq = max_blocks_per_seq;
     p.max_len = max_len;
@@ -316,7 +327,7 @@ pa_status decode_common(void* out, const void* q, const void* k_pool, const void
     p.seg_units = lp.mma ? PA_SEG_UNITS_MMA : PA_SEG_UNITS_FMA;
     p.scale_log2 = scale * 1.4426950408889634f * k_scale;
     p.out_scale = v_scale;
-    lp.v.launch(p, tk, tv, lp.grid, lp.smem, static_cast<cudaStream_t>(stream));
+    lp.v.launch(p, tk, tv, lp.grid, lp.smem, lp.merge_grid, lp.merge_smem, static_cast<cudaStream_t>(stream));
     return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }
 

@@ -52,7 +52,6 @@ constexpr int kProducerWarp = 1;
 constexpr int kThreads = 64;
 constexpr int kMaxGroup = 8;
 constexpr int kQSlots = 2;          // query-row slots: the producer may run this many pieces ahead
-constexpr int kMaxMergeChunk = 32;  // partial slots staged at a time when merging a split segment
 
 template <typename T>
 struct ElemBytes;
@@ -111,10 +110,8 @@ struct Layout {
     static constexpr int kQfBytes = MMA ? 0 : GN * D * 4;
     static constexpr int kPTileOff = kQfOff + kQfBytes;
     static constexpr int kPTileBytes = MMA ? 0 : 16 * GN * 4;
-    // the CTA's split segments (at most two): sequence, KV head, first CTA, pieces
-    static constexpr int kPendOff = kPTileOff + kPTileBytes;
-    static constexpr int kBarOff = kPendOff + 2 * 4 * 4;
-    static constexpr int kMiscOff = kBarOff + (2 * S + 2 * kQSlots + 1) * 8;
+    static constexpr int kBarOff = kPTileOff + kPTileBytes;
+    static constexpr int kMiscOff = kBarOff + (2 * S + 2 * kQSlots) * 8;
     static constexpr int kPrefixOff = kMiscOff + 64;
     static_assert(kTileBytes % 1024 == 0, "tiles must keep 1024-byte alignment for the 128B swizzle");
     static_assert(kQSlotBytes % 16 == 0, "bulk-copy destination alignment");
@@ -255,6 +252,96 @@ __device__ __forceinline__ bool role_wait(uint32_t bar, uint32_t parity, volatil
 }
 
 __device__ __forceinline__ int clamp_len(int len, int max_len) { return len < 0 ? 0 : (len > max_len ? max_len : len); }
+
+// Per-sequence blocks (and partitions) of the batch as exclusive prefix sums
+// in shared memory: pref[b] (pref[B] = the total), upref likewise in
+// partitions when p.partition_tiles > 0, and lens_s[b] = the clamped length.
+// Run by all NT threads; wsum holds 2 * NT / 32 ints.  The caller syncs after.
+template <int BS, int NT>
+__device__ __forceinline__ void scan_lengths(const DecodeParams& p, bool flag_bad, int32_t* pref, int32_t* upref,
+                                             int32_t* lens_s, int32_t* wsum) {
+    constexpr int NW = NT / 32;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int B = p.num_seqs;
+    const bool fixed = p.partition_tiles > 0;
+    const int per = (B + NT - 1) / NT;
+    const int lo = min(B, tid * per), hi = min(B, lo + per);
+    int32_t nblk = 0, nprt = 0;
+    for (int b = lo; b < hi; ++b) {
+        const int raw_len = __ldg(p.seq_lens + b);
+        if ((raw_len < 0 || raw_len > p.max_len) && flag_bad) flag_status(p.status, PA_DEV_BAD_SEQ_LEN);
+        const int nb = (clamp_len(raw_len, p.max_len) + BS - 1) / BS;
+        nblk += nb;
+        if (fixed) nprt += (nb + p.partition_tiles - 1) / p.partition_tiles;
+    }
+    int32_t xb = nblk, xp = nprt;  // inclusive warp scans
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        const int32_t yb = __shfl_up_sync(0xffffffffu, xb, off);
+        const int32_t yp = __shfl_up_sync(0xffffffffu, xp, off);
+        if (lane >= off) {
+            xb += yb;
+            xp += yp;
+        }
+    }
+    if (lane == 31) {
+        wsum[warp] = xb;
+        wsum[NW + warp] = xp;
+    }
+    __syncthreads();
+    int32_t ob = 0, op = 0;
+    for (int w = 0; w < warp; ++w) {
+        ob += wsum[w];
+        op += wsum[NW + w];
+    }
+    int32_t rb = ob + xb - nblk, rp = op + xp - nprt;
+    for (int b = lo; b < hi; ++b) {
+        const int len = clamp_len(__ldg(p.seq_lens + b), p.max_len);
+        const int nb = (len + BS - 1) / BS;
+        lens_s[b] = len;
+        pref[b] = rb;
+        rb += nb;
+        if (fixed) {
+            upref[b] = rp;
+            rp += (nb + p.partition_tiles - 1) / p.partition_tiles;
+        }
+    }
+    if (tid == NT - 1) {
+        pref[B] = ob + xb;
+        if (fixed) upref[B] = op + xp;
+    }
+}
+
+// The plan of a decode launch of C CTAs over the scanned batch.  Only the first
+// min(C, T) CTAs (min(C, U) with partitions) take work.  A split segment's
+// pieces then come from consecutive CTAs, which the slot rule and the merge
+// rely on: with partitions every working CTA owns at least one; without, a
+// range is at least K units wide, so no range falls between two tiles of one
+// segment (only in the gap at a segment's start can one be empty).
+__device__ __forceinline__ Plan make_plan(const DecodeParams& p, const int32_t* pref, const int32_t* upref) {
+    Plan P;
+    const int B = p.num_seqs, Hkv = p.num_kv_heads;
+    const bool fixed = p.partition_tiles > 0;
+    P.pref = pref;
+    P.upref = upref;
+    P.B = B;
+    P.Hkv = Hkv;
+    P.PT = p.partition_tiles;
+    P.A = p.seg_units;
+    P.T = (int64_t)Hkv * pref[B];
+    P.U = fixed ? (int64_t)Hkv * upref[B] : (int64_t)P.K * P.T + (int64_t)P.A * Hkv * B;
+    const int64_t units = fixed ? P.U : P.T;
+    int64_t ce = units < (int64_t)p.num_ctas ? units : p.num_ctas;
+    if (fixed && ce > 0) {
+        // Partitions are coarse: give every working CTA the same number of them
+        // (the fewest CTAs with the same largest share), so none is left with
+        // one partition more than the rest at the end of the kernel.
+        const int64_t per = (units + ce - 1) / ce;
+        ce = (units + per - 1) / per;
+    }
+    P.C = (int32_t)ce;
+    return P;
+}
 
 template <typename T>
 __device__ __forceinline__ T from_float(float x);
@@ -642,17 +729,6 @@ __device__ __forceinline__ const float* piece_slot(const float* partials, size_t
     return partials + (size_t)(2 * cc + (cc == ca ? 1 : 0)) * slot_floats;
 }
 
-// Lane 0: bulk-copy the partial slots of pieces ca+c0 .. ca+c0+nc-1 to shared
-// address dst, completing on mbar (whose expected bytes the caller sets).
-// Other CTAs wrote the slots (made visible by the counter protocol) and this
-// warp last read the destination through the generic proxy.
-__device__ __forceinline__ void stage_pieces(const float* partials, size_t slot_floats, int ca, int c0, int nc,
-                                             uint32_t dst, uint32_t mbar) {
-    const uint32_t slot_bytes = (uint32_t)(slot_floats * 4);
-    for (int i = 0; i < nc; ++i)
-        bulk_load(dst + i * slot_bytes, piece_slot(partials, slot_floats, ca + c0 + i, ca), slot_bytes, mbar);
-}
-
 // 16 output elements (fp32 sums times sc) to 16-byte-aligned global memory.
 template <typename T>
 __device__ __forceinline__ void store16(T* dst, const float (&a)[16], float sc) {
@@ -669,92 +745,58 @@ __device__ __forceinline__ void store16(T* dst, const float (&a)[16], float sc) 
     }
 }
 
-// Merge of a split segment, done by the consumer warp of the CTA that
-// completed its last piece, after that warp's own pieces are done:
+// Merge of one split segment by a group of lps lanes (sl = this lane's index
+// in the group), from the pieces' partial slots in global memory (L2: the
+// decode grid that wrote them has finished):
 //   M = max_p m_p,   out = sum_p e^(m_p-M) o_p / sum_p e^(m_p-M) l_p.
-// The np pieces' partial slots are bulk-copied into the idle stage ring a
-// chunk at a time (one round trip per chunk).  Each lane owns 16 consecutive
-// output elements of one head per pass of 512 elements: it folds that head's
-// max and sum itself and sums its elements over the staged slots with 16-byte
-// shared loads.  So the merge needs no scratch and no warp synchronisation,
-// and stays short: it runs once per CTA, from a cold instruction cache.  When
-// the pieces take more than one chunk, each lane keeps its running sums at
-// the end of the ring, after the staged slots.
-// staged_at >= 0: the caller already staged all the slots, in one chunk, at
-// that byte offset of the ring.
+// Each lane owns 16 consecutive output elements of one head per pass of
+// 16 * lps elements and folds that head's max and sum itself, four pieces at a
+// time with their loads in flight together.
 template <typename T, int D>
-__device__ __forceinline__ bool merge_staged(const float* partials, size_t slot_floats, T* orow, int ca, int np, int G,
-                                             int lane, uint32_t ring_s, int ring_bytes,
-                                             int staged_at, uint32_t mbar, uint32_t& mphase, float oscale) {
-    constexpr int kPass = (kMaxGroup * D + 511) / 512;
-    const uint32_t slot_bytes = (uint32_t)(slot_floats * 4);
+__device__ __forceinline__ void merge_pieces(const float* partials, size_t slot_floats, T* orow, int ca, int np, int G,
+                                             int sl, int lps, float oscale) {
     const int nel = G * D;
-    const int acc_bytes = (nel * 4 + 15) & ~15;
-    int per_chunk = min(ring_bytes / (int)slot_bytes, kMaxMergeChunk);
-    const bool multi = np > per_chunk;
-    if (multi) per_chunk = min((ring_bytes - acc_bytes) / (int)slot_bytes, kMaxMergeChunk);
-    if (per_chunk < 1 || (staged_at >= 0 && multi)) return false;  // cannot happen for the instantiated shapes
-    const uint32_t acc_s = ring_s + (uint32_t)(ring_bytes - acc_bytes);
-    const uint32_t buf = ring_s + (uint32_t)(staged_at >= 0 ? staged_at : 0);
-    float mrun[kPass], lrun[kPass];
+    for (int e0 = sl * 16; e0 < nel; e0 += 16 * lps) {
+        const int ml = nel + 2 * (e0 / D);  // (m, l) of this lane's head within a slot
+        float mrun = -INFINITY, lrun = 0.f, a[16];
 #pragma unroll
-    for (int ps = 0; ps < kPass; ++ps) mrun[ps] = -INFINITY, lrun[ps] = 0.f;
-    for (int c0 = 0; c0 < np; c0 += per_chunk) {
-        const int nc = min(per_chunk, np - c0);
-        if (staged_at < 0) {
-            __syncwarp();
-            if (lane == 0) {
-                fence_proxy_async_global();
-                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-                mbar_arrive_expect_tx(mbar, nc * slot_bytes);
-                stage_pieces(partials, slot_floats, ca, c0, nc, buf, mbar);
-            }
-            // a bounded wait that also runs after an abort, so no copy is left in flight
-            bool ok = mbar_wait(mbar, mphase & 1);
-            ok = __all_sync(0xffffffffu, ok);
-            ++mphase;
-            if (!ok) return false;
-        }
+        for (int k = 0; k < 16; ++k) a[k] = 0.f;
+        for (int i0 = 0; i0 < np; i0 += 4) {
+            float2 m_l[4];
+            float4 x[4][4];
 #pragma unroll
-        for (int ps = 0; ps < kPass; ++ps) {
-            const int e0 = ps * 512 + lane * 16;
-            if (e0 < nel) {
-                const uint32_t ml = buf + (uint32_t)(nel + 2 * (e0 / D)) * 4;  // (m, l) of this head, slot 0
-                float mc = mrun[ps];
-                for (int i = 0; i < nc; ++i) mc = fmaxf(mc, lds_f32(ml + i * slot_bytes));
-                const float resc = exp2f(mrun[ps] - mc);  // 0 on the first chunk
-                float lr = lrun[ps] * resc;
-                float a[16];
+            for (int i = 0; i < 4; ++i) {
+                if (i0 + i < np) {
+                    const float* sl = piece_slot(partials, slot_floats, ca + i0 + i, ca);
+                    m_l[i] = __ldcg(reinterpret_cast<const float2*>(sl + ml));
 #pragma unroll
-                for (int v = 0; v < 4; ++v) {
-                    const float4 x = c0 > 0 ? lds_f32x4(acc_s + (uint32_t)(e0 + 4 * v) * 4) : make_float4(0.f, 0.f, 0.f, 0.f);
-                    a[4 * v] = x.x * resc, a[4 * v + 1] = x.y * resc, a[4 * v + 2] = x.z * resc, a[4 * v + 3] = x.w * resc;
+                    for (int v = 0; v < 4; ++v) x[i][v] = __ldcg(reinterpret_cast<const float4*>(sl + e0) + v);
                 }
-                for (int i = 0; i < nc; ++i) {
-                    const float2 m_l = lds_f32x2(ml + i * slot_bytes);
-                    const float w = exp2f(m_l.x - mc);
-                    lr = fmaf(w, m_l.y, lr);
-                    const uint32_t src = buf + i * slot_bytes + (uint32_t)e0 * 4;
+            }
+            float mc = mrun;
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+                if (i0 + i < np) mc = fmaxf(mc, m_l[i].x);
+            const float resc = exp2f(mrun - mc);  // 0 for the first four pieces
+            lrun *= resc;
+#pragma unroll
+            for (int k = 0; k < 16; ++k) a[k] *= resc;
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                if (i0 + i < np) {
+                    const float w = exp2f(m_l[i].x - mc);
+                    lrun = fmaf(w, m_l[i].y, lrun);
 #pragma unroll
                     for (int v = 0; v < 4; ++v) {
-                        const float4 x = lds_f32x4(src + 16 * v);
-                        a[4 * v] = fmaf(w, x.x, a[4 * v]), a[4 * v + 1] = fmaf(w, x.y, a[4 * v + 1]);
-                        a[4 * v + 2] = fmaf(w, x.z, a[4 * v + 2]), a[4 * v + 3] = fmaf(w, x.w, a[4 * v + 3]);
+                        a[4 * v] = fmaf(w, x[i][v].x, a[4 * v]), a[4 * v + 1] = fmaf(w, x[i][v].y, a[4 * v + 1]);
+                        a[4 * v + 2] = fmaf(w, x[i][v].z, a[4 * v + 2]), a[4 * v + 3] = fmaf(w, x[i][v].w, a[4 * v + 3]);
                     }
                 }
-                mrun[ps] = mc, lrun[ps] = lr;
-                if (c0 + nc >= np) {
-                    store16(orow + e0, a, __fdividef(oscale, lr));  // lr >= 1: the largest piece max weighs 1
-                } else {
-#pragma unroll
-                    for (int v = 0; v < 4; ++v)
-                        sts_f32x4(acc_s + (uint32_t)(e0 + 4 * v) * 4, a[4 * v], a[4 * v + 1], a[4 * v + 2], a[4 * v + 3]);
-                }
             }
+            mrun = mc;
         }
+        store16(orow + e0, a, __fdividef(oscale, lrun));  // lrun >= 1: the largest piece max weighs 1
     }
-    __syncwarp();
-    return true;
 }
 
 // Widen one stage of an FP8 pool (K then V, BS rows of D codes each, one
@@ -817,7 +859,6 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const DecodeParams p, 
     auto empty_bar = [&](int s) { return bar0 + 8u * (S + s); };
     auto qfull_bar = [&](int i) { return bar0 + 8u * (2 * S + i); };
     auto qempty_bar = [&](int i) { return bar0 + 8u * (2 * S + kQSlots + i); };
-    const uint32_t merge_bar = bar0 + 8u * (2 * S + 2 * kQSlots);
 
     if (tid == 0) {
         for (int s = 0; s < S; ++s) {
@@ -828,86 +869,17 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const DecodeParams p, 
             mbar_init(qfull_bar(i), 1);
             mbar_init(qempty_bar(i), 1);
         }
-        mbar_init(merge_bar, 1);
         fence_barrier_init();
         misc[0] = 0;  // abort flag
     }
 
-    // ---- plan: blocks (and partitions) per sequence, exclusive prefix sums ----
-    {
-        const int per = (B + kThreads - 1) / kThreads;
-        const int lo = min(B, tid * per), hi = min(B, lo + per);
-        int32_t nblk = 0, nprt = 0;
-        for (int b = lo; b < hi; ++b) {
-            const int raw_len = __ldg(p.seq_lens + b);
-            if ((raw_len < 0 || raw_len > p.max_len) && c == 0) flag_status(p.status, PA_DEV_BAD_SEQ_LEN);
-            const int nb = (clamp_len(raw_len, p.max_len) + BS - 1) / BS;
-            nblk += nb;
-            if (fixed) nprt += (nb + p.partition_tiles - 1) / p.partition_tiles;
-        }
-        int32_t xb = nblk, xp = nprt;  // inclusive warp scans
-#pragma unroll
-        for (int off = 1; off < 32; off <<= 1) {
-            const int32_t yb = __shfl_up_sync(0xffffffffu, xb, off);
-            const int32_t yp = __shfl_up_sync(0xffffffffu, xp, off);
-            if (lane >= off) {
-                xb += yb;
-                xp += yp;
-            }
-        }
-        if (lane == 31) {
-            wsum[warp] = xb;
-            wsum[2 + warp] = xp;
-        }
-        __syncthreads();
-        int32_t ob = 0, op = 0;
-        for (int w = 0; w < warp; ++w) {
-            ob += wsum[w];
-            op += wsum[2 + w];
-        }
-        int32_t rb = ob + xb - nblk, rp = op + xp - nprt;
-        for (int b = lo; b < hi; ++b) {
-            const int len = clamp_len(__ldg(p.seq_lens + b), p.max_len);
-            const int nb = (len + BS - 1) / BS;
-            lens_s[b] = len;
-            pref[b] = rb;
-            rb += nb;
-            if (fixed) {
-                upref[b] = rp;
-                rp += (nb + p.partition_tiles - 1) / p.partition_tiles;
-            }
-        }
-        if (tid == kThreads - 1) {
-            pref[B] = ob + xb;
-            if (fixed) upref[B] = op + xp;
-        }
-    }
+    scan_lengths<BS, kThreads>(p, c == 0, pref, upref, lens_s, wsum);
     __syncthreads();
 
-    Plan P;
-    P.pref = pref;
-    P.upref = upref;
-    P.B = B;
-    P.Hkv = Hkv;
-    P.PT = p.partition_tiles;
-    P.A = p.seg_units;
-    P.T = (int64_t)Hkv * pref[B];
-    P.U = fixed ? (int64_t)Hkv * upref[B] : (int64_t)P.K * P.T + (int64_t)P.A * Hkv * B;
-    // Only the first min(C, T) CTAs (min(C, U) with partitions) take work.  A split
-    // segment's pieces then come from consecutive CTAs, which the merge count and
-    // slot rule rely on: with partitions every working CTA owns at least one;
-    // without, a range is at least K units wide, so no range falls between two
-    // tiles of one segment (only in the gap at a segment's start can one be empty).
-    const int64_t units = fixed ? P.U : P.T;
-    int64_t ce = units < (int64_t)C ? units : C;
-    if (fixed && ce > 0) {
-        // Partitions are coarse: give every working CTA the same number of them
-        // (the fewest CTAs with the same largest share), so none is left with
-        // one partition more than the rest at the end of the kernel.
-        const int64_t per = (units + ce - 1) / ce;
-        ce = (units + per - 1) / per;
-    }
-    P.C = (int32_t)ce;
+    const Plan P = make_plan(p, pref, upref);
+    // the merge kernel that follows may start its own plan now; it waits for
+    // this grid to finish before it reads a partial
+    if (tid == 0) pdl_launch_dependents();
     const bool works = P.T > 0 && c < P.C;
     // the two ends of the range are two independent searches: lanes 0 and 1 of
     // each warp run one each
@@ -1022,10 +994,6 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const DecodeParams p, 
         it.init(P, t0, t1);
         int b, h, j0, j1;
         bool at_t0;
-        // split pieces of this CTA, counted after the loop (at most two: its range's
-        // ends); pend[4 i ..] = sequence, KV head, first CTA of the segment, pieces
-        int npend = 0;
-        int32_t* pend = reinterpret_cast<int32_t*>(base + L::kPendOff);
         while (it.next(P, b, h, j0, j1, at_t0)) {
             const int qs = pi % kQSlots;
             const uint8_t* qslot = base + L::kQOff + qs * L::kQSlotBytes;
@@ -1079,86 +1047,78 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const DecodeParams p, 
             if (j0 == 0 && j1 == nb) {
                 st.store_out(orow, G, lane, p.out_scale);
             } else {
-                // Split segment: store the partial now; its completion is counted
-                // after the loop, so the fence and the atomic round trip stall
-                // this warp once, not once per split piece.  A CTA holds at most
-                // two split pieces (the first and the last of its range).
+                // Split segment: store the unnormalised partial; merge_kernel, the
+                // programmatic dependent of this launch, combines the pieces.  A
+                // piece that continues a segment starts this CTA's range (slot 0);
+                // a split segment's first piece ends it (slot 1).
                 float* slot = p.partials + (size_t)(2 * c + (j0 > 0 ? 0 : 1)) * slot_floats;
                 st.store_partial(slot, G, lane);
-                if (lane == 0) {
-                    const int64_t s0 = P.seg_start(b, h);
-                    const int ca = P.cta_of_seg(s0, b, h);
-                    int32_t* r = pend + 4 * npend;
-                    r[0] = b, r[1] = h, r[2] = ca, r[3] = P.cta_of_seg(s0 + nb - 1, b, h) - ca + 1;
-                }
-                ++npend;
             }
             ++pi;
         }
-        // Count this CTA's split pieces; the CTA that completes the last piece of
-        // segment (b, h) (an atomic counter per segment) merges its partials.
-        // Both counters are bumped before either result is read, so the two
-        // atomics take one round trip.
-        __syncwarp();
-        int lastmask = 0;
-        if (npend > 0) {
-            __threadfence();
-            __syncwarp();
-            if (lane == 0) {
-                const int old0 = atomicAdd(p.counters + (size_t)pend[0] * Hkv + pend[1], 1);
-                const int old1 = npend > 1 ? atomicAdd(p.counters + (size_t)pend[4] * Hkv + pend[5], 1) : -1;
-                if (old0 == pend[3] - 1) lastmask |= 1;
-                if (npend > 1 && old1 == pend[7] - 1) lastmask |= 2;
-                if (lastmask) __threadfence();
-            }
-            lastmask = __shfl_sync(0xffffffffu, lastmask, 0);
-        }
-        // The stage ring is idle now (every issued tile has been consumed): use it
-        // to stage the partials of the split segments this CTA completed.  When it
-        // completed both, and both sets of slots fit in the ring together, they are
-        // staged with one round trip.
-        uint32_t mphase = 0;
-        const int ring_bytes = S * L::kStageBytes;
-        const uint32_t slot_bytes = (uint32_t)(slot_floats * 4);
-        int staged0 = -1, staged1 = -1;  // ring offsets of pre-staged slots
-        if (lastmask == 3 && (pend[3] + pend[7]) * (int)slot_bytes <= ring_bytes && pend[3] <= kMaxMergeChunk &&
-            pend[7] <= kMaxMergeChunk) {
-            if (lane == 0) {
-                fence_proxy_async_global();
-                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-                mbar_arrive_expect_tx(merge_bar, (pend[3] + pend[7]) * slot_bytes);
-                stage_pieces(p.partials, slot_floats, pend[2], 0, pend[3], base_s, merge_bar);
-                stage_pieces(p.partials, slot_floats, pend[6], 0, pend[7],
-                             base_s + pend[3] * slot_bytes, merge_bar);
-            }
-            // bounded, and run by every lane, so no copy is left in flight
-            bool ok = mbar_wait(merge_bar, mphase & 1);
-            ok = __all_sync(0xffffffffu, ok);
-            ++mphase;
-            if (!ok) {
-                misc[0] = 1;
-                if (lane == 0) flag_status(p.status, PA_DEV_WAIT_TIMEOUT);
-                lastmask = 0;
-            } else {
-                staged0 = 0;
-                staged1 = pend[3] * (int)slot_bytes;
-            }
-        }
-#pragma unroll 1
-        for (int i = 0; i < npend; ++i) {
-            if (!(lastmask & (1 << i))) continue;
-            const int32_t* r = pend + 4 * i;
-            T* orow = static_cast<T*>(p.out) + ((size_t)r[0] * Hq + (size_t)r[1] * G) * D;
-            if (!merge_staged<T, D>(p.partials, slot_floats, orow, r[2], r[3], G, lane, base_s,
-                                    ring_bytes, i ? staged1 : staged0, merge_bar, mphase, p.out_scale)) {
-                misc[0] = 1;
-                if (lane == 0) flag_status(p.status, PA_DEV_WAIT_TIMEOUT);
-                break;
-            }
-            if (lane == 0) p.counters[(size_t)r[0] * Hkv + r[1]] = 0;
-        }
     }
     __syncthreads();
+}
+
+// ---------------------------------------------------------------------------
+// The merge of split segments (flash-decoding's reduce)
+// ---------------------------------------------------------------------------
+// Launched right after decode_kernel as its programmatic dependent: it builds
+// the same plan from seq_lens while the decode streams, then waits for the
+// decode grid to finish (its partials visible) and merges every split
+// segment.  The decode CTAs never wait for each other and never count pieces:
+// the reduce costs them nothing at their tails.
+// A split segment is one with a CTA range boundary strictly inside it; the
+// first such boundary c (the segment starts in CTA c - 1) names it once.  So
+// the work items are the boundaries c = 1 .. C-1, each taken by a group of
+// lps = min(32, G D / 16) lanes (several groups per warp for small G D).
+template <typename T, int D, int BS>
+__global__ void __launch_bounds__(kMergeThreads) merge_kernel(const DecodeParams p) {
+    extern __shared__ int32_t msm[];
+    const int B = p.num_seqs, Hkv = p.num_kv_heads;
+    const bool fixed = p.partition_tiles > 0;
+    int32_t* pref = msm;
+    int32_t* upref = pref + (B + 1);
+    int32_t* lens_s = upref + (fixed ? B + 1 : 0);
+    int32_t* wsum = lens_s + B;
+    scan_lengths<BS, kMergeThreads>(p, false, pref, upref, lens_s, wsum);
+    __syncthreads();
+    const Plan P = make_plan(p, pref, upref);
+    const int lane = threadIdx.x & 31;
+    const int G = p.group;
+    const int lps = min(32, G * D / 16), spw = 32 / lps;  // lanes per group, groups per warp
+    const int grp = lane / lps, sl = lane % lps;
+    if (grp >= spw) return;  // lanes left over when lps does not divide 32
+    const size_t slot_floats = partial_slot_floats(G, D);
+    const int ngroups = gridDim.x * (kMergeThreads / 32) * spw;
+    // The segment boundary c names, if any: its sequence, KV head, first CTA and pieces.
+    auto named = [&](int c, int& b, int& h, int& ca, int& np) -> bool {
+        const int64_t t = P.cta_start(c);
+        if (t >= P.T) return false;
+        b = P.find_seq(P.pref, t);
+        const int nb = P.nblocks(b);
+        const int64_t local = t - (int64_t)Hkv * P.pref[b];
+        h = (int)(local / nb);
+        const int j = (int)(local - (int64_t)h * nb);
+        if (j == 0) return false;  // the boundary falls between segments
+        const int64_t s0 = t - j;
+        ca = P.cta_of_seg(s0, b, h);
+        if (ca != c - 1) return false;  // an earlier boundary of this segment names it
+        np = P.cta_of_seg(s0 + nb - 1, b, h) - ca + 1;
+        return true;
+    };
+    int c = 1 + (blockIdx.x * (kMergeThreads / 32) + (threadIdx.x >> 5)) * spw + grp;
+    int b = 0, h = 0, ca = 0, np = 0;
+    bool have = c < P.C && named(c, b, h, ca, np);  // the first item is found while the decode runs
+    pdl_wait_prerequisites();  // the decode grid has finished; its partials are in memory
+    while (c < P.C) {
+        if (have) {
+            T* orow = static_cast<T*>(p.out) + ((size_t)b * p.num_q_heads + (size_t)h * G) * D;
+            merge_pieces<T, D>(p.partials, slot_floats, orow, ca, np, G, sl, lps, p.out_scale);
+        }
+        c += ngroups;
+        have = c < P.C && named(c, b, h, ca, np);
+    }
 }
 
 // Host-side handle of one instantiation.
@@ -1167,22 +1127,31 @@ struct VariantOf {
     static int smem_bytes(int num_seqs, bool fixed) { return Layout<T, D, BS, MMA, GF, KV>::bytes(num_seqs, fixed); }
     // Launched as a programmatic dependent of the preceding kernel on the stream:
     // the grid may start while that kernel finishes if it allowed it.
+    // Both kernels are launched as programmatic dependents of what precedes them
+    // on the stream: the decode of the preceding kernel (which may allow an early
+    // start), the merge of the decode.
     static void launch(const DecodeParams& p, const CUtensorMap& tk, const CUtensorMap& tv, int grid, int smem,
-                       cudaStream_t stream) {
+                       int merge_grid, int merge_smem, cudaStream_t stream) {
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
         cudaLaunchConfig_t cfg = {};
         cfg.gridDim = dim3(grid);
         cfg.blockDim = dim3(kThreads);
         cfg.dynamicSmemBytes = smem;
         cfg.stream = stream;
-        cudaLaunchAttribute attr[1];
-        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-        attr[0].val.programmaticStreamSerializationAllowed = 1;
         cfg.attrs = attr;
         cfg.numAttrs = 1;
-        cudaLaunchKernelEx(&cfg, decode_kernel<T, D, BS, MMA, GF, KV>, p, tk, tv);
+        if (cudaLaunchKernelEx(&cfg, decode_kernel<T, D, BS, MMA, GF, KV>, p, tk, tv) != cudaSuccess) return;
+        cudaLaunchConfig_t mcfg = cfg;
+        mcfg.gridDim = dim3(merge_grid);
+        mcfg.blockDim = dim3(kMergeThreads);
+        mcfg.dynamicSmemBytes = merge_smem;
+        cudaLaunchKernelEx(&mcfg, merge_kernel<T, D, BS>, p);
     }
     static DecodeVariant get() {
         return DecodeVariant{reinterpret_cast<const void*>(&decode_kernel<T, D, BS, MMA, GF, KV>),
+                             reinterpret_cast<const void*>(&merge_kernel<T, D, BS>),
                              Layout<T, D, BS, MMA, GF, KV>::S,
                              kThreads, &smem_bytes, &launch};
     }

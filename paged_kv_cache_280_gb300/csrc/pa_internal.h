@@ -13,7 +13,6 @@ constexpr int kMaxCtasPerSm = 8;
 constexpr int kDefaultCtasPerSmMma = 4;  // default CTAs per SM on the tensor-core path  // bound used to size the decode workspace
 // Decode workspace: one merge counter per (sequence, KV head); per partial
 // slot [G][D] floats of o plus [G][2] floats of (m, l).
-constexpr int kCountersPerSegment = 1;
 constexpr int kSlotExtraFloatsPerHead = 2;
 // floats of one partial slot, a multiple of 4 so that slots can be bulk-copied
 inline __host__ __device__ size_t partial_slot_floats(int G, int D) {
@@ -39,7 +38,6 @@ struct DecodeParams {
     const int32_t* block_tables;
     const int32_t* seq_lens;
     int32_t* status;    // workspace word 0
-    int32_t* counters;  // [num_seqs * num_kv_heads], zero between calls
     float* partials;    // [2 * num_ctas][G * (D + 2)]
     int32_t max_blocks_per_seq;
     int32_t max_len;  // min(max_seq_len, max_blocks_per_seq * block_size)
@@ -59,13 +57,20 @@ struct DecodeParams {
 };
 
 // One compiled decode kernel (dtype, head_dim, block_size, compute path).
+// The merge of split segments: a second, small kernel (see pa_decode.cuh).
+constexpr int kMergeThreads = 128;
+// its shared memory for num_seqs sequences: the plan's prefix sums, the
+// clamped lengths and the scan's warp sums
+inline int merge_smem_bytes(int num_seqs, bool fixed) { return ((num_seqs + 1) * (fixed ? 2 : 1) + num_seqs + 8) * 4; }
+
 struct DecodeVariant {
     const void* kernel;
+    const void* merge_kernel;  // launched right after `kernel` as its programmatic dependent
     int stages;
     int threads;
     int (*smem_bytes)(int num_seqs, bool fixed);
     void (*launch)(const DecodeParams& p, const CUtensorMap& tk, const CUtensorMap& tv, int grid, int smem,
-                   cudaStream_t stream);
+                   int merge_grid, int merge_smem, cudaStream_t stream);
 };
 
 // Compiled variants.  `group` is Hq / Hkv; the CUDA-core path has exact

@@ -4,8 +4,8 @@
 // Some callers of this library have no way to obtain scratch memory: a plugin
 // inside a host framework that owns every device allocation, or a serving
 // loop that must not allocate once it is running.  They cannot hand
-// pa_decode_attention the workspace it needs for split-sequence partials and
-// merge counters.  This entry point instead uses one statically sized buffer
+// pa_decode_attention the workspace it needs for split-sequence partials.
+// This entry point instead uses one statically sized buffer
 // per GPU, held in this library's device image for as long as the process
 // runs, and otherwise runs the same decode path.
 #include <mutex>
@@ -39,7 +39,6 @@ pa_status static_workspace(void** out) {
     return PA_OK;
 }
 
-size_t round256(size_t x) { return (x + 255) & ~(size_t)255; }
 
 }  // namespace
 
@@ -59,9 +58,9 @@ extern "C" pa_status pa_decode_attention_static(void* out, const void* q, const 
     void* ws = nullptr;
     s = static_workspace(&ws);
     if (s != PA_OK) return s;
-    // The buffer keeps the previous call's contents.  The status word and the
-    // per-(sequence, KV head) merge counters at its head must start at zero.
-    const size_t head = 256 + round256((size_t)num_seqs * num_kv_heads * pa::kCountersPerSegment * sizeof(int32_t));
+    // The buffer keeps the previous call's contents.  The status word at its head
+    // must start at zero; the partial slots are written before they are read.
+    const size_t head = 256;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     if (cudaMemsetAsync(ws, 0, head, st) != cudaSuccess) return PA_ERR_CUDA;
     s = pa_decode_attention(out, q, k_pool, v_pool, block_tables, max_blocks_per_seq, seq_lens, max_seq_len,

@@ -65,13 +65,12 @@ def test_split_modes_and_grid_sizes(partition_tokens, ctas):
         pa.pa_decode_set_ctas_per_sm(ctas)
         ws = c.run(partition_tokens=partition_tokens)
         first = to_numpy(c.dout).copy()
-        c.run(ws=ws, partition_tokens=partition_tokens)  # workspace reused: counters were reset
-        assert np.array_equal(first, to_numpy(c.dout))  # deterministic merge order
+        c.dout.fill_(float("nan"))
+        c.run(ws=ws, partition_tokens=partition_tokens)  # workspace reused
+        assert np.array_equal(first, to_numpy(c.dout))  # deterministic merge order, every row rewritten
     finally:
         pa.pa_decode_set_ctas_per_sm(0)
     check_close(first, ref, "bf16")
-    counters = ws[256:256 + 4 * 9 * 2].view(dtype=__import__("torch").int32)  # one per (sequence, KV head)
-    assert int(counters.abs().sum().item()) == 0
 
 
 def test_more_ctas_than_tiles():
@@ -86,9 +85,8 @@ def test_empty_ranges_and_long_merges(dtype, hq, hkv, d, bs):
     """Runs of empty sequences between long ones, at 8 CTAs per SM over a few hundred
     tiles.  Without partitions the ranges balance tiles plus a fixed cost per segment, so
     ranges that fall in the gap before a segment are empty; long segments split into
-    pieces of a tile or two and merge over several staged chunks."""
+    pieces of a tile or two, 40 and more per segment, all merged by one warp."""
     import paged_kv_cache_280_gb300 as pa
-    import torch
 
     w = W.random_case(31 + hq, 24, hq, hkv, d, bs, dtype, max_len=700, min_len=1)
     lens = np.zeros(24, np.int32)
@@ -99,6 +97,7 @@ def test_empty_ranges_and_long_merges(dtype, hq, hkv, d, bs):
         pa.pa_decode_set_ctas_per_sm(8)
         ws = c.run()
         first = to_numpy(c.dout).copy()
+        c.dout.fill_(float("nan"))
         c.run(ws=ws)
         assert np.array_equal(first, to_numpy(c.dout))
     finally:
@@ -106,8 +105,6 @@ def test_empty_ranges_and_long_merges(dtype, hq, hkv, d, bs):
     check_close(first, ref, dtype)
     assert status_word(ws) == 0
     assert not first[lens == 0].any()
-    counters = ws[256:256 + 4 * 24 * hkv].view(dtype=torch.int32)
-    assert int(counters.abs().sum().item()) == 0
 
 
 def test_all_sequences_empty():

@@ -6,7 +6,7 @@ running -- use this entry point, which keeps its split-sequence scratch in a
 static per-GPU buffer inside the library.  These tests call it through the
 C ABI twice in a row and compare each result with the regular entry point
 (caller-supplied workspace), element by element, within the parity bound of
-the other decode tests.  The shapes differ between calls, so a counter or
+the other decode tests.  The shapes differ between calls, so a status word or
 partial left over in the shared buffer by the previous call would show.
 This file is collected last on purpose: if it fails, a run that stops at the
 first failure has already run every other test.
@@ -54,8 +54,9 @@ def test_static_workspace_rejects_oversized_scratch():
     import torch
     import paged_kv_cache_280_gb300 as pa
 
-    # 270000 sequences x 8 KV heads need 8.64 MB of merge counters: more than the 8 MiB static buffer
-    B, hq, hkv, d, bs = 270000, 8, 8, 64, 16
+    # 8 query heads per KV head at d 128: two partial slots of 4160 B for each of up to 8 CTAs
+    # on every SM (10.1 MB on 152 SMs), more than the 8 MiB static buffer
+    B, hq, hkv, d, bs = 4, 64, 8, 128, 16
     assert pa.pa_decode_workspace_bytes(B, hq, hkv, d) > pa.STATIC_WORKSPACE_BYTES
     q = torch.zeros(B, hq, d, dtype=torch.bfloat16, device="cuda")
     pool = torch.zeros(1, hkv, bs, d, dtype=torch.bfloat16, device="cuda")
