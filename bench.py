@@ -531,7 +531,7 @@ def run_ours(args, rank, world, local_rank):
         },
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
                      "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured" else "fallback",
-                     "kernel": "pa_decode_attention (decode_kernel)", "traffic": recorded_traffic()},
+                     "kernel": "pa_decode_attention (decode_kernel, then merge_kernel)", "traffic": recorded_traffic()},
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d // max(1, K_e2e),
                 "d2h_bytes_per_step": d2h // max(1, K_e2e), "steps": K_e2e,
                 "includes": "host allocator writing into pinned staging, one H2D of q/k_new/v_new/slots/pairs/tables/lens, "
