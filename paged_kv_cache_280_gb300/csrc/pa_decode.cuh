@@ -49,6 +49,7 @@ namespace pa {
 
 constexpr int kConsumerWarp = 0;
 constexpr int kProducerWarp = 1;
+constexpr int kConverterWarp = 2;  // FP8 pools on the tensor cores only
 constexpr int kThreads = 64;
 constexpr int kMaxGroup = 8;
 constexpr int kQSlots = 2;          // query-row slots: the producer may run this many pieces ahead
@@ -100,18 +101,21 @@ struct Layout {
     static constexpr int kStageBytes = 2 * kTileBytes;
     static constexpr int kQSlotBytes = GN * D * EQ;
     static constexpr int kStagesOff = 0;
-    // tensor-core path over an FP8 pool: one tile of K and one of V widened to f16
+    // tensor-core path over an FP8 pool: a converter warp widens each stage to
+    // f16 (one tile of K and one of V) into one of two buffers, which the
+    // consumer computes on
     static constexpr bool kCvt = MMA && E == 1;
+    static constexpr int kThreadsCta = kCvt ? 96 : kThreads;
     static constexpr int kCvtTileBytes = kCvt ? BS * D * 2 : 0;
     static constexpr int kCvtOff = kStagesOff + S * kStageBytes;
-    static constexpr int kQOff = kCvtOff + 2 * kCvtTileBytes;
+    static constexpr int kQOff = kCvtOff + 4 * kCvtTileBytes;
     // CUDA-core path only: fp32 query rows (pre-scaled) and one step's weights.
     static constexpr int kQfOff = kQOff + kQSlots * kQSlotBytes;
     static constexpr int kQfBytes = MMA ? 0 : GN * D * 4;
     static constexpr int kPTileOff = kQfOff + kQfBytes;
     static constexpr int kPTileBytes = MMA ? 0 : 16 * GN * 4;
     static constexpr int kBarOff = kPTileOff + kPTileBytes;
-    static constexpr int kMiscOff = kBarOff + (2 * S + 2 * kQSlots) * 8;
+    static constexpr int kMiscOff = kBarOff + (2 * S + 2 * kQSlots + (kCvt ? 4 : 0)) * 8;
     static constexpr int kPrefixOff = kMiscOff + 64;
     static_assert(kTileBytes % 1024 == 0, "tiles must keep 1024-byte alignment for the 128B swizzle");
     static_assert(kQSlotBytes % 16 == 0, "bulk-copy destination alignment");
@@ -835,8 +839,8 @@ __device__ __forceinline__ void widen_fp8_stage(uint32_t src, uint32_t dst, int 
 // The kernel
 // ---------------------------------------------------------------------------
 template <typename T, int D, int BS, bool MMA, int GF, typename KV>
-__global__ void __launch_bounds__(kThreads) decode_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tmap_k,
-                                                          const __grid_constant__ CUtensorMap tmap_v) {
+__global__ void __launch_bounds__(Layout<T, D, BS, MMA, GF, KV>::kThreadsCta)
+    decode_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__ CUtensorMap tmap_v) {
     using L = Layout<T, D, BS, MMA, GF, KV>;
     constexpr int S = L::S;
     constexpr int E = L::E;
@@ -853,12 +857,16 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const DecodeParams p, 
     int32_t* upref = pref + (B + 1);
     int32_t* lens_s = upref + (fixed ? B + 1 : 0);  // clamped seq_lens
     volatile int32_t* misc = reinterpret_cast<volatile int32_t*>(base + L::kMiscOff);
-    int32_t* wsum = reinterpret_cast<int32_t*>(base + L::kMiscOff + 16);  // [2] blocks, [2] partitions
+    int32_t* wsum = reinterpret_cast<int32_t*>(base + L::kMiscOff + 16);  // per warp: blocks, then partitions
     const uint32_t bar0 = base_s + L::kBarOff;
     auto full_bar = [&](int s) { return bar0 + 8u * s; };
     auto empty_bar = [&](int s) { return bar0 + 8u * (S + s); };
     auto qfull_bar = [&](int i) { return bar0 + 8u * (2 * S + i); };
     auto qempty_bar = [&](int i) { return bar0 + 8u * (2 * S + kQSlots + i); };
+    // FP8 on the tensor cores: widened buffer i (K, then V) and its full / empty barriers
+    auto cvt_buf = [&](int i) { return base_s + L::kCvtOff + (uint32_t)i * 2u * L::kCvtTileBytes; };
+    auto cvt_full = [&](int i) { return bar0 + 8u * (2 * S + 2 * kQSlots + i); };
+    auto cvt_empty = [&](int i) { return bar0 + 8u * (2 * S + 2 * kQSlots + 2 + i); };
 
     if (tid == 0) {
         for (int s = 0; s < S; ++s) {
@@ -869,11 +877,17 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const DecodeParams p, 
             mbar_init(qfull_bar(i), 1);
             mbar_init(qempty_bar(i), 1);
         }
+        if constexpr (L::kCvt) {
+            for (int i = 0; i < 2; ++i) {
+                mbar_init(cvt_full(i), 1);
+                mbar_init(cvt_empty(i), 1);
+            }
+        }
         fence_barrier_init();
         misc[0] = 0;  // abort flag
     }
 
-    scan_lengths<BS, kThreads>(p, c == 0, pref, upref, lens_s, wsum);
+    scan_lengths<BS, L::kThreadsCta>(p, c == 0, pref, upref, lens_s, wsum);
     __syncthreads();
 
     const Plan P = make_plan(p, pref, upref);
@@ -1012,17 +1026,15 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const DecodeParams p, 
             for (int i = 0; i < ntile; ++i) {
                 const uint32_t kk = k + i;
                 const int sidx = kk % S;
-                bool released = false;
-                if (role_wait(full_bar(sidx), (kk / S) & 1, misc, p.status)) {
+                // FP8 on the tensor cores: the converter warp has widened this stage
+                // into buffer kk % 2 and handed the stage back to the producer
+                const bool ready = L::kCvt ? role_wait(cvt_full(kk & 1), (kk >> 1) & 1, misc, p.status)
+                                           : role_wait(full_bar(sidx), (kk / S) & 1, misc, p.status);
+                if (ready) {
                     uint32_t kb = base_s + L::kStagesOff + sidx * L::kStageBytes;
                     uint32_t vb = kb + L::kTileBytes;
                     if constexpr (L::kCvt) {
-                        // widen the codes, hand the stage back to the producer, compute on the copy
-                        widen_fp8_stage<D, BS>(kb, base_s + L::kCvtOff, lane);
-                        __syncwarp();
-                        if (lane == 0) mbar_arrive(empty_bar(sidx));
-                        released = true;
-                        kb = base_s + L::kCvtOff;
+                        kb = cvt_buf(kk & 1);
                         vb = kb + L::kCvtTileBytes;
                     }
                     const int tok0 = (j0 + i) * BS;
@@ -1038,7 +1050,7 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const DecodeParams p, 
                     }
                 }
                 __syncwarp();
-                if (lane == 0 && !released) mbar_arrive(empty_bar(sidx));
+                if (lane == 0) mbar_arrive(L::kCvt ? cvt_empty(kk & 1) : empty_bar(sidx));
             }
             k += ntile;
             if constexpr (MMA) st.finish();
@@ -1055,6 +1067,25 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(const DecodeParams p, 
                 st.store_partial(slot, G, lane);
             }
             ++pi;
+        }
+    } else if constexpr (L::kCvt) {
+        if (warp == kConverterWarp) {
+            // ========================= converter =========================
+            // Every tile of the range in issue order: wait for the stage to land
+            // and for widened buffer kk % 2 to be free, widen, then hand the stage
+            // back to the producer and the buffer to the consumer.
+            const uint32_t n = (uint32_t)(t1 - t0);
+            for (uint32_t kk = 0; kk < n; ++kk) {
+                const int sidx = kk % S, cb = kk & 1;
+                if (role_wait(full_bar(sidx), (kk / S) & 1, misc, p.status) &&
+                    role_wait(cvt_empty(cb), ((kk >> 1) & 1) ^ 1, misc, p.status))
+                    widen_fp8_stage<D, BS>(base_s + L::kStagesOff + sidx * L::kStageBytes, cvt_buf(cb), lane);
+                __syncwarp();
+                if (lane == 0) {
+                    mbar_arrive(empty_bar(sidx));
+                    mbar_arrive(cvt_full(cb));
+                }
+            }
         }
     }
     __syncthreads();
@@ -1137,7 +1168,7 @@ struct VariantOf {
         attr[0].val.programmaticStreamSerializationAllowed = 1;
         cudaLaunchConfig_t cfg = {};
         cfg.gridDim = dim3(grid);
-        cfg.blockDim = dim3(kThreads);
+        cfg.blockDim = dim3(Layout<T, D, BS, MMA, GF, KV>::kThreadsCta);
         cfg.dynamicSmemBytes = smem;
         cfg.stream = stream;
         cfg.attrs = attr;
@@ -1153,7 +1184,7 @@ struct VariantOf {
         return DecodeVariant{reinterpret_cast<const void*>(&decode_kernel<T, D, BS, MMA, GF, KV>),
                              reinterpret_cast<const void*>(&merge_kernel<T, D, BS>),
                              Layout<T, D, BS, MMA, GF, KV>::S,
-                             kThreads, &smem_bytes, &launch};
+                             Layout<T, D, BS, MMA, GF, KV>::kThreadsCta, &smem_bytes, &launch};
     }
 };
 
