@@ -481,16 +481,18 @@ def run_ours(args, rank, world, local_rank):
                 device_step(hb, cap_len, torch.cuda.current_stream())
             graphs.append(g)
         torch.cuda.synchronize()
+    # numpy views of each staging buffer's allocator regions, made once
+    host_views = [(region(hb, "slots", torch.int64, (B,)).numpy(), region(hb, "pairs", torch.int32, (B, 2)).numpy(),
+                   region(hb, "tables", torch.int32, (B, max_blocks)).numpy(), region(hb, "lens", torch.int32, (B,)).numpy())
+                  for hb in host_stage]
+
     def host_prepare(s):
         # the allocator's step: new slots (and CoW pairs), block tables and lengths,
         # written in place into staging buffer s
-        hb = host_stage[s]
-        h_lens = region(hb, "lens", torch.int32, (B,)).numpy()
-        _, pr = lib.append_batch(ids_arr, slots_out=region(hb, "slots", torch.int64, (B,)).numpy(),
-                                 pairs_out=region(hb, "pairs", torch.int32, (B, 2)).numpy())
-        lib.export_tables(ids_arr, max_blocks, tables_out=region(hb, "tables", torch.int32, (B, max_blocks)).numpy(),
-                          lens_out=h_lens)
-        return pr, int(np.sum(h_lens, dtype=np.int64))
+        h_slots, h_pairs, h_tables, h_lens = host_views[s]
+        _, pr = lib.append_batch(ids_arr, slots_out=h_slots, pairs_out=h_pairs)
+        lib.export_tables(ids_arr, max_blocks, tables_out=h_tables, lens_out=h_lens)
+        return pr, int(h_lens.sum(dtype=np.int64))
 
     def gpu_step(s, pr):
         if graphs and not len(pr):

@@ -80,7 +80,7 @@ struct ElemBytes<__nv_fp8_e4m3> {  // FP8 pools (OCP E4M3 codes)
 #ifndef PA_STAGE_BYTES_FMA
 #define PA_STAGE_BYTES_FMA 16384
 #endif
-#ifndef PA_STAGE_BYTES_FP8  // tensor-core path over FP8 pools: a shallower ring, more CTAs per SM
+#ifndef PA_STAGE_BYTES_FP8  // tensor-core path over FP8 pools: 4 stages of codes at bs 16; 5 CTAs per SM
 #define PA_STAGE_BYTES_FP8 16384
 #endif
 constexpr int stages_for(int ring_bytes, int bs, int d, int e) {
@@ -101,14 +101,14 @@ struct Layout {
     static constexpr int kStageBytes = 2 * kTileBytes;
     static constexpr int kQSlotBytes = GN * D * EQ;
     static constexpr int kStagesOff = 0;
-    // tensor-core path over an FP8 pool: a converter warp widens each stage to
-    // f16 (one tile of K and one of V) into one of two buffers, which the
-    // consumer computes on
+    // tensor-core path over an FP8 pool: the consumer reads K's codes from the
+    // stage; a converter warp widens the stage's V tile to f16 into one of two
+    // buffers, which the consumer's P V step reads
     static constexpr bool kCvt = MMA && E == 1;
     static constexpr int kThreadsCta = kCvt ? 96 : kThreads;
     static constexpr int kCvtTileBytes = kCvt ? BS * D * 2 : 0;
     static constexpr int kCvtOff = kStagesOff + S * kStageBytes;
-    static constexpr int kQOff = kCvtOff + 4 * kCvtTileBytes;
+    static constexpr int kQOff = kCvtOff + 2 * kCvtTileBytes;
     // CUDA-core path only: fp32 query rows (pre-scaled) and one step's weights.
     static constexpr int kQfOff = kQOff + kQSlots * kQSlotBytes;
     static constexpr int kQfBytes = MMA ? 0 : GN * D * 4;
@@ -431,7 +431,12 @@ __device__ __forceinline__ void load_vec_f32(uint32_t addr, float* v) {
 // 16mt+g, 16mt+g+8 x columns (heads) 2tig, 2tig+1.
 // F16: operands in f16 instead of bf16 (tiles widened from an FP8 pool; the
 // bf16 query rows are rounded to f16 when loaded).
-template <int D, int BS, bool F16 = false>
+// F16: K and V tiles are f16 (widened from an FP8 pool), q is converted to f16.
+// K8 (with F16): K is read as E4M3 codes straight from the stage and widened in
+// registers; V is f16.  The dot product's order over head_dim is free, so a
+// 16-dim k-step takes the dims 16 s + 4 t .. + 3 for thread quad t = lane % 4
+// (the codes one ldmatrix row gives a thread) and q's fragments use the same.
+template <int D, int BS, bool F16 = false, bool K8 = false>
 struct MmaState {
     static constexpr int MT = D / 16;
     uint32_t qb[MT][2];  // B fragments of q^T per 16-dim k-step
@@ -468,8 +473,8 @@ struct MmaState {
             uint32_t lo = 0, hi = 0;
             if (g < G) {
                 const uint32_t* row = reinterpret_cast<const uint32_t*>(qslot + (size_t)g * D * 2);
-                lo = row[(16 * s + 2 * tig) >> 1];
-                hi = row[(16 * s + 2 * tig + 8) >> 1];
+                lo = row[(K8 ? 16 * s + 4 * tig : 16 * s + 2 * tig) >> 1];
+                hi = row[(K8 ? 16 * s + 4 * tig + 2 : 16 * s + 2 * tig + 8) >> 1];
                 if constexpr (F16) {
                     lo = pack_f16x2(bf16_lo(lo), bf16_hi(lo));
                     hi = pack_f16x2(bf16_lo(hi), bf16_hi(hi));
@@ -488,11 +493,27 @@ struct MmaState {
         {
             const int row = row0 + (lane & 7) + (((lane >> 3) & 1) << 3);
             const int csel = lane >> 4;
+            if constexpr (K8) {
+                // one ldmatrix: 16 code rows x 32 dims; each thread's four codes of a
+                // row are the k-slots 2t, 2t+1 (lo pair) and 2t+8, 2t+9 (hi pair)
 #pragma unroll
-            for (int s = 0; s < MT; ++s) {
-                uint32_t a0, a1, a2, a3;
-                ldmatrix_x4(kbase + tile_chunk_offset<BS>(row, 2 * s + csel), a0, a1, a2, a3);
-                mma16816(acc[s & 1], a0, a1, a2, a3, qb[s][0], qb[s][1]);
+                for (int s2 = 0; s2 < MT / 2; ++s2) {
+                    uint32_t r0, r1, r2, r3, a0, a1, a2, a3;
+                    ldmatrix_x4(kbase + tile_chunk_offset<BS>(row, 2 * s2 + csel), r0, r1, r2, r3);
+                    e4m3x4_to_f16x2(r0, a0, a2);
+                    e4m3x4_to_f16x2(r1, a1, a3);
+                    mma16816(acc[0], a0, a1, a2, a3, qb[2 * s2][0], qb[2 * s2][1]);
+                    e4m3x4_to_f16x2(r2, a0, a2);
+                    e4m3x4_to_f16x2(r3, a1, a3);
+                    mma16816(acc[1], a0, a1, a2, a3, qb[2 * s2 + 1][0], qb[2 * s2 + 1][1]);
+                }
+            } else {
+#pragma unroll
+                for (int s = 0; s < MT; ++s) {
+                    uint32_t a0, a1, a2, a3;
+                    ldmatrix_x4(kbase + tile_chunk_offset<BS>(row, 2 * s + csel), a0, a1, a2, a3);
+                    mma16816(acc[s & 1], a0, a1, a2, a3, qb[s][0], qb[s][1]);
+                }
             }
         }
         // (token g, head 2tig), (g, 2tig+1), (g+8, 2tig), (g+8, 2tig+1)
@@ -803,14 +824,14 @@ __device__ __forceinline__ void merge_pieces(const float* partials, size_t slot_
     }
 }
 
-// Widen one stage of an FP8 pool (K then V, BS rows of D codes each, one
+// Widen NT consecutive tiles of an FP8 pool (BS rows of D codes each, one
 // 128-byte panel per row) to f16 tiles (BS rows of D halves, 128-byte panels),
 // both in the 128-byte-swizzled layout.  Every E4M3 value is exact in f16.
-template <int D, int BS>
-__device__ __forceinline__ void widen_fp8_stage(uint32_t src, uint32_t dst, int lane) {
+template <int D, int BS, int NT>
+__device__ __forceinline__ void widen_fp8_tiles(uint32_t src, uint32_t dst, int lane) {
     constexpr int kSrcTile = BS * D, kDstTile = BS * D * 2, CPR = D / 16;  // 16-byte code chunks per row
 #pragma unroll
-    for (int i = lane; i < 2 * BS * CPR; i += 32) {
+    for (int i = lane; i < NT * BS * CPR; i += 32) {
         const int kv = i / (BS * CPR), r = (i / CPR) % BS, c = i % CPR;
         uint32_t w[4];
         asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
@@ -818,13 +839,7 @@ __device__ __forceinline__ void widen_fp8_stage(uint32_t src, uint32_t dst, int 
                      : "r"(src + kv * kSrcTile + tile_chunk_offset<BS>(r, c)));
         uint32_t h[8];
 #pragma unroll
-        for (int j = 0; j < 4; ++j)  // each code pair to an f16 pair, low code to the low half
-            asm("{\n\t.reg .b16 lo, hi;\n\t"
-                "mov.b32 {lo, hi}, %2;\n\t"
-                "cvt.rn.f16x2.e4m3x2 %0, lo;\n\t"
-                "cvt.rn.f16x2.e4m3x2 %1, hi;\n\t}"
-                : "=r"(h[2 * j]), "=r"(h[2 * j + 1])
-                : "r"(w[j]));
+        for (int j = 0; j < 4; ++j) e4m3x4_to_f16x2(w[j], h[2 * j], h[2 * j + 1]);
         const uint32_t d = dst + kv * kDstTile;
         asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(d + tile_chunk_offset<BS>(r, 2 * c)), "r"(h[0]),
                      "r"(h[1]), "r"(h[2]), "r"(h[3])
@@ -863,15 +878,15 @@ __global__ void __launch_bounds__(Layout<T, D, BS, MMA, GF, KV>::kThreadsCta)
     auto empty_bar = [&](int s) { return bar0 + 8u * (S + s); };
     auto qfull_bar = [&](int i) { return bar0 + 8u * (2 * S + i); };
     auto qempty_bar = [&](int i) { return bar0 + 8u * (2 * S + kQSlots + i); };
-    // FP8 on the tensor cores: widened buffer i (K, then V) and its full / empty barriers
-    auto cvt_buf = [&](int i) { return base_s + L::kCvtOff + (uint32_t)i * 2u * L::kCvtTileBytes; };
+    // FP8 on the tensor cores: widened V buffer i and its full / empty barriers
+    auto cvt_buf = [&](int i) { return base_s + L::kCvtOff + (uint32_t)i * L::kCvtTileBytes; };
     auto cvt_full = [&](int i) { return bar0 + 8u * (2 * S + 2 * kQSlots + i); };
     auto cvt_empty = [&](int i) { return bar0 + 8u * (2 * S + 2 * kQSlots + 2 + i); };
 
     if (tid == 0) {
         for (int s = 0; s < S; ++s) {
             mbar_init(full_bar(s), 1);
-            mbar_init(empty_bar(s), 1);
+            mbar_init(empty_bar(s), L::kCvt ? 2 : 1);  // FP8 on the tensor cores: consumer and converter
         }
         for (int i = 0; i < kQSlots; ++i) {
             mbar_init(qfull_bar(i), 1);
@@ -1002,7 +1017,7 @@ __global__ void __launch_bounds__(Layout<T, D, BS, MMA, GF, KV>::kThreadsCta)
         }
         float* qf = reinterpret_cast<float*>(base + L::kQfOff);
         float* ptile = reinterpret_cast<float*>(base + L::kPTileOff);
-        typename std::conditional<MMA, MmaState<D, BS, L::kCvt>, FmaState<KV, D, BS, GF>>::type st;
+        typename std::conditional<MMA, MmaState<D, BS, L::kCvt, L::kCvt>, FmaState<KV, D, BS, GF>>::type st;
         uint32_t k = 0, pi = 0;
         PieceIter it;
         it.init(P, t0, t1);
@@ -1026,17 +1041,13 @@ __global__ void __launch_bounds__(Layout<T, D, BS, MMA, GF, KV>::kThreadsCta)
             for (int i = 0; i < ntile; ++i) {
                 const uint32_t kk = k + i;
                 const int sidx = kk % S;
-                // FP8 on the tensor cores: the converter warp has widened this stage
-                // into buffer kk % 2 and handed the stage back to the producer
-                const bool ready = L::kCvt ? role_wait(cvt_full(kk & 1), (kk >> 1) & 1, misc, p.status)
-                                           : role_wait(full_bar(sidx), (kk / S) & 1, misc, p.status);
+                // FP8 on the tensor cores: K is read from the stage, V from the buffer
+                // the converter warp widened it into (kk % 2)
+                const bool ready = role_wait(full_bar(sidx), (kk / S) & 1, misc, p.status) &&
+                                   (!L::kCvt || role_wait(cvt_full(kk & 1), (kk >> 1) & 1, misc, p.status));
                 if (ready) {
-                    uint32_t kb = base_s + L::kStagesOff + sidx * L::kStageBytes;
-                    uint32_t vb = kb + L::kTileBytes;
-                    if constexpr (L::kCvt) {
-                        kb = cvt_buf(kk & 1);
-                        vb = kb + L::kCvtTileBytes;
-                    }
+                    const uint32_t kb = base_s + L::kStagesOff + sidx * L::kStageBytes;
+                    const uint32_t vb = L::kCvt ? cvt_buf(kk & 1) : kb + L::kTileBytes;
                     const int tok0 = (j0 + i) * BS;
 #pragma unroll
                     for (int sub = 0; sub < BS / 16; ++sub) {
@@ -1050,7 +1061,10 @@ __global__ void __launch_bounds__(Layout<T, D, BS, MMA, GF, KV>::kThreadsCta)
                     }
                 }
                 __syncwarp();
-                if (lane == 0) mbar_arrive(L::kCvt ? cvt_empty(kk & 1) : empty_bar(sidx));
+                if (lane == 0) {
+                    mbar_arrive(empty_bar(sidx));
+                    if constexpr (L::kCvt) mbar_arrive(cvt_empty(kk & 1));
+                }
             }
             k += ntile;
             if constexpr (MMA) st.finish();
@@ -1072,14 +1086,16 @@ __global__ void __launch_bounds__(Layout<T, D, BS, MMA, GF, KV>::kThreadsCta)
         if (warp == kConverterWarp) {
             // ========================= converter =========================
             // Every tile of the range in issue order: wait for the stage to land
-            // and for widened buffer kk % 2 to be free, widen, then hand the stage
-            // back to the producer and the buffer to the consumer.
+            // and for V buffer kk % 2 to be free, widen the stage's V tile, then
+            // release the stage (the consumer releases it too, after its K) and
+            // hand the buffer to the consumer.
             const uint32_t n = (uint32_t)(t1 - t0);
             for (uint32_t kk = 0; kk < n; ++kk) {
                 const int sidx = kk % S, cb = kk & 1;
                 if (role_wait(full_bar(sidx), (kk / S) & 1, misc, p.status) &&
                     role_wait(cvt_empty(cb), ((kk >> 1) & 1) ^ 1, misc, p.status))
-                    widen_fp8_stage<D, BS>(base_s + L::kStagesOff + sidx * L::kStageBytes, cvt_buf(cb), lane);
+                    widen_fp8_tiles<D, BS, 1>(base_s + L::kStagesOff + sidx * L::kStageBytes + L::kTileBytes,
+                                              cvt_buf(cb), lane);
                 __syncwarp();
                 if (lane == 0) {
                     mbar_arrive(empty_bar(sidx));
