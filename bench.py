@@ -238,9 +238,11 @@ def decode_bytes(lens, w, kv_elem=None) -> int:
 
 
 def kernel_source_hash() -> str:
+    """Hash of the sources the decode and merge kernels and their launch are built from."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "paged_kv_cache_280_gb300", "csrc")
-    for f in sorted(x for x in os.listdir(csrc) if x.endswith((".cu", ".cuh", ".h", ".cpp"))):
+    keep = ("pa_decode", "pa_device.cuh", "pa_internal.h", "pa_api.cu")
+    for f in sorted(x for x in os.listdir(csrc) if x.startswith(keep) and x.endswith((".cu", ".cuh", ".h"))):
         with open(os.path.join(csrc, f), "rb") as fh:
             h.update(f.encode() + fh.read())
     return h.hexdigest()[:16]
