@@ -321,7 +321,7 @@ def run_ours(args, rank, world, local_rank):
     import paged_kv_cache_280_gb300 as pa
 
     K, Wm = args.steps, args.warmup
-    K_e2e = min(K, args.e2e_steps)
+    K_e2e = args.e2e_steps
     w = build_workload(args.workload, rank, world, extra_steps=1 + K_e2e + 2)
     Hq, Hkv, D, bs, PT = w.num_q_heads, w.num_kv_heads, w.head_dim, w.block_size, w.partition_tokens
     lib = pa.Allocator(w.num_blocks, bs, free_order=w.free_order())
@@ -449,7 +449,10 @@ def run_ours(args, rank, world, local_rank):
         o, n = offs[name]
         return buf[o:o + n].view(dtype).view(shape)
 
-    host_stage = [torch.empty(stage_bytes, dtype=torch.uint8).pin_memory() for _ in range(K_e2e)]
+    # Two pinned staging buffers, used in turn: the allocator fills one while the GPU copies the
+    # other.  Their q and new K/V (made upstream) alternate between two draws.
+    n_stage = min(2, K_e2e)
+    host_stage = [torch.empty(stage_bytes, dtype=torch.uint8).pin_memory() for _ in range(n_stage)]
     for s, hb in enumerate(host_stage):
         for name, src in (("q", w.queries(step=2 + s)), ("kn", w.new_tokens("k", B, step=2 + s)),
                           ("vn", w.new_tokens("v", B, step=2 + s))):
@@ -490,17 +493,17 @@ def run_ours(args, rank, world, local_rank):
 
     def host_prepare(s):
         # the allocator's step: new slots (and CoW pairs), block tables and lengths,
-        # written in place into staging buffer s
-        h_slots, h_pairs, h_tables, h_lens = host_views[s]
+        # written in place into staging buffer s % 2
+        h_slots, h_pairs, h_tables, h_lens = host_views[s % n_stage]
         _, pr = lib.append_batch(ids_arr, slots_out=h_slots, pairs_out=h_pairs)
         lib.export_tables(ids_arr, max_blocks, tables_out=h_tables, lens_out=h_lens)
         return pr, int(h_lens.sum(dtype=np.int64))
 
     def gpu_step(s, pr):
         if graphs and not len(pr):
-            graphs[s].replay()
+            graphs[s % n_stage].replay()
         else:  # copy-on-write pairs go between the H2D copy and the append: launched one by one
-            dev_stage.copy_(host_stage[s], non_blocking=True)
+            dev_stage.copy_(host_stage[s % n_stage], non_blocking=True)
             if len(pr):
                 pa.pa_copy_blocks(dk, dv, e_pairs[: len(pr)], stream=stream)
             append(e_kn, e_vn, e_slots, stream=stream)
@@ -556,7 +559,7 @@ def run_ours(args, rank, world, local_rank):
                 "includes": "host allocator writing into pinned staging one step ahead of the GPU, one H2D of "
                             "q/k_new/v_new/slots/pairs/tables/lens, kernels, D2H of out; no L2 flush inside the loop "
                             "(the KV read per step is larger than L2 and loaded evict-first)",
-                "launch": "eager" if args.e2e_eager else "one CUDA graph per staging buffer (H2D, append, decode, D2H)"},
+                "launch": "eager" if args.e2e_eager else "one CUDA graph per staging buffer (H2D, append, decode, merge, D2H)"},
         "gpu_launches": K * (3 + (1 if d_pairs is not None else 0)),  # append, decode, merge (+ CoW copy)
         "clocks": clocks.summary(),
     }
@@ -1004,7 +1007,7 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="gqa4_b64", choices=sorted(WORKLOADS))
-    ap.add_argument("--e2e-steps", type=int, default=32)
+    ap.add_argument("--e2e-steps", type=int, default=128)
     ap.add_argument("--e2e-eager", action="store_true", help="e2e: launch the step's calls one by one, no CUDA graph")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
