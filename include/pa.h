@@ -222,11 +222,10 @@ pa_status pa_decode_set_ctas_per_sm(int32_t ctas);
  * pa_decode_attention_fp8: pa_decode_attention over FP8 pools with bf16 q
  * and out: out = softmax(scale q . (K code values * k_scale)) (V code values
  * * v_scale).  Same layouts, workspace (pa_decode_workspace_bytes), split
- * modes and error reporting.  4 or more query heads per KV head run on the
- * tensor cores (each stage's codes widened to f16 in shared memory, f16
- * mma.sync; the bf16 queries are rounded to f16, so their magnitudes must stay
- * within f16 range), fewer on the CUDA cores.  k_scale and v_scale must be
- * finite and > 0.
+ * modes and error reporting.  Every group size runs on the tensor cores:
+ * the codes are widened to f16 in registers and the MMAs run in f16 (the
+ * bf16 queries are rounded to f16, so their magnitudes must stay within f16
+ * range).  k_scale and v_scale must be finite and > 0.
  */
 pa_status pa_reshape_and_cache_fp8(const void* k_new, const void* v_new, void* k_pool, void* v_pool,
                                    const int64_t* slot_mapping, int32_t num_tokens, int32_t num_kv_heads,

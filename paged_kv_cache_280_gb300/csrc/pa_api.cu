@@ -183,8 +183,9 @@ pa_status plan_launch(int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_head
     int dev = 0;
     if (!current_device(&dev, &lp->sms)) return PA_ERR_CUDA;
     const int G = num_q_heads / num_kv_heads;
-    // dtype is the pool's: PA_FP8_E4M3 pools pair with bf16 queries and take the CUDA-core path
-    lp->mma = ((dtype == PA_BF16 || dtype == PA_FP8_E4M3) && G >= 4);
+    // dtype is the pool's: PA_FP8_E4M3 pools pair with bf16 queries and always take the
+    // tensor cores (their codes are widened in registers); bf16 does for 4+ query heads
+    lp->mma = (dtype == PA_BF16 && G >= 4) || dtype == PA_FP8_E4M3;
     bool found = dtype == PA_F32         ? decode_variant_f32(head_dim, block_size, G, &lp->v)
                  : dtype == PA_FP8_E4M3 ? decode_variant_fp8(head_dim, block_size, G, &lp->v)
                  : lp->mma              ? decode_variant_bf16_mma(head_dim, block_size, &lp->v)

@@ -29,10 +29,11 @@
 // is no merge between warps and no CTA-wide barrier in the loop.
 //
 // Two compute paths:
-//   MMA (bf16, G >= 4): tensor-core mma.sync m16n8k16.  S^T = K q^T with the
-//     16 tokens of a half-block as M and the (padded) 8 query heads as N;
-//     P^T is moved into B-fragment layout with movmatrix; O^T = V^T P^T with
-//     the head dimension as M.
+//   MMA (bf16 with G >= 4, and every FP8 pool): tensor-core mma.sync m16n8k16.
+//     S^T = K q^T with the 16 tokens of a half-block as M and the (padded) 8
+//     query heads as N; P^T is moved into B-fragment layout with movmatrix;
+//     O^T = V^T P^T with the head dimension as M.  FP8 codes are widened to f16
+//     in registers (see MmaState).
 //   FMA (fp32, or bf16 with G < 4): CUDA cores; lane (t, half) forms the dot
 //     products of token t over half the head dimension, lanes own D/32
 //     output dimensions for P V.
@@ -49,7 +50,6 @@ namespace pa {
 
 constexpr int kConsumerWarp = 0;
 constexpr int kProducerWarp = 1;
-constexpr int kConverterWarp = 2;  // FP8 pools on the tensor cores only
 constexpr int kThreads = 64;
 constexpr int kMaxGroup = 8;
 constexpr int kQSlots = 2;          // query-row slots: the producer may run this many pieces ahead
@@ -80,7 +80,7 @@ struct ElemBytes<__nv_fp8_e4m3> {  // FP8 pools (OCP E4M3 codes)
 #ifndef PA_STAGE_BYTES_FMA
 #define PA_STAGE_BYTES_FMA 16384
 #endif
-#ifndef PA_STAGE_BYTES_FP8  // tensor-core path over FP8 pools: 4 stages of codes at bs 16; 5 CTAs per SM
+#ifndef PA_STAGE_BYTES_FP8  // tensor-core path over FP8 pools: 4 stages of codes at bs 16
 #define PA_STAGE_BYTES_FP8 16384
 #endif
 constexpr int stages_for(int ring_bytes, int bs, int d, int e) {
@@ -101,21 +101,17 @@ struct Layout {
     static constexpr int kStageBytes = 2 * kTileBytes;
     static constexpr int kQSlotBytes = GN * D * EQ;
     static constexpr int kStagesOff = 0;
-    // tensor-core path over an FP8 pool: the consumer reads K's codes from the
-    // stage; a converter warp widens the stage's V tile to f16 into one of two
-    // buffers, which the consumer's P V step reads
-    static constexpr bool kCvt = MMA && E == 1;
-    static constexpr int kThreadsCta = kCvt ? 96 : kThreads;
-    static constexpr int kCvtTileBytes = kCvt ? BS * D * 2 : 0;
-    static constexpr int kCvtOff = kStagesOff + S * kStageBytes;
-    static constexpr int kQOff = kCvtOff + 2 * kCvtTileBytes;
+    // tensor-core path over an FP8 pool: K and V codes are widened in registers
+    static constexpr bool kF8 = MMA && E == 1;
+    static constexpr int kThreadsCta = kThreads;
+    static constexpr int kQOff = kStagesOff + S * kStageBytes;
     // CUDA-core path only: fp32 query rows (pre-scaled) and one step's weights.
     static constexpr int kQfOff = kQOff + kQSlots * kQSlotBytes;
     static constexpr int kQfBytes = MMA ? 0 : GN * D * 4;
     static constexpr int kPTileOff = kQfOff + kQfBytes;
     static constexpr int kPTileBytes = MMA ? 0 : 16 * GN * 4;
     static constexpr int kBarOff = kPTileOff + kPTileBytes;
-    static constexpr int kMiscOff = kBarOff + (2 * S + 2 * kQSlots + (kCvt ? 4 : 0)) * 8;
+    static constexpr int kMiscOff = kBarOff + (2 * S + 2 * kQSlots) * 8;
     static constexpr int kPrefixOff = kMiscOff + 64;
     static_assert(kTileBytes % 1024 == 0, "tiles must keep 1024-byte alignment for the 128B swizzle");
     static_assert(kQSlotBytes % 16 == 0, "bulk-copy destination alignment");
@@ -373,35 +369,10 @@ __device__ __forceinline__ void load_chunk_f32<float>(uint32_t addr, float* v) {
     asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];" : "=f"(v[0]), "=f"(v[1]), "=f"(v[2]), "=f"(v[3]) : "r"(addr));
 }
 
-// Two E4M3 codes (low byte first) widened exactly to fp32, through fp16.
-__device__ __forceinline__ float2 e4m3x2_to_f32(uint32_t two) {
-    const __half2_raw h = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(two & 0xffffu), __NV_E4M3);
-    return __half22float2(*reinterpret_cast<const __half2*>(&h));
-}
-template <>
-__device__ __forceinline__ void load_chunk_f32<__nv_fp8_e4m3>(uint32_t addr, float* v) {
-    uint32_t r[4];
-    asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]) : "r"(addr));
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        const float2 lo = e4m3x2_to_f32(r[i]), hi = e4m3x2_to_f32(r[i] >> 16);
-        v[4 * i] = lo.x;
-        v[4 * i + 1] = lo.y;
-        v[4 * i + 2] = hi.x;
-        v[4 * i + 3] = hi.y;
-    }
-}
-
 // Load N consecutive elements (N * E <= 16 bytes, naturally aligned) and widen.
 template <typename T, int N>
 __device__ __forceinline__ void load_vec_f32(uint32_t addr, float* v) {
-    if constexpr (sizeof(T) == 1) {
-        static_assert(N == 4, "fp8 vector of 4");
-        uint32_t r;
-        asm volatile("ld.shared.u32 %0, [%1];" : "=r"(r) : "r"(addr));
-        const float2 lo = e4m3x2_to_f32(r), hi = e4m3x2_to_f32(r >> 16);
-        v[0] = lo.x; v[1] = lo.y; v[2] = hi.x; v[3] = hi.y;
-    } else if constexpr (sizeof(T) == 2) {
+    if constexpr (sizeof(T) == 2) {
         if constexpr (N == 2) {
             uint32_t r;
             asm volatile("ld.shared.u32 %0, [%1];" : "=r"(r) : "r"(addr));
@@ -431,13 +402,20 @@ __device__ __forceinline__ void load_vec_f32(uint32_t addr, float* v) {
 // 16mt+g, 16mt+g+8 x columns (heads) 2tig, 2tig+1.
 // F16: operands in f16 instead of bf16 (tiles widened from an FP8 pool; the
 // bf16 query rows are rounded to f16 when loaded).
-// F16: K and V tiles are f16 (widened from an FP8 pool), q is converted to f16.
-// K8 (with F16): K is read as E4M3 codes straight from the stage and widened in
-// registers; V is f16.  The dot product's order over head_dim is free, so a
-// 16-dim k-step takes the dims 16 s + 4 t .. + 3 for thread quad t = lane % 4
-// (the codes one ldmatrix row gives a thread) and q's fragments use the same.
-template <int D, int BS, bool F16 = false, bool K8 = false>
+// F8: K and V are E4M3 codes read straight from the stage and widened to f16 in
+// registers (q is converted to f16 once per piece).  An ldmatrix over code
+// pairs gives each thread four codes, and the fragments are built from them:
+// - S = K q^T: a thread's four codes of a K row are four consecutive dims, so
+//   a 16-dim k-step takes the dims 16 s + 4 t .. + 3 for thread quad t = lane % 4
+//   instead of the usual ones (the dot product's order is free) and q's
+//   fragments use the same dims.
+// - O^T = V^T P^T: ldmatrix.trans gives a thread the codes of tokens 2t, 2t+1
+//   at dims 16 c + 2 g and + 1; a byte permute makes the token pair of each dim
+//   one f16 pair, so an m16 block's rows g and g + 8 are the dims 16 c + 2 g and
+//   16 c + 2 g + 1, which the output stores undo.
+template <int D, int BS, bool F8 = false>
 struct MmaState {
+    static constexpr bool F16 = F8;  // the MMA runs in f16 over an FP8 pool, else in bf16
     static constexpr int MT = D / 16;
     uint32_t qb[MT][2];  // B fragments of q^T per 16-dim k-step
     float m[2], l[2];
@@ -473,8 +451,8 @@ struct MmaState {
             uint32_t lo = 0, hi = 0;
             if (g < G) {
                 const uint32_t* row = reinterpret_cast<const uint32_t*>(qslot + (size_t)g * D * 2);
-                lo = row[(K8 ? 16 * s + 4 * tig : 16 * s + 2 * tig) >> 1];
-                hi = row[(K8 ? 16 * s + 4 * tig + 2 : 16 * s + 2 * tig + 8) >> 1];
+                lo = row[(F8 ? 16 * s + 4 * tig : 16 * s + 2 * tig) >> 1];
+                hi = row[(F8 ? 16 * s + 4 * tig + 2 : 16 * s + 2 * tig + 8) >> 1];
                 if constexpr (F16) {
                     lo = pack_f16x2(bf16_lo(lo), bf16_hi(lo));
                     hi = pack_f16x2(bf16_lo(hi), bf16_hi(hi));
@@ -493,7 +471,7 @@ struct MmaState {
         {
             const int row = row0 + (lane & 7) + (((lane >> 3) & 1) << 3);
             const int csel = lane >> 4;
-            if constexpr (K8) {
+            if constexpr (F8) {
                 // one ldmatrix: 16 code rows x 32 dims; each thread's four codes of a
                 // row are the k-slots 2t, 2t+1 (lo pair) and 2t+8, 2t+9 (hi pair)
 #pragma unroll
@@ -550,15 +528,36 @@ struct MmaState {
             m01 = (2 * tig < valid ? 0x0000ffffu : 0u) | (2 * tig + 1 < valid ? 0xffff0000u : 0u);
             m89 = (2 * tig + 8 < valid ? 0x0000ffffu : 0u) | (2 * tig + 9 < valid ? 0xffff0000u : 0u);
         }
-        const int row = row0 + (lane & 7) + ((lane >> 4) << 3);
-        const int csel = (lane >> 3) & 1;
+        if constexpr (F8) {
+            // one ldmatrix.trans: registers (tokens 0-7, chunk c), (8-15, c), (0-7, c+1), (8-15, c+1)
+            const int row = row0 + (lane & 7) + (((lane >> 3) & 1) << 3);
+            const int csel = lane >> 4;
 #pragma unroll
-        for (int i = 0; i < MT; ++i) {
-            uint32_t a0, a1, a2, a3;
-            ldmatrix_x4_trans(vbase + tile_chunk_offset<BS>(row, 2 * i + csel), a0, a1, a2, a3);
-            mma16816(o[i], a0 & m01, a1 & m01, a2 & m89, a3 & m89, b0, b1);
+            for (int i2 = 0; i2 < MT / 2; ++i2) {
+                uint32_t r0, r1, r2, r3, a0, a1, a2, a3;
+                ldmatrix_x4_trans(vbase + tile_chunk_offset<BS>(row, 2 * i2 + csel), r0, r1, r2, r3);
+                e4m3x4_to_f16x2(__byte_perm(r0, 0, 0x3120), a0, a1);  // even dim, odd dim; tokens 2t, 2t+1
+                e4m3x4_to_f16x2(__byte_perm(r1, 0, 0x3120), a2, a3);  // same dims, tokens 2t+8, 2t+9
+                mma16816(o[2 * i2], a0 & m01, a1 & m01, a2 & m89, a3 & m89, b0, b1);
+                e4m3x4_to_f16x2(__byte_perm(r2, 0, 0x3120), a0, a1);
+                e4m3x4_to_f16x2(__byte_perm(r3, 0, 0x3120), a2, a3);
+                mma16816(o[2 * i2 + 1], a0 & m01, a1 & m01, a2 & m89, a3 & m89, b0, b1);
+            }
+        } else {
+            const int row = row0 + (lane & 7) + ((lane >> 4) << 3);
+            const int csel = (lane >> 3) & 1;
+#pragma unroll
+            for (int i = 0; i < MT; ++i) {
+                uint32_t a0, a1, a2, a3;
+                ldmatrix_x4_trans(vbase + tile_chunk_offset<BS>(row, 2 * i + csel), a0, a1, a2, a3);
+                mma16816(o[i], a0 & m01, a1 & m01, a2 & m89, a3 & m89, b0, b1);
+            }
         }
     }
+
+    // Head dims of accumulator rows g and g + 8 of m16 block i.
+    __device__ static __forceinline__ int dim_lo(int i, int g) { return F8 ? 16 * i + 2 * g : 16 * i + g; }
+    __device__ static __forceinline__ int dim_hi(int i, int g) { return F8 ? 16 * i + 2 * g + 1 : 16 * i + g + 8; }
 
     // Sum the running sums over the 8 token rows (lanes with the same tig).
     __device__ __forceinline__ void finish() {
@@ -577,14 +576,14 @@ struct MmaState {
         const float r0 = oscale / l[0], r1 = oscale / l[1];
 #pragma unroll
         for (int i = 0; i < MT; ++i) {
-            const int d0 = 16 * i + g;
+            const int dl = dim_lo(i, g), dh = dim_hi(i, g);
             if (h0 < G) {
-                o_rows[h0 * D + d0] = from_float<T>(o[i][0] * r0);
-                o_rows[h0 * D + d0 + 8] = from_float<T>(o[i][2] * r0);
+                o_rows[h0 * D + dl] = from_float<T>(o[i][0] * r0);
+                o_rows[h0 * D + dh] = from_float<T>(o[i][2] * r0);
             }
             if (h1 < G) {
-                o_rows[h1 * D + d0] = from_float<T>(o[i][1] * r1);
-                o_rows[h1 * D + d0 + 8] = from_float<T>(o[i][3] * r1);
+                o_rows[h1 * D + dl] = from_float<T>(o[i][1] * r1);
+                o_rows[h1 * D + dh] = from_float<T>(o[i][3] * r1);
             }
         }
     }
@@ -594,14 +593,14 @@ struct MmaState {
         const int g = lane >> 2, h0 = 2 * (lane & 3), h1 = h0 + 1;
 #pragma unroll
         for (int i = 0; i < MT; ++i) {
-            const int d0 = 16 * i + g;
+            const int dl = dim_lo(i, g), dh = dim_hi(i, g);
             if (h0 < G) {
-                slot[h0 * D + d0] = o[i][0];
-                slot[h0 * D + d0 + 8] = o[i][2];
+                slot[h0 * D + dl] = o[i][0];
+                slot[h0 * D + dh] = o[i][2];
             }
             if (h1 < G) {
-                slot[h1 * D + d0] = o[i][1];
-                slot[h1 * D + d0 + 8] = o[i][3];
+                slot[h1 * D + dl] = o[i][1];
+                slot[h1 * D + dh] = o[i][3];
             }
         }
         if (g == 0) {
@@ -824,32 +823,6 @@ __device__ __forceinline__ void merge_pieces(const float* partials, size_t slot_
     }
 }
 
-// Widen NT consecutive tiles of an FP8 pool (BS rows of D codes each, one
-// 128-byte panel per row) to f16 tiles (BS rows of D halves, 128-byte panels),
-// both in the 128-byte-swizzled layout.  Every E4M3 value is exact in f16.
-template <int D, int BS, int NT>
-__device__ __forceinline__ void widen_fp8_tiles(uint32_t src, uint32_t dst, int lane) {
-    constexpr int kSrcTile = BS * D, kDstTile = BS * D * 2, CPR = D / 16;  // 16-byte code chunks per row
-#pragma unroll
-    for (int i = lane; i < NT * BS * CPR; i += 32) {
-        const int kv = i / (BS * CPR), r = (i / CPR) % BS, c = i % CPR;
-        uint32_t w[4];
-        asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
-                     : "=r"(w[0]), "=r"(w[1]), "=r"(w[2]), "=r"(w[3])
-                     : "r"(src + kv * kSrcTile + tile_chunk_offset<BS>(r, c)));
-        uint32_t h[8];
-#pragma unroll
-        for (int j = 0; j < 4; ++j) e4m3x4_to_f16x2(w[j], h[2 * j], h[2 * j + 1]);
-        const uint32_t d = dst + kv * kDstTile;
-        asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(d + tile_chunk_offset<BS>(r, 2 * c)), "r"(h[0]),
-                     "r"(h[1]), "r"(h[2]), "r"(h[3])
-                     : "memory");
-        asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(d + tile_chunk_offset<BS>(r, 2 * c + 1)),
-                     "r"(h[4]), "r"(h[5]), "r"(h[6]), "r"(h[7])
-                     : "memory");
-    }
-}
-
 // ---------------------------------------------------------------------------
 // The kernel
 // ---------------------------------------------------------------------------
@@ -878,25 +851,15 @@ __global__ void __launch_bounds__(Layout<T, D, BS, MMA, GF, KV>::kThreadsCta)
     auto empty_bar = [&](int s) { return bar0 + 8u * (S + s); };
     auto qfull_bar = [&](int i) { return bar0 + 8u * (2 * S + i); };
     auto qempty_bar = [&](int i) { return bar0 + 8u * (2 * S + kQSlots + i); };
-    // FP8 on the tensor cores: widened V buffer i and its full / empty barriers
-    auto cvt_buf = [&](int i) { return base_s + L::kCvtOff + (uint32_t)i * L::kCvtTileBytes; };
-    auto cvt_full = [&](int i) { return bar0 + 8u * (2 * S + 2 * kQSlots + i); };
-    auto cvt_empty = [&](int i) { return bar0 + 8u * (2 * S + 2 * kQSlots + 2 + i); };
 
     if (tid == 0) {
         for (int s = 0; s < S; ++s) {
             mbar_init(full_bar(s), 1);
-            mbar_init(empty_bar(s), L::kCvt ? 2 : 1);  // FP8 on the tensor cores: consumer and converter
+            mbar_init(empty_bar(s), 1);
         }
         for (int i = 0; i < kQSlots; ++i) {
             mbar_init(qfull_bar(i), 1);
             mbar_init(qempty_bar(i), 1);
-        }
-        if constexpr (L::kCvt) {
-            for (int i = 0; i < 2; ++i) {
-                mbar_init(cvt_full(i), 1);
-                mbar_init(cvt_empty(i), 1);
-            }
         }
         fence_barrier_init();
         misc[0] = 0;  // abort flag
@@ -1017,7 +980,7 @@ __global__ void __launch_bounds__(Layout<T, D, BS, MMA, GF, KV>::kThreadsCta)
         }
         float* qf = reinterpret_cast<float*>(base + L::kQfOff);
         float* ptile = reinterpret_cast<float*>(base + L::kPTileOff);
-        typename std::conditional<MMA, MmaState<D, BS, L::kCvt, L::kCvt>, FmaState<KV, D, BS, GF>>::type st;
+        typename std::conditional<MMA, MmaState<D, BS, L::kF8>, FmaState<KV, D, BS, GF>>::type st;
         uint32_t k = 0, pi = 0;
         PieceIter it;
         it.init(P, t0, t1);
@@ -1041,13 +1004,9 @@ __global__ void __launch_bounds__(Layout<T, D, BS, MMA, GF, KV>::kThreadsCta)
             for (int i = 0; i < ntile; ++i) {
                 const uint32_t kk = k + i;
                 const int sidx = kk % S;
-                // FP8 on the tensor cores: K is read from the stage, V from the buffer
-                // the converter warp widened it into (kk % 2)
-                const bool ready = role_wait(full_bar(sidx), (kk / S) & 1, misc, p.status) &&
-                                   (!L::kCvt || role_wait(cvt_full(kk & 1), (kk >> 1) & 1, misc, p.status));
-                if (ready) {
+                if (role_wait(full_bar(sidx), (kk / S) & 1, misc, p.status)) {
                     const uint32_t kb = base_s + L::kStagesOff + sidx * L::kStageBytes;
-                    const uint32_t vb = L::kCvt ? cvt_buf(kk & 1) : kb + L::kTileBytes;
+                    const uint32_t vb = kb + L::kTileBytes;
                     const int tok0 = (j0 + i) * BS;
 #pragma unroll
                     for (int sub = 0; sub < BS / 16; ++sub) {
@@ -1061,10 +1020,7 @@ __global__ void __launch_bounds__(Layout<T, D, BS, MMA, GF, KV>::kThreadsCta)
                     }
                 }
                 __syncwarp();
-                if (lane == 0) {
-                    mbar_arrive(empty_bar(sidx));
-                    if constexpr (L::kCvt) mbar_arrive(cvt_empty(kk & 1));
-                }
+                if (lane == 0) mbar_arrive(empty_bar(sidx));
             }
             k += ntile;
             if constexpr (MMA) st.finish();
@@ -1081,27 +1037,6 @@ __global__ void __launch_bounds__(Layout<T, D, BS, MMA, GF, KV>::kThreadsCta)
                 st.store_partial(slot, G, lane);
             }
             ++pi;
-        }
-    } else if constexpr (L::kCvt) {
-        if (warp == kConverterWarp) {
-            // ========================= converter =========================
-            // Every tile of the range in issue order: wait for the stage to land
-            // and for V buffer kk % 2 to be free, widen the stage's V tile, then
-            // release the stage (the consumer releases it too, after its K) and
-            // hand the buffer to the consumer.
-            const uint32_t n = (uint32_t)(t1 - t0);
-            for (uint32_t kk = 0; kk < n; ++kk) {
-                const int sidx = kk % S, cb = kk & 1;
-                if (role_wait(full_bar(sidx), (kk / S) & 1, misc, p.status) &&
-                    role_wait(cvt_empty(cb), ((kk >> 1) & 1) ^ 1, misc, p.status))
-                    widen_fp8_tiles<D, BS, 1>(base_s + L::kStagesOff + sidx * L::kStageBytes + L::kTileBytes,
-                                              cvt_buf(cb), lane);
-                __syncwarp();
-                if (lane == 0) {
-                    mbar_arrive(empty_bar(sidx));
-                    mbar_arrive(cvt_full(cb));
-                }
-            }
         }
     }
     __syncthreads();
