@@ -237,14 +237,18 @@ def decode_bytes(lens, w, kv_elem=None) -> int:
     return kv + tables + 4 * len(lens) + qo
 
 
-def kernel_source_hash() -> str:
-    """Hash of the sources the decode and merge kernels and their launch are built from."""
+def kernel_source_hash(csrc=None) -> str:
+    """Hash of the code (comments and spacing dropped) the decode and merge kernels and their launch
+    are built from, so that a recorded ncu figure survives edits to comments only."""
+    import re
     h = hashlib.sha256()
-    csrc = os.path.join(ROOT, "paged_kv_cache_280_gb300", "csrc")
+    csrc = csrc or os.path.join(ROOT, "paged_kv_cache_280_gb300", "csrc")
     keep = ("pa_decode", "pa_device.cuh", "pa_internal.h", "pa_api.cu")
     for f in sorted(x for x in os.listdir(csrc) if x.startswith(keep) and x.endswith((".cu", ".cuh", ".h"))):
-        with open(os.path.join(csrc, f), "rb") as fh:
-            h.update(f.encode() + fh.read())
+        with open(os.path.join(csrc, f), encoding="utf-8") as fh:
+            code = re.sub(r"/\*.*?\*/", " ", fh.read(), flags=re.S)
+        code = re.sub(r"//[^\n]*", " ", code)
+        h.update(f.encode() + " ".join(code.split()).encode())
     return h.hexdigest()[:16]
 
 

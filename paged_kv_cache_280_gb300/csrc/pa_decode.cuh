@@ -9,15 +9,15 @@
 // tokens x D elements of K plus the same of V, contiguous in the pool.  The
 // tiles of segment (b, g) are its n_b = ceil(len_b / BS) blocks.  All tiles of
 // all segments are laid end to end (sequence-major, then KV head, then
-// block) and the grid's C CTAs take equal contiguous ranges of that list
-// (or, with a partition size P, ranges whose ends fall on multiples of P
-// tokens).  So every CTA moves the same number of bytes whatever the
-// length mix.  A CTA walks its range as "pieces" (the part of one segment
-// that lies in its range): a piece covering a whole segment is normalised
-// and written straight to `out`; a piece of a segment that straddles CTAs is
-// written as an unnormalised partial (m, l, o) to the workspace, and the
-// last CTA to finish a piece of that segment (an atomic counter per
-// segment) merges them:  M = max m_p,  out = sum e^(m_p-M) o_p / sum e^(m_p-M) l_p.
+// block) and the grid's C CTAs take contiguous ranges of that list, equal in
+// a cost of tiles plus a fixed cost per segment (or, with a partition size P,
+// ranges whose ends fall on multiples of P tokens).  A CTA walks its range as
+// "pieces" (the part of one segment that lies in its range): a piece covering
+// a whole segment is normalised and written straight to `out`; a piece of a
+// segment that straddles CTAs is written as an unnormalised partial (m, l, o)
+// to the workspace, and merge_kernel, launched right after as a programmatic
+// dependent, merges them once the decode grid has finished:
+//   M = max m_p,  out = sum e^(m_p-M) o_p / sum e^(m_p-M) l_p.
 //
 // CTA layout: two warps and several CTAs per SM.  The producer warp reads
 // block-table entries 32 at a time (one chunk ahead) and moves each tile with

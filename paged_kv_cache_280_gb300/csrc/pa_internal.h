@@ -10,11 +10,12 @@
 namespace pa {
 
 constexpr int kMaxCtasPerSm = 8;
-constexpr int kDefaultCtasPerSmMma = 4;  // default CTAs per SM on the tensor-core path  // bound used to size the decode workspace
-// Decode workspace: one merge counter per (sequence, KV head); per partial
-// slot [G][D] floats of o plus [G][2] floats of (m, l).
+constexpr int kDefaultCtasPerSmMma = 4;  // default CTAs per SM on the bf16 tensor-core path
+// Decode workspace: the status word, then two partial slots per CTA (sized
+// for kMaxCtasPerSm CTAs on every SM); a slot is [G][D] floats of o plus
+// [G][2] floats of (m, l).
 constexpr int kSlotExtraFloatsPerHead = 2;
-// floats of one partial slot, a multiple of 4 so that slots can be bulk-copied
+// floats of one partial slot, a multiple of 4 so that every slot is 16-byte aligned
 inline __host__ __device__ size_t partial_slot_floats(int G, int D) {
     return ((size_t)G * (D + kSlotExtraFloatsPerHead) + 3) & ~(size_t)3;
 }
