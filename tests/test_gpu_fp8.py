@@ -96,3 +96,41 @@ def test_fp8_decode_ignores_nan_in_unused_slots():
     got = _run_fp8(c)
     ref = oracle.decode_attention_fp8(c.q, c.kq, c.vq, *c.scales, c.ref_tables, c.lengths, c.w.scale, threads=8)
     check_close(got, ref, "bf16")
+
+
+@pytest.mark.parametrize("wl", ["long_context", "mha_b256"])
+def test_fp8_full_size_workloads(wl):
+    """The benchmark's FP8 configurations at full size, checked on sampled sequences: 4 x 131072
+    tokens at 8 query heads per KV head with 2048-token partitions, and the 256-sequence MHA batch
+    (one query head per KV head, the MMA's N padded)."""
+    import torch
+    import paged_kv_cache_280_gb300 as pa
+
+    if wl == "long_context":
+        w, pt = W.long_context(block_size=16), 2048
+    else:
+        w, pt = W.mha_b256_append(), 0
+    c = DecodeCase(w)
+    ks = vs = 1.0 / 64
+    # Seeded codes spread over every finite E4M3 value (the NaN codes 0x7F and 0xFF left out):
+    # inputs for both sides.  The oracle's encoder, a search over all codes per value, is too slow
+    # for the pools' billion values, and the decode does not care where its codes came from.
+    def codes(seed, shape):
+        u = synth.uniform_ints(seed, int(np.prod(shape)), 0, 253)
+        return np.where(u < 0x7F, u, u + 1).astype(np.uint8).reshape(shape)
+    kq, vq = codes(280101, c.k_pool.shape), codes(280102, c.v_pool.shape)
+    B = len(c.lengths)
+    if wl == "long_context":
+        sample = [0, 3]
+    else:
+        order = np.argsort(c.lengths)
+        sample = sorted(set(order[:3].tolist() + order[-3:].tolist() + list(range(0, B, 41))))
+    dq, dt, dl = to_torch(c.q), to_torch(c.tables), to_torch(c.lengths)
+    dk, dv = torch.from_numpy(kq).cuda(), torch.from_numpy(vq).cuda()
+    out = torch.empty_like(dq)
+    ws = torch.zeros(pa.pa_decode_workspace_bytes(B, w.num_q_heads, w.num_kv_heads, 128), dtype=torch.uint8,
+                     device="cuda")
+    pa.pa_decode_attention_fp8(out, dq, dk, dv, ks, vs, dt, dl, int(c.lengths.max()), w.scale, ws, partition_tokens=pt)
+    ref = oracle.decode_attention_fp8(c.q, kq, vq, ks, vs, c.ref_tables, c.lengths, w.scale, seqs=sample, threads=8)
+    check_close(to_numpy(out), ref, "bf16", rows=sample)
+    assert int(ws[:4].view(torch.int32).item()) == 0
