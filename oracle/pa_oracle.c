@@ -34,26 +34,30 @@
 
 enum { ORACLE_OK = 0, ORACLE_BAD_ARG = -1, ORACLE_BAD_BLOCK = -2, ORACLE_BAD_SLOT = -3, ORACLE_NOMEM = -4 };
 
+double oracle_e4m3_value(uint8_t c);
+
+/* dtype: 0 fp32, 1 bf16 bits, 3 OCP E4M3 codes (their value; the pool scale is applied by the caller) */
 static double load_elem(int dtype, const void* base, size_t idx) {
     if (dtype == 0) return (double)((const float*)base)[idx];
-    if (dtype == 2) return ((const double*)base)[idx]; /* widened FP8 pools */
+    if (dtype == 3) return oracle_e4m3_value(((const uint8_t*)base)[idx]);
     uint32_t bits = (uint32_t)((const uint16_t*)base)[idx] << 16; /* bf16 -> fp32 is exact */
     float f;
     memcpy(&f, &bits, sizeof f);
     return (double)f;
 }
 
-/* Gather K^ and V^ of (sequence b, KV head g) into contiguous [len][D] arrays. */
+/* Gather K^ and V^ of (sequence b, KV head g) into contiguous [len][D] arrays; element values
+   times the pool scales (1 unless the pools hold FP8 codes). */
 static int gather_kv(int dtype, const void* k_pool, const void* v_pool, const int32_t* table,
                      int32_t len, int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
-                     int32_t num_blocks, int32_t g, double* K, double* V) {
+                     int32_t num_blocks, int32_t g, double k_scale, double v_scale, double* K, double* V) {
     for (int32_t t = 0; t < len; ++t) {
         int32_t phys = table[t / block_size];
         if (phys < 0 || phys >= num_blocks) return ORACLE_BAD_BLOCK;
         size_t row = (((size_t)phys * num_kv_heads + g) * block_size + (size_t)(t % block_size)) * head_dim;
         for (int32_t i = 0; i < head_dim; ++i) {
-            K[(size_t)t * head_dim + i] = load_elem(dtype, k_pool, row + i);
-            V[(size_t)t * head_dim + i] = load_elem(dtype, v_pool, row + i);
+            K[(size_t)t * head_dim + i] = load_elem(dtype, k_pool, row + i) * k_scale;
+            V[(size_t)t * head_dim + i] = load_elem(dtype, v_pool, row + i) * v_scale;
         }
     }
     return ORACLE_OK;
@@ -69,10 +73,10 @@ static int check_common(int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_he
 
 /* Decode attention with separate element types for q and for the pools. */
 static int decode_impl(int q_dtype, const void* q, int kv_dtype, const void* k_pool, const void* v_pool,
-                       const int32_t* block_tables, int32_t max_blocks_per_seq, const int32_t* seq_lens,
-                       int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
-                       int32_t block_size, int32_t num_blocks, double scale, int32_t seq_begin, int32_t seq_end,
-                       double* out);
+                       double k_scale, double v_scale, const int32_t* block_tables, int32_t max_blocks_per_seq,
+                       const int32_t* seq_lens, int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads,
+                       int32_t head_dim, int32_t block_size, int32_t num_blocks, double scale, int32_t seq_begin,
+                       int32_t seq_end, double* out);
 
 /* Decode attention for sequences [seq_begin, seq_end); writes out[b] for those b only. */
 int oracle_decode_attention(int dtype, const void* q, const void* k_pool, const void* v_pool,
@@ -81,15 +85,16 @@ int oracle_decode_attention(int dtype, const void* q, const void* k_pool, const 
                             int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
                             int32_t num_blocks, double scale, int32_t seq_begin, int32_t seq_end,
                             double* out) {
-    return decode_impl(dtype, q, dtype, k_pool, v_pool, block_tables, max_blocks_per_seq, seq_lens, num_seqs,
-                       num_q_heads, num_kv_heads, head_dim, block_size, num_blocks, scale, seq_begin, seq_end, out);
+    return decode_impl(dtype, q, dtype, k_pool, v_pool, 1.0, 1.0, block_tables, max_blocks_per_seq, seq_lens,
+                       num_seqs, num_q_heads, num_kv_heads, head_dim, block_size, num_blocks, scale, seq_begin,
+                       seq_end, out);
 }
 
 static int decode_impl(int q_dtype, const void* q, int kv_dtype, const void* k_pool, const void* v_pool,
-                       const int32_t* block_tables, int32_t max_blocks_per_seq, const int32_t* seq_lens,
-                       int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
-                       int32_t block_size, int32_t num_blocks, double scale, int32_t seq_begin, int32_t seq_end,
-                       double* out) {
+                       double k_scale, double v_scale, const int32_t* block_tables, int32_t max_blocks_per_seq,
+                       const int32_t* seq_lens, int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads,
+                       int32_t head_dim, int32_t block_size, int32_t num_blocks, double scale, int32_t seq_begin,
+                       int32_t seq_end, double* out) {
     int rc = check_common(num_seqs, num_q_heads, num_kv_heads, head_dim, block_size, seq_begin, seq_end);
     if (rc) return rc;
     const int32_t G = num_q_heads / num_kv_heads;
@@ -111,7 +116,7 @@ static int decode_impl(int q_dtype, const void* q, int kv_dtype, const void* k_p
         const int32_t* table = block_tables + (size_t)b * max_blocks_per_seq;
         for (int32_t g = 0; g < num_kv_heads && rc == ORACLE_OK; ++g) {
             rc = gather_kv(kv_dtype, k_pool, v_pool, table, len, num_kv_heads, head_dim, block_size,
-                           num_blocks, g, K, V);
+                           num_blocks, g, k_scale, v_scale, K, V);
             if (rc) break;
             for (int32_t h = g * G; h < (g + 1) * G; ++h) {
                 size_t qrow = ((size_t)b * num_q_heads + h) * head_dim;
@@ -172,7 +177,7 @@ int oracle_decode_partials(int dtype, const void* q, const void* k_pool, const v
         const int32_t* table = block_tables + (size_t)b * max_blocks_per_seq;
         for (int32_t g = 0; g < num_kv_heads && rc == ORACLE_OK; ++g) {
             rc = gather_kv(dtype, k_pool, v_pool, table, len, num_kv_heads, head_dim, block_size,
-                           num_blocks, g, K, V);
+                           num_blocks, g, 1.0, 1.0, K, V);
             if (rc) break;
             for (int32_t h = g * G; h < (g + 1) * G; ++h) {
                 size_t qrow = ((size_t)b * num_q_heads + h) * head_dim;
@@ -319,7 +324,7 @@ int oracle_prefill_attention(int dtype, const void* q, const void* k_pool, const
         const int32_t* table = block_tables + (size_t)b * max_blocks_per_seq;
         for (int32_t g = 0; g < num_kv_heads && rc == ORACLE_OK; ++g) {
             rc = gather_kv(dtype, k_pool, v_pool, table, len, num_kv_heads, head_dim, block_size,
-                           num_blocks, g, K, V);
+                           num_blocks, g, 1.0, 1.0, K, V);
             if (rc) break;
             for (int32_t i = 0; i < n; ++i) {
                 const int32_t p = len - n + i; /* this token's position: keys 0..p are visible */
@@ -416,23 +421,11 @@ int oracle_decode_attention_fp8(int q_dtype, const void* q, const uint8_t* k_poo
                                 int32_t seq_begin, int32_t seq_end, double* out) {
     int rc = check_common(num_seqs, num_q_heads, num_kv_heads, head_dim, block_size, seq_begin, seq_end);
     if (rc) return rc;
-    /* widen the pools exactly (a 4-bit code value times an fp32 scale fits a double) and reuse the definition */
-    const size_t n = (size_t)num_blocks * num_kv_heads * block_size * head_dim;
-    double* kd = (double*)malloc(sizeof(double) * n);
-    double* vd = (double*)malloc(sizeof(double) * n);
-    if (!kd || !vd) {
-        free(kd); free(vd);
-        return ORACLE_NOMEM;
-    }
-    for (size_t i = 0; i < n; ++i) {
-        kd[i] = oracle_e4m3_value(k_pool[i]) * (double)k_scale;
-        vd[i] = oracle_e4m3_value(v_pool[i]) * (double)v_scale;
-    }
-    rc = decode_impl(q_dtype, q, 2, kd, vd, block_tables, max_blocks_per_seq, seq_lens, num_seqs, num_q_heads,
-                     num_kv_heads, head_dim, block_size, num_blocks, scale, seq_begin, seq_end, out);
-    free(kd);
-    free(vd);
-    return rc;
+    /* each code's value times its pool's scale, in double (exact: a 4-bit significand times an fp32
+       scale), then the definition; the values are widened per sequence as the definition reads them */
+    return decode_impl(q_dtype, q, 3, k_pool, v_pool, (double)k_scale, (double)v_scale, block_tables,
+                       max_blocks_per_seq, seq_lens, num_seqs, num_q_heads, num_kv_heads, head_dim, block_size,
+                       num_blocks, scale, seq_begin, seq_end, out);
 }
 
 /* Element-wise forms for the tests: out[i] = encode(x[i]); val[i] = value(codes[i]). */

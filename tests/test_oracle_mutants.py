@@ -37,8 +37,8 @@ C_MUTANTS = {
     "e4m3_subnormal_scale": ("ldexp((double)m, -9)", "ldexp((double)m, -10)"),
     "e4m3_bias_8": ("ldexp(1.0 + m / 8.0, e - 7)", "ldexp(1.0 + m / 8.0, e - 8)"),
     "e4m3_saturates_at_416": ("for (int c = 1; c <= 0x7E; ++c) {", "for (int c = 1; c <= 0x7D; ++c) {"),
-    "fp8_v_scale_dropped": ("vd[i] = oracle_e4m3_value(v_pool[i]) * (double)v_scale;",
-                            "vd[i] = oracle_e4m3_value(v_pool[i]);"),
+    "fp8_v_scale_dropped": ("V[(size_t)t * head_dim + i] = load_elem(dtype, v_pool, row + i) * v_scale;",
+                            "V[(size_t)t * head_dim + i] = load_elem(dtype, v_pool, row + i);"),
 }
 PIN_FILES = ["test_oracle_pins.py", "test_oracle_prefill_pins.py", "test_oracle_fp8_pins.py"]
 
