@@ -140,7 +140,7 @@ bool kernel_occupancy(int dev, const void* kernel, int threads, int smem, int* o
 
 namespace {
 
-size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
+size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }  // unused since the merge counters left the workspace
 
 struct WorkspaceLayout {
     size_t partials_off, total;

@@ -211,8 +211,9 @@ struct Plan {
 };
 
 // The pieces of a CTA range [t0, t1) in order.  at_t0 marks the piece that
-// starts at t0 (it owns partial slot 0 of the CTA; a later partial piece can
-// only be the last one, which owns slot 1).
+// starts at t0.  (The partial slots follow j0 instead: a piece with j0 > 0
+// continues its segment and starts the range, slot 0; a split segment's first
+// piece ends the range, slot 1.)
 struct PieceIter {
     int64_t t, t1, t0;
     int b;
