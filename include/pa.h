@@ -201,9 +201,10 @@ pa_status pa_decode_launch_info(int32_t num_seqs, int32_t num_q_heads, int32_t n
 
 /*
  * Tuning: CTAs per SM of the decode grid (1..8; 0 restores the default: 4 on
- * the bf16 tensor-core path, otherwise as many as fit, at most 8).  Process-wide; affects later pa_decode_attention
- * calls.  More CTAs per SM keep more tiles in flight but add split points
- * (partials) at CTA edges.
+ * the bf16 tensor-core path, otherwise, FP8 pools included, as many as fit,
+ * at most 8).  Process-wide; affects later pa_decode_attention and
+ * pa_decode_attention_fp8 calls.  More CTAs per SM keep more tiles in flight
+ * but add split points (partials) at CTA edges.
  */
 pa_status pa_decode_set_ctas_per_sm(int32_t ctas);
 
