@@ -1,0 +1,141 @@
+"""CPU: the decode work plan's arithmetic, as stated for the kernels (tile t of segment (b, h) at
+weighted unit K t + A (Hkv b + h + 1); CTA c takes units [ceil(cU/C), ceil((c+1)U/C)); with a
+partition size, ranges end on partition multiples), re-enacted in integers on random batches.
+Checks the properties the kernels rely on: every tile has exactly one owner and cta_of agrees with
+the range starts; no range is empty between two tiles of one segment, so a split segment's pieces
+come from consecutive CTAs; and the CTA boundaries that fall strictly inside a segment, taken at
+the first one, name every split segment exactly once (the merge kernel's work items).  The GPU
+parity tests check the kernels themselves."""
+import random
+
+
+def plan(lens_blocks, Hkv, C, PT, K=4, A=4):
+    B = len(lens_blocks)
+    pref = [0]
+    for n in lens_blocks:
+        pref.append(pref[-1] + n)
+    T = Hkv * pref[B]
+    upref = [0]
+    for n in lens_blocks:
+        upref.append(upref[-1] + ((n + PT - 1) // PT if PT else 0))
+    U = Hkv * upref[B] if PT else K * T + A * Hkv * B
+    units = U if PT else T
+    ce = min(units, C)
+    if PT and ce > 0:
+        per = (units + ce - 1) // ce
+        ce = (units + per - 1) // per
+    C = ce
+
+    def find_seq(pre, x):
+        lo, hi = 0, B - 1
+        while lo < hi:
+            mid = (lo + hi + 1) >> 1
+            if Hkv * pre[mid] <= x:
+                lo = mid
+            else:
+                hi = mid - 1
+        return lo
+
+    nbk = lambda b: pref[b + 1] - pref[b]
+    seg_start = lambda b, h: Hkv * pref[b] + h * nbk(b)
+
+    def first_tile_at_unit(x):
+        lo, hi = 0, B - 1
+        while lo < hi:
+            mid = (lo + hi + 1) >> 1
+            if Hkv * (K * pref[mid] + A * mid) <= x:
+                lo = mid
+            else:
+                hi = mid - 1
+        b = lo
+        nb = nbk(b)
+        local = x - Hkv * (K * pref[b] + A * b)
+        span = K * nb + A
+        if span == 0:
+            return Hkv * pref[b]
+        h, r = local // span, local % span
+        j = 0 if r <= A else (r - A + K - 1) // K
+        return Hkv * pref[b] + h * nb + j
+
+    def tile_of_unit(u):
+        if u >= U:
+            return T
+        b = find_seq(upref, u)
+        local = u - Hkv * upref[b]
+        ub = upref[b + 1] - upref[b]
+        return seg_start(b, local // ub) + (local % ub) * PT
+
+    def cta_start(c):
+        if PT == 0:
+            return T if c >= C else first_tile_at_unit((c * U + C - 1) // C)
+        return tile_of_unit(c * U // C)
+
+    def cta_of(t):
+        b = find_seq(pref, t)
+        local = t - Hkv * pref[b]
+        nb = nbk(b)
+        h, j = local // nb, local % nb
+        if PT == 0:
+            return (K * t + A * (Hkv * b + h + 1)) * C // U
+        ub = upref[b + 1] - upref[b]
+        u = Hkv * upref[b] + h * ub + j // PT
+        return ((u + 1) * C - 1) // U
+
+    return dict(B=B, C=C, T=T, pref=pref, nbk=nbk, seg_start=seg_start, find_seq=find_seq, cta_start=cta_start,
+                cta_of=cta_of)
+
+
+def _check(lens_blocks, Hkv, C, PT):
+    P = plan(lens_blocks, Hkv, C, PT)
+    if P["T"] == 0:
+        return
+    starts = [P["cta_start"](c) for c in range(P["C"] + 1)]
+    assert starts[0] == 0 and starts[-1] == P["T"]
+    assert all(a <= b for a, b in zip(starts, starts[1:]))
+    split = set()
+    for b in range(P["B"]):
+        nb = P["nbk"](b)
+        for h in range(Hkv if nb else 0):
+            s0 = P["seg_start"](b, h)
+            owners = [P["cta_of"](t) for t in range(s0, s0 + nb)]
+            for t, c in zip(range(s0, s0 + nb), owners):
+                assert starts[c] <= t < starts[c + 1]
+            ca, cb = owners[0], owners[-1]
+            assert sorted(set(owners)) == list(range(ca, cb + 1))  # consecutive, none skipped
+            if ca != cb:
+                split.add((b, h, ca, cb - ca + 1))
+    named = []
+    for c in range(1, P["C"]):
+        t = starts[c]
+        if t >= P["T"]:
+            continue
+        b = P["find_seq"](P["pref"], t)
+        nb = P["nbk"](b)
+        local = t - Hkv * P["pref"][b]
+        h, j = local // nb, local % nb
+        if j == 0:
+            continue
+        ca = P["cta_of"](t - j)
+        if ca != c - 1:
+            continue
+        named.append((b, h, ca, P["cta_of"](t - j + nb - 1) - ca + 1))
+    assert len(named) == len(set(named)) and set(named) == split
+
+
+def test_plan_properties_on_random_batches():
+    rng = random.Random(280)
+    for _ in range(1500):
+        B = rng.randint(1, 10)
+        Hkv = rng.choice([1, 2, 4, 8])
+        lens = [rng.choice([0, 0, 1, 2, 3, 5, 9, 17, 40]) for _ in range(B)]
+        _check(lens, Hkv, rng.randint(1, 64), rng.choice([0, 0, 0, 1, 2, 4]))
+
+
+def test_weighted_balance_spreads_segment_cost():
+    # a batch of one long sequence and many one-block ones: with a segment weight the CTAs that
+    # take the many short segments get fewer tiles than those inside the long one
+    lens = [64] + [1] * 32
+    P = plan(lens, 1, 8, 0)
+    starts = [P["cta_start"](c) for c in range(P["C"] + 1)]
+    tiles = [b - a for a, b in zip(starts, starts[1:])]
+    assert max(tiles[:3]) > min(tiles[-3:])
