@@ -1,8 +1,8 @@
 """Planted mistakes in the oracle must be caught by its pins.
 
 Each mutant is a copy of the oracle's C source with one plausible slip
-(compiled on the CPU into a temporary directory); the pin tests of
-test_oracle_pins.py are rerun against it and at least one must fail.  The
+(compiled on the CPU into a temporary directory); the pin tests (PIN_FILES)
+are rerun against it and at least one must fail.  The
 allocator model gets the same treatment through small subclasses.
 """
 import os
@@ -37,10 +37,23 @@ C_MUTANTS = {
     "e4m3_subnormal_scale": ("ldexp((double)m, -9)", "ldexp((double)m, -10)"),
     "e4m3_bias_8": ("ldexp(1.0 + m / 8.0, e - 7)", "ldexp(1.0 + m / 8.0, e - 8)"),
     "e4m3_saturates_at_416": ("for (int c = 1; c <= 0x7E; ++c) {", "for (int c = 1; c <= 0x7D; ++c) {"),
+    "append_slot_before_head": ("size_t dst = (((size_t)blk * num_kv_heads + h) * block_size + (size_t)off) * head_dim + e;",
+                                "size_t dst = (((size_t)blk * block_size + (size_t)off) * num_kv_heads + h) * head_dim + e;"),
+    "append_k_only": ("memcpy((char*)v_pool + dst * elem_bytes, (const char*)v_new + src * elem_bytes, elem_bytes);", ""),
+    "append_skips_slot_zero": ("if (s < 0) continue;\n        int64_t blk = s / block_size, off = s % block_size;",
+                               "if (s <= 0) continue;\n        int64_t blk = s / block_size, off = s % block_size;"),
+    "append_offset_from_block": ("int64_t blk = s / block_size, off = s % block_size;",
+                                 "int64_t blk = s / block_size, off = blk % block_size;"),
+    "copy_k_only": ("memcpy((char*)v_pool + ((size_t)dst * block_elems + e) * elem_bytes,\n"
+                    "                   (const char*)v_pool + ((size_t)src * block_elems + e) * elem_bytes, elem_bytes);", ""),
+    "copy_one_head": ("for (size_t e = 0; e < block_elems; ++e) {", "for (size_t e = 0; e < block_elems / num_kv_heads; ++e) {"),
+    "copy_direction_reversed": ("int32_t src = pairs[2 * p], dst = pairs[2 * p + 1];",
+                                "int32_t dst = pairs[2 * p], src = pairs[2 * p + 1];"),
     "fp8_v_scale_dropped": ("V[(size_t)t * head_dim + i] = load_elem(dtype, v_pool, row + i) * v_scale;",
                             "V[(size_t)t * head_dim + i] = load_elem(dtype, v_pool, row + i);"),
 }
-PIN_FILES = ["test_oracle_pins.py", "test_oracle_prefill_pins.py", "test_oracle_fp8_pins.py"]
+PIN_FILES = ["test_oracle_pins.py", "test_oracle_prefill_pins.py", "test_oracle_fp8_pins.py",
+             "test_oracle_cache_ops_pins.py"]
 
 
 @pytest.fixture(scope="module")
