@@ -2,10 +2,14 @@
 """Benchmark of the paged-attention decode step on GB300.
 
 Metric: paged decode attention KV-tokens/s (and HBM GB/s as a fraction of
-the measured HBM peak) at 1 GPU.  Workload (default): the bf16 decode batch
-of 64 sequences with the pages' skewed length mix (70 % U[32,511], 25 %
-U[512,2047], 5 % U[2048,4095]), 32 query / 8 KV heads, head_dim 128,
-16-token blocks scattered through a pool sized to demand + 10 %.
+the measured HBM peak) at 1 GPU.  Headline workload (default): the largest
+single-GPU one, the bf16 decode batch of 256 sequences with the pages' skewed
+length mix (70 % U[32,511], 25 % U[512,2047], 5 % U[2048,4095]), MHA 32 heads,
+head_dim 128, 16-token blocks scattered through a pool sized to demand + 10 %,
+one new token appended per sequence and step.  Every other workload of the
+pages (the tiny fp32 case, the GQA-4 batch of 64, parallel sampling with
+copy-on-write, and 4 x 128K-token contexts at block size 16 and 32) is
+measured the same way in the same run and reported under `per_config`.
 
 One step = the whole hot path for one decode iteration of the batch:
   a1 host allocator appends one token per sequence (slots, CoW pairs, tables)
@@ -18,7 +22,7 @@ its time is reported separately.  `e2e` runs genuine decode steps through
 the public API: host allocator, pinned host -> device copies of the step's
 inputs, the kernels, and the device -> host copy of the output.
 
-N > 1 (torchrun): every rank owns its own 64 sequences (weak scaling, no
+N > 1 (torchrun): every rank owns its own batch (weak scaling, no
 data-path collective); the timed region is bracketed by barriers and the
 max time over ranks is used.
 """
@@ -165,6 +169,7 @@ class ClockSampler:
 # workload
 # ---------------------------------------------------------------------------
 WORKLOADS = {
+    "tiny_f32": "fp32 decode of 4 sequences with lengths {5,17,33,48}, MHA 4 heads, d 64, 16-token blocks, 32-block pool",
     "gqa4_b64": "bf16 decode batch of 64 skew-mixed lengths, 32 query / 8 KV heads, d 128, 16-token blocks",
     "mha_b256_append": "bf16 decode batch of 256 skew-mixed lengths, MHA 32 heads, d 128, one appended token per step",
     "cow_sampling": "16 prompts of 1031 tokens forked into 8 samples each (refcount-shared blocks), tails U[0,256], "
@@ -182,6 +187,10 @@ def build_workload(name: str, rank: int, world: int, extra_steps: int):
     if name not in WORKLOADS:
         raise SystemExit(f"unknown workload {name}; one of {sorted(WORKLOADS)}")
     seed_shift = 7919 * rank
+    if name == "tiny_f32":
+        base = W.tiny_fp32()
+        demand = int(sum(-(-(int(x) + extra_steps) // base.block_size) for x in base.lengths))
+        return W.scaled(base, num_blocks=max(base.num_blocks, demand), seed=base.seed + seed_shift)
     if name == "gqa4_b64":
         # every rank owns its own slice of one global length draw
         base = W.gqa4_b64()
@@ -262,10 +271,16 @@ def measured_peaks():
         return FALLBACK_HBM_GBS, "fallback"
 
 
-def recorded_traffic():
-    """DRAM bytes per decode call on gqa4_b64 (bf16) from the committed ncu summary, if it was taken on
-    this kernel source."""
-    path = os.path.join(ROOT, "profiles", "decode_gqa4_b64_traffic.txt")
+# the headline: the largest single-GPU workload (2.66 GB of algorithmic bytes per decode)
+DEFAULT_WORKLOAD = "mha_b256_append"
+# every workload of the pages, in config order; the headline is one of them, the others go to per_config
+PER_CONFIG = ["tiny_f32", "gqa4_b64", "mha_b256_append", "cow_sampling", "long_context_bs16", "long_context_bs32"]
+
+
+def recorded_traffic(workload: str):
+    """DRAM bytes per decode call (decode and merge kernels, bf16 pools) on this workload from the committed ncu
+    summary, if it was taken on this kernel source; else None."""
+    path = os.path.join(ROOT, "profiles", f"decode_{workload}_traffic.txt")
     try:
         with open(path) as f:
             kv = dict(line.split("=", 1) for line in f.read().split("\n") if "=" in line and not line.startswith("#"))
@@ -291,32 +306,182 @@ def fp8_codes(bf16_bits: np.ndarray, scale: float) -> np.ndarray:
 
 
 def cpu_baseline(w, q, k_pool, v_pool, tables, lens, seconds: float, scales=None):
+    """The oracle on the host cores over a bounded sample of the workload's sequences: rounds of as many
+    sequences as there are threads (rotating through the batch) until `seconds` have passed, one round at
+    least."""
     import oracle
 
     threads = os.cpu_count() or 1
     B = len(lens)
-    done_tokens, t0, rounds = 0, time.perf_counter(), 0
-    seqs_done = 0
+    chunk = max(1, min(B, threads))
+    done_tokens, evals, rounds, start = 0, 0, 0, 0
+    t0 = time.perf_counter()
     while True:
-        chunk = list(range(B))
+        seqs = sorted({(start + j) % B for j in range(chunk)})
         if scales:
-            oracle.decode_attention_fp8(q, k_pool, v_pool, *scales, tables, lens, w.scale, seqs=chunk, threads=threads)
+            oracle.decode_attention_fp8(q, k_pool, v_pool, *scales, tables, lens, w.scale, seqs=seqs, threads=threads)
         else:
-            oracle.decode_attention(q, k_pool, v_pool, tables, lens, w.scale, seqs=chunk, threads=threads)
-        done_tokens += int(np.sum(lens, dtype=np.int64))
-        seqs_done += len(chunk)
+            oracle.decode_attention(q, k_pool, v_pool, tables, lens, w.scale, seqs=seqs, threads=threads)
+        done_tokens += int(sum(int(lens[s]) for s in seqs))
+        evals += len(seqs)
         rounds += 1
+        start += chunk
         if time.perf_counter() - t0 >= seconds:
             break
     dt = time.perf_counter() - t0
-    return {"value": done_tokens / dt, "unit": UNIT, "cores": threads, "kind": "oracle",
-            "sample": f"fp64 C oracle over the whole {B}-sequence batch, {rounds} pass(es) ({dt:.1f} s), "
-                      f"{threads} threads over sequences"}
+    return {"value": done_tokens / dt, "unit": UNIT, "cores": min(threads, chunk), "kind": "oracle",
+            "sample": f"fp64 C oracle, {rounds} round(s) of {chunk} of the {B} sequences (rotating), {evals} "
+                      f"sequence evaluations in {dt:.1f} s, one thread per sequence"}
 
 
 # ---------------------------------------------------------------------------
 # our arm
 # ---------------------------------------------------------------------------
+class DecodeSetup:
+    """One workload's decode step, device-resident: pools, the step's allocator outputs, q, out, workspace."""
+
+    def __init__(self, name, args, rank, world, dev, pa, e2e_steps):
+        import torch
+
+        self.name, self.pa, self.dev = name, pa, dev
+        self.w = w = build_workload(name, rank, world, extra_steps=1 + e2e_steps + 2)
+        self.fp8 = fp8 = args.kv == "fp8"
+        self.Hq, self.Hkv, self.D, self.bs, self.PT = w.num_q_heads, w.num_kv_heads, w.head_dim, w.block_size, w.partition_tokens
+        self.lib = pa.Allocator(w.num_blocks, self.bs, free_order=w.free_order())
+        self.ids = populate(self.lib, w)
+        self.B = B = len(self.ids)
+        self.max_blocks = int(-(-(max(self.lib.length(s) for s in self.ids) + 2 + e2e_steps) // self.bs))
+        self.k_host, self.v_host = w.pool_values("k"), w.pool_values("v")
+        self.KS, self.VS = FP8_K_SCALE, FP8_V_SCALE
+        if fp8:
+            # FP8 pools: E4M3 codes of the same N(0,1) draws over the pool scales (input data, made on the host)
+            self.k_host, self.v_host = fp8_codes(self.k_host, self.KS), fp8_codes(self.v_host, self.VS)
+            self.dk, self.dv = torch.from_numpy(self.k_host).to(dev), torch.from_numpy(self.v_host).to(dev)
+        else:
+            self.dk, self.dv = self.to_dev(self.k_host), self.to_dev(self.v_host)
+        # ---- a1 once: the step's allocator outputs become device-resident inputs ----
+        t_alloc = time.perf_counter()
+        slots, pairs = self.lib.append_batch(self.ids)
+        self.tables, self.lens = self.lib.export_tables(self.ids, self.max_blocks)
+        self.host_alloc_us = (time.perf_counter() - t_alloc) * 1e6
+        self.q = w.queries(step=1)
+        k_new, v_new = w.new_tokens("k", B, step=1), w.new_tokens("v", B, step=1)
+        self.d_q, self.d_kn, self.d_vn = self.to_dev(self.q), self.to_dev(k_new), self.to_dev(v_new)
+        self.d_slots, self.d_tables, self.d_lens = self.to_dev(slots), self.to_dev(self.tables), self.to_dev(self.lens)
+        self.d_pairs = self.to_dev(pairs) if len(pairs) else None
+        self.out = torch.empty_like(self.d_q)
+        self.ws = torch.zeros(pa.pa_decode_workspace_bytes(B, self.Hq, self.Hkv, self.D), dtype=torch.uint8, device=dev)
+        self.max_len = int(self.lens.max())
+
+    def to_dev(self, a):
+        import torch
+
+        if a.dtype == np.uint16:
+            return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).to(self.dev)
+        return torch.from_numpy(np.ascontiguousarray(a)).to(self.dev)
+
+    def append(self, kn_, vn_, slots_, **kw):
+        if self.fp8:
+            self.pa.pa_reshape_and_cache_fp8(kn_, vn_, self.dk, self.dv, slots_, self.KS, self.VS, **kw)
+        else:
+            self.pa.pa_reshape_and_cache(kn_, vn_, self.dk, self.dv, slots_, **kw)
+
+    def attend(self, q_, tables_, lens_, max_len_, **kw):
+        if self.fp8:
+            self.pa.pa_decode_attention_fp8(self.out, q_, self.dk, self.dv, self.KS, self.VS, tables_, lens_, max_len_,
+                                            self.w.scale, self.ws, partition_tokens=self.PT, **kw)
+        else:
+            self.pa.pa_decode_attention(self.out, q_, self.dk, self.dv, tables_, lens_, max_len_, self.w.scale, self.ws,
+                                        partition_tokens=self.PT, **kw)
+
+    def step(self, stream):
+        """a2 (when the allocator emitted copy-on-write pairs) and a3."""
+        st = self.ws[:4].view(__import__("torch").int32)
+        if self.d_pairs is not None:
+            self.pa.pa_copy_blocks(self.dk, self.dv, self.d_pairs, status=st, stream=stream)
+        self.append(self.d_kn, self.d_vn, self.d_slots, status=st, stream=stream)
+
+    def decode(self, stream):
+        """a4 + a5: the decode call (decode and merge kernels)."""
+        self.attend(self.d_q, self.d_tables, self.d_lens, self.max_len, stream=stream)
+
+    def time_steps(self, K, Wm, flush_l2, stream, dist, on_timed=None):
+        """W untimed steps, then K timed steps (events at their ends only) and K decode calls timed alone.
+
+        An event between the append and the decode would keep the decode from starting its prologue while
+        the append runs (it is launched as the append's programmatic dependent), so the steps carry events
+        at their two ends only; the decode call alone is timed in a second loop of K, for the roofline."""
+        import torch
+
+        for _ in range(Wm):
+            flush_l2()
+            self.step(stream)
+            self.decode(stream)
+        torch.cuda.synchronize()
+        if dist:
+            dist.barrier()
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+        dev_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+        if on_timed:
+            on_timed(True)
+        torch.cuda.synchronize()
+        for i in range(K):
+            flush_l2()
+            ev[i][0].record(stream)
+            self.step(stream)
+            self.decode(stream)
+            ev[i][1].record(stream)
+        torch.cuda.synchronize()
+        if dist:
+            dist.barrier()
+        for i in range(K):
+            flush_l2()
+            self.step(stream)
+            dev_ev[i][0].record(stream)
+            self.decode(stream)
+            dev_ev[i][1].record(stream)
+        torch.cuda.synchronize()
+        if dist:
+            dist.barrier()
+        if on_timed:
+            on_timed(False)
+        status = int(self.ws[:4].view(torch.int32).item())
+        if status:
+            raise SystemExit(f"{self.name}: device status word {status:#x}")
+        return [a.elapsed_time(b) for a, b in ev], [a.elapsed_time(b) for a, b in dev_ev]
+
+    def bytes_and_unique(self):
+        elem = 1 if self.fp8 else self.w.elem_bytes
+        dbytes = decode_bytes(self.lens, self.w, kv_elem=elem)
+        # KV bytes of the distinct physical blocks the step reads (below the per-sequence
+        # bytes when sequences share prefix blocks, which L2 then serves more than once)
+        used = [self.tables[i, : -(-int(n) // self.bs)] for i, n in enumerate(self.lens)]
+        unique_kv = int(np.unique(np.concatenate(used)).size) * self.bs * self.Hkv * self.D * 2 * elem if self.B else 0
+        return dbytes, unique_kv
+
+    def summary(self, step_ms, dec_ms, peak):
+        """Per-config figures: decode call time (median, mean), algorithmic GB/s and its fraction of the peak."""
+        dbytes, unique_kv = self.bytes_and_unique()
+        mean_s = statistics.mean(dec_ms) / 1e3
+        tokens = int(np.sum(self.lens, dtype=np.int64))
+        ctas, stages, smem, mma = self.pa.pa_decode_launch_info(self.B, self.Hq, self.Hkv, self.D, self.bs, self.max_blocks,
+                                                                self.pa.PA_FP8_E4M3 if self.fp8 else
+                                                                (self.pa.PA_F32 if self.w.dtype == "f32" else self.pa.PA_BF16))
+        d = {
+            "workload": self.w.name + ("_fp8kv" if self.fp8 else ""), "dtype": self.w.dtype,
+            "kv_tokens_per_step": tokens, "decode_bytes_per_step": dbytes,
+            "step_ms_mean": statistics.mean(step_ms), "value_kv_tokens_per_s": tokens * len(step_ms) / (sum(step_ms) / 1e3),
+            "decode_us_median": 1e3 * statistics.median(dec_ms), "decode_us_mean": 1e3 * statistics.mean(dec_ms),
+            "decode_us_min": 1e3 * min(dec_ms), "decode_gbs": dbytes / mean_s / 1e9,
+            "frac_of_measured_hbm": dbytes / mean_s / 1e9 / peak, "decode_ctas": ctas, "stages": stages,
+            "path": "mma.sync" if mma else "fma", "partition_tokens": self.PT, "steps": len(step_ms),
+        }
+        if self.w.prompts:  # shared prompt blocks: L2 serves them more than once
+            d["unique_block_kv_bytes_per_step"] = unique_kv
+            d["unique_block_gbs"] = unique_kv / mean_s / 1e9
+        return d
+
+
 def run_ours(args, rank, world, local_rank):
     import torch
 
@@ -327,53 +492,9 @@ def run_ours(args, rank, world, local_rank):
 
     K, Wm = args.steps, args.warmup
     K_e2e = args.e2e_steps
-    w = build_workload(args.workload, rank, world, extra_steps=1 + K_e2e + 2)
-    Hq, Hkv, D, bs, PT = w.num_q_heads, w.num_kv_heads, w.head_dim, w.block_size, w.partition_tokens
-    lib = pa.Allocator(w.num_blocks, bs, free_order=w.free_order())
-    ids = populate(lib, w)
-    B = len(ids)
-    max_blocks = int(-(-(max(lib.length(s) for s in ids) + 2 + K_e2e) // bs))
-
-    def to_dev(a):
-        if a.dtype == np.uint16:
-            return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).to(dev)
-        return torch.from_numpy(np.ascontiguousarray(a)).to(dev)
-
-    k_host, v_host = w.pool_values("k"), w.pool_values("v")
-    fp8 = args.kv == "fp8"
-    KS, VS = FP8_K_SCALE, FP8_V_SCALE
-    if fp8:
-        # FP8 pools: E4M3 codes of the same N(0,1) draws over the pool scales (input data, made on the host)
-        k_host, v_host = fp8_codes(k_host, KS), fp8_codes(v_host, VS)
-        dk, dv = torch.from_numpy(k_host).to(dev), torch.from_numpy(v_host).to(dev)
-    else:
-        dk, dv = to_dev(k_host), to_dev(v_host)
-
-    def append(kn_, vn_, slots_, **kw):
-        if fp8:
-            pa.pa_reshape_and_cache_fp8(kn_, vn_, dk, dv, slots_, KS, VS, **kw)
-        else:
-            pa.pa_reshape_and_cache(kn_, vn_, dk, dv, slots_, **kw)
-
-    def attend(q_, tables_, lens_, max_len_, **kw):
-        if fp8:
-            pa.pa_decode_attention_fp8(out, q_, dk, dv, KS, VS, tables_, lens_, max_len_, w.scale, ws,
-                                       partition_tokens=PT, **kw)
-        else:
-            pa.pa_decode_attention(out, q_, dk, dv, tables_, lens_, max_len_, w.scale, ws, partition_tokens=PT, **kw)
-
-    # ---- a1 once: the step's allocator outputs become device-resident inputs ----
-    t_alloc = time.perf_counter()
-    slots, pairs = lib.append_batch(ids)
-    tables, lens = lib.export_tables(ids, max_blocks)
-    host_alloc_us = (time.perf_counter() - t_alloc) * 1e6
-    q = w.queries(step=1)
-    k_new, v_new = w.new_tokens("k", B, step=1), w.new_tokens("v", B, step=1)
-    d_q, d_kn, d_vn = to_dev(q), to_dev(k_new), to_dev(v_new)
-    d_slots, d_tables, d_lens = to_dev(slots), to_dev(tables), to_dev(lens)
-    d_pairs = to_dev(pairs) if len(pairs) else None
-    out = torch.empty_like(d_q)
-    ws = torch.zeros(pa.pa_decode_workspace_bytes(B, Hq, Hkv, D), dtype=torch.uint8, device=dev)
+    S = DecodeSetup(args.workload, args, rank, world, dev, pa, K_e2e)
+    w, B, Hq, Hkv, D, bs = S.w, S.B, S.Hq, S.Hkv, S.D, S.bs
+    fp8, ids, lib, max_blocks, out = S.fp8, S.ids, S.lib, S.max_blocks, S.out
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
 
     def flush_l2():
@@ -383,78 +504,30 @@ def run_ours(args, rank, world, local_rank):
         flush.zero_()
         flush[: L2_FLUSH_BYTES // 2].view(torch.int32).sum()
 
-    max_len = int(lens.max())
     stream = torch.cuda.current_stream()
-
-    def step():
-        if d_pairs is not None:
-            pa.pa_copy_blocks(dk, dv, d_pairs, status=ws[:4].view(torch.int32), stream=stream)
-        append(d_kn, d_vn, d_slots, status=ws[:4].view(torch.int32), stream=stream)
-
-    def decode():
-        attend(d_q, d_tables, d_lens, max_len, stream=stream)
-
-    for _ in range(Wm):
-        flush_l2()
-        step()
-        decode()
-    torch.cuda.synchronize()
-    if dist:
-        dist.barrier()
-    # The K timed steps carry events only at their two ends: an event between the append and the
-    # decode would keep the decode from starting its prologue while the append runs (it is
-    # launched as the append's programmatic dependent).  The decode call alone (decode and merge
-    # kernels) is timed in a second loop of K, for the roofline.
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
-    dev_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
     clocks = ClockSampler(local_rank)
-    clocks.start()
-    torch.cuda.synchronize()
-    for i in range(K):
-        flush_l2()
-        ev[i][0].record(stream)
-        step()
-        decode()
-        ev[i][1].record(stream)
-    torch.cuda.synchronize()
-    if dist:
-        dist.barrier()
-    for i in range(K):
-        flush_l2()
-        step()
-        dev_ev[i][0].record(stream)
-        decode()
-        dev_ev[i][1].record(stream)
-    torch.cuda.synchronize()
-    if dist:
-        dist.barrier()
-    clocks.stop()
-    step_ms = [a.elapsed_time(b) for a, b in ev]
-    dec_ms = [a.elapsed_time(b) for a, b in dev_ev]
-    status = int(ws[:4].view(torch.int32).item())
-    if status:
-        raise SystemExit(f"device status word {status:#x}")
+    step_ms, dec_ms = S.time_steps(K, Wm, flush_l2, stream, dist,
+                                   on_timed=lambda on: clocks.start() if on else clocks.stop())
     total_s = reduce_max(sum(step_ms) / 1e3, dist, dev)
-    tokens_step = int(np.sum(lens, dtype=np.int64))
+    tokens_step = int(np.sum(S.lens, dtype=np.int64))
     all_tokens = reduce_sum(float(tokens_step * K), dist, dev)
     value = all_tokens / total_s
-    dbytes = decode_bytes(lens, w, kv_elem=1 if fp8 else w.elem_bytes)
-    # KV bytes of the distinct physical blocks the step reads (below the per-sequence
-    # bytes when sequences share prefix blocks, which L2 then serves more than once)
-    used = [tables[i, : -(-int(n) // bs)] for i, n in enumerate(lens)]
-    unique_kv = int(np.unique(np.concatenate(used)).size) * bs * Hkv * D * 2 * (1 if fp8 else w.elem_bytes) if B else 0
+    dbytes, unique_kv = S.bytes_and_unique()
     dec_mean_s = statistics.mean(dec_ms) / 1e3
     peak, peak_kind = measured_peaks()
     achieved = dbytes / dec_mean_s / 1e9
     ctas, stages, smem, mma = pa.pa_decode_launch_info(B, Hq, Hkv, D, bs, max_blocks,
-                                                       pa.PA_FP8_E4M3 if fp8 else pa.PA_BF16)
+                                                       pa.PA_FP8_E4M3 if fp8 else
+                                                       (pa.PA_F32 if w.dtype == "f32" else pa.PA_BF16))
 
     # ---- e2e: genuine decode steps through the public API with host buffers ----
     # Each step's inputs travel in one pinned staging buffer, copied to the device
     # with one H2D copy: q, k_new, v_new (produced upstream, filled before the
     # loop), then the allocator's slots, CoW pairs, block tables and lengths,
     # which the allocator writes in place during the step.
-    regions = [("q", B * Hq * D * 2), ("kn", B * Hkv * D * 2), ("vn", B * Hkv * D * 2), ("slots", B * 8),
+    e = w.elem_bytes
+    tdt, hdt = (torch.float32, torch.int32) if e == 4 else (torch.bfloat16, torch.int16)
+    regions = [("q", B * Hq * D * e), ("kn", B * Hkv * D * e), ("vn", B * Hkv * D * e), ("slots", B * 8),
                ("pairs", B * 2 * 4), ("tables", B * max_blocks * 4), ("lens", B * 4)]
     offs, pos = {}, 0
     for name, n in regions:
@@ -476,22 +549,22 @@ def run_ours(args, rank, world, local_rank):
             o, n = offs[name]
             hb.numpy()[o:o + n] = np.ascontiguousarray(src).view(np.uint8).reshape(-1)
     dev_stage = torch.empty(stage_bytes, dtype=torch.uint8, device=dev)
-    e_q = region(dev_stage, "q", torch.bfloat16, (B, Hq, D))
-    e_kn = region(dev_stage, "kn", torch.bfloat16, (B, Hkv, D))
-    e_vn = region(dev_stage, "vn", torch.bfloat16, (B, Hkv, D))
+    e_q = region(dev_stage, "q", tdt, (B, Hq, D))
+    e_kn = region(dev_stage, "kn", tdt, (B, Hkv, D))
+    e_vn = region(dev_stage, "vn", tdt, (B, Hkv, D))
     e_slots = region(dev_stage, "slots", torch.int64, (B,))
     e_pairs = region(dev_stage, "pairs", torch.int32, (B, 2))
     e_tables = region(dev_stage, "tables", torch.int32, (B, max_blocks))
     e_lens = region(dev_stage, "lens", torch.int32, (B,))
-    h_out = torch.empty((B, Hq, D), dtype=torch.int16).pin_memory()
+    h_out = torch.empty((B, Hq, D), dtype=hdt).pin_memory()
     ids_arr = np.asarray(ids, np.int64)
     cap_len = max_blocks * bs  # a length bound every step's tables respect
 
     def device_step(hb, max_len_, st):
         dev_stage.copy_(hb, non_blocking=True)
-        append(e_kn, e_vn, e_slots, stream=st)
-        attend(e_q, e_tables, e_lens, max_len_, stream=st)
-        h_out.copy_(out.view(torch.int16), non_blocking=True)
+        S.append(e_kn, e_vn, e_slots, stream=st)
+        S.attend(e_q, e_tables, e_lens, max_len_, stream=st)
+        h_out.copy_(out.view(hdt), non_blocking=True)
 
     graphs = []
     if not args.e2e_eager:
@@ -522,10 +595,10 @@ def run_ours(args, rank, world, local_rank):
         else:  # copy-on-write pairs go between the H2D copy and the append: launched one by one
             dev_stage.copy_(host_stage[s % n_stage], non_blocking=True)
             if len(pr):
-                pa.pa_copy_blocks(dk, dv, e_pairs[: len(pr)], stream=stream)
-            append(e_kn, e_vn, e_slots, stream=stream)
-            attend(e_q, e_tables, e_lens, cap_len, stream=stream)
-            h_out.copy_(out.view(torch.int16), non_blocking=True)
+                pa.pa_copy_blocks(S.dk, S.dv, e_pairs[: len(pr)], stream=stream)
+            S.append(e_kn, e_vn, e_slots, stream=stream)
+            S.attend(e_q, e_tables, e_lens, cap_len, stream=stream)
+            h_out.copy_(out.view(hdt), non_blocking=True)
 
     # The allocator runs one step ahead of the GPU, as a serving loop's scheduler does: step s+1's
     # slots and tables are written into their own staging buffer while the GPU runs step s.  Every
@@ -541,7 +614,7 @@ def run_ours(args, rank, world, local_rank):
         gpu_step(s, pr)
         e2e_tokens += toks
         h2d += stage_bytes
-        d2h += h_out.numel() * 2
+        d2h += h_out.numel() * e
         launches += 3 + (1 if len(pr) else 0)
         if s + 1 < K_e2e:
             pr, toks = host_prepare(s + 1)
@@ -553,7 +626,7 @@ def run_ours(args, rank, world, local_rank):
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K, "warmup": Wm,
         "ms_per_step": total_s * 1e3 / K, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": "fp8_e4m3 kv, bf16 q/out" if fp8 else "bf16",
+        "dtype": "fp8_e4m3 kv, bf16 q/out" if fp8 else w.dtype,
         "data": f"synthetic, seeded: {WORKLOADS[args.workload]}; blocks scattered by a seeded free-list order",
         "config": {
             "workload": (w.name + ("_fp8kv" if fp8 else "")) if world == 1 else f"{w.name} per rank",
@@ -564,27 +637,57 @@ def run_ours(args, rank, world, local_rank):
                       "(decode and merge kernels) timed alone in a second loop of as many steps",
             "l2": f"flushed between timed steps ({L2_FLUSH_BYTES >> 20} MiB write, then a {L2_FLUSH_BYTES >> 21} MiB read "
                   "so that no dirty line is left; untimed)",
-            "host_alloc_us_per_step": round(host_alloc_us, 1), "decode_ctas": ctas, "stages": stages,
-            "smem_bytes": smem, "path": "mma.sync" if mma else "fma", "partition_tokens": PT,
-            "kv_dtype": "fp8_e4m3" if fp8 else "bf16", **({"k_scale": KS, "v_scale": VS} if fp8 else {}),
+            "host_alloc_us_per_step": round(S.host_alloc_us, 1), "decode_ctas": ctas, "stages": stages,
+            "smem_bytes": smem, "path": "mma.sync" if mma else "fma", "partition_tokens": S.PT,
+            "kv_dtype": "fp8_e4m3" if fp8 else "bf16", **({"k_scale": S.KS, "v_scale": S.VS} if fp8 else {}),
             "decode_ms_median": statistics.median(dec_ms), "decode_ms_min": min(dec_ms),
             "step_gbs": (dbytes + 4 * B * Hkv * D * 2) / (total_s / K) / 1e9,
         },
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
                      "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured" else "fallback",
-                     "kernel": "pa_decode_attention (decode_kernel, then merge_kernel)", "traffic": recorded_traffic() if args.workload == "gqa4_b64" and not fp8 else None},
+                     "kernel": "pa_decode_attention (decode_kernel, then merge_kernel)",
+                     "traffic": None if fp8 else recorded_traffic(args.workload)},
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d // max(1, K_e2e),
                 "d2h_bytes_per_step": d2h // max(1, K_e2e), "steps": K_e2e,
                 "includes": "host allocator writing into pinned staging one step ahead of the GPU, one H2D of "
                             "q/k_new/v_new/slots/pairs/tables/lens, kernels, D2H of out; no L2 flush inside the loop "
                             "(the KV read per step is larger than L2 and loaded evict-first)",
                 "launch": "eager" if args.e2e_eager else "one CUDA graph per staging buffer (H2D, append, decode, merge, D2H)"},
-        "gpu_launches": K * (3 + (1 if d_pairs is not None else 0)),  # append, decode, merge (+ CoW copy)
+        "gpu_launches": K * (3 + (1 if S.d_pairs is not None else 0)),  # append, decode, merge (+ CoW copy)
         "clocks": clocks.summary(),
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline(w, q, k_host, v_host, tables, lens, args.cpu_seconds,
-                                            scales=(KS, VS) if fp8 else None)
+        line["cpu_baseline"] = cpu_baseline(w, S.q, S.k_host, S.v_host, S.tables, S.lens, args.cpu_seconds,
+                                            scales=(S.KS, S.VS) if fp8 else None)
+    # The other workloads of the pages (every config that is not the headline), each measured the same way
+    # on this machine in this run, with its own bounded CPU baseline.  Single-GPU runs only.
+    if world == 1 and not args.no_per_config:
+        del S, dev_stage, graphs, host_stage
+        torch.cuda.empty_cache()
+        per = {}
+        all_samples = []
+        for name in PER_CONFIG:
+            if name == args.workload or (fp8 and name == "tiny_f32"):
+                continue
+            C = DecodeSetup(name, args, 0, 1, dev, pa, 0)
+            cs = ClockSampler(local_rank)
+            sm, dm = C.time_steps(args.per_config_steps, 3, flush_l2, stream, None,
+                                  on_timed=lambda on, cs=cs: cs.start() if on else cs.stop())
+            d = C.summary(sm, dm, peak)
+            d["clocks"] = cs.summary()
+            all_samples += cs.samples
+            d["traffic"] = None if fp8 else recorded_traffic(name)
+            if not args.no_cpu_baseline:
+                d["cpu_baseline"] = cpu_baseline(C.w, C.q, C.k_host, C.v_host, C.tables, C.lens,
+                                                 args.per_config_cpu_seconds, scales=(C.KS, C.VS) if fp8 else None)
+            per[name] = d
+            del C
+            torch.cuda.empty_cache()
+        line["per_config"] = per
+        agg = ClockSampler.__new__(ClockSampler)
+        agg.samples, agg.max_mhz, agg._nvml = all_samples, line["clocks"].get("sm_max_mhz"), True
+        line["per_config_clocks"] = agg.summary()
+        line["gpu_launches_per_config"] = {k: v["steps"] * 3 for k, v in per.items()}
     if rank == 0:
         print(json.dumps(line), flush=True)
     if dist:
@@ -757,7 +860,7 @@ def run_prefill(args, rank, world, local_rank):
         dev_stage.copy_(host_stage, non_blocking=True)
         append(e_kn, e_vn, e_slots)
         prefill(e_q, e_tables, e_lens, e_cu)
-        h_out.copy_(out.view(torch.int16), non_blocking=True)
+        h_out.copy_(out.view(hdt), non_blocking=True)
         stream.synchronize()
         e2e_s += time.perf_counter() - t0
     e2e_total = reduce_max(e2e_s, dist, dev)
@@ -1025,7 +1128,11 @@ def main(argv=None):
     ap.add_argument("--steps", type=int, default=300)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", default="gqa4_b64", choices=sorted(WORKLOADS))
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(WORKLOADS),
+                    help="headline workload (default: the largest single-GPU one); the others go to per_config")
+    ap.add_argument("--no-per-config", action="store_true", help="measure the headline workload only")
+    ap.add_argument("--per-config-steps", type=int, default=20)
+    ap.add_argument("--per-config-cpu-seconds", type=float, default=2.0)
     ap.add_argument("--e2e-steps", type=int, default=128)
     ap.add_argument("--e2e-eager", action="store_true", help="e2e: launch the step's calls one by one, no CUDA graph")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)

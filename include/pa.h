@@ -59,7 +59,7 @@ typedef enum pa_status {
     PA_ERR_NO_SUCH_SEQ = 4,        /* unknown sequence id */
     PA_ERR_SEQ_EXISTS = 5,         /* sequence id already in use */
     PA_ERR_REFCOUNT_LIMIT = 6,     /* fork would push a block past the refcount cap */
-    PA_ERR_WORKSPACE_TOO_SMALL = 7,/* decode workspace smaller than pa_decode_workspace_bytes */
+    PA_ERR_WORKSPACE_TOO_SMALL = 7,/* decode workspace smaller than the launch needs (see pa_decode_workspace_bytes) */
     PA_ERR_BUFFER_TOO_SMALL = 8,   /* a host output array is too short */
     PA_ERR_CUDA = 9,               /* a CUDA runtime call or launch failed */
     PA_ERR_INTERNAL = 10,          /* unexpected host failure (e.g. host memory exhausted) */
@@ -117,9 +117,14 @@ pa_status pa_copy_blocks(void* k_pool, void* v_pool, const int32_t* src_dst_pair
  * Size in bytes of the device workspace pa_decode_attention needs for these
  * shapes on the current CUDA device.  The workspace holds the status word
  * (first int32, in a 256-byte head) and two split-sequence partial slots per
- * CTA the device can hold.  The caller allocates it ONCE, with the status word
- * zeroed, and may reuse it across calls on one stream: the partial slots are
- * written before they are read, and the status word only gathers error bits.
+ * CTA of the decode grid; this size covers the largest grid the device can
+ * take (8 CTAs on every SM), so it suffices for every call with these head
+ * shapes whatever pa_decode_set_ctas_per_sm says.  A call refuses (with
+ * PA_ERR_WORKSPACE_TOO_SMALL, before launching) only a workspace smaller than
+ * what its own grid touches.  The caller allocates it ONCE, with the status
+ * word zeroed, and may reuse it across calls on one stream: the partial slots
+ * are written before they are read, and the status word only gathers error
+ * bits.
  */
 pa_status pa_decode_workspace_bytes(int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads,
                                     int32_t head_dim, size_t* bytes_out);
@@ -152,9 +157,9 @@ pa_status pa_decode_workspace_bytes(int32_t num_seqs, int32_t num_q_heads, int32
  * The kernel is launched as a programmatic dependent of the preceding kernel
  * on `stream`: when that kernel allows an early start (pa_reshape_and_cache
  * does), this one computes its work split from seq_lens and block_tables and
- * starts reading them while that kernel finishes; it reads the pools and q
- * only after that kernel has completed.  So a kernel that allows early start
- * must not write seq_lens or block_tables.
+ * starts reading them while that kernel finishes; it reads the pools and q,
+ * and writes out and the workspace, only after that kernel has completed.  So
+ * a kernel that allows early start must not write seq_lens or block_tables.
  */
 pa_status pa_decode_attention(void* out, const void* q, const void* k_pool, const void* v_pool,
                               const int32_t* block_tables, int32_t max_blocks_per_seq, const int32_t* seq_lens,
@@ -171,11 +176,17 @@ pa_status pa_decode_attention(void* out, const void* q, const void* k_pool, cons
  * Arguments and results are those of pa_decode_attention, minus the
  * workspace.  Its scratch is a static buffer of PA_STATIC_WORKSPACE_BYTES
  * (8 MiB) in the library's device image, held on every GPU that loads the
- * library until the process exits.  Shapes whose scratch
- * (pa_decode_workspace_bytes) exceeds it return PA_ERR_WORKSPACE_TOO_SMALL
- * before anything runs.  The call allocates nothing: it clears the status word
- * at the head of the buffer (cudaMemsetAsync) and enqueues the decode.  If dev_status_out is not NULL, the call's device status word
- * (PA_DEV_* bits) is copied there on `stream` afterwards.
+ * library until the process exits.  A call whose decode grid needs more
+ * scratch than that (the status head plus two partial slots of
+ * G * (head_dim + 2) floats per CTA) returns PA_ERR_WORKSPACE_TOO_SMALL before
+ * anything runs; on a 152-SM GB300 every supported shape fits at the default
+ * CTAs per SM.  The call allocates nothing: after its argument checks it
+ * clears the status word at the head of the buffer (cudaMemsetAsync) and
+ * enqueues the decode.  That memset sits between the decode and the kernel
+ * before it on the stream, so unlike pa_decode_attention this call does not
+ * overlap its start with a preceding pa_reshape_and_cache.  If
+ * dev_status_out is not NULL, the call's device status word (PA_DEV_* bits)
+ * is copied there on `stream` afterwards.
  * The first call on a device looks up the buffer's device address; make that
  * first call before any stream capture.  Every call on a device shares the
  * one buffer, so calls that can overlap on the GPU (different streams, or
@@ -207,6 +218,20 @@ pa_status pa_decode_launch_info(int32_t num_seqs, int32_t num_q_heads, int32_t n
  * but add split points (partials) at CTA edges.
  */
 pa_status pa_decode_set_ctas_per_sm(int32_t ctas);
+
+/*
+ * Testing aid for failure detection (no counterpart on the pages): the time
+ * limit, in nanoseconds, of the decode kernel's waits for its query rows and
+ * KV tiles (consumer side).  Every on-chip wait of the kernels is bounded; one
+ * that runs out sets PA_DEV_WAIT_TIMEOUT in the status word, the CTA stops
+ * issuing and consuming, waits (with the full limit) for the copies it has
+ * already issued, and exits, so the context stays usable and the output of
+ * that call is not valid.  A limit far below a DRAM round trip makes the waits
+ * run out on purpose.  0 restores the default (2 s); values above it return
+ * PA_ERR_INVALID_ARG.  Process-wide; affects later pa_decode_attention,
+ * pa_decode_attention_fp8 and pa_decode_attention_static calls.
+ */
+pa_status pa_debug_set_wait_limit_ns(uint64_t ns);
 
 /*
  * FP8 KV pools (an extrapolation: the pages list FP8 among the quantisation

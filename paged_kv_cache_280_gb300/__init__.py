@@ -73,6 +73,7 @@ _SIGS = {
     "pa_prefill_attention": (_i32, [_vp, _vp, _vp, _vp, _vp, _i32, _vp, _vp, _i32, _i32, _i32, _i32, _i32, _i32,
                                     _i32, _i32, ctypes.c_float, _i32, _vp, _vp]),
     "pa_decode_set_ctas_per_sm": (_i32, [_i32]),
+    "pa_debug_set_wait_limit_ns": (_i32, [ctypes.c_uint64]),
     "pa_alloc_create": (_i32, [_i32, _i32, _vp, ctypes.POINTER(_vp)]),
     "pa_alloc_destroy": (None, [_vp]),
     "pa_alloc_set_max_refcount": (_i32, [_vp, _i32]),
@@ -285,6 +286,11 @@ def pa_prefill_attention(out, q, k_pool, v_pool, block_tables, seq_lens, cu_q_le
 
 def pa_decode_set_ctas_per_sm(ctas: int) -> None:
     _ok(_lib.pa_decode_set_ctas_per_sm(int(ctas)), "pa_decode_set_ctas_per_sm")
+
+
+def pa_debug_set_wait_limit_ns(ns: int) -> None:
+    """Testing aid: time limit of the decode consumer's waits (0 restores the 2 s default)."""
+    _ok(_lib.pa_debug_set_wait_limit_ns(int(ns)), "pa_debug_set_wait_limit_ns")
 
 
 # ---------------------------------------------------------------------------

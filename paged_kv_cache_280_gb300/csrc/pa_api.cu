@@ -13,6 +13,7 @@ namespace {
 
 constexpr int kMaxDevices = 64;
 std::atomic<int> g_ctas_per_sm{0};  // 0 = the per-path default
+std::atomic<uint64_t> g_wait_limit_ns{0};  // 0 = kWaitLimitNs
 
 struct DeviceInfo {
     int sms = 0;
@@ -140,18 +141,16 @@ bool kernel_occupancy(int dev, const void* kernel, int threads, int smem, int* o
 
 namespace {
 
-size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }  // unused since the merge counters left the workspace
-
 struct WorkspaceLayout {
     size_t partials_off, total;
 };
 
-WorkspaceLayout workspace_layout(int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
-                                 int sms) {
+// The status head, then two partial slots for each of `ctas` CTAs.
+WorkspaceLayout workspace_layout(int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim, int64_t ctas) {
     WorkspaceLayout w;
     const size_t G = (size_t)(num_q_heads / num_kv_heads);
-    w.partials_off = 256;  // after the status word
-    w.total = w.partials_off + (size_t)2 * sms * kMaxCtasPerSm * partial_slot_floats((int)G, head_dim) * 4;
+    w.partials_off = kStatusHeadBytes;
+    w.total = w.partials_off + (size_t)2 * ctas * partial_slot_floats((int)G, head_dim) * 4;
     return w;
 }
 
@@ -234,13 +233,20 @@ extern "C" pa_status pa_decode_workspace_bytes(int32_t num_seqs, int32_t num_q_h
         return PA_ERR_INVALID_ARG;
     int dev = 0, sms = 0;
     if (!current_device(&dev, &sms)) return PA_ERR_CUDA;
-    *bytes_out = workspace_layout(num_seqs, num_q_heads, num_kv_heads, head_dim, sms).total;
+    // enough for the largest grid any launch on this device can take
+    *bytes_out = workspace_layout(num_q_heads, num_kv_heads, head_dim, (int64_t)sms * kMaxCtasPerSm).total;
     return PA_OK;
 }
 
 extern "C" pa_status pa_decode_set_ctas_per_sm(int32_t ctas) {
     if (ctas < 0 || ctas > kMaxCtasPerSm) return PA_ERR_INVALID_ARG;
     g_ctas_per_sm.store(ctas);
+    return PA_OK;
+}
+
+extern "C" pa_status pa_debug_set_wait_limit_ns(uint64_t ns) {
+    if (ns > kWaitLimitNs) return PA_ERR_INVALID_ARG;
+    g_wait_limit_ns.store(ns);
     return PA_OK;
 }
 
@@ -263,15 +269,17 @@ extern "C" pa_status pa_decode_launch_info(int32_t num_seqs, int32_t num_q_heads
 }
 
 namespace pa {
-namespace {
 
-// Shared by pa_decode_attention (pools of the query dtype) and
-// pa_decode_attention_fp8 (FP8 pools, bf16 queries, K and V scales).
+// Shared by pa_decode_attention (pools of the query dtype),
+// pa_decode_attention_fp8 (FP8 pools, bf16 queries, K and V scales) and the
+// static-workspace entry point (clear_status: zero the status head on the
+// stream once every check has passed, right before the launch).
 pa_status decode_common(void* out, const void* q, const void* k_pool, const void* v_pool, const int32_t* block_tables,
                         int32_t max_blocks_per_seq, const int32_t* seq_lens, int32_t max_seq_len, int32_t num_seqs,
                         int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
                         int32_t num_blocks, float scale, int32_t partition_tokens, void* workspace,
-                        size_t workspace_bytes, pa_dtype dtype, float k_scale, float v_scale, void* stream) {
+                        size_t workspace_bytes, pa_dtype dtype, float k_scale, float v_scale, void* stream,
+                        bool clear_status) {
     if (dtype != PA_F32 && dtype != PA_BF16 && dtype != PA_FP8_E4M3) return PA_ERR_UNSUPPORTED;
     pa_status s = check_shapes(num_seqs, num_q_heads, num_kv_heads, head_dim, block_size);
     if (s != PA_OK) return s;
@@ -298,7 +306,8 @@ pa_status decode_common(void* out, const void* q, const void* k_pool, const void
     s = plan_launch(num_seqs, num_q_heads, num_kv_heads, head_dim, block_size, max_tiles > 0 ? max_tiles : 1, fixed,
                     dtype, &lp);
     if (s != PA_OK) return s;
-    const WorkspaceLayout wl = workspace_layout(num_seqs, num_q_heads, num_kv_heads, head_dim, lp.sms);
+    // the bytes this launch touches: the status head and two partial slots per CTA of its grid
+    const WorkspaceLayout wl = workspace_layout(num_q_heads, num_kv_heads, head_dim, lp.grid);
     if (workspace_bytes < wl.total) return PA_ERR_WORKSPACE_TOO_SMALL;
 
     CUtensorMap tk, tv;
@@ -328,11 +337,14 @@ pa_status decode_common(void* out, const void* q, const void* k_pool, const void
     p.seg_units = lp.mma ? PA_SEG_UNITS_MMA : PA_SEG_UNITS_FMA;
     p.scale_log2 = scale * 1.4426950408889634f * k_scale;
     p.out_scale = v_scale;
+    const uint64_t lim = g_wait_limit_ns.load();
+    p.wait_limit_ns = lim ? lim : kWaitLimitNs;
+    if (clear_status && cudaMemsetAsync(workspace, 0, kStatusHeadBytes, static_cast<cudaStream_t>(stream)) != cudaSuccess)
+        return PA_ERR_CUDA;
     lp.v.launch(p, tk, tv, lp.grid, lp.smem, lp.merge_grid, lp.merge_smem, static_cast<cudaStream_t>(stream));
     return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }
 
-}  // namespace
 }  // namespace pa
 
 extern "C" pa_status pa_decode_attention(void* out, const void* q, const void* k_pool, const void* v_pool,
@@ -344,7 +356,7 @@ extern "C" pa_status pa_decode_attention(void* out, const void* q, const void* k
     if (dtype != PA_F32 && dtype != PA_BF16) return PA_ERR_UNSUPPORTED;
     return pa::decode_common(out, q, k_pool, v_pool, block_tables, max_blocks_per_seq, seq_lens, max_seq_len, num_seqs,
                              num_q_heads, num_kv_heads, head_dim, block_size, num_blocks, scale, partition_tokens,
-                             workspace, workspace_bytes, dtype, 1.f, 1.f, stream);
+                             workspace, workspace_bytes, dtype, 1.f, 1.f, stream, false);
 }
 
 extern "C" pa_status pa_decode_attention_fp8(void* out, const void* q, const void* k_pool, const void* v_pool,
@@ -356,5 +368,5 @@ extern "C" pa_status pa_decode_attention_fp8(void* out, const void* q, const voi
                                              void* workspace, size_t workspace_bytes, void* stream) {
     return pa::decode_common(out, q, k_pool, v_pool, block_tables, max_blocks_per_seq, seq_lens, max_seq_len, num_seqs,
                              num_q_heads, num_kv_heads, head_dim, block_size, num_blocks, scale, partition_tokens,
-                             workspace, workspace_bytes, PA_FP8_E4M3, k_scale, v_scale, stream);
+                             workspace, workspace_bytes, PA_FP8_E4M3, k_scale, v_scale, stream, false);
 }

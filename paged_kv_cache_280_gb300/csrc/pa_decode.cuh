@@ -240,10 +240,15 @@ struct PieceIter {
 };
 
 // Warp-collective wait used by both roles: every lane of the warp calls it.
+// It gives up after limit_ns, or as soon as the other role has given up (the
+// CTA's abort flag): the giving-up warp flags PA_DEV_WAIT_TIMEOUT and sets the
+// abort flag.  After an abort the consumer releases no stage or query slot and
+// the producer issues no copy, so no copy can land in a buffer that another is
+// still filling; the producer then waits (full limit) for the copies it issued.
 __device__ __forceinline__ bool role_wait(uint32_t bar, uint32_t parity, volatile int32_t* abort_flag,
-                                          int32_t* status) {
+                                          int32_t* status, uint64_t limit_ns = kWaitLimitNs) {
     if (__any_sync(0xffffffffu, *abort_flag != 0)) return false;
-    bool ok = mbar_wait(bar, parity);
+    bool ok = mbar_wait(bar, parity, limit_ns, abort_flag);
     ok = __all_sync(0xffffffffu, ok);
     if (!ok) {
         *abort_flag = 1;
@@ -972,7 +977,11 @@ __global__ void __launch_bounds__(Layout<T, D, BS, MMA, GF, KV>::kThreadsCta)
             mbar_wait(qfull_bar(qq % kQSlots), (qq / kQSlots) & 1);
     } else if (warp == kConsumerWarp) {
         // =========================== consumer ===========================
-        // zero outputs of empty sequences
+        // `out` may be read or written by the preceding kernel on the stream: wait
+        // for it before the first store (the consumer's first query wait comes
+        // after the producer's own, so this costs nothing), then zero the outputs
+        // of empty sequences
+        pdl_wait_prerequisites();
         for (int bb = c; bb < B; bb += C) {
             if (pref[bb + 1] == pref[bb]) {
                 T* o = static_cast<T*>(p.out) + (size_t)bb * Hq * D;
@@ -990,7 +999,7 @@ __global__ void __launch_bounds__(Layout<T, D, BS, MMA, GF, KV>::kThreadsCta)
         while (it.next(P, b, h, j0, j1, at_t0)) {
             const int qs = pi % kQSlots;
             const uint8_t* qslot = base + L::kQOff + qs * L::kQSlotBytes;
-            const bool qok = role_wait(qfull_bar(qs), (pi / kQSlots) & 1, misc, p.status);
+            const bool qok = role_wait(qfull_bar(qs), (pi / kQSlots) & 1, misc, p.status, p.wait_limit_ns);
             if constexpr (MMA) {
                 if (qok) st.load_q(qslot, G, lane);
             } else {
@@ -998,14 +1007,15 @@ __global__ void __launch_bounds__(Layout<T, D, BS, MMA, GF, KV>::kThreadsCta)
                 for (int e = lane; e < G * D; e += 32) qf[e] = qok ? static_cast<float>(qsrc[e]) * p.scale_log2 : 0.f;
             }
             __syncwarp();
-            if (lane == 0) mbar_arrive(qempty_bar(qs));
+            if (lane == 0 && qok) mbar_arrive(qempty_bar(qs));  // after an abort the slot stays held
             st.reset();
             const int len = lens_s[b];
             const int ntile = j1 - j0;
             for (int i = 0; i < ntile; ++i) {
                 const uint32_t kk = k + i;
                 const int sidx = kk % S;
-                if (role_wait(full_bar(sidx), (kk / S) & 1, misc, p.status)) {
+                const bool ok = role_wait(full_bar(sidx), (kk / S) & 1, misc, p.status, p.wait_limit_ns);
+                if (ok) {
                     const uint32_t kb = base_s + L::kStagesOff + sidx * L::kStageBytes;
                     const uint32_t vb = kb + L::kTileBytes;
                     const int tok0 = (j0 + i) * BS;
@@ -1021,7 +1031,7 @@ __global__ void __launch_bounds__(Layout<T, D, BS, MMA, GF, KV>::kThreadsCta)
                     }
                 }
                 __syncwarp();
-                if (lane == 0) mbar_arrive(empty_bar(sidx));
+                if (lane == 0 && ok) mbar_arrive(empty_bar(sidx));  // after an abort the stage stays held
             }
             k += ntile;
             if constexpr (MMA) st.finish();

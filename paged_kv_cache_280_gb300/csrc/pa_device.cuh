@@ -10,12 +10,9 @@
 #include <stdint.h>
 
 #include "../../include/pa.h"
+#include "pa_internal.h"
 
 namespace pa {
-
-// Longest a pipeline wait may spin before the kernel gives up (flags
-// PA_DEV_WAIT_TIMEOUT and skips the rest of its work).
-constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
 
 __device__ __forceinline__ void flag_status(int32_t* status, int32_t bit) {
     if (status) atomicOr(status, bit);
@@ -61,13 +58,18 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 }
 
 // Wait for the phase of `bar` with the given parity to complete.  Returns
-// false if it did not within kWaitLimitNs (the caller then flags and aborts).
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
+// false if it did not within limit_ns (the caller then flags and aborts), or,
+// when abort_flag is given, once another warp of the CTA has set it.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint64_t limit_ns = kWaitLimitNs,
+                                          volatile int32_t* abort_flag = nullptr) {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = global_timer_ns();
     for (uint32_t it = 1;; ++it) {
         if (mbar_try_wait(bar, parity)) return true;
-        if ((it & 63u) == 0 && global_timer_ns() - t0 > kWaitLimitNs) return false;
+        if ((it & 63u) == 0) {
+            if (abort_flag && *abort_flag) return false;
+            if (global_timer_ns() - t0 > limit_ns) return false;
+        }
     }
 }
 

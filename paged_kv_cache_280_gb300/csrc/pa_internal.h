@@ -9,11 +9,16 @@
 
 namespace pa {
 
+// Longest a pipeline wait may spin before the kernel gives up (flags
+// PA_DEV_WAIT_TIMEOUT and skips the rest of its work).
+constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
+
 constexpr int kMaxCtasPerSm = 8;
 constexpr int kDefaultCtasPerSmMma = 4;  // default CTAs per SM on the bf16 tensor-core path
-// Decode workspace: the status word, then two partial slots per CTA (sized
-// for kMaxCtasPerSm CTAs on every SM); a slot is [G][D] floats of o plus
-// [G][2] floats of (m, l).
+// Decode workspace: the status word, then two partial slots per CTA of the
+// launch's grid (pa_decode_workspace_bytes sizes it for kMaxCtasPerSm CTAs on
+// every SM, the largest grid); a slot is [G][D] floats of o plus [G][2] floats
+// of (m, l).
 constexpr int kSlotExtraFloatsPerHead = 2;
 // floats of one partial slot, a multiple of 4 so that every slot is 16-byte aligned
 inline __host__ __device__ size_t partial_slot_floats(int G, int D) {
@@ -55,6 +60,9 @@ struct DecodeParams {
     int32_t seg_units;
     float scale_log2;  // scale * log2(e) (times the K scale of an FP8 pool): scores in the base-2 domain
     float out_scale;   // multiplies the output: the V scale of an FP8 pool, else 1
+    // time limit of the consumer's waits for query rows and tiles (the producer's
+    // waits, and its final wait for the copies it issued, keep the full limit)
+    uint64_t wait_limit_ns;
 };
 
 // One compiled decode kernel (dtype, head_dim, block_size, compute path).
@@ -82,6 +90,18 @@ bool decode_variant_bf16_mma(int head_dim, int block_size, DecodeVariant* out);
 bool decode_variant_bf16_fma(int head_dim, int block_size, int group, DecodeVariant* out);
 // bf16 queries and outputs over FP8 (E4M3) pools, CUDA-core path.
 bool decode_variant_fp8(int head_dim, int block_size, int group, DecodeVariant* out);
+
+// The decode of pa_decode_attention / _fp8 (pa_api.cu): checks, plan and launch.
+// Refuses a workspace smaller than the bytes its own grid touches (the status
+// head and two partial slots per CTA).  clear_status zeroes the status head on
+// the stream after every check has passed, right before the launch.
+constexpr size_t kStatusHeadBytes = 256;
+pa_status decode_common(void* out, const void* q, const void* k_pool, const void* v_pool, const int32_t* block_tables,
+                        int32_t max_blocks_per_seq, const int32_t* seq_lens, int32_t max_seq_len, int32_t num_seqs,
+                        int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
+                        int32_t num_blocks, float scale, int32_t partition_tokens, void* workspace,
+                        size_t workspace_bytes, pa_dtype dtype, float k_scale, float v_scale, void* stream,
+                        bool clear_status);
 
 // Host launch helpers shared by the attention entry points (pa_api.cu).
 // The TMA map of a pool viewed as [num_blocks * Hkv * block_size][head_dim]

@@ -49,26 +49,22 @@ extern "C" pa_status pa_decode_attention_static(void* out, const void* q, const 
                                                 int32_t block_size, int32_t num_blocks, float scale,
                                                 int32_t partition_tokens, pa_dtype dtype, int32_t* dev_status_out,
                                                 void* stream) {
-    // Size check first: shapes whose scratch would not fit are refused before anything runs.
-    size_t need = 0;
-    pa_status s = pa_decode_workspace_bytes(num_seqs, num_q_heads, num_kv_heads, head_dim, &need);
-    if (s != PA_OK) return s;
-    if (need > kStaticWorkspaceBytes) return PA_ERR_WORKSPACE_TOO_SMALL;
+    if (dtype != PA_F32 && dtype != PA_BF16) return PA_ERR_UNSUPPORTED;
     if (reinterpret_cast<uintptr_t>(dev_status_out) & 3u) return PA_ERR_INVALID_ARG;
     void* ws = nullptr;
-    s = static_workspace(&ws);
+    pa_status s = static_workspace(&ws);
     if (s != PA_OK) return s;
-    // The buffer keeps the previous call's contents.  The status word at its head
-    // must start at zero; the partial slots are written before they are read.
-    const size_t head = 256;
-    cudaStream_t st = static_cast<cudaStream_t>(stream);
-    if (cudaMemsetAsync(ws, 0, head, st) != cudaSuccess) return PA_ERR_CUDA;
-    s = pa_decode_attention(out, q, k_pool, v_pool, block_tables, max_blocks_per_seq, seq_lens, max_seq_len,
-                            num_seqs, num_q_heads, num_kv_heads, head_dim, block_size, num_blocks, scale,
-                            partition_tokens, ws, kStaticWorkspaceBytes, dtype, stream);
+    // The buffer keeps the previous call's contents.  The decode checks every
+    // argument first, refuses a launch whose grid needs more scratch than the
+    // buffer holds (PA_ERR_WORKSPACE_TOO_SMALL, nothing enqueued), and only then
+    // zeroes the status word at the buffer's head; the partial slots are written
+    // before they are read.
+    s = pa::decode_common(out, q, k_pool, v_pool, block_tables, max_blocks_per_seq, seq_lens, max_seq_len, num_seqs,
+                          num_q_heads, num_kv_heads, head_dim, block_size, num_blocks, scale, partition_tokens, ws,
+                          kStaticWorkspaceBytes, dtype, 1.f, 1.f, stream, /*clear_status=*/true);
     if (s != PA_OK) return s;
-    if (dev_status_out &&
-        cudaMemcpyAsync(dev_status_out, ws, sizeof(int32_t), cudaMemcpyDeviceToDevice, st) != cudaSuccess)
+    if (dev_status_out && cudaMemcpyAsync(dev_status_out, ws, sizeof(int32_t), cudaMemcpyDeviceToDevice,
+                                          static_cast<cudaStream_t>(stream)) != cudaSuccess)
         return PA_ERR_CUDA;
     return PA_OK;
 }

@@ -62,3 +62,13 @@ def test_swap_host_checks_run_before_any_launch():
     bad[4] = ctypes.c_void_p((1 << 20) + 8)  # misaligned store
     assert pa._lib.pa_swap_out(*bad) == 1
     assert pa._lib.pa_swap_in(*ok_args[:3], 0, *ok_args[4:]) == 0  # nothing to copy
+
+
+def test_wait_limit_knob_checks_its_argument():
+    """The failure-detection testing aid runs on the host: above the 2 s default is refused, 0 restores it."""
+    import pytest
+    import paged_kv_cache_280_gb300 as pa
+
+    with pytest.raises(pa.PAError):
+        pa.pa_debug_set_wait_limit_ns(3_000_000_000)
+    pa.pa_debug_set_wait_limit_ns(0)

@@ -22,7 +22,9 @@ def test_reference_arm_json_line():
     sys.path.insert(0, ROOT)
     import bench
 
-    d = _run("--steps", "1", "--warmup", "3", "--ref-seqs-per-step", "2")
+    # the headline workload is the largest one; the line for a smaller one has the same form
+    assert bench.DEFAULT_WORKLOAD == "mha_b256_append" and bench.DEFAULT_WORKLOAD in bench.PER_CONFIG
+    d = _run("--workload", "gqa4_b64", "--steps", "1", "--warmup", "3", "--ref-seqs-per-step", "2")
     for key in ("impl", "metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step", "higher_is_better",
                 "scaling", "vs_baseline", "dtype", "data", "config", "cpu_baseline", "e2e"):
         assert key in d, key
