@@ -57,19 +57,43 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
     return done != 0;
 }
 
+// Non-blocking test of the same phase.
+__device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
+    uint32_t done;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(done)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return done != 0;
+}
+
+// Limits below this are a testing aid (pa_debug_set_wait_limit_ns): they are
+// timed on the SM clock with non-blocking polls, since one try_wait may
+// suspend the thread for longer than the whole limit.
+constexpr uint64_t kShortWaitNs = 1000000;  // 1 ms
+
 // Wait for the phase of `bar` with the given parity to complete.  Returns
 // false if it did not within limit_ns (the caller then flags and aborts), or,
 // when abort_flag is given, once another warp of the CTA has set it.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint64_t limit_ns = kWaitLimitNs,
                                           volatile int32_t* abort_flag = nullptr) {
+    if (limit_ns < kShortWaitNs) {  // never suspend: one try_wait could outlast the limit
+        const long long c0 = clock64(), lim = 2 * (long long)limit_ns;  // about 2 SM cycles per ns
+        for (;;) {
+            if (mbar_test_wait(bar, parity)) return true;
+            if (abort_flag && *abort_flag) return false;
+            if (clock64() - c0 >= lim) return false;
+        }
+    }
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = global_timer_ns();
-    for (uint32_t it = 1;; ++it) {
-        if (mbar_try_wait(bar, parity)) return true;
-        if ((it & 63u) == 0) {
-            if (abort_flag && *abort_flag) return false;
-            if (global_timer_ns() - t0 > limit_ns) return false;
-        }
+    for (;;) {
+        if (mbar_try_wait(bar, parity)) return true;  // try_wait itself suspends the thread a while
+        if (abort_flag && *abort_flag) return false;
+        if (global_timer_ns() - t0 >= limit_ns) return false;
     }
 }
 

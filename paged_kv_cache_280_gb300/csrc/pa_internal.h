@@ -125,7 +125,7 @@ struct PrefillParams {
     int32_t num_kv_heads;
     int32_t num_blocks;
     int32_t group;          // G = num_q_heads / num_kv_heads
-    int32_t tile_tokens;    // chunk tokens per 64-row query tile: 64 / G
+    int32_t tile_tokens;    // chunk tokens per 128-row query tile: 128 / G (rounded down)
     int32_t num_q_tokens;   // rows of q and out
     int32_t max_q_len;      // bound on every chunk (the grid is sized by it)
     float scale_log2;
