@@ -877,7 +877,7 @@ def run_prefill(args, rank, world, local_rank):
                    "num_q_heads": Hq, "num_kv_heads": Hkv, "head_dim": D, "block_size": bs,
                    "flops_per_step": flops, "l2": "flushed between timed steps (512 MiB write, then a 256 MiB read)",
                    "prefill_ms_median": statistics.median(pf_ms), "prefill_ms_min": min(pf_ms),
-                   "path": "mma.sync m16n8k16, TMA ring"},
+                   "path": "tcgen05.mma (TMEM accumulators, P in TMEM), TMA ring"},
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
                      "peak_source": peak_kind, "kernel": "pa_prefill_attention (prefill_kernel)", "traffic": None},
         "e2e": {"value": e2e_value, "unit": PREFILL_UNIT, "h2d_bytes_per_step": pos,

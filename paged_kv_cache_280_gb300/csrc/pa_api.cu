@@ -102,6 +102,49 @@ bool pool_map(CUtensorMap* map, int dev, const void* pool, int64_t rows, int hea
     return true;
 }
 
+// Query rows of a prefill tile: q [tokens][heads][head_dim] bf16 as a 3-D tensor
+// (head_dim, heads, tokens); one box = 64 elements (128 bytes, 128-byte swizzle)
+// x box_heads heads x box_tokens tokens, i.e. box_heads * box_tokens rows of 128
+// bytes in token-major order.  Out-of-range tokens read as zero.  Cached per
+// (device, q, shape) like the pool maps.
+struct QMapEntry {
+    int dev;
+    const void* q;
+    int64_t tokens;
+    int heads, head_dim, box_heads, box_tokens;
+    CUtensorMap map;
+};
+static QMapEntry g_qmaps[kPoolMapCache];
+static int g_qmaps_used = 0, g_qmaps_next = 0;
+
+bool prefill_q_map(CUtensorMap* map, int dev, const void* q, int64_t tokens, int heads, int head_dim, int box_heads,
+                   int box_tokens) {
+    std::lock_guard<std::mutex> lk(g_mu);
+    for (int i = 0; i < g_qmaps_used; ++i) {
+        const QMapEntry& e = g_qmaps[i];
+        if (e.dev == dev && e.q == q && e.tokens == tokens && e.heads == heads && e.head_dim == head_dim &&
+            e.box_heads == box_heads && e.box_tokens == box_tokens) {
+            *map = e.map;
+            return true;
+        }
+    }
+    auto enc = tensor_map_encoder();
+    if (!enc) return false;
+    cuuint64_t dims[3] = {(cuuint64_t)head_dim, (cuuint64_t)heads, (cuuint64_t)tokens};
+    cuuint64_t strides[2] = {(cuuint64_t)head_dim * 2, (cuuint64_t)heads * head_dim * 2};
+    cuuint32_t box[3] = {64u, (cuuint32_t)box_heads, (cuuint32_t)box_tokens};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(q), dims, strides, box, estr,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return false;
+    QMapEntry& e = g_qmaps[g_qmaps_next];
+    e = QMapEntry{dev, q, tokens, heads, head_dim, box_heads, box_tokens, *map};
+    g_qmaps_next = (g_qmaps_next + 1) % kPoolMapCache;
+    if (g_qmaps_used < kPoolMapCache) ++g_qmaps_used;
+    return true;
+}
+
 // Dynamic shared memory opted into, and the occupancy found, per (device,
 // kernel, shared-memory size): set and queried once instead of every call.
 struct KernelEntry {

@@ -108,6 +108,11 @@ pa_status decode_common(void* out, const void* q, const void* k_pool, const void
 // rows, one box = block_size rows x 128 bytes with the 128-byte swizzle;
 // cached per (device, pool, shape).
 bool pool_map(CUtensorMap* map, int dev, const void* pool, int64_t rows, int head_dim, int block_size, pa_dtype dt);
+// The TMA map of prefill query rows: q [tokens][heads][head_dim] bf16 viewed as
+// (head_dim, heads, tokens), one box = 64 elements x box_heads x box_tokens with
+// the 128-byte swizzle; cached per (device, q, shape).
+bool prefill_q_map(CUtensorMap* map, int dev, const void* q, int64_t tokens, int heads, int head_dim, int box_heads,
+                   int box_tokens);
 // Opts the kernel into `smem` bytes of dynamic shared memory and returns its
 // CTAs per SM; cached per (device, kernel, smem).
 bool kernel_occupancy(int dev, const void* kernel, int threads, int smem, int* occ);
@@ -121,6 +126,7 @@ struct PrefillParams {
     const int32_t* cu_q_lens;
     int32_t* status;
     int32_t max_blocks_per_seq;
+    int32_t num_seqs;
     int32_t num_q_heads;
     int32_t num_kv_heads;
     int32_t num_blocks;

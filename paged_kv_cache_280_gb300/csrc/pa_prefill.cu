@@ -10,31 +10,35 @@
 // + i) attends to the keys at positions 0..p:  out = softmax(scale q K^T) V.
 //
 // Work decomposition.  For one (sequence, KV head) the G query heads of each
-// chunk token are stacked into rows (token-major), and a CTA takes a tile of
-// 128 rows (128 / G chunk tokens): the M of every MMA, one row per TMEM lane.
-// All rows of a tile share each K/V stage, so S = Q K^T and O = P V are dense
-// 128-row contractions.  Tiles that end later in the chunk see more keys; the
-// grid hands them out first.  Two CTAs share an SM, so one's softmax overlaps
-// the other's MMAs.
+// chunk token are stacked into rows (token-major); a tile is 128 rows
+// (128 / G chunk tokens): the M of every MMA, one row per TMEM lane.  A work
+// unit is two consecutive tiles of one (sequence, KV head), which share every
+// K/V stage of 128 keys.  The grid is persistent (one CTA per SM) and walks
+// the units from the latest tiles (the most keys) to the earliest.
 //
-// CTA: six warps.
-//   - Producer (warp 4): walks the block table and moves 64 keys of K and V per
-//     stage with TMA (cp.async.bulk.tensor, 128-byte swizzle, evict-last L2
-//     policy: the segment's other tiles read the same blocks) into a 2-stage
-//     ring guarded by full / empty mbarriers.
-//   - MMA (warp 5, one thread): S_j = Q K_j^T into one of two TMEM buffers
-//     (M 128, N 64, K = head_dim), issued one stage ahead of the softmax; then
-//     O += P_j V_j (M 128, N = head_dim, K 64) with P_j from shared memory and
-//     V_j an MN-major operand.  Completion is signalled by tcgen05.commit.
-//   - Softmax (warps 0-3, one thread per query row): loads the tile's Q rows
-//     into the swizzled layout once; per stage reads its S row from TMEM,
-//     applies the causal mask and scale, keeps a running max and sum in the
-//     base-2 domain, and writes its row of P (bf16) over the stage's K, which
-//     S_j has finished reading.  O is rescaled in TMEM only when a row's max
-//     grows by more than 2^8 (the weights stay <= 256, exact in the final
-//     ratio); the final O / l is written from TMEM.  On the stage that holds
-//     the tile's last position it zeroes the V rows past it: their slots may
-//     hold any bits, and zero weight times NaN is NaN.
+// CTA: ten warps.
+//   - Producer (warp 8): per unit, both tiles' query rows by TMA (a 3-D box of
+//     64 elements x G heads x 128 / G tokens), then per stage K and V, each
+//     into its own slot of a 5-slot ring (one box of BS rows x 128 bytes per
+//     block and 64-element panel, 128-byte swizzle, evict-last L2 policy: the
+//     segment's other units read the same blocks).  A block past the unit's
+//     last one is loaded from past the pool's end, which TMA fills with zeros.
+//   - MMA (warp 9, one thread): S_t = Q_t K^T into tile t's TMEM (M 128, N 128,
+//     K = head_dim, both operands K-major in shared memory), and O_t += P_t V
+//     with P_t read from TMEM, where the softmax wrote it over S_t, and V an
+//     MN-major operand.  Per stage it issues tile 0's P V and next S, then tile
+//     1's, so the tensor core works on one tile while the other's softmax runs.
+//     The tensor core performs one CTA's MMAs in issue order, so the S that
+//     overwrites P is issued right after the P V that reads it.
+//   - Softmax (warps 4t .. 4t + 3 for tile t, one thread per query row): reads
+//     its S row from TMEM, applies the causal mask, keeps the row's running
+//     max and sum with the scale folded into one fma per weight (base 2),
+//     writes its row of P (bf16) back to TMEM, and, when the row max has grown
+//     by more than 2^8 since O was last scaled, rescales its O row in TMEM
+//     (the weights stay <= 256; the final ratio is exact).  The final O / l is
+//     written from TMEM.  When a unit ends at the sequence's last token inside
+//     a partial block, the last tile's warps zero the V rows of the unfilled
+//     slots: they may hold any bits, and zero weight times NaN is NaN.
 // Every wait is bounded; a timeout sets PA_DEV_WAIT_TIMEOUT, every role stops,
 // and the CTA waits for its own copies and MMAs before freeing TMEM.
 #include <cmath>
@@ -46,16 +50,16 @@
 namespace pa {
 namespace {
 
-constexpr int kPfSoftmaxWarps = 4;
-constexpr int kPfProducer = 4;  // warp index
-constexpr int kPfMma = 5;       // warp index
-constexpr int kPfThreads = 192;
-constexpr int kPfRows = 128;    // query rows per CTA = MMA M = TMEM lanes
-constexpr int kPfKeys = 64;     // keys per stage: N of S, K of P V
-constexpr int kPfStages = 2;
-constexpr int kPfCtasPerSm = 2;
-constexpr uint32_t kPfTmemCols = 256;  // O in columns [0, D), S buffer i in [128 + 64 i, 192 + 64 i)
-constexpr uint32_t kPfTmemS = 128;
+constexpr int kPfTiles = 2;         // query tiles per work unit
+constexpr int kPfSoftmaxWarps = 4;  // per tile
+constexpr int kPfProducer = 8;      // warp index
+constexpr int kPfMma = 9;           // warp index
+constexpr int kPfThreads = 320;
+constexpr int kPfRows = 128;        // query rows per tile = MMA M = TMEM lanes
+constexpr int kPfKeys = 128;        // keys per stage: N of S, K of P V
+constexpr uint32_t kPfTmemCols = 512;  // tile t: S (P over its first 64 columns) in 256 t + [0, 128), O in 256 t + 128 + [0, D)
+constexpr uint32_t kPfTmemTile = 256;
+constexpr uint32_t kPfTmemO = 128;
 constexpr float kPfRescaleLog2 = 8.f;  // rescale O only when a row max grows by more than this (log2)
 
 __device__ __forceinline__ uint64_t policy_evict_last() {
@@ -72,47 +76,39 @@ __device__ __forceinline__ float fast_exp2(float x) {
 }
 
 // Shared memory of one CTA (1024-byte aligned regions, 128-byte swizzle):
-//   Q      [D / 64 panels][128 rows][128 B]
-//   stage  K|P: K as [D / 64 panels][64 keys][128 B], later P as [128 rows][128 B]
-//          V:   [D / 64 panels][64 keys][128 B]
+//   Q[t]     [D / 64 panels][128 rows][128 B]
+//   slot[i]  K or V of one stage: [D / 64 panels][128 keys][128 B]
 template <int D, int BS>
 struct PfLayout {
     static constexpr int kPanels = D / 64;
     static constexpr int kQPanel = kPfRows * 128;
-    static constexpr int kKVPanel = kPfKeys * 128;
     static constexpr int kQBytes = kPanels * kQPanel;
-    static constexpr int kKBytes = kPanels * kKVPanel;
-    static constexpr int kPBytes = kPfRows * kPfKeys * 2;
-    static constexpr int kKPBytes = kKBytes > kPBytes ? kKBytes : kPBytes;
-    static constexpr int kVBytes = kPanels * kKVPanel;
-    static constexpr int kStageBytes = kKPBytes + kVBytes;
+    static constexpr int kSlotPanel = kPfKeys * 128;
+    static constexpr int kSlotBytes = kPanels * kSlotPanel;
+    static constexpr int kSlots = D == 128 ? 5 : 8;
     static constexpr int kBlocksPerStage = kPfKeys / BS;
     static constexpr int kQOff = 0;
-    static constexpr int kRingOff = kQBytes;
-    static constexpr int kBarOff = kRingOff + kPfStages * kStageBytes;
-    // mbarriers: kv_full[2], kv_empty[2], s_full[2], s_free[2], p_ready[2], o_done, o_final, q_ready, mma_drain
-    static constexpr int kNumBars = 5 * kPfStages + 4;
+    static constexpr int kRingOff = kPfTiles * kQBytes;
+    static constexpr int kBarOff = kRingOff + kSlots * kSlotBytes;
+    static constexpr int kNumBars = 2 * kSlots + 3 * kPfTiles + 3;
     static constexpr int kMiscOff = kBarOff + kNumBars * 8;  // abort flag, TMEM address
-    static constexpr int kUsed = kMiscOff + 64 + 1024;       // +1 KB to align the base
-    // at least a third of the SM's shared memory, so that no third CTA (and no TMEM request
-    // beyond the SM's 512 columns) lands on an SM
-    static constexpr int kBytes = kUsed > 80 * 1024 ? kUsed : 80 * 1024;
-    static_assert(kQPanel % 1024 == 0 && kKVPanel % 1024 == 0 && kStageBytes % 1024 == 0, "1024-byte alignment");
+    static constexpr int kBytes = kMiscOff + 64 + 1024;      // +1 KB to align the base
+    static_assert(kQPanel % 1024 == 0 && kSlotPanel % 1024 == 0, "1024-byte alignment");
+    static_assert(kBytes <= 227 * 1024, "shared memory");
 };
 
+template <int NS>
 struct PfBars {
     uint32_t base;
-    __device__ uint32_t kv_full(int s) const { return base + 8u * s; }
-    __device__ uint32_t kv_empty(int s) const { return base + 8u * (kPfStages + s); }
-    __device__ uint32_t s_full(int s) const { return base + 8u * (2 * kPfStages + s); }
-    __device__ uint32_t s_free(int s) const { return base + 8u * (3 * kPfStages + s); }
-    __device__ uint32_t p_ready(int s) const { return base + 8u * (4 * kPfStages + s); }
-    // phase k completes with P_k V_k
-    __device__ uint32_t o_done() const { return base + 8u * (5 * kPfStages); }
-    // its one phase completes with the last P V
-    __device__ uint32_t o_final() const { return base + 8u * (5 * kPfStages + 1); }
-    __device__ uint32_t q_ready() const { return base + 8u * (5 * kPfStages + 2); }
-    __device__ uint32_t mma_drain() const { return base + 8u * (5 * kPfStages + 3); }
+    __device__ uint32_t at(int i) const { return base + 8u * i; }
+    __device__ uint32_t slot_full(int s) const { return at(s); }
+    __device__ uint32_t slot_empty(int s) const { return at(NS + s); }
+    __device__ uint32_t s_full(int t) const { return at(2 * NS + t); }    // S_t in TMEM
+    __device__ uint32_t p_ready(int t) const { return at(2 * NS + kPfTiles + t); }  // P_t in TMEM, O_t rescaled
+    __device__ uint32_t o_final(int t) const { return at(2 * NS + 2 * kPfTiles + t); }  // a unit's last P V
+    __device__ uint32_t q_full() const { return at(2 * NS + 3 * kPfTiles); }
+    __device__ uint32_t q_empty() const { return at(2 * NS + 3 * kPfTiles + 1); }
+    __device__ uint32_t mma_drain() const { return at(2 * NS + 3 * kPfTiles + 2); }
 };
 
 // Warp-collective bounded wait (every lane calls it); gives up once the CTA's abort flag is set.
@@ -136,304 +132,378 @@ __device__ __forceinline__ bool pf_wait1(uint32_t bar, uint32_t parity, volatile
     return false;
 }
 
-// Producer warp: stage k holds keys [64 k, 64 k + 64): the segment's blocks 64 k / BS .. of K and
-// V, each block as D / 64 boxes of BS rows x 128 bytes.  Blocks past the last needed one are not
-// loaded (the stage's byte count follows); their rows lie past every query's position.
+// One work unit: tiles 2m and 2m + 1 of (sequence b, KV head g).  Every role
+// walks the same units in the same order and derives the same fields.
+struct PfUnit {
+    int b, g, c0, n, len;
+    int i0[kPfTiles], i1[kPfTiles];
+    int ntiles;      // 1 or 2 (the chunk's last unit may hold one tile)
+    int nkeys;       // keys up to the unit's last position
+    int nst;         // 128-key stages
+    int nblk;        // blocks
+    bool zero_tail;  // the unit ends at the sequence's last token inside a partial block
+};
+
+// 0: empty unit (skipped by every role); 1: a unit to compute; -1: a malformed
+// sequence (flagged once, skipped).
+template <int BS>
+__device__ __forceinline__ int pf_unit(const PrefillParams& p, int u, int pairs, PfUnit& w) {
+    const int bh = p.num_seqs * p.num_kv_heads;
+    const int m = pairs - 1 - u / bh, rem = u - (u / bh) * bh;
+    w.b = rem / p.num_kv_heads;
+    w.g = rem - w.b * p.num_kv_heads;
+    w.c0 = __ldg(p.cu_q_lens + w.b);
+    w.n = __ldg(p.cu_q_lens + w.b + 1) - w.c0;
+    w.len = __ldg(p.seq_lens + w.b);
+    const int tt = p.tile_tokens;
+    w.i0[0] = 2 * m * tt;
+    if (w.n <= 0 || w.i0[0] >= w.n) return 0;
+    if (w.n > w.len || w.n > p.max_q_len || (int64_t)w.len > (int64_t)p.max_blocks_per_seq * BS || w.c0 < 0 ||
+        (int64_t)w.c0 + w.n > p.num_q_tokens)
+        return -1;
+    w.i1[0] = min(w.n, w.i0[0] + tt);
+    w.i0[1] = w.i0[0] + tt;
+    w.i1[1] = min(w.n, w.i0[1] + tt);
+    w.ntiles = w.i0[1] < w.n ? 2 : 1;
+    w.nkeys = w.len - w.n + (w.ntiles == 2 ? w.i1[1] : w.i1[0]);
+    w.nst = (w.nkeys + kPfKeys - 1) / kPfKeys;
+    w.nblk = (w.nkeys + BS - 1) / BS;
+    w.zero_tail = w.nkeys == w.len && (w.len % BS) != 0;
+    return 1;
+}
+
+// Producer warp: per unit, Q of both tiles, then K(0), V(0), K(1), V(1), ... through the slot ring.
 template <int D, int BS>
-__device__ __forceinline__ void pf_produce(const PrefillParams& p, const CUtensorMap* tk, const CUtensorMap* tv, int b,
-                                           int g, int nblk, int nst, uint32_t ring_s, const PfBars& bars,
-                                           volatile int32_t* abort_flag, int lane) {
+__device__ __forceinline__ void pf_produce(const PrefillParams& p, const CUtensorMap* tk, const CUtensorMap* tv,
+                                           const CUtensorMap* tq, int pairs, int total, uint32_t base_s,
+                                           const PfBars<PfLayout<D, BS>::kSlots>& bars, volatile int32_t* abort_flag,
+                                           int lane) {
     using L = PfLayout<D, BS>;
-    constexpr int BPS = L::kBlocksPerStage;
+    constexpr int BPS = L::kBlocksPerStage, NS = L::kSlots;
     if (lane == 0) {
         prefetch_tensormap(tk);
         prefetch_tensormap(tv);
+        prefetch_tensormap(tq);
     }
     const uint64_t policy = policy_evict_last();
-    const int32_t* tab = p.block_tables + (size_t)b * p.max_blocks_per_seq;
-    int issued = 0;
-    int32_t blk = 0;
-    for (int k = 0; k < nst; ++k) {
-        const int jb0 = k * BPS;  // first block of the stage
-        if ((jb0 & 31) == 0) blk = jb0 + lane < nblk ? __ldg(tab + jb0 + lane) : 0;  // 32 table entries at a time
-        const int s = k % kPfStages;
-        if (!pf_wait(bars.kv_empty(s), ((k / kPfStages) & 1) ^ 1, abort_flag, p.status)) break;
-        const int nb = min(BPS, nblk - jb0);
-        int32_t bids[BPS];
-#pragma unroll
-        for (int t = 0; t < BPS; ++t) {
-            int32_t bid = __shfl_sync(0xffffffffu, blk, (jb0 + t) & 31);
-            if (t < nb && (bid < 0 || bid >= p.num_blocks)) {  // warp-uniform
-                if (lane == 0) flag_status(p.status, PA_DEV_BAD_BLOCK_ID);
-                bid = 0;
-            }
-            bids[t] = bid;
-        }
+    const int32_t oob_row = p.num_blocks * p.num_kv_heads * BS;  // past the pool: TMA reads zeros
+    const int G = p.group;
+    const uint32_t q_tile_bytes = (uint32_t)(L::kPanels * G * p.tile_tokens * 128);
+    int sc = 0, uc = 0;
+    bool ok = true;
+    for (int u = blockIdx.x; ok && u < total; u += gridDim.x) {
+        PfUnit w;
+        const int kind = pf_unit<BS>(p, u, pairs, w);
+        if (kind < 0 && lane == 0 && w.g == 0) flag_status(p.status, PA_DEV_BAD_SEQ_LEN);
+        if (kind <= 0) continue;
+        // query rows of both tiles, once the previous unit's Q K^T have completed
+        if (!pf_wait(bars.q_empty(), (uc & 1) ^ 1, abort_flag, p.status)) break;
         if (lane == 0) {
-            mbar_arrive_expect_tx(bars.kv_full(s), (uint32_t)(nb * BS * 128 * L::kPanels * 2));
-            const uint32_t kdst = ring_s + s * L::kStageBytes, vdst = kdst + L::kKPBytes;
+            mbar_arrive_expect_tx(bars.q_full(), q_tile_bytes * w.ntiles);
+#pragma unroll
+            for (int t = 0; t < kPfTiles; ++t)
+                if (t < w.ntiles)
+#pragma unroll
+                    for (int pn = 0; pn < L::kPanels; ++pn)
+                        tma_load_3d(base_s + L::kQOff + t * L::kQBytes + pn * L::kQPanel, tq, pn * 64, w.g * G,
+                                    w.c0 + w.i0[t], bars.q_full());
+        }
+        ++uc;
+        const int32_t* tab = p.block_tables + (size_t)w.b * p.max_blocks_per_seq;
+        int32_t blk = 0;
+        for (int k = 0; ok && k < w.nst; ++k) {
+            const int jb0 = k * BPS;
+            if ((jb0 & 31) == 0) blk = jb0 + lane < w.nblk ? __ldg(tab + jb0 + lane) : 0;  // 32 entries at a time
+            int32_t rows[BPS];
 #pragma unroll
             for (int t = 0; t < BPS; ++t) {
-                if (t < nb) {
-                    const int32_t y = (bids[t] * p.num_kv_heads + g) * BS;
-#pragma unroll
-                    for (int pn = 0; pn < L::kPanels; ++pn) {
-                        const uint32_t off = pn * L::kKVPanel + t * BS * 128;
-                        tma_load_2d(kdst + off, tk, pn * 64, y, bars.kv_full(s), policy);
-                        tma_load_2d(vdst + off, tv, pn * 64, y, bars.kv_full(s), policy);
+                int32_t bid = __shfl_sync(0xffffffffu, blk, (jb0 + t) & 31);
+                if (jb0 + t >= w.nblk) {
+                    rows[t] = oob_row;
+                } else {
+                    if (bid < 0 || bid >= p.num_blocks) {  // warp-uniform
+                        if (lane == 0) flag_status(p.status, PA_DEV_BAD_BLOCK_ID);
+                        bid = 0;
                     }
+                    rows[t] = (bid * p.num_kv_heads + w.g) * BS;
+                }
+            }
+#pragma unroll
+            for (int half = 0; half < 2; ++half, ++sc) {  // K, then V
+                const int s = sc % NS;
+                if (!pf_wait(bars.slot_empty(s), ((sc / NS) & 1) ^ 1, abort_flag, p.status)) {
+                    ok = false;
+                    break;
+                }
+                if (lane == 0) {
+                    mbar_arrive_expect_tx(bars.slot_full(s), (uint32_t)L::kSlotBytes);
+                    const uint32_t dst = base_s + L::kRingOff + s * L::kSlotBytes;
+                    const CUtensorMap* map = half ? tv : tk;
+#pragma unroll
+                    for (int t = 0; t < BPS; ++t)
+#pragma unroll
+                        for (int pn = 0; pn < L::kPanels; ++pn)
+                            tma_load_2d(dst + pn * L::kSlotPanel + t * BS * 128, map, pn * 64, rows[t], bars.slot_full(s),
+                                        policy);
                 }
             }
         }
-        issued = k + 1;
     }
-    // never leave the CTA with copies still landing in its shared memory
-    for (int kk = issued > kPfStages ? issued - kPfStages : 0; kk < issued; ++kk)
-        mbar_wait(bars.kv_full(kk % kPfStages), (kk / kPfStages) & 1);
+    // never leave the CTA with copies still landing in its shared memory (a slot's phase completes
+    // only when its copies have landed)
+    for (int kk = sc > NS ? sc - NS : 0; kk < sc; ++kk) mbar_wait(bars.slot_full(kk % NS), (kk / NS) & 1);
+    if (uc > 0) mbar_wait(bars.q_full(), (uc - 1) & 1);
 }
 
-// MMA issuer (one thread).  S_{k+1} is issued before waiting for P_k, so the tensor core computes
-// the next scores while the softmax works on this stage.
+// MMA issuer (one thread).
 template <int D, int BS>
-__device__ __forceinline__ void pf_mma(const PrefillParams& p, int nst, uint32_t q_s, uint32_t ring_s, uint32_t tmem,
-                                       const PfBars& bars, volatile int32_t* abort_flag) {
+__device__ __forceinline__ void pf_mma(const PrefillParams& p, int pairs, int total, uint32_t base_s, uint32_t tmem,
+                                       const PfBars<PfLayout<D, BS>::kSlots>& bars, volatile int32_t* abort_flag) {
     using L = PfLayout<D, BS>;
+    constexpr int NS = L::kSlots;
     constexpr uint32_t idesc_s = umma_idesc_bf16(kPfRows, kPfKeys, 0, 0);  // Q (K-major) x K^T (K-major)
-    constexpr uint32_t idesc_o = umma_idesc_bf16(kPfRows, D, 0, 1);         // P (K-major) x V (MN-major)
-    auto issue_s = [&](int k) {
-        const int s = k % kPfStages;
-        const uint32_t kst = ring_s + s * L::kStageBytes;
+    constexpr uint32_t idesc_o = umma_idesc_bf16(kPfRows, D, 0, 1);         // P (TMEM) x V (MN-major)
+    int sc = 0, uc = 0, ck0 = 0, ck1 = 0;  // slots; units; stages of tile 0 and of tile 1
+    bool ok = true;
+    auto slot_addr = [&](int s) { return base_s + L::kRingOff + s * L::kSlotBytes; };
+    auto issue_s = [&](int t, int ks_slot) {
+        const uint32_t q = base_s + L::kQOff + t * L::kQBytes, kst = slot_addr(ks_slot);
 #pragma unroll
         for (int ks = 0; ks < D / 16; ++ks) {
-            const uint64_t a = umma_smem_desc(q_s + (ks >> 2) * L::kQPanel + (ks & 3) * 32, 16, 1024);
-            const uint64_t bd = umma_smem_desc(kst + (ks >> 2) * L::kKVPanel + (ks & 3) * 32, 16, 1024);
-            umma_bf16(tmem + kPfTmemS + kPfKeys * s, a, bd, idesc_s, ks > 0);
+            const uint64_t a = umma_smem_desc(q + (ks >> 2) * L::kQPanel + (ks & 3) * 32, 16, 1024);
+            const uint64_t bd = umma_smem_desc(kst + (ks >> 2) * L::kSlotPanel + (ks & 3) * 32, 16, 1024);
+            umma_bf16(tmem + kPfTmemTile * t, a, bd, idesc_s, ks > 0);
         }
-        umma_commit(bars.s_full(s));
+        umma_commit(bars.s_full(t));
     };
-    bool ok = pf_wait1(bars.q_ready(), 0, abort_flag, p.status) &&
-              pf_wait1(bars.kv_full(0), 0, abort_flag, p.status);
-    if (ok) {
-        tc_fence_after();
-        issue_s(0);
-    }
-    for (int k = 0; ok && k < nst; ++k) {
-        if (k + 1 < nst) {
-            const int s1 = (k + 1) % kPfStages, ph = ((k + 1) / kPfStages) & 1;
-            ok = pf_wait1(bars.kv_full(s1), ph, abort_flag, p.status) &&
-                 pf_wait1(bars.s_free(s1), ph ^ 1, abort_flag, p.status);
-            if (!ok) break;
-            tc_fence_after();
-            issue_s(k + 1);
-        }
-        const int s = k % kPfStages;
-        if (!pf_wait1(bars.p_ready(s), (k / kPfStages) & 1, abort_flag, p.status)) break;
-        tc_fence_after();
-        const uint32_t pst = ring_s + s * L::kStageBytes, vst = pst + L::kKPBytes;
+    auto issue_o = [&](int t, int vs_slot, bool first) {
+        const uint32_t vst = slot_addr(vs_slot);
 #pragma unroll
         for (int kk = 0; kk < kPfKeys / 16; ++kk) {
-            const uint64_t a = umma_smem_desc(pst + kk * 32, 16, 1024);
-            const uint64_t bd = umma_smem_desc(vst + kk * 16 * 128, L::kKVPanel, 1024);
-            umma_bf16(tmem, a, bd, idesc_o, (k > 0 || kk > 0) ? 1u : 0u);
+            const uint64_t bd = umma_smem_desc(vst + kk * 16 * 128, L::kSlotPanel, 1024);
+            umma_bf16_tmem_a(tmem + kPfTmemTile * t + kPfTmemO, tmem + kPfTmemTile * t + kk * 8, bd, idesc_o,
+                             (!first || kk > 0) ? 1u : 0u);
         }
-        umma_commit(bars.kv_empty(s));  // the stage may be refilled
-        umma_commit(bars.o_done());
-        if (k == nst - 1) umma_commit(bars.o_final());
+    };
+    for (int u = blockIdx.x; ok && u < total; u += gridDim.x) {
+        PfUnit w;
+        if (pf_unit<BS>(p, u, pairs, w) <= 0) continue;
+        const int T = w.ntiles;
+        // S_t(0) for every tile of the unit
+        const int k0 = sc++;
+        ok = pf_wait1(bars.q_full(), uc & 1, abort_flag, p.status) &&
+             pf_wait1(bars.slot_full(k0 % NS), (k0 / NS) & 1, abort_flag, p.status);
+        if (!ok) break;
+        tc_fence_after();
+        for (int t = 0; t < T; ++t) issue_s(t, k0 % NS);
+        umma_commit(bars.slot_empty(k0 % NS));
+        if (w.nst == 1) umma_commit(bars.q_empty());  // the unit's last Q K^T
+        for (int k = 0; k < w.nst; ++k) {
+            const bool last = k + 1 == w.nst;
+            const int vs = sc++;
+            const int ks1 = last ? -1 : sc++;
+            if (!pf_wait1(bars.slot_full(vs % NS), (vs / NS) & 1, abort_flag, p.status)) {
+                ok = false;
+                break;
+            }
+            // On the unit's last stage the last tile's warps may zero V rows: every tile waits for them.
+            const bool all = last && w.zero_tail;
+            for (int t = 0; ok && all && t < T; ++t) ok = pf_wait1(bars.p_ready(t), (t ? ck1 : ck0) & 1, abort_flag, p.status);
+            for (int t = 0; ok && t < T; ++t) {
+                int& ck = t ? ck1 : ck0;
+                if (!all && !pf_wait1(bars.p_ready(t), ck & 1, abort_flag, p.status)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                issue_o(t, vs % NS, k == 0);
+                if (last) {
+                    umma_commit(bars.o_final(t));
+                } else {
+                    if (t == 0 && !pf_wait1(bars.slot_full(ks1 % NS), (ks1 / NS) & 1, abort_flag, p.status)) {
+                        ok = false;
+                        break;
+                    }
+                    issue_s(t, ks1 % NS);
+                }
+                ++ck;
+            }
+            if (!ok) break;
+            umma_commit(bars.slot_empty(vs % NS));  // V(k) may be refilled once both P V complete
+            if (!last) {
+                umma_commit(bars.slot_empty(ks1 % NS));
+                if (k + 2 == w.nst) umma_commit(bars.q_empty());  // the unit's last Q K^T were just issued
+            }
+        }
+        ++uc;
     }
     // every MMA issued has completed before the CTA may free TMEM or its shared memory
     umma_commit(bars.mma_drain());
     mbar_wait(bars.mma_drain(), 0);
 }
 
-// Softmax warp w (0..3): query row r = 32 w + lane of the tile, TMEM lane r.
+// Softmax warps of tile t: query row r = 32 (warp % 4) + lane, TMEM lane r.
 template <int D, int BS>
-__device__ __forceinline__ void pf_softmax(const PrefillParams& p, int b, int g, int c0, int n, int len, int i0, int i1,
-                                           int nst, uint8_t* base, uint32_t base_s, uint32_t tmem, const PfBars& bars,
+__device__ __forceinline__ void pf_softmax(const PrefillParams& p, int pairs, int total, int t, uint8_t* base,
+                                           uint32_t tmem, const PfBars<PfLayout<D, BS>::kSlots>& bars,
                                            volatile int32_t* abort_flag, int warp, int lane) {
     using L = PfLayout<D, BS>;
+    constexpr int NS = L::kSlots;
     const int G = p.group, Hq = p.num_q_heads;
     const int rows_used = p.tile_tokens * G;
-    const int r = 32 * warp + lane;
-    const int tok = i0 + r / G;
-    const bool valid = r < rows_used && tok < i1;
-    const int pos_last = len - n + i1 - 1;
-    // padding rows take the tile's last position: their scores stay finite and they are never stored
-    const int pos = valid ? len - n + tok : pos_last;
-    const int nkeys = pos_last + 1;
-    const uint32_t lane_tmem = tmem + ((uint32_t)(32 * warp) << 16);
-
-    // ---- Q row r into the swizzled K-major tile ----
-    {
-        const size_t qrow = ((size_t)(c0 + (valid ? tok : i0)) * Hq + (size_t)g * G + r % G) * D;
-        const uint4* src = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(p.q) + qrow);
+    const int r = 32 * (warp & 3) + lane;
+    const uint32_t row_tmem = tmem + ((uint32_t)(32 * (warp & 3)) << 16) + kPfTmemTile * t;
+    const float c = p.scale_log2;  // > 0 (checked on the host)
+    int sc = 0, ck = 0, uc = 0;
+    for (int u = blockIdx.x; u < total; u += gridDim.x) {
+        PfUnit w;
+        if (pf_unit<BS>(p, u, pairs, w) <= 0) continue;
+        const int sc0 = sc;
+        sc += 2 * w.nst;
+        if (t >= w.ntiles) continue;
+        const int i0 = t ? w.i0[1] : w.i0[0], i1 = t ? w.i1[1] : w.i1[0];
+        const int tok = i0 + r / G;
+        const bool valid = r < rows_used && tok < i1;
+        // padding rows take the tile's last position: their scores stay finite and they are never stored
+        const int pos = w.len - w.n + (valid ? tok : i1 - 1);
+        float m_raw = -INFINITY, l_run = 0.f;  // running max of the raw scores (the scale is > 0), and sum
+        for (int k = 0; k < w.nst; ++k, ++ck) {
+            if (!pf_wait(bars.s_full(t), ck & 1, abort_flag, p.status)) return;
+            tc_fence_after();
+            // S_t(k) was issued after P_t(k-1) V(k-1) and completes after it: O is up to date and
+            // no MMA touches this tile's TMEM until this warp arrives on p_ready.
+            // pass 1: the row max over the stage's 128 scores, 32 at a time (causal mask: key j is
+            // visible to the row at position pos iff j <= pos)
+            const int key0 = k * kPfKeys;
+            const bool diag = key0 + kPfKeys - 1 > pos;
+            float mx = -INFINITY;
+#pragma unroll 1
+            for (int q = 0; q < kPfKeys / 32; ++q) {
+                uint32_t sv[32];
+                tmem_ld32(row_tmem + 32 * q, sv);
+                tmem_wait_ld();
 #pragma unroll
-        for (int c = 0; c < D / 8; ++c) {
-            const uint4 v = valid ? __ldg(src + c) : make_uint4(0u, 0u, 0u, 0u);
-            *reinterpret_cast<uint4*>(base + L::kQOff + (c >> 3) * L::kQPanel + r * 128 + (((c & 7) ^ (r & 7)) << 4)) = v;
+                for (int e = 0; e < 32; ++e)
+                    mx = fmaxf(mx, diag && key0 + 32 * q + e > pos ? -INFINITY : __uint_as_float(sv[e]));
+            }
+            const float m_new = fmaxf(m_raw, mx);  // finite: stage 0 holds key 0, which every row sees
+            if (k == 0) {
+                m_raw = m_new;
+            } else {
+                const bool need = (m_new - m_raw) * c > kPfRescaleLog2;
+                if (__any_sync(0xffffffffu, need)) {
+                    const float f = need ? fast_exp2((m_raw - m_new) * c) : 1.f;
+#pragma unroll
+                    for (int c0o = 0; c0o < D; c0o += 32) {
+                        uint32_t ov[32];
+                        tmem_ld32(row_tmem + kPfTmemO + c0o, ov);
+                        tmem_wait_ld();
+#pragma unroll
+                        for (int e = 0; e < 32; ++e) ov[e] = __float_as_uint(__uint_as_float(ov[e]) * f);
+                        tmem_st32(row_tmem + kPfTmemO + c0o, ov);
+                    }
+                    if (need) {
+                        l_run *= f;
+                        m_raw = m_new;
+                    }
+                }
+            }
+            // pass 2: P = 2^(c s - c m) as bf16 pairs over the first 64 columns of S; keys
+            // 32 q .. 32 q + 31 go to columns 16 q .. 16 q + 15, after those scores were read
+            const float mc = m_raw * c;
+            float sum = 0.f;
+#pragma unroll 1
+            for (int q = 0; q < kPfKeys / 32; ++q) {
+                uint32_t sv[32], pw[16];
+                tmem_ld32(row_tmem + 32 * q, sv);
+                tmem_wait_ld();
+#pragma unroll
+                for (int e = 0; e < 16; ++e) {
+                    const int j = key0 + 32 * q + 2 * e;
+                    const float a = diag && j > pos ? 0.f : fast_exp2(fmaf(__uint_as_float(sv[2 * e]), c, -mc));
+                    const float b = diag && j + 1 > pos ? 0.f : fast_exp2(fmaf(__uint_as_float(sv[2 * e + 1]), c, -mc));
+                    sum += a + b;
+                    pw[e] = pack_bf16x2(a, b);
+                }
+                tmem_st16(row_tmem + 16 * q, pw);
+            }
+            l_run += sum;
+            // The unit ends at the sequence's last token inside a partial block: the block's unfilled
+            // slots may hold any bits; zero their V rows before any P V reads the stage.
+            if (k + 1 == w.nst && w.zero_tail && t == w.ntiles - 1) {
+                const int vs = sc0 + 2 * k + 1, s = vs % NS;
+                if (!pf_wait(bars.slot_full(s), (vs / NS) & 1, abort_flag, p.status)) return;
+                uint8_t* vst = base + L::kRingOff + s * L::kSlotBytes;
+                const int z0 = w.len - key0, z1 = w.nblk * BS - key0;  // rows [z0, z1) of the stage
+                const int nz = (z1 - z0) * 8 * L::kPanels;              // 16-byte chunks
+                for (int i = r; i < nz; i += kPfRows) {
+                    const int pn = i / ((z1 - z0) * 8), rem = i - pn * ((z1 - z0) * 8);
+                    *reinterpret_cast<uint4*>(vst + pn * L::kSlotPanel + (z0 + rem / 8) * 128 + (rem & 7) * 16) =
+                        make_uint4(0u, 0u, 0u, 0u);
+                }
+                fence_proxy_async_smem();
+            }
+            tmem_wait_st();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bars.p_ready(t));
         }
-    }
-    fence_proxy_async_smem();
-    __syncwarp();
-    if (lane == 0) mbar_arrive(bars.q_ready());
-
-    float m_run = -INFINITY, l_run = 0.f;
-    bool ok = true;
-    for (int k = 0; k < nst; ++k) {
-        const int s = k % kPfStages, ph = (k / kPfStages) & 1;
-        if (!pf_wait(bars.s_full(s), ph, abort_flag, p.status)) {
-            ok = false;
-            break;
-        }
+        // ---- O / l from TMEM to out (bf16) ----
+        if (!pf_wait(bars.o_final(t), uc & 1, abort_flag, p.status)) return;
+        ++uc;
         tc_fence_after();
-        uint32_t sv0[32], sv1[32];
-        tmem_ld32(lane_tmem + kPfTmemS + kPfKeys * s, sv0);
-        tmem_ld32(lane_tmem + kPfTmemS + kPfKeys * s + 32, sv1);
-        tmem_wait_ld();
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(bars.s_free(s));
-
-        // base-2 scores with the causal mask: key t is visible to the row at position pos iff t <= pos
-        const int key0 = k * kPfKeys;
-        float x[kPfKeys];
-        float mx = -INFINITY;
+        const float inv = 1.f / l_run;
+        uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.out) +
+                                              ((size_t)(w.c0 + (valid ? tok : i0)) * Hq + (size_t)w.g * G + r % G) * D);
 #pragma unroll
-        for (int c = 0; c < kPfKeys; ++c) {
-            x[c] = key0 + c <= pos ? __uint_as_float(c < 32 ? sv0[c] : sv1[c - 32]) * p.scale_log2 : -INFINITY;
-            mx = fmaxf(mx, x[c]);
-        }
-        const float m_new = fmaxf(m_run, mx);  // finite: stage 0 holds key 0, which every row sees
-        if (k == 0) {
-            m_run = m_new;
-        } else {
-            const bool need = m_new > m_run + kPfRescaleLog2;
-            if (__any_sync(0xffffffffu, need)) {
-                // O holds P V of the earlier stages: rescale it in TMEM once P_{k-1} V_{k-1} is done.
-                // S_k was issued after P_{k-2} V_{k-2}, so that one has completed, and P_k V_k waits
-                // for this warp: the phase of parity k - 1 is the one in progress or just completed.
-                if (!pf_wait(bars.o_done(), (k - 1) & 1, abort_flag, p.status)) {
-                    ok = false;
-                    break;
-                }
-                tc_fence_after();
-                const float f = need ? fast_exp2(m_run - m_new) : 1.f;
+        for (int c0o = 0; c0o < D; c0o += 32) {
+            uint32_t ov[32];
+            tmem_ld32(row_tmem + kPfTmemO + c0o, ov);
+            tmem_wait_ld();
+            if (valid) {
 #pragma unroll
-                for (int c0o = 0; c0o < D; c0o += 32) {
-                    uint32_t ov[32];
-                    tmem_ld32(lane_tmem + c0o, ov);
-                    tmem_wait_ld();
+                for (int q4 = 0; q4 < 4; ++q4) {
+                    uint32_t wv[4];
 #pragma unroll
-                    for (int e = 0; e < 32; ++e) ov[e] = __float_as_uint(__uint_as_float(ov[e]) * f);
-                    tmem_st32(lane_tmem + c0o, ov);
-                }
-                tmem_wait_st();
-                if (need) {
-                    l_run *= f;
-                    m_run = m_new;
+                    for (int e = 0; e < 4; ++e)
+                        wv[e] = pack_bf16x2(__uint_as_float(ov[8 * q4 + 2 * e]) * inv,
+                                            __uint_as_float(ov[8 * q4 + 2 * e + 1]) * inv);
+                    dst[c0o / 8 + q4] = make_uint4(wv[0], wv[1], wv[2], wv[3]);
                 }
             }
         }
-        // P row r (bf16) over the stage's K, which S_k has finished reading; the sum uses the
-        // rounded weights that P V uses
-        uint8_t* pst = base + L::kRingOff + s * L::kStageBytes;
-        float sum = 0.f;
-#pragma unroll
-        for (int c8 = 0; c8 < kPfKeys / 8; ++c8) {
-            uint32_t w[4];
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                w[e] = pack_bf16x2(fast_exp2(x[8 * c8 + 2 * e] - m_run), fast_exp2(x[8 * c8 + 2 * e + 1] - m_run));
-                sum += bf16_lo(w[e]) + bf16_hi(w[e]);
-            }
-            *reinterpret_cast<uint4*>(pst + r * 128 + ((c8 ^ (r & 7)) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
-        }
-        l_run += sum;
-        // V rows past the tile's last position carry zero weight in every row, but their slots may
-        // hold any bits (unfilled slots, or rows no block was loaded into): zero them
-        const int vlim = nkeys - key0;
-        if (vlim < kPfKeys) {
-            if (!pf_wait(bars.kv_full(s), ph, abort_flag, p.status)) {
-                ok = false;
-                break;
-            }
-            uint8_t* vst = pst + L::kKPBytes;
-            const int nz = (kPfKeys - vlim) * 8 * L::kPanels;  // 16-byte chunks to clear
-            for (int i = r; i < nz; i += kPfRows) {
-                const int pn = i / ((kPfKeys - vlim) * 8), rem = i - pn * ((kPfKeys - vlim) * 8);
-                *reinterpret_cast<uint4*>(vst + pn * L::kKVPanel + (vlim + rem / 8) * 128 + (rem & 7) * 16) =
-                    make_uint4(0u, 0u, 0u, 0u);
-            }
-        }
-        fence_proxy_async_smem();
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(bars.p_ready(s));
-    }
-    if (!ok || !pf_wait(bars.o_final(), 0, abort_flag, p.status)) return;
-    tc_fence_after();
-
-    // ---- O / l from TMEM to out (bf16) ----
-    const float inv = 1.f / l_run;
-    uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.out) +
-                                          ((size_t)(c0 + (valid ? tok : i0)) * Hq + (size_t)g * G + r % G) * D);
-#pragma unroll
-    for (int c0o = 0; c0o < D; c0o += 32) {
-        uint32_t ov[32];
-        tmem_ld32(lane_tmem + c0o, ov);
-        tmem_wait_ld();
-        if (valid) {
-#pragma unroll
-            for (int q4 = 0; q4 < 4; ++q4) {
-                uint32_t w[4];
-#pragma unroll
-                for (int e = 0; e < 4; ++e)
-                    w[e] = pack_bf16x2(__uint_as_float(ov[8 * q4 + 2 * e]) * inv, __uint_as_float(ov[8 * q4 + 2 * e + 1]) * inv);
-                dst[c0o / 8 + q4] = make_uint4(w[0], w[1], w[2], w[3]);
-            }
-        }
+        tc_fence_before();  // the O reads are ordered before this warp's next p_ready arrival
     }
 }
 
 template <int D, int BS>
-__global__ void __launch_bounds__(kPfThreads, kPfCtasPerSm) prefill_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmap_k,
-                                                             const __grid_constant__ CUtensorMap tmap_v) {
+__global__ void __launch_bounds__(kPfThreads, 1)
+    prefill_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmap_k,
+                   const __grid_constant__ CUtensorMap tmap_v, const __grid_constant__ CUtensorMap tmap_q) {
     using L = PfLayout<D, BS>;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_s = smem_u32(smem_raw);
     const uint32_t base_s = (raw_s + 1023u) & ~1023u;
     uint8_t* base = smem_raw + (base_s - raw_s);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-
-    // unit: sequence b, KV head g, query tile j (the tiles that end latest go first)
-    const int b = blockIdx.z, g = blockIdx.y;
-    const int j = (int)gridDim.x - 1 - (int)blockIdx.x;
-    const int c0 = __ldg(p.cu_q_lens + b), n = __ldg(p.cu_q_lens + b + 1) - c0;
-    const int len = __ldg(p.seq_lens + b);
-    const int i0 = j * p.tile_tokens;
-    if (n <= 0 || i0 >= n) return;  // the whole CTA
-    if (n > len || n > p.max_q_len || (int64_t)len > (int64_t)p.max_blocks_per_seq * BS || c0 < 0 ||
-        (int64_t)c0 + n > p.num_q_tokens) {
-        if (tid == 0 && j == 0 && g == 0) flag_status(p.status, PA_DEV_BAD_SEQ_LEN);
-        return;
-    }
-    const int i1 = min(n, i0 + p.tile_tokens);
-    const int nkeys = len - n + i1;                    // keys up to the tile's last position
-    const int nblk = (nkeys + BS - 1) / BS;
-    const int nst = (nkeys + kPfKeys - 1) / kPfKeys;   // 64-key stages
+    const int tiles = (p.max_q_len + p.tile_tokens - 1) / p.tile_tokens;
+    const int pairs = (tiles + 1) / 2;
+    const int total = pairs * p.num_seqs * p.num_kv_heads;
 
     volatile int32_t* misc = reinterpret_cast<volatile int32_t*>(base + L::kMiscOff);
-    PfBars bars{base_s + L::kBarOff};
+    PfBars<L::kSlots> bars{base_s + L::kBarOff};
     if (tid == 0) {
-        for (int s = 0; s < kPfStages; ++s) {
-            mbar_init(bars.kv_full(s), 1);                  // the producer's expect_tx
-            mbar_init(bars.kv_empty(s), 1);                 // tcgen05.commit after P V
-            mbar_init(bars.s_full(s), 1);                   // tcgen05.commit after Q K^T
-            mbar_init(bars.s_free(s), kPfSoftmaxWarps);     // each softmax warp has read its S rows
-            mbar_init(bars.p_ready(s), kPfSoftmaxWarps);    // each softmax warp has written its P rows
+        for (int s = 0; s < L::kSlots; ++s) {
+            mbar_init(bars.slot_full(s), 1);   // the producer's expect_tx
+            mbar_init(bars.slot_empty(s), 1);  // tcgen05.commit after the slot's last MMA
         }
-        mbar_init(bars.o_done(), 1);
-        mbar_init(bars.o_final(), 1);
-        mbar_init(bars.q_ready(), kPfSoftmaxWarps);
+        for (int t = 0; t < kPfTiles; ++t) {
+            mbar_init(bars.s_full(t), 1);                 // tcgen05.commit after Q K^T
+            mbar_init(bars.p_ready(t), kPfSoftmaxWarps);  // each softmax warp has written its P rows
+            mbar_init(bars.o_final(t), 1);
+        }
+        mbar_init(bars.q_full(), 1);
+        mbar_init(bars.q_empty(), 1);
         mbar_init(bars.mma_drain(), 1);
         fence_barrier_init();
         misc[0] = 0;  // abort flag
@@ -445,12 +515,12 @@ __global__ void __launch_bounds__(kPfThreads, kPfCtasPerSm) prefill_kernel(const
     const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(base + L::kMiscOff + 16);
 
     if (warp == kPfProducer)
-        pf_produce<D, BS>(p, &tmap_k, &tmap_v, b, g, nblk, nst, base_s + L::kRingOff, bars, misc, lane);
+        pf_produce<D, BS>(p, &tmap_k, &tmap_v, &tmap_q, pairs, total, base_s, bars, misc, lane);
     else if (warp == kPfMma) {
-        if (lane == 0) pf_mma<D, BS>(p, nst, base_s + L::kQOff, base_s + L::kRingOff, tmem, bars, misc);
+        if (lane == 0) pf_mma<D, BS>(p, pairs, total, base_s, tmem, bars, misc);
         __syncwarp();
     } else
-        pf_softmax<D, BS>(p, b, g, c0, n, len, i0, i1, nst, base, base_s, tmem, bars, misc, warp, lane);
+        pf_softmax<D, BS>(p, pairs, total, warp >> 2, base, tmem, bars, misc, warp, lane);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -461,16 +531,21 @@ template <int D, int BS>
 pa_status launch_prefill(const PrefillParams& p, const void* k_pool, const void* v_pool, int64_t rows, int num_seqs,
                          int max_q_len, cudaStream_t stream) {
     using L = PfLayout<D, BS>;
-    int dev = 0, occ = 0;
+    int dev = 0, occ = 0, sms = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return PA_ERR_CUDA;
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0) return PA_ERR_CUDA;
     const void* kfn = reinterpret_cast<const void*>(&prefill_kernel<D, BS>);
     if (!kernel_occupancy(dev, kfn, kPfThreads, L::kBytes, &occ)) return PA_ERR_CUDA;
     if (occ <= 0) return PA_ERR_UNSUPPORTED;
-    CUtensorMap tk, tv;
-    if (!pool_map(&tk, dev, k_pool, rows, D, BS, PA_BF16) || !pool_map(&tv, dev, v_pool, rows, D, BS, PA_BF16))
+    CUtensorMap tk, tv, tq;
+    if (!pool_map(&tk, dev, k_pool, rows, D, BS, PA_BF16) || !pool_map(&tv, dev, v_pool, rows, D, BS, PA_BF16) ||
+        !prefill_q_map(&tq, dev, p.q, p.num_q_tokens, p.num_q_heads, D, p.group, p.tile_tokens))
         return PA_ERR_CUDA;
-    const dim3 grid((max_q_len + p.tile_tokens - 1) / p.tile_tokens, p.num_kv_heads, num_seqs);
-    prefill_kernel<D, BS><<<grid, kPfThreads, L::kBytes, stream>>>(p, tk, tv);
+    const int tiles = (max_q_len + p.tile_tokens - 1) / p.tile_tokens;
+    const int64_t total = (int64_t)((tiles + 1) / 2) * num_seqs * p.num_kv_heads;
+    if (total >= INT32_MAX) return PA_ERR_UNSUPPORTED;
+    const int grid = (int)(total < (int64_t)sms ? total : sms);  // persistent: one CTA per SM
+    prefill_kernel<D, BS><<<grid, kPfThreads, L::kBytes, stream>>>(p, tk, tv, tq);
     return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }
 
@@ -489,7 +564,7 @@ extern "C" pa_status pa_prefill_attention(void* out, const void* q, const void* 
     if (dtype != PA_BF16) return PA_ERR_UNSUPPORTED;
     if (num_seqs <= 0 || num_q_heads <= 0 || num_kv_heads <= 0 || num_q_heads % num_kv_heads || max_q_len < 0 ||
         num_q_tokens < 0 ||
-        max_blocks_per_seq <= 0 || num_blocks <= 0 || !std::isfinite(scale))
+        max_blocks_per_seq <= 0 || num_blocks <= 0 || !std::isfinite(scale) || !(scale > 0.f))
         return PA_ERR_INVALID_ARG;
     if (num_q_heads / num_kv_heads > 8 || (head_dim != 64 && head_dim != 128) || (block_size != 16 && block_size != 32) ||
         num_seqs > 65535 || num_kv_heads > 65535)
@@ -512,6 +587,7 @@ extern "C" pa_status pa_prefill_attention(void* out, const void* q, const void* 
     p.cu_q_lens = cu_q_lens;
     p.status = dev_status;
     p.max_blocks_per_seq = max_blocks_per_seq;
+    p.num_seqs = num_seqs;
     p.num_q_heads = num_q_heads;
     p.num_kv_heads = num_kv_heads;
     p.num_blocks = num_blocks;
