@@ -54,7 +54,7 @@ constexpr int kPfTiles = 2;         // query tiles per work unit
 constexpr int kPfSoftmaxWarps = 4;  // per tile
 constexpr int kPfProducer = 8;      // warp index
 constexpr int kPfMma = 9;           // warp index
-constexpr int kPfThreads = 320;
+constexpr int kPfThreads = 384;  // warps 10 and 11 complete the third warpgroup and only give up registers
 constexpr int kPfRows = 128;        // query rows per tile = MMA M = TMEM lanes
 constexpr int kPfKeys = 128;        // keys per stage: N of S, K of P V
 constexpr uint32_t kPfTmemCols = 512;  // tile t: S (P over its first 64 columns) in 256 t + [0, 128), O in 256 t + 128 + [0, D)
@@ -372,20 +372,29 @@ __device__ __forceinline__ void pf_softmax(const PrefillParams& p, int pairs, in
             tc_fence_after();
             // S_t(k) was issued after P_t(k-1) V(k-1) and completes after it: O is up to date and
             // no MMA touches this tile's TMEM until this warp arrives on p_ready.
-            // pass 1: the row max over the stage's 128 scores, 32 at a time (causal mask: key j is
-            // visible to the row at position pos iff j <= pos)
+            // the stage's 128 scores of this row, one TMEM round trip; causal mask: key j is visible
+            // to the row at position pos iff j <= pos (masked scores become -inf, so weigh 0 below)
             const int key0 = k * kPfKeys;
-            const bool diag = key0 + kPfKeys - 1 > pos;
-            float mx = -INFINITY;
-#pragma unroll 1
-            for (int q = 0; q < kPfKeys / 32; ++q) {
-                uint32_t sv[32];
-                tmem_ld32(row_tmem + 32 * q, sv);
-                tmem_wait_ld();
+            uint32_t sv[4][32];
 #pragma unroll
-                for (int e = 0; e < 32; ++e)
-                    mx = fmaxf(mx, diag && key0 + 32 * q + e > pos ? -INFINITY : __uint_as_float(sv[e]));
+            for (int q = 0; q < 4; ++q) tmem_ld32(row_tmem + 32 * q, sv[q]);
+            tmem_wait_ld();
+            if (key0 + kPfKeys - 1 > pos) {
+#pragma unroll
+                for (int q = 0; q < 4; ++q)
+#pragma unroll
+                    for (int e = 0; e < 32; ++e)
+                        if (key0 + 32 * q + e > pos) sv[q][e] = __float_as_uint(-INFINITY);
             }
+            float mx0 = -INFINITY, mx1 = -INFINITY;
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+#pragma unroll
+                for (int e = 0; e < 32; e += 2) {
+                    mx0 = fmaxf(mx0, __uint_as_float(sv[q][e]));
+                    mx1 = fmaxf(mx1, __uint_as_float(sv[q][e + 1]));
+                }
+            const float mx = fmaxf(mx0, mx1);
             const float m_new = fmaxf(m_raw, mx);  // finite: stage 0 holds key 0, which every row sees
             if (k == 0) {
                 m_raw = m_new;
@@ -408,25 +417,23 @@ __device__ __forceinline__ void pf_softmax(const PrefillParams& p, int pairs, in
                     }
                 }
             }
-            // pass 2: P = 2^(c s - c m) as bf16 pairs over the first 64 columns of S; keys
-            // 32 q .. 32 q + 31 go to columns 16 q .. 16 q + 15, after those scores were read
+            // P = 2^(c s - c m) as bf16 pairs over the first 64 columns of S (its scores are in registers)
             const float mc = m_raw * c;
-            float sum = 0.f;
-#pragma unroll 1
-            for (int q = 0; q < kPfKeys / 32; ++q) {
-                uint32_t sv[32], pw[16];
-                tmem_ld32(row_tmem + 32 * q, sv);
-                tmem_wait_ld();
+            float sa = 0.f, sb = 0.f;
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                uint32_t pw[16];
 #pragma unroll
                 for (int e = 0; e < 16; ++e) {
-                    const int j = key0 + 32 * q + 2 * e;
-                    const float a = diag && j > pos ? 0.f : fast_exp2(fmaf(__uint_as_float(sv[2 * e]), c, -mc));
-                    const float b = diag && j + 1 > pos ? 0.f : fast_exp2(fmaf(__uint_as_float(sv[2 * e + 1]), c, -mc));
-                    sum += a + b;
-                    pw[e] = pack_bf16x2(a, b);
+                    const float x0 = fast_exp2(fmaf(__uint_as_float(sv[q][2 * e]), c, -mc));
+                    const float x1 = fast_exp2(fmaf(__uint_as_float(sv[q][2 * e + 1]), c, -mc));
+                    sa += x0;
+                    sb += x1;
+                    pw[e] = pack_bf16x2(x0, x1);
                 }
                 tmem_st16(row_tmem + 16 * q, pw);
             }
+            const float sum = sa + sb;
             l_run += sum;
             // The unit ends at the sequence's last token inside a partial block: the block's unfilled
             // slots may hold any bits; zero their V rows before any P V reads the stage.
@@ -514,13 +521,20 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     tc_fence_after();
     const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(base + L::kMiscOff + 16);
 
-    if (warp == kPfProducer)
-        pf_produce<D, BS>(p, &tmap_k, &tmap_v, &tmap_q, pairs, total, base_s, bars, misc, lane);
-    else if (warp == kPfMma) {
-        if (lane == 0) pf_mma<D, BS>(p, pairs, total, base_s, tmem, bars, misc);
-        __syncwarp();
-    } else
+    // Registers: the launch gives every thread 168 (384 x 168 = 64512); the producer / MMA warpgroup
+    // keeps 56 and the two softmax warpgroups take 224 each: 2 x 128 x 224 + 128 x 56 = 64512.
+    if (warp >= 8) {
+        asm volatile("setmaxnreg.dec.sync.aligned.u32 56;" ::: "memory");
+        if (warp == kPfProducer)
+            pf_produce<D, BS>(p, &tmap_k, &tmap_v, &tmap_q, pairs, total, base_s, bars, misc, lane);
+        else if (warp == kPfMma) {
+            if (lane == 0) pf_mma<D, BS>(p, pairs, total, base_s, tmem, bars, misc);
+            __syncwarp();
+        }
+    } else {
+        asm volatile("setmaxnreg.inc.sync.aligned.u32 224;" ::: "memory");
         pf_softmax<D, BS>(p, pairs, total, warp >> 2, base, tmem, bars, misc, warp, lane);
+    }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
