@@ -235,16 +235,19 @@ __device__ __forceinline__ void pf_produce(const PrefillParams& p, const CUtenso
                     ok = false;
                     break;
                 }
-                if (lane == 0) {
-                    mbar_arrive_expect_tx(bars.slot_full(s), (uint32_t)L::kSlotBytes);
-                    const uint32_t dst = base_s + L::kRingOff + s * L::kSlotBytes;
+                // one lane per block issues that block's boxes, so the copies are requested in parallel
+                if (lane == 0) mbar_arrive_expect_tx(bars.slot_full(s), (uint32_t)L::kSlotBytes);
+                __syncwarp();
+                if (lane < BPS) {
+                    const uint32_t dst = base_s + L::kRingOff + s * L::kSlotBytes + lane * BS * 128;
                     const CUtensorMap* map = half ? tv : tk;
+                    int32_t row = rows[0];
 #pragma unroll
-                    for (int t = 0; t < BPS; ++t)
+                    for (int t = 1; t < BPS; ++t)
+                        if (lane == t) row = rows[t];
 #pragma unroll
-                        for (int pn = 0; pn < L::kPanels; ++pn)
-                            tma_load_2d(dst + pn * L::kSlotPanel + t * BS * 128, map, pn * 64, rows[t], bars.slot_full(s),
-                                        policy);
+                    for (int pn = 0; pn < L::kPanels; ++pn)
+                        tma_load_2d(dst + pn * L::kSlotPanel, map, pn * 64, row, bars.slot_full(s), policy);
                 }
             }
         }
