@@ -393,9 +393,9 @@ __device__ __forceinline__ void pf_softmax(const PrefillParams& p, int pairs, in
 #pragma unroll
             for (int q = 0; q < 4; ++q)
 #pragma unroll
-                for (int e = 0; e < 32; e += 2) {
-                    mx0 = fmaxf(mx0, __uint_as_float(sv[q][e]));
-                    mx1 = fmaxf(mx1, __uint_as_float(sv[q][e + 1]));
+                for (int e = 0; e < 32; e += 4) {
+                    mx0 = fmax3(mx0, __uint_as_float(sv[q][e]), __uint_as_float(sv[q][e + 1]));
+                    mx1 = fmax3(mx1, __uint_as_float(sv[q][e + 2]), __uint_as_float(sv[q][e + 3]));
                 }
             const float mx = fmaxf(mx0, mx1);
             const float m_new = fmaxf(m_raw, mx);  // finite: stage 0 holds key 0, which every row sees
@@ -421,21 +421,27 @@ __device__ __forceinline__ void pf_softmax(const PrefillParams& p, int pairs, in
                 }
             }
             // P = 2^(c s - c m) as bf16 pairs over the first 64 columns of S (its scores are in registers)
+            // (packed pairs: one fma.f32x2 forms two exponents, one add.f32x2 adds two weights)
             const float mc = m_raw * c;
-            float sa = 0.f, sb = 0.f;
+            const uint64_t c2 = f2_pack(c, c), nmc2 = f2_pack(-mc, -mc);
+            uint64_t sum2 = f2_pack(0.f, 0.f);
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
                 uint32_t pw[16];
 #pragma unroll
                 for (int e = 0; e < 16; ++e) {
-                    const float x0 = fast_exp2(fmaf(__uint_as_float(sv[q][2 * e]), c, -mc));
-                    const float x1 = fast_exp2(fmaf(__uint_as_float(sv[q][2 * e + 1]), c, -mc));
-                    sa += x0;
-                    sb += x1;
+                    float x0, x1;
+                    f2_unpack(f2_fma(f2_pack(__uint_as_float(sv[q][2 * e]), __uint_as_float(sv[q][2 * e + 1])), c2, nmc2),
+                              x0, x1);
+                    x0 = fast_exp2(x0);
+                    x1 = fast_exp2(x1);
+                    sum2 = f2_add(sum2, f2_pack(x0, x1));
                     pw[e] = pack_bf16x2(x0, x1);
                 }
                 tmem_st16(row_tmem + 16 * q, pw);
             }
+            float sa, sb;
+            f2_unpack(sum2, sa, sb);
             const float sum = sa + sb;
             l_run += sum;
             // The unit ends at the sequence's last token inside a partial block: the block's unfilled
