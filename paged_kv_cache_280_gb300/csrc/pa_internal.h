@@ -134,6 +134,7 @@ struct PrefillParams {
     int32_t tile_tokens;    // chunk tokens per 128-row query tile: 128 / G (rounded down)
     int32_t num_q_tokens;   // rows of q and out
     int32_t max_q_len;      // bound on every chunk (the grid is sized by it)
+    int32_t out_align32;    // out is 32-byte aligned: 32-byte stores
     float scale_log2;
 };
 

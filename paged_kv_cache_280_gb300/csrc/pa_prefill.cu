@@ -469,23 +469,31 @@ __device__ __forceinline__ void pf_softmax(const PrefillParams& p, int pairs, in
         ++uc;
         tc_fence_after();
         const float inv = 1.f / l_run;
-        uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.out) +
-                                              ((size_t)(w.c0 + (valid ? tok : i0)) * Hq + (size_t)w.g * G + r % G) * D);
+        uint16_t* dst = static_cast<uint16_t*>(p.out) +
+                        ((size_t)(w.c0 + (valid ? tok : i0)) * Hq + (size_t)w.g * G + r % G) * D;
+        // the whole O row in one TMEM round trip, then its bf16 row in 32-byte stores (16-byte
+        // stores when out is only 16-byte aligned)
+        uint32_t ov[D / 32][32];
 #pragma unroll
-        for (int c0o = 0; c0o < D; c0o += 32) {
-            uint32_t ov[32];
-            tmem_ld32(row_tmem + kPfTmemO + c0o, ov);
-            tmem_wait_ld();
-            if (valid) {
+        for (int q = 0; q < D / 32; ++q) tmem_ld32(row_tmem + kPfTmemO + 32 * q, ov[q]);
+        tmem_wait_ld();
+        if (valid) {
+            uint32_t wv[D / 2];
 #pragma unroll
-                for (int q4 = 0; q4 < 4; ++q4) {
-                    uint32_t wv[4];
+            for (int e = 0; e < D / 2; ++e)
+                wv[e] = pack_bf16x2(__uint_as_float(ov[e >> 4][(2 * e) & 31]) * inv,
+                                    __uint_as_float(ov[e >> 4][(2 * e + 1) & 31]) * inv);
+            if (p.out_align32) {
 #pragma unroll
-                    for (int e = 0; e < 4; ++e)
-                        wv[e] = pack_bf16x2(__uint_as_float(ov[8 * q4 + 2 * e]) * inv,
-                                            __uint_as_float(ov[8 * q4 + 2 * e + 1]) * inv);
-                    dst[c0o / 8 + q4] = make_uint4(wv[0], wv[1], wv[2], wv[3]);
-                }
+                for (int v = 0; v < D / 16; ++v)
+                    asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(dst + 16 * v),
+                                 "r"(wv[8 * v]), "r"(wv[8 * v + 1]), "r"(wv[8 * v + 2]), "r"(wv[8 * v + 3]),
+                                 "r"(wv[8 * v + 4]), "r"(wv[8 * v + 5]), "r"(wv[8 * v + 6]), "r"(wv[8 * v + 7])
+                                 : "memory");
+            } else {
+#pragma unroll
+                for (int v = 0; v < D / 8; ++v)
+                    reinterpret_cast<uint4*>(dst)[v] = make_uint4(wv[4 * v], wv[4 * v + 1], wv[4 * v + 2], wv[4 * v + 3]);
             }
         }
         tc_fence_before();  // the O reads are ordered before this warp's next p_ready arrival
@@ -619,6 +627,7 @@ extern "C" pa_status pa_prefill_attention(void* out, const void* q, const void* 
     p.num_q_tokens = num_q_tokens;
     p.max_q_len = max_q_len;
     p.scale_log2 = scale * 1.4426950408889634f;
+    p.out_align32 = (reinterpret_cast<uintptr_t>(out) & 31u) == 0 ? 1 : 0;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     if (head_dim == 128 && block_size == 16) return launch_prefill<128, 16>(p, k_pool, v_pool, rows, num_seqs, max_q_len, st);
     if (head_dim == 128 && block_size == 32) return launch_prefill<128, 32>(p, k_pool, v_pool, rows, num_seqs, max_q_len, st);
