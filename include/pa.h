@@ -202,7 +202,8 @@ pa_status pa_decode_attention_static(void* out, const void* q, const void* k_poo
 
 /*
  * Launch facts of pa_decode_attention for these shapes on the current device
- * (no launch): CTAs in the grid, pipeline stages per CTA, dynamic shared
+ * (no launch): CTAs in the grid, pipeline stages per CTA (on the tensor-core
+ * path at block size 16 a stage holds two blocks' tiles), dynamic shared
  * memory per CTA in bytes, and 1 if the tensor-core (mma) path is used, else
  * 0 (CUDA-core FMA path).  Any output pointer may be NULL.
  */

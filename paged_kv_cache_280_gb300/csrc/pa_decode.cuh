@@ -94,11 +94,14 @@ template <typename T, int D, int BS, bool MMA, int GF, typename KV = T>
 struct Layout {
     static constexpr int E = ElemBytes<KV>::value;  // pool element bytes
     static constexpr int EQ = ElemBytes<T>::value;  // query / output element bytes
-    static constexpr int S = stages_for(MMA ? (E == 1 ? PA_STAGE_BYTES_FP8 : PA_STAGE_BYTES) : PA_STAGE_BYTES_FMA, BS, D, E);
+    // tiles per stage: two 16-token tiles on the tensor-core path (one handshake and one softmax
+    // update per 32 tokens), one tile otherwise
+    static constexpr int TPS = MMA && BS == 16 ? 2 : 1;
+    static constexpr int S = stages_for(MMA ? (E == 1 ? PA_STAGE_BYTES_FP8 : PA_STAGE_BYTES) : PA_STAGE_BYTES_FMA, BS * TPS, D, E);
     static constexpr int GN = GF > 0 ? GF : kMaxGroup;  // query rows a q slot holds
     static constexpr int kTileBytes = BS * D * E;  // K (or V) of one tile
     static constexpr int kPanels = D * E / 128;    // 128-byte column panels per row
-    static constexpr int kStageBytes = 2 * kTileBytes;
+    static constexpr int kStageBytes = 2 * TPS * kTileBytes;  // K of its tiles, then their V
     static constexpr int kQSlotBytes = GN * D * EQ;
     static constexpr int kStagesOff = 0;
     // tensor-core path over an FP8 pool: K and V codes are widened in registers
@@ -469,66 +472,41 @@ struct MmaState {
         }
     }
 
-    // One 16-token step: rows row0..row0+15 of the tile, `valid` of them real.
-    __device__ __forceinline__ void step(uint32_t kbase, uint32_t vbase, int row0, int valid, float scale_log2,
-                                         int lane) {
-        const int g = lane >> 2, tig = lane & 3;
-        float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};  // two chains over the k-steps
-        {
-            const int row = row0 + (lane & 7) + (((lane >> 3) & 1) << 3);
-            const int csel = lane >> 4;
-            if constexpr (F8) {
-                // one ldmatrix: 16 code rows x 32 dims; each thread's four codes of a
-                // row are the k-slots 2t, 2t+1 (lo pair) and 2t+8, 2t+9 (hi pair)
+    // S^T = K q^T for rows row0..row0+15 of a tile: acc[c] are two independent accumulation chains
+    // over the k-steps, (token g, head 2tig), (g, 2tig+1), (g+8, 2tig), (g+8, 2tig+1).
+    __device__ __forceinline__ void scores(uint32_t kbase, int row0, int lane, float (&acc)[2][4]) const {
 #pragma unroll
-                for (int s2 = 0; s2 < MT / 2; ++s2) {
-                    uint32_t r0, r1, r2, r3, a0, a1, a2, a3;
-                    ldmatrix_x4(kbase + tile_chunk_offset<BS>(row, 2 * s2 + csel), r0, r1, r2, r3);
-                    e4m3x4_to_f16x2(r0, a0, a2);
-                    e4m3x4_to_f16x2(r1, a1, a3);
-                    mma16816(acc[0], a0, a1, a2, a3, qb[2 * s2][0], qb[2 * s2][1]);
-                    e4m3x4_to_f16x2(r2, a0, a2);
-                    e4m3x4_to_f16x2(r3, a1, a3);
-                    mma16816(acc[1], a0, a1, a2, a3, qb[2 * s2 + 1][0], qb[2 * s2 + 1][1]);
-                }
-            } else {
+        for (int c = 0; c < 2; ++c) acc[c][0] = acc[c][1] = acc[c][2] = acc[c][3] = 0.f;
+        const int row = row0 + (lane & 7) + (((lane >> 3) & 1) << 3);
+        const int csel = lane >> 4;
+        if constexpr (F8) {
+            // one ldmatrix: 16 code rows x 32 dims; each thread's four codes of a
+            // row are the k-slots 2t, 2t+1 (lo pair) and 2t+8, 2t+9 (hi pair)
 #pragma unroll
-                for (int s = 0; s < MT; ++s) {
-                    uint32_t a0, a1, a2, a3;
-                    ldmatrix_x4(kbase + tile_chunk_offset<BS>(row, 2 * s + csel), a0, a1, a2, a3);
-                    mma16816(acc[s & 1], a0, a1, a2, a3, qb[s][0], qb[s][1]);
-                }
+            for (int s2 = 0; s2 < MT / 2; ++s2) {
+                uint32_t r0, r1, r2, r3, a0, a1, a2, a3;
+                ldmatrix_x4(kbase + tile_chunk_offset<BS>(row, 2 * s2 + csel), r0, r1, r2, r3);
+                e4m3x4_to_f16x2(r0, a0, a2);
+                e4m3x4_to_f16x2(r1, a1, a3);
+                mma16816(acc[0], a0, a1, a2, a3, qb[2 * s2][0], qb[2 * s2][1]);
+                e4m3x4_to_f16x2(r2, a0, a2);
+                e4m3x4_to_f16x2(r3, a1, a3);
+                mma16816(acc[1], a0, a1, a2, a3, qb[2 * s2 + 1][0], qb[2 * s2 + 1][1]);
+            }
+        } else {
+#pragma unroll
+            for (int s = 0; s < MT; ++s) {
+                uint32_t a0, a1, a2, a3;
+                ldmatrix_x4(kbase + tile_chunk_offset<BS>(row, 2 * s + csel), a0, a1, a2, a3);
+                mma16816(acc[s & 1], a0, a1, a2, a3, qb[s][0], qb[s][1]);
             }
         }
-        // (token g, head 2tig), (g, 2tig+1), (g+8, 2tig), (g+8, 2tig+1)
-        const bool v0 = g < valid, v1 = g + 8 < valid;
-        const float x0 = v0 ? (acc[0][0] + acc[1][0]) * scale_log2 : -INFINITY;
-        const float x1 = v0 ? (acc[0][1] + acc[1][1]) * scale_log2 : -INFINITY;
-        const float x2 = v1 ? (acc[0][2] + acc[1][2]) * scale_log2 : -INFINITY;
-        const float x3 = v1 ? (acc[0][3] + acc[1][3]) * scale_log2 : -INFINITY;
-        float mx0 = fmaxf(x0, x2), mx1 = fmaxf(x1, x3);
-#pragma unroll
-        for (int off = 4; off < 32; off <<= 1) {
-            mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
-            mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
-        }
-        const float mn0 = fmaxf(m[0], mx0), mn1 = fmaxf(m[1], mx1);
-        const float al0 = exp2f(m[0] - mn0), al1 = exp2f(m[1] - mn1);
-        const uint32_t P0 = pack16(exp2f(x0 - mn0), exp2f(x1 - mn1));
-        const uint32_t P1 = pack16(exp2f(x2 - mn0), exp2f(x3 - mn1));
-        // the sum uses the rounded weights that P V uses
-        l[0] = l[0] * al0 + lo16(P0) + lo16(P1);
-        l[1] = l[1] * al1 + hi16(P0) + hi16(P1);
-        m[0] = mn0;
-        m[1] = mn1;
-#pragma unroll
-        for (int i = 0; i < MT; ++i) {
-            o[i][0] *= al0;
-            o[i][1] *= al1;
-            o[i][2] *= al0;
-            o[i][3] *= al1;
-        }
-        const uint32_t b0 = movmatrix_trans(P0), b1 = movmatrix_trans(P1);
+    }
+
+    // O^T += V^T P^T for rows row0..row0+15 of a tile; b0, b1: P^T as B fragments.
+    __device__ __forceinline__ void accumulate_pv(uint32_t vbase, int row0, int valid, uint32_t b0, uint32_t b1,
+                                                  int lane) {
+        const int tig = lane & 3;
         uint32_t m01 = 0xffffffffu, m89 = 0xffffffffu;
         if (valid < 16) {  // zero V rows past the sequence end (their slots may hold anything)
             m01 = (2 * tig < valid ? 0x0000ffffu : 0u) | (2 * tig + 1 < valid ? 0xffff0000u : 0u);
@@ -559,6 +537,84 @@ struct MmaState {
                 mma16816(o[i], a0 & m01, a1 & m01, a2 & m89, a3 & m89, b0, b1);
             }
         }
+    }
+
+    // Base-2 scores of one 16-token step: (token g, head 2tig), (g, 2tig+1), (g+8, 2tig), (g+8, 2tig+1),
+    // -inf past `valid`.
+    __device__ static __forceinline__ void base2(const float (&acc)[2][4], int valid, float scale_log2, int lane,
+                                                 float (&x)[4]) {
+        const int g = lane >> 2;
+        const bool v0 = g < valid, v1 = g + 8 < valid;
+        x[0] = v0 ? (acc[0][0] + acc[1][0]) * scale_log2 : -INFINITY;
+        x[1] = v0 ? (acc[0][1] + acc[1][1]) * scale_log2 : -INFINITY;
+        x[2] = v1 ? (acc[0][2] + acc[1][2]) * scale_log2 : -INFINITY;
+        x[3] = v1 ? (acc[0][3] + acc[1][3]) * scale_log2 : -INFINITY;
+    }
+
+    // Online-softmax update over the scores of n steps (n = 1 or 2); P[s][0..1] receive step s's
+    // weights, packed as the MMA's A operand rows (token g, token g+8).
+    template <int N>
+    __device__ __forceinline__ void softmax(const float (&x)[N][4], uint32_t (&P)[N][2]) {
+        float mx0 = fmaxf(x[0][0], x[0][2]), mx1 = fmaxf(x[0][1], x[0][3]);
+#pragma unroll
+        for (int s = 1; s < N; ++s) {
+            mx0 = fmaxf(mx0, fmaxf(x[s][0], x[s][2]));
+            mx1 = fmaxf(mx1, fmaxf(x[s][1], x[s][3]));
+        }
+#pragma unroll
+        for (int off = 4; off < 32; off <<= 1) {
+            mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
+            mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
+        }
+        const float mn0 = fmaxf(m[0], mx0), mn1 = fmaxf(m[1], mx1);
+        const float al0 = exp2f(m[0] - mn0), al1 = exp2f(m[1] - mn1);
+        float s0 = 0.f, s1 = 0.f;
+#pragma unroll
+        for (int s = 0; s < N; ++s) {
+            P[s][0] = pack16(exp2f(x[s][0] - mn0), exp2f(x[s][1] - mn1));
+            P[s][1] = pack16(exp2f(x[s][2] - mn0), exp2f(x[s][3] - mn1));
+            // the sum uses the rounded weights that P V uses
+            s0 += lo16(P[s][0]) + lo16(P[s][1]);
+            s1 += hi16(P[s][0]) + hi16(P[s][1]);
+        }
+        l[0] = l[0] * al0 + s0;
+        l[1] = l[1] * al1 + s1;
+        m[0] = mn0;
+        m[1] = mn1;
+#pragma unroll
+        for (int i = 0; i < MT; ++i) {
+            o[i][0] *= al0;
+            o[i][1] *= al1;
+            o[i][2] *= al0;
+            o[i][3] *= al1;
+        }
+    }
+
+    // One 16-token step: rows row0..row0+15 of the tile, `valid` of them real.
+    __device__ __forceinline__ void step(uint32_t kbase, uint32_t vbase, int row0, int valid, float scale_log2,
+                                         int lane) {
+        float acc[2][4], x[1][4];
+        uint32_t P[1][2];
+        scores(kbase, row0, lane, acc);
+        base2(acc, valid, scale_log2, lane, x[0]);
+        softmax<1>(x, P);
+        accumulate_pv(vbase, row0, valid, movmatrix_trans(P[0][0]), movmatrix_trans(P[0][1]), lane);
+    }
+
+    // Two 16-token steps with one softmax update: their score chains are independent, and the
+    // running max, sum and the rescale of O are done once for 32 tokens.
+    __device__ __forceinline__ void step2(uint32_t kbase_a, uint32_t vbase_a, int row0_a, int valid_a,
+                                          uint32_t kbase_b, uint32_t vbase_b, int row0_b, int valid_b,
+                                          float scale_log2, int lane) {
+        float acc_a[2][4], acc_b[2][4], x[2][4];
+        uint32_t P[2][2];
+        scores(kbase_a, row0_a, lane, acc_a);
+        scores(kbase_b, row0_b, lane, acc_b);
+        base2(acc_a, valid_a, scale_log2, lane, x[0]);
+        base2(acc_b, valid_b, scale_log2, lane, x[1]);
+        softmax<2>(x, P);
+        accumulate_pv(vbase_a, row0_a, valid_a, movmatrix_trans(P[0][0]), movmatrix_trans(P[0][1]), lane);
+        accumulate_pv(vbase_b, row0_b, valid_b, movmatrix_trans(P[1][0]), movmatrix_trans(P[1][1]), lane);
     }
 
     // Head dims of accumulator rows g and g + 8 of m16 block i.
@@ -936,23 +992,37 @@ __global__ void __launch_bounds__(Layout<T, D, BS, MMA, GF, KV>::kThreadsCta)
                 blk_nxt = table_chunk(b, jb + 32, j1);
             else if (have_next)
                 blk_nxt = table_chunk(nb_, nj0, nj1);
-            for (int i = 0; i < n; ++i) {
-                int32_t bid = __shfl_sync(0xffffffffu, blk_cur, i);
-                if (bid < 0 || bid >= p.num_blocks) {  // warp-uniform
-                    if (lane == 0) flag_status(p.status, PA_DEV_BAD_BLOCK_ID);
-                    bid = 0;
+            // stages of TPS consecutive tiles of the piece (a chunk holds an even number of them
+            // except at the piece's end, so the pairs are tiles 2m, 2m + 1 from the piece start)
+            for (int i = 0; i < n; i += L::TPS) {
+                const int nt = min(L::TPS, n - i);
+                int32_t bids[L::TPS];
+#pragma unroll
+                for (int t = 0; t < L::TPS; ++t) {
+                    int32_t bid = __shfl_sync(0xffffffffu, blk_cur, (i + t) & 31);
+                    if (t < nt && (bid < 0 || bid >= p.num_blocks)) {  // warp-uniform
+                        if (lane == 0) flag_status(p.status, PA_DEV_BAD_BLOCK_ID);
+                        bid = 0;
+                    }
+                    bids[t] = bid;
                 }
                 const int st = k % S;
                 if (role_wait(empty_bar(st), ((k / S) & 1) ^ 1, misc, p.status)) {
                     if (lane == 0) {
-                        mbar_arrive_expect_tx(full_bar(st), (uint32_t)L::kStageBytes);
-                        const int32_t y = (bid * Hkv + h) * BS;
+                        mbar_arrive_expect_tx(full_bar(st), (uint32_t)(nt * 2 * L::kTileBytes));
                         const uint32_t ks = base_s + L::kStagesOff + st * L::kStageBytes;
 #pragma unroll
-                        for (int pn = 0; pn < L::kPanels; ++pn) {
-                            tma_load_2d(ks + pn * BS * 128, &tmap_k, pn * (128 / E), y, full_bar(st), policy);
-                            tma_load_2d(ks + L::kTileBytes + pn * BS * 128, &tmap_v, pn * (128 / E), y, full_bar(st),
-                                        policy);
+                        for (int t = 0; t < L::TPS; ++t) {
+                            if (t < nt) {
+                                const int32_t y = (bids[t] * Hkv + h) * BS;
+#pragma unroll
+                                for (int pn = 0; pn < L::kPanels; ++pn) {
+                                    tma_load_2d(ks + t * L::kTileBytes + pn * BS * 128, &tmap_k, pn * (128 / E), y,
+                                                full_bar(st), policy);
+                                    tma_load_2d(ks + (L::TPS + t) * L::kTileBytes + pn * BS * 128, &tmap_v,
+                                                pn * (128 / E), y, full_bar(st), policy);
+                                }
+                            }
                         }
                     }
                     k_issued = k + 1;
@@ -1011,29 +1081,54 @@ __global__ void __launch_bounds__(Layout<T, D, BS, MMA, GF, KV>::kThreadsCta)
             st.reset();
             const int len = lens_s[b];
             const int ntile = j1 - j0;
-            for (int i = 0; i < ntile; ++i) {
-                const uint32_t kk = k + i;
-                const int sidx = kk % S;
-                const bool ok = role_wait(full_bar(sidx), (kk / S) & 1, misc, p.status, p.wait_limit_ns);
-                if (ok) {
-                    const uint32_t kb = base_s + L::kStagesOff + sidx * L::kStageBytes;
-                    const uint32_t vb = kb + L::kTileBytes;
-                    const int tok0 = (j0 + i) * BS;
-#pragma unroll
-                    for (int sub = 0; sub < BS / 16; ++sub) {
-                        const int valid = min(16, len - (tok0 + sub * 16));
-                        if (valid > 0) {
-                            if constexpr (MMA)
-                                st.step(kb, vb, sub * 16, valid, p.scale_log2, lane);
+            if constexpr (MMA) {
+                // Two 16-token steps per softmax update: the two 16-token tiles of a stage, or the two
+                // halves of a 32-token tile.
+                for (int i = 0; i < ntile; i += L::TPS) {
+                    const uint32_t kk = k + i / L::TPS;
+                    const int sidx = kk % S;
+                    const bool ok = role_wait(full_bar(sidx), (kk / S) & 1, misc, p.status, p.wait_limit_ns);
+                    if (ok) {
+                        const uint32_t kb = base_s + L::kStagesOff + sidx * L::kStageBytes;
+                        const uint32_t vb = kb + L::TPS * L::kTileBytes;
+                        const int tok0 = (j0 + i) * BS;
+                        // a second 16-token step: the tile's second half (32-token tiles), or the
+                        // stage's second tile, which exists only if the piece holds one more tile
+                        // (a piece may end before its sequence does)
+                        const int v0 = min(16, len - tok0), v1 = min(16, len - tok0 - 16);
+                        if (BS == 32 ? v1 > 0 : i + 1 < ntile) {
+                            if (BS == 32)
+                                st.step2(kb, vb, 0, v0, kb, vb, 16, v1, p.scale_log2, lane);
                             else
-                                st.step(kb, vb, sub * 16, valid, G, qf, ptile, lane);
+                                st.step2(kb, vb, 0, v0, kb + L::kTileBytes, vb + L::kTileBytes, 0, v1, p.scale_log2, lane);
+                        } else {
+                            st.step(kb, vb, 0, v0, p.scale_log2, lane);
                         }
                     }
+                    __syncwarp();
+                    if (lane == 0 && ok) mbar_arrive(empty_bar(sidx));  // after an abort the stage stays held
                 }
-                __syncwarp();
-                if (lane == 0 && ok) mbar_arrive(empty_bar(sidx));  // after an abort the stage stays held
+                k += (ntile + L::TPS - 1) / L::TPS;
+            } else {
+                for (int i = 0; i < ntile; ++i) {
+                    const uint32_t kk = k + i;
+                    const int sidx = kk % S;
+                    const bool ok = role_wait(full_bar(sidx), (kk / S) & 1, misc, p.status, p.wait_limit_ns);
+                    if (ok) {
+                        const uint32_t kb = base_s + L::kStagesOff + sidx * L::kStageBytes;
+                        const uint32_t vb = kb + L::kTileBytes;
+                        const int tok0 = (j0 + i) * BS;
+#pragma unroll
+                        for (int sub = 0; sub < BS / 16; ++sub) {
+                            const int valid = min(16, len - (tok0 + sub * 16));
+                            if (valid > 0) st.step(kb, vb, sub * 16, valid, G, qf, ptile, lane);
+                        }
+                    }
+                    __syncwarp();
+                    if (lane == 0 && ok) mbar_arrive(empty_bar(sidx));  // after an abort the stage stays held
+                }
+                k += ntile;
             }
-            k += ntile;
             if constexpr (MMA) st.finish();
             const int nb = P.nblocks(b);
             T* orow = static_cast<T*>(p.out) + ((size_t)b * Hq + (size_t)h * G) * D;
