@@ -147,11 +147,13 @@ struct Plan {
         return (int64_t)Hkv * pref[b] + (int64_t)h * nblocks(b);
     }
     // largest b in [0, B) with Hkv * pre[b] <= x
+    // (Hkv * pre[b] <= Hkv * pre[B] < 2^31: tiles and partitions are counted in 32 bits; x < 2^31)
     __device__ __forceinline__ int find_seq(const int32_t* pre, int64_t x) const {
+        const int32_t x32 = (int32_t)x;
         int lo = 0, hi = B - 1;
         while (lo < hi) {
             int mid = (lo + hi + 1) >> 1;
-            if ((int64_t)Hkv * pre[mid] <= x)
+            if (Hkv * pre[mid] <= x32)
                 lo = mid;
             else
                 hi = mid - 1;
@@ -218,23 +220,25 @@ struct Plan {
 // continues its segment and starts the range, slot 0; a split segment's first
 // piece ends the range, slot 1.)
 struct PieceIter {
-    int64_t t, t1, t0;
+    // Tile indices fit in 32 bits (the host refuses num_seqs * Hkv * max_blocks_per_seq >= 2^31),
+    // so the walk uses 32-bit arithmetic: it runs before any tile is requested.
+    int32_t t, t1, t0;
     int b;
     __device__ __forceinline__ void init(const Plan& P, int64_t t0_, int64_t t1_) {
-        t0 = t0_;
-        t = t0_;
-        t1 = t1_;
+        t0 = (int32_t)t0_;
+        t = (int32_t)t0_;
+        t1 = (int32_t)t1_;
         b = t0_ < t1_ ? P.find_seq(P.pref, t0_) : 0;
     }
     __device__ __forceinline__ bool next(const Plan& P, int& b_out, int& h, int& j0, int& j1, bool& at_t0) {
         if (t >= t1) return false;
-        while ((int64_t)P.Hkv * P.pref[b + 1] <= t) ++b;
+        while (P.Hkv * P.pref[b + 1] <= t) ++b;
         const int nb = P.nblocks(b);
-        const int64_t local = t - (int64_t)P.Hkv * P.pref[b];
-        h = (int)(local / nb);
-        j0 = (int)(local % nb);
-        const int64_t room = t1 - t;
-        j1 = (int)((int64_t)(nb - j0) < room ? nb : j0 + room);
+        const uint32_t local = (uint32_t)(t - P.Hkv * P.pref[b]);
+        h = (int)(local / (uint32_t)nb);
+        j0 = (int)(local - (uint32_t)h * (uint32_t)nb);
+        const int32_t room = t1 - t;
+        j1 = nb - j0 < room ? nb : j0 + room;
         at_t0 = (t == t0);
         t += j1 - j0;
         b_out = b;
@@ -914,6 +918,15 @@ __global__ void __launch_bounds__(Layout<T, D, BS, MMA, GF, KV>::kThreadsCta)
     auto qfull_bar = [&](int i) { return bar0 + 8u * (2 * S + i); };
     auto qempty_bar = [&](int i) { return bar0 + 8u * (2 * S + kQSlots + i); };
 
+    // the producer's tensor maps and cache policy, requested before the plan is known
+    uint64_t policy = 0;
+    if (warp == kProducerWarp) {
+        if (lane == 0) {
+            prefetch_tensormap(&tmap_k);
+            prefetch_tensormap(&tmap_v);
+        }
+        policy = policy_evict_first();
+    }
     if (tid == 0) {
         for (int s = 0; s < S; ++s) {
             mbar_init(full_bar(s), 1);
@@ -947,11 +960,7 @@ __global__ void __launch_bounds__(Layout<T, D, BS, MMA, GF, KV>::kThreadsCta)
 
     if (warp == kProducerWarp) {
         // =========================== producer ===========================
-        if (lane == 0) {
-            prefetch_tensormap(&tmap_k);
-            prefetch_tensormap(&tmap_v);
-        }
-        const uint64_t policy = policy_evict_first();
+        // (the tensor maps were prefetched at the kernel's start)
         const uint32_t q_bytes = (uint32_t)(G * D * L::EQ);
         uint32_t k = 0, pi = 0, k_issued = 0, pi_issued = 0;
         // Walk the range in chunks of up to 32 tiles of one piece.  The block-table
