@@ -311,6 +311,11 @@ pa_status pa_swap_in(const void* k_store, const void* v_store, const int32_t* bl
  * it).  Supported: bf16, head_dim 64 or 128, block_size 16 or 32,
  * num_q_heads / num_kv_heads <= 8, num_seqs <= 65535.
  *
+ * scale must be finite and > 0 (the kernel folds it into one fma per weight
+ * against the raw row maximum); otherwise PA_ERR_INVALID_ARG.
+ * Runs on the fifth-generation tensor cores (tcgen05.mma with TMEM
+ * accumulators), one persistent CTA per SM.
+ *
  * Errors: host checks return a status before any launch.  A sequence with
  * n_b > seq_lens[b], n_b > max_q_len, rows past num_q_tokens, or seq_lens[b]
  * beyond its block table sets PA_DEV_BAD_SEQ_LEN in *dev_status (if not NULL)

@@ -50,6 +50,10 @@ def test_prefill_host_checks_run_before_any_launch():
     bad = list(args(pa.PA_BF16, 128, 16))
     bad[1] = ctypes.c_void_p((1 << 20) + 2)  # misaligned q
     assert pa._lib.pa_prefill_attention(*bad) == 1  # PA_ERR_INVALID_ARG
+    for scale in (0.0, -0.1):  # the tensor-core prefill needs a positive scale
+        bad = list(args(pa.PA_BF16, 128, 16))
+        bad[16] = scale
+        assert pa._lib.pa_prefill_attention(*bad) == 1
 
 
 def test_swap_host_checks_run_before_any_launch():
