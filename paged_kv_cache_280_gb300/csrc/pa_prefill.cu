@@ -16,13 +16,16 @@
 // K/V stage of 128 keys.  The grid is persistent (one CTA per SM) and walks
 // the units from the latest tiles (the most keys) to the earliest.
 //
-// CTA: ten warps.
-//   - Producer (warp 8): per unit, both tiles' query rows by TMA (a 3-D box of
-//     64 elements x G heads x 128 / G tokens), then per stage K and V, each
-//     into its own slot of a 5-slot ring (one box of BS rows x 128 bytes per
-//     block and 64-element panel, 128-byte swizzle, evict-last L2 policy: the
-//     segment's other units read the same blocks).  A block past the unit's
-//     last one is loaded from past the pool's end, which TMA fills with zeros.
+// CTA: twelve warps (eleven at work, the last only completes a warpgroup).
+//   - Query loads (warp 10): per unit, both tiles' query rows by TMA (a 3-D
+//     box of 64 elements x G heads x 128 / G tokens), once the previous unit's
+//     Q K^T have completed.
+//   - K/V producer (warp 8): per stage K and V, each into its own slot of a
+//     5-slot ring (one box of BS rows x 128 bytes per block and 64-element
+//     panel, 128-byte swizzle, evict-last L2 policy: the segment's other units
+//     read the same blocks).  A block past the unit's last one is loaded from
+//     past the pool's end, which TMA fills with zeros.  Without the query rows
+//     to wait for, it runs ahead into the next unit as far as the ring allows.
 //   - MMA (warp 9, one thread): S_t = Q_t K^T into tile t's TMEM (M 128, N 128,
 //     K = head_dim, both operands K-major in shared memory), and O_t += P_t V
 //     with P_t read from TMEM, where the softmax wrote it over S_t, and V an
@@ -54,7 +57,8 @@ constexpr int kPfTiles = 2;         // query tiles per work unit
 constexpr int kPfSoftmaxWarps = 4;  // per tile
 constexpr int kPfProducer = 8;      // warp index
 constexpr int kPfMma = 9;           // warp index
-constexpr int kPfThreads = 384;  // warps 10 and 11 complete the third warpgroup and only give up registers
+constexpr int kPfQWarp = 10;        // warp index: query-row loads
+constexpr int kPfThreads = 384;  // warp 11 completes the third warpgroup and only gives up registers
 constexpr int kPfRows = 128;        // query rows per tile = MMA M = TMEM lanes
 constexpr int kPfKeys = 128;        // keys per stage: N of S, K of P V
 constexpr uint32_t kPfTmemCols = 512;  // tile t: S (P over its first 64 columns) in 256 t + [0, 128), O in 256 t + 128 + [0, D)
@@ -172,10 +176,12 @@ __device__ __forceinline__ int pf_unit(const PrefillParams& p, int u, int pairs,
     return 1;
 }
 
-// Producer warp: per unit, Q of both tiles, then K(0), V(0), K(1), V(1), ... through the slot ring.
+// K/V producer warp: per unit, K(0), V(0), K(1), V(1), ... through the slot ring.  The query
+// rows are loaded by a warp of their own, so this one never waits for a unit's Q K^T to complete
+// and runs ahead into the next unit as far as the ring allows.
 template <int D, int BS>
 __device__ __forceinline__ void pf_produce(const PrefillParams& p, const CUtensorMap* tk, const CUtensorMap* tv,
-                                           const CUtensorMap* tq, int pairs, int total, uint32_t base_s,
+                                           int pairs, int total, uint32_t base_s,
                                            const PfBars<PfLayout<D, BS>::kSlots>& bars, volatile int32_t* abort_flag,
                                            int lane) {
     using L = PfLayout<D, BS>;
@@ -183,32 +189,16 @@ __device__ __forceinline__ void pf_produce(const PrefillParams& p, const CUtenso
     if (lane == 0) {
         prefetch_tensormap(tk);
         prefetch_tensormap(tv);
-        prefetch_tensormap(tq);
     }
     const uint64_t policy = policy_evict_last();
     const int32_t oob_row = p.num_blocks * p.num_kv_heads * BS;  // past the pool: TMA reads zeros
-    const int G = p.group;
-    const uint32_t q_tile_bytes = (uint32_t)(L::kPanels * G * p.tile_tokens * 128);
-    int sc = 0, uc = 0;
+    int sc = 0;
     bool ok = true;
     for (int u = blockIdx.x; ok && u < total; u += gridDim.x) {
         PfUnit w;
         const int kind = pf_unit<BS>(p, u, pairs, w);
         if (kind < 0 && lane == 0 && w.g == 0) flag_status(p.status, PA_DEV_BAD_SEQ_LEN);
         if (kind <= 0) continue;
-        // query rows of both tiles, once the previous unit's Q K^T have completed
-        if (!pf_wait(bars.q_empty(), (uc & 1) ^ 1, abort_flag, p.status)) break;
-        if (lane == 0) {
-            mbar_arrive_expect_tx(bars.q_full(), q_tile_bytes * w.ntiles);
-#pragma unroll
-            for (int t = 0; t < kPfTiles; ++t)
-                if (t < w.ntiles)
-#pragma unroll
-                    for (int pn = 0; pn < L::kPanels; ++pn)
-                        tma_load_3d(base_s + L::kQOff + t * L::kQBytes + pn * L::kQPanel, tq, pn * 64, w.g * G,
-                                    w.c0 + w.i0[t], bars.q_full());
-        }
-        ++uc;
         const int32_t* tab = p.block_tables + (size_t)w.b * p.max_blocks_per_seq;
         int32_t blk = 0;
         for (int k = 0; ok && k < w.nst; ++k) {
@@ -255,7 +245,36 @@ __device__ __forceinline__ void pf_produce(const PrefillParams& p, const CUtenso
     // never leave the CTA with copies still landing in its shared memory (a slot's phase completes
     // only when its copies have landed)
     for (int kk = sc > NS ? sc - NS : 0; kk < sc; ++kk) mbar_wait(bars.slot_full(kk % NS), (kk / NS) & 1);
-    if (uc > 0) mbar_wait(bars.q_full(), (uc - 1) & 1);
+}
+
+// Query warp: per unit, both tiles' query rows, once the previous unit's Q K^T have completed.  A
+// warp of its own, so that the K/V producer never waits for that and runs ahead into the next unit.
+template <int D, int BS>
+__device__ __forceinline__ void pf_produce_q(const PrefillParams& p, const CUtensorMap* tq, int pairs, int total,
+                                             uint32_t base_s, const PfBars<PfLayout<D, BS>::kSlots>& bars,
+                                             volatile int32_t* abort_flag, int lane) {
+    using L = PfLayout<D, BS>;
+    if (lane == 0) prefetch_tensormap(tq);
+    const int G = p.group;
+    const uint32_t q_tile_bytes = (uint32_t)(L::kPanels * G * p.tile_tokens * 128);
+    int uc = 0;
+    for (int u = blockIdx.x; u < total; u += gridDim.x) {
+        PfUnit w;
+        if (pf_unit<BS>(p, u, pairs, w) <= 0) continue;
+        if (!pf_wait(bars.q_empty(), (uc & 1) ^ 1, abort_flag, p.status)) break;
+        if (lane == 0) {
+            mbar_arrive_expect_tx(bars.q_full(), q_tile_bytes * w.ntiles);
+#pragma unroll
+            for (int t = 0; t < kPfTiles; ++t)
+                if (t < w.ntiles)
+#pragma unroll
+                    for (int pn = 0; pn < L::kPanels; ++pn)
+                        tma_load_3d(base_s + L::kQOff + t * L::kQBytes + pn * L::kQPanel, tq, pn * 64, w.g * G,
+                                    w.c0 + w.i0[t], bars.q_full());
+        }
+        ++uc;
+    }
+    if (uc > 0) mbar_wait(bars.q_full(), (uc - 1) & 1);  // the last box has landed
 }
 
 // MMA issuer (one thread).
@@ -543,7 +562,9 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     if (warp >= 8) {
         asm volatile("setmaxnreg.dec.sync.aligned.u32 56;" ::: "memory");
         if (warp == kPfProducer)
-            pf_produce<D, BS>(p, &tmap_k, &tmap_v, &tmap_q, pairs, total, base_s, bars, misc, lane);
+            pf_produce<D, BS>(p, &tmap_k, &tmap_v, pairs, total, base_s, bars, misc, lane);
+        else if (warp == kPfQWarp)
+            pf_produce_q<D, BS>(p, &tmap_q, pairs, total, base_s, bars, misc, lane);
         else if (warp == kPfMma) {
             if (lane == 0) pf_mma<D, BS>(p, pairs, total, base_s, tmem, bars, misc);
             __syncwarp();
