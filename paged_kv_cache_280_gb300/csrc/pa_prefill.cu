@@ -39,12 +39,16 @@
 //     writes its row of P (bf16) back to TMEM, and, when the row max has grown
 //     by more than 2^8 since O was last scaled, rescales its O row in TMEM
 //     (the weights stay <= 256; the final ratio is exact).  The final O / l is
-//     written from TMEM.  When a unit ends at the sequence's last token inside
-//     a partial block, the last tile's warps zero the V rows of the unfilled
-//     slots: they may hold any bits, and zero weight times NaN is NaN.
+//     written from TMEM.  When a unit's last block is the sequence's partial
+//     last block, the last tile's warps zero the V rows past the context's
+//     end: they may hold any bits, and zero weight times NaN is NaN.
+// Causal trimming: tile 0 skips a last stage that only tile 1 reaches, and on a
+// tile's last stage the softmax forms weights only up to the last key the
+// tile's last row sees (rounded up to 32 keys) and writes zeros past it.
 // Every wait is bounded; a timeout sets PA_DEV_WAIT_TIMEOUT, every role stops,
 // and the CTA waits for its own copies and MMAs before freeing TMEM.
 #include <cmath>
+#include <type_traits>
 
 #include "pa_device.cuh"
 #include "pa_internal.h"
@@ -65,6 +69,19 @@ constexpr uint32_t kPfTmemCols = 512;  // tile t: S (P over its first 64 columns
 constexpr uint32_t kPfTmemTile = 256;
 constexpr uint32_t kPfTmemO = 128;
 constexpr float kPfRescaleLog2 = 8.f;  // rescale O only when a row max grows by more than this (log2)
+
+// f(std::integral_constant<int, i>) for i = 0 .. N - 1, unrolled at compile time.
+template <int I = 0, int N, class F>
+__device__ __forceinline__ void static_for_impl(F& f) {
+    if constexpr (I < N) {
+        f(std::integral_constant<int, I>{});
+        static_for_impl<I + 1, N>(f);
+    }
+}
+template <int N, class F>
+__device__ __forceinline__ void static_for(F&& f) {
+    static_for_impl<0, N>(f);
+}
 
 __device__ __forceinline__ uint64_t policy_evict_last() {
     uint64_t p;
@@ -143,10 +160,19 @@ struct PfUnit {
     int i0[kPfTiles], i1[kPfTiles];
     int ntiles;      // 1 or 2 (the chunk's last unit may hold one tile)
     int nkeys;       // keys up to the unit's last position
-    int nst;         // 128-key stages
+    int nst;         // 128-key stages (those of the last tile)
+    int nst0;        // stages of tile 0 (nst, or nst - 1 when tile 1 reaches into one more)
+    int kend0, kend1;  // keys visible to the last row of tile 0 / tile 1 (positions 0 .. kend - 1)
     int nblk;        // blocks
-    bool zero_tail;  // the unit ends at the sequence's last token inside a partial block
+    bool zero_tail;  // the unit's last block is the sequence's partial last block
 };
+
+// Columns of a tile's S at stage k that its last row can see (keys below kend), rounded up to 32
+// (one TMEM load of the softmax), at most a whole stage.  Positive while k < the tile's stages.
+__device__ __forceinline__ int pf_cols(int kend, int k) {
+    const int nv = kend - k * kPfKeys;
+    return nv >= kPfKeys ? kPfKeys : ((nv + 31) & ~31);
+}
 
 // 0: empty unit (skipped by every role); 1: a unit to compute; -1: a malformed
 // sequence (flagged once, skipped).
@@ -171,8 +197,13 @@ __device__ __forceinline__ int pf_unit(const PrefillParams& p, int u, int pairs,
     w.ntiles = w.i0[1] < w.n ? 2 : 1;
     w.nkeys = w.len - w.n + (w.ntiles == 2 ? w.i1[1] : w.i1[0]);
     w.nst = (w.nkeys + kPfKeys - 1) / kPfKeys;
+    w.kend0 = w.len - w.n + w.i1[0];
+    w.kend1 = w.nkeys;
+    w.nst0 = (w.kend0 + kPfKeys - 1) / kPfKeys;
     w.nblk = (w.nkeys + BS - 1) / BS;
-    w.zero_tail = w.nkeys == w.len && (w.len % BS) != 0;
+    // Past the context's end the block's slots may hold any bits.  This holds for the unit that ends
+    // at the last token, and also for one that ends fewer than BS tokens before it.
+    w.zero_tail = (int64_t)w.nblk * BS > w.len;
     return 1;
 }
 
@@ -284,28 +315,44 @@ __device__ __forceinline__ void pf_mma(const PrefillParams& p, int pairs, int to
     using L = PfLayout<D, BS>;
     constexpr int NS = L::kSlots;
     constexpr uint32_t idesc_s = umma_idesc_bf16(kPfRows, kPfKeys, 0, 0);  // Q (K-major) x K^T (K-major)
-    constexpr uint32_t idesc_o = umma_idesc_bf16(kPfRows, D, 0, 1);         // P (TMEM) x V (MN-major)
+    constexpr uint32_t idesc_o = umma_idesc_bf16(kPfRows, D, 0, 1);  // P (TMEM) x V (MN-major)
     int sc = 0, uc = 0, ck0 = 0, ck1 = 0;  // slots; units; stages of tile 0 and of tile 1
     bool ok = true;
-    auto slot_addr = [&](int s) { return base_s + L::kRingOff + s * L::kSlotBytes; };
+    // Descriptors: the upper word is a constant per operand kind; the lower word holds the start
+    // address / 16 (bits 0..13, below 256 KB: never carries into the leading offset) and the
+    // leading byte offset, so an operand at a byte offset adds offset / 16 to the lower word.
+    const uint32_t q_lo = (uint32_t)umma_smem_desc(base_s + L::kQOff, 16, 1024);     // K-major Q, tile 0
+    const uint32_t k_lo = (uint32_t)umma_smem_desc(base_s + L::kRingOff, 16, 1024);  // K-major K, slot 0
+    const uint32_t v_lo = (uint32_t)umma_smem_desc(base_s + L::kRingOff, L::kSlotPanel, 1024);  // MN-major V
+    constexpr uint32_t hi = (uint32_t)(umma_smem_desc(0, 0, 1024) >> 32);  // SBO 1024, version, swizzle
+    // S_t = Q_t K^T
     auto issue_s = [&](int t, int ks_slot) {
-        const uint32_t q = base_s + L::kQOff + t * L::kQBytes, kst = slot_addr(ks_slot);
-#pragma unroll
-        for (int ks = 0; ks < D / 16; ++ks) {
-            const uint64_t a = umma_smem_desc(q + (ks >> 2) * L::kQPanel + (ks & 3) * 32, 16, 1024);
-            const uint64_t bd = umma_smem_desc(kst + (ks >> 2) * L::kSlotPanel + (ks & 3) * 32, 16, 1024);
-            umma_bf16(tmem + kPfTmemTile * t, a, bd, idesc_s, ks > 0);
-        }
+        const uint32_t qa = q_lo + (uint32_t)(t * (L::kQBytes >> 4));
+        const uint32_t kb = k_lo + (uint32_t)(ks_slot * (L::kSlotBytes >> 4));
+        const uint32_t d = tmem + kPfTmemTile * t;
+        // K steps of 16 elements: 32 bytes along a 128-byte row, 64-element panels further apart
+        auto step = [&](auto ks_c) {
+            constexpr int ks = decltype(ks_c)::value;
+            constexpr uint32_t oa = ((ks >> 2) * L::kQPanel + (ks & 3) * 32) >> 4;
+            constexpr uint32_t ob = ((ks >> 2) * L::kSlotPanel + (ks & 3) * 32) >> 4;
+            umma_bf16_lo<oa, ob>(d, qa, kb, hi, idesc_s, ks > 0 ? 1u : 0u);
+        };
+        static_for<D / 16>(step);
         umma_commit(bars.s_full(t));
     };
+    // O_t += P_t V over the stage's 128 keys (8 steps of K = 16).  A tile's last stage could stop
+    // after the keys its last row sees, but on GB300 that measured slower than the full stage (the
+    // softmax writes zero weights past them instead).
     auto issue_o = [&](int t, int vs_slot, bool first) {
-        const uint32_t vst = slot_addr(vs_slot);
-#pragma unroll
-        for (int kk = 0; kk < kPfKeys / 16; ++kk) {
-            const uint64_t bd = umma_smem_desc(vst + kk * 16 * 128, L::kSlotPanel, 1024);
-            umma_bf16_tmem_a(tmem + kPfTmemTile * t + kPfTmemO, tmem + kPfTmemTile * t + kk * 8, bd, idesc_o,
-                             (!first || kk > 0) ? 1u : 0u);
-        }
+        const uint32_t vb = v_lo + (uint32_t)(vs_slot * (L::kSlotBytes >> 4));
+        const uint32_t d = tmem + kPfTmemTile * t;
+        const uint32_t acc0 = first ? 0u : 1u;
+        auto step = [&](auto kk_c) {
+            constexpr int kk = decltype(kk_c)::value;
+            constexpr uint32_t ob = (kk * 16 * 128) >> 4;  // 16 keys = 16 rows of 128 bytes of every panel
+            umma_bf16_tmem_a_lo<ob>(d + kPfTmemO, d + kk * 8, vb, hi, idesc_o, kk > 0 ? 1u : acc0);
+        };
+        static_for<kPfKeys / 16>(step);
     };
     for (int u = blockIdx.x; ok && u < total; u += gridDim.x) {
         PfUnit w;
@@ -328,24 +375,31 @@ __device__ __forceinline__ void pf_mma(const PrefillParams& p, int pairs, int to
                 ok = false;
                 break;
             }
+            // tile 0 may have one stage fewer than the unit (its last row sees fewer keys)
+            const bool skip0 = k >= w.nst0;
             // On the unit's last stage the last tile's warps may zero V rows: every tile waits for them.
             const bool all = last && w.zero_tail;
-            for (int t = 0; ok && all && t < T; ++t) ok = pf_wait1(bars.p_ready(t), (t ? ck1 : ck0) & 1, abort_flag, p.status);
+            for (int t = 0; ok && all && t < T; ++t)
+                if (t > 0 || !skip0) ok = pf_wait1(bars.p_ready(t), (t ? ck1 : ck0) & 1, abort_flag, p.status);
+            bool k_ready = false;
             for (int t = 0; ok && t < T; ++t) {
+                if (t == 0 && skip0) continue;
                 int& ck = t ? ck1 : ck0;
+                const int nst_t = t ? w.nst : w.nst0;
                 if (!all && !pf_wait1(bars.p_ready(t), ck & 1, abort_flag, p.status)) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
                 issue_o(t, vs % NS, k == 0);
-                if (last) {
+                if (k + 1 == nst_t) {
                     umma_commit(bars.o_final(t));
                 } else {
-                    if (t == 0 && !pf_wait1(bars.slot_full(ks1 % NS), (ks1 / NS) & 1, abort_flag, p.status)) {
+                    if (!k_ready && !pf_wait1(bars.slot_full(ks1 % NS), (ks1 / NS) & 1, abort_flag, p.status)) {
                         ok = false;
                         break;
                     }
+                    k_ready = true;
                     issue_s(t, ks1 % NS);
                 }
                 ++ck;
@@ -389,14 +443,16 @@ __device__ __forceinline__ void pf_softmax(const PrefillParams& p, int pairs, in
         // padding rows take the tile's last position: their scores stay finite and they are never stored
         const int pos = w.len - w.n + (valid ? tok : i1 - 1);
         float m_raw = -INFINITY, l_run = 0.f;  // running max of the raw scores (the scale is > 0), and sum
-        for (int k = 0; k < w.nst; ++k, ++ck) {
+        const int kend = t ? w.kend1 : w.kend0, nst_t = t ? w.nst : w.nst0;
+        for (int k = 0; k < nst_t; ++k, ++ck) {
             if (!pf_wait(bars.s_full(t), ck & 1, abort_flag, p.status)) return;
             tc_fence_after();
             // S_t(k) was issued after P_t(k-1) V(k-1) and completes after it: O is up to date and
             // no MMA touches this tile's TMEM until this warp arrives on p_ready.
             // the stage's 128 scores of this row, one TMEM round trip; causal mask: key j is visible
-            // to the row at position pos iff j <= pos (masked scores become -inf, so weigh 0 below)
-            const int key0 = k * kPfKeys;
+            // to the row at position pos iff j <= pos (masked scores become -inf, so weigh 0 below).
+            // Only the first nq x 32 columns can hold a key that some row of the tile sees.
+            const int key0 = k * kPfKeys, nq = pf_cols(kend, k) >> 5;
             uint32_t sv[4][32];
 #pragma unroll
             for (int q = 0; q < 4; ++q) tmem_ld32(row_tmem + 32 * q, sv[q]);
@@ -446,6 +502,11 @@ __device__ __forceinline__ void pf_softmax(const PrefillParams& p, int pairs, in
             uint64_t sum2 = f2_pack(0.f, 0.f);
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
+                if (q >= nq) {  // past the tile's last position: zero weights, no exponentials
+                    const uint32_t z[16] = {0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};
+                    tmem_st16(row_tmem + 16 * q, z);
+                    continue;
+                }
                 uint32_t pw[16];
 #pragma unroll
                 for (int e = 0; e < 16; ++e) {
@@ -463,9 +524,9 @@ __device__ __forceinline__ void pf_softmax(const PrefillParams& p, int pairs, in
             f2_unpack(sum2, sa, sb);
             const float sum = sa + sb;
             l_run += sum;
-            // The unit ends at the sequence's last token inside a partial block: the block's unfilled
-            // slots may hold any bits; zero their V rows before any P V reads the stage.
-            if (k + 1 == w.nst && w.zero_tail && t == w.ntiles - 1) {
+            // The unit's last block is the sequence's partial last block: its slots past the context's
+            // end may hold any bits; zero their V rows before any P V reads the stage.
+            if (k + 1 == nst_t && w.zero_tail && t == w.ntiles - 1) {
                 const int vs = sc0 + 2 * k + 1, s = vs % NS;
                 if (!pf_wait(bars.slot_full(s), (vs / NS) & 1, abort_flag, p.status)) return;
                 uint8_t* vst = base + L::kRingOff + s * L::kSlotBytes;

@@ -21,7 +21,7 @@ namespace pa {
 // LBO is unused while one MMA's 16-element K slice stays inside a 128-byte row.
 // MN-major: LBO = distance between 64-element panels along M/N, SBO = distance
 // between 8-row atoms along K.
-__device__ __forceinline__ uint64_t umma_smem_desc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+__host__ __device__ constexpr uint64_t umma_smem_desc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
     uint64_t d = 0;
     d |= (uint64_t)((saddr >> 4) & 0x3FFFu);
     d |= (uint64_t)((lbo >> 4) & 0x3FFFu) << 16;
@@ -76,6 +76,32 @@ __device__ __forceinline__ void umma_bf16_tmem_a(uint32_t d_tmem, uint32_t a_tme
         "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
         "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
         "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+// The same two MMAs with each shared-memory descriptor given as its lower word plus a byte offset
+// / 16 (an immediate) and a common upper word: the descriptor is assembled inside the asm, so an
+// unrolled loop of MMAs keeps one register per operand base instead of one descriptor pair per MMA.
+template <uint32_t A_OFF16, uint32_t B_OFF16>
+__device__ __forceinline__ void umma_bf16_lo(uint32_t d_tmem, uint32_t a_lo, uint32_t b_lo, uint32_t hi, uint32_t idesc,
+                                             uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t.reg .b32 al, bl;\n\t.reg .b64 ad, bd;\n\t"
+        "add.u32 al, %1, %6;\n\tadd.u32 bl, %2, %7;\n\t"
+        "mov.b64 ad, {al, %3};\n\tmov.b64 bd, {bl, %3};\n\t"
+        "setp.ne.b32 p, %5, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], ad, bd, %4, p;\n\t}" ::"r"(d_tmem),
+        "r"(a_lo), "r"(b_lo), "r"(hi), "r"(idesc), "r"(accumulate), "n"(A_OFF16), "n"(B_OFF16)
+        : "memory");
+}
+template <uint32_t B_OFF16>
+__device__ __forceinline__ void umma_bf16_tmem_a_lo(uint32_t d_tmem, uint32_t a_tmem, uint32_t b_lo, uint32_t hi,
+                                                    uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t.reg .b32 bl;\n\t.reg .b64 bd;\n\t"
+        "add.u32 bl, %2, %6;\n\tmov.b64 bd, {bl, %3};\n\t"
+        "setp.ne.b32 p, %5, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], bd, %4, p;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "r"(b_lo), "r"(hi), "r"(idesc), "r"(accumulate), "n"(B_OFF16)
         : "memory");
 }
 // Arrive once on `bar` when every tcgen05.mma this thread issued before has completed.

@@ -104,3 +104,15 @@ def test_prefill_ignores_nan_in_unused_slots(bs):
     assert poison_unused_slots(case.c.k_pool, case.c.v_pool, case.c.ref_tables, case.c.lengths) > 0
     got = case.run()
     check_close(got, case.oracle(), "bf16")
+
+
+@pytest.mark.parametrize("hq,hkv,bs", [(32, 8, 16), (32, 8, 32), (16, 2, 16)])
+def test_prefill_nan_tail_read_by_an_earlier_unit(hq, hkv, bs):
+    """A unit that ends a few tokens before its chunk's end can still load the sequence's partial
+    last block (the NaN slots past the context's end): its output must not see them."""
+    lengths = [106, 116, 200]
+    chunks = [69, 69, 133]  # each chunk's last unit holds 5 tokens, so the unit before ends 5 keys short
+    case = PrefillCase(280110 + hq + bs, lengths, chunks, hq, hkv, 128, bs)
+    assert poison_unused_slots(case.c.k_pool, case.c.v_pool, case.c.ref_tables, case.c.lengths) > 0
+    got = case.run()
+    check_close(got, case.oracle(), "bf16")
