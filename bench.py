@@ -15,7 +15,7 @@ One step = the whole hot path for one decode iteration of the batch:
   a1 host allocator appends one token per sequence (slots, CoW pairs, tables)
   a2 copy-on-write block copy (only when the allocator emitted pairs)
   a3 slot-mapped append of the new K/V
-  a4/a5 paged decode attention over len + 1 tokens (split + on-device merge)
+  a4/a5 paged decode attention over len + 1 tokens (split, merged on the device)
 `value` times a2-a5 on the device (CUDA events, inputs resident in HBM, L2
 flushed between steps); the host allocator runs before the timed loop and
 its time is reported separately.  `e2e` runs genuine decode steps through
@@ -369,6 +369,11 @@ class DecodeSetup:
         self.d_q, self.d_kn, self.d_vn = self.to_dev(self.q), self.to_dev(k_new), self.to_dev(v_new)
         self.d_slots, self.d_tables, self.d_lens = self.to_dev(slots), self.to_dev(self.tables), self.to_dev(self.lens)
         self.d_pairs = self.to_dev(pairs) if len(pairs) else None
+        # kernels of one step: (CoW copy,) append, decode (and the merge kernel, when the call uses it)
+        dt = pa.PA_FP8_E4M3 if self.fp8 else (pa.PA_F32 if w.dtype == "f32" else pa.PA_BF16)
+        self.decode_kernels = pa.pa_decode_kernels_per_call(B, self.Hq, self.Hkv, self.D, self.bs, self.max_blocks,
+                                                            self.PT, dt)
+        self.launches_per_step = 1 + self.decode_kernels + (1 if self.d_pairs is not None else 0)
         self.out = torch.empty_like(self.d_q)
         self.ws = torch.zeros(pa.pa_decode_workspace_bytes(B, self.Hq, self.Hkv, self.D), dtype=torch.uint8, device=dev)
         self.max_len = int(self.lens.max())
@@ -402,7 +407,7 @@ class DecodeSetup:
         self.append(self.d_kn, self.d_vn, self.d_slots, status=st, stream=stream)
 
     def decode(self, stream):
-        """a4 + a5: the decode call (decode and merge kernels)."""
+        """a4 + a5: the decode call (the decode kernel, and the merge kernel when the call uses one)."""
         self.attend(self.d_q, self.d_tables, self.d_lens, self.max_len, stream=stream)
 
     def time_steps(self, K, Wm, flush_l2, stream, dist, on_timed=None):
@@ -475,6 +480,7 @@ class DecodeSetup:
             "decode_us_min": 1e3 * min(dec_ms), "decode_gbs": dbytes / mean_s / 1e9,
             "frac_of_measured_hbm": dbytes / mean_s / 1e9 / peak, "decode_ctas": ctas, "stages": stages,
             "path": "mma.sync" if mma else "fma", "partition_tokens": self.PT, "steps": len(step_ms),
+            "launches_per_step": self.launches_per_step,
         }
         if self.w.prompts:  # shared prompt blocks: L2 serves them more than once
             d["unique_block_kv_bytes_per_step"] = unique_kv
@@ -492,6 +498,7 @@ def run_ours(args, rank, world, local_rank):
 
     K, Wm = args.steps, args.warmup
     K_e2e = args.e2e_steps
+    pa.pa_debug_set_merge_mode(args.merge_mode)
     S = DecodeSetup(args.workload, args, rank, world, dev, pa, K_e2e)
     w, B, Hq, Hkv, D, bs = S.w, S.B, S.Hq, S.Hkv, S.D, S.bs
     fp8, ids, lib, max_blocks, out = S.fp8, S.ids, S.lib, S.max_blocks, S.out
@@ -634,7 +641,7 @@ def run_ours(args, rank, world, local_rank):
             "num_kv_heads": Hkv, "head_dim": D, "block_size": bs, "kv_tokens_per_step": tokens_step,
             "decode_bytes_per_step": dbytes, "unique_block_kv_bytes_per_step": unique_kv, "pool_blocks": w.num_blocks,
             "timing": "steps (append + decode call) timed with events at their ends only; the decode call "
-                      "(decode and merge kernels) timed alone in a second loop of as many steps",
+                      "(decode kernel, and merge kernel when used) timed alone in a second loop of as many steps",
             "l2": f"flushed between timed steps ({L2_FLUSH_BYTES >> 20} MiB write, then a {L2_FLUSH_BYTES >> 21} MiB read "
                   "so that no dirty line is left; untimed)",
             "host_alloc_us_per_step": round(S.host_alloc_us, 1), "decode_ctas": ctas, "stages": stages,
@@ -645,15 +652,16 @@ def run_ours(args, rank, world, local_rank):
         },
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
                      "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured" else "fallback",
-                     "kernel": "pa_decode_attention (decode_kernel, then merge_kernel)",
+                     "kernel": "pa_decode_attention (" + ("decode kernel, merging split segments itself)"
+                                                          if S.decode_kernels == 1 else "decode kernel, then merge kernel)"),
                      "traffic": None if fp8 else recorded_traffic(args.workload)},
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d // max(1, K_e2e),
                 "d2h_bytes_per_step": d2h // max(1, K_e2e), "steps": K_e2e,
                 "includes": "host allocator writing into pinned staging one step ahead of the GPU, one H2D of "
                             "q/k_new/v_new/slots/pairs/tables/lens, kernels, D2H of out; no L2 flush inside the loop "
                             "(the KV read per step is larger than L2 and loaded evict-first)",
-                "launch": "eager" if args.e2e_eager else "one CUDA graph per staging buffer (H2D, append, decode, merge, D2H)"},
-        "gpu_launches": K * (3 + (1 if S.d_pairs is not None else 0)),  # append, decode, merge (+ CoW copy)
+                "launch": "eager" if args.e2e_eager else "one CUDA graph per staging buffer (H2D, append, decode (+ merge), D2H)"},
+        "gpu_launches": K * S.launches_per_step,
         "clocks": clocks.summary(),
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -687,7 +695,7 @@ def run_ours(args, rank, world, local_rank):
         agg = ClockSampler.__new__(ClockSampler)
         agg.samples, agg.max_mhz, agg._nvml = all_samples, line["clocks"].get("sm_max_mhz"), True
         line["per_config_clocks"] = agg.summary()
-        line["gpu_launches_per_config"] = {k: v["steps"] * 3 for k, v in per.items()}
+        line["gpu_launches_per_config"] = {k: v["steps"] * v["launches_per_step"] for k, v in per.items()}
     if rank == 0:
         print(json.dumps(line), flush=True)
     if dist:
@@ -1146,6 +1154,9 @@ def main(argv=None):
                     help="decode path: pool element type (fp8: E4M3 codes with per-pool scales, bf16 queries)")
     ap.add_argument("--prefix-cached", action="store_true",
                     help="prefill path: the prompts share all but their last 7 tokens, already cached")
+    ap.add_argument("--merge-mode", type=int, choices=[0, 1, 2], default=0,
+                    help="decode path: where split segments are merged (0: chosen per call, 1: in the decode "
+                         "kernel, 2: by the merge kernel); a comparison aid")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         raise SystemExit("at least 3 warm-up steps")

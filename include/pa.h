@@ -116,15 +116,17 @@ pa_status pa_copy_blocks(void* k_pool, void* v_pool, const int32_t* src_dst_pair
 /*
  * Size in bytes of the device workspace pa_decode_attention needs for these
  * shapes on the current CUDA device.  The workspace holds the status word
- * (first int32, in a 256-byte head) and two split-sequence partial slots per
- * CTA of the decode grid; this size covers the largest grid the device can
- * take (8 CTAs on every SM), so it suffices for every call with these head
- * shapes whatever pa_decode_set_ctas_per_sm says.  A call refuses (with
- * PA_ERR_WORKSPACE_TOO_SMALL, before launching) only a workspace smaller than
- * what its own grid touches.  The caller allocates it ONCE, with the status
- * word zeroed, and may reuse it across calls on one stream: the partial slots
- * are written before they are read, and the status word only gathers error
- * bits.
+ * (first int32, in a 256-byte head), one merge counter (int32) per CTA of the
+ * decode grid and two split-sequence partial slots per CTA; this size covers
+ * the largest grid the device can take (8 CTAs on every SM), so it suffices
+ * for every call with these head shapes whatever pa_decode_set_ctas_per_sm
+ * says.  A call refuses (with PA_ERR_WORKSPACE_TOO_SMALL, before launching)
+ * only a workspace smaller than what its own grid touches.  The caller
+ * allocates it ONCE, zero-filled (the status word and the merge counters must
+ * start at zero), and may reuse it across calls on one stream: the partial
+ * slots are written before they are read, the status word only gathers error
+ * bits, and every call leaves the merge counters at zero again (also when a
+ * wait timed out: every piece is still stored and counted).
  */
 pa_status pa_decode_workspace_bytes(int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads,
                                     int32_t head_dim, size_t* bytes_out);
@@ -142,10 +144,14 @@ pa_status pa_decode_workspace_bytes(int32_t num_seqs, int32_t num_q_heads, int32
  * `dtype`, output in `dtype` (bf16 rounds to nearest even).  An empty
  * sequence gives a zero output.
  * Long sequences are split across CTAs (flash-decoding) and the partial
- * results merged on the device by a second kernel, launched right after the
- * decode kernel as its programmatic dependent: it waits for the decode grid
- * to finish and writes the output rows of split (sequence, KV head)
- * segments; the decode kernel writes the others.  partition_tokens = 0 splits anywhere on a
+ * results merged on the device, in one of two ways chosen per call from the
+ * shapes and the grid: in the decode kernel itself (each piece of a split
+ * (sequence, KV head) segment is stored to the workspace and counted on the
+ * segment's counter; the CTA whose piece completes the count combines the
+ * pieces and writes the segment's output rows), or by a second kernel
+ * launched right after the decode kernel as its programmatic dependent, which
+ * waits for the decode grid to finish and writes the output rows of split
+ * segments.  partition_tokens = 0 splits anywhere on a
  * block boundary, so that every CTA gets the same share of blocks plus a
  * fixed cost per (sequence, KV head) it touches; partition_tokens = P > 0
  * (a multiple of block_size) allows splits only at multiples of P tokens.
@@ -177,14 +183,15 @@ pa_status pa_decode_attention(void* out, const void* q, const void* k_pool, cons
  * workspace.  Its scratch is a static buffer of PA_STATIC_WORKSPACE_BYTES
  * (8 MiB) in the library's device image, held on every GPU that loads the
  * library until the process exits.  A call whose decode grid needs more
- * scratch than that (the status head plus two partial slots of
- * G * (head_dim + 2) floats per CTA) returns PA_ERR_WORKSPACE_TOO_SMALL before
- * anything runs; on a 152-SM GB300 every supported shape fits at the default
- * CTAs per SM.  The call allocates nothing: after its argument checks it
- * clears the status word at the head of the buffer (cudaMemsetAsync) and
- * enqueues the decode.  That memset sits between the decode and the kernel
- * before it on the stream, so unlike pa_decode_attention this call does not
- * overlap its start with a preceding pa_reshape_and_cache.  If
+ * scratch than that (the status head, then per CTA a merge counter and two
+ * partial slots of G * (head_dim + 2) floats) returns
+ * PA_ERR_WORKSPACE_TOO_SMALL before anything runs; on a 152-SM GB300 every
+ * supported shape fits at the default CTAs per SM.  The call allocates
+ * nothing: after its argument checks it clears the status head and the merge
+ * counters of the buffer (one cudaMemsetAsync) and enqueues the decode.
+ * That memset sits between the decode and the kernel before it on the
+ * stream, so unlike pa_decode_attention this call does not overlap its start
+ * with a preceding pa_reshape_and_cache.  If
  * dev_status_out is not NULL, the call's device status word (PA_DEV_* bits)
  * is copied there on `stream` afterwards.
  * The first call on a device looks up the buffer's device address; make that
@@ -212,6 +219,17 @@ pa_status pa_decode_launch_info(int32_t num_seqs, int32_t num_q_heads, int32_t n
                                 int32_t* stages, int32_t* smem_bytes, int32_t* uses_mma);
 
 /*
+ * Kernels one pa_decode_attention (or _fp8, _static) call with these shapes
+ * launches on the current device (no launch): 1 when it merges split
+ * segments in the decode kernel, 2 when the merge kernel follows it.
+ * max_blocks_per_seq bounds the blocks of every sequence, as for
+ * pa_decode_launch_info.  partition_tokens: as for pa_decode_attention.
+ */
+pa_status pa_decode_kernels_per_call(int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
+                                     int32_t block_size, int32_t max_blocks_per_seq, int32_t partition_tokens,
+                                     pa_dtype dtype, int32_t* kernels);
+
+/*
  * Tuning: CTAs per SM of the decode grid (1..8; 0 restores the default: 4 on
  * the bf16 tensor-core path, otherwise, FP8 pools included, as many as fit,
  * at most 8).  Process-wide; affects later pa_decode_attention and
@@ -233,6 +251,15 @@ pa_status pa_decode_set_ctas_per_sm(int32_t ctas);
  * pa_decode_attention_fp8 and pa_decode_attention_static calls.
  */
 pa_status pa_debug_set_wait_limit_ns(uint64_t ns);
+
+/*
+ * Testing aid (no counterpart on the pages): where pa_decode_attention,
+ * pa_decode_attention_fp8 and pa_decode_attention_static merge split
+ * segments.  0: chosen per call (the default); 1: always in the decode
+ * kernel; 2: always by the second kernel.  Results agree within rounding
+ * order.  Other values return PA_ERR_INVALID_ARG.  Process-wide.
+ */
+pa_status pa_debug_set_merge_mode(int32_t mode);
 
 /*
  * FP8 KV pools (an extrapolation: the pages list FP8 among the quantisation

@@ -59,6 +59,7 @@ _SIGS = {
     "pa_decode_attention_static": (_i32, [_vp, _vp, _vp, _vp, _vp, _i32, _vp, _i32, _i32, _i32, _i32, _i32, _i32,
                                           _i32, _f32, _i32, _i32, _vp, _vp]),
     "pa_decode_launch_info": (_i32, [_i32, _i32, _i32, _i32, _i32, _i32, _i32, _pi32, _pi32, _pi32, _pi32]),
+    "pa_decode_kernels_per_call": (_i32, [_i32, _i32, _i32, _i32, _i32, _i32, _i32, _i32, _pi32]),
     "pa_seq_create_cached": (_i32, [_vp, _i64, _vp, _i32, _pi32]),
     "pa_seq_cache_prefix": (_i32, [_vp, _i64, _vp, _i32]),
     "pa_prefix_cache_stats": (_i32, [_vp, _pi32, _pi32]),
@@ -74,6 +75,7 @@ _SIGS = {
                                     _i32, _i32, ctypes.c_float, _i32, _vp, _vp]),
     "pa_decode_set_ctas_per_sm": (_i32, [_i32]),
     "pa_debug_set_wait_limit_ns": (_i32, [ctypes.c_uint64]),
+    "pa_debug_set_merge_mode": (_i32, [ctypes.c_int32]),
     "pa_alloc_create": (_i32, [_i32, _i32, _vp, ctypes.POINTER(_vp)]),
     "pa_alloc_destroy": (None, [_vp]),
     "pa_alloc_set_max_refcount": (_i32, [_vp, _i32]),
@@ -224,6 +226,15 @@ def pa_decode_launch_info(num_seqs, num_q_heads, num_kv_heads, head_dim, block_s
     return tuple(int(v.value) for v in vals)
 
 
+def pa_decode_kernels_per_call(num_seqs, num_q_heads, num_kv_heads, head_dim, block_size, max_blocks_per_seq,
+                               partition_tokens, dtype):
+    """1 if a decode call with these shapes merges split segments in the decode kernel, 2 if a merge kernel follows."""
+    v = _i32(0)
+    _ok(_lib.pa_decode_kernels_per_call(num_seqs, num_q_heads, num_kv_heads, head_dim, block_size, max_blocks_per_seq,
+                                        int(partition_tokens), dtype, ctypes.byref(v)), "pa_decode_kernels_per_call")
+    return int(v.value)
+
+
 def pa_reshape_and_cache_fp8(k_new, v_new, k_pool, v_pool, slot_mapping, k_scale, v_scale, status=None,
                              stream=None):
     """Slot-mapped append into FP8 pools (uint8 E4M3 codes [num_blocks][Hkv][bs][128]) of bf16/fp32 K/V."""
@@ -291,6 +302,14 @@ def pa_decode_set_ctas_per_sm(ctas: int) -> None:
 def pa_debug_set_wait_limit_ns(ns: int) -> None:
     """Testing aid: time limit of the decode consumer's waits (0 restores the 2 s default)."""
     _ok(_lib.pa_debug_set_wait_limit_ns(int(ns)), "pa_debug_set_wait_limit_ns")
+
+
+MERGE_AUTO, MERGE_IN_KERNEL, MERGE_KERNEL = 0, 1, 2
+
+
+def pa_debug_set_merge_mode(mode: int) -> None:
+    """Testing aid: where decode calls merge split segments (MERGE_AUTO, MERGE_IN_KERNEL or MERGE_KERNEL)."""
+    _ok(_lib.pa_debug_set_merge_mode(int(mode)), "pa_debug_set_merge_mode")
 
 
 # ---------------------------------------------------------------------------

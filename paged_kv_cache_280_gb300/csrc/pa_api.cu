@@ -14,6 +14,7 @@ namespace {
 constexpr int kMaxDevices = 64;
 std::atomic<int> g_ctas_per_sm{0};  // 0 = the per-path default
 std::atomic<uint64_t> g_wait_limit_ns{0};  // 0 = kWaitLimitNs
+std::atomic<int> g_merge_mode{0};          // 0 = chosen per launch, 1 = in the decode kernel, 2 = merge_kernel
 
 struct DeviceInfo {
     int sms = 0;
@@ -182,17 +183,40 @@ bool kernel_occupancy(int dev, const void* kernel, int threads, int smem, int* o
     return true;
 }
 
+// Registers per thread of a kernel (cudaFuncGetAttributes), cached per kernel.
+static bool kernel_regs(const void* kernel, int* regs) {
+    static const void* keys[kKernelCache];
+    static int vals[kKernelCache];
+    static int used = 0;
+    std::lock_guard<std::mutex> lk(g_mu);
+    for (int i = 0; i < used; ++i)
+        if (keys[i] == kernel) {
+            *regs = vals[i];
+            return true;
+        }
+    cudaFuncAttributes a;
+    if (cudaFuncGetAttributes(&a, kernel) != cudaSuccess) return false;
+    if (used < kKernelCache) {
+        keys[used] = kernel;
+        vals[used++] = a.numRegs;
+    }
+    *regs = a.numRegs;
+    return true;
+}
+
 namespace {
 
 struct WorkspaceLayout {
-    size_t partials_off, total;
+    size_t counts_off, partials_off, total;
 };
 
-// The status head, then two partial slots for each of `ctas` CTAs.
+// The status head, one merge counter per CTA (rounded up to 256 bytes), then two partial slots
+// for each of `ctas` CTAs.
 WorkspaceLayout workspace_layout(int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim, int64_t ctas) {
     WorkspaceLayout w;
     const size_t G = (size_t)(num_q_heads / num_kv_heads);
-    w.partials_off = kStatusHeadBytes;
+    w.counts_off = kStatusHeadBytes;
+    w.partials_off = w.counts_off + (((size_t)ctas * 4 + 255) & ~(size_t)255);
     w.total = w.partials_off + (size_t)2 * ctas * partial_slot_floats((int)G, head_dim) * 4;
     return w;
 }
@@ -218,6 +242,7 @@ struct LaunchPlan {
     int sms;
     int merge_smem;
     int merge_grid;
+    bool merge_in_kernel;
 };
 
 pa_status plan_launch(int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
@@ -235,8 +260,12 @@ pa_status plan_launch(int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_head
     if (!found) return PA_ERR_UNSUPPORTED;
     lp->smem = lp->v.smem_bytes(num_seqs, fixed);
     if (lp->smem > kMaxSmem) return PA_ERR_UNSUPPORTED;
-    int occ = 0;
-    if (!kernel_occupancy(dev, lp->v.kernel, lp->v.threads, lp->smem, &occ)) return PA_ERR_CUDA;
+    // (both builds get the shared-memory attribute; the grid fits either)
+    int occ = 0, occ_mk = 0;
+    if (!kernel_occupancy(dev, lp->v.kernel, lp->v.threads, lp->smem, &occ) ||
+        !kernel_occupancy(dev, lp->v.kernel_mk, lp->v.threads, lp->smem, &occ_mk))
+        return PA_ERR_CUDA;
+    if (occ_mk < occ) occ = occ_mk;
     if (occ <= 0) return PA_ERR_UNSUPPORTED;
     // Default: the bf16 tensor-core path, which spends little time per tile,
     // keeps four CTAs per SM (about 128 KB of tiles in flight, enough to cover
@@ -250,8 +279,8 @@ pa_status plan_launch(int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_head
     if (grid > tiles_bound) grid = tiles_bound;
     if (grid < 1) grid = 1;
     lp->grid = (int)grid;
-    // the merge: a group of min(32, G D / 16) lanes per CTA boundary (at most one
-    // split segment each), at most one CTA per SM
+    // the merge kernel: a group of min(32, G D / 16) lanes per CTA boundary (at
+    // most one split segment each), at most one CTA per SM
     lp->merge_smem = merge_smem_bytes(num_seqs, fixed);
     if (lp->merge_smem > kMaxSmem) return PA_ERR_UNSUPPORTED;
     int mocc = 0;
@@ -261,6 +290,31 @@ pa_status plan_launch(int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_head
     const int64_t groups_per_cta = (kMergeThreads / 32) * (32 / lps);
     const int64_t merge_ctas = (grid - 1 + groups_per_cta - 1) / groups_per_cta;
     lp->merge_grid = (int)(merge_ctas < 1 ? 1 : merge_ctas < lp->sms ? merge_ctas : lp->sms);
+    // Where split segments are merged.  merge_kernel costs the decode CTAs nothing and
+    // runs its plan while they stream, but only if one of its CTAs fits on an SM beside
+    // the decode's (registers: 256 per warp granule; shared memory: 1 KB reserved per
+    // CTA); it then merges right after the grid.  The in-kernel merge costs each split
+    // piece a release fence and a count, and its merges run mid-range when CTAs hold
+    // several segments each (the piece shared with the next CTA is walked first).  On
+    // the HBM-bound paths (bf16) it takes over when segments outnumber CTAs 3:2, or when
+    // merge_kernel could only start once decode CTAs exit.  On the FP8 path the consumer
+    // is the bound and pays for every fence and count, so only when merge_kernel could
+    // not start early and CTAs hold at most half a segment each (the late start of
+    // merge_kernel then weighs most).  With fixed partitions (long contexts) a segment
+    // spans many CTAs and is merged after the streaming either way: merge_kernel.
+    // (Measured on GB300 on the workloads of the pages: each rule picked the faster mode
+    // or one within 0.5% of it.)
+    int dregs = 0, mregs = 0;
+    if (!kernel_regs(lp->v.kernel_mk, &dregs) || !kernel_regs(lp->v.merge_kernel, &mregs)) return PA_ERR_CUDA;
+    auto warp_regs = [](int r) { return (int64_t)(r * 32 + 255) / 256 * 256; };
+    const int64_t regs_used = (int64_t)per_sm * (lp->v.threads / 32) * warp_regs(dregs);
+    const bool merge_fits = regs_used + (kMergeThreads / 32) * warp_regs(mregs) <= 65536 &&
+                            (int64_t)per_sm * (lp->smem + 1024) + lp->merge_smem + 1024 <= 228 * 1024;
+    const int64_t segments = (int64_t)num_seqs * num_kv_heads;
+    const int mode = g_merge_mode.load();
+    const bool auto_in_kernel = dtype == PA_FP8_E4M3 ? !merge_fits && 2 * segments < grid
+                                                     : 2 * segments >= 3 * grid || !merge_fits;
+    lp->merge_in_kernel = lp->v.merge_in_kernel_ok && (mode == 1 || (mode == 0 && !fixed && auto_in_kernel));
     return PA_OK;
 }
 
@@ -287,6 +341,12 @@ extern "C" pa_status pa_decode_set_ctas_per_sm(int32_t ctas) {
     return PA_OK;
 }
 
+extern "C" pa_status pa_debug_set_merge_mode(int32_t mode) {
+    if (mode < 0 || mode > 2) return PA_ERR_INVALID_ARG;
+    g_merge_mode.store(mode);
+    return PA_OK;
+}
+
 extern "C" pa_status pa_debug_set_wait_limit_ns(uint64_t ns) {
     if (ns > kWaitLimitNs) return PA_ERR_INVALID_ARG;
     g_wait_limit_ns.store(ns);
@@ -308,6 +368,22 @@ extern "C" pa_status pa_decode_launch_info(int32_t num_seqs, int32_t num_q_heads
     if (stages) *stages = lp.v.stages;
     if (smem_bytes) *smem_bytes = lp.smem;
     if (uses_mma) *uses_mma = lp.mma ? 1 : 0;
+    return PA_OK;
+}
+
+extern "C" pa_status pa_decode_kernels_per_call(int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads,
+                                                int32_t head_dim, int32_t block_size, int32_t max_blocks_per_seq,
+                                                int32_t partition_tokens, pa_dtype dtype, int32_t* kernels) {
+    if (dtype != PA_F32 && dtype != PA_BF16 && dtype != PA_FP8_E4M3) return PA_ERR_UNSUPPORTED;
+    if (!kernels) return PA_ERR_INVALID_ARG;
+    pa_status s = check_shapes(num_seqs, num_q_heads, num_kv_heads, head_dim, block_size);
+    if (s != PA_OK) return s;
+    if (max_blocks_per_seq <= 0 || partition_tokens < 0 || partition_tokens % block_size) return PA_ERR_INVALID_ARG;
+    LaunchPlan lp;
+    s = plan_launch(num_seqs, num_q_heads, num_kv_heads, head_dim, block_size, max_blocks_per_seq,
+                    partition_tokens > 0, dtype, &lp);
+    if (s != PA_OK) return s;
+    *kernels = lp.merge_in_kernel ? 1 : 2;
     return PA_OK;
 }
 
@@ -349,7 +425,7 @@ pa_status decode_common(void* out, const void* q, const void* k_pool, const void
     s = plan_launch(num_seqs, num_q_heads, num_kv_heads, head_dim, block_size, max_tiles > 0 ? max_tiles : 1, fixed,
                     dtype, &lp);
     if (s != PA_OK) return s;
-    // the bytes this launch touches: the status head and two partial slots per CTA of its grid
+    // the bytes this launch touches: the status head, a merge counter and two partial slots per CTA of its grid
     const WorkspaceLayout wl = workspace_layout(num_q_heads, num_kv_heads, head_dim, lp.grid);
     if (workspace_bytes < wl.total) return PA_ERR_WORKSPACE_TOO_SMALL;
 
@@ -367,6 +443,7 @@ pa_status decode_common(void* out, const void* q, const void* k_pool, const void
     p.block_tables = block_tables;
     p.seq_lens = seq_lens;
     p.status = reinterpret_cast<int32_t*>(ws);
+    p.merge_counts = reinterpret_cast<int32_t*>(ws + wl.counts_off);
     p.partials = reinterpret_cast<float*>(ws + wl.partials_off);
     p.max_blocks_per_seq = max_blocks_per_seq;
     p.max_len = max_len;
@@ -382,7 +459,8 @@ pa_status decode_common(void* out, const void* q, const void* k_pool, const void
     p.out_scale = v_scale;
     const uint64_t lim = g_wait_limit_ns.load();
     p.wait_limit_ns = lim ? lim : kWaitLimitNs;
-    if (clear_status && cudaMemsetAsync(workspace, 0, kStatusHeadBytes, static_cast<cudaStream_t>(stream)) != cudaSuccess)
+    p.merge_in_kernel = lp.merge_in_kernel ? 1 : 0;
+    if (clear_status && cudaMemsetAsync(workspace, 0, wl.partials_off, static_cast<cudaStream_t>(stream)) != cudaSuccess)
         return PA_ERR_CUDA;
     lp.v.launch(p, tk, tv, lp.grid, lp.smem, lp.merge_grid, lp.merge_smem, static_cast<cudaStream_t>(stream));
     return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ERR_CUDA;

@@ -15,8 +15,9 @@
 // "pieces" (the part of one segment that lies in its range): a piece covering
 // a whole segment is normalised and written straight to `out`; a piece of a
 // segment that straddles CTAs is written as an unnormalised partial (m, l, o)
-// to the workspace, and merge_kernel, launched right after as a programmatic
-// dependent, merges them once the decode grid has finished:
+// to the workspace and counted on a per-segment counter; the CTA whose piece
+// completes the count merges the segment after its own range (flash-decoding's
+// reduce, with no second kernel and no CTA waiting for another):
 //   M = max m_p,  out = sum e^(m_p-M) o_p / sum e^(m_p-M) l_p.
 //
 // CTA layout: two warps and several CTAs per SM.  The producer warp reads
@@ -53,6 +54,7 @@ constexpr int kProducerWarp = 1;
 constexpr int kThreads = 64;
 constexpr int kMaxGroup = 8;
 constexpr int kQSlots = 2;          // query-row slots: the producer may run this many pieces ahead
+constexpr int kMergeNowPieces = 3;  // an in-kernel merge of at most this many pieces may run mid-range
 
 template <typename T>
 struct ElemBytes;
@@ -160,12 +162,15 @@ struct Plan {
         }
         return lo;
     }
-    __device__ __forceinline__ int64_t tile_of_unit(int64_t u) const {
+    // *split = the first tile of the segment the returned tile falls strictly inside, else -1
+    __device__ __forceinline__ int64_t tile_of_unit(int64_t u, int64_t* split) const {
+        *split = -1;
         if (u >= U) return T;
         int b = find_seq(upref, u);
         int64_t local = u - (int64_t)Hkv * upref[b];
         int ub = upref[b + 1] - upref[b];
         int h = (int)(local / ub), part = (int)(local % ub);
+        if (part > 0) *split = seg_start(b, h);
         return seg_start(b, h) + (int64_t)part * PT;
     }
     // Weighted units (no partitions): tile t of segment (b, h) sits at unit
@@ -176,8 +181,9 @@ struct Plan {
         const int h = (int)((t - (int64_t)Hkv * pref[b]) / nblocks(b));
         return (int64_t)K * t + (int64_t)A * ((int64_t)Hkv * b + h + 1);
     }
-    // the first tile at or after weighted unit x
-    __device__ __forceinline__ int64_t first_tile_at_unit(int64_t x) const {
+    // the first tile at or after weighted unit x; *split as in tile_of_unit
+    __device__ __forceinline__ int64_t first_tile_at_unit(int64_t x, int64_t* split) const {
+        *split = -1;
         int lo = 0, hi = B - 1;  // largest b whose units start at or before x
         while (lo < hi) {
             const int mid = (lo + hi + 1) >> 1;
@@ -192,11 +198,15 @@ struct Plan {
         if (span == 0) return (int64_t)Hkv * pref[b];  // A = 0 and b empty: not reached (b is the last with its start)
         const int64_t h = div_nonneg(local, span), r = local - h * span;
         const int64_t j = r <= A ? 0 : (r - A + K - 1) / K;  // at most nb: then the next segment's first tile
+        if (j > 0 && j < nb) *split = (int64_t)Hkv * pref[b] + h * nb;
         return (int64_t)Hkv * pref[b] + h * nb + j;
     }
-    __device__ __forceinline__ int64_t cta_start(int c) const {
-        if (PT == 0) return c >= C ? T : first_tile_at_unit(div_nonneg(c * U + C - 1, C));
-        return tile_of_unit((int64_t)c * U / C);
+    // the first tile of CTA c's range; *split: the first tile of the segment that tile splits
+    // (it then continues the range of CTA c - 1), else -1
+    __device__ __forceinline__ int64_t cta_start(int c, int64_t* split) const {
+        *split = -1;
+        if (PT == 0) return c >= C ? T : first_tile_at_unit(div_nonneg(c * U + C - 1, C), split);
+        return tile_of_unit((int64_t)c * U / C, split);
     }
     // the CTA whose range holds tile t of segment (b, h)
     __device__ __forceinline__ int cta_of_seg(int64_t t, int b, int h) const {
@@ -215,23 +225,32 @@ struct Plan {
     }
 };
 
-// The pieces of a CTA range [t0, t1) in order.  at_t0 marks the piece that
-// starts at t0.  (The partial slots follow j0 instead: a piece with j0 > 0
-// continues its segment and starts the range, slot 0; a split segment's first
-// piece ends the range, slot 1.)
+// The pieces of a CTA range [t0, t1).  When the range ends inside a segment that starts inside
+// it at tile ta (the first piece of a segment split with the next CTA), the walk takes [ta, t1)
+// first and then [t0, ta): a CTA's split pieces then both come early in its range, and so does
+// the merge of a segment split between two CTAs, while the grid still streams.  (The partial
+// slots follow j0: a piece with j0 > 0 continues its segment, slot 0; a split segment's first
+// piece, slot 1.)  ROT = false: no rotation (the walk is [t0, t1) in order).
+template <bool ROT>
 struct PieceIter {
     // Tile indices fit in 32 bits (the host refuses num_seqs * Hkv * max_blocks_per_seq >= 2^31),
     // so the walk uses 32-bit arithmetic: it runs before any tile is requested.
-    int32_t t, t1, t0;
+    int32_t t, t1, t0, ta;  // walking [t, t1); then [t0, ta) while ta > t0
     int b;
-    __device__ __forceinline__ void init(const Plan& P, int64_t t0_, int64_t t1_) {
+    __device__ __forceinline__ void init(const Plan& P, int64_t t0_, int64_t t1_, int64_t ta_) {
         t0 = (int32_t)t0_;
-        t = (int32_t)t0_;
         t1 = (int32_t)t1_;
-        b = t0_ < t1_ ? P.find_seq(P.pref, t0_) : 0;
+        ta = ROT && ta_ > t0_ && ta_ < t1_ ? (int32_t)ta_ : t0;
+        t = ta;
+        b = t < t1 ? P.find_seq(P.pref, t) : 0;
     }
-    __device__ __forceinline__ bool next(const Plan& P, int& b_out, int& h, int& j0, int& j1, bool& at_t0) {
-        if (t >= t1) return false;
+    __device__ __forceinline__ bool next(const Plan& P, int& b_out, int& h, int& j0, int& j1) {
+        if (t >= t1) {
+            if (!ROT || ta <= t0) return false;
+            t1 = ta;  // the part before the rotated piece
+            ta = t = t0;
+            b = P.find_seq(P.pref, t);
+        }
         while (P.Hkv * P.pref[b + 1] <= t) ++b;
         const int nb = P.nblocks(b);
         const uint32_t local = (uint32_t)(t - P.Hkv * P.pref[b]);
@@ -239,11 +258,12 @@ struct PieceIter {
         j0 = (int)(local - (uint32_t)h * (uint32_t)nb);
         const int32_t room = t1 - t;
         j1 = nb - j0 < room ? nb : j0 + room;
-        at_t0 = (t == t0);
         t += j1 - j0;
         b_out = b;
         return true;
     }
+    // no piece left after the one next() returned last
+    __device__ __forceinline__ bool done() const { return t >= t1 && (!ROT || ta <= t0); }
 };
 
 // Warp-collective wait used by both roles: every lane of the warp calls it.
@@ -836,15 +856,19 @@ __device__ __forceinline__ void store16(T* dst, const float (&a)[16], float sc) 
 }
 
 // Merge of one split segment by a group of lps lanes (sl = this lane's index
-// in the group), from the pieces' partial slots in global memory (L2: the
-// decode grid that wrote them has finished):
+// in the group), from the pieces' partial slots in global memory (read from
+// L2, once every piece is visible: its CTA released its stores before counting
+// the piece in, or the decode grid that wrote them has finished):
 //   M = max_p m_p,   out = sum_p e^(m_p-M) o_p / sum_p e^(m_p-M) l_p.
 // Each lane owns 16 consecutive output elements of one head per pass of
-// 16 * lps elements and folds that head's max and sum itself, four pieces at a
-// time with their loads in flight together.
-template <typename T, int D>
+// 16 * lps elements and folds that head's max and sum itself, pieces in order,
+// four at a time: their (m, l) loads in flight together, then XB pieces' o
+// loads at a time (XB = 4 or 1: fewer registers).  The arithmetic does not
+// depend on XB, so every merge of a segment gives the same bits.
+template <typename T, int D, int XB>
 __device__ __forceinline__ void merge_pieces(const float* partials, size_t slot_floats, T* orow, int ca, int np, int G,
                                              int sl, int lps, float oscale) {
+    static_assert(XB == 1 || XB == 4, "o loads in flight: 1 or 4 pieces");
     const int nel = G * D;
     for (int e0 = sl * 16; e0 < nel; e0 += 16 * lps) {
         const int ml = nel + 2 * (e0 / D);  // (m, l) of this lane's head within a slot
@@ -853,16 +877,21 @@ __device__ __forceinline__ void merge_pieces(const float* partials, size_t slot_
         for (int k = 0; k < 16; ++k) a[k] = 0.f;
         for (int i0 = 0; i0 < np; i0 += 4) {
             float2 m_l[4];
-            float4 x[4][4];
+            float4 x[XB][4];
+            auto load_o = [&](int i) {  // o of pieces i .. i + XB - 1 of this group
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                if (i0 + i < np) {
-                    const float* sl = piece_slot(partials, slot_floats, ca + i0 + i, ca);
-                    m_l[i] = __ldcg(reinterpret_cast<const float2*>(sl + ml));
+                for (int j = 0; j < XB; ++j)
+                    if (i0 + i + j < np) {
+                        const float* sp = piece_slot(partials, slot_floats, ca + i0 + i + j, ca);
 #pragma unroll
-                    for (int v = 0; v < 4; ++v) x[i][v] = __ldcg(reinterpret_cast<const float4*>(sl + e0) + v);
-                }
-            }
+                        for (int v = 0; v < 4; ++v) x[j][v] = __ldcg(reinterpret_cast<const float4*>(sp + e0) + v);
+                    }
+            };
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+                if (i0 + i < np)
+                    m_l[i] = __ldcg(reinterpret_cast<const float2*>(piece_slot(partials, slot_floats, ca + i0 + i, ca) + ml));
+            load_o(0);
             float mc = mrun;
 #pragma unroll
             for (int i = 0; i < 4; ++i)
@@ -872,14 +901,18 @@ __device__ __forceinline__ void merge_pieces(const float* partials, size_t slot_
 #pragma unroll
             for (int k = 0; k < 16; ++k) a[k] *= resc;
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                if (i0 + i < np) {
-                    const float w = exp2f(m_l[i].x - mc);
-                    lrun = fmaf(w, m_l[i].y, lrun);
+            for (int i = 0; i < 4; i += XB) {
+                if (i > 0) load_o(i);
 #pragma unroll
-                    for (int v = 0; v < 4; ++v) {
-                        a[4 * v] = fmaf(w, x[i][v].x, a[4 * v]), a[4 * v + 1] = fmaf(w, x[i][v].y, a[4 * v + 1]);
-                        a[4 * v + 2] = fmaf(w, x[i][v].z, a[4 * v + 2]), a[4 * v + 3] = fmaf(w, x[i][v].w, a[4 * v + 3]);
+                for (int j = 0; j < XB; ++j) {
+                    if (i0 + i + j < np) {
+                        const float w = exp2f(m_l[i + j].x - mc);
+                        lrun = fmaf(w, m_l[i + j].y, lrun);
+#pragma unroll
+                        for (int v = 0; v < 4; ++v) {
+                            a[4 * v] = fmaf(w, x[j][v].x, a[4 * v]), a[4 * v + 1] = fmaf(w, x[j][v].y, a[4 * v + 1]);
+                            a[4 * v + 2] = fmaf(w, x[j][v].z, a[4 * v + 2]), a[4 * v + 3] = fmaf(w, x[j][v].w, a[4 * v + 3]);
+                        }
                     }
                 }
             }
@@ -889,12 +922,17 @@ __device__ __forceinline__ void merge_pieces(const float* partials, size_t slot_
     }
 }
 
+// GPU-scope acquire-release fence: a release before a relaxed atomic publishes this thread's
+// earlier writes (and those a barrier ordered before it); an acquire after a relaxed atomic makes
+// the writes its value was published with visible to this thread's later reads.
+__device__ __forceinline__ void fence_acq_rel_gpu() { asm volatile("fence.acq_rel.gpu;" ::: "memory"); }
+
 // ---------------------------------------------------------------------------
 // The kernel
 // ---------------------------------------------------------------------------
-template <typename T, int D, int BS, bool MMA, int GF, typename KV>
-__global__ void __launch_bounds__(Layout<T, D, BS, MMA, GF, KV>::kThreadsCta)
-    decode_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__ CUtensorMap tmap_v) {
+// IKM: the in-kernel merge is compiled in (it runs when p.merge_in_kernel is set).
+template <typename T, int D, int BS, bool MMA, int GF, typename KV, bool IKM>
+__device__ __forceinline__ void decode_body(const DecodeParams& p, const CUtensorMap& tmap_k, const CUtensorMap& tmap_v) {
     using L = Layout<T, D, BS, MMA, GF, KV>;
     constexpr int S = L::S;
     constexpr int E = L::E;
@@ -944,16 +982,19 @@ __global__ void __launch_bounds__(Layout<T, D, BS, MMA, GF, KV>::kThreadsCta)
     __syncthreads();
 
     const Plan P = make_plan(p, pref, upref);
-    // the merge kernel that follows may start its own plan now; it waits for
-    // this grid to finish before it reads a partial
+    // a programmatic dependent that follows on the stream may start its prologue now; it waits
+    // for this grid to finish before it reads what the grid writes
     if (tid == 0) pdl_launch_dependents();
     const bool works = P.T > 0 && c < P.C;
     // the two ends of the range are two independent searches: lanes 0 and 1 of
-    // each warp run one each
-    int64_t tb = 0;
-    if (works && lane < 2) tb = P.cta_start(c + lane);
+    // each warp run one each; lane 1's also gives the start of the segment the
+    // range ends inside (the walk's rotation point)
+    int64_t tb = 0, split = -1;
+    if (works && lane < 2) tb = P.cta_start(c + lane, &split);
     const int64_t t0 = __shfl_sync(0xffffffffu, tb, 0);
     const int64_t t1 = __shfl_sync(0xffffffffu, tb, 1);
+    const bool merge_here = IKM && p.merge_in_kernel;
+    const int64_t ta = __shfl_sync(0xffffffffu, merge_here ? split : -1, 1);
     const int Hq = p.num_q_heads;
     // one partial slot: [G][D] unnormalised o, then [G] (m, l)
     const size_t slot_floats = partial_slot_floats(G, D);
@@ -966,12 +1007,11 @@ __global__ void __launch_bounds__(Layout<T, D, BS, MMA, GF, KV>::kThreadsCta)
         // Walk the range in chunks of up to 32 tiles of one piece.  The block-table
         // entries of the next chunk (of this piece or of the next one) are loaded
         // before this chunk's tiles are issued, so their latency overlaps the issue.
-        PieceIter it;
-        it.init(P, t0, t1);
+        PieceIter<IKM> it;
+        it.init(P, t0, t1, ta);
         int b = 0, h = 0, j0 = 0, j1 = 0, nb_ = 0, nh = 0, nj0 = 0, nj1 = 0;
-        bool at0 = false;
-        bool have = it.next(P, b, h, j0, j1, at0);
-        bool have_next = have && it.next(P, nb_, nh, nj0, nj1, at0);
+        bool have = it.next(P, b, h, j0, j1);
+        bool have_next = have && it.next(P, nb_, nh, nj0, nj1);
         auto table_chunk = [&](int bb, int jfrom, int jend) -> int32_t {
             return lane < jend - jfrom && lane < 32 ? __ldg(p.block_tables + (size_t)bb * p.max_blocks_per_seq + jfrom + lane)
                                                     : 0;
@@ -1045,7 +1085,7 @@ __global__ void __launch_bounds__(Layout<T, D, BS, MMA, GF, KV>::kThreadsCta)
                 b = nb_, h = nh, j0 = nj0, j1 = nj1;
                 jb = j0;
                 have = have_next;
-                have_next = have && it.next(P, nb_, nh, nj0, nj1, at0);
+                have_next = have && it.next(P, nb_, nh, nj0, nj1);
             }
             blk_cur = blk_nxt;
         }
@@ -1071,11 +1111,16 @@ __global__ void __launch_bounds__(Layout<T, D, BS, MMA, GF, KV>::kThreadsCta)
         float* ptile = reinterpret_cast<float*>(base + L::kPTileOff);
         typename std::conditional<MMA, MmaState<D, BS, L::kF8>, FmaState<KV, D, BS, GF>>::type st;
         uint32_t k = 0, pi = 0;
-        PieceIter it;
-        it.init(P, t0, t1);
+        // In-kernel merges this CTA completes wait for the end of its range when they would
+        // otherwise come last (its last piece) or take many round trips (more than
+        // kMergeNowPieces pieces): lane 0 notes (b, h, ca, np) of at most two (slot 0 and
+        // slot 1) in shared memory, np = 0 for none.
+        int32_t* pend = reinterpret_cast<int32_t*>(base + L::kMiscOff + 32);  // [2][4]
+        if (IKM && lane == 0) pend[3] = pend[7] = 0;
+        PieceIter<IKM> it;
+        it.init(P, t0, t1, ta);
         int b, h, j0, j1;
-        bool at_t0;
-        while (it.next(P, b, h, j0, j1, at_t0)) {
+        while (it.next(P, b, h, j0, j1)) {
             const int qs = pi % kQSlots;
             const uint8_t* qslot = base + L::kQOff + qs * L::kQSlotBytes;
             const bool qok = role_wait(qfull_bar(qs), (pi / kQSlots) & 1, misc, p.status, p.wait_limit_ns);
@@ -1144,23 +1189,79 @@ __global__ void __launch_bounds__(Layout<T, D, BS, MMA, GF, KV>::kThreadsCta)
             if (j0 == 0 && j1 == nb) {
                 st.store_out(orow, G, lane, p.out_scale);
             } else {
-                // Split segment: store the unnormalised partial; merge_kernel, the
-                // programmatic dependent of this launch, combines the pieces.  A
-                // piece that continues a segment starts this CTA's range (slot 0);
-                // a split segment's first piece ends it (slot 1).
+                // Split segment: store the unnormalised partial and count it in.  A piece that
+                // continues a segment starts this CTA's range (slot 0); a split segment's first
+                // piece ends it (slot 1).  The segment's pieces come from CTAs ca .. ca + np - 1,
+                // one each, and ca's counter is the segment's.  A release fence orders every
+                // lane's partial stores (the warp barrier puts them before it) ahead of the count;
+                // the CTA whose piece completes the count merges the segment, after an acquire
+                // fence (every other piece is then visible), and resets the counter for the next
+                // call: right away when more pieces follow and it has few pieces (one piece per
+                // round trip, few registers next to the loop's), else after the range (four per
+                // round trip).  With the merge kernel instead, the piece is only stored.
                 float* slot = p.partials + (size_t)(2 * c + (j0 > 0 ? 0 : 1)) * slot_floats;
                 st.store_partial(slot, G, lane);
+                if (merge_here) {
+                    const int64_t s0 = P.seg_start(b, h);
+                    const int ca = P.cta_of_seg(s0, b, h);
+                    const int np = P.cta_of_seg(s0 + nb - 1, b, h) - ca + 1;
+                    __syncwarp();
+                    int old = 0;
+                    if (lane == 0) {
+                        fence_acq_rel_gpu();
+                        old = atomicAdd(p.merge_counts + ca, 1);
+                        if (old == np - 1) fence_acq_rel_gpu();
+                    }
+                    if (__shfl_sync(0xffffffffu, old, 0) == np - 1) {
+                        if (np <= kMergeNowPieces && !it.done()) {
+                            merge_pieces<T, D, 1>(p.partials, slot_floats, orow, ca, np, G, lane, 32, p.out_scale);
+                            if (lane == 0) p.merge_counts[ca] = 0;
+                        } else if (lane == 0) {
+                            int32_t* e = pend + (j0 > 0 ? 0 : 4);
+                            e[0] = b, e[1] = h, e[2] = ca, e[3] = np;
+                        }
+                    }
+                }
             }
             ++pi;
+        }
+        __syncwarp();
+#pragma unroll
+        for (int i = 0; i < (IKM ? 2 : 0); ++i) {
+            const int32_t* e = pend + 4 * i;
+            const int np = e[3];
+            if (np == 0) continue;
+            const int ca = e[2];
+            T* orow = static_cast<T*>(p.out) + ((size_t)e[0] * Hq + (size_t)e[1] * G) * D;
+            merge_pieces<T, D, 4>(p.partials, slot_floats, orow, ca, np, G, lane, 32, p.out_scale);
+            if (lane == 0) p.merge_counts[ca] = 0;
         }
     }
     __syncthreads();
 }
 
+// The two builds of the decode kernel.  With the in-kernel merge the kernel takes the
+// register budget of kMaxCtasPerSm CTAs on an SM, 128 per thread, so that the rare merge
+// path inside the piece loop does not raise the allocation of the whole kernel; without
+// it the compiler keeps its own choice (an explicit minimum of one CTA per SM would let it
+// take up to 255).
+template <typename T, int D, int BS, bool MMA, int GF, typename KV>
+__global__ void __launch_bounds__(Layout<T, D, BS, MMA, GF, KV>::kThreadsCta, kMaxCtasPerSm)
+    decode_kernel_ikm(const DecodeParams p, const __grid_constant__ CUtensorMap tmap_k,
+                      const __grid_constant__ CUtensorMap tmap_v) {
+    decode_body<T, D, BS, MMA, GF, KV, true>(p, tmap_k, tmap_v);
+}
+template <typename T, int D, int BS, bool MMA, int GF, typename KV>
+__global__ void __launch_bounds__(Layout<T, D, BS, MMA, GF, KV>::kThreadsCta)
+    decode_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__ CUtensorMap tmap_v) {
+    decode_body<T, D, BS, MMA, GF, KV, false>(p, tmap_k, tmap_v);
+}
+
 // ---------------------------------------------------------------------------
 // The merge of split segments (flash-decoding's reduce)
 // ---------------------------------------------------------------------------
-// Launched right after decode_kernel as its programmatic dependent: it builds
+// The launch's other mode of merging (p.merge_in_kernel = 0; see pa_api.cu for
+// the choice).  Launched right after decode_kernel as its programmatic dependent: it builds
 // the same plan from seq_lens while the decode streams, then waits for the
 // decode grid to finish (its partials visible) and merges every split
 // segment.  The decode CTAs never wait for each other and never count pieces:
@@ -1190,7 +1291,8 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const DecodeParams
     const int ngroups = gridDim.x * (kMergeThreads / 32) * spw;
     // The segment boundary c names, if any: its sequence, KV head, first CTA and pieces.
     auto named = [&](int c, int& b, int& h, int& ca, int& np) -> bool {
-        const int64_t t = P.cta_start(c);
+        int64_t split;
+        const int64_t t = P.cta_start(c, &split);
         if (t >= P.T) return false;
         b = P.find_seq(P.pref, t);
         const int nb = P.nblocks(b);
@@ -1211,7 +1313,7 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const DecodeParams
     while (c < P.C) {
         if (have) {
             T* orow = static_cast<T*>(p.out) + ((size_t)b * p.num_q_heads + (size_t)h * G) * D;
-            merge_pieces<T, D>(p.partials, slot_floats, orow, ca, np, G, sl, lps, p.out_scale);
+            merge_pieces<T, D, 4>(p.partials, slot_floats, orow, ca, np, G, sl, lps, p.out_scale);
         }
         c += ngroups;
         have = c < P.C && named(c, b, h, ca, np);
@@ -1221,12 +1323,26 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const DecodeParams
 // Host-side handle of one instantiation.
 template <typename T, int D, int BS, bool MMA, int GF, typename KV = T>
 struct VariantOf {
+    // The in-kernel merge is built for bf16 and FP8 pools (fp32 pools, a reference-precision
+    // path whose loop leaves no registers to spare, always merge with merge_kernel).  On the
+    // tensor-core path its code costs the loop even when unused (the FP8 consumer is the
+    // bound), so launches that merge with merge_kernel take a build without it.
+    static constexpr bool kIkm = !std::is_same<T, float>::value;
+    static constexpr bool kTwoBuilds = kIkm && MMA;
+    using KernelFn = void (*)(const DecodeParams, const CUtensorMap, const CUtensorMap);
+    static constexpr KernelFn build(bool ikm) {
+        if constexpr (kIkm) {
+            if (ikm) return &decode_kernel_ikm<T, D, BS, MMA, GF, KV>;
+        }
+        if constexpr (!kIkm || kTwoBuilds) return &decode_kernel<T, D, BS, MMA, GF, KV>;
+        return nullptr;
+    }
+    static constexpr KernelFn kIn = build(true);
+    static constexpr KernelFn kOut = kIkm && !kTwoBuilds ? kIn : build(false);
     static int smem_bytes(int num_seqs, bool fixed) { return Layout<T, D, BS, MMA, GF, KV>::bytes(num_seqs, fixed); }
-    // Launched as a programmatic dependent of the preceding kernel on the stream:
-    // the grid may start while that kernel finishes if it allowed it.
     // Both kernels are launched as programmatic dependents of what precedes them
     // on the stream: the decode of the preceding kernel (which may allow an early
-    // start), the merge of the decode.
+    // start), the merge kernel (when the launch merges with it) of the decode.
     static void launch(const DecodeParams& p, const CUtensorMap& tk, const CUtensorMap& tv, int grid, int smem,
                        int merge_grid, int merge_smem, cudaStream_t stream) {
         cudaLaunchAttribute attr[1];
@@ -1239,7 +1355,8 @@ struct VariantOf {
         cfg.stream = stream;
         cfg.attrs = attr;
         cfg.numAttrs = 1;
-        if (cudaLaunchKernelEx(&cfg, decode_kernel<T, D, BS, MMA, GF, KV>, p, tk, tv) != cudaSuccess) return;
+        if (cudaLaunchKernelEx(&cfg, p.merge_in_kernel ? kIn : kOut, p, tk, tv) != cudaSuccess) return;
+        if (p.merge_in_kernel) return;
         cudaLaunchConfig_t mcfg = cfg;
         mcfg.gridDim = dim3(merge_grid);
         mcfg.blockDim = dim3(kMergeThreads);
@@ -1247,8 +1364,8 @@ struct VariantOf {
         cudaLaunchKernelEx(&mcfg, merge_kernel<T, D, BS>, p);
     }
     static DecodeVariant get() {
-        return DecodeVariant{reinterpret_cast<const void*>(&decode_kernel<T, D, BS, MMA, GF, KV>),
-                             reinterpret_cast<const void*>(&merge_kernel<T, D, BS>),
+        return DecodeVariant{reinterpret_cast<const void*>(kIn), reinterpret_cast<const void*>(kOut),
+                             reinterpret_cast<const void*>(&merge_kernel<T, D, BS>), kIkm,
                              Layout<T, D, BS, MMA, GF, KV>::S,
                              Layout<T, D, BS, MMA, GF, KV>::kThreadsCta, &smem_bytes, &launch};
     }

@@ -15,10 +15,10 @@ constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
 
 constexpr int kMaxCtasPerSm = 8;
 constexpr int kDefaultCtasPerSmMma = 4;  // default CTAs per SM on the bf16 tensor-core path
-// Decode workspace: the status word, then two partial slots per CTA of the
-// launch's grid (pa_decode_workspace_bytes sizes it for kMaxCtasPerSm CTAs on
-// every SM, the largest grid); a slot is [G][D] floats of o plus [G][2] floats
-// of (m, l).
+// Decode workspace: the status head, one merge counter per CTA, then two
+// partial slots per CTA of the launch's grid (pa_decode_workspace_bytes sizes
+// it for kMaxCtasPerSm CTAs on every SM, the largest grid); a slot is [G][D]
+// floats of o plus [G][2] floats of (m, l).
 constexpr int kSlotExtraFloatsPerHead = 2;
 // floats of one partial slot, a multiple of 4 so that every slot is 16-byte aligned
 inline __host__ __device__ size_t partial_slot_floats(int G, int D) {
@@ -44,6 +44,9 @@ struct DecodeParams {
     const int32_t* block_tables;
     const int32_t* seq_lens;
     int32_t* status;    // workspace word 0
+    // [num_ctas]: pieces of the split segment whose first piece CTA c holds that have been
+    // stored so far; zero between calls (the CTA that completes the count resets it)
+    int32_t* merge_counts;
     float* partials;    // [2 * num_ctas][G * (D + 2)]
     int32_t max_blocks_per_seq;
     int32_t max_len;  // min(max_seq_len, max_blocks_per_seq * block_size)
@@ -63,18 +66,24 @@ struct DecodeParams {
     // time limit of the consumer's waits for query rows and tiles (the producer's
     // waits, and its final wait for the copies it issued, keep the full limit)
     uint64_t wait_limit_ns;
+    // 1: split segments are merged inside the decode kernel (merge_counts); 0: by
+    // merge_kernel, launched after it (the host picks per launch, see pa_api.cu)
+    int32_t merge_in_kernel;
 };
 
 // One compiled decode kernel (dtype, head_dim, block_size, compute path).
-// The merge of split segments: a second, small kernel (see pa_decode.cuh).
+// The merge of split segments when it is not done in the decode kernel: a
+// second, small kernel (see pa_decode.cuh).
 constexpr int kMergeThreads = 128;
 // its shared memory for num_seqs sequences: the plan's prefix sums, the
 // clamped lengths and the scan's warp sums
 inline int merge_smem_bytes(int num_seqs, bool fixed) { return ((num_seqs + 1) * (fixed ? 2 : 1) + num_seqs + 8) * 4; }
 
 struct DecodeVariant {
-    const void* kernel;
-    const void* merge_kernel;  // launched right after `kernel` as its programmatic dependent
+    const void* kernel;        // the build that merges in the kernel (and may also merge with merge_kernel)
+    const void* kernel_mk;     // the build launched when merge_kernel merges (may be `kernel`)
+    const void* merge_kernel;  // launched right after the decode as its programmatic dependent, when used
+    bool merge_in_kernel_ok;   // `kernel` has the in-kernel merge
     int stages;
     int threads;
     int (*smem_bytes)(int num_seqs, bool fixed);
@@ -93,8 +102,9 @@ bool decode_variant_fp8(int head_dim, int block_size, int group, DecodeVariant* 
 
 // The decode of pa_decode_attention / _fp8 (pa_api.cu): checks, plan and launch.
 // Refuses a workspace smaller than the bytes its own grid touches (the status
-// head and two partial slots per CTA).  clear_status zeroes the status head on
-// the stream after every check has passed, right before the launch.
+// head, a merge counter and two partial slots per CTA).  clear_status zeroes
+// the status head and the merge counters on the stream after every check has
+// passed, right before the launch.
 constexpr size_t kStatusHeadBytes = 256;
 pa_status decode_common(void* out, const void* q, const void* k_pool, const void* v_pool, const int32_t* block_tables,
                         int32_t max_blocks_per_seq, const int32_t* seq_lens, int32_t max_seq_len, int32_t num_seqs,

@@ -57,8 +57,8 @@ extern "C" pa_status pa_decode_attention_static(void* out, const void* q, const 
     // The buffer keeps the previous call's contents.  The decode checks every
     // argument first, refuses a launch whose grid needs more scratch than the
     // buffer holds (PA_ERR_WORKSPACE_TOO_SMALL, nothing enqueued), and only then
-    // zeroes the status word at the buffer's head; the partial slots are written
-    // before they are read.
+    // zeroes the status word and the merge counters at the buffer's head; the
+    // partial slots are written before they are read.
     s = pa::decode_common(out, q, k_pool, v_pool, block_tables, max_blocks_per_seq, seq_lens, max_seq_len, num_seqs,
                           num_q_heads, num_kv_heads, head_dim, block_size, num_blocks, scale, partition_tokens, ws,
                           kStaticWorkspaceBytes, dtype, 1.f, 1.f, stream, /*clear_status=*/true);

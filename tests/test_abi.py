@@ -76,3 +76,13 @@ def test_wait_limit_knob_checks_its_argument():
     with pytest.raises(pa.PAError):
         pa.pa_debug_set_wait_limit_ns(3_000_000_000)
     pa.pa_debug_set_wait_limit_ns(0)
+
+
+def test_merge_mode_knob_checks_its_argument():
+    import pytest
+    import paged_kv_cache_280_gb300 as pa
+
+    for bad in (-1, 3):
+        with pytest.raises(pa.PAError):
+            pa.pa_debug_set_merge_mode(bad)
+    pa.pa_debug_set_merge_mode(pa.MERGE_AUTO)

@@ -53,9 +53,10 @@ def test_tiny_fp32_workload():
     assert err <= 1e-5 and status_word(ws) == 0
 
 
+@pytest.mark.parametrize("merge", [1, 2])  # in the decode kernel; by the merge kernel
 @pytest.mark.parametrize("partition_tokens", [0, 16, 32, 64, 2048])
 @pytest.mark.parametrize("ctas", [1, 2, 5, 8])
-def test_split_modes_and_grid_sizes(partition_tokens, ctas):
+def test_split_modes_and_grid_sizes(partition_tokens, ctas, merge):
     import paged_kv_cache_280_gb300 as pa
 
     w = W.random_case(7, 9, 16, 2, 128, 16, "bf16", max_len=2500, min_len=1)
@@ -63,6 +64,7 @@ def test_split_modes_and_grid_sizes(partition_tokens, ctas):
     ref = c.oracle()
     try:
         pa.pa_decode_set_ctas_per_sm(ctas)
+        pa.pa_debug_set_merge_mode(merge)
         ws = c.run(partition_tokens=partition_tokens)
         first = to_numpy(c.dout).copy()
         c.dout.fill_(float("nan"))
@@ -70,7 +72,55 @@ def test_split_modes_and_grid_sizes(partition_tokens, ctas):
         assert np.array_equal(first, to_numpy(c.dout))  # deterministic merge order, every row rewritten
     finally:
         pa.pa_decode_set_ctas_per_sm(0)
+        pa.pa_debug_set_merge_mode(0)
     check_close(first, ref, "bf16")
+    # every merge counter (one int32 per CTA after the 256-byte status head) is back at zero
+    import torch
+
+    ctas = 8 * torch.cuda.get_device_properties(0).multi_processor_count
+    assert not to_numpy(ws[256:256 + 4 * ctas].view(torch.int32)).any()
+
+
+def test_kernels_per_call_follows_the_merge_mode():
+    """Fixed partitions and fp32 pools merge with the second kernel; the testing knob forces either mode
+    where both are built; many segments per CTA merge in the decode kernel."""
+    import paged_kv_cache_280_gb300 as pa
+
+    assert pa.pa_decode_kernels_per_call(4, 64, 8, 128, 16, 8192, 2048, pa.PA_BF16) == 2
+    assert pa.pa_decode_kernels_per_call(64, 16, 4, 128, 16, 64, 0, pa.PA_F32) == 2
+    assert pa.pa_decode_kernels_per_call(256, 32, 32, 128, 16, 64, 0, pa.PA_BF16) == 1  # 8192 segments
+    try:
+        for mode, want in ((1, 1), (2, 2)):
+            pa.pa_debug_set_merge_mode(mode)
+            assert pa.pa_decode_kernels_per_call(64, 32, 8, 128, 16, 64, 0, pa.PA_BF16) == want
+            assert pa.pa_decode_kernels_per_call(64, 32, 8, 128, 16, 64, 0, pa.PA_F32) == 2
+    finally:
+        pa.pa_debug_set_merge_mode(0)
+
+
+@pytest.mark.parametrize("dtype,hq,hkv,d,bs", [("bf16", 32, 8, 128, 16), ("bf16", 8, 8, 128, 16),
+                                               ("bf16", 16, 2, 64, 32), ("f32", 8, 2, 128, 16)])
+def test_merge_modes_agree_bit_for_bit(dtype, hq, hkv, d, bs):
+    """The in-kernel merge (by whichever CTA completes a segment, mid-range or after its range)
+    and the merge kernel fold the pieces in the same order with the same arithmetic."""
+    import paged_kv_cache_280_gb300 as pa
+
+    w = W.random_case(41 + hq, 40, hq, hkv, d, bs, dtype, max_len=1500, min_len=1)
+    c = DecodeCase(w).device()
+    outs = []
+    try:
+        pa.pa_decode_set_ctas_per_sm(8)
+        for mode in (1, 2, 1):
+            pa.pa_debug_set_merge_mode(mode)
+            c.dout.fill_(float("nan"))
+            ws = c.run()
+            outs.append(to_numpy(c.dout).copy())
+            assert status_word(ws) == 0
+    finally:
+        pa.pa_decode_set_ctas_per_sm(0)
+        pa.pa_debug_set_merge_mode(0)
+    assert np.array_equal(outs[0], outs[1]) and np.array_equal(outs[0], outs[2])
+    check_close(outs[0], c.oracle(), dtype)
 
 
 def test_more_ctas_than_tiles():
@@ -80,8 +130,9 @@ def test_more_ctas_than_tiles():
     check_close(to_numpy(c.dout), c.oracle(), "f32")
 
 
+@pytest.mark.parametrize("merge", [1, 2])
 @pytest.mark.parametrize("dtype,hq,hkv,d,bs", [("bf16", 8, 2, 128, 16), ("f32", 2, 2, 64, 16)])
-def test_empty_ranges_and_long_merges(dtype, hq, hkv, d, bs):
+def test_empty_ranges_and_long_merges(dtype, hq, hkv, d, bs, merge):
     """Runs of empty sequences between long ones, at 8 CTAs per SM over a few hundred
     tiles.  Without partitions the ranges balance tiles plus a fixed cost per segment, so
     ranges that fall in the gap before a segment are empty; long segments split into
@@ -95,6 +146,7 @@ def test_empty_ranges_and_long_merges(dtype, hq, hkv, d, bs):
     ref = c.oracle()
     try:
         pa.pa_decode_set_ctas_per_sm(8)
+        pa.pa_debug_set_merge_mode(merge)
         ws = c.run()
         first = to_numpy(c.dout).copy()
         c.dout.fill_(float("nan"))
@@ -102,6 +154,7 @@ def test_empty_ranges_and_long_merges(dtype, hq, hkv, d, bs):
         assert np.array_equal(first, to_numpy(c.dout))
     finally:
         pa.pa_decode_set_ctas_per_sm(0)
+        pa.pa_debug_set_merge_mode(0)
     check_close(first, ref, dtype)
     assert status_word(ws) == 0
     assert not first[lens == 0].any()

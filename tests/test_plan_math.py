@@ -3,9 +3,12 @@ weighted unit K t + A (Hkv b + h + 1); CTA c takes units [ceil(cU/C), ceil((c+1)
 partition size, ranges end on partition multiples), re-enacted in integers on random batches.
 Checks the properties the kernels rely on: every tile has exactly one owner and cta_of agrees with
 the range starts; no range is empty between two tiles of one segment, so a split segment's pieces
-come from consecutive CTAs; and the CTA boundaries that fall strictly inside a segment, taken at
-the first one, name every split segment exactly once (the merge kernel's work items).  The GPU
-parity tests check the kernels themselves."""
+come from consecutive CTAs; and the counting merge: each CTA walks its range as pieces, and every
+piece of a split segment names the same first CTA ca and piece count np, ca names no other split
+segment (its counter is the segment's), the pieces come one from each CTA ca .. ca + np - 1 (so
+the count reaches np exactly once), and a CTA's pieces use its partial slots as the kernel's slot
+rule says (slot 0 only by the range's first piece, slot 1 only by its last).  The GPU parity tests
+check the kernels themselves."""
 import random
 
 
@@ -104,22 +107,34 @@ def _check(lens_blocks, Hkv, C, PT):
             assert sorted(set(owners)) == list(range(ca, cb + 1))  # consecutive, none skipped
             if ca != cb:
                 split.add((b, h, ca, cb - ca + 1))
-    named = []
-    for c in range(1, P["C"]):
-        t = starts[c]
-        if t >= P["T"]:
-            continue
-        b = P["find_seq"](P["pref"], t)
-        nb = P["nbk"](b)
-        local = t - Hkv * P["pref"][b]
-        h, j = local // nb, local % nb
-        if j == 0:
-            continue
-        ca = P["cta_of"](t - j)
-        if ca != c - 1:
-            continue
-        named.append((b, h, ca, P["cta_of"](t - j + nb - 1) - ca + 1))
-    assert len(named) == len(set(named)) and set(named) == split
+    counters = {}
+    for c in range(P["C"]):
+        t, t_end = starts[c], starts[c + 1]
+        slots = []
+        while t < t_end:  # the kernel's piece walk
+            b = P["find_seq"](P["pref"], t)
+            nb = P["nbk"](b)
+            local = t - Hkv * P["pref"][b]
+            h, j0 = local // nb, local % nb
+            j1 = min(nb, j0 + (t_end - t))
+            if not (j0 == 0 and j1 == nb):
+                s0 = P["seg_start"](b, h)
+                ca = P["cta_of"](s0)
+                np_ = P["cta_of"](s0 + nb - 1) - ca + 1
+                slot = 0 if j0 > 0 else 1
+                assert t == starts[c] if slot == 0 else t + (j1 - j0) == t_end
+                slots.append(slot)
+                counters.setdefault(ca, []).append((b, h, np_, c))
+            t += j1 - j0
+        assert len(slots) == len(set(slots))
+    merged = set()
+    for ca, pieces in counters.items():
+        assert len({(b, h) for b, h, _, _ in pieces}) == 1  # one split segment per counter
+        b, h, np_, _ = pieces[0]
+        assert all(x[2] == np_ for x in pieces) and len(pieces) == np_ >= 2
+        assert sorted(x[3] for x in pieces) == list(range(ca, ca + np_))
+        merged.add((b, h, ca, np_))
+    assert merged == split
 
 
 def test_plan_properties_on_random_batches():
