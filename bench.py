@@ -471,7 +471,8 @@ class DecodeSetup:
         tokens = int(np.sum(self.lens, dtype=np.int64))
         ctas, stages, smem, mma = self.pa.pa_decode_launch_info(self.B, self.Hq, self.Hkv, self.D, self.bs, self.max_blocks,
                                                                 self.pa.PA_FP8_E4M3 if self.fp8 else
-                                                                (self.pa.PA_F32 if self.w.dtype == "f32" else self.pa.PA_BF16))
+                                                                (self.pa.PA_F32 if self.w.dtype == "f32" else self.pa.PA_BF16),
+                                                                partition_tokens=self.PT)
         d = {
             "workload": self.w.name + ("_fp8kv" if self.fp8 else ""), "dtype": self.w.dtype,
             "kv_tokens_per_step": tokens, "decode_bytes_per_step": dbytes,
@@ -499,6 +500,7 @@ def run_ours(args, rank, world, local_rank):
     K, Wm = args.steps, args.warmup
     K_e2e = args.e2e_steps
     pa.pa_debug_set_merge_mode(args.merge_mode)
+    pa.pa_decode_set_ctas_per_sm(args.ctas_per_sm)
     S = DecodeSetup(args.workload, args, rank, world, dev, pa, K_e2e)
     w, B, Hq, Hkv, D, bs = S.w, S.B, S.Hq, S.Hkv, S.D, S.bs
     fp8, ids, lib, max_blocks, out = S.fp8, S.ids, S.lib, S.max_blocks, S.out
@@ -525,7 +527,8 @@ def run_ours(args, rank, world, local_rank):
     achieved = dbytes / dec_mean_s / 1e9
     ctas, stages, smem, mma = pa.pa_decode_launch_info(B, Hq, Hkv, D, bs, max_blocks,
                                                        pa.PA_FP8_E4M3 if fp8 else
-                                                       (pa.PA_F32 if w.dtype == "f32" else pa.PA_BF16))
+                                                       (pa.PA_F32 if w.dtype == "f32" else pa.PA_BF16),
+                                                       partition_tokens=S.PT)
 
     # ---- e2e: genuine decode steps through the public API with host buffers ----
     # Each step's inputs travel in one pinned staging buffer, copied to the device
@@ -1154,6 +1157,8 @@ def main(argv=None):
                     help="decode path: pool element type (fp8: E4M3 codes with per-pool scales, bf16 queries)")
     ap.add_argument("--prefix-cached", action="store_true",
                     help="prefill path: the prompts share all but their last 7 tokens, already cached")
+    ap.add_argument("--ctas-per-sm", type=int, default=0,
+                    help="decode path: CTAs per SM of the decode grid (0: the per-path default); a comparison aid")
     ap.add_argument("--merge-mode", type=int, choices=[0, 1, 2], default=0,
                     help="decode path: where split segments are merged (0: chosen per call, 1: in the decode "
                          "kernel, 2: by the merge kernel); a comparison aid")

@@ -212,11 +212,14 @@ pa_status pa_decode_attention_static(void* out, const void* q, const void* k_poo
  * (no launch): CTAs in the grid, pipeline stages per CTA (on the tensor-core
  * path at block size 16 a stage holds two blocks' tiles), dynamic shared
  * memory per CTA in bytes, and 1 if the tensor-core (mma) path is used, else
- * 0 (CUDA-core FMA path).  Any output pointer may be NULL.
+ * 0 (CUDA-core FMA path).  max_blocks_per_seq bounds the blocks of every
+ * sequence; partition_tokens is as for pa_decode_attention (the build and the
+ * grid can depend on it).  Any output pointer may be NULL.
  */
 pa_status pa_decode_launch_info(int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
-                                int32_t block_size, int32_t max_blocks_per_seq, pa_dtype dtype, int32_t* ctas,
-                                int32_t* stages, int32_t* smem_bytes, int32_t* uses_mma);
+                                int32_t block_size, int32_t max_blocks_per_seq, int32_t partition_tokens,
+                                pa_dtype dtype, int32_t* ctas, int32_t* stages, int32_t* smem_bytes,
+                                int32_t* uses_mma);
 
 /*
  * Kernels one pa_decode_attention (or _fp8, _static) call with these shapes

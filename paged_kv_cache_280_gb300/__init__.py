@@ -58,7 +58,7 @@ _SIGS = {
                                    _f32, _i32, _vp, _sz, _i32, _vp]),
     "pa_decode_attention_static": (_i32, [_vp, _vp, _vp, _vp, _vp, _i32, _vp, _i32, _i32, _i32, _i32, _i32, _i32,
                                           _i32, _f32, _i32, _i32, _vp, _vp]),
-    "pa_decode_launch_info": (_i32, [_i32, _i32, _i32, _i32, _i32, _i32, _i32, _pi32, _pi32, _pi32, _pi32]),
+    "pa_decode_launch_info": (_i32, [_i32, _i32, _i32, _i32, _i32, _i32, _i32, _i32, _pi32, _pi32, _pi32, _pi32]),
     "pa_decode_kernels_per_call": (_i32, [_i32, _i32, _i32, _i32, _i32, _i32, _i32, _i32, _pi32]),
     "pa_seq_create_cached": (_i32, [_vp, _i64, _vp, _i32, _pi32]),
     "pa_seq_cache_prefix": (_i32, [_vp, _i64, _vp, _i32]),
@@ -217,11 +217,12 @@ def pa_decode_attention_static(out, q, k_pool, v_pool, block_tables, seq_lens, m
         "pa_decode_attention_static")
 
 
-def pa_decode_launch_info(num_seqs, num_q_heads, num_kv_heads, head_dim, block_size, max_blocks_per_seq, dtype):
-    """(ctas, stages, smem_bytes, uses_mma) for these shapes on the current device; dtype is PA_F32/PA_BF16."""
+def pa_decode_launch_info(num_seqs, num_q_heads, num_kv_heads, head_dim, block_size, max_blocks_per_seq, dtype,
+                          partition_tokens=0):
+    """(ctas, stages, smem_bytes, uses_mma) of a decode call with these shapes on the current device."""
     vals = [_i32(0) for _ in range(4)]
     _ok(_lib.pa_decode_launch_info(num_seqs, num_q_heads, num_kv_heads, head_dim, block_size, max_blocks_per_seq,
-                                   dtype, *[ctypes.byref(v) for v in vals]),
+                                   int(partition_tokens), dtype, *[ctypes.byref(v) for v in vals]),
         "pa_decode_launch_info")
     return tuple(int(v.value) for v in vals)
 

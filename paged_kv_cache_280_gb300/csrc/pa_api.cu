@@ -233,13 +233,15 @@ pa_status check_shapes(int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_hea
     return PA_OK;
 }
 
-// Picks the compiled variant and the grid for these shapes on the current device.
+// Picks the compiled variant, the build and the grid for these shapes on the current device.
 struct LaunchPlan {
     DecodeVariant v;
     bool mma;
     int smem;
     int grid;
     int sms;
+    int stages;
+    int threads;
     int merge_smem;
     int merge_grid;
     bool merge_in_kernel;
@@ -258,29 +260,34 @@ pa_status plan_launch(int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_head
                  : lp->mma              ? decode_variant_bf16_mma(head_dim, block_size, &lp->v)
                                         : decode_variant_bf16_fma(head_dim, block_size, G, &lp->v);
     if (!found) return PA_ERR_UNSUPPORTED;
-    lp->smem = lp->v.smem_bytes(num_seqs, fixed);
-    if (lp->smem > kMaxSmem) return PA_ERR_UNSUPPORTED;
-    // (both builds get the shared-memory attribute; the grid fits either)
-    int occ = 0, occ_mk = 0;
-    if (!kernel_occupancy(dev, lp->v.kernel, lp->v.threads, lp->smem, &occ) ||
-        !kernel_occupancy(dev, lp->v.kernel_mk, lp->v.threads, lp->smem, &occ_mk))
-        return PA_ERR_CUDA;
-    if (occ_mk < occ) occ = occ_mk;
-    if (occ <= 0) return PA_ERR_UNSUPPORTED;
-    // Default: the bf16 tensor-core path, which spends little time per tile,
-    // keeps four CTAs per SM (about 128 KB of tiles in flight, enough to cover
-    // HBM latency with fewer split points); the CUDA-core path and the FP8
-    // tensor-core path (which widens every stage first) take as many as fit.
+    // Default CTAs per SM: the bf16 tensor-core path, which spends little time per tile,
+    // keeps four (about 128 KB of tiles in flight, enough to cover HBM latency with fewer
+    // split points); the CUDA-core path and the FP8 tensor-core path (which widens every
+    // stage first) take as many as fit.
     int want = g_ctas_per_sm.load();
     if (want <= 0) want = lp->mma && dtype == PA_BF16 ? kDefaultCtasPerSmMma : kMaxCtasPerSm;
-    const int per_sm = occ < want ? occ : want;
-    int64_t grid = (int64_t)lp->sms * per_sm;
     const int64_t tiles_bound = (int64_t)num_seqs * num_kv_heads * max_tiles_per_head;
-    if (grid > tiles_bound) grid = tiles_bound;
-    if (grid < 1) grid = 1;
-    lp->grid = (int)grid;
-    // the merge kernel: a group of min(32, G D / 16) lanes per CTA boundary (at
-    // most one split segment each), at most one CTA per SM
+    struct Shape {
+        int smem, per_sm, grid;
+    };
+    auto shape_of = [&](const DecodeBuild& b, Shape* sh) -> pa_status {
+        sh->smem = b.smem_bytes(num_seqs, fixed);
+        if (sh->smem > kMaxSmem) return PA_ERR_UNSUPPORTED;
+        int occ = 0;
+        if (!kernel_occupancy(dev, b.kernel, b.threads, sh->smem, &occ)) return PA_ERR_CUDA;
+        if (occ <= 0) return PA_ERR_UNSUPPORTED;
+        sh->per_sm = occ < want ? occ : want;
+        int64_t grid = (int64_t)lp->sms * sh->per_sm;
+        if (grid > tiles_bound) grid = tiles_bound;
+        sh->grid = (int)(grid < 1 ? 1 : grid);
+        return PA_OK;
+    };
+    Shape in{}, mk{};
+    pa_status st = shape_of(lp->v.in, &in);
+    if (st == PA_OK) st = shape_of(lp->v.mk, &mk);
+    if (st != PA_OK) return st;
+    // the merge kernel (with the mk build): a group of min(32, G D / 16) lanes per CTA
+    // boundary (at most one split segment each), at most one CTA per SM
     lp->merge_smem = merge_smem_bytes(num_seqs, fixed);
     if (lp->merge_smem > kMaxSmem) return PA_ERR_UNSUPPORTED;
     int mocc = 0;
@@ -288,7 +295,7 @@ pa_status plan_launch(int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_head
     if (mocc <= 0) return PA_ERR_UNSUPPORTED;
     const int lps = G * head_dim / 16 < 32 ? G * head_dim / 16 : 32;
     const int64_t groups_per_cta = (kMergeThreads / 32) * (32 / lps);
-    const int64_t merge_ctas = (grid - 1 + groups_per_cta - 1) / groups_per_cta;
+    const int64_t merge_ctas = (mk.grid - 1 + groups_per_cta - 1) / groups_per_cta;
     lp->merge_grid = (int)(merge_ctas < 1 ? 1 : merge_ctas < lp->sms ? merge_ctas : lp->sms);
     // Where split segments are merged.  merge_kernel costs the decode CTAs nothing and
     // runs its plan while they stream, but only if one of its CTAs fits on an SM beside
@@ -297,24 +304,31 @@ pa_status plan_launch(int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_head
     // piece a release fence and a count, and its merges run mid-range when CTAs hold
     // several segments each (the piece shared with the next CTA is walked first).  On
     // the HBM-bound paths (bf16) it takes over when segments outnumber CTAs 3:2, or when
-    // merge_kernel could only start once decode CTAs exit.  On the FP8 path the consumer
-    // is the bound and pays for every fence and count, so only when merge_kernel could
-    // not start early and CTAs hold at most half a segment each (the late start of
-    // merge_kernel then weighs most).  With fixed partitions (long contexts) a segment
-    // spans many CTAs and is merged after the streaming either way: merge_kernel.
-    // (Measured on GB300 on the workloads of the pages: each rule picked the faster mode
-    // or one within 0.5% of it.)
+    // merge_kernel could only start once decode CTAs exit.  Over FP8 pools the two
+    // builds differ: the in-kernel one has one consumer warp per CTA and 8 CTAs per SM,
+    // the merge-kernel one three consumer warps per CTA (the consumer is the bound);
+    // the first wins only when CTAs hold at most half a segment each (few pieces to
+    // stream per CTA, so merge_kernel's late start weighs most).  With fixed partitions
+    // (long contexts) a segment spans many CTAs and is merged after the streaming either
+    // way: merge_kernel.  (Measured on GB300 on the workloads of the pages: each rule
+    // picked the faster choice or one within 0.5 % of it.)
     int dregs = 0, mregs = 0;
-    if (!kernel_regs(lp->v.kernel_mk, &dregs) || !kernel_regs(lp->v.merge_kernel, &mregs)) return PA_ERR_CUDA;
+    if (!kernel_regs(lp->v.mk.kernel, &dregs) || !kernel_regs(lp->v.merge_kernel, &mregs)) return PA_ERR_CUDA;
     auto warp_regs = [](int r) { return (int64_t)(r * 32 + 255) / 256 * 256; };
-    const int64_t regs_used = (int64_t)per_sm * (lp->v.threads / 32) * warp_regs(dregs);
+    const int64_t regs_used = (int64_t)mk.per_sm * (lp->v.mk.threads / 32) * warp_regs(dregs);
     const bool merge_fits = regs_used + (kMergeThreads / 32) * warp_regs(mregs) <= 65536 &&
-                            (int64_t)per_sm * (lp->smem + 1024) + lp->merge_smem + 1024 <= 228 * 1024;
+                            (int64_t)mk.per_sm * (mk.smem + 1024) + lp->merge_smem + 1024 <= 228 * 1024;
     const int64_t segments = (int64_t)num_seqs * num_kv_heads;
     const int mode = g_merge_mode.load();
-    const bool auto_in_kernel = dtype == PA_FP8_E4M3 ? !merge_fits && 2 * segments < grid
-                                                     : 2 * segments >= 3 * grid || !merge_fits;
+    const bool auto_in_kernel = dtype == PA_FP8_E4M3 ? 2 * segments < in.grid
+                                                     : 2 * segments >= 3 * in.grid || !merge_fits;
     lp->merge_in_kernel = lp->v.merge_in_kernel_ok && (mode == 1 || (mode == 0 && !fixed && auto_in_kernel));
+    const DecodeBuild& b = lp->merge_in_kernel ? lp->v.in : lp->v.mk;
+    const Shape& sh = lp->merge_in_kernel ? in : mk;
+    lp->smem = sh.smem;
+    lp->grid = sh.grid;
+    lp->stages = b.stages;
+    lp->threads = b.threads;
     return PA_OK;
 }
 
@@ -355,17 +369,18 @@ extern "C" pa_status pa_debug_set_wait_limit_ns(uint64_t ns) {
 
 extern "C" pa_status pa_decode_launch_info(int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads,
                                            int32_t head_dim, int32_t block_size, int32_t max_blocks_per_seq,
-                                           pa_dtype dtype, int32_t* ctas, int32_t* stages, int32_t* smem_bytes,
-                                           int32_t* uses_mma) {
+                                           int32_t partition_tokens, pa_dtype dtype, int32_t* ctas,
+                                           int32_t* stages, int32_t* smem_bytes, int32_t* uses_mma) {
     if (dtype != PA_F32 && dtype != PA_BF16 && dtype != PA_FP8_E4M3) return PA_ERR_UNSUPPORTED;
     pa_status s = check_shapes(num_seqs, num_q_heads, num_kv_heads, head_dim, block_size);
     if (s != PA_OK) return s;
-    if (max_blocks_per_seq <= 0) return PA_ERR_INVALID_ARG;
+    if (max_blocks_per_seq <= 0 || partition_tokens < 0 || partition_tokens % block_size) return PA_ERR_INVALID_ARG;
     LaunchPlan lp;
-    s = plan_launch(num_seqs, num_q_heads, num_kv_heads, head_dim, block_size, max_blocks_per_seq, false, dtype, &lp);
+    s = plan_launch(num_seqs, num_q_heads, num_kv_heads, head_dim, block_size, max_blocks_per_seq,
+                    partition_tokens > 0, dtype, &lp);
     if (s != PA_OK) return s;
     if (ctas) *ctas = lp.grid;
-    if (stages) *stages = lp.v.stages;
+    if (stages) *stages = lp.stages;
     if (smem_bytes) *smem_bytes = lp.smem;
     if (uses_mma) *uses_mma = lp.mma ? 1 : 0;
     return PA_OK;

@@ -49,9 +49,6 @@
 
 namespace pa {
 
-constexpr int kConsumerWarp = 0;
-constexpr int kProducerWarp = 1;
-constexpr int kThreads = 64;
 constexpr int kMaxGroup = 8;
 constexpr int kQSlots = 2;          // query-row slots: the producer may run this many pieces ahead
 constexpr int kMergeNowPieces = 3;  // an in-kernel merge of at most this many pieces may run mid-range
@@ -82,8 +79,11 @@ struct ElemBytes<__nv_fp8_e4m3> {  // FP8 pools (OCP E4M3 codes)
 #ifndef PA_STAGE_BYTES_FMA
 #define PA_STAGE_BYTES_FMA 16384
 #endif
-#ifndef PA_STAGE_BYTES_FP8  // tensor-core path over FP8 pools: 4 stages of codes at bs 16
-#define PA_STAGE_BYTES_FP8 16384
+#ifndef PA_STAGE_BYTES_FP8  // tensor-core path over FP8 pools, three consumer warps: 4 stages of codes
+#define PA_STAGE_BYTES_FP8 32768
+#endif
+#ifndef PA_STAGE_BYTES_FP8_ONE  // the same with one consumer warp (8 CTAs per SM): 2 stages
+#define PA_STAGE_BYTES_FP8_ONE 16384
 #endif
 constexpr int stages_for(int ring_bytes, int bs, int d, int e) {
     int n = ring_bytes / (2 * bs * d * e);
@@ -92,30 +92,44 @@ constexpr int stages_for(int ring_bytes, int bs, int d, int e) {
 
 // Shared-memory layout of one CTA.  Query-row buffers are sized for the
 // group size of the instantiation (GF > 0) or for the largest group.
-template <typename T, int D, int BS, bool MMA, int GF, typename KV = T>
+template <typename T, int D, int BS, bool MMA, int GF, typename KV = T, int NC_ = 1>
 struct Layout {
     static constexpr int E = ElemBytes<KV>::value;  // pool element bytes
     static constexpr int EQ = ElemBytes<T>::value;  // query / output element bytes
     // tiles per stage: two 16-token tiles on the tensor-core path (one handshake and one softmax
     // update per 32 tokens), one tile otherwise
     static constexpr int TPS = MMA && BS == 16 ? 2 : 1;
-    static constexpr int S = stages_for(MMA ? (E == 1 ? PA_STAGE_BYTES_FP8 : PA_STAGE_BYTES) : PA_STAGE_BYTES_FMA, BS * TPS, D, E);
+    static constexpr int S = stages_for(
+        MMA ? (E == 1 ? (NC_ > 1 ? PA_STAGE_BYTES_FP8 : PA_STAGE_BYTES_FP8_ONE) : PA_STAGE_BYTES) : PA_STAGE_BYTES_FMA,
+        BS * TPS, D, E);
+    // tensor-core path over an FP8 pool: K and V codes are widened in registers
+    static constexpr bool kF8 = MMA && E == 1;
+    // Consumer warps (warps 0 .. NC - 1; the producer is warp NC).  Over FP8 pools the consumer,
+    // which widens every code, is the bound: with NC = 3 three consumer warps take a piece's
+    // stages in turn and fold their softmax states together at the piece's end.
+    static constexpr int NC = NC_;
+    static constexpr int kThreadsCta = 32 * (NC + 1);
+    static constexpr int kProducer = NC;  // warp index
+    // CTAs per SM that the register budget is planned for: that of 8 two-warp CTAs
+    static constexpr int kMinCtas = kMaxCtasPerSm * 64 / kThreadsCta;
     static constexpr int GN = GF > 0 ? GF : kMaxGroup;  // query rows a q slot holds
     static constexpr int kTileBytes = BS * D * E;  // K (or V) of one tile
     static constexpr int kPanels = D * E / 128;    // 128-byte column panels per row
     static constexpr int kStageBytes = 2 * TPS * kTileBytes;  // K of its tiles, then their V
     static constexpr int kQSlotBytes = GN * D * EQ;
     static constexpr int kStagesOff = 0;
-    // tensor-core path over an FP8 pool: K and V codes are widened in registers
-    static constexpr bool kF8 = MMA && E == 1;
-    static constexpr int kThreadsCta = kThreads;
     static constexpr int kQOff = kStagesOff + S * kStageBytes;
     // CUDA-core path only: fp32 query rows (pre-scaled) and one step's weights.
     static constexpr int kQfOff = kQOff + kQSlots * kQSlotBytes;
     static constexpr int kQfBytes = MMA ? 0 : GN * D * 4;
     static constexpr int kPTileOff = kQfOff + kQfBytes;
     static constexpr int kPTileBytes = MMA ? 0 : 16 * GN * 4;
-    static constexpr int kBarOff = kPTileOff + kPTileBytes;
+    // consumers 1 .. NC - 1 hand their softmax state to consumer 0 here at a piece's end:
+    // per consumer, 4 + 4 (D / 16) floats per lane, lane-minor
+    static constexpr int kCombFloats = 32 * (4 + 4 * (D / 16));
+    static constexpr int kCombOff = kPTileOff + kPTileBytes;
+    static constexpr int kCombBytes = (NC - 1) * kCombFloats * 4;
+    static constexpr int kBarOff = kCombOff + kCombBytes;
     static constexpr int kMiscOff = kBarOff + (2 * S + 2 * kQSlots) * 8;
     static constexpr int kPrefixOff = kMiscOff + 64;
     static_assert(kTileBytes % 1024 == 0, "tiles must keep 1024-byte alignment for the 128B swizzle");
@@ -282,6 +296,32 @@ __device__ __forceinline__ bool role_wait(uint32_t bar, uint32_t parity, volatil
         if ((threadIdx.x & 31) == 0) flag_status(status, PA_DEV_WAIT_TIMEOUT);
     }
     return ok;
+}
+
+// Several consumer warps share one stage ring; a stage's full barrier may only be waited on once
+// the stage before it has been taken, so that the slot's previous fill has landed (else a
+// parity wait could see the completed phase of the fill before it).  `ticket` holds the next
+// stage to take.  Warp-collective, bounded like role_wait; gives up at once after an abort.
+__device__ __forceinline__ bool ticket_wait(volatile int32_t* ticket, int32_t want, volatile int32_t* abort_flag,
+                                            int32_t* status, uint64_t limit_ns) {
+    bool ok = true;
+    if (*ticket != want) {
+        const uint64_t t0 = global_timer_ns();
+        while (*ticket != want) {
+            if (*abort_flag) {
+                ok = false;
+                break;
+            }
+            if (global_timer_ns() - t0 >= limit_ns) {
+                *abort_flag = 1;
+                if ((threadIdx.x & 31) == 0) flag_status(status, PA_DEV_WAIT_TIMEOUT);
+                ok = false;
+                break;
+            }
+            __nanosleep(32);
+        }
+    }
+    return __all_sync(0xffffffffu, ok);
 }
 
 __device__ __forceinline__ int clamp_len(int len, int max_len) { return len < 0 ? 0 : (len > max_len ? max_len : len); }
@@ -645,6 +685,38 @@ struct MmaState {
     __device__ static __forceinline__ int dim_lo(int i, int g) { return F8 ? 16 * i + 2 * g : 16 * i + g; }
     __device__ static __forceinline__ int dim_hi(int i, int g) { return F8 ? 16 * i + 2 * g + 1 : 16 * i + g + 8; }
 
+    // This lane's state as 4 + 4 MT floats at scr[f * 32 + lane] (another consumer warp of the
+    // CTA folds it in with combine(); both warps hold the same fragments in the same lanes).
+    __device__ __forceinline__ void save(float* scr, int lane) const {
+        scr[lane] = m[0];
+        scr[32 + lane] = m[1];
+        scr[64 + lane] = l[0];
+        scr[96 + lane] = l[1];
+#pragma unroll
+        for (int i = 0; i < MT; ++i)
+#pragma unroll
+            for (int j = 0; j < 4; ++j) scr[(4 + 4 * i + j) * 32 + lane] = o[i][j];
+    }
+    // Fold a saved state (same tokens' heads, other tokens) into this one: the online-softmax
+    // merge of two partial states.  A side that saw no token has m = -inf and weighs 0.
+    __device__ __forceinline__ void combine(const float* scr, int lane) {
+        const float om0 = scr[lane], om1 = scr[32 + lane];
+        const float n0 = fmaxf(m[0], om0), n1 = fmaxf(m[1], om1);
+        const float a0 = n0 == -INFINITY ? 0.f : exp2f(m[0] - n0), b0 = n0 == -INFINITY ? 0.f : exp2f(om0 - n0);
+        const float a1 = n1 == -INFINITY ? 0.f : exp2f(m[1] - n1), b1 = n1 == -INFINITY ? 0.f : exp2f(om1 - n1);
+        l[0] = l[0] * a0 + scr[64 + lane] * b0;
+        l[1] = l[1] * a1 + scr[96 + lane] * b1;
+#pragma unroll
+        for (int i = 0; i < MT; ++i) {
+            o[i][0] = o[i][0] * a0 + scr[(4 + 4 * i) * 32 + lane] * b0;
+            o[i][1] = o[i][1] * a1 + scr[(5 + 4 * i) * 32 + lane] * b1;
+            o[i][2] = o[i][2] * a0 + scr[(6 + 4 * i) * 32 + lane] * b0;
+            o[i][3] = o[i][3] * a1 + scr[(7 + 4 * i) * 32 + lane] * b1;
+        }
+        m[0] = n0;
+        m[1] = n1;
+    }
+
     // Sum the running sums over the 8 token rows (lanes with the same tig).
     __device__ __forceinline__ void finish() {
 #pragma unroll
@@ -931,9 +1003,9 @@ __device__ __forceinline__ void fence_acq_rel_gpu() { asm volatile("fence.acq_re
 // The kernel
 // ---------------------------------------------------------------------------
 // IKM: the in-kernel merge is compiled in (it runs when p.merge_in_kernel is set).
-template <typename T, int D, int BS, bool MMA, int GF, typename KV, bool IKM>
+template <typename T, int D, int BS, bool MMA, int GF, typename KV, bool IKM, int NC>
 __device__ __forceinline__ void decode_body(const DecodeParams& p, const CUtensorMap& tmap_k, const CUtensorMap& tmap_v) {
-    using L = Layout<T, D, BS, MMA, GF, KV>;
+    using L = Layout<T, D, BS, MMA, GF, KV, NC>;
     constexpr int S = L::S;
     constexpr int E = L::E;
     extern __shared__ uint8_t smem_raw[];
@@ -958,7 +1030,7 @@ __device__ __forceinline__ void decode_body(const DecodeParams& p, const CUtenso
 
     // the producer's tensor maps and cache policy, requested before the plan is known
     uint64_t policy = 0;
-    if (warp == kProducerWarp) {
+    if (warp == L::kProducer) {
         if (lane == 0) {
             prefetch_tensormap(&tmap_k);
             prefetch_tensormap(&tmap_v);
@@ -972,10 +1044,11 @@ __device__ __forceinline__ void decode_body(const DecodeParams& p, const CUtenso
         }
         for (int i = 0; i < kQSlots; ++i) {
             mbar_init(qfull_bar(i), 1);
-            mbar_init(qempty_bar(i), 1);
+            mbar_init(qempty_bar(i), L::NC);  // every consumer warp has read the rows
         }
         fence_barrier_init();
         misc[0] = 0;  // abort flag
+        misc[1] = 0;  // the next ring stage a consumer warp may take (several consumer warps)
     }
 
     scan_lengths<BS, L::kThreadsCta>(p, c == 0, pref, upref, lens_s, wsum);
@@ -999,7 +1072,7 @@ __device__ __forceinline__ void decode_body(const DecodeParams& p, const CUtenso
     // one partial slot: [G][D] unnormalised o, then [G] (m, l)
     const size_t slot_floats = partial_slot_floats(G, D);
 
-    if (warp == kProducerWarp) {
+    if (warp == L::kProducer) {
         // =========================== producer ===========================
         // (the tensor maps were prefetched at the kernel's start)
         const uint32_t q_bytes = (uint32_t)(G * D * L::EQ);
@@ -1094,14 +1167,17 @@ __device__ __forceinline__ void decode_body(const DecodeParams& p, const CUtenso
             mbar_wait(full_bar(kk % S), (kk / S) & 1);
         for (uint32_t qq = pi_issued > (uint32_t)kQSlots ? pi_issued - kQSlots : 0; qq < pi_issued; ++qq)
             mbar_wait(qfull_bar(qq % kQSlots), (qq / kQSlots) & 1);
-    } else if (warp == kConsumerWarp) {
-        // =========================== consumer ===========================
+    } else if (warp < L::NC) {
+        // =========================== consumers ===========================
+        // Consumer warp cw takes the stages kk with kk % NC == cw; at a piece's end the others
+        // hand their softmax state to consumer 0, which finishes the piece.
+        const int cw = warp;
         // `out` may be read or written by the preceding kernel on the stream: wait
         // for it before the first store (the consumer's first query wait comes
         // after the producer's own, so this costs nothing), then zero the outputs
         // of empty sequences
         pdl_wait_prerequisites();
-        for (int bb = c; bb < B; bb += C) {
+        for (int bb = c; cw == 0 && bb < B; bb += C) {
             if (pref[bb + 1] == pref[bb]) {
                 T* o = static_cast<T*>(p.out) + (size_t)bb * Hq * D;
                 for (int e = lane; e < Hq * D; e += 32) o[e] = from_float<T>(0.f);
@@ -1116,7 +1192,8 @@ __device__ __forceinline__ void decode_body(const DecodeParams& p, const CUtenso
         // kMergeNowPieces pieces): lane 0 notes (b, h, ca, np) of at most two (slot 0 and
         // slot 1) in shared memory, np = 0 for none.
         int32_t* pend = reinterpret_cast<int32_t*>(base + L::kMiscOff + 32);  // [2][4]
-        if (IKM && lane == 0) pend[3] = pend[7] = 0;
+        if (IKM && cw == 0 && lane == 0) pend[3] = pend[7] = 0;
+        float* comb = reinterpret_cast<float*>(base + L::kCombOff);
         PieceIter<IKM> it;
         it.init(P, t0, t1, ta);
         int b, h, j0, j1;
@@ -1140,8 +1217,14 @@ __device__ __forceinline__ void decode_body(const DecodeParams& p, const CUtenso
                 // halves of a 32-token tile.
                 for (int i = 0; i < ntile; i += L::TPS) {
                     const uint32_t kk = k + i / L::TPS;
+                    if (L::NC > 1 && (int)(kk % L::NC) != cw) continue;  // another consumer's stage
                     const int sidx = kk % S;
-                    const bool ok = role_wait(full_bar(sidx), (kk / S) & 1, misc, p.status, p.wait_limit_ns);
+                    bool ok = L::NC == 1 || ticket_wait(misc + 1, (int32_t)kk, misc, p.status, p.wait_limit_ns);
+                    ok = role_wait(full_bar(sidx), (kk / S) & 1, misc, p.status, p.wait_limit_ns) && ok;
+                    if (L::NC > 1) {
+                        __syncwarp();
+                        if (lane == 0) misc[1] = (int32_t)kk + 1;  // taken (or given up): the next may go
+                    }
                     if (ok) {
                         const uint32_t kb = base_s + L::kStagesOff + sidx * L::kStageBytes;
                         const uint32_t vb = kb + L::TPS * L::kTileBytes;
@@ -1163,6 +1246,19 @@ __device__ __forceinline__ void decode_body(const DecodeParams& p, const CUtenso
                     if (lane == 0 && ok) mbar_arrive(empty_bar(sidx));  // after an abort the stage stays held
                 }
                 k += (ntile + L::TPS - 1) / L::TPS;
+                if constexpr (L::NC > 1) {
+                    // consumer 0 folds in the others' states (in warp order: the same bits every call)
+                    if (cw > 0) st.save(comb + (cw - 1) * L::kCombFloats, lane);
+                    named_barrier(1, 32 * L::NC);
+                    if (cw == 0)
+#pragma unroll
+                        for (int w = 1; w < L::NC; ++w) st.combine(comb + (w - 1) * L::kCombFloats, lane);
+                    named_barrier(1, 32 * L::NC);  // the hand-over area is free again
+                    if (cw > 0) {
+                        ++pi;
+                        continue;  // consumer 0 finishes the piece
+                    }
+                }
             } else {
                 for (int i = 0; i < ntile; ++i) {
                     const uint32_t kk = k + i;
@@ -1227,7 +1323,7 @@ __device__ __forceinline__ void decode_body(const DecodeParams& p, const CUtenso
         }
         __syncwarp();
 #pragma unroll
-        for (int i = 0; i < (IKM ? 2 : 0); ++i) {
+        for (int i = 0; i < (IKM ? 2 : 0) && cw == 0; ++i) {
             const int32_t* e = pend + 4 * i;
             const int np = e[3];
             if (np == 0) continue;
@@ -1241,20 +1337,20 @@ __device__ __forceinline__ void decode_body(const DecodeParams& p, const CUtenso
 }
 
 // The two builds of the decode kernel.  With the in-kernel merge the kernel takes the
-// register budget of kMaxCtasPerSm CTAs on an SM, 128 per thread, so that the rare merge
-// path inside the piece loop does not raise the allocation of the whole kernel; without
+// register budget of kMaxCtasPerSm two-warp CTAs on an SM, 128 per thread, so that the rare
+// merge path inside the piece loop does not raise the allocation of the whole kernel; without
 // it the compiler keeps its own choice (an explicit minimum of one CTA per SM would let it
 // take up to 255).
-template <typename T, int D, int BS, bool MMA, int GF, typename KV>
-__global__ void __launch_bounds__(Layout<T, D, BS, MMA, GF, KV>::kThreadsCta, kMaxCtasPerSm)
+template <typename T, int D, int BS, bool MMA, int GF, typename KV, int NC>
+__global__ void __launch_bounds__(Layout<T, D, BS, MMA, GF, KV, NC>::kThreadsCta, Layout<T, D, BS, MMA, GF, KV, NC>::kMinCtas)
     decode_kernel_ikm(const DecodeParams p, const __grid_constant__ CUtensorMap tmap_k,
                       const __grid_constant__ CUtensorMap tmap_v) {
-    decode_body<T, D, BS, MMA, GF, KV, true>(p, tmap_k, tmap_v);
+    decode_body<T, D, BS, MMA, GF, KV, true, NC>(p, tmap_k, tmap_v);
 }
-template <typename T, int D, int BS, bool MMA, int GF, typename KV>
-__global__ void __launch_bounds__(Layout<T, D, BS, MMA, GF, KV>::kThreadsCta)
+template <typename T, int D, int BS, bool MMA, int GF, typename KV, int NC>
+__global__ void __launch_bounds__(Layout<T, D, BS, MMA, GF, KV, NC>::kThreadsCta)
     decode_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__ CUtensorMap tmap_v) {
-    decode_body<T, D, BS, MMA, GF, KV, false>(p, tmap_k, tmap_v);
+    decode_body<T, D, BS, MMA, GF, KV, false, NC>(p, tmap_k, tmap_v);
 }
 
 // ---------------------------------------------------------------------------
@@ -1320,26 +1416,30 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const DecodeParams
     }
 }
 
-// Host-side handle of one instantiation.
+// Host-side handle of one instantiation: two builds.
+//  - `in`: with the in-kernel merge, one consumer warp (bf16 and FP8 pools; fp32 pools, a
+//    reference-precision path whose loop leaves no registers to spare, have none).
+//  - `mk`: for launches that merge with merge_kernel.  On the tensor-core path the in-kernel
+//    merge's code costs the loop even when unused, so this build leaves it out; over FP8 pools,
+//    whose consumer is the bound, it has three consumer warps.  Elsewhere it is `in`.
 template <typename T, int D, int BS, bool MMA, int GF, typename KV = T>
 struct VariantOf {
-    // The in-kernel merge is built for bf16 and FP8 pools (fp32 pools, a reference-precision
-    // path whose loop leaves no registers to spare, always merge with merge_kernel).  On the
-    // tensor-core path its code costs the loop even when unused (the FP8 consumer is the
-    // bound), so launches that merge with merge_kernel take a build without it.
     static constexpr bool kIkm = !std::is_same<T, float>::value;
-    static constexpr bool kTwoBuilds = kIkm && MMA;
+    static constexpr bool kOwnMk = kIkm && MMA;
+    static constexpr int kNcMk = MMA && sizeof(KV) == 1 ? 3 : 1;
+    using LIn = Layout<T, D, BS, MMA, GF, KV, 1>;
+    using LMk = Layout<T, D, BS, MMA, GF, KV, kOwnMk ? kNcMk : 1>;
     using KernelFn = void (*)(const DecodeParams, const CUtensorMap, const CUtensorMap);
-    static constexpr KernelFn build(bool ikm) {
-        if constexpr (kIkm) {
-            if (ikm) return &decode_kernel_ikm<T, D, BS, MMA, GF, KV>;
-        }
-        if constexpr (!kIkm || kTwoBuilds) return &decode_kernel<T, D, BS, MMA, GF, KV>;
-        return nullptr;
+    static constexpr KernelFn in_kernel() {
+        if constexpr (kIkm) return &decode_kernel_ikm<T, D, BS, MMA, GF, KV, 1>;
+        else return &decode_kernel<T, D, BS, MMA, GF, KV, 1>;
     }
-    static constexpr KernelFn kIn = build(true);
-    static constexpr KernelFn kOut = kIkm && !kTwoBuilds ? kIn : build(false);
-    static int smem_bytes(int num_seqs, bool fixed) { return Layout<T, D, BS, MMA, GF, KV>::bytes(num_seqs, fixed); }
+    static constexpr KernelFn mk_kernel() {
+        if constexpr (kOwnMk) return &decode_kernel<T, D, BS, MMA, GF, KV, kNcMk>;
+        else return in_kernel();
+    }
+    static int smem_in(int num_seqs, bool fixed) { return LIn::bytes(num_seqs, fixed); }
+    static int smem_mk(int num_seqs, bool fixed) { return LMk::bytes(num_seqs, fixed); }
     // Both kernels are launched as programmatic dependents of what precedes them
     // on the stream: the decode of the preceding kernel (which may allow an early
     // start), the merge kernel (when the launch merges with it) of the decode.
@@ -1350,12 +1450,12 @@ struct VariantOf {
         attr[0].val.programmaticStreamSerializationAllowed = 1;
         cudaLaunchConfig_t cfg = {};
         cfg.gridDim = dim3(grid);
-        cfg.blockDim = dim3(Layout<T, D, BS, MMA, GF, KV>::kThreadsCta);
+        cfg.blockDim = dim3(p.merge_in_kernel ? LIn::kThreadsCta : LMk::kThreadsCta);
         cfg.dynamicSmemBytes = smem;
         cfg.stream = stream;
         cfg.attrs = attr;
         cfg.numAttrs = 1;
-        if (cudaLaunchKernelEx(&cfg, p.merge_in_kernel ? kIn : kOut, p, tk, tv) != cudaSuccess) return;
+        if (cudaLaunchKernelEx(&cfg, p.merge_in_kernel ? in_kernel() : mk_kernel(), p, tk, tv) != cudaSuccess) return;
         if (p.merge_in_kernel) return;
         cudaLaunchConfig_t mcfg = cfg;
         mcfg.gridDim = dim3(merge_grid);
@@ -1364,10 +1464,9 @@ struct VariantOf {
         cudaLaunchKernelEx(&mcfg, merge_kernel<T, D, BS>, p);
     }
     static DecodeVariant get() {
-        return DecodeVariant{reinterpret_cast<const void*>(kIn), reinterpret_cast<const void*>(kOut),
-                             reinterpret_cast<const void*>(&merge_kernel<T, D, BS>), kIkm,
-                             Layout<T, D, BS, MMA, GF, KV>::S,
-                             Layout<T, D, BS, MMA, GF, KV>::kThreadsCta, &smem_bytes, &launch};
+        return DecodeVariant{DecodeBuild{reinterpret_cast<const void*>(in_kernel()), LIn::S, LIn::kThreadsCta, &smem_in},
+                             DecodeBuild{reinterpret_cast<const void*>(mk_kernel()), LMk::S, LMk::kThreadsCta, &smem_mk},
+                             reinterpret_cast<const void*>(&merge_kernel<T, D, BS>), kIkm, &launch};
     }
 };
 

@@ -79,14 +79,19 @@ constexpr int kMergeThreads = 128;
 // clamped lengths and the scan's warp sums
 inline int merge_smem_bytes(int num_seqs, bool fixed) { return ((num_seqs + 1) * (fixed ? 2 : 1) + num_seqs + 8) * 4; }
 
-struct DecodeVariant {
-    const void* kernel;        // the build that merges in the kernel (and may also merge with merge_kernel)
-    const void* kernel_mk;     // the build launched when merge_kernel merges (may be `kernel`)
-    const void* merge_kernel;  // launched right after the decode as its programmatic dependent, when used
-    bool merge_in_kernel_ok;   // `kernel` has the in-kernel merge
+// One compiled build of the decode kernel: its threads per CTA, ring stages and shared memory.
+struct DecodeBuild {
+    const void* kernel;
     int stages;
     int threads;
     int (*smem_bytes)(int num_seqs, bool fixed);
+};
+
+struct DecodeVariant {
+    DecodeBuild in;            // merges split segments in the kernel (when merge_in_kernel_ok)
+    DecodeBuild mk;            // launched when merge_kernel merges (may be the same kernel as `in`)
+    const void* merge_kernel;  // launched right after the decode as its programmatic dependent, when used
+    bool merge_in_kernel_ok;   // `in` has the in-kernel merge
     void (*launch)(const DecodeParams& p, const CUtensorMap& tk, const CUtensorMap& tv, int grid, int smem,
                    int merge_grid, int merge_smem, cudaStream_t stream);
 };

@@ -72,7 +72,8 @@ def test_static_workspace_matches_oracle_and_regular_entry_point_twice():
 
 
 def test_static_workspace_sizes_by_the_launched_grid():
-    """The refusal follows the grid the call launches: two partial slots of G (D + 2) floats per CTA.
+    """The refusal follows the grid the call launches: per CTA a merge counter and two partial slots of
+    G (D + 2) floats, after the 256-byte status head.
 
     The widest head shape (8 query heads per KV head, d 128) at the most CTAs per SM the kernel can hold
     is checked either way: refused with PA_ERR_WORKSPACE_TOO_SMALL if its grid needs more than the static
@@ -88,7 +89,7 @@ def test_static_workspace_sizes_by_the_launched_grid():
     try:
         pa.pa_decode_set_ctas_per_sm(8)
         ctas, _, _, _ = pa.pa_decode_launch_info(B, hq, hkv, d, bs, c.max_blocks, pa.PA_BF16)
-        need = 256 + 2 * ctas * slot_bytes
+        need = 256 + -(-4 * ctas // 256) * 256 + 2 * ctas * slot_bytes
         out = torch.full_like(c.dout, float("nan"))
         args = (out, c.dq, c.dk, c.dv, c.dtables, c.dlens, int(c.lengths.max()), w.scale)
         if need > pa.STATIC_WORKSPACE_BYTES:
