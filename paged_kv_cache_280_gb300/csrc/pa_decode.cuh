@@ -948,7 +948,7 @@ __device__ __forceinline__ void store16(T* dst, const float (&a)[16], float sc) 
 // four at a time: their (m, l) loads in flight together, then XB pieces' o
 // loads at a time (XB = 4 or 1: fewer registers).  The arithmetic does not
 // depend on XB, so every merge of a segment gives the same bits.
-template <typename T, int D, int XB>
+template <typename T, int D, int XB, bool STORE = true>
 __device__ __forceinline__ void merge_pieces(const float* partials, size_t slot_floats, T* orow, int ca, int np, int G,
                                              int sl, int lps, float oscale) {
     static_assert(XB == 1 || XB == 4, "o loads in flight: 1 or 4 pieces");
@@ -1001,7 +1001,8 @@ __device__ __forceinline__ void merge_pieces(const float* partials, size_t slot_
             }
             mrun = mc;
         }
-        store16(orow + e0, a, __fdividef(oscale, lrun));  // lrun >= 1: the largest piece max weighs 1
+        if constexpr (STORE) store16(orow + e0, a, __fdividef(oscale, lrun));  // lrun >= 1: the largest piece max weighs 1
+        else asm volatile("" ::"f"(a[0]), "f"(a[15]), "f"(lrun));  // keep the dry run's arithmetic
     }
 }
 
@@ -1416,6 +1417,10 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const DecodeParams
     int c = 1 + (blockIdx.x * (kMergeThreads / 32) + (threadIdx.x >> 5)) * spw + grp;
     int b = 0, h = 0, ca = 0, np = 0;
     bool have = c < P.C && named(c, b, h, ca, np);  // the first item is found while the decode runs
+    // A dry run of the merge loop while the decode streams, over the zeroed status head and merge
+    // counters (no store): its instructions are then in this SM's caches when the grid ends.
+    if (have)
+        merge_pieces<T, D, 4, false>(reinterpret_cast<const float*>(p.merge_counts), 0, nullptr, 0, 1, 1, sl, lps, 1.f);
     pdl_wait_prerequisites();  // the decode grid has finished; its partials are in memory
     while (c < P.C) {
         if (have) {
