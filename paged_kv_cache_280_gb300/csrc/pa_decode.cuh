@@ -176,11 +176,14 @@ struct Plan {
         }
         return lo;
     }
-    // *split = the first tile of the segment the returned tile falls strictly inside, else -1
-    __device__ __forceinline__ int64_t tile_of_unit(int64_t u, int64_t* split) const {
+    // *split = the first tile of the segment the returned tile falls strictly inside, else -1;
+    // *seq = a sequence at or before the one that holds the returned tile
+    __device__ __forceinline__ int64_t tile_of_unit(int64_t u, int64_t* split, int* seq) const {
         *split = -1;
+        *seq = 0;
         if (u >= U) return T;
         int b = find_seq(upref, u);
+        *seq = b;
         int64_t local = u - (int64_t)Hkv * upref[b];
         int ub = upref[b + 1] - upref[b];
         int h = (int)(local / ub), part = (int)(local % ub);
@@ -195,8 +198,8 @@ struct Plan {
         const int h = (int)((t - (int64_t)Hkv * pref[b]) / nblocks(b));
         return (int64_t)K * t + (int64_t)A * ((int64_t)Hkv * b + h + 1);
     }
-    // the first tile at or after weighted unit x; *split as in tile_of_unit
-    __device__ __forceinline__ int64_t first_tile_at_unit(int64_t x, int64_t* split) const {
+    // the first tile at or after weighted unit x; *split and *seq as in tile_of_unit
+    __device__ __forceinline__ int64_t first_tile_at_unit(int64_t x, int64_t* split, int* seq) const {
         *split = -1;
         int lo = 0, hi = B - 1;  // largest b whose units start at or before x
         while (lo < hi) {
@@ -207,6 +210,7 @@ struct Plan {
                 hi = mid - 1;
         }
         const int b = lo, nb = nblocks(b);
+        *seq = b;
         const int64_t local = x - (int64_t)Hkv * ((int64_t)K * pref[b] + (int64_t)A * b);
         const int64_t span = (int64_t)K * nb + A;  // units of one segment of sequence b
         if (span == 0) return (int64_t)Hkv * pref[b];  // A = 0 and b empty: not reached (b is the last with its start)
@@ -216,11 +220,13 @@ struct Plan {
         return (int64_t)Hkv * pref[b] + h * nb + j;
     }
     // the first tile of CTA c's range; *split: the first tile of the segment that tile splits
-    // (it then continues the range of CTA c - 1), else -1
-    __device__ __forceinline__ int64_t cta_start(int c, int64_t* split) const {
+    // (it then continues the range of CTA c - 1), else -1; *seq: a sequence at or before the one
+    // that holds the tile (a start for the piece walk's forward search)
+    __device__ __forceinline__ int64_t cta_start(int c, int64_t* split, int* seq) const {
         *split = -1;
-        if (PT == 0) return c >= C ? T : first_tile_at_unit(div_nonneg(c * U + C - 1, C), split);
-        return tile_of_unit((int64_t)c * U / C, split);
+        *seq = 0;
+        if (PT == 0) return c >= C ? T : first_tile_at_unit(div_nonneg(c * U + C - 1, C), split, seq);
+        return tile_of_unit((int64_t)c * U / C, split, seq);
     }
     // the CTA whose range holds tile t of segment (b, h)
     __device__ __forceinline__ int cta_of_seg(int64_t t, int b, int h) const {
@@ -250,20 +256,22 @@ struct PieceIter {
     // Tile indices fit in 32 bits (the host refuses num_seqs * Hkv * max_blocks_per_seq >= 2^31),
     // so the walk uses 32-bit arithmetic: it runs before any tile is requested.
     int32_t t, t1, t0, ta;  // walking [t, t1); then [t0, ta) while ta > t0
-    int b;
-    __device__ __forceinline__ void init(const Plan& P, int64_t t0_, int64_t t1_, int64_t ta_) {
+    int b, b0;              // the walk's sequence; a sequence at or before the one holding t0
+    // seq0 / seq1: sequences at or before the ones holding t0 / the tile t1 splits
+    __device__ __forceinline__ void init(const Plan& P, int64_t t0_, int64_t t1_, int64_t ta_, int seq0, int seq1) {
         t0 = (int32_t)t0_;
         t1 = (int32_t)t1_;
         ta = ROT && ta_ > t0_ && ta_ < t1_ ? (int32_t)ta_ : t0;
         t = ta;
-        b = t < t1 ? P.find_seq(P.pref, t) : 0;
+        b0 = seq0;
+        b = ta > t0 ? seq1 : seq0;
     }
     __device__ __forceinline__ bool next(const Plan& P, int& b_out, int& h, int& j0, int& j1) {
         if (t >= t1) {
             if (!ROT || ta <= t0) return false;
             t1 = ta;  // the part before the rotated piece
             ta = t = t0;
-            b = P.find_seq(P.pref, t);
+            b = b0;
         }
         while (P.Hkv * P.pref[b + 1] <= t) ++b;
         const int nb = P.nblocks(b);
@@ -1075,9 +1083,11 @@ __device__ __forceinline__ void decode_body(const DecodeParams& p, const CUtenso
     // each warp run one each; lane 1's also gives the start of the segment the
     // range ends inside (the walk's rotation point)
     int64_t tb = 0, split = -1;
-    if (works && lane < 2) tb = P.cta_start(c + lane, &split);
+    int seqh = 0;
+    if (works && lane < 2) tb = P.cta_start(c + lane, &split, &seqh);
     const int64_t t0 = __shfl_sync(0xffffffffu, tb, 0);
     const int64_t t1 = __shfl_sync(0xffffffffu, tb, 1);
+    const int seq0 = __shfl_sync(0xffffffffu, seqh, 0), seq1 = __shfl_sync(0xffffffffu, seqh, 1);
     const bool merge_here = IKM && p.merge_in_kernel;
     const int64_t ta = __shfl_sync(0xffffffffu, merge_here ? split : -1, 1);
     const int Hq = p.num_q_heads;
@@ -1093,7 +1103,7 @@ __device__ __forceinline__ void decode_body(const DecodeParams& p, const CUtenso
         // entries of the next chunk (of this piece or of the next one) are loaded
         // before this chunk's tiles are issued, so their latency overlaps the issue.
         PieceIter<IKM> it;
-        it.init(P, t0, t1, ta);
+        it.init(P, t0, t1, ta, seq0, seq1);
         int b = 0, h = 0, j0 = 0, j1 = 0, nb_ = 0, nh = 0, nj0 = 0, nj1 = 0;
         bool have = it.next(P, b, h, j0, j1);
         bool have_next = have && it.next(P, nb_, nh, nj0, nj1);
@@ -1207,7 +1217,7 @@ __device__ __forceinline__ void decode_body(const DecodeParams& p, const CUtenso
         if (IKM && cw == 0 && lane == 0) pend[3] = pend[7] = 0;
         float* comb = reinterpret_cast<float*>(base + L::kCombOff);
         PieceIter<IKM> it;
-        it.init(P, t0, t1, ta);
+        it.init(P, t0, t1, ta, seq0, seq1);
         int b, h, j0, j1;
         while (it.next(P, b, h, j0, j1)) {
             const int qs = pi % kQSlots;
@@ -1400,7 +1410,8 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const DecodeParams
     // The segment boundary c names, if any: its sequence, KV head, first CTA and pieces.
     auto named = [&](int c, int& b, int& h, int& ca, int& np) -> bool {
         int64_t split;
-        const int64_t t = P.cta_start(c, &split);
+        int seq;
+        const int64_t t = P.cta_start(c, &split, &seq);
         if (t >= P.T) return false;
         b = P.find_seq(P.pref, t);
         const int nb = P.nblocks(b);
