@@ -252,7 +252,7 @@ def kernel_source_hash(csrc=None) -> str:
     import re
     h = hashlib.sha256()
     csrc = csrc or os.path.join(ROOT, "paged_kv_cache_280_gb300", "csrc")
-    keep = ("pa_decode", "pa_device.cuh", "pa_internal.h", "pa_api.cu")
+    keep = ("pa_decode", "pa_device.cuh", "pa_internal.h", "pa_api.cu", "pa_plan.h")
     for f in sorted(x for x in os.listdir(csrc) if x.startswith(keep) and x.endswith((".cu", ".cuh", ".h"))):
         with open(os.path.join(csrc, f), encoding="utf-8") as fh:
             code = re.sub(r"/\*.*?\*/", " ", fh.read(), flags=re.S)
@@ -377,6 +377,16 @@ class DecodeSetup:
         self.out = torch.empty_like(self.d_q)
         self.ws = torch.zeros(pa.pa_decode_workspace_bytes(B, self.Hq, self.Hkv, self.D), dtype=torch.uint8, device=dev)
         self.max_len = int(self.lens.max())
+        # the host's work plan of the decode call (built from the allocator's tables and lengths, uploaded
+        # with them), unless --no-plan
+        self.dtype_code = dt
+        self.d_plan = None
+        if not getattr(args, "no_plan", False):
+            self.d_plan = self.to_dev(self.build_plan(self.tables, self.lens, self.max_len))
+
+    def build_plan(self, tables, lens, max_len, out=None):
+        return self.pa.pa_decode_build_plan(tables, lens, max_len, self.Hq, self.Hkv, self.D, self.bs, self.PT,
+                                            self.dtype_code, out=out)
 
     def to_dev(self, a):
         import torch
@@ -392,6 +402,7 @@ class DecodeSetup:
             self.pa.pa_reshape_and_cache(kn_, vn_, self.dk, self.dv, slots_, **kw)
 
     def attend(self, q_, tables_, lens_, max_len_, **kw):
+        kw.setdefault("plan", self.d_plan)
         if self.fp8:
             self.pa.pa_decode_attention_fp8(self.out, q_, self.dk, self.dv, self.KS, self.VS, tables_, lens_, max_len_,
                                             self.w.scale, self.ws, partition_tokens=self.PT, **kw)
@@ -539,6 +550,10 @@ def run_ours(args, rank, world, local_rank):
     tdt, hdt = (torch.float32, torch.int32) if e == 4 else (torch.bfloat16, torch.int16)
     regions = [("q", B * Hq * D * e), ("kn", B * Hkv * D * e), ("vn", B * Hkv * D * e), ("slots", B * 8),
                ("pairs", B * 2 * 4), ("tables", B * max_blocks * 4), ("lens", B * 4)]
+    cap_len = max_blocks * bs  # a length bound every step's tables respect
+    use_plan = S.d_plan is not None
+    if use_plan:  # the host's work plan of each step's decode call travels with its tables
+        regions.append(("plan", pa.pa_decode_plan_bytes(B, Hq, Hkv, D, bs, max_blocks, cap_len, S.PT, S.dtype_code)))
     offs, pos = {}, 0
     for name, n in regions:
         offs[name] = (pos, n)
@@ -566,14 +581,14 @@ def run_ours(args, rank, world, local_rank):
     e_pairs = region(dev_stage, "pairs", torch.int32, (B, 2))
     e_tables = region(dev_stage, "tables", torch.int32, (B, max_blocks))
     e_lens = region(dev_stage, "lens", torch.int32, (B,))
+    e_plan = region(dev_stage, "plan", torch.int32, (-1,)) if use_plan else None
     h_out = torch.empty((B, Hq, D), dtype=hdt).pin_memory()
     ids_arr = np.asarray(ids, np.int64)
-    cap_len = max_blocks * bs  # a length bound every step's tables respect
 
     def device_step(hb, max_len_, st):
         dev_stage.copy_(hb, non_blocking=True)
         S.append(e_kn, e_vn, e_slots, stream=st)
-        S.attend(e_q, e_tables, e_lens, max_len_, stream=st)
+        S.attend(e_q, e_tables, e_lens, max_len_, stream=st, plan=e_plan)
         h_out.copy_(out.view(hdt), non_blocking=True)
 
     graphs = []
@@ -588,15 +603,18 @@ def run_ours(args, rank, world, local_rank):
         torch.cuda.synchronize()
     # numpy views of each staging buffer's allocator regions, made once
     host_views = [(region(hb, "slots", torch.int64, (B,)).numpy(), region(hb, "pairs", torch.int32, (B, 2)).numpy(),
-                   region(hb, "tables", torch.int32, (B, max_blocks)).numpy(), region(hb, "lens", torch.int32, (B,)).numpy())
+                   region(hb, "tables", torch.int32, (B, max_blocks)).numpy(), region(hb, "lens", torch.int32, (B,)).numpy(),
+                   region(hb, "plan", torch.int32, (-1,)).numpy() if use_plan else None)
                   for hb in host_stage]
 
     def host_prepare(s):
         # the allocator's step: new slots (and CoW pairs), block tables and lengths,
         # written in place into staging buffer s % 2
-        h_slots, h_pairs, h_tables, h_lens = host_views[s % n_stage]
+        h_slots, h_pairs, h_tables, h_lens, h_plan = host_views[s % n_stage]
         _, pr = lib.append_batch(ids_arr, slots_out=h_slots, pairs_out=h_pairs)
         lib.export_tables(ids_arr, max_blocks, tables_out=h_tables, lens_out=h_lens)
+        if use_plan:
+            S.build_plan(h_tables, h_lens, cap_len, out=h_plan)
         return pr, int(h_lens.sum(dtype=np.int64))
 
     def gpu_step(s, pr):
@@ -607,7 +625,7 @@ def run_ours(args, rank, world, local_rank):
             if len(pr):
                 pa.pa_copy_blocks(S.dk, S.dv, e_pairs[: len(pr)], stream=stream)
             S.append(e_kn, e_vn, e_slots, stream=stream)
-            S.attend(e_q, e_tables, e_lens, cap_len, stream=stream)
+            S.attend(e_q, e_tables, e_lens, cap_len, stream=stream, plan=e_plan)
             h_out.copy_(out.view(hdt), non_blocking=True)
 
     # The allocator runs one step ahead of the GPU, as a serving loop's scheduler does: step s+1's
@@ -1157,6 +1175,9 @@ def main(argv=None):
                     help="decode path: pool element type (fp8: E4M3 codes with per-pool scales, bf16 queries)")
     ap.add_argument("--prefix-cached", action="store_true",
                     help="prefill path: the prompts share all but their last 7 tokens, already cached")
+    ap.add_argument("--no-plan", action="store_true",
+                    help="decode path: let the decode compute its work plan on the device instead of taking the "
+                         "host-built one")
     ap.add_argument("--ctas-per-sm", type=int, default=0,
                     help="decode path: CTAs per SM of the decode grid (0: the per-path default); a comparison aid")
     ap.add_argument("--merge-mode", type=int, choices=[0, 1, 2], default=0,

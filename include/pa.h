@@ -175,6 +175,63 @@ pa_status pa_decode_attention(void* out, const void* q, const void* k_pool, cons
                               void* stream);
 
 /*
+ * A host-built work plan for one pa_decode_attention (or _fp8) call, and
+ * the calls that take it.  A decode launch first scans seq_lens into
+ * per-sequence block prefix sums, searches each CTA's range of the tile
+ * list, walks to its first piece and fetches that piece's block-table
+ * entries: four dependent steps before the first tile is requested.  The
+ * host allocator already holds every length and table entry (it exported
+ * them), so it can compute all of that; the launch then reads it in one
+ * round trip.  (The pages have no counterpart: an optimisation of the
+ * decode's start, not a change to what it computes.)
+ *
+ * pa_decode_plan_bytes: the plan's size for these shapes on the current
+ * device (it holds one 160-byte record per CTA of the launch's grid).
+ *
+ * pa_decode_build_plan: writes the plan into plan_out (host memory, 4-byte
+ * aligned, plan_bytes long) from HOST copies of block_tables
+ * ([num_seqs][max_blocks_per_seq]) and seq_lens, equal to the device copies
+ * the call will read.  max_seq_len, partition_tokens and dtype (the pool's:
+ * PA_F32, PA_BF16 or PA_FP8_E4M3) must be the call's.  Returns
+ * PA_ERR_WORKSPACE_TOO_SMALL if plan_bytes is short; out-of-range lengths are
+ * clamped as the decode clamps them (the decode still flags them).
+ *
+ * pa_decode_attention_planned / pa_decode_attention_fp8_planned: the decode
+ * calls with a device copy of that plan (4-byte aligned, plan_bytes long;
+ * shorter is PA_ERR_INVALID_ARG).  A plan whose header does not name this
+ * call's batch size, grid, KV heads, partition size, block size, length
+ * bound, table width and merge mode is ignored (the launch computes its own);
+ * a plan built from other lengths or table entries than the device copies
+ * hold gives wrong outputs: rebuild it whenever either changes.  The launch
+ * trusts a matching plan's prefix sums (only its block ids are checked, as
+ * table entries are), so a buffer not written by pa_decode_build_plan for
+ * these inputs may make it read block_tables out of range.  Everything
+ * else is as for pa_decode_attention and pa_decode_attention_fp8; the results
+ * are bit for bit those of the unplanned calls.
+ */
+pa_status pa_decode_plan_bytes(int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
+                               int32_t block_size, int32_t max_blocks_per_seq, int32_t max_seq_len,
+                               int32_t partition_tokens, pa_dtype dtype, size_t* bytes_out);
+pa_status pa_decode_build_plan(const int32_t* block_tables, int32_t max_blocks_per_seq, const int32_t* seq_lens,
+                               int32_t max_seq_len, int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads,
+                               int32_t head_dim, int32_t block_size, int32_t partition_tokens, pa_dtype dtype,
+                               void* plan_out, size_t plan_bytes);
+pa_status pa_decode_attention_planned(void* out, const void* q, const void* k_pool, const void* v_pool,
+                                      const int32_t* block_tables, int32_t max_blocks_per_seq,
+                                      const int32_t* seq_lens, int32_t max_seq_len, int32_t num_seqs,
+                                      int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
+                                      int32_t block_size, int32_t num_blocks, float scale, int32_t partition_tokens,
+                                      void* workspace, size_t workspace_bytes, pa_dtype dtype, const void* plan,
+                                      size_t plan_bytes, void* stream);
+pa_status pa_decode_attention_fp8_planned(void* out, const void* q, const void* k_pool, const void* v_pool,
+                                          float k_scale, float v_scale, const int32_t* block_tables,
+                                          int32_t max_blocks_per_seq, const int32_t* seq_lens, int32_t max_seq_len,
+                                          int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads,
+                                          int32_t head_dim, int32_t block_size, int32_t num_blocks, float scale,
+                                          int32_t partition_tokens, void* workspace, size_t workspace_bytes,
+                                          const void* plan, size_t plan_bytes, void* stream);
+
+/*
  * Paged decode attention without a caller-supplied workspace.  The pages have
  * no counterpart to this entry point: it exists for callers that cannot
  * allocate device memory, such as a plugin inside a framework that owns every

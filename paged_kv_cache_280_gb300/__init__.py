@@ -60,6 +60,13 @@ _SIGS = {
                                           _i32, _f32, _i32, _i32, _vp, _vp]),
     "pa_decode_launch_info": (_i32, [_i32, _i32, _i32, _i32, _i32, _i32, _i32, _i32, _pi32, _pi32, _pi32, _pi32]),
     "pa_decode_kernels_per_call": (_i32, [_i32, _i32, _i32, _i32, _i32, _i32, _i32, _i32, _pi32]),
+    "pa_decode_plan_bytes": (_i32, [_i32, _i32, _i32, _i32, _i32, _i32, _i32, _i32, _i32, _psz]),
+    "pa_decode_build_plan": (_i32, [_vp, _i32, _vp, _i32, _i32, _i32, _i32, _i32, _i32, _i32, _i32, _vp, _sz]),
+    "pa_decode_attention_planned": (_i32, [_vp, _vp, _vp, _vp, _vp, _i32, _vp, _i32, _i32, _i32, _i32, _i32, _i32,
+                                           _i32, _f32, _i32, _vp, _sz, _i32, _vp, _sz, _vp]),
+    "pa_decode_attention_fp8_planned": (_i32, [_vp, _vp, _vp, _vp, ctypes.c_float, ctypes.c_float, _vp, _i32, _vp,
+                                               _i32, _i32, _i32, _i32, _i32, _i32, _i32, ctypes.c_float, _i32, _vp,
+                                               _sz, _vp, _sz, _vp]),
     "pa_seq_create_cached": (_i32, [_vp, _i64, _vp, _i32, _pi32]),
     "pa_seq_cache_prefix": (_i32, [_vp, _i64, _vp, _i32]),
     "pa_prefix_cache_stats": (_i32, [_vp, _pi32, _pi32]),
@@ -185,17 +192,51 @@ def pa_decode_workspace_bytes(num_seqs, num_q_heads, num_kv_heads, head_dim) -> 
 
 
 def pa_decode_attention(out, q, k_pool, v_pool, block_tables, seq_lens, max_seq_len, scale, workspace,
-                        partition_tokens=0, stream=None):
+                        partition_tokens=0, stream=None, plan=None):
     """out/q [B][Hq][D]; pools [num_blocks][Hkv][bs][D]; block_tables int32 [B][max_blocks]; seq_lens int32 [B];
-    workspace: a zero-initialised uint8 CUDA tensor of pa_decode_workspace_bytes bytes."""
+    workspace: a zero-initialised uint8 CUDA tensor of pa_decode_workspace_bytes bytes.  plan: optional device copy
+    (int32 CUDA tensor) of a pa_decode_build_plan result for this call."""
     b, hq, d = q.shape
     nb, hkv, bs, _ = k_pool.shape
-    _ok(_lib.pa_decode_attention(_dev_ptr(out, "out"), _dev_ptr(q, "q"), _dev_ptr(k_pool, "k_pool"),
-                                 _dev_ptr(v_pool, "v_pool"), _dev_ptr(block_tables, "block_tables"),
-                                 block_tables.shape[1], _dev_ptr(seq_lens, "seq_lens"), int(max_seq_len), b, hq, hkv,
-                                 d, bs, nb, float(scale), int(partition_tokens), _dev_ptr(workspace, "workspace"),
-                                 workspace.numel() * workspace.element_size(), _dtype_code(q), _stream(stream)),
-        "pa_decode_attention")
+    args = [_dev_ptr(out, "out"), _dev_ptr(q, "q"), _dev_ptr(k_pool, "k_pool"), _dev_ptr(v_pool, "v_pool"),
+            _dev_ptr(block_tables, "block_tables"), block_tables.shape[1], _dev_ptr(seq_lens, "seq_lens"),
+            int(max_seq_len), b, hq, hkv, d, bs, nb, float(scale), int(partition_tokens),
+            _dev_ptr(workspace, "workspace"), workspace.numel() * workspace.element_size(), _dtype_code(q)]
+    if plan is None:
+        _ok(_lib.pa_decode_attention(*args, _stream(stream)), "pa_decode_attention")
+    else:
+        _ok(_lib.pa_decode_attention_planned(*args, _dev_ptr(plan, "plan"), plan.numel() * plan.element_size(),
+                                             _stream(stream)), "pa_decode_attention_planned")
+
+
+def pa_decode_plan_bytes(num_seqs, num_q_heads, num_kv_heads, head_dim, block_size, max_blocks_per_seq, max_seq_len,
+                         partition_tokens, dtype):
+    n = _sz(0)
+    _ok(_lib.pa_decode_plan_bytes(num_seqs, num_q_heads, num_kv_heads, head_dim, block_size, max_blocks_per_seq,
+                                  int(max_seq_len), int(partition_tokens), dtype, ctypes.byref(n)),
+        "pa_decode_plan_bytes")
+    return int(n.value)
+
+
+def pa_decode_build_plan(block_tables, seq_lens, max_seq_len, num_q_heads, num_kv_heads, head_dim, block_size,
+                         partition_tokens, dtype, out=None):
+    """The decode plan (int32 numpy array) from host copies of the block tables ([B][max_blocks] int32) and
+    lengths ([B] int32).  ``out``: an int32 numpy array (e.g. a view of a pinned staging buffer) to write into."""
+    import numpy as np
+
+    tables = np.ascontiguousarray(block_tables, dtype=np.int32)
+    lens = np.ascontiguousarray(seq_lens, dtype=np.int32)
+    b, mb = tables.shape
+    n = pa_decode_plan_bytes(b, num_q_heads, num_kv_heads, head_dim, block_size, mb, max_seq_len, partition_tokens,
+                             dtype)
+    if out is None:
+        out = np.empty(n // 4, dtype=np.int32)
+    if out.dtype != np.int32 or not out.flags["C_CONTIGUOUS"] or out.nbytes < n:
+        raise ValueError("pa_decode_build_plan: out must be a contiguous int32 array of pa_decode_plan_bytes bytes")
+    _ok(_lib.pa_decode_build_plan(tables.ctypes.data, mb, lens.ctypes.data, int(max_seq_len), b, num_q_heads,
+                                  num_kv_heads, head_dim, block_size, int(partition_tokens), dtype, out.ctypes.data,
+                                  out.nbytes), "pa_decode_build_plan")
+    return out
 
 
 STATIC_WORKSPACE_BYTES = 8 << 20
@@ -249,17 +290,20 @@ def pa_reshape_and_cache_fp8(k_new, v_new, k_pool, v_pool, slot_mapping, k_scale
 
 
 def pa_decode_attention_fp8(out, q, k_pool, v_pool, k_scale, v_scale, block_tables, seq_lens, max_seq_len, scale,
-                            workspace, partition_tokens=0, stream=None):
-    """Decode over FP8 pools (uint8 E4M3 codes) with bf16 q/out; K^ = code value * k_scale, V^ likewise."""
+                            workspace, partition_tokens=0, stream=None, plan=None):
+    """Decode over FP8 pools (uint8 E4M3 codes) with bf16 q/out; K^ = code value * k_scale, V^ likewise.
+    plan: as for pa_decode_attention (built with dtype PA_FP8_E4M3)."""
     b, hq, d = q.shape
     nb, hkv, bs, _ = k_pool.shape
-    _ok(_lib.pa_decode_attention_fp8(_dev_ptr(out, "out"), _dev_ptr(q, "q"), _dev_ptr(k_pool, "k_pool"),
-                                     _dev_ptr(v_pool, "v_pool"), float(k_scale), float(v_scale),
-                                     _dev_ptr(block_tables, "block_tables"), block_tables.shape[1],
-                                     _dev_ptr(seq_lens, "seq_lens"), int(max_seq_len), b, hq, hkv, d, bs, nb,
-                                     float(scale), int(partition_tokens), _dev_ptr(workspace, "workspace"),
-                                     workspace.numel() * workspace.element_size(), _stream(stream)),
-        "pa_decode_attention_fp8")
+    args = [_dev_ptr(out, "out"), _dev_ptr(q, "q"), _dev_ptr(k_pool, "k_pool"), _dev_ptr(v_pool, "v_pool"),
+            float(k_scale), float(v_scale), _dev_ptr(block_tables, "block_tables"), block_tables.shape[1],
+            _dev_ptr(seq_lens, "seq_lens"), int(max_seq_len), b, hq, hkv, d, bs, nb, float(scale),
+            int(partition_tokens), _dev_ptr(workspace, "workspace"), workspace.numel() * workspace.element_size()]
+    if plan is None:
+        _ok(_lib.pa_decode_attention_fp8(*args, _stream(stream)), "pa_decode_attention_fp8")
+    else:
+        _ok(_lib.pa_decode_attention_fp8_planned(*args, _dev_ptr(plan, "plan"), plan.numel() * plan.element_size(),
+                                                 _stream(stream)), "pa_decode_attention_fp8_planned")
 
 
 def pa_swap_out(k_pool, v_pool, blocks, k_store, v_store, status=None, stream=None):

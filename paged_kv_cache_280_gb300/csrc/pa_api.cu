@@ -7,6 +7,7 @@
 #include <mutex>
 
 #include "pa_internal.h"
+#include "pa_plan.h"
 
 namespace pa {
 namespace {
@@ -413,7 +414,7 @@ pa_status decode_common(void* out, const void* q, const void* k_pool, const void
                         int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
                         int32_t num_blocks, float scale, int32_t partition_tokens, void* workspace,
                         size_t workspace_bytes, pa_dtype dtype, float k_scale, float v_scale, void* stream,
-                        bool clear_status) {
+                        bool clear_status, const void* plan, size_t plan_bytes) {
     if (dtype != PA_F32 && dtype != PA_BF16 && dtype != PA_FP8_E4M3) return PA_ERR_UNSUPPORTED;
     pa_status s = check_shapes(num_seqs, num_q_heads, num_kv_heads, head_dim, block_size);
     if (s != PA_OK) return s;
@@ -443,6 +444,8 @@ pa_status decode_common(void* out, const void* q, const void* k_pool, const void
     // the bytes this launch touches: the status head, a merge counter and two partial slots per CTA of its grid
     const WorkspaceLayout wl = workspace_layout(num_q_heads, num_kv_heads, head_dim, lp.grid);
     if (workspace_bytes < wl.total) return PA_ERR_WORKSPACE_TOO_SMALL;
+    if (plan && ((reinterpret_cast<uintptr_t>(plan) & 3u) || plan_bytes < (size_t)plan_words(num_seqs, lp.grid) * 4))
+        return PA_ERR_INVALID_ARG;
 
     CUtensorMap tk, tv;
     int dev = 0;
@@ -475,6 +478,7 @@ pa_status decode_common(void* out, const void* q, const void* k_pool, const void
     const uint64_t lim = g_wait_limit_ns.load();
     p.wait_limit_ns = lim ? lim : kWaitLimitNs;
     p.merge_in_kernel = lp.merge_in_kernel ? 1 : 0;
+    p.plan = static_cast<const int32_t*>(plan);
     if (clear_status && cudaMemsetAsync(workspace, 0, wl.partials_off, static_cast<cudaStream_t>(stream)) != cudaSuccess)
         return PA_ERR_CUDA;
     lp.v.launch(p, tk, tv, lp.grid, lp.smem, lp.merge_grid, lp.merge_smem, static_cast<cudaStream_t>(stream));
@@ -505,4 +509,144 @@ extern "C" pa_status pa_decode_attention_fp8(void* out, const void* q, const voi
     return pa::decode_common(out, q, k_pool, v_pool, block_tables, max_blocks_per_seq, seq_lens, max_seq_len, num_seqs,
                              num_q_heads, num_kv_heads, head_dim, block_size, num_blocks, scale, partition_tokens,
                              workspace, workspace_bytes, PA_FP8_E4M3, k_scale, v_scale, stream, false);
+}
+
+namespace {
+
+// The launch a decode call with these arguments makes: its length bound, plan and grid.
+pa_status decode_shape(int32_t max_blocks_per_seq, int32_t max_seq_len, int32_t num_seqs, int32_t num_q_heads,
+                       int32_t num_kv_heads, int32_t head_dim, int32_t block_size, int32_t partition_tokens,
+                       pa_dtype dtype, int32_t* max_len_out, LaunchPlan* lp) {
+    if (dtype != PA_F32 && dtype != PA_BF16 && dtype != PA_FP8_E4M3) return PA_ERR_UNSUPPORTED;
+    pa_status s = check_shapes(num_seqs, num_q_heads, num_kv_heads, head_dim, block_size);
+    if (s != PA_OK) return s;
+    if (dtype == PA_FP8_E4M3 && head_dim != 128) return PA_ERR_UNSUPPORTED;
+    if (max_blocks_per_seq <= 0 || max_seq_len < 0) return PA_ERR_INVALID_ARG;
+    if (partition_tokens < 0 || (partition_tokens % block_size) != 0) return PA_ERR_INVALID_ARG;
+    if ((int64_t)num_seqs * num_kv_heads * max_blocks_per_seq >= INT32_MAX) return PA_ERR_UNSUPPORTED;
+    const int64_t table_len = (int64_t)max_blocks_per_seq * block_size;
+    const int32_t max_len = (int32_t)(max_seq_len < table_len ? max_seq_len : table_len);
+    const int32_t max_tiles = (max_len + block_size - 1) / block_size;
+    *max_len_out = max_len;
+    return plan_launch(num_seqs, num_q_heads, num_kv_heads, head_dim, block_size, max_tiles > 0 ? max_tiles : 1,
+                       partition_tokens > 0, dtype, lp);
+}
+
+}  // namespace
+
+extern "C" pa_status pa_decode_plan_bytes(int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads,
+                                          int32_t head_dim, int32_t block_size, int32_t max_blocks_per_seq,
+                                          int32_t max_seq_len, int32_t partition_tokens, pa_dtype dtype,
+                                          size_t* bytes_out) {
+    if (!bytes_out) return PA_ERR_INVALID_ARG;
+    int32_t max_len = 0;
+    LaunchPlan lp;
+    pa_status s = decode_shape(max_blocks_per_seq, max_seq_len, num_seqs, num_q_heads, num_kv_heads, head_dim,
+                               block_size, partition_tokens, dtype, &max_len, &lp);
+    if (s != PA_OK) return s;
+    *bytes_out = (size_t)plan_words(num_seqs, lp.grid) * 4;
+    return PA_OK;
+}
+
+extern "C" pa_status pa_decode_build_plan(const int32_t* block_tables, int32_t max_blocks_per_seq,
+                                          const int32_t* seq_lens, int32_t max_seq_len, int32_t num_seqs,
+                                          int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
+                                          int32_t block_size, int32_t partition_tokens, pa_dtype dtype,
+                                          void* plan_out, size_t plan_bytes) {
+    if (!block_tables || !seq_lens || !plan_out || (reinterpret_cast<uintptr_t>(plan_out) & 3u))
+        return PA_ERR_INVALID_ARG;
+    int32_t max_len = 0;
+    LaunchPlan lp;
+    pa_status s = decode_shape(max_blocks_per_seq, max_seq_len, num_seqs, num_q_heads, num_kv_heads, head_dim,
+                               block_size, partition_tokens, dtype, &max_len, &lp);
+    if (s != PA_OK) return s;
+    const int B = num_seqs, Hkv = num_kv_heads, C = lp.grid;
+    if (plan_bytes < (size_t)plan_words(B, C) * 4) return PA_ERR_WORKSPACE_TOO_SMALL;
+    int32_t* pl = static_cast<int32_t*>(plan_out);
+    const int PT = partition_tokens / block_size;
+    const int A = lp.mma ? PA_SEG_UNITS_MMA : PA_SEG_UNITS_FMA;
+    for (int w = 0; w < kPlanHeaderWords; ++w) pl[w] = 0;
+    pl[kPlanWMagic] = kPlanMagic;
+    pl[kPlanWNumSeqs] = B;
+    pl[kPlanWGrid] = C;
+    pl[kPlanWKvHeads] = Hkv;
+    pl[kPlanWPartitionTiles] = PT;
+    pl[kPlanWSegUnits] = A;
+    pl[kPlanWBlockSize] = block_size;
+    pl[kPlanWMaxLen] = max_len;
+    pl[kPlanWMergeInKernel] = lp.merge_in_kernel ? 1 : 0;
+    pl[kPlanWMaxBlocks] = max_blocks_per_seq;
+    // the lengths scan of the kernels: clamped lengths, block and partition prefix sums
+    int32_t* pref = pl + kPlanHeaderWords;
+    int32_t* upref = pref + (B + 1);
+    int32_t* lens = upref + (B + 1);
+    int32_t nb_sum = 0, np_sum = 0;
+    for (int b = 0; b < B; ++b) {
+        const int len = clamp_len(seq_lens[b], max_len);
+        const int nb = (len + block_size - 1) / block_size;
+        lens[b] = len;
+        pref[b] = nb_sum;
+        upref[b] = PT > 0 ? np_sum : 0;
+        nb_sum += nb;
+        if (PT > 0) np_sum += (nb + PT - 1) / PT;
+    }
+    pref[B] = nb_sum;
+    upref[B] = PT > 0 ? np_sum : 0;
+    const Plan P = plan_from_prefix(pref, upref, B, Hkv, PT, A, C);
+    for (int c = 0; c < C; ++c) {
+        int32_t* rec = pl + plan_rec_off(B, c);
+        for (int w = 0; w < kPlanRecWords; ++w) rec[w] = 0;
+        if (!(P.T > 0 && c < P.C)) {
+            rec[kRecTa] = -1;
+            continue;
+        }
+        int64_t s0 = -1, s1 = -1;
+        int q0 = 0, q1 = 0;
+        const int64_t t0 = P.cta_start(c, &s0, &q0), t1 = P.cta_start(c + 1, &s1, &q1);
+        const int64_t ta = lp.merge_in_kernel ? s1 : -1;
+        rec[kRecT0] = (int32_t)t0;
+        rec[kRecT1] = (int32_t)t1;
+        rec[kRecTa] = (int32_t)ta;
+        rec[kRecSeq0] = q0;
+        rec[kRecSeq1] = q1;
+        // the table entries of the first (up to) 32 tiles of the range's first piece
+        PieceIter<true> it;
+        it.init(P, t0, t1, ta, q0, q1);
+        int b = 0, h = 0, j0 = 0, j1 = 0;
+        if (it.next(P, b, h, j0, j1)) {
+            const int n = j1 - j0 < kPlanChunk ? j1 - j0 : kPlanChunk;
+            for (int l = 0; l < n; ++l) rec[kRecFirst + l] = block_tables[(size_t)b * max_blocks_per_seq + j0 + l];
+        }
+    }
+    return PA_OK;
+}
+
+extern "C" pa_status pa_decode_attention_planned(void* out, const void* q, const void* k_pool, const void* v_pool,
+                                                 const int32_t* block_tables, int32_t max_blocks_per_seq,
+                                                 const int32_t* seq_lens, int32_t max_seq_len, int32_t num_seqs,
+                                                 int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
+                                                 int32_t block_size, int32_t num_blocks, float scale,
+                                                 int32_t partition_tokens, void* workspace, size_t workspace_bytes,
+                                                 pa_dtype dtype, const void* plan, size_t plan_bytes, void* stream) {
+    if (dtype != PA_F32 && dtype != PA_BF16) return PA_ERR_UNSUPPORTED;
+    if (!plan) return PA_ERR_INVALID_ARG;
+    return pa::decode_common(out, q, k_pool, v_pool, block_tables, max_blocks_per_seq, seq_lens, max_seq_len, num_seqs,
+                             num_q_heads, num_kv_heads, head_dim, block_size, num_blocks, scale, partition_tokens,
+                             workspace, workspace_bytes, dtype, 1.f, 1.f, stream, false, plan, plan_bytes);
+}
+
+extern "C" pa_status pa_decode_attention_fp8_planned(void* out, const void* q, const void* k_pool,
+                                                     const void* v_pool, float k_scale, float v_scale,
+                                                     const int32_t* block_tables, int32_t max_blocks_per_seq,
+                                                     const int32_t* seq_lens, int32_t max_seq_len, int32_t num_seqs,
+                                                     int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
+                                                     int32_t block_size, int32_t num_blocks, float scale,
+                                                     int32_t partition_tokens, void* workspace,
+                                                     size_t workspace_bytes, const void* plan, size_t plan_bytes,
+                                                     void* stream) {
+    if (!plan) return PA_ERR_INVALID_ARG;
+    return pa::decode_common(out, q, k_pool, v_pool, block_tables, max_blocks_per_seq, seq_lens, max_seq_len, num_seqs,
+                             num_q_heads, num_kv_heads, head_dim, block_size, num_blocks, scale, partition_tokens,
+                             workspace, workspace_bytes, PA_FP8_E4M3, k_scale, v_scale, stream, false, plan,
+                             plan_bytes);
 }

@@ -46,6 +46,7 @@
 
 #include "pa_device.cuh"
 #include "pa_internal.h"
+#include "pa_plan.h"
 
 namespace pa {
 
@@ -142,152 +143,6 @@ struct Layout {
     }
 };
 
-// a / b with a 32-bit divide when both fit (the common case): the 64-bit one
-// is a long instruction sequence, and the plan runs before any tile is issued
-__device__ __forceinline__ int64_t div_nonneg(int64_t a, int64_t b) {
-    if (((uint64_t)a >> 32) == 0 && ((uint64_t)b >> 32) == 0) return (int64_t)((uint32_t)a / (uint32_t)b);
-    return a / b;
-}
-
-// Where the tiles of one CTA start and end, and who holds which partial.
-struct Plan {
-    const int32_t* pref;   // pref[b] = blocks of sequences < b (per KV head)
-    const int32_t* upref;  // same in partitions (fixed mode)
-    int32_t B, Hkv, C, PT;
-    int32_t A;     // no partitions: a tile weighs kTileUnits units, a segment A more
-    static constexpr int K = kTileUnits;
-    int64_t T, U;  // total tiles; total partitions, or total weighted units
-
-    __device__ __forceinline__ int nblocks(int b) const { return pref[b + 1] - pref[b]; }
-    __device__ __forceinline__ int64_t seg_start(int b, int h) const {
-        return (int64_t)Hkv * pref[b] + (int64_t)h * nblocks(b);
-    }
-    // largest b in [0, B) with Hkv * pre[b] <= x
-    // (Hkv * pre[b] <= Hkv * pre[B] < 2^31: tiles and partitions are counted in 32 bits; x < 2^31)
-    __device__ __forceinline__ int find_seq(const int32_t* pre, int64_t x) const {
-        const int32_t x32 = (int32_t)x;
-        int lo = 0, hi = B - 1;
-        while (lo < hi) {
-            int mid = (lo + hi + 1) >> 1;
-            if (Hkv * pre[mid] <= x32)
-                lo = mid;
-            else
-                hi = mid - 1;
-        }
-        return lo;
-    }
-    // *split = the first tile of the segment the returned tile falls strictly inside, else -1;
-    // *seq = a sequence at or before the one that holds the returned tile
-    __device__ __forceinline__ int64_t tile_of_unit(int64_t u, int64_t* split, int* seq) const {
-        *split = -1;
-        *seq = 0;
-        if (u >= U) return T;
-        int b = find_seq(upref, u);
-        *seq = b;
-        int64_t local = u - (int64_t)Hkv * upref[b];
-        int ub = upref[b + 1] - upref[b];
-        int h = (int)(local / ub), part = (int)(local % ub);
-        if (part > 0) *split = seg_start(b, h);
-        return seg_start(b, h) + (int64_t)part * PT;
-    }
-    // Weighted units (no partitions): tile t of segment (b, h) sits at unit
-    //   K t + A (Hkv b + h + 1),
-    // i.e. every segment's tiles are preceded by A units of fixed work.
-    __device__ __forceinline__ int64_t unit_of_tile(int64_t t) const {
-        const int b = find_seq(pref, t);
-        const int h = (int)((t - (int64_t)Hkv * pref[b]) / nblocks(b));
-        return (int64_t)K * t + (int64_t)A * ((int64_t)Hkv * b + h + 1);
-    }
-    // the first tile at or after weighted unit x; *split and *seq as in tile_of_unit
-    __device__ __forceinline__ int64_t first_tile_at_unit(int64_t x, int64_t* split, int* seq) const {
-        *split = -1;
-        int lo = 0, hi = B - 1;  // largest b whose units start at or before x
-        while (lo < hi) {
-            const int mid = (lo + hi + 1) >> 1;
-            if ((int64_t)Hkv * ((int64_t)K * pref[mid] + (int64_t)A * mid) <= x)
-                lo = mid;
-            else
-                hi = mid - 1;
-        }
-        const int b = lo, nb = nblocks(b);
-        *seq = b;
-        const int64_t local = x - (int64_t)Hkv * ((int64_t)K * pref[b] + (int64_t)A * b);
-        const int64_t span = (int64_t)K * nb + A;  // units of one segment of sequence b
-        if (span == 0) return (int64_t)Hkv * pref[b];  // A = 0 and b empty: not reached (b is the last with its start)
-        const int64_t h = div_nonneg(local, span), r = local - h * span;
-        const int64_t j = r <= A ? 0 : (r - A + K - 1) / K;  // at most nb: then the next segment's first tile
-        if (j > 0 && j < nb) *split = (int64_t)Hkv * pref[b] + h * nb;
-        return (int64_t)Hkv * pref[b] + h * nb + j;
-    }
-    // the first tile of CTA c's range; *split: the first tile of the segment that tile splits
-    // (it then continues the range of CTA c - 1), else -1; *seq: a sequence at or before the one
-    // that holds the tile (a start for the piece walk's forward search)
-    __device__ __forceinline__ int64_t cta_start(int c, int64_t* split, int* seq) const {
-        *split = -1;
-        *seq = 0;
-        if (PT == 0) return c >= C ? T : first_tile_at_unit(div_nonneg(c * U + C - 1, C), split, seq);
-        return tile_of_unit((int64_t)c * U / C, split, seq);
-    }
-    // the CTA whose range holds tile t of segment (b, h)
-    __device__ __forceinline__ int cta_of_seg(int64_t t, int b, int h) const {
-        if (PT == 0) return (int)div_nonneg(((int64_t)K * t + (int64_t)A * ((int64_t)Hkv * b + h + 1)) * C, U);
-        return cta_of(t);
-    }
-    // the CTA whose range holds tile t
-    __device__ __forceinline__ int cta_of(int64_t t) const {
-        if (PT == 0) return (int)(unit_of_tile(t) * C / U);
-        int b = find_seq(pref, t);
-        int64_t local = t - (int64_t)Hkv * pref[b];
-        int nb = nblocks(b), ub = upref[b + 1] - upref[b];
-        int h = (int)(local / nb), j = (int)(local % nb);
-        int64_t u = (int64_t)Hkv * upref[b] + (int64_t)h * ub + j / PT;
-        return (int)(((u + 1) * C - 1) / U);
-    }
-};
-
-// The pieces of a CTA range [t0, t1).  When the range ends inside a segment that starts inside
-// it at tile ta (the first piece of a segment split with the next CTA), the walk takes [ta, t1)
-// first and then [t0, ta): a CTA's split pieces then both come early in its range, and so does
-// the merge of a segment split between two CTAs, while the grid still streams.  (The partial
-// slots follow j0: a piece with j0 > 0 continues its segment, slot 0; a split segment's first
-// piece, slot 1.)  ROT = false: no rotation (the walk is [t0, t1) in order).
-template <bool ROT>
-struct PieceIter {
-    // Tile indices fit in 32 bits (the host refuses num_seqs * Hkv * max_blocks_per_seq >= 2^31),
-    // so the walk uses 32-bit arithmetic: it runs before any tile is requested.
-    int32_t t, t1, t0, ta;  // walking [t, t1); then [t0, ta) while ta > t0
-    int b, b0;              // the walk's sequence; a sequence at or before the one holding t0
-    // seq0 / seq1: sequences at or before the ones holding t0 / the tile t1 splits
-    __device__ __forceinline__ void init(const Plan& P, int64_t t0_, int64_t t1_, int64_t ta_, int seq0, int seq1) {
-        t0 = (int32_t)t0_;
-        t1 = (int32_t)t1_;
-        ta = ROT && ta_ > t0_ && ta_ < t1_ ? (int32_t)ta_ : t0;
-        t = ta;
-        b0 = seq0;
-        b = ta > t0 ? seq1 : seq0;
-    }
-    __device__ __forceinline__ bool next(const Plan& P, int& b_out, int& h, int& j0, int& j1) {
-        if (t >= t1) {
-            if (!ROT || ta <= t0) return false;
-            t1 = ta;  // the part before the rotated piece
-            ta = t = t0;
-            b = b0;
-        }
-        while (P.Hkv * P.pref[b + 1] <= t) ++b;
-        const int nb = P.nblocks(b);
-        const uint32_t local = (uint32_t)(t - P.Hkv * P.pref[b]);
-        h = (int)(local / (uint32_t)nb);
-        j0 = (int)(local - (uint32_t)h * (uint32_t)nb);
-        const int32_t room = t1 - t;
-        j1 = nb - j0 < room ? nb : j0 + room;
-        t += j1 - j0;
-        b_out = b;
-        return true;
-    }
-    // no piece left after the one next() returned last
-    __device__ __forceinline__ bool done() const { return t >= t1 && (!ROT || ta <= t0); }
-};
-
 // Warp-collective wait used by both roles: every lane of the warp calls it.
 // It gives up after limit_ns, or as soon as the other role has given up (the
 // CTA's abort flag): the giving-up warp flags PA_DEV_WAIT_TIMEOUT and sets the
@@ -332,7 +187,6 @@ __device__ __forceinline__ bool ticket_wait(volatile int32_t* ticket, int32_t wa
     return __all_sync(0xffffffffu, ok);
 }
 
-__device__ __forceinline__ int clamp_len(int len, int max_len) { return len < 0 ? 0 : (len > max_len ? max_len : len); }
 
 // Per-sequence blocks (and partitions) of the batch as exclusive prefix sums
 // in shared memory: pref[b] (pref[B] = the total), upref likewise in
@@ -393,35 +247,61 @@ __device__ __forceinline__ void scan_lengths(const DecodeParams& p, bool flag_ba
     }
 }
 
-// The plan of a decode launch of C CTAs over the scanned batch.  Only the first
-// min(C, T) CTAs (min(C, U) with partitions) take work.  A split segment's
-// pieces then come from consecutive CTAs, which the slot rule and the merge
-// rely on: with partitions every working CTA owns at least one; without, a
-// range is at least K units wide, so no range falls between two tiles of one
-// segment (only in the gap at a segment's start can one be empty).
-__device__ __forceinline__ Plan make_plan(const DecodeParams& p, const int32_t* pref, const int32_t* upref) {
-    Plan P;
-    const int B = p.num_seqs, Hkv = p.num_kv_heads;
-    const bool fixed = p.partition_tiles > 0;
-    P.pref = pref;
-    P.upref = upref;
-    P.B = B;
-    P.Hkv = Hkv;
-    P.PT = p.partition_tiles;
-    P.A = p.seg_units;
-    P.T = (int64_t)Hkv * pref[B];
-    P.U = fixed ? (int64_t)Hkv * upref[B] : (int64_t)P.K * P.T + (int64_t)P.A * Hkv * B;
-    const int64_t units = fixed ? P.U : P.T;
-    int64_t ce = units < (int64_t)p.num_ctas ? units : p.num_ctas;
-    if (fixed && ce > 0) {
-        // Partitions are coarse: give every working CTA the same number of them
-        // (the fewest CTAs with the same largest share), so none is left with
-        // one partition more than the rest at the end of the kernel.
-        const int64_t per = (units + ce - 1) / ce;
-        ce = (units + per - 1) / per;
+// A host-built plan (pa_decode_build_plan) for exactly this launch: its header must name the
+// same batch, grid and split parameters, else the launch computes its own.  Every thread of
+// the CTA checks the header (one cache line).
+__device__ __forceinline__ bool plan_matches(const DecodeParams& p, int bs) {
+    const int32_t* pl = p.plan;
+    if (pl == nullptr) return false;
+    return __ldg(pl + kPlanWMagic) == kPlanMagic && __ldg(pl + kPlanWNumSeqs) == p.num_seqs &&
+           __ldg(pl + kPlanWGrid) == p.num_ctas && __ldg(pl + kPlanWKvHeads) == p.num_kv_heads &&
+           __ldg(pl + kPlanWPartitionTiles) == p.partition_tiles && __ldg(pl + kPlanWSegUnits) == p.seg_units &&
+           __ldg(pl + kPlanWBlockSize) == bs && __ldg(pl + kPlanWMaxLen) == p.max_len &&
+           __ldg(pl + kPlanWMergeInKernel) == p.merge_in_kernel &&
+           __ldg(pl + kPlanWMaxBlocks) == p.max_blocks_per_seq;
+}
+// The plan's prefix sums and clamped lengths go into the shared-memory arrays the scan would
+// fill (pref[B + 1], then upref[B + 1] with partitions, then lens_s[B]).  Each of the NT threads
+// holds kPlanPass words of a pass in registers: the first pass is loaded with the plan's record
+// (plan_words_load), the later ones while the previous pass is stored.
+constexpr int kPlanPass = 8;
+template <int NT>
+__device__ __forceinline__ void plan_words_load(const DecodeParams& p, int pass, int32_t (&v)[kPlanPass]) {
+    const int n = 3 * p.num_seqs + 2;
+    const int32_t* arr = p.plan + kPlanHeaderWords;
+#pragma unroll
+    for (int u = 0; u < kPlanPass; ++u) {
+        const int w = (pass * kPlanPass + u) * NT + (int)threadIdx.x;
+        v[u] = w < n ? __ldg(arr + w) : 0;
     }
-    P.C = (int32_t)ce;
-    return P;
+}
+template <int NT>
+__device__ __forceinline__ void load_plan_arrays(const DecodeParams& p, int32_t (&v)[kPlanPass], int32_t* pref,
+                                                 int32_t* upref, int32_t* lens_s) {
+    const int B = p.num_seqs, n = 3 * B + 2;
+    const bool fixed = p.partition_tiles > 0;
+    for (int pass = 0; pass * kPlanPass * NT < n; ++pass) {
+        int32_t nv[kPlanPass];
+        plan_words_load<NT>(p, pass + 1, nv);
+#pragma unroll
+        for (int u = 0; u < kPlanPass; ++u) {
+            const int w = (pass * kPlanPass + u) * NT + (int)threadIdx.x;
+            if (w >= n) break;
+            if (w <= B)
+                pref[w] = v[u];
+            else if (w <= 2 * B + 1) {
+                if (fixed) upref[w - B - 1] = v[u];
+            } else
+                lens_s[w - 2 * B - 2] = v[u];
+        }
+#pragma unroll
+        for (int u = 0; u < kPlanPass; ++u) v[u] = nv[u];
+    }
+}
+
+// The plan of this launch over the scanned batch (pa_plan.h).
+__device__ __forceinline__ Plan make_plan(const DecodeParams& p, const int32_t* pref, const int32_t* upref) {
+    return plan_from_prefix(pref, upref, p.num_seqs, p.num_kv_heads, p.partition_tiles, p.seg_units, p.num_ctas);
 }
 
 template <typename T>
@@ -1071,7 +951,24 @@ __device__ __forceinline__ void decode_body(const DecodeParams& p, const CUtenso
         misc[1] = 0;  // the next ring stage a consumer warp may take (several consumer warps)
     }
 
-    scan_lengths<BS, L::kThreadsCta>(p, c == 0, pref, upref, lens_s, wsum);
+    // With a host-built plan the lengths scan, the range searches and the first table chunk's
+    // fetch are replaced by loads from the plan.  The host checked that the plan holds this
+    // launch's words, so the header, this CTA's record and the arrays' first pass are loaded in
+    // one round trip, before the header is compared; a plan for another launch is then unused.
+    bool planned = false;
+    int32_t rec = 0, first_chunk = 0;  // lane < 8: the CTA's record word `lane`; all: its first chunk
+    int32_t pw[kPlanPass];
+    if (p.plan != nullptr) {
+        const int32_t* r = p.plan + plan_rec_off(B, c);
+        if (lane < kRecFirst) rec = __ldg(r + lane);
+        first_chunk = __ldg(r + kRecFirst + lane);
+        plan_words_load<L::kThreadsCta>(p, 0, pw);
+        planned = plan_matches(p, BS);
+    }
+    if (planned)
+        load_plan_arrays<L::kThreadsCta>(p, pw, pref, upref, lens_s);
+    else
+        scan_lengths<BS, L::kThreadsCta>(p, c == 0, pref, upref, lens_s, wsum);
     __syncthreads();
 
     const Plan P = make_plan(p, pref, upref);
@@ -1084,12 +981,14 @@ __device__ __forceinline__ void decode_body(const DecodeParams& p, const CUtenso
     // range ends inside (the walk's rotation point)
     int64_t tb = 0, split = -1;
     int seqh = 0;
-    if (works && lane < 2) tb = P.cta_start(c + lane, &split, &seqh);
-    const int64_t t0 = __shfl_sync(0xffffffffu, tb, 0);
-    const int64_t t1 = __shfl_sync(0xffffffffu, tb, 1);
-    const int seq0 = __shfl_sync(0xffffffffu, seqh, 0), seq1 = __shfl_sync(0xffffffffu, seqh, 1);
+    if (!planned && works && lane < 2) tb = P.cta_start(c + lane, &split, &seqh);
     const bool merge_here = IKM && p.merge_in_kernel;
-    const int64_t ta = __shfl_sync(0xffffffffu, merge_here ? split : -1, 1);
+    const int64_t t0 = planned ? __shfl_sync(0xffffffffu, rec, kRecT0) : __shfl_sync(0xffffffffu, tb, 0);
+    const int64_t t1 = planned ? __shfl_sync(0xffffffffu, rec, kRecT1) : __shfl_sync(0xffffffffu, tb, 1);
+    const int seq0 = planned ? __shfl_sync(0xffffffffu, rec, kRecSeq0) : __shfl_sync(0xffffffffu, seqh, 0);
+    const int seq1 = planned ? __shfl_sync(0xffffffffu, rec, kRecSeq1) : __shfl_sync(0xffffffffu, seqh, 1);
+    const int64_t ta = planned ? __shfl_sync(0xffffffffu, rec, kRecTa)
+                               : __shfl_sync(0xffffffffu, merge_here ? split : -1, 1);
     const int Hq = p.num_q_heads;
     // one partial slot: [G][D] unnormalised o, then [G] (m, l)
     const size_t slot_floats = partial_slot_floats(G, D);
@@ -1111,7 +1010,7 @@ __device__ __forceinline__ void decode_body(const DecodeParams& p, const CUtenso
             return lane < jend - jfrom && lane < 32 ? __ldg(p.block_tables + (size_t)bb * p.max_blocks_per_seq + jfrom + lane)
                                                     : 0;
         };
-        int32_t blk_cur = have ? table_chunk(b, j0, j1) : 0;
+        int32_t blk_cur = have ? (planned ? first_chunk : table_chunk(b, j0, j1)) : 0;
         // Everything above reads only seq_lens and block_tables, which the append and
         // copy kernels of this library never write; pool and query reads wait for the
         // preceding kernel (launched as a programmatic dependent, see pa_api.cu).
@@ -1397,7 +1296,12 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const DecodeParams
     int32_t* upref = pref + (B + 1);
     int32_t* lens_s = upref + (fixed ? B + 1 : 0);
     int32_t* wsum = lens_s + B;
-    scan_lengths<BS, kMergeThreads>(p, false, pref, upref, lens_s, wsum);
+    int32_t pw[kPlanPass];
+    if (p.plan != nullptr) plan_words_load<kMergeThreads>(p, 0, pw);  // in bounds: the host checked its size
+    if (plan_matches(p, BS))  // the decode launch used the same plan
+        load_plan_arrays<kMergeThreads>(p, pw, pref, upref, lens_s);
+    else
+        scan_lengths<BS, kMergeThreads>(p, false, pref, upref, lens_s, wsum);
     __syncthreads();
     const Plan P = make_plan(p, pref, upref);
     const int lane = threadIdx.x & 31;

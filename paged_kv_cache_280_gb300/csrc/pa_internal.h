@@ -69,6 +69,9 @@ struct DecodeParams {
     // 1: split segments are merged inside the decode kernel (merge_counts); 0: by
     // merge_kernel, launched after it (the host picks per launch, see pa_api.cu)
     int32_t merge_in_kernel;
+    // a host-built plan of this launch in device memory (pa_plan.h), or null: the kernels then
+    // scan the lengths and search the CTA ranges themselves
+    const int32_t* plan;
 };
 
 // One compiled decode kernel (dtype, head_dim, block_size, compute path).
@@ -116,7 +119,7 @@ pa_status decode_common(void* out, const void* q, const void* k_pool, const void
                         int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
                         int32_t num_blocks, float scale, int32_t partition_tokens, void* workspace,
                         size_t workspace_bytes, pa_dtype dtype, float k_scale, float v_scale, void* stream,
-                        bool clear_status);
+                        bool clear_status, const void* plan = nullptr, size_t plan_bytes = 0);
 
 // Host launch helpers shared by the attention entry points (pa_api.cu).
 // The TMA map of a pool viewed as [num_blocks * Hkv * block_size][head_dim]
