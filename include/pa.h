@@ -322,6 +322,18 @@ pa_status pa_debug_set_wait_limit_ns(uint64_t ns);
 pa_status pa_debug_set_merge_mode(int32_t mode);
 
 /*
+ * Tuning aid (no counterpart on the pages): the weight of one (sequence, KV
+ * head) segment in the balance of the decode's CTA ranges, in units of which
+ * a tile weighs 4.  0 restores each compute path's own weight; 1 .. 4096 sets
+ * it for every later pa_decode_attention, pa_decode_attention_fp8,
+ * pa_decode_attention_static and pa_decode_build_plan call (a plan records
+ * the weight it was built with and is used only by calls with the same one).
+ * Results agree within rounding order.  Other values return
+ * PA_ERR_INVALID_ARG.  Process-wide.
+ */
+pa_status pa_debug_set_seg_units(int32_t units);
+
+/*
  * FP8 KV pools (an extrapolation: the pages list FP8 among the quantisation
  * formats the ecosystem supports, data.6616ai.com "PagedAttention 之外").
  * Pools hold OCP E4M3 codes (PA_FP8_E4M3, one byte per element, head_dim

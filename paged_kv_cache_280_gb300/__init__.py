@@ -83,6 +83,7 @@ _SIGS = {
     "pa_decode_set_ctas_per_sm": (_i32, [_i32]),
     "pa_debug_set_wait_limit_ns": (_i32, [ctypes.c_uint64]),
     "pa_debug_set_merge_mode": (_i32, [ctypes.c_int32]),
+    "pa_debug_set_seg_units": (_i32, [ctypes.c_int32]),
     "pa_alloc_create": (_i32, [_i32, _i32, _vp, ctypes.POINTER(_vp)]),
     "pa_alloc_destroy": (None, [_vp]),
     "pa_alloc_set_max_refcount": (_i32, [_vp, _i32]),
@@ -355,6 +356,12 @@ MERGE_AUTO, MERGE_IN_KERNEL, MERGE_KERNEL = 0, 1, 2
 def pa_debug_set_merge_mode(mode: int) -> None:
     """Testing aid: where decode calls merge split segments (MERGE_AUTO, MERGE_IN_KERNEL or MERGE_KERNEL)."""
     _ok(_lib.pa_debug_set_merge_mode(int(mode)), "pa_debug_set_merge_mode")
+
+
+def pa_debug_set_seg_units(units: int) -> None:
+    """Tuning aid: a segment's weight in the balance of the decode's CTA ranges (a tile weighs 4); 0 restores
+    each compute path's own."""
+    _ok(_lib.pa_debug_set_seg_units(int(units)), "pa_debug_set_seg_units")
 
 
 # ---------------------------------------------------------------------------

@@ -16,6 +16,7 @@ constexpr int kMaxDevices = 64;
 std::atomic<int> g_ctas_per_sm{0};  // 0 = the per-path default
 std::atomic<uint64_t> g_wait_limit_ns{0};  // 0 = kWaitLimitNs
 std::atomic<int> g_merge_mode{0};          // 0 = chosen per launch, 1 = in the decode kernel, 2 = merge_kernel
+std::atomic<int> g_seg_units{0};           // 0 = the compute path's weight of a segment, else this many units
 
 struct DeviceInfo {
     int sms = 0;
@@ -246,6 +247,7 @@ struct LaunchPlan {
     int merge_smem;
     int merge_grid;
     bool merge_in_kernel;
+    int seg_units;  // the range balance's weight of a segment (DecodeParams::seg_units)
 };
 
 pa_status plan_launch(int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
@@ -307,9 +309,10 @@ pa_status plan_launch(int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_head
     // the HBM-bound paths (bf16) it takes over when segments outnumber CTAs 3:2, or when
     // merge_kernel could only start once decode CTAs exit.  Over FP8 pools the two
     // builds differ: the in-kernel one has one consumer warp per CTA and 8 CTAs per SM,
-    // the merge-kernel one three consumer warps per CTA (the consumer is the bound);
-    // the first wins only when CTAs hold at most half a segment each (few pieces to
-    // stream per CTA, so merge_kernel's late start weighs most).  With fixed partitions
+    // the merge-kernel one three consumer warps per CTA (the consumer is the bound, and
+    // its fence and count stall the only consumer warp); with segments weighted as FP8
+    // ranges weigh them the second is faster on every workload measured, so the first
+    // is taken only when merge_kernel could not be resident.  With fixed partitions
     // (long contexts) a segment spans many CTAs and is merged after the streaming either
     // way: merge_kernel.  (Measured on GB300 on the workloads of the pages: each rule
     // picked the faster choice or one within 0.5 % of it.)
@@ -321,11 +324,15 @@ pa_status plan_launch(int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_head
                             (int64_t)mk.per_sm * (mk.smem + 1024) + lp->merge_smem + 1024 <= 228 * 1024;
     const int64_t segments = (int64_t)num_seqs * num_kv_heads;
     const int mode = g_merge_mode.load();
-    const bool auto_in_kernel = dtype == PA_FP8_E4M3 ? 2 * segments < in.grid
-                                                     : 2 * segments >= 3 * in.grid || !merge_fits;
+    const bool auto_in_kernel = dtype == PA_FP8_E4M3 ? !merge_fits : 2 * segments >= 3 * in.grid || !merge_fits;
     lp->merge_in_kernel = lp->v.merge_in_kernel_ok && (mode == 1 || (mode == 0 && !fixed && auto_in_kernel));
     const DecodeBuild& b = lp->merge_in_kernel ? lp->v.in : lp->v.mk;
     const Shape& sh = lp->merge_in_kernel ? in : mk;
+    const int su = g_seg_units.load();
+    lp->seg_units = su > 0                     ? su
+                    : dtype == PA_FP8_E4M3     ? PA_SEG_UNITS_FP8
+                    : lp->mma                  ? PA_SEG_UNITS_MMA
+                                               : PA_SEG_UNITS_FMA;
     lp->smem = sh.smem;
     lp->grid = sh.grid;
     lp->stages = b.stages;
@@ -359,6 +366,12 @@ extern "C" pa_status pa_decode_set_ctas_per_sm(int32_t ctas) {
 extern "C" pa_status pa_debug_set_merge_mode(int32_t mode) {
     if (mode < 0 || mode > 2) return PA_ERR_INVALID_ARG;
     g_merge_mode.store(mode);
+    return PA_OK;
+}
+
+extern "C" pa_status pa_debug_set_seg_units(int32_t units) {
+    if (units < 0 || units > kMaxSegUnits) return PA_ERR_INVALID_ARG;
+    g_seg_units.store(units);
     return PA_OK;
 }
 
@@ -472,7 +485,7 @@ pa_status decode_common(void* out, const void* q, const void* k_pool, const void
     p.group = num_q_heads / num_kv_heads;
     p.partition_tiles = partition_tokens / block_size;
     p.num_ctas = lp.grid;
-    p.seg_units = lp.mma ? PA_SEG_UNITS_MMA : PA_SEG_UNITS_FMA;
+    p.seg_units = lp.seg_units;
     p.scale_log2 = scale * 1.4426950408889634f * k_scale;
     p.out_scale = v_scale;
     const uint64_t lim = g_wait_limit_ns.load();
@@ -564,7 +577,7 @@ extern "C" pa_status pa_decode_build_plan(const int32_t* block_tables, int32_t m
     if (plan_bytes < (size_t)plan_words(B, C) * 4) return PA_ERR_WORKSPACE_TOO_SMALL;
     int32_t* pl = static_cast<int32_t*>(plan_out);
     const int PT = partition_tokens / block_size;
-    const int A = lp.mma ? PA_SEG_UNITS_MMA : PA_SEG_UNITS_FMA;
+    const int A = lp.seg_units;
     for (int w = 0; w < kPlanHeaderWords; ++w) pl[w] = 0;
     pl[kPlanWMagic] = kPlanMagic;
     pl[kPlanWNumSeqs] = B;

@@ -30,6 +30,11 @@ constexpr int kMaxSmem = 227 * 1024;
 // segment's fixed work in units per compute path.  Measured per-CTA loop ends
 // put a piece's fixed work near one tile of the stream on the tensor-core path
 // (4 CTAs per SM) and near half a tile on the CUDA-core path (8 CTAs per SM).
+// Over FP8 pools, where the consumer's instructions are the bound, a segment
+// (its query rows, the softmax's end, the partial store and merge count) costs
+// about six FP8 tiles: a fit of loop ends against tiles and segments per CTA
+// gave 5.8, and a sweep of the weight was fastest at 24 units on all three
+// unpartitioned workloads.
 constexpr int kTileUnits = 4;
 #ifndef PA_SEG_UNITS_MMA
 #define PA_SEG_UNITS_MMA 4
@@ -37,6 +42,10 @@ constexpr int kTileUnits = 4;
 #ifndef PA_SEG_UNITS_FMA
 #define PA_SEG_UNITS_FMA 2
 #endif
+#ifndef PA_SEG_UNITS_FP8
+#define PA_SEG_UNITS_FP8 24
+#endif
+constexpr int kMaxSegUnits = 4096;  // bound of pa_debug_set_seg_units
 
 struct DecodeParams {
     void* out;

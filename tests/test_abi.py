@@ -86,3 +86,13 @@ def test_merge_mode_knob_checks_its_argument():
         with pytest.raises(pa.PAError):
             pa.pa_debug_set_merge_mode(bad)
     pa.pa_debug_set_merge_mode(pa.MERGE_AUTO)
+
+
+def test_seg_units_knob_checks_its_argument():
+    import pytest
+    import paged_kv_cache_280_gb300 as pa
+
+    for bad in (-1, 4097):
+        with pytest.raises(pa.PAError):
+            pa.pa_debug_set_seg_units(bad)
+    pa.pa_debug_set_seg_units(0)

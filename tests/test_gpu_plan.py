@@ -4,6 +4,7 @@ plan for other shapes is ignored; the plan's own words follow from the lengths a
 import numpy as np
 import pytest
 
+import oracle
 import synth.workloads as W
 from gpu_cases import DecodeCase, check_close, status_word, to_numpy, to_torch
 from test_gpu_fp8 import _fp8_case
@@ -140,3 +141,35 @@ def test_matching_plan_is_read(dtype):
     assert not np.array_equal(base.view(np.uint8), _decode(c, pa, dtype, 0, plan=bent).view(np.uint8))
     bent[1] += 1  # another batch size in the header: the plan is not used
     assert np.array_equal(base.view(np.uint8), _decode(c, pa, dtype, 0, plan=bent).view(np.uint8))
+
+
+@pytest.mark.parametrize("units", [1, 24, 4096])
+@pytest.mark.parametrize("dtype", ["bf16", "fp8"])
+def test_segment_weight_moves_ranges_not_results(dtype, units):
+    """Another segment weight gives other CTA ranges (so other splits and merges), outputs within the
+    tolerance of the oracle's, and a plan built under it matches the unplanned call bit for bit."""
+    import paged_kv_cache_280_gb300 as pa
+
+    lens = np.asarray([700, 0, 1, 33, 1500, 16, 17, 260, 0, 999, 64, 5], np.int32)
+    hq, hkv, d, bs = 32, 8, 128, 16
+    if dtype == "fp8":
+        c = _fp8_case(73, hq, hkv, bs, lens=lens, max_len=1500)
+    else:
+        c = DecodeCase(W.random_case(73, len(lens), hq, hkv, d, bs, dtype, max_len=1500, min_len=1), lengths=lens)
+    ml = int(lens.max())
+    try:
+        pa.pa_debug_set_seg_units(units)
+        pa.pa_decode_set_ctas_per_sm(8)
+        plan = pa.pa_decode_build_plan(c.tables, c.lengths, ml, hq, hkv, d, bs, 0, _dtype_code(pa, dtype))
+        assert plan[5] == units
+        base = _decode(c, pa, dtype, 0)
+        got = _decode(c, pa, dtype, 0, plan=plan)
+    finally:
+        pa.pa_debug_set_seg_units(0)
+        pa.pa_decode_set_ctas_per_sm(0)
+    assert np.array_equal(base.view(np.uint8), got.view(np.uint8))
+    if dtype == "fp8":
+        ref = oracle.decode_attention_fp8(c.q, c.kq, c.vq, *c.scales, c.ref_tables, c.lengths, c.w.scale, threads=8)
+        check_close(got, ref, "bf16")
+    else:
+        check_close(got, c.oracle(), dtype)
