@@ -311,8 +311,9 @@ pa_status plan_launch(int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_head
     // builds differ: the in-kernel one has one consumer warp per CTA and 8 CTAs per SM,
     // the merge-kernel one three consumer warps per CTA (the consumer is the bound, and
     // its fence and count stall the only consumer warp); with segments weighted as FP8
-    // ranges weigh them the second is faster on every workload measured, so the first
-    // is taken only when merge_kernel could not be resident.  With fixed partitions
+    // ranges weigh them the second is faster on every workload measured, though its four
+    // CTAs fill an SM's registers and merge_kernel starts only as they exit, so FP8 calls
+    // always take it.  With fixed partitions
     // (long contexts) a segment spans many CTAs and is merged after the streaming either
     // way: merge_kernel.  (Measured on GB300 on the workloads of the pages: each rule
     // picked the faster choice or one within 0.5 % of it.)
@@ -324,7 +325,7 @@ pa_status plan_launch(int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_head
                             (int64_t)mk.per_sm * (mk.smem + 1024) + lp->merge_smem + 1024 <= 228 * 1024;
     const int64_t segments = (int64_t)num_seqs * num_kv_heads;
     const int mode = g_merge_mode.load();
-    const bool auto_in_kernel = dtype == PA_FP8_E4M3 ? !merge_fits : 2 * segments >= 3 * in.grid || !merge_fits;
+    const bool auto_in_kernel = dtype != PA_FP8_E4M3 && (2 * segments >= 3 * in.grid || !merge_fits);
     lp->merge_in_kernel = lp->v.merge_in_kernel_ok && (mode == 1 || (mode == 0 && !fixed && auto_in_kernel));
     const DecodeBuild& b = lp->merge_in_kernel ? lp->v.in : lp->v.mk;
     const Shape& sh = lp->merge_in_kernel ? in : mk;

@@ -89,7 +89,7 @@ def test_kernels_per_call_follows_the_merge_mode():
     assert pa.pa_decode_kernels_per_call(4, 64, 8, 128, 16, 8192, 2048, pa.PA_BF16) == 2
     assert pa.pa_decode_kernels_per_call(64, 16, 4, 128, 16, 64, 0, pa.PA_F32) == 2
     assert pa.pa_decode_kernels_per_call(256, 32, 32, 128, 16, 64, 0, pa.PA_BF16) == 1  # 8192 segments
-    # FP8 pools: the merge kernel (three consumer warps per CTA) wherever it can be resident
+    # FP8 pools: the merge kernel (the build with three consumer warps per CTA)
     assert pa.pa_decode_kernels_per_call(64, 32, 8, 128, 16, 256, 0, pa.PA_FP8_E4M3) == 2
     assert pa.pa_decode_kernels_per_call(256, 32, 32, 128, 16, 64, 0, pa.PA_FP8_E4M3) == 2
     try:
