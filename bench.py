@@ -513,6 +513,7 @@ def run_ours(args, rank, world, local_rank):
     pa.pa_debug_set_merge_mode(args.merge_mode)
     pa.pa_decode_set_ctas_per_sm(args.ctas_per_sm)
     pa.pa_debug_set_seg_units(args.seg_units)
+    pa.pa_debug_set_wave_skew(args.wave_skew)
     S = DecodeSetup(args.workload, args, rank, world, dev, pa, K_e2e)
     w, B, Hq, Hkv, D, bs = S.w, S.B, S.Hq, S.Hkv, S.D, S.bs
     fp8, ids, lib, max_blocks, out = S.fp8, S.ids, S.lib, S.max_blocks, S.out
@@ -1184,6 +1185,9 @@ def main(argv=None):
     ap.add_argument("--seg-units", type=int, default=0,
                     help="decode path: a segment's weight in the CTA range balance, a tile weighing 4 (0: the "
                          "per-path default); a comparison aid")
+    ap.add_argument("--wave-skew", type=int, default=-1,
+                    help="decode path: skew of the CTA shares by dispatch wave (-1: the per-path default, 0: "
+                         "equal shares); a comparison aid")
     ap.add_argument("--merge-mode", type=int, choices=[0, 1, 2], default=0,
                     help="decode path: where split segments are merged (0: chosen per call, 1: in the decode "
                          "kernel, 2: by the merge kernel); a comparison aid")

@@ -334,6 +334,36 @@ pa_status pa_debug_set_merge_mode(int32_t mode);
 pa_status pa_debug_set_seg_units(int32_t units);
 
 /*
+ * Tuning aid (no counterpart on the pages): the skew of the decode's CTA
+ * shares by dispatch wave.  A launch's CTAs take the SMs in waves of one per
+ * SM, and an SM's warp scheduler favours the CTAs dispatched to it first;
+ * without partitions, wave v of n then takes 64 + skew (n - 1 - 2 v) parts of
+ * the work (equal parts at skew 0; the shares stay equal whenever the lightest
+ * range would be under one tile).  -1 restores each compute path's own skew;
+ * 0 .. 8 sets it for every later decode call and pa_decode_build_plan (a plan
+ * records the skew and the wave size it was built with and is used only by
+ * calls with the same).  Results agree within rounding order.  Other values
+ * return PA_ERR_INVALID_ARG.  Process-wide.
+ */
+pa_status pa_debug_set_wave_skew(int32_t skew);
+
+/*
+ * Testing aid (no GPU needed): the decode's CTA ranges as a launch computes
+ * them, from block_counts[num_seqs] (blocks per sequence, per KV head) and the
+ * launch's grid (num_ctas), segment weight, partition size (in tiles, 0 for
+ * none), wave size and skew.  Writes the working CTAs' count to
+ * *working_ctas_out (W <= num_ctas), their range starts to starts_out[0 .. W]
+ * (tile indices; starts_out needs num_ctas + 1 entries), and, when owners_out
+ * is not null, the owning CTA of every tile (owners_cap entries at least;
+ * PA_ERR_WORKSPACE_TOO_SMALL otherwise).  Tiles are numbered sequence-major,
+ * then KV head, then block.  Bad arguments return PA_ERR_INVALID_ARG.
+ */
+pa_status pa_debug_plan_ranges(const int32_t* block_counts, int32_t num_seqs, int32_t num_kv_heads,
+                               int32_t partition_tiles, int32_t seg_units, int32_t num_ctas, int32_t wave_ctas,
+                               int32_t wave_skew, int64_t* starts_out, int32_t* owners_out, size_t owners_cap,
+                               int32_t* working_ctas_out);
+
+/*
  * FP8 KV pools (an extrapolation: the pages list FP8 among the quantisation
  * formats the ecosystem supports, data.6616ai.com "PagedAttention 之外").
  * Pools hold OCP E4M3 codes (PA_FP8_E4M3, one byte per element, head_dim

@@ -84,6 +84,8 @@ _SIGS = {
     "pa_debug_set_wait_limit_ns": (_i32, [ctypes.c_uint64]),
     "pa_debug_set_merge_mode": (_i32, [ctypes.c_int32]),
     "pa_debug_set_seg_units": (_i32, [ctypes.c_int32]),
+    "pa_debug_set_wave_skew": (_i32, [ctypes.c_int32]),
+    "pa_debug_plan_ranges": (_i32, [_vp, _i32, _i32, _i32, _i32, _i32, _i32, _i32, _vp, _vp, _sz, _vp]),
     "pa_alloc_create": (_i32, [_i32, _i32, _vp, ctypes.POINTER(_vp)]),
     "pa_alloc_destroy": (None, [_vp]),
     "pa_alloc_set_max_refcount": (_i32, [_vp, _i32]),
@@ -362,6 +364,30 @@ def pa_debug_set_seg_units(units: int) -> None:
     """Tuning aid: a segment's weight in the balance of the decode's CTA ranges (a tile weighs 4); 0 restores
     each compute path's own."""
     _ok(_lib.pa_debug_set_seg_units(int(units)), "pa_debug_set_seg_units")
+
+
+def pa_debug_plan_ranges(block_counts, num_kv_heads, partition_tiles, seg_units, num_ctas, wave_ctas, wave_skew,
+                         owners=True):
+    """Testing aid (no GPU): (range starts [W + 1] int64, owners [T] int32 or None) of a decode launch's CTA
+    ranges, W the working CTAs, from per-sequence block counts."""
+    import numpy as np
+
+    counts = np.ascontiguousarray(block_counts, dtype=np.int32)
+    starts = np.zeros(int(num_ctas) + 1, np.int64)
+    total = int(counts.sum()) * int(num_kv_heads)
+    own = np.zeros(max(total, 1), np.int32) if owners else None
+    working = ctypes.c_int32(0)
+    _ok(_lib.pa_debug_plan_ranges(counts.ctypes.data, len(counts), int(num_kv_heads), int(partition_tiles),
+                                  int(seg_units), int(num_ctas), int(wave_ctas), int(wave_skew), starts.ctypes.data,
+                                  own.ctypes.data if owners else None, own.size if owners else 0,
+                                  ctypes.byref(working)), "pa_debug_plan_ranges")
+    return starts[: working.value + 1], (own[:total] if owners else None)
+
+
+def pa_debug_set_wave_skew(skew: int) -> None:
+    """Tuning aid: the skew of the decode's CTA shares by dispatch wave (0: equal shares); -1 restores each
+    compute path's own."""
+    _ok(_lib.pa_debug_set_wave_skew(int(skew)), "pa_debug_set_wave_skew")
 
 
 # ---------------------------------------------------------------------------

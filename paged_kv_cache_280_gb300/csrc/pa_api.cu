@@ -5,6 +5,7 @@
 #include <atomic>
 #include <cmath>
 #include <mutex>
+#include <vector>
 
 #include "pa_internal.h"
 #include "pa_plan.h"
@@ -17,6 +18,7 @@ std::atomic<int> g_ctas_per_sm{0};  // 0 = the per-path default
 std::atomic<uint64_t> g_wait_limit_ns{0};  // 0 = kWaitLimitNs
 std::atomic<int> g_merge_mode{0};          // 0 = chosen per launch, 1 = in the decode kernel, 2 = merge_kernel
 std::atomic<int> g_seg_units{0};           // 0 = the compute path's weight of a segment, else this many units
+std::atomic<int> g_wave_skew{-1};          // -1 = the compute path's skew of the CTA shares, else this one
 
 struct DeviceInfo {
     int sms = 0;
@@ -248,6 +250,7 @@ struct LaunchPlan {
     int merge_grid;
     bool merge_in_kernel;
     int seg_units;  // the range balance's weight of a segment (DecodeParams::seg_units)
+    int wave_skew;  // the CTA shares' skew by dispatch wave (DecodeParams::wave_skew)
 };
 
 pa_status plan_launch(int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
@@ -334,6 +337,8 @@ pa_status plan_launch(int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_head
                     : dtype == PA_FP8_E4M3     ? PA_SEG_UNITS_FP8
                     : lp->mma                  ? PA_SEG_UNITS_MMA
                                                : PA_SEG_UNITS_FMA;
+    const int ws = g_wave_skew.load();
+    lp->wave_skew = ws >= 0 ? ws : dtype == PA_FP8_E4M3 ? PA_WAVE_SKEW_FP8 : 0;
     lp->smem = sh.smem;
     lp->grid = sh.grid;
     lp->stages = b.stages;
@@ -373,6 +378,46 @@ extern "C" pa_status pa_debug_set_merge_mode(int32_t mode) {
 extern "C" pa_status pa_debug_set_seg_units(int32_t units) {
     if (units < 0 || units > kMaxSegUnits) return PA_ERR_INVALID_ARG;
     g_seg_units.store(units);
+    return PA_OK;
+}
+
+extern "C" pa_status pa_debug_plan_ranges(const int32_t* block_counts, int32_t num_seqs, int32_t num_kv_heads,
+                                          int32_t partition_tiles, int32_t seg_units, int32_t num_ctas,
+                                          int32_t wave_ctas, int32_t wave_skew, int64_t* starts_out,
+                                          int32_t* owners_out, size_t owners_cap, int32_t* working_ctas_out) {
+    if (!block_counts || !starts_out || !working_ctas_out || num_seqs <= 0 || num_kv_heads <= 0 ||
+        partition_tiles < 0 || seg_units < 0 || seg_units > kMaxSegUnits || num_ctas <= 0 || wave_ctas <= 0 ||
+        wave_skew < 0 || wave_skew > kWaveWeight / 8)
+        return PA_ERR_INVALID_ARG;
+    std::vector<int32_t> pref(num_seqs + 1), upref(num_seqs + 1);
+    int64_t nb = 0, np = 0;
+    for (int b = 0; b < num_seqs; ++b) {
+        if (block_counts[b] < 0) return PA_ERR_INVALID_ARG;
+        pref[b] = (int32_t)nb;
+        upref[b] = (int32_t)np;
+        nb += block_counts[b];
+        if (partition_tiles > 0) np += (block_counts[b] + partition_tiles - 1) / partition_tiles;
+        if (nb * num_kv_heads >= (int64_t)1 << 31) return PA_ERR_INVALID_ARG;
+    }
+    pref[num_seqs] = (int32_t)nb;
+    upref[num_seqs] = (int32_t)np;
+    const Plan P = plan_from_prefix(pref.data(), upref.data(), num_seqs, num_kv_heads, partition_tiles, seg_units,
+                                    num_ctas, wave_ctas, wave_skew);
+    if (owners_out && owners_cap < (size_t)P.T) return PA_ERR_WORKSPACE_TOO_SMALL;
+    *working_ctas_out = P.C;
+    for (int c = 0; c <= P.C; ++c) {
+        int64_t split = -1;
+        int seq = 0;
+        starts_out[c] = P.T > 0 ? P.cta_start(c, &split, &seq) : 0;
+    }
+    if (owners_out)
+        for (int64_t t = 0; t < P.T; ++t) owners_out[t] = P.cta_of(t);
+    return PA_OK;
+}
+
+extern "C" pa_status pa_debug_set_wave_skew(int32_t skew) {
+    if (skew < -1 || skew > kWaveWeight / 8) return PA_ERR_INVALID_ARG;
+    g_wave_skew.store(skew);
     return PA_OK;
 }
 
@@ -487,6 +532,8 @@ pa_status decode_common(void* out, const void* q, const void* k_pool, const void
     p.partition_tiles = partition_tokens / block_size;
     p.num_ctas = lp.grid;
     p.seg_units = lp.seg_units;
+    p.wave_ctas = lp.sms;
+    p.wave_skew = lp.wave_skew;
     p.scale_log2 = scale * 1.4426950408889634f * k_scale;
     p.out_scale = v_scale;
     const uint64_t lim = g_wait_limit_ns.load();
@@ -590,6 +637,8 @@ extern "C" pa_status pa_decode_build_plan(const int32_t* block_tables, int32_t m
     pl[kPlanWMaxLen] = max_len;
     pl[kPlanWMergeInKernel] = lp.merge_in_kernel ? 1 : 0;
     pl[kPlanWMaxBlocks] = max_blocks_per_seq;
+    pl[kPlanWWaveCtas] = lp.sms;
+    pl[kPlanWWaveSkew] = lp.wave_skew;
     // the lengths scan of the kernels: clamped lengths, block and partition prefix sums
     int32_t* pref = pl + kPlanHeaderWords;
     int32_t* upref = pref + (B + 1);
@@ -606,7 +655,7 @@ extern "C" pa_status pa_decode_build_plan(const int32_t* block_tables, int32_t m
     }
     pref[B] = nb_sum;
     upref[B] = PT > 0 ? np_sum : 0;
-    const Plan P = plan_from_prefix(pref, upref, B, Hkv, PT, A, C);
+    const Plan P = plan_from_prefix(pref, upref, B, Hkv, PT, A, C, lp.sms, lp.wave_skew);
     for (int c = 0; c < C; ++c) {
         int32_t* rec = pl + plan_rec_off(B, c);
         for (int w = 0; w < kPlanRecWords; ++w) rec[w] = 0;

@@ -131,8 +131,14 @@ struct Layout {
     static constexpr int kCombOff = kPTileOff + kPTileBytes;
     static constexpr int kCombBytes = (NC - 1) * kCombFloats * 4;
     static constexpr int kBarOff = kCombOff + kCombBytes;
+    // Small words: [0] abort flag, [1] the consumers' stage ticket; at kPendOff the in-kernel
+    // merge's two pending merges ([2][4]); at kWsumOff the lengths scan's per-warp sums (blocks,
+    // then partitions: two words per warp).
     static constexpr int kMiscOff = kBarOff + (2 * S + 2 * kQSlots) * 8;
-    static constexpr int kPrefixOff = kMiscOff + 64;
+    static constexpr int kPendOff = 16;
+    static constexpr int kWsumOff = kPendOff + 32;
+    static constexpr int kMiscBytes = (kWsumOff + 2 * 4 * (NC + 1) + 15) / 16 * 16;
+    static constexpr int kPrefixOff = kMiscOff + kMiscBytes;
     static_assert(kTileBytes % 1024 == 0, "tiles must keep 1024-byte alignment for the 128B swizzle");
     static_assert(kQSlotBytes % 16 == 0, "bulk-copy destination alignment");
     static_assert(kBarOff % 8 == 0, "mbarrier alignment");
@@ -258,7 +264,8 @@ __device__ __forceinline__ bool plan_matches(const DecodeParams& p, int bs) {
            __ldg(pl + kPlanWPartitionTiles) == p.partition_tiles && __ldg(pl + kPlanWSegUnits) == p.seg_units &&
            __ldg(pl + kPlanWBlockSize) == bs && __ldg(pl + kPlanWMaxLen) == p.max_len &&
            __ldg(pl + kPlanWMergeInKernel) == p.merge_in_kernel &&
-           __ldg(pl + kPlanWMaxBlocks) == p.max_blocks_per_seq;
+           __ldg(pl + kPlanWMaxBlocks) == p.max_blocks_per_seq && __ldg(pl + kPlanWWaveCtas) == p.wave_ctas &&
+           __ldg(pl + kPlanWWaveSkew) == p.wave_skew;
 }
 // The plan's prefix sums and clamped lengths go into the shared-memory arrays the scan would
 // fill (pref[B + 1], then upref[B + 1] with partitions, then lens_s[B]).  Each of the NT threads
@@ -301,7 +308,8 @@ __device__ __forceinline__ void load_plan_arrays(const DecodeParams& p, int32_t 
 
 // The plan of this launch over the scanned batch (pa_plan.h).
 __device__ __forceinline__ Plan make_plan(const DecodeParams& p, const int32_t* pref, const int32_t* upref) {
-    return plan_from_prefix(pref, upref, p.num_seqs, p.num_kv_heads, p.partition_tiles, p.seg_units, p.num_ctas);
+    return plan_from_prefix(pref, upref, p.num_seqs, p.num_kv_heads, p.partition_tiles, p.seg_units, p.num_ctas,
+                            p.wave_ctas, p.wave_skew);
 }
 
 template <typename T>
@@ -921,7 +929,7 @@ __device__ __forceinline__ void decode_body(const DecodeParams& p, const CUtenso
     int32_t* upref = pref + (B + 1);
     int32_t* lens_s = upref + (fixed ? B + 1 : 0);  // clamped seq_lens
     volatile int32_t* misc = reinterpret_cast<volatile int32_t*>(base + L::kMiscOff);
-    int32_t* wsum = reinterpret_cast<int32_t*>(base + L::kMiscOff + 16);  // per warp: blocks, then partitions
+    int32_t* wsum = reinterpret_cast<int32_t*>(base + L::kMiscOff + L::kWsumOff);  // per warp: blocks, then partitions
     const uint32_t bar0 = base_s + L::kBarOff;
     auto full_bar = [&](int s) { return bar0 + 8u * s; };
     auto empty_bar = [&](int s) { return bar0 + 8u * (S + s); };
@@ -1112,7 +1120,7 @@ __device__ __forceinline__ void decode_body(const DecodeParams& p, const CUtenso
         // otherwise come last (its last piece) or take many round trips (more than
         // kMergeNowPieces pieces): lane 0 notes (b, h, ca, np) of at most two (slot 0 and
         // slot 1) in shared memory, np = 0 for none.
-        int32_t* pend = reinterpret_cast<int32_t*>(base + L::kMiscOff + 32);  // [2][4]
+        int32_t* pend = reinterpret_cast<int32_t*>(base + L::kMiscOff + L::kPendOff);  // [2][4]
         if (IKM && cw == 0 && lane == 0) pend[3] = pend[7] = 0;
         float* comb = reinterpret_cast<float*>(base + L::kCombOff);
         PieceIter<IKM> it;

@@ -46,6 +46,14 @@ constexpr int kTileUnits = 4;
 #define PA_SEG_UNITS_FP8 24
 #endif
 constexpr int kMaxSegUnits = 4096;  // bound of pa_debug_set_seg_units
+// Shares of the decode's CTAs by dispatch wave (the CTAs of a launch take the SMs in waves of one
+// per SM): wave v of NWV takes kWaveWeight + skew (NWV - 1 - 2 v) parts.  An SM's warp scheduler
+// favours the CTAs dispatched to it first, which on the issue-bound FP8 path end their equal
+// shares several microseconds before the last-dispatched ones; the skew hands the first waves more.
+constexpr int kWaveWeight = 64;
+#ifndef PA_WAVE_SKEW_FP8
+#define PA_WAVE_SKEW_FP8 0
+#endif
 
 struct DecodeParams {
     void* out;
@@ -70,6 +78,9 @@ struct DecodeParams {
     // kTileUnits and every (sequence, KV head) segment seg_units more: the
     // fixed work of a piece (query load, softmax state, output store).
     int32_t seg_units;
+    // ... and CTA c takes a share by its dispatch wave c / wave_ctas (see kWaveWeight)
+    int32_t wave_ctas;
+    int32_t wave_skew;
     float scale_log2;  // scale * log2(e) (times the K scale of an FP8 pool): scores in the base-2 domain
     float out_scale;   // multiplies the output: the V scale of an FP8 pool, else 1
     // time limit of the consumer's waits for query rows and tiles (the producer's

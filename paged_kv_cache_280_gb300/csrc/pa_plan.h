@@ -30,6 +30,36 @@ struct Plan {
     int32_t A;     // no partitions: a tile weighs kTileUnits units, a segment A more
     static constexpr int K = kTileUnits;
     int64_t T, U;  // total tiles; total partitions, or total weighted units
+    // Shares of the CTAs (no partitions): CTA c belongs to dispatch wave c / WV (WV = the SM count,
+    // NWV waves) and takes a share kWaveWeight + KS (NWV - 1 - 2 wave) of the units, so with KS > 0
+    // the CTAs dispatched first to an SM, which its warp scheduler favours, take more.  KS = 0:
+    // equal shares.  WC = the weight of CTAs 0 .. C - 1.
+    int32_t WV, NWV, KS;
+    int64_t WC;
+
+    // weight of CTAs 0 .. c - 1 (c <= C)
+    PA_HD int64_t weight_before(int c) const {
+        if (KS == 0) return c;
+        const int s = c / WV;
+        int64_t w = 0;
+        for (int v = 0; v < s; ++v) w += (int64_t)WV * (kWaveWeight + KS * (NWV - 1 - 2 * v));
+        return w + (int64_t)(c - s * WV) * (kWaveWeight + KS * (NWV - 1 - 2 * s));
+    }
+    // largest c in [0, C - 1] with weight_before(c) <= y (y >= 0)
+    PA_HD int cta_at_weight(int64_t y) const {
+        if (KS == 0) return (int)(y < C - 1 ? y : C - 1);
+        int64_t w0 = 0;
+        for (int s = 0;; ++s) {
+            const int64_t ws = kWaveWeight + KS * (NWV - 1 - 2 * s);
+            const int64_t c = (int64_t)s * WV + (y - w0) / ws;
+            if (c < (int64_t)(s + 1) * WV || s + 1 >= NWV) return (int)(c < C - 1 ? c : C - 1);
+            w0 += (int64_t)WV * ws;
+        }
+    }
+    // the first unit of CTA c's range (no partitions): ceil(W(c) U / W(C))
+    PA_HD int64_t start_unit(int c) const { return div_nonneg(weight_before(c) * U + WC - 1, WC); }
+    // the CTA whose range holds unit x < U (no partitions): the largest c with start_unit(c) <= x
+    PA_HD int cta_of_unit(int64_t x) const { return cta_at_weight(div_nonneg(x * WC, U)); }
 
     PA_HD int nblocks(int b) const { return pref[b + 1] - pref[b]; }
     PA_HD int64_t seg_start(int b, int h) const {
@@ -98,17 +128,17 @@ struct Plan {
     PA_HD int64_t cta_start(int c, int64_t* split, int* seq) const {
         *split = -1;
         *seq = 0;
-        if (PT == 0) return c >= C ? T : first_tile_at_unit(div_nonneg(c * U + C - 1, C), split, seq);
+        if (PT == 0) return c >= C ? T : first_tile_at_unit(start_unit(c), split, seq);
         return tile_of_unit((int64_t)c * U / C, split, seq);
     }
     // the CTA whose range holds tile t of segment (b, h)
     PA_HD int cta_of_seg(int64_t t, int b, int h) const {
-        if (PT == 0) return (int)div_nonneg(((int64_t)K * t + (int64_t)A * ((int64_t)Hkv * b + h + 1)) * C, U);
+        if (PT == 0) return cta_of_unit((int64_t)K * t + (int64_t)A * ((int64_t)Hkv * b + h + 1));
         return cta_of(t);
     }
     // the CTA whose range holds tile t
     PA_HD int cta_of(int64_t t) const {
-        if (PT == 0) return (int)(unit_of_tile(t) * C / U);
+        if (PT == 0) return cta_of_unit(unit_of_tile(t));
         int b = find_seq(pref, t);
         int64_t local = t - (int64_t)Hkv * pref[b];
         int nb = nblocks(b), ub = upref[b + 1] - upref[b];
@@ -169,8 +199,12 @@ PA_HD int clamp_len(int len, int max_len) { return len < 0 ? 0 : (len > max_len 
 // rely on: with partitions every working CTA owns at least one; without, a
 // range is at least K units wide, so no range falls between two tiles of one
 // segment (only in the gap at a segment's start can one be empty).
+//
+// wave_ctas (the SM count) and wave_skew weigh the CTAs by dispatch wave as Plan describes, over
+// num_ctas / wave_ctas waves.  The weights apply only without partitions, and only when the
+// lightest range still spans K units (U w_min >= K C w_max); otherwise the shares are equal.
 PA_HD Plan plan_from_prefix(const int32_t* pref, const int32_t* upref, int B, int Hkv, int partition_tiles,
-                           int seg_units, int num_ctas) {
+                           int seg_units, int num_ctas, int wave_ctas, int wave_skew) {
     Plan P;
     const bool fixed = partition_tiles > 0;
     P.pref = pref;
@@ -191,6 +225,18 @@ PA_HD Plan plan_from_prefix(const int32_t* pref, const int32_t* upref, int B, in
         ce = (units + per - 1) / per;
     }
     P.C = (int32_t)ce;
+    P.WV = wave_ctas > 0 ? wave_ctas : 1;
+    P.NWV = (num_ctas + P.WV - 1) / P.WV;
+    P.KS = 0;
+    P.WC = P.C;
+    if (!fixed && wave_skew > 0 && P.NWV > 1 && kWaveWeight - wave_skew * (P.NWV - 1) > 0) {
+        const int64_t wmin = kWaveWeight - (int64_t)wave_skew * (P.NWV - 1);
+        const int64_t wmax = kWaveWeight + (int64_t)wave_skew * (P.NWV - 1);
+        if (P.U * wmin >= (int64_t)P.K * P.C * wmax) {
+            P.KS = wave_skew;
+            P.WC = P.weight_before(P.C);
+        }
+    }
     return P;
 }
 
@@ -214,6 +260,8 @@ enum PlanHeaderWord {
     kPlanWMaxLen,
     kPlanWMergeInKernel,
     kPlanWMaxBlocks,
+    kPlanWWaveCtas,
+    kPlanWWaveSkew,
 };
 enum PlanRecWord { kRecT0 = 0, kRecT1, kRecTa, kRecSeq0, kRecSeq1, kRecFirst = 8 };
 PA_HD int64_t plan_words(int num_seqs, int grid) {

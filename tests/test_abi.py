@@ -96,3 +96,13 @@ def test_seg_units_knob_checks_its_argument():
         with pytest.raises(pa.PAError):
             pa.pa_debug_set_seg_units(bad)
     pa.pa_debug_set_seg_units(0)
+
+
+def test_wave_skew_knob_checks_its_argument():
+    import pytest
+    import paged_kv_cache_280_gb300 as pa
+
+    for bad in (-2, 9):
+        with pytest.raises(pa.PAError):
+            pa.pa_debug_set_wave_skew(bad)
+    pa.pa_debug_set_wave_skew(-1)

@@ -173,3 +173,33 @@ def test_segment_weight_moves_ranges_not_results(dtype, units):
         check_close(got, ref, "bf16")
     else:
         check_close(got, c.oracle(), dtype)
+
+
+@pytest.mark.parametrize("skew", [0, 3, 8])
+@pytest.mark.parametrize("dtype", ["bf16", "fp8"])
+def test_wave_shares_move_ranges_not_results(dtype, skew):
+    """CTA shares skewed by dispatch wave: outputs within the oracle's tolerance, and a plan built under the
+    same skew matches the unplanned call bit for bit."""
+    import paged_kv_cache_280_gb300 as pa
+
+    lens = np.asarray([700, 0, 1, 33, 1500, 16, 17, 260, 0, 999, 64, 5, 1200, 800], np.int32)
+    hq, hkv, d, bs = 32, 8, 128, 16
+    if dtype == "fp8":
+        c = _fp8_case(75, hq, hkv, bs, lens=lens, max_len=1500)
+    else:
+        c = DecodeCase(W.random_case(75, len(lens), hq, hkv, d, bs, dtype, max_len=1500, min_len=1), lengths=lens)
+    ml = int(lens.max())
+    try:
+        pa.pa_debug_set_wave_skew(skew)
+        plan = pa.pa_decode_build_plan(c.tables, c.lengths, ml, hq, hkv, d, bs, 0, _dtype_code(pa, dtype))
+        assert plan[11] == skew
+        base = _decode(c, pa, dtype, 0)
+        got = _decode(c, pa, dtype, 0, plan=plan)
+    finally:
+        pa.pa_debug_set_wave_skew(-1)
+    assert np.array_equal(base.view(np.uint8), got.view(np.uint8))
+    if dtype == "fp8":
+        ref = oracle.decode_attention_fp8(c.q, c.kq, c.vq, *c.scales, c.ref_tables, c.lengths, c.w.scale, threads=8)
+        check_close(got, ref, "bf16")
+    else:
+        check_close(got, c.oracle(), dtype)

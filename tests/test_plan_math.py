@@ -1,6 +1,9 @@
 """CPU: the decode work plan's arithmetic, as stated for the kernels (tile t of segment (b, h) at
 weighted unit K t + A (Hkv b + h + 1); CTA c takes units [ceil(cU/C), ceil((c+1)U/C)); with a
-partition size, ranges end on partition multiples), re-enacted in integers on random batches.
+partition size, ranges end on partition multiples; without, CTA c may instead take a share by its
+dispatch wave c / WV: wave v of n weighs 64 + KS (n - 1 - 2 v), and CTA c starts at unit
+ceil(W(c) U / W(C)), W the weight of the CTAs before it), re-enacted in integers on random batches
+and compared with the library's own ranges (pa_debug_plan_ranges, host code, no GPU).
 Checks the properties the kernels rely on: every tile has exactly one owner and cta_of agrees with
 the range starts; no range is empty between two tiles of one segment, so a split segment's pieces
 come from consecutive CTAs; and the counting merge: each CTA walks its range as pieces, and every
@@ -12,7 +15,11 @@ check the kernels themselves."""
 import random
 
 
-def plan(lens_blocks, Hkv, C, PT, K=4, A=4):
+WAVE_WEIGHT = 64
+
+
+def plan(lens_blocks, Hkv, C, PT, K=4, A=4, WV=1, KS=0):
+    grid = C
     B = len(lens_blocks)
     pref = [0]
     for n in lens_blocks:
@@ -28,6 +35,22 @@ def plan(lens_blocks, Hkv, C, PT, K=4, A=4):
         per = (units + ce - 1) // ce
         ce = (units + per - 1) // per
     C = ce
+    nwv = (grid + WV - 1) // WV
+    wave_w = lambda v: WAVE_WEIGHT + KS * (nwv - 1 - 2 * v)
+    if PT or KS == 0 or nwv < 2 or wave_w(nwv - 1) <= 0 or U * wave_w(nwv - 1) < K * C * wave_w(0):
+        KS = 0
+
+    def weight_before(c):  # the weight of CTAs 0 .. c - 1
+        return c if KS == 0 else sum(wave_w(x // WV) for x in range(c))
+
+    WC = weight_before(C)
+
+    def cta_of_unit(x):  # the largest c < C with ceil(W(c) U / WC) <= x
+        y = x * WC // U
+        c = 0
+        while c + 1 < C and weight_before(c + 1) <= y:
+            c += 1
+        return c
 
     def find_seq(pre, x):
         lo, hi = 0, B - 1
@@ -70,7 +93,7 @@ def plan(lens_blocks, Hkv, C, PT, K=4, A=4):
 
     def cta_start(c):
         if PT == 0:
-            return T if c >= C else first_tile_at_unit((c * U + C - 1) // C)
+            return T if c >= C else first_tile_at_unit((weight_before(c) * U + WC - 1) // WC)
         return tile_of_unit(c * U // C)
 
     def cta_of(t):
@@ -79,7 +102,7 @@ def plan(lens_blocks, Hkv, C, PT, K=4, A=4):
         nb = nbk(b)
         h, j = local // nb, local % nb
         if PT == 0:
-            return (K * t + A * (Hkv * b + h + 1)) * C // U
+            return cta_of_unit(K * t + A * (Hkv * b + h + 1))
         ub = upref[b + 1] - upref[b]
         u = Hkv * upref[b] + h * ub + j // PT
         return ((u + 1) * C - 1) // U
@@ -88,11 +111,15 @@ def plan(lens_blocks, Hkv, C, PT, K=4, A=4):
                 cta_of=cta_of)
 
 
-def _check(lens_blocks, Hkv, C, PT):
-    P = plan(lens_blocks, Hkv, C, PT)
+def _check(lens_blocks, Hkv, C, PT, WV=1, KS=0, lib=None):
+    P = plan(lens_blocks, Hkv, C, PT, WV=WV, KS=KS)
     if P["T"] == 0:
         return
     starts = [P["cta_start"](c) for c in range(P["C"] + 1)]
+    if lib is not None:  # the library's host build of the same arithmetic
+        got, owners = lib.pa_debug_plan_ranges(lens_blocks, Hkv, PT, 4, C, WV, KS)
+        assert list(got) == starts
+        assert list(owners) == [P["cta_of"](t) for t in range(P["T"])]
     assert starts[0] == 0 and starts[-1] == P["T"]
     assert all(a <= b for a, b in zip(starts, starts[1:]))
     split = set()
@@ -138,12 +165,44 @@ def _check(lens_blocks, Hkv, C, PT):
 
 
 def test_plan_properties_on_random_batches():
+    import paged_kv_cache_280_gb300 as pa
+
     rng = random.Random(280)
-    for _ in range(1500):
+    for i in range(1500):
         B = rng.randint(1, 10)
         Hkv = rng.choice([1, 2, 4, 8])
         lens = [rng.choice([0, 0, 1, 2, 3, 5, 9, 17, 40]) for _ in range(B)]
-        _check(lens, Hkv, rng.randint(1, 64), rng.choice([0, 0, 0, 1, 2, 4]))
+        _check(lens, Hkv, rng.randint(1, 64), rng.choice([0, 0, 0, 1, 2, 4]), lib=pa if i % 3 == 0 else None)
+
+
+def test_wave_shares_on_random_batches():
+    """CTA shares skewed by dispatch wave keep every property above and agree with the library."""
+    import paged_kv_cache_280_gb300 as pa
+
+    rng = random.Random(281)
+    for _ in range(600):
+        B = rng.randint(1, 12)
+        Hkv = rng.choice([1, 2, 4, 8])
+        lens = [rng.choice([0, 1, 2, 3, 5, 9, 17, 40, 90]) for _ in range(B)]
+        WV = rng.randint(1, 12)
+        _check(lens, Hkv, WV * rng.randint(1, 8), 0, WV=WV, KS=rng.choice([0, 1, 2, 4, 8]), lib=pa)
+
+
+def test_wave_shares_follow_the_weights():
+    """On a large uniform batch the first dispatch wave takes more tiles than the last, about in the
+    ratio of their weights; partitioned launches keep equal shares."""
+    import numpy as np
+    import paged_kv_cache_280_gb300 as pa
+
+    lens = [50] * 64
+    starts, _ = pa.pa_debug_plan_ranges(lens, 8, 0, 4, 608, 152, 2, owners=False)
+    tiles = np.diff(starts)
+    first, last = tiles[:152].mean(), tiles[456:].mean()
+    assert abs(first / last - 70 / 58) < 0.05
+    even, _ = pa.pa_debug_plan_ranges(lens, 8, 0, 4, 608, 152, 0, owners=False)
+    assert np.diff(even).max() - np.diff(even).min() <= 2
+    part, _ = pa.pa_debug_plan_ranges(lens, 8, 5, 4, 608, 152, 2, owners=False)
+    assert len(set(np.diff(part).tolist())) <= 2  # partitions: equal numbers of them
 
 
 def test_weighted_balance_spreads_segment_cost():
