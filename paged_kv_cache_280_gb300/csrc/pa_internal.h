@@ -50,9 +50,10 @@ constexpr int kMaxSegUnits = 4096;  // bound of pa_debug_set_seg_units
 // per SM): wave v of NWV takes kWaveWeight + skew (NWV - 1 - 2 v) parts.  An SM's warp scheduler
 // favours the CTAs dispatched to it first, which on the issue-bound FP8 path end their equal
 // shares several microseconds before the last-dispatched ones; the skew hands the first waves more.
+// Measured over FP8 pools: skew 2 about 1.5 % faster on mha_b256_append, neutral elsewhere.
 constexpr int kWaveWeight = 64;
 #ifndef PA_WAVE_SKEW_FP8
-#define PA_WAVE_SKEW_FP8 0
+#define PA_WAVE_SKEW_FP8 2
 #endif
 
 struct DecodeParams {
