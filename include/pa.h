@@ -199,8 +199,9 @@ pa_status pa_decode_attention(void* out, const void* q, const void* k_pool, cons
  * pa_decode_attention_planned / pa_decode_attention_fp8_planned: the decode
  * calls with a device copy of that plan (4-byte aligned, plan_bytes long;
  * shorter is PA_ERR_INVALID_ARG).  A plan whose header does not name this
- * call's batch size, grid, KV heads, partition size, block size, length
- * bound, table width and merge mode is ignored (the launch computes its own);
+ * call's batch size, grid, KV heads, partition size, segment weight, block
+ * size, length bound, table width, merge mode, wave size and wave skew is
+ * ignored (the launch computes its own);
  * a plan built from other lengths or table entries than the device copies
  * hold gives wrong outputs: rebuild it whenever either changes.  The launch
  * trusts a matching plan's prefix sums (only its block ids are checked, as
