@@ -609,14 +609,18 @@ def run_ours(args, rank, world, local_rank):
                    region(hb, "plan", torch.int32, (-1,)).numpy() if use_plan else None)
                   for hb in host_stage]
 
+    host_us = []
+
     def host_prepare(s):
         # the allocator's step: new slots (and CoW pairs), block tables and lengths,
-        # written in place into staging buffer s % 2
+        # written in place into staging buffer s % 2, and the decode call's plan
+        t_host = time.perf_counter()
         h_slots, h_pairs, h_tables, h_lens, h_plan = host_views[s % n_stage]
         _, pr = lib.append_batch(ids_arr, slots_out=h_slots, pairs_out=h_pairs)
         lib.export_tables(ids_arr, max_blocks, tables_out=h_tables, lens_out=h_lens)
         if use_plan:
             S.build_plan(h_tables, h_lens, cap_len, out=h_plan)
+        host_us.append((time.perf_counter() - t_host) * 1e6)
         return pr, int(h_lens.sum(dtype=np.int64))
 
     def gpu_step(s, pr):
@@ -667,7 +671,11 @@ def run_ours(args, rank, world, local_rank):
                       "(decode kernel, and merge kernel when used) timed alone in a second loop of as many steps",
             "l2": f"flushed between timed steps ({L2_FLUSH_BYTES >> 20} MiB write, then a {L2_FLUSH_BYTES >> 21} MiB read "
                   "so that no dirty line is left; untimed)",
-            "host_alloc_us_per_step": round(S.host_alloc_us, 1), "decode_ctas": ctas, "stages": stages,
+            "host_alloc_us_first_call": round(S.host_alloc_us, 1),
+            "host_prepare_us_median": round(statistics.median(host_us), 1) if host_us else None,
+            "host_prepare": "the allocator's step (slots, CoW pairs, block tables, lengths) and the decode plan, "
+                            "written into pinned staging; median over the end-to-end steps",
+            "decode_ctas": ctas, "stages": stages,
             "smem_bytes": smem, "path": "mma.sync" if mma else "fma", "partition_tokens": S.PT,
             "kv_dtype": "fp8_e4m3" if fp8 else "bf16", **({"k_scale": S.KS, "v_scale": S.VS} if fp8 else {}),
             "decode_ms_median": statistics.median(dec_ms), "decode_ms_min": min(dec_ms),
@@ -680,8 +688,9 @@ def run_ours(args, rank, world, local_rank):
                      "traffic": None if fp8 else recorded_traffic(args.workload)},
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d // max(1, K_e2e),
                 "d2h_bytes_per_step": d2h // max(1, K_e2e), "steps": K_e2e,
-                "includes": "host allocator writing into pinned staging one step ahead of the GPU, one H2D of "
-                            "q/k_new/v_new/slots/pairs/tables/lens, kernels, D2H of out; no L2 flush inside the loop "
+                "includes": "host allocator" + (" and decode plan" if use_plan else "") + " writing into pinned "
+                            "staging one step ahead of the GPU, one H2D of q/k_new/v_new/slots/pairs/tables/lens"
+                            + ("/plan" if use_plan else "") + ", kernels, D2H of out; no L2 flush inside the loop "
                             "(the KV read per step is larger than L2 and loaded evict-first)",
                 "launch": "eager" if args.e2e_eager else "one CUDA graph per staging buffer (H2D, append, decode (+ merge), D2H)"},
         "gpu_launches": K * S.launches_per_step,

@@ -224,18 +224,20 @@ def pa_decode_plan_bytes(num_seqs, num_q_heads, num_kv_heads, head_dim, block_si
 def pa_decode_build_plan(block_tables, seq_lens, max_seq_len, num_q_heads, num_kv_heads, head_dim, block_size,
                          partition_tokens, dtype, out=None):
     """The decode plan (int32 numpy array) from host copies of the block tables ([B][max_blocks] int32) and
-    lengths ([B] int32).  ``out``: an int32 numpy array (e.g. a view of a pinned staging buffer) to write into."""
+    lengths ([B] int32).  ``out``: an int32 numpy array (e.g. a view of a pinned staging buffer) to write into,
+    of pa_decode_plan_bytes bytes at least (shorter raises PAError: PA_ERR_WORKSPACE_TOO_SMALL); without it the
+    plan's size is asked for first."""
     import numpy as np
 
     tables = np.ascontiguousarray(block_tables, dtype=np.int32)
     lens = np.ascontiguousarray(seq_lens, dtype=np.int32)
     b, mb = tables.shape
-    n = pa_decode_plan_bytes(b, num_q_heads, num_kv_heads, head_dim, block_size, mb, max_seq_len, partition_tokens,
-                             dtype)
     if out is None:
+        n = pa_decode_plan_bytes(b, num_q_heads, num_kv_heads, head_dim, block_size, mb, max_seq_len,
+                                 partition_tokens, dtype)
         out = np.empty(n // 4, dtype=np.int32)
-    if out.dtype != np.int32 or not out.flags["C_CONTIGUOUS"] or out.nbytes < n:
-        raise ValueError("pa_decode_build_plan: out must be a contiguous int32 array of pa_decode_plan_bytes bytes")
+    if out.dtype != np.int32 or not out.flags["C_CONTIGUOUS"]:
+        raise ValueError("pa_decode_build_plan: out must be a contiguous int32 array")
     _ok(_lib.pa_decode_build_plan(tables.ctypes.data, mb, lens.ctypes.data, int(max_seq_len), b, num_q_heads,
                                   num_kv_heads, head_dim, block_size, int(partition_tokens), dtype, out.ctypes.data,
                                   out.nbytes), "pa_decode_build_plan")
